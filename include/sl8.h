@@ -1,0 +1,228 @@
+/*
+ * sl8 -- W8A8 INT8 attention for NVIDIA GB300 (sm_103a): C ABI.
+ *
+ * The operations follow the "SuperL8" README (github.com/jajmangold/superl8):
+ *   - "Supporting kernels" table, quant_rowwise: symmetric per-row int8 quantisation;
+ *   - "Quantization" table, "Per-row int8": symmetric, with K-smoothing;
+ *   - "Attention kernels" table, attn_int8_fwd: W8A8 FlashAttention-2 forward,
+ *     causal, GQA/MQA, head dims 32/64/128/256 (this library: 64, 128, 256);
+ *     attn_varlen_fwd: ragged variable-length prefill; attn_decode: split-KV decode
+ *     with an int8 KV cache, int8-V variant;
+ *   - "Quick start" section: q [B, Hq, N, d], k/v [B, Hkv, N, d],
+ *     attn_int8_fwd(q, k, v, causal=True), quantising internally.
+ * The pages give no formulas; the readings this library implements are:
+ *   scale s = max|x| / 127 (IEEE fp32 division); code = clamp(round-half-even(x / s),
+ *   -127, 127); a row with s == 0 has all-zero codes.  K-smoothing subtracts, per
+ *   (sequence, kv head, channel), the fp32 mean of K over all the sequence's tokens
+ *   (summed in 64-token chunks in token order, then the chunk sums in order).
+ *   Logits x = int32(q_i8 . k_i8) * s_q * s_k / sqrt(d); the causal mask is top-left
+ *   aligned (key j visible to query i iff j <= i); softmax is computed online
+ *   (FlashAttention-2 style); O = P . V with P rounded to V's dtype and fp32
+ *   accumulation.  GQA maps query head hq to kv head hq / (Hq / Hkv).
+ *
+ * Conventions for every entry point:
+ *   - Pointers named as device pointers must be device memory of the current CUDA
+ *     device, 16-byte aligned, holding contiguous tensors in the stated layout.  The
+ *     caller owns every buffer; the library allocates no device memory.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call only
+ *     validates its arguments on the host and enqueues kernels on `stream`; it does
+ *     not synchronise.
+ *   - Argument errors are reported synchronously, before anything is launched.
+ *     Conditions only the device can see (a cu_seqlens / seqlens entry out of range,
+ *     a bounded device-side wait that gave up) are recorded in a per-device status
+ *     word that sl8_last_device_status() reads.
+ *   - No C++ exception crosses this interface.
+ */
+#ifndef SL8_H_
+#define SL8_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SL8_API __attribute__((visibility("default")))
+#else
+#define SL8_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sl8_status {
+  SL8_OK = 0,
+  SL8_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad shape or dtype, Hq % Hkv != 0 */
+  SL8_ERR_UNSUPPORTED = 2, /* valid but not implemented here (e.g. d = 32, Hq/Hkv > 8 in decode) */
+  SL8_ERR_WORKSPACE = 3,   /* workspace missing or smaller than the size query returned */
+  SL8_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+  SL8_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up (see sl8_last_device_status) */
+  SL8_ERR_DEVICE_ARG = 6   /* the device found an out-of-range length (cu_seqlens / seqlens) */
+} sl8_status;
+
+typedef enum sl8_dtype { SL8_F16 = 0, SL8_BF16 = 1, SL8_F32 = 2, SL8_I8 = 3 } sl8_dtype;
+
+/* Human-readable name of a status code (static string). */
+SL8_API const char* sl8_status_string(int status);
+
+/* Library version, as major * 10000 + minor * 100 + patch. */
+SL8_API int sl8_version(void);
+
+/*
+ * Symmetric per-row int8 quantisation ("Supporting kernels" table, quant_rowwise;
+ * "Quantization" table, per-row int8).
+ *   x          device, `rows` rows of `cols` elements of x_dtype (F16, BF16 or F32);
+ *              row r starts at element r * row_stride_elems.
+ *   sub_mean   device, nullable: [groups][cols] fp32; row r first has
+ *              sub_mean[r / rows_per_group] subtracted (fp32), which is K-smoothing
+ *              when the groups are (sequence, kv head) blocks of a dense [B,H,N,d] K.
+ *   q_out      device, [rows][cols] int8 codes (contiguous).
+ *   scale_out  device, [rows] fp32 scales s = max|x - mean| / 127.
+ * Errors: SL8_ERR_INVALID_ARG for null x/q_out/scale_out, rows < 0, cols < 1,
+ * row_stride_elems < cols, rows_per_group < 1 with sub_mean set, or a bad dtype.
+ * rows == 0 returns SL8_OK at once (the pointers may then be null).
+ */
+SL8_API int sl8_quant_rowwise(const void* x, int x_dtype, int64_t rows, int32_t cols, int64_t row_stride_elems,
+                      const float* sub_mean, int64_t rows_per_group, int8_t* q_out, float* scale_out,
+                      void* stream);
+
+/*
+ * Per-channel mean of K over each sequence's tokens, the K-smoothing statistic
+ * ("Quantization" table, per-row int8 with K-smoothing).
+ *   k           device.  Dense (cu_seqlens NULL): [B][Hkv][N][d]; varlen:
+ *               [total_tokens][Hkv][d] packed, sequence s = tokens
+ *               [cu_seqlens[s], cu_seqlens[s+1]).
+ *   cu_seqlens  device, nullable, [B + 1] int32, nondecreasing, each length <= N.
+ *   mean_out    device, [B][Hkv][d] fp32.
+ *   workspace   device scratch of at least sl8_k_channel_mean_workspace_size() bytes.
+ */
+SL8_API size_t sl8_k_channel_mean_workspace_size(int32_t B, int32_t Hkv, int32_t N, int32_t d);
+SL8_API int sl8_k_channel_mean(const void* k, int k_dtype, int32_t B, int32_t Hkv, int32_t N, int32_t d,
+                       const int32_t* cu_seqlens, int64_t total_tokens, float* mean_out, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/*
+ * W8A8 INT8 attention prefill ("Attention kernels" table, attn_int8_fwd and
+ * attn_varlen_fwd; "Quick start" section for the layouts).
+ *   q, k, v     device.  Dense (cu_seqlens NULL): q [B][Hq][N][d], k/v [B][Hkv][N][d].
+ *               Varlen: q [total_tokens][Hq][d], k/v [total_tokens][Hkv][d] packed,
+ *               B = number of sequences, N = the longest sequence length (an upper
+ *               bound every cu_seqlens length must respect).
+ *   qk_dtype    F16 or BF16 (q and k); v_dtype F16 or BF16.
+ *   d           64, 128 or 256.  Hq must be a multiple of Hkv.
+ *   causal      nonzero: key j is visible to query i iff j <= i (positions within the
+ *               sequence).
+ *   smooth_k    nonzero: subtract K's per-channel mean before quantising K.
+ *   out         device, same layout as q, of out_dtype (v_dtype, or F32).
+ *   lse_out     device, nullable: fp32 log-sum-exp (natural log) per query row,
+ *               dense [B][Hq][N], varlen [total_tokens][Hq].
+ *   workspace   device scratch of at least sl8_attn_int8_fwd_workspace_size() bytes
+ *               (the quantised codes, scales, K means and the work list live there).
+ * Errors: SL8_ERR_INVALID_ARG, SL8_ERR_UNSUPPORTED (d not in {64,128,256}),
+ * SL8_ERR_WORKSPACE, SL8_ERR_CUDA.  Empty inputs (B, N or total_tokens 0) return
+ * SL8_OK without launching.
+ */
+SL8_API size_t sl8_attn_int8_fwd_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t N, int32_t d,
+                                        int64_t total_tokens);
+SL8_API int sl8_attn_int8_fwd(const void* q, const void* k, const void* v, int qk_dtype, int v_dtype, int32_t B, int32_t Hq,
+                      int32_t Hkv, int32_t N, int32_t d, const int32_t* cu_seqlens, int64_t total_tokens,
+                      int causal, int smooth_k, void* out, int out_dtype, float* lse_out, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/*
+ * Debug view of the prefill's quantisation and int32 logits (same kernels and
+ * tensor-core path as sl8_attn_int8_fwd, without the mask).  Dense layout only.
+ *   logits_out  device, nullable, [B][Hq][row_end - row_begin][N] int32:
+ *               logits_out[b][h][i - row_begin][j] = int32(q_i8[b,h,i] . k_i8[b,hkv,j])
+ *               for every key j < N, 0 <= row_begin <= i < row_end <= N.
+ *   q_codes/q_scales    device, nullable, [B][Hq][N][d] int8 / [B][Hq][N] fp32.
+ *   k_codes/k_scales    device, nullable, [B][Hkv][N][d] int8 / [B][Hkv][N] fp32
+ *                       (after smoothing when smooth_k is set).
+ *   workspace   as for sl8_attn_int8_fwd (same size query).
+ */
+SL8_API int sl8_attn_int8_qk_logits_debug(const void* q, const void* k, int qk_dtype, int32_t B, int32_t Hq, int32_t Hkv,
+                                  int32_t N, int32_t d, int smooth_k, int32_t row_begin, int32_t row_end,
+                                  int32_t* logits_out, int8_t* q_codes, float* q_scales, int8_t* k_codes,
+                                  float* k_scales, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Split-KV decode over an int8 KV cache ("Attention kernels" table, attn_decode,
+ * int8-V variant): one query token per sequence against its cached keys t < L_b.
+ *   q                  device, [B][Hq][d] of q_dtype (F16, BF16 or F32); quantised
+ *                      per row inside the kernel.
+ *   k_cache, v_cache   device, [B][Hkv][Lmax][d] int8 codes.
+ *   k_scale, v_scale   device, [B][Hkv][Lmax] fp32 per-token scales.
+ *   seqlens            device, [B] int32, 0 <= L_b <= Lmax.
+ *   num_splits         requested number of contiguous key splits (0 = automatic: one
+ *                      split per 32 KB of K codes).  The effective count is
+ *                      S = sl8_attn_decode_num_splits(Lmax, d, num_splits) (the request,
+ *                      capped at Lmax), and split s covers tokens
+ *                      [s * split_size, (s + 1) * split_size), split_size = ceil(Lmax / S).
+ *   o_partial          device, [B][Hq][S][d] fp32; each split's normalised partial.
+ *   lse_partial        device, [B][Hq][S] fp32 log-sum-exp per split (-inf if empty).
+ * Hq / Hkv must be at most 8 (SL8_ERR_UNSUPPORTED otherwise).
+ */
+SL8_API int32_t sl8_attn_decode_num_splits(int32_t Lmax, int32_t d, int32_t num_splits);
+SL8_API int32_t sl8_attn_decode_split_size(int32_t Lmax, int32_t d, int32_t num_splits);
+SL8_API int sl8_attn_int8_decode_splitkv(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale,
+                                 const int8_t* v_cache, const float* v_scale, const int32_t* seqlens, int32_t B,
+                                 int32_t Hq, int32_t Hkv, int32_t Lmax, int32_t d, int32_t num_splits,
+                                 float* o_partial, float* lse_partial, void* stream);
+
+/*
+ * Decode combine: merge the split partials of each (b, hq) row,
+ * O = sum_s e^(lse_s - M) O_s / sum_s e^(lse_s - M), M = max_s lse_s, over the
+ * non-empty splits.  A row with L_b = 0 gets O = 0 (lse -inf).
+ *   out      device, [B][Hq][d] of out_dtype (F16, BF16 or F32).
+ *   lse_out  device, nullable, [B][Hq] fp32.
+ *   num_splits must be the effective count S of the split call (same Lmax); the split
+ *   size is ceil(Lmax / S) as there.
+ */
+SL8_API int sl8_attn_decode_combine(const float* o_partial, const float* lse_partial, const int32_t* seqlens, int32_t B,
+                            int32_t Hq, int32_t Lmax, int32_t d, int32_t num_splits, void* out, int out_dtype,
+                            float* lse_out, void* stream);
+
+/*
+ * Debug view of the decode's q quantisation and int32 logits (same kernel as the
+ * split call, with num_splits automatic).
+ *   logits_out  device, [B][Hq][Lmax] int32: entry t < L_b is int32(q_i8 . k_i8[t]);
+ *               entries t >= L_b are left untouched.
+ *   q_codes/q_scales  device, nullable, [B][Hq][d] int8 / [B][Hq] fp32.
+ *   o_partial/lse_partial  scratch as for the split call.
+ */
+SL8_API int sl8_attn_int8_decode_logits_debug(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale,
+                                      const int8_t* v_cache, const float* v_scale, const int32_t* seqlens,
+                                      int32_t B, int32_t Hq, int32_t Hkv, int32_t Lmax, int32_t d,
+                                      int32_t* logits_out, int8_t* q_codes, float* q_scales, float* o_partial,
+                                      float* lse_partial, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status word:
+ * SL8_OK, SL8_ERR_TIMEOUT (a bounded wait gave up; *site names the wait) or
+ * SL8_ERR_DEVICE_ARG (an out-of-range device-side length).  site may be NULL.
+ */
+SL8_API int sl8_last_device_status(void* stream, int* site);
+
+/* Upper bound, in nanoseconds, on every device-side wait (default 2e9). */
+SL8_API void sl8_set_spin_limit_ns(uint64_t limit_ns);
+SL8_API uint64_t sl8_get_spin_limit_ns(void);
+
+/*
+ * Self-test of the bounded waits: launches one kernel whose wait on a barrier that
+ * nothing arrives on must give up after limit_ns and record SL8_ERR_TIMEOUT.
+ */
+SL8_API int sl8_selftest_timeout(uint64_t limit_ns, void* stream);
+
+/*
+ * Kernel tracing.  While enabled, every kernel the library launches is bracketed by
+ * CUDA events on its stream.  sl8_trace_collect() synchronises those events and
+ * returns, per kernel name, the number of launches and their summed device time;
+ * it then clears the record.  Returns the number of names written (at most max).
+ */
+SL8_API void sl8_trace_enable(int on);
+SL8_API int sl8_trace_collect(const char** names, int64_t* launches, double* total_ms, int max);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SL8_H_ */

@@ -1,0 +1,153 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and loads,
+exports every function include/sl8.h declares, and rejects bad arguments
+synchronously, before anything is launched."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import w8a8_int8_flashattention_gb300 as sl8
+from w8a8_int8_flashattention_gb300 import build as sl8_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    sl8_build.build()
+    return sl8.lib()
+
+
+def test_exports_every_header_function(lib):
+    names = sl8.header_functions()
+    assert len(names) >= 19
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    # and the binding declares a signature for each of them
+    assert set(names) == set(sl8._SIGNATURES)
+
+
+def test_exported_symbols_are_only_the_abi(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", sl8.LIB_PATH], capture_output=True, text=True).stdout
+    sl8_syms = sorted(set(re.findall(r"\b(sl8_[a-z0-9_]+)\b", out)))
+    assert sl8_syms == sl8.header_functions()
+
+
+def test_status_strings_and_version(lib):
+    assert lib.sl8_status_string(0) == b"ok"
+    assert b"workspace" in lib.sl8_status_string(3)
+    assert lib.sl8_status_string(99) == b"unknown status"
+    assert lib.sl8_version() >= 100
+
+
+def test_workspace_sizes(lib):
+    # dense: codes for Q and K (bf16) + scales + table; grows with N and heads
+    a = lib.sl8_attn_int8_fwd_workspace_size(1, 32, 8, 4096, 128, 0)
+    assert a >= 32 * 4096 * 128 * 2 + 8 * 4096 * 128 * 2
+    assert lib.sl8_attn_int8_fwd_workspace_size(1, 32, 8, 4097, 128, 0) > a
+    # varlen bound: total tokens + 127 per sequence of padding
+    v = lib.sl8_attn_int8_fwd_workspace_size(32, 64, 8, 3000, 128, 48000)
+    assert v >= (48000 + 32 * 127) // 128 * 128 * 72 * 128 * 2 * 0.99
+    assert lib.sl8_attn_int8_fwd_workspace_size(-1, 32, 8, 4096, 128, 0) == 0
+    assert lib.sl8_k_channel_mean_workspace_size(2, 8, 8192, 256) > 0
+
+
+def test_decode_split_plan(lib):
+    assert lib.sl8_attn_decode_split_size(8192, 128, 0) == 256
+    assert lib.sl8_attn_decode_num_splits(8192, 128, 0) == 32
+    assert lib.sl8_attn_decode_num_splits(8192, 128, 5) == 5
+    assert lib.sl8_attn_decode_split_size(8192, 128, 5) == 1639
+    assert lib.sl8_attn_decode_num_splits(8192, 128, 1) == 1
+    assert lib.sl8_attn_decode_num_splits(100, 32, 0) == 0  # unsupported head dim
+    assert lib.sl8_attn_decode_num_splits(700, 128, 0) == 3
+    assert lib.sl8_attn_decode_split_size(700, 128, 0) == 234  # ceil(700 / 3), within one chunk
+    assert lib.sl8_attn_decode_num_splits(10, 128, 64) == 10   # capped at Lmax
+    for lmax in range(1, 300, 7):
+        for n in range(0, 40, 3):
+            S = lib.sl8_attn_decode_num_splits(lmax, 128, n)
+            ss = lib.sl8_attn_decode_split_size(lmax, 128, n)
+            assert S >= 1 and ss * S >= lmax and ss <= 256
+
+
+def _host_buf(nbytes):
+    # 16-byte aligned host memory: only used for argument checks that fail before any access
+    raw = np.zeros(nbytes + 32, np.uint8)
+    off = (-raw.ctypes.data) % 16
+    return raw, raw.ctypes.data + off
+
+
+def test_prefill_argument_errors(lib):
+    keep, p = _host_buf(1 << 12)
+    f = lib.sl8_attn_int8_fwd
+    # (q, k, v, qk_dtype, v_dtype, B, Hq, Hkv, N, d, cu, T, causal, smooth, out, out_dtype, lse, ws, ws_bytes, stream)
+    base = [p, p, p, sl8.SL8_BF16, sl8.SL8_BF16, 1, 4, 2, 128, 128, None, 0, 1, 1, p, sl8.SL8_BF16, None, p, 16, None]
+
+    def call(**kw):
+        args = list(base)
+        idx = dict(q=0, k=1, v=2, qk=3, vdt=4, B=5, Hq=6, Hkv=7, N=8, d=9, out=14, odt=15, ws=17, wsb=18)
+        for k, val in kw.items():
+            args[idx[k]] = val
+        return f(*args)
+
+    assert call(q=None) == sl8.SL8_ERR_INVALID_ARG
+    assert call(q=p + 2) == sl8.SL8_ERR_INVALID_ARG           # misaligned
+    assert call(Hkv=3) == sl8.SL8_ERR_INVALID_ARG             # Hq % Hkv != 0
+    assert call(d=32) == sl8.SL8_ERR_UNSUPPORTED
+    assert call(d=96) == sl8.SL8_ERR_UNSUPPORTED
+    assert call(qk=sl8.SL8_F32) == sl8.SL8_ERR_INVALID_ARG
+    assert call(odt=sl8.SL8_F16) == sl8.SL8_ERR_INVALID_ARG   # out must be V's dtype or F32
+    assert call(ws=None) == sl8.SL8_ERR_WORKSPACE
+    assert call(wsb=16) == sl8.SL8_ERR_WORKSPACE
+    assert call(B=0) == sl8.SL8_OK                            # empty: nothing to do
+    assert call(N=0) == sl8.SL8_OK
+
+
+def test_decode_and_quant_argument_errors(lib):
+    keep, p = _host_buf(1 << 12)
+    f = lib.sl8_attn_int8_decode_splitkv
+    ok_args = [p, sl8.SL8_BF16, p, p, p, p, p, 64, 32, 8, 8192, 128, 0, p, p, None]
+    a = list(ok_args); a[0] = None
+    assert f(*a) == sl8.SL8_ERR_INVALID_ARG
+    a = list(ok_args); a[8] = 64; a[9] = 4                   # Hq/Hkv = 16 > 8
+    assert f(*a) == sl8.SL8_ERR_UNSUPPORTED
+    a = list(ok_args); a[11] = 80
+    assert f(*a) == sl8.SL8_ERR_UNSUPPORTED
+    a = list(ok_args); a[7] = 0
+    assert f(*a) == sl8.SL8_OK
+    q = lib.sl8_quant_rowwise
+    assert q(None, sl8.SL8_F32, 4, 4, 4, None, 0, p, p, None) == sl8.SL8_ERR_INVALID_ARG
+    assert q(p, sl8.SL8_I8, 4, 4, 4, None, 0, p, p, None) == sl8.SL8_ERR_INVALID_ARG
+    assert q(p, sl8.SL8_F32, 4, 4, 2, None, 0, p, p, None) == sl8.SL8_ERR_INVALID_ARG  # stride < cols
+    assert q(p, sl8.SL8_F32, 4, 4, 4, p, 0, p, p, None) == sl8.SL8_ERR_INVALID_ARG    # group size 0
+    assert q(p, sl8.SL8_F32, 0, 4, 4, None, 0, p, p, None) == sl8.SL8_OK
+    c = lib.sl8_attn_decode_combine
+    assert c(p, p, p, 2, 4, 100, 128, 0, p, sl8.SL8_BF16, None, None) == sl8.SL8_ERR_INVALID_ARG
+    assert c(p, p, p, 2, 4, 100, 128, 1, p, sl8.SL8_I8, None, None) == sl8.SL8_ERR_INVALID_ARG
+
+
+def test_spin_limit_knob(lib):
+    old = sl8.get_spin_limit_ns()
+    sl8.set_spin_limit_ns(12345)
+    assert sl8.get_spin_limit_ns() == 12345
+    sl8.set_spin_limit_ns(old)
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    x = torch.zeros(4, 64)
+    with pytest.raises(ValueError):
+        sl8.quant_rowwise(x)
+
+
+def test_oracle_builds_independently():
+    import oracle
+    path = oracle.build()
+    assert os.path.exists(path)
+    # the oracle shares no code with the library: no include of csrc or the ABI header
+    src = open(os.path.join(ROOT, "oracle", "sl8_oracle.c")).read()
+    assert "csrc" not in src and "sl8.h" not in src
+    for f in os.listdir(os.path.join(ROOT, "w8a8_int8_flashattention_gb300", "csrc")):
+        assert "oracle" not in open(os.path.join(ROOT, "w8a8_int8_flashattention_gb300", "csrc", f)).read().lower()

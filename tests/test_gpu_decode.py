@@ -1,0 +1,140 @@
+"""GPU parity of the split-KV int8-cache decode (and its combine) against the oracle.
+
+Operation: the "SuperL8" README, "Attention kernels" table, attn_decode (split-KV
+decode with an int8 KV cache, int8-V variant).  The cache is built from the same
+seeded fp32 values on both sides: the GPU path quantises them with
+sl8_quant_rowwise, the oracle with its own quantiser, and the two caches must be
+byte-identical.  Bit-exact: q codes/scales and int32 logits; outputs within the
+tolerances of tests/_parity.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+import w8a8_int8_flashattention_gb300 as sl8
+from _parity import check_f32, check_half, to_np32
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from w8a8_int8_flashattention_gb300 import build
+    build.build()
+    sl8.lib()
+
+
+def build_cache(w, lmax, batches=None):
+    """GPU and oracle caches for workload w: codes [B,Hkv,Lmax,d] int8, scales [B,Hkv,Lmax]."""
+    B, Hkv, d = w.B, w.Hkv, w.d
+    lens = W.seq_lengths(w)
+    g = {n: torch.zeros((B, Hkv, lmax, d), dtype=torch.int8, device=DEV) for n in ("k", "v")}
+    gs = {n: torch.zeros((B, Hkv, lmax), dtype=torch.float32, device=DEV) for n in ("k", "v")}
+    o = {n: np.zeros((B, Hkv, lmax, d), np.int8) for n in ("k", "v")}
+    os_ = {n: np.zeros((B, Hkv, lmax), np.float32) for n in ("k", "v")}
+    for b in range(B):
+        L = int(lens[b])
+        for n in ("k", "v"):
+            vals = W.decode_cache_values(w, b, n)  # [Hkv, L, d] fp32
+            c, s = sl8.quant_rowwise(torch.from_numpy(vals).to(DEV))
+            g[n][b, :, :L] = c
+            gs[n][b, :, :L] = s
+            if batches is None or b in batches:
+                oc, osc = oracle.quant_rowwise(vals)
+                o[n][b, :, :L] = oc
+                os_[n][b, :, :L] = osc
+    return lens, g, gs, o, os_
+
+
+CASES = [
+    # wid, B, Hq, Hkv, d, lengths, lmax
+    (3001, 6, 8, 2, 128, [1, 255, 256, 257, 700, 0], 700),
+    (3002, 3, 4, 4, 64, [513, 1, 1024], 1024),
+    (3003, 3, 8, 1, 256, [129, 300, 5], 300),
+    (3004, 2, 16, 2, 128, [2000, 77], 2000),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"w{c[0]}_d{c[4]}_G{c[2] // c[3]}" for c in CASES])
+def test_decode_small(case):
+    wid, B, Hq, Hkv, d, lens, lmax = case
+    w = W.custom(wid, kind="decode", B=B, Hq=Hq, Hkv=Hkv, d=d, dtype="bf16", extra={"lengths": lens})
+    lens_np, g, gs, o, os_ = build_cache(w, lmax)
+    torch.cuda.synchronize()
+    for n in ("k", "v"):
+        np.testing.assert_array_equal(g[n].cpu().numpy(), o[n])
+        np.testing.assert_array_equal(gs[n].cpu().numpy(), os_[n])
+    q = W.decode_query(w)
+    qd = q.to(DEV)
+    seq = torch.from_numpy(lens_np.astype(np.int32)).to(DEV)
+    dbg = sl8.attn_int8_decode_logits_debug(qd, g["k"], gs["k"], g["v"], gs["v"], seq)
+    ref = oracle.attn_decode(q.float().numpy(), o["k"], os_["k"], o["v"], os_["v"], lens_np, num_splits=1,
+                             want_logits=True)
+    np.testing.assert_array_equal(dbg["q_codes"].cpu().numpy(), ref["q_codes"])
+    np.testing.assert_array_equal(dbg["q_scales"].cpu().numpy(), ref["q_scales"])
+    lg = dbg["logits"].cpu().numpy()
+    for b in range(B):
+        for h in range(Hq):
+            np.testing.assert_array_equal(lg[b, h, :lens_np[b]], ref["logits"][(b, h)])
+    outs = {}
+    for ns in (0, 1, 3, 7):
+        o32, lse = sl8.attn_int8_decode(qd, g["k"], gs["k"], g["v"], gs["v"], seq, num_splits=ns,
+                                        out_dtype=torch.float32, return_lse=True)
+        ob = sl8.attn_int8_decode(qd, g["k"], gs["k"], g["v"], gs["v"], seq, num_splits=ns)
+        torch.cuda.synchronize()
+        outs[ns] = to_np32(o32)
+        check_f32(outs[ns], ref["out"], f"w{wid} splits={ns} f32")
+        check_half(ob, ref["out"], f"w{wid} splits={ns} bf16")
+        ok = lens_np > 0
+        np.testing.assert_allclose(to_np32(lse)[ok], ref["lse"][ok], rtol=0, atol=1e-4)
+        assert np.all(np.isneginf(to_np32(lse)[~ok]))
+    st, site = sl8.last_device_status()
+    assert st == sl8.SL8_OK, (st, site)
+
+
+def test_decode_partials_match_oracle_splits():
+    w = W.custom(3101, kind="decode", B=2, Hq=4, Hkv=2, d=128, dtype="bf16", extra={"lengths": [600, 130]})
+    lens_np, g, gs, o, os_ = build_cache(w, 600)
+    q = W.decode_query(w)
+    seq = torch.from_numpy(lens_np.astype(np.int32)).to(DEV)
+    op, lp = sl8.attn_int8_decode_splitkv(q.to(DEV), g["k"], gs["k"], g["v"], gs["v"], seq, num_splits=3)
+    torch.cuda.synchronize()
+    ref = oracle.attn_decode(q.float().numpy(), o["k"], os_["k"], o["v"], os_["v"], lens_np, split_size=200)
+    lpn = to_np32(lp)
+    live = np.isfinite(ref["lse_partial"])
+    np.testing.assert_array_equal(np.isneginf(lpn), ~live)
+    np.testing.assert_allclose(lpn[live], ref["lse_partial"][live], rtol=0, atol=1e-4)
+    check_f32(to_np32(op)[live], ref["o_partial"][live], "partials")
+
+
+def test_full_size_decode_workload():
+    w = W.get("decode")
+    sample_b = [0, 1, 17, 63]
+    lens_np, g, gs, o, os_ = build_cache(w, w.lmax, batches=set(sample_b))
+    q = W.decode_query(w)
+    seq = torch.from_numpy(lens_np.astype(np.int32)).to(DEV)
+    o32 = sl8.attn_int8_decode(q.to(DEV), g["k"], gs["k"], g["v"], gs["v"], seq, out_dtype=torch.float32)
+    ob = sl8.attn_int8_decode(q.to(DEV), g["k"], gs["k"], g["v"], gs["v"], seq)
+    dbg = sl8.attn_int8_decode_logits_debug(q.to(DEV), g["k"], gs["k"], g["v"], gs["v"], seq)
+    torch.cuda.synchronize()
+    st, site = sl8.last_device_status()
+    assert st == sl8.SL8_OK, (st, site)
+    rows = [(b, h) for b in sample_b for h in range(w.Hq)]
+    ref = oracle.attn_decode(q.float().numpy(), o["k"], os_["k"], o["v"], os_["v"], lens_np, rows=rows,
+                             want_logits=True)
+    sel = np.zeros((w.B, w.Hq), bool)
+    for b, h in rows:
+        sel[b, h] = True
+    refo = np.where(sel[..., None], ref["out"], np.nan)
+    check_f32(to_np32(o32), refo, "decode full f32")
+    check_half(ob, refo, "decode full bf16")
+    lg = dbg["logits"].cpu().numpy()
+    for (b, h) in rows:
+        np.testing.assert_array_equal(lg[b, h, :lens_np[b]], ref["logits"][(b, h)])
+    for b in sample_b:
+        np.testing.assert_array_equal(g["k"][b].cpu().numpy(), o["k"][b])

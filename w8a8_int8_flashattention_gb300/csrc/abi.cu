@@ -1,0 +1,578 @@
+// C ABI of libsl8: argument validation, workspace planning, the per-device status
+// word, tensor-map encoding and kernel tracing.  The kernels live in quant.cu,
+// prefill.cu and decode.cu; every entry point here only validates and enqueues.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "sl8_internal.h"
+
+namespace sl8 {
+
+// ---------------------------------------------------------------- device status
+// One status word per device (a __device__ variable: loaded with the module, no
+// allocation).  Its address is looked up once per device.
+static __device__ DeviceStatus g_device_status;
+
+static constexpr int kMaxDevices = 64;
+static std::mutex g_mu;
+static DeviceStatus* g_status_ptr[kMaxDevices] = {};
+static int g_num_sms[kMaxDevices] = {};
+static std::atomic<uint64_t> g_spin_limit_ns{2000000000ull};
+
+static int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+
+DeviceStatus* device_status_ptr() {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<DeviceStatus*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+int num_sms() {
+  const int dev = current_device();
+  if (dev < 0) return 1;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_num_sms[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    g_num_sms[dev] = n;
+  }
+  return g_num_sms[dev];
+}
+
+uint64_t spin_limit_ns() { return g_spin_limit_ns.load(std::memory_order_relaxed); }
+
+// ---------------------------------------------------------------- tensor maps
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// 3-D tiled map with 128-byte swizzle and zero fill out of bounds.
+CUtensorMap make_tmap_3d(const void* base, CUtensorMapDataType dt, uint64_t d0, uint64_t d1, uint64_t d2,
+                         uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2,
+                         bool* ok) {
+  CUtensorMap m;
+  memset(&m, 0, sizeof(m));
+  auto fn = encode_fn();
+  if (!fn) {
+    *ok = false;
+    return m;
+  }
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(&m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) *ok = false;
+  return m;
+}
+
+// ---------------------------------------------------------------- tracing
+struct TraceRec {
+  const char* name;
+  cudaEvent_t start, stop;
+};
+static std::atomic<int> g_trace_on{0};
+static std::mutex g_trace_mu;
+static std::vector<TraceRec> g_trace;
+static std::vector<cudaEvent_t> g_event_pool;
+
+static cudaEvent_t take_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+TraceScope::TraceScope(const char* name, cudaStream_t s) : slot(-1), stream(s) {
+  if (!g_trace_on.load(std::memory_order_relaxed)) return;
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  TraceRec r{name, take_event(), take_event()};
+  if (!r.start || !r.stop) return;
+  cudaEventRecord(r.start, s);
+  g_trace.push_back(r);
+  slot = static_cast<int>(g_trace.size()) - 1;
+}
+
+TraceScope::~TraceScope() {
+  if (slot < 0) return;
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (slot < static_cast<int>(g_trace.size())) cudaEventRecord(g_trace[slot].stop, stream);
+}
+
+// ---------------------------------------------------------------- workspace plans
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+PrefillWorkspace plan_prefill_workspace(int32_t nseq, int32_t Hq, int32_t Hkv, int32_t N, int32_t d,
+                                        int64_t total_tokens, bool varlen) {
+  PrefillWorkspace w{};
+  w.max_tiles = (N + kQTile - 1) / kQTile;
+  w.max_chunks = (N + kMeanChunk - 1) / kMeanChunk;
+  const int64_t dense_rows = static_cast<int64_t>(nseq) * w.max_tiles * kPadRows;
+  if (varlen) {
+    const int64_t bound = (total_tokens + static_cast<int64_t>(nseq) * (kPadRows - 1)) / kPadRows * kPadRows;
+    w.t_pad_max = bound < dense_rows ? bound : dense_rows;
+    const int64_t pb = (total_tokens + kQTile - 1) / kQTile + nseq;
+    w.max_pairs = pb < static_cast<int64_t>(nseq) * w.max_tiles ? pb : static_cast<int64_t>(nseq) * w.max_tiles;
+  } else {
+    w.t_pad_max = dense_rows;
+    w.max_pairs = static_cast<int64_t>(nseq) * w.max_tiles;
+  }
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  w.q_codes = take(static_cast<size_t>(Hq) * w.t_pad_max * d * 2);
+  w.q_scales = take(static_cast<size_t>(Hq) * w.t_pad_max * 4);
+  w.k_codes = take(static_cast<size_t>(Hkv) * w.t_pad_max * d * 2);
+  w.k_scales = take(static_cast<size_t>(Hkv) * w.t_pad_max * 4);
+  w.v16 = take(static_cast<size_t>(Hkv) * w.t_pad_max * d * 2);
+  w.k_mean = take(static_cast<size_t>(nseq) * Hkv * d * 4);
+  w.k_partials = take(static_cast<size_t>(nseq) * Hkv * w.max_chunks * d * 4);
+  w.v_partials = take(static_cast<size_t>(nseq) * Hkv * w.max_chunks * 4);
+  w.v_exp = take(static_cast<size_t>(nseq) * Hkv * 4);
+  w.pstart = take(static_cast<size_t>(nseq) * 4);
+  w.len = take(static_cast<size_t>(nseq) * 4);
+  w.tok0 = take(static_cast<size_t>(nseq) * 4);
+  w.pair_seq = take(static_cast<size_t>(w.max_pairs) * 4);
+  w.pair_qt = take(static_cast<size_t>(w.max_pairs) * 4);
+  w.counts = take(16);
+  w.hist = take(static_cast<size_t>(3) * (w.max_tiles + 2) * 4);
+  w.sorted = take(static_cast<size_t>(nseq) * 4);
+  w.total = off;
+  return w;
+}
+
+static SeqTable table_at(void* ws, const PrefillWorkspace& p) {
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  SeqTable t;
+  t.pstart = reinterpret_cast<int32_t*>(b + p.pstart);
+  t.len = reinterpret_cast<int32_t*>(b + p.len);
+  t.tok0 = reinterpret_cast<int32_t*>(b + p.tok0);
+  t.pair_seq = reinterpret_cast<int32_t*>(b + p.pair_seq);
+  t.pair_qt = reinterpret_cast<int32_t*>(b + p.pair_qt);
+  t.counts = reinterpret_cast<int32_t*>(b + p.counts);
+  t.hist = reinterpret_cast<int32_t*>(b + p.hist);
+  t.sorted = reinterpret_cast<int32_t*>(b + p.sorted);
+  return t;
+}
+
+}  // namespace sl8
+
+using namespace sl8;
+
+// ---------------------------------------------------------------- validation helpers
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool is_half(int dt) { return dt == SL8_F16 || dt == SL8_BF16; }
+bool head_dim_ok(int32_t d) { return d == 64 || d == 128 || d == 256; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? SL8_OK : SL8_ERR_CUDA; }
+
+#define SL8_CHECK(cond, code) \
+  do {                        \
+    if (!(cond)) return (code); \
+  } while (0)
+
+#define SL8_LAUNCH(expr)                     \
+  do {                                       \
+    cudaError_t e_ = (expr);                 \
+    if (e_ != cudaSuccess) return SL8_ERR_CUDA; \
+  } while (0)
+
+int validate_prefill(const void* q, const void* k, int qk_dtype, int32_t B, int32_t Hq, int32_t Hkv, int32_t N,
+                     int32_t d) {
+  SL8_CHECK(q && k, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(aligned16(q) && aligned16(k), SL8_ERR_INVALID_ARG);
+  SL8_CHECK(is_half(qk_dtype), SL8_ERR_INVALID_ARG);
+  SL8_CHECK(B >= 0 && N >= 0 && Hq > 0 && Hkv > 0 && d > 0, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(Hq % Hkv == 0, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(head_dim_ok(d), SL8_ERR_UNSUPPORTED);
+  SL8_CHECK(N <= (1 << 24) && B <= (1 << 24), SL8_ERR_UNSUPPORTED);
+  return SL8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sl8_status_string(int status) {
+  switch (status) {
+    case SL8_OK: return "ok";
+    case SL8_ERR_INVALID_ARG: return "invalid argument";
+    case SL8_ERR_UNSUPPORTED: return "unsupported configuration";
+    case SL8_ERR_WORKSPACE: return "workspace missing or too small";
+    case SL8_ERR_CUDA: return "CUDA error";
+    case SL8_ERR_TIMEOUT: return "device-side wait timed out";
+    case SL8_ERR_DEVICE_ARG: return "device-side argument out of range";
+    default: return "unknown status";
+  }
+}
+
+int sl8_version(void) { return 100; }
+
+int sl8_quant_rowwise(const void* x, int x_dtype, int64_t rows, int32_t cols, int64_t row_stride_elems,
+                      const float* sub_mean, int64_t rows_per_group, int8_t* q_out, float* scale_out, void* stream) {
+  if (rows == 0 && cols >= 1) return SL8_OK;  // nothing to read or write; pointers may be null
+  SL8_CHECK(x && q_out && scale_out, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(x_dtype == SL8_F16 || x_dtype == SL8_BF16 || x_dtype == SL8_F32, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(rows >= 0 && cols >= 1 && row_stride_elems >= cols, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(!sub_mean || rows_per_group >= 1, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(rows / 8 < (1ll << 31), SL8_ERR_UNSUPPORTED);
+  if (rows == 0) return SL8_OK;
+  return cuda_status(launch_quant_rowwise(x, static_cast<sl8_dtype>(x_dtype), rows, cols, row_stride_elems, sub_mean,
+                                          sub_mean ? rows_per_group : 1, q_out, scale_out,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+size_t sl8_k_channel_mean_workspace_size(int32_t B, int32_t Hkv, int32_t N, int32_t d) {
+  if (B < 0 || Hkv <= 0 || N < 0 || d <= 0) return 0;
+  // the table part of the prefill plan (Hq = Hkv) plus the chunk partials
+  const PrefillWorkspace p = plan_prefill_workspace(B, Hkv, Hkv, N, d, 0, false);
+  return p.total - p.k_mean;
+}
+
+int sl8_k_channel_mean(const void* k, int k_dtype, int32_t B, int32_t Hkv, int32_t N, int32_t d,
+                       const int32_t* cu_seqlens, int64_t total_tokens, float* mean_out, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  SL8_CHECK(k && mean_out && aligned16(k), SL8_ERR_INVALID_ARG);
+  SL8_CHECK(k_dtype == SL8_F16 || k_dtype == SL8_BF16 || k_dtype == SL8_F32, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(B >= 0 && Hkv > 0 && N >= 0 && d > 0 && d <= 1024, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(!cu_seqlens || total_tokens >= 0, SL8_ERR_INVALID_ARG);
+  if (B == 0 || N == 0) return SL8_OK;
+  const size_t need = sl8_k_channel_mean_workspace_size(B, Hkv, N, d);
+  SL8_CHECK(workspace && workspace_bytes >= need && aligned16(workspace), SL8_ERR_WORKSPACE);
+  // reuse the prefill plan's layout shifted so that k_mean starts at the workspace base
+  const PrefillWorkspace p = plan_prefill_workspace(B, Hkv, Hkv, N, d, 0, false);
+  uint8_t* base = static_cast<uint8_t*>(workspace) - p.k_mean;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const SeqTable t = table_at(base, p);
+  SL8_LAUNCH(launch_schedule(cu_seqlens, B, N, cu_seqlens ? total_tokens : static_cast<int64_t>(B) * N,
+                             static_cast<int64_t>(B) * p.max_tiles * kPadRows, t, p.max_tiles, s));
+  SL8_LAUNCH(launch_kv_stats(k, static_cast<sl8_dtype>(k_dtype), nullptr, cu_seqlens != nullptr, B, Hkv, N, d, t.len,
+                             t.tok0, reinterpret_cast<float*>(base + p.k_partials), nullptr, p.max_chunks, mean_out,
+                             nullptr, s));
+  return SL8_OK;
+}
+
+size_t sl8_attn_int8_fwd_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t N, int32_t d,
+                                        int64_t total_tokens) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || N < 0 || d <= 0 || total_tokens < 0) return 0;
+  return plan_prefill_workspace(B, Hq, Hkv, N, d, total_tokens, total_tokens > 0).total;
+}
+
+// Scheduler, K/V statistics and quantisation ahead of the attention kernel.  With a
+// bf16 V (v non-null) V is also re-expressed in fp16 (scaled by 2^-e) for the P.V MMA.
+static int prefill_prepare(const void* q, const void* k, const void* v, int qk_dtype, int v_dtype, int32_t B,
+                           int32_t Hq, int32_t Hkv, int32_t N, int32_t d, const int32_t* cu_seqlens,
+                           int64_t total_tokens, int smooth_k, void* workspace, size_t workspace_bytes,
+                           cudaStream_t s, PrefillWorkspace* plan, SeqTable* table) {
+  const bool varlen = cu_seqlens != nullptr;
+  const PrefillWorkspace p = plan_prefill_workspace(B, Hq, Hkv, N, d, varlen ? total_tokens : 0, varlen);
+  SL8_CHECK(workspace && aligned16(workspace) && workspace_bytes >= p.total, SL8_ERR_WORKSPACE);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const SeqTable t = table_at(ws, p);
+  const int64_t tokens = varlen ? total_tokens : static_cast<int64_t>(B) * N;
+  const bool convert_v = v && v_dtype == SL8_BF16;
+  SL8_LAUNCH(launch_schedule(cu_seqlens, B, N, tokens, p.t_pad_max, t, p.max_tiles, s));
+  float* mean = smooth_k ? reinterpret_cast<float*>(ws + p.k_mean) : nullptr;
+  int32_t* v_exp = convert_v ? reinterpret_cast<int32_t*>(ws + p.v_exp) : nullptr;
+  if (smooth_k || convert_v) {
+    SL8_LAUNCH(launch_kv_stats(k, static_cast<sl8_dtype>(qk_dtype), convert_v ? v : nullptr, varlen, B, Hkv, N, d,
+                               t.len, t.tok0, smooth_k ? reinterpret_cast<float*>(ws + p.k_partials) : nullptr,
+                               convert_v ? reinterpret_cast<float*>(ws + p.v_partials) : nullptr, p.max_chunks, mean,
+                               v_exp, s));
+  }
+  SL8_LAUNCH(launch_quant_codes(k, static_cast<sl8_dtype>(qk_dtype), varlen, B, Hkv, N, d, tokens, t, p.t_pad_max,
+                                mean, reinterpret_cast<uint16_t*>(ws + p.k_codes),
+                                reinterpret_cast<float*>(ws + p.k_scales), convert_v ? v : nullptr, v_exp,
+                                convert_v ? reinterpret_cast<uint16_t*>(ws + p.v16) : nullptr, true, s));
+  SL8_LAUNCH(launch_quant_codes(q, static_cast<sl8_dtype>(qk_dtype), varlen, B, Hq, N, d, tokens, t, p.t_pad_max,
+                                nullptr, reinterpret_cast<uint16_t*>(ws + p.q_codes),
+                                reinterpret_cast<float*>(ws + p.q_scales), nullptr, nullptr, nullptr, false, s));
+  *plan = p;
+  *table = t;
+  return SL8_OK;
+}
+
+int sl8_attn_int8_fwd(const void* q, const void* k, const void* v, int qk_dtype, int v_dtype, int32_t B, int32_t Hq,
+                      int32_t Hkv, int32_t N, int32_t d, const int32_t* cu_seqlens, int64_t total_tokens,
+                      int causal, int smooth_k, void* out, int out_dtype, float* lse_out, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  int rc = validate_prefill(q, k, qk_dtype, B, Hq, Hkv, N, d);
+  if (rc != SL8_OK) return rc;
+  SL8_CHECK(v && out && aligned16(v) && aligned16(out), SL8_ERR_INVALID_ARG);
+  SL8_CHECK(is_half(v_dtype), SL8_ERR_INVALID_ARG);
+  SL8_CHECK(out_dtype == v_dtype || out_dtype == SL8_F32, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(!cu_seqlens || total_tokens >= 0, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(!cu_seqlens || total_tokens < (1ll << 31), SL8_ERR_UNSUPPORTED);
+  SL8_CHECK(static_cast<int64_t>(B) * N < (1ll << 31), SL8_ERR_UNSUPPORTED);
+  if (B == 0 || N == 0 || (cu_seqlens && total_tokens == 0)) return SL8_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PrefillWorkspace p;
+  SeqTable t;
+  rc = prefill_prepare(q, k, v, qk_dtype, v_dtype, B, Hq, Hkv, N, d, cu_seqlens, total_tokens, smooth_k, workspace,
+                       workspace_bytes, s, &p, &t);
+  if (rc != SL8_OK) return rc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  PrefillArgs a{};
+  a.q_codes = reinterpret_cast<const uint16_t*>(ws + p.q_codes);
+  a.q_scales = reinterpret_cast<const float*>(ws + p.q_scales);
+  a.k_codes = reinterpret_cast<const uint16_t*>(ws + p.k_codes);
+  a.k_scales = reinterpret_cast<const float*>(ws + p.k_scales);
+  a.v = v;
+  a.v_dtype = static_cast<sl8_dtype>(v_dtype);
+  if (v_dtype == SL8_BF16) {
+    a.v16 = reinterpret_cast<const uint16_t*>(ws + p.v16);
+    a.v_exp = reinterpret_cast<const int32_t*>(ws + p.v_exp);
+  }
+  a.varlen = cu_seqlens != nullptr;
+  a.nseq = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.N = N;
+  a.d = d;
+  a.total_tokens = a.varlen ? total_tokens : static_cast<int64_t>(B) * N;
+  a.t_pad_max = p.t_pad_max;
+  a.table = t;
+  a.max_pairs = p.max_pairs;
+  a.causal = causal != 0;
+  a.out = out;
+  a.out_dtype = static_cast<sl8_dtype>(out_dtype);
+  a.lse = lse_out;
+  a.logits = nullptr;
+  SL8_LAUNCH(launch_prefill(a, s));
+  return SL8_OK;
+}
+
+int sl8_attn_int8_qk_logits_debug(const void* q, const void* k, int qk_dtype, int32_t B, int32_t Hq, int32_t Hkv,
+                                  int32_t N, int32_t d, int smooth_k, int32_t row_begin, int32_t row_end,
+                                  int32_t* logits_out, int8_t* q_codes, float* q_scales, int8_t* k_codes,
+                                  float* k_scales, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = validate_prefill(q, k, qk_dtype, B, Hq, Hkv, N, d);
+  if (rc != SL8_OK) return rc;
+  SL8_CHECK(0 <= row_begin && row_begin <= row_end && row_end <= N, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(static_cast<int64_t>(B) * N < (1ll << 31), SL8_ERR_UNSUPPORTED);
+  SL8_CHECK(!q_codes == !q_scales && !k_codes == !k_scales, SL8_ERR_INVALID_ARG);
+  if (B == 0 || N == 0) return SL8_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PrefillWorkspace p;
+  SeqTable t;
+  rc = prefill_prepare(q, k, nullptr, qk_dtype, qk_dtype, B, Hq, Hkv, N, d, nullptr, 0, smooth_k, workspace,
+                       workspace_bytes, s, &p, &t);
+  if (rc != SL8_OK) return rc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (q_codes)
+    SL8_LAUNCH(launch_export_codes(reinterpret_cast<const uint16_t*>(ws + p.q_codes),
+                                   reinterpret_cast<const float*>(ws + p.q_scales), false, B, Hq, N, d, t, p.t_pad_max,
+                                   q_codes, q_scales, s));
+  if (k_codes)
+    SL8_LAUNCH(launch_export_codes(reinterpret_cast<const uint16_t*>(ws + p.k_codes),
+                                   reinterpret_cast<const float*>(ws + p.k_scales), false, B, Hkv, N, d, t,
+                                   p.t_pad_max, k_codes, k_scales, s));
+  if (logits_out && row_end > row_begin) {
+    PrefillArgs a{};
+    a.q_codes = reinterpret_cast<const uint16_t*>(ws + p.q_codes);
+    a.q_scales = reinterpret_cast<const float*>(ws + p.q_scales);
+    a.k_codes = reinterpret_cast<const uint16_t*>(ws + p.k_codes);
+    a.k_scales = reinterpret_cast<const float*>(ws + p.k_scales);
+    a.v = q;  // V is not used for logits; any readable [B, Hkv, N, d] tensor keeps the map valid
+    a.v_dtype = SL8_F16;
+    a.varlen = false;
+    a.nseq = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.N = N;
+    a.d = d;
+    a.total_tokens = static_cast<int64_t>(B) * N;
+    a.t_pad_max = p.t_pad_max;
+    a.table = t;
+    a.max_pairs = p.max_pairs;
+    a.causal = false;
+    a.out = nullptr;
+    a.out_dtype = SL8_F32;
+    a.lse = nullptr;
+    a.logits = logits_out;
+    a.row_begin = row_begin;
+    a.row_end = row_end;
+    SL8_LAUNCH(launch_prefill(a, s));
+  }
+  return SL8_OK;
+}
+
+// The split plan: S = num_splits (or ceil(Lmax / chunk) when 0), capped at Lmax; every
+// split but possibly the last covers split_size = ceil(Lmax / S) tokens.  Both the split
+// kernel and the combine derive split_size from (Lmax, S) with this one formula.
+int32_t sl8_attn_decode_num_splits(int32_t Lmax, int32_t d, int32_t num_splits) {
+  if (Lmax <= 0 || !head_dim_ok(d) || num_splits < 0) return 0;
+  int32_t n = num_splits > 0 ? num_splits : (Lmax + decode_chunk_tokens(d) - 1) / decode_chunk_tokens(d);
+  return n < Lmax ? n : Lmax;
+}
+
+int32_t sl8_attn_decode_split_size(int32_t Lmax, int32_t d, int32_t num_splits) {
+  const int32_t S = sl8_attn_decode_num_splits(Lmax, d, num_splits);
+  return S > 0 ? (Lmax + S - 1) / S : 0;
+}
+
+static int decode_validate(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale,
+                           const int8_t* v_cache, const float* v_scale, const int32_t* seqlens, int32_t B, int32_t Hq,
+                           int32_t Hkv, int32_t Lmax, int32_t d) {
+  SL8_CHECK(q && k_cache && k_scale && v_cache && v_scale && seqlens, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(aligned16(q) && aligned16(k_cache) && aligned16(v_cache), SL8_ERR_INVALID_ARG);
+  SL8_CHECK(q_dtype == SL8_F16 || q_dtype == SL8_BF16 || q_dtype == SL8_F32, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(B >= 0 && Hq > 0 && Hkv > 0 && Lmax >= 0 && d > 0, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(Hq % Hkv == 0, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(head_dim_ok(d), SL8_ERR_UNSUPPORTED);
+  SL8_CHECK(Hq / Hkv <= 8, SL8_ERR_UNSUPPORTED);
+  SL8_CHECK(B <= 65535 && Hkv <= 65535, SL8_ERR_UNSUPPORTED);
+  return SL8_OK;
+}
+
+static int decode_launch(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale, const int8_t* v_cache,
+                         const float* v_scale, const int32_t* seqlens, int32_t B, int32_t Hq, int32_t Hkv, int32_t Lmax,
+                         int32_t d, int32_t num_splits, float* o_partial, float* lse_partial, int32_t* logits,
+                         int8_t* q_codes, float* q_scales, void* stream) {
+  int rc = decode_validate(q, q_dtype, k_cache, k_scale, v_cache, v_scale, seqlens, B, Hq, Hkv, Lmax, d);
+  if (rc != SL8_OK) return rc;
+  SL8_CHECK(o_partial && lse_partial && num_splits >= 0, SL8_ERR_INVALID_ARG);
+  if (B == 0 || Lmax == 0) return SL8_OK;
+  DecodeArgs a{};
+  a.q = q;
+  a.q_dtype = static_cast<sl8_dtype>(q_dtype);
+  a.k_cache = k_cache;
+  a.k_scale = k_scale;
+  a.v_cache = v_cache;
+  a.v_scale = v_scale;
+  a.seqlens = seqlens;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Lmax = Lmax;
+  a.d = d;
+  a.split_size = sl8_attn_decode_split_size(Lmax, d, num_splits);
+  a.num_splits = sl8_attn_decode_num_splits(Lmax, d, num_splits);
+  SL8_CHECK(a.num_splits > 0 && a.num_splits <= 65535, SL8_ERR_UNSUPPORTED);
+  a.o_partial = o_partial;
+  a.lse_partial = lse_partial;
+  a.logits = logits;
+  a.q_codes = q_codes;
+  a.q_scales = q_scales;
+  SL8_LAUNCH(launch_decode_split(a, static_cast<cudaStream_t>(stream)));
+  return SL8_OK;
+}
+
+int sl8_attn_int8_decode_splitkv(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale,
+                                 const int8_t* v_cache, const float* v_scale, const int32_t* seqlens, int32_t B,
+                                 int32_t Hq, int32_t Hkv, int32_t Lmax, int32_t d, int32_t num_splits,
+                                 float* o_partial, float* lse_partial, void* stream) {
+  return decode_launch(q, q_dtype, k_cache, k_scale, v_cache, v_scale, seqlens, B, Hq, Hkv, Lmax, d, num_splits,
+                       o_partial, lse_partial, nullptr, nullptr, nullptr, stream);
+}
+
+int sl8_attn_decode_combine(const float* o_partial, const float* lse_partial, const int32_t* seqlens, int32_t B,
+                            int32_t Hq, int32_t Lmax, int32_t d, int32_t num_splits, void* out, int out_dtype,
+                            float* lse_out, void* stream) {
+  SL8_CHECK(o_partial && lse_partial && seqlens && out, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(out_dtype == SL8_F16 || out_dtype == SL8_BF16 || out_dtype == SL8_F32, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(B >= 0 && Hq > 0 && Lmax >= 0 && num_splits >= 1, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(head_dim_ok(d), SL8_ERR_UNSUPPORTED);
+  if (B == 0) return SL8_OK;
+  SL8_CHECK(num_splits <= (Lmax > 0 ? Lmax : 1), SL8_ERR_INVALID_ARG);
+  const int32_t split_size = Lmax > 0 ? (Lmax + num_splits - 1) / num_splits : 1;
+  SL8_LAUNCH(launch_decode_combine(o_partial, lse_partial, seqlens, B, Hq, d, num_splits, split_size, out,
+                                   static_cast<sl8_dtype>(out_dtype), lse_out, static_cast<cudaStream_t>(stream)));
+  return SL8_OK;
+}
+
+int sl8_attn_int8_decode_logits_debug(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale,
+                                      const int8_t* v_cache, const float* v_scale, const int32_t* seqlens,
+                                      int32_t B, int32_t Hq, int32_t Hkv, int32_t Lmax, int32_t d,
+                                      int32_t* logits_out, int8_t* q_codes, float* q_scales, float* o_partial,
+                                      float* lse_partial, void* stream) {
+  SL8_CHECK(logits_out, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(!q_codes == !q_scales, SL8_ERR_INVALID_ARG);
+  return decode_launch(q, q_dtype, k_cache, k_scale, v_cache, v_scale, seqlens, B, Hq, Hkv, Lmax, d, 0, o_partial,
+                       lse_partial, logits_out, q_codes, q_scales, stream);
+}
+
+int sl8_last_device_status(void* stream, int* site) {
+  if (site) *site = 0;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SL8_ERR_CUDA;
+  DeviceStatus* p = device_status_ptr();
+  if (!p) return SL8_ERR_CUDA;
+  DeviceStatus h{};
+  if (cudaMemcpy(&h, p, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return SL8_ERR_CUDA;
+  if (h.code == kStatusOk) return SL8_OK;
+  if (cudaMemset(p, 0, sizeof(DeviceStatus)) != cudaSuccess) return SL8_ERR_CUDA;
+  if (site) *site = h.site;
+  return h.code == kStatusTimeout ? SL8_ERR_TIMEOUT : SL8_ERR_DEVICE_ARG;
+}
+
+void sl8_set_spin_limit_ns(uint64_t limit_ns) {
+  g_spin_limit_ns.store(limit_ns ? limit_ns : 1, std::memory_order_relaxed);
+}
+uint64_t sl8_get_spin_limit_ns(void) { return spin_limit_ns(); }
+
+int sl8_selftest_timeout(uint64_t limit_ns, void* stream) {
+  SL8_LAUNCH(launch_timeout_selftest(limit_ns, static_cast<cudaStream_t>(stream)));
+  return SL8_OK;
+}
+
+void sl8_trace_enable(int on) { g_trace_on.store(on ? 1 : 0); }
+
+int sl8_trace_collect(const char** names, int64_t* launches, double* total_ms, int max) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  int n = 0;
+  for (const TraceRec& r : g_trace) {
+    float ms = 0.0f;
+    if (cudaEventSynchronize(r.stop) == cudaSuccess) cudaEventElapsedTime(&ms, r.start, r.stop);
+    int i = 0;
+    while (i < n && std::strcmp(names[i], r.name) != 0) ++i;
+    if (i == n) {
+      if (n == max) continue;
+      names[n] = r.name;
+      launches[n] = 0;
+      total_ms[n] = 0.0;
+      ++n;
+    }
+    launches[i] += 1;
+    total_ms[i] += ms;
+    g_event_pool.push_back(r.start);
+    g_event_pool.push_back(r.stop);
+  }
+  g_trace.clear();
+  return n;
+}
+
+}  // extern "C"

@@ -1,0 +1,133 @@
+// Internal declarations shared by the ABI layer and the kernel translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/sl8.h"
+#include "sm103_ptx.cuh"
+
+namespace sl8 {
+
+constexpr int kQTile = 128;      // query rows per prefill work item (MMA M)
+constexpr int kPadRows = 128;    // each sequence starts at a multiple of this in the code workspace
+constexpr int kMeanChunk = 64;   // K-smoothing summation chunk (tokens)
+
+// Per-sequence table and work list written by the scheduler kernel into the
+// prefill workspace.  All arrays are int32.
+struct SeqTable {
+  int32_t* pstart;   // [nseq]  first padded row of the sequence in the code workspace
+  int32_t* len;      // [nseq]  sequence length
+  int32_t* tok0;     // [nseq]  first token of the sequence in the caller's tensors (varlen: cu_seqlens[s])
+  int32_t* pair_seq; // [max_pairs] work list: sequence of each (sequence, q-tile) pair
+  int32_t* pair_qt;  // [max_pairs] q-tile index of each pair
+  int32_t* counts;   // [4]: 0 = number of pairs, 1 = total padded rows
+  int32_t* hist;     // [max_tiles + 2] scratch for the scheduler
+  int32_t* sorted;   // [nseq] scratch: sequences ordered by tile count, longest first
+};
+
+// Carve-up of the prefill workspace (byte offsets from its base).
+struct PrefillWorkspace {
+  size_t q_codes, q_scales, k_codes, k_scales, v16, k_mean, k_partials, v_partials, v_exp;
+  size_t pstart, len, tok0, pair_seq, pair_qt, counts, hist, sorted;
+  size_t total;
+  int64_t t_pad_max;   // rows reserved per head in the code workspace
+  int32_t max_chunks;  // 64-token chunks per sequence (upper bound)
+  int32_t max_tiles;   // q tiles per sequence (upper bound)
+  int64_t max_pairs;
+};
+PrefillWorkspace plan_prefill_workspace(int32_t nseq, int32_t Hq, int32_t Hkv, int32_t N, int32_t d,
+                                        int64_t total_tokens, bool varlen);
+
+// Device pointer of the library's status word on the current device.
+DeviceStatus* device_status_ptr();
+uint64_t spin_limit_ns();
+int num_sms();
+
+// ---- tracing (CUDA events around each launch when enabled)
+struct TraceScope {
+  TraceScope(const char* name, cudaStream_t s);
+  ~TraceScope();
+  int slot;
+  cudaStream_t stream;
+};
+
+// ---- launchers (return a cudaError_t from the launch)
+// cu_seqlens (nullable = dense) must describe sequences inside [0, total_tokens) whose
+// padded rows fit in t_pad_max; violations are recorded as a device-side argument
+// error and the affected work is dropped.
+cudaError_t launch_schedule(const int32_t* cu_seqlens, int32_t nseq, int32_t N, int64_t total_tokens,
+                            int64_t t_pad_max, const SeqTable& t, int32_t max_tiles, cudaStream_t s);
+// K chunk sums (k_partials, nullable) and V chunk abs-max (v_partials, nullable; V bf16),
+// then the K mean [nseq][Hkv][d] and the V power-of-two exponent [nseq][Hkv].
+cudaError_t launch_kv_stats(const void* k, sl8_dtype dt, const void* v, bool varlen, int32_t nseq, int32_t Hkv,
+                            int32_t N, int32_t d, const int32_t* len, const int32_t* tok0, float* k_partials,
+                            float* v_partials, int32_t max_chunks, float* mean, int32_t* v_exp, cudaStream_t s);
+// Quantise Q or K rows of the caller's tensor into the padded bf16-code workspace; with
+// v16 set (K pass, V bf16) also write V as fp16 * 2^-v_exp into the padded layout.
+cudaError_t launch_quant_codes(const void* x, sl8_dtype dt, bool varlen, int32_t nseq, int32_t H, int32_t N,
+                               int32_t d, int64_t total_tokens, const SeqTable& t, int64_t t_pad_max,
+                               const float* mean, uint16_t* codes, float* scales, const void* v,
+                               const int32_t* v_exp, uint16_t* v16, bool is_k, cudaStream_t s);
+cudaError_t launch_quant_rowwise(const void* x, sl8_dtype dt, int64_t rows, int32_t cols, int64_t row_stride,
+                                 const float* sub_mean, int64_t rows_per_group, int8_t* q_out, float* scale_out,
+                                 cudaStream_t s);
+cudaError_t launch_export_codes(const uint16_t* codes, const float* scales, bool varlen, int32_t nseq, int32_t H,
+                                int32_t N, int32_t d, const SeqTable& t, int64_t t_pad_max, int8_t* codes_out,
+                                float* scales_out, cudaStream_t s);
+
+struct PrefillArgs {
+  const uint16_t* q_codes;  // [Hq][t_pad][d] bf16 codes
+  const float* q_scales;    // [Hq][t_pad]
+  const uint16_t* k_codes;  // [Hkv][t_pad][d]
+  const float* k_scales;    // [Hkv][t_pad]
+  const void* v;            // caller's V (used when it is fp16)
+  sl8_dtype v_dtype;
+  const uint16_t* v16;      // [Hkv][t_pad][d] fp16 copy of a bf16 V scaled by 2^-v_exp (nullable)
+  const int32_t* v_exp;     // [nseq][Hkv] (nullable = 0)
+  bool varlen;
+  int32_t nseq, Hq, Hkv, N, d;
+  int64_t total_tokens;
+  int64_t t_pad_max;
+  SeqTable table;
+  int64_t max_pairs;
+  bool causal;
+  void* out;                // caller's output
+  sl8_dtype out_dtype;
+  float* lse;               // nullable
+  int32_t* logits;          // debug mode: [nseq][Hq][row_end-row_begin][N] int32 (dense only)
+  int32_t row_begin, row_end;
+};
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
+
+struct DecodeArgs {
+  const void* q;
+  sl8_dtype q_dtype;
+  const int8_t* k_cache;
+  const float* k_scale;
+  const int8_t* v_cache;
+  const float* v_scale;
+  const int32_t* seqlens;
+  int32_t B, Hq, Hkv, Lmax, d, num_splits, split_size;
+  float* o_partial;
+  float* lse_partial;
+  int32_t* logits;   // debug: [B][Hq][Lmax] int32 (nullable)
+  int8_t* q_codes;   // nullable
+  float* q_scales;   // nullable
+};
+cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_combine(const float* o_partial, const float* lse_partial, const int32_t* seqlens,
+                                  int32_t B, int32_t Hq, int32_t d, int32_t num_splits, int32_t split_size,
+                                  void* out, sl8_dtype out_dtype, float* lse_out, cudaStream_t s);
+cudaError_t launch_timeout_selftest(uint64_t limit_ns, cudaStream_t s);
+
+// tokens per decode sub-chunk for head dim d (the automatic split size)
+int decode_chunk_tokens(int d);
+
+// 3-D tiled tensor map, 128-byte swizzle, zero fill out of bounds; *ok = false on failure.
+CUtensorMap make_tmap_3d(const void* base, CUtensorMapDataType dt, uint64_t d0, uint64_t d1, uint64_t d2,
+                         uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2,
+                         bool* ok);
+
+}  // namespace sl8

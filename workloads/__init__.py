@@ -170,3 +170,10 @@ def decode_cache_values(w: Workload, b: int, which: str) -> np.ndarray:
     L = int(seq_lengths(w)[b])
     tag = TAG_K if which == "k" else TAG_V
     return _rng(w, tag, b).standard_normal((w.Hkv, L, w.d), dtype=np.float32)
+
+
+def custom(wid: int, kind: str = "prefill", **fields) -> Workload:
+    """A workload of any shape with its own seed id (test cases beyond the five above)."""
+    base = dict(name=f"custom{wid}", kind=kind, B=1, Hq=1, Hkv=1, d=128)
+    base.update(fields)
+    return Workload(wid=wid, **base)
