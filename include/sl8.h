@@ -196,6 +196,30 @@ SL8_API int sl8_attn_int8_decode_logits_debug(const void* q, int q_dtype, const 
                                       float* lse_partial, void* stream);
 
 /*
+ * Decode without any allocation (no counterpart on the SuperL8 pages: it exists for
+ * callers that cannot allocate GPU memory where they run decode -- a serving loop with
+ * a fixed memory budget, code that only holds tensors another framework owns, a C
+ * caller without an allocator -- and for whom cudaMalloc would also stall the device).
+ * Same inputs and result as sl8_attn_int8_decode_splitkv followed by
+ * sl8_attn_decode_combine (out [B][Hq][d] of out_dtype, F16/BF16/F32), but the split
+ * partials live in a fixed SL8_NOALLOC_SCRATCH_BYTES device array inside the library,
+ * which every GPU that loads the library holds until the process exits.
+ *   - The automatic split count is lowered to what the array holds; a problem whose
+ *     single split needs more than the array (B * Hq * (d + 1) * 4 bytes >
+ *     SL8_NOALLOC_SCRATCH_BYTES) is refused with SL8_ERR_WORKSPACE before any launch.
+ *   - The first call on each device looks up the array's device address (with that
+ *     device current); make that first call before any stream capture.
+ *   - Every call uses the same array: calls whose work overlaps on the GPU (other
+ *     streams, other threads) race on it and must be serialised by the caller.
+ *   - Calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+#define SL8_NOALLOC_SCRATCH_BYTES (16u << 20)
+SL8_API int sl8_attn_int8_decode_noalloc(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale,
+                                         const int8_t* v_cache, const float* v_scale, const int32_t* seqlens,
+                                         int32_t B, int32_t Hq, int32_t Hkv, int32_t Lmax, int32_t d, void* out,
+                                         int out_dtype, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status word:
  * SL8_OK, SL8_ERR_TIMEOUT (a bounded wait gave up; *site names the wait) or
  * SL8_ERR_DEVICE_ARG (an out-of-range device-side length).  site may be NULL.

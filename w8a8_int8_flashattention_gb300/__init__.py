@@ -69,6 +69,8 @@ _SIGNATURES = {
     "sl8_attn_decode_combine": (_INT, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _INT, _P, _P]),
     "sl8_attn_int8_decode_logits_debug": (_INT, [_P, _INT, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P,
                                                  _P, _P, _P, _P]),
+    "sl8_attn_int8_decode_noalloc": (_INT, [_P, _INT, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _INT,
+                                            _P]),
     "sl8_last_device_status": (_INT, [_P, ctypes.POINTER(_INT)]),
     "sl8_set_spin_limit_ns": (None, [_U64]),
     "sl8_get_spin_limit_ns": (_U64, []),

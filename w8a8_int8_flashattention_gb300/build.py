@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build", "sl8")
 LIB = os.path.join(PKG, "libsl8.so")
-SOURCES = ["abi.cu", "quant.cu", "prefill.cu", "decode.cu"]
+SOURCES = ["abi.cu", "quant.cu", "prefill.cu", "decode.cu", "noalloc.cu"]
 HEADERS = [os.path.join(CSRC, "sl8_internal.h"), os.path.join(CSRC, "sm103_ptx.cuh"),
            os.path.join(ROOT, "include", "sl8.h")]
 
