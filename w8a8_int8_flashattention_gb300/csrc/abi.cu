@@ -279,7 +279,7 @@ int sl8_k_channel_mean(const void* k, int k_dtype, int32_t B, int32_t Hkv, int32
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const SeqTable t = table_at(base, p);
   SL8_LAUNCH(launch_schedule(cu_seqlens, B, N, cu_seqlens ? total_tokens : static_cast<int64_t>(B) * N,
-                             static_cast<int64_t>(B) * p.max_tiles * kPadRows, t, p.max_tiles, s));
+                             static_cast<int64_t>(B) * p.max_tiles * kPadRows, t, kQTile, s));
   SL8_LAUNCH(launch_kv_stats(k, static_cast<sl8_dtype>(k_dtype), nullptr, cu_seqlens != nullptr, B, Hkv, N, d, t.len,
                              t.tok0, reinterpret_cast<float*>(base + p.k_partials), nullptr, p.max_chunks, mean_out,
                              nullptr, s));
@@ -305,7 +305,7 @@ static int prefill_prepare(const void* q, const void* k, const void* v, int qk_d
   const SeqTable t = table_at(ws, p);
   const int64_t tokens = varlen ? total_tokens : static_cast<int64_t>(B) * N;
   const bool convert_v = v && v_dtype == SL8_BF16;
-  SL8_LAUNCH(launch_schedule(cu_seqlens, B, N, tokens, p.t_pad_max, t, p.max_tiles, s));
+  SL8_LAUNCH(launch_schedule(cu_seqlens, B, N, tokens, p.t_pad_max, t, prefill_item_rows(d), s));
   float* mean = smooth_k ? reinterpret_cast<float*>(ws + p.k_mean) : nullptr;
   int32_t* v_exp = convert_v ? reinterpret_cast<int32_t*>(ws + p.v_exp) : nullptr;
   if (smooth_k || convert_v) {

@@ -7,23 +7,29 @@
 // of its "Quick start" section.  Per (sequence, query head):
 //   S = int32(Q_i8 . K_i8^T);  x = S * s_q * s_k / sqrt(d);  causal mask (key j
 //   allowed for query i iff j <= i, top-left aligned);  online softmax
-//   (FlashAttention-2);  O = P . V with P rounded to V's dtype, fp32 accumulation.
+//   (FlashAttention-2);  O = P . V with fp32 accumulation.
 //
 // GB300 design (not the pages' DP4A CUDA-core design):
 //   * sm_103a has no tcgen05 kind::i8 MMA.  The int8 codes are held as bf16 (every
 //     integer in [-127, 127] is exact in bf16) and QK^T runs as tcgen05 kind::f16
 //     with fp32 accumulation in TMEM.  Every partial sum is an integer of
 //     magnitude <= 256 * 127^2 < 2^24, so S is the exact int32 dot.
-//   * Persistent CTAs walk a longest-first list of (sequence, 128-row q-tile,
-//     head) items built on the device.  Roles: warp 0 issues TMA loads of Q, K
-//     (128B-swizzled code tiles from the workspace) and V (the caller's tensor);
-//     warp 1 issues tcgen05.mma from one thread (S = Q K^T into one of two TMEM
-//     buffers; O += P V with P read from TMEM); warps 4..7 (one thread per query
-//     row) load S from TMEM, dequantise, mask, run the online softmax, write P
-//     back over S in TMEM, rescale O when the running max grows by more than
-//     2^8, and write the normalised output.
-//   * Every mbarrier wait is bounded in time; a timeout is recorded in the
-//     library's status word and the CTA winds down.
+//   * P.V runs in fp16 (P in [0, 2^8], V fp16 or a bf16 V re-expressed in fp16 with a
+//     per-(sequence, kv head) power-of-two scale that the epilogue undoes).
+//   * Persistent CTAs walk a longest-first list of (sequence, row block, head) items
+//     built on the device.  One warp issues TMA loads (Q and K as 128B-swizzled code
+//     tiles from the workspace, V), one thread issues tcgen05.mma, and softmax
+//     warpgroups (one thread per query row = one TMEM lane) load S from TMEM,
+//     dequantise, mask, run the online softmax, write P back over S in TMEM and
+//     scale O in place when the running max grows by more than 2^8.
+//   * d <= 128: two 128-row Q tiles per CTA, one softmax warpgroup each, so the tensor
+//     core runs one tile's MMAs while the other tile's softmax runs (TMEM: S and O of
+//     both tiles, 4 x 128 columns) and each K/V tile serves 256 query rows.
+//   * d = 256: one Q tile per CTA with two S buffers (TMEM: 2 x 64 + 256 columns).
+//   * Every mbarrier wait is bounded in time; a timeout is recorded in the library's
+//     status word and the CTA winds down with all threads leaving together.
+#include <cfloat>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -33,34 +39,335 @@ namespace sl8 {
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kSoftmaxWarp0 = 4;  // warps 4..7: TMEM lanes 0..127
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: O is rescaled when the max grows by more
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 
+// ------------------------------------------------------------------ small helpers
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t pack_out2(float lo, float hi, bool bf16) {
+  if (bf16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+  return pack_half2(lo, hi);
+}
+
+// OR of a flag over the 128 threads of a softmax warpgroup (named barrier `id`); also
+// orders their shared-memory accesses like bar.sync.
+__device__ __forceinline__ bool wg_any(bool v, int id) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, %2, 128, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id)
+      : "memory");
+  return r != 0;
+}
+
+// Wait on an mbarrier phase with the result made uniform across the warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns, DeviceStatus* st,
+                                          int site) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, limit_ns, st, site));
+}
+
+// ------------------------------------------------------------------ work items
+// An item is a block of consecutive 128-row Q tiles of one (sequence, query head).
+struct Item {
+  int32_t s, it, hq, hkv, L, pstart, tok0;
+};
+
+__device__ __forceinline__ Item decode_item(const PrefillArgs& a, int64_t item, int group) {
+  Item w;
+  const int64_t pair = item / a.Hq;
+  w.hq = static_cast<int32_t>(item - pair * a.Hq);
+  w.hkv = w.hq / group;
+  w.s = a.table.pair_seq[pair];
+  w.it = a.table.pair_qt[pair];
+  w.L = a.table.len[w.s];
+  w.pstart = a.table.pstart[w.s];
+  w.tok0 = a.table.tok0[w.s];
+  return w;
+}
+
+// Key tiles of BN keys that Q tile qt (128 rows) visits; 0 if the tile is past the end.
+template <int BN>
+__device__ __forceinline__ int tile_nkv(int qt, int L, bool causal) {
+  if (qt * kQTile >= L) return 0;
+  const int kend = causal ? min(L, (qt + 1) * kQTile) : L;
+  return (kend + BN - 1) / BN;
+}
+
+// ------------------------------------------------------------------ softmax step
+// One online-softmax step for this thread's query row over a BN-key S tile in TMEM:
+// dequantise (S * s_k[key], times alpha = s_q log2(e)/sqrt(d) folded into the
+// exponent), mask, update the running max m / sum l, write P (fp16) over the S
+// columns and, when the max grew by more than 2^8, scale the row's O in TMEM.
+// o_bar (nullable): barrier to wait on before touching O.  Returns false on timeout.
+template <int BN, int D>
+__device__ __forceinline__ bool softmax_step(uint32_t s_taddr, uint32_t o_taddr, const float* __restrict__ ks,
+                                             float alpha, bool need_mask, int key0, int row_abs, int L, bool causal,
+                                             bool first, float& m, float& l, uint64_t* o_bar, uint32_t o_parity,
+                                             uint64_t limit_ns, DeviceStatus* st) {
+  float x[BN];
+#pragma unroll
+  for (int c0 = 0; c0 < BN; c0 += 32) {
+    uint32_t v[32];
+    tmem_ld32(s_taddr + c0, v);
+#pragma unroll
+    for (int c = 0; c < 32; ++c) x[c0 + c] = __uint_as_float(v[c]);
+  }
+  tmem_wait_ld();
+#pragma unroll
+  for (int c = 0; c < BN; c += 4) {
+    const float4 k4 = *reinterpret_cast<const float4*>(ks + c);
+    upk2(mul2(pk2(x[c], x[c + 1]), pk2(k4.x, k4.y)), x[c], x[c + 1]);
+    upk2(mul2(pk2(x[c + 2], x[c + 3]), pk2(k4.z, k4.w)), x[c + 2], x[c + 3]);
+  }
+  if (need_mask) {
+#pragma unroll
+    for (int c = 0; c < BN; ++c) {
+      const int key = key0 + c;
+      if (!(key < L && (!causal || key <= row_abs))) x[c] = -INFINITY;
+    }
+  }
+  float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < BN; c += 8) {
+    m0 = max3(m0, x[c], x[c + 1]);
+    m1 = max3(m1, x[c + 2], x[c + 3]);
+    m2 = max3(m2, x[c + 4], x[c + 5]);
+    m3 = max3(m3, x[c + 6], x[c + 7]);
+  }
+  const float m_tile = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * alpha;
+  float o_scale = 1.0f;
+  bool rescale = false;
+  if (first) {
+    m = m_tile;
+  } else if (m_tile > m + kRescaleThreshold) {
+    o_scale = ex2(m - m_tile);
+    l *= o_scale;
+    m = m_tile;
+    rescale = true;
+  }
+  const uint64_t a2 = pk2(alpha, alpha), nm2 = pk2(-m, -m);
+  uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int c0 = 0; c0 < BN; c0 += 32) {
+    uint32_t pw[16];
+#pragma unroll
+    for (int c = 0; c < 32; c += 2) {
+      float t0, t1;
+      upk2(fma2(pk2(x[c0 + c], x[c0 + c + 1]), a2, nm2), t0, t1);
+      const float e0 = ex2(t0), e1 = ex2(t1);
+      acc[(c / 2) & 3] = add2(acc[(c / 2) & 3], pk2(e0, e1));
+      pw[c / 2] = pack_half2(e0, e1);
+    }
+    tmem_st16(s_taddr + c0 / 2, pw);
+  }
+  float s0, s1, s2, s3, s4, s5, s6, s7;
+  upk2(acc[0], s0, s1);
+  upk2(acc[1], s2, s3);
+  upk2(acc[2], s4, s5);
+  upk2(acc[3], s6, s7);
+  l += ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+  if (__any_sync(0xffffffffu, rescale)) {
+    if (o_bar && !warp_wait(o_bar, o_parity, limit_ns, st, 31)) return false;
+    tc_fence_after();
+    const uint64_t sc = pk2(o_scale, o_scale);
+#pragma unroll
+    for (int c0 = 0; c0 < D; c0 += 16) {
+      uint32_t v[16];
+      tmem_ld16(o_taddr + c0, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 16; c += 2) {
+        float a, b;
+        upk2(mul2(pk2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), sc), a, b);
+        v[c] = __float_as_uint(a);
+        v[c + 1] = __float_as_uint(b);
+      }
+      tmem_st16(o_taddr + c0, v);
+    }
+  }
+  tmem_wait_st();
+  return true;
+}
+
+// Debug: write this row's exact int32 logits (S of the tile) for keys < L.
+template <int BN>
+__device__ __forceinline__ void logits_step(uint32_t s_taddr, const PrefillArgs& a, const Item& w, int row_abs,
+                                            int key0) {
+  float x[BN];
+#pragma unroll
+  for (int c0 = 0; c0 < BN; c0 += 32) {
+    uint32_t v[32];
+    tmem_ld32(s_taddr + c0, v);
+#pragma unroll
+    for (int c = 0; c < 32; ++c) x[c0 + c] = __uint_as_float(v[c]);
+  }
+  tmem_wait_ld();
+  if (row_abs >= a.row_begin && row_abs < a.row_end && row_abs < w.L) {
+    int32_t* dst = a.logits + ((static_cast<int64_t>(w.s) * a.Hq + w.hq) * (a.row_end - a.row_begin) +
+                               (row_abs - a.row_begin)) * a.N;
+#pragma unroll
+    for (int c = 0; c < BN; ++c)
+      if (key0 + c < w.L) dst[key0 + c] = __float2int_rn(x[c]);
+  }
+}
+
+// Normalised output row (and LSE) from O in TMEM.
 template <int D>
-struct Cfg {
-  static constexpr int BN = D <= 128 ? 128 : 64;         // keys per KV tile
-  static constexpr int kBoxes = D / 64;                    // 64-element (128 B) boxes along d
+__device__ __forceinline__ void store_row(uint32_t o_taddr, const PrefillArgs& a, const Item& w, int row_abs, float m,
+                                          float l, float v_unscale) {
+  const bool row_ok = row_abs < w.L;
+  const float scale = v_unscale / l;
+  const bool out_f32 = a.out_dtype == SL8_F32, out_bf16 = a.out_dtype == SL8_BF16;
+  const int64_t orow = a.varlen ? (static_cast<int64_t>(w.tok0) + row_abs) * a.Hq + w.hq
+                                : (static_cast<int64_t>(w.s) * a.Hq + w.hq) * a.N + row_abs;
+#pragma unroll
+  for (int c0 = 0; c0 < D; c0 += 16) {
+    uint32_t v[16];
+    tmem_ld16(o_taddr + c0, v);
+    tmem_wait_ld();
+    if (row_ok) {
+      if (out_f32) {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow * D + c0);
+#pragma unroll
+        for (int c = 0; c < 16; c += 4)
+          dst[c / 4] = make_float4(__uint_as_float(v[c]) * scale, __uint_as_float(v[c + 1]) * scale,
+                                   __uint_as_float(v[c + 2]) * scale, __uint_as_float(v[c + 3]) * scale);
+      } else {
+        uint32_t p[8];
+#pragma unroll
+        for (int c = 0; c < 16; c += 2)
+          p[c / 2] = pack_out2(__uint_as_float(v[c]) * scale, __uint_as_float(v[c + 1]) * scale, out_bf16);
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow * D + c0);
+        dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
+        dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+      }
+    }
+  }
+  if (row_ok && a.lse) a.lse[orow] = (m + __log2f(l)) * kLn2;
+}
+
+// Issue the D/16 MMAs of S = Q . K^T (M = 128, N = BN) into TMEM column d_col.
+template <int D, int BN>
+__device__ __forceinline__ void issue_qk(uint32_t d_col, uint32_t qaddr, uint32_t kaddr) {
+  constexpr uint32_t idesc = idesc_f16(kQTile, BN, true, false, false);
+#pragma unroll
+  for (int k = 0; k < D / 16; ++k) {
+    const uint64_t da = desc_sw128(qaddr + (k / 4) * (kQTile * 128) + (k % 4) * 32, 16, 1024);
+    const uint64_t db = desc_sw128(kaddr + (k / 4) * (BN * 128) + (k % 4) * 32, 16, 1024);
+    mma_ss(d_col, da, db, idesc, k > 0 ? 1u : 0u);
+  }
+}
+
+// Issue the BN/16 MMAs of O (+)= P . V (M = 128, N = D), P fp16 in TMEM at p_col.
+template <int D, int BN>
+__device__ __forceinline__ void issue_pv(uint32_t o_col, uint32_t p_col, uint32_t vaddr, bool accumulate) {
+  constexpr uint32_t idesc = idesc_f16(kQTile, D, false, false, true);  // fp16 P x fp16 V (MN-major)
+#pragma unroll
+  for (int k = 0; k < BN / 16; ++k) {
+    const uint64_t db = desc_sw128(vaddr + k * 2048, BN * 128, 1024);
+    mma_ts(o_col, p_col + k * 8, db, idesc, (accumulate || k > 0) ? 1u : 0u);
+  }
+}
+
+__device__ __forceinline__ void load_q_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int boxes, int row,
+                                            int head) {
+  for (int b = 0; b < boxes; ++b) tma_load_3d(dst + b * (kQTile * 128), map, bar, b * 64, row, head);
+}
+
+// K and V tiles j of item w into one pipeline stage (V waits for its stage to drain).
+template <int BN>
+__device__ __forceinline__ void load_kv_tile(uint8_t* kdst, uint8_t* vdst, const CUtensorMap* map_k,
+                                             const CUtensorMap* map_v, uint64_t* kbar, uint64_t* vbar, int boxes,
+                                             const PrefillArgs& a, const Item& w, int j, uint32_t bytes,
+                                             uint64_t* v_empty, uint32_t v_parity, bool wait_v, uint64_t limit_ns,
+                                             DeviceStatus* st, bool* ok) {
+  mbar_arrive_expect_tx(kbar, bytes);
+  for (int b = 0; b < boxes; ++b) tma_load_3d(kdst + b * (BN * 128), map_k, kbar, b * 64, w.pstart + j * BN, w.hkv);
+  if (wait_v && !mbar_wait(v_empty, v_parity, limit_ns, st, 12)) {
+    *ok = false;
+    return;
+  }
+  mbar_arrive_expect_tx(vbar, bytes);
+  for (int b = 0; b < boxes; ++b) {
+    if (a.v16)
+      tma_load_3d(vdst + b * (BN * 128), map_v, vbar, b * 64, w.pstart + j * BN, w.hkv);
+    else if (a.varlen)
+      tma_load_3d(vdst + b * (BN * 128), map_v, vbar, b * 64, w.hkv, w.tok0 + j * BN);
+    else
+      tma_load_3d(vdst + b * (BN * 128), map_v, vbar, b * 64, j * BN, w.s * a.Hkv + w.hkv);
+  }
+}
+
+// ==================================================================== d <= 128: two Q tiles per CTA
+template <int D>
+struct PairCfg {
+  static constexpr int BN = 128;
+  static constexpr int kBoxes = D / 64;
   static constexpr int kQBytes = kQTile * D * 2;
-  static constexpr int kKBytes = BN * D * 2;
-  static constexpr int kVBytes = BN * D * 2;
+  static constexpr int kKVBytes = BN * D * 2;
   static constexpr int kStages = 2;
-  static constexpr int kQStages = D <= 128 ? 2 : 1;
-  static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQOff + kQStages * kQBytes;
-  static constexpr int kVOff = kKOff + kStages * kKBytes;
-  static constexpr int kScaleOff = kVOff + kStages * kVBytes;  // 2 x BN floats
-  static constexpr int kBarOff = kScaleOff + 2 * BN * 4;
-  // + barriers + alignment slack; at least 116 KB so that a second CTA never shares the SM
-  // (each CTA holds all 512 TMEM columns)
-  static constexpr int kSmemBytes = kBarOff + 256 + 1024 > 118784 ? kBarOff + 256 + 1024 : 118784;
+  static constexpr int kQOff = 0;                                   // 2 Q tiles
+  static constexpr int kKOff = kQOff + 2 * kQBytes;
+  static constexpr int kVOff = kKOff + kStages * kKVBytes;
+  static constexpr int kScaleOff = kVOff + kStages * kKVBytes;     // [2 wg][2 buf][BN] floats
+  static constexpr int kBarOff = kScaleOff + 4 * BN * 4;
+  static constexpr int kUsed = kBarOff + 256 + 1024;
+  // at least 116 KB so that a second CTA never shares the SM (each holds all 512 TMEM columns)
+  static constexpr int kSmemBytes = kUsed > 118784 ? kUsed : 118784;
+  // warps 0-3 / 4-7: softmax of tile 0 / 1; 8: TMA; 9: MMA; 10-11 idle.  Launched at 168
+  // registers per thread (384 x 168 = 64512); then the TMA/MMA warpgroup drops to 72 and
+  // the softmax warpgroups rise to 216: 8 x 32 x 216 + 4 x 32 x 72 = 64512, and per SMSP
+  // (warps k, k+4, k+8) 216 + 216 + 72 = 504 <= 512 registers per lane slot.
+  static constexpr int kThreads = 384;
+  static constexpr int kRegsSoftmax = 216;
+  static constexpr int kRegsOther = 72;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kOCol = 2 * BN;
-  static_assert(kOCol + D <= kTmemCols, "TMEM budget");
+  static_assert(2 * (BN + D) <= 512, "TMEM budget");
   static_assert(kSmemBytes <= 232448, "smem budget");
 };
 
-struct Bars {
+struct PairBars {
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
   uint64_t s_full[2], p_full[2], o_done[2];
@@ -69,61 +376,17 @@ struct Bars {
   int abort;
 };
 
-struct Item {
-  int32_t s, qt, hq, hkv, L, pstart, tok0, nkv;
-};
-
-template <int D>
-__device__ __forceinline__ Item decode_item(const PrefillArgs& a, int64_t item, int group, bool causal) {
-  Item it;
-  const int64_t pair = item / a.Hq;
-  it.hq = static_cast<int32_t>(item - pair * a.Hq);
-  it.hkv = it.hq / group;
-  it.s = a.table.pair_seq[pair];
-  it.qt = a.table.pair_qt[pair];
-  it.L = a.table.len[it.s];
-  it.pstart = a.table.pstart[it.s];
-  it.tok0 = a.table.tok0[it.s];
-  constexpr int BN = Cfg<D>::BN;
-  const int kend = causal ? min(it.L, (it.qt + 1) * kQTile) : it.L;
-  it.nkv = (kend + BN - 1) / BN;
-  return it;
-}
-
-__device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
-  if (bf16) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-  }
-  __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-
-// OR of a flag over the 128 softmax threads (named barrier 1); also orders their
-// shared-memory accesses like bar.sync.
-__device__ __forceinline__ bool wg_any(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, 1, 128, q;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(v))
-      : "memory");
-  return r != 0;
-}
-
 template <int D, bool kLogits>
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap map_q,
-                                                              const __grid_constant__ CUtensorMap map_k,
-                                                              const __grid_constant__ CUtensorMap map_v,
-                                                              const PrefillArgs a, DeviceStatus* st,
-                                                              uint64_t limit_ns) {
-  using C = Cfg<D>;
+__global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
+    prefill_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                        const __grid_constant__ CUtensorMap map_v, const PrefillArgs a, DeviceStatus* st,
+                        uint64_t limit_ns) {
+  using C = PairCfg<D>;
   constexpr int BN = C::BN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Bars& bars = *reinterpret_cast<Bars*>(smem + C::kBarOff);
-  float* sks = reinterpret_cast<float*>(smem + C::kScaleOff);
+  PairBars& bars = *reinterpret_cast<PairBars*>(smem + C::kBarOff);
+  float* sks_all = reinterpret_cast<float*>(smem + C::kScaleOff);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const bool causal = kLogits ? false : a.causal;
@@ -146,7 +409,277 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     bars.abort = 0;
     fence_barrier_init();
   }
-  if (warp == 1) {
+  if (warp == 9) {
+    tmem_alloc(&bars.tmem_base, C::kTmemCols);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = bars.tmem_base;
+  volatile int* abort_flag = &bars.abort;
+  static_assert(8 * 32 * C::kRegsSoftmax + 4 * 32 * C::kRegsOther <= C::kThreads * 168, "register split");
+
+  if (warp >= 8) {
+    // warps 8-11: TMA producer, MMA issuer, two idle warps
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsOther));
+    if (warp == 8 && lane == 0) {
+      // ---------------------------------------------------------- TMA producer
+      prefetch_tensormap(&map_q);
+      prefetch_tensormap(&map_k);
+      prefetch_tensormap(&map_v);
+      uint32_t g = 0, it = 0;
+      bool ok = true;
+      for (int64_t item = blockIdx.x; item < n_items && ok && !*abort_flag; item += gridDim.x, ++it) {
+        const Item w = decode_item(a, item, group);
+        const int nkv = max(tile_nkv<BN>(2 * w.it, w.L, causal), tile_nkv<BN>(2 * w.it + 1, w.L, causal));
+        // both Q tiles are always loaded (a tile past the end reads rows no one uses)
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (it >= 1) ok = mbar_wait(&bars.q_empty[t], (it - 1) & 1, limit_ns, st, 10);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&bars.q_full[t], C::kQBytes);
+          load_q_tile(smem + C::kQOff + t * C::kQBytes, &map_q, &bars.q_full[t], C::kBoxes,
+                      w.pstart + (2 * w.it + t) * kQTile, w.hq);
+        }
+        for (int j = 0; j < nkv && ok; ++j, ++g) {
+          const uint32_t stg = g % C::kStages, n = g / C::kStages;
+          if (g >= C::kStages) ok = mbar_wait(&bars.k_empty[stg], (n - 1) & 1, limit_ns, st, 11);
+          if (!ok || *abort_flag) break;
+          load_kv_tile<BN>(smem + C::kKOff + stg * C::kKVBytes, smem + C::kVOff + stg * C::kKVBytes, &map_k, &map_v,
+                           &bars.k_full[stg], &bars.v_full[stg], C::kBoxes, a, w, j, C::kKVBytes, &bars.v_empty[stg],
+                           (n - 1) & 1, g >= C::kStages, limit_ns, st, &ok);
+        }
+      }
+      if (!ok) *abort_flag = 1;
+    } else if (warp == 9 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      // Per key tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1): while one tile's softmax
+      // runs, the tensor core works on the other tile.
+      uint32_t g = 0, it = 0, np[2] = {0, 0};
+      bool ok = true, issued = false;
+      for (int64_t item = blockIdx.x; item < n_items && ok && !*abort_flag; item += gridDim.x, ++it) {
+        const Item w = decode_item(a, item, group);
+        const int nkv_t[2] = {tile_nkv<BN>(2 * w.it, w.L, causal), tile_nkv<BN>(2 * w.it + 1, w.L, causal)};
+        const int nkv = max(nkv_t[0], nkv_t[1]);
+        ok = mbar_wait(&bars.q_full[0], it & 1, limit_ns, st, 20) &&
+             mbar_wait(&bars.q_full[1], it & 1, limit_ns, st, 20);
+        if (ok) ok = mbar_wait(&bars.k_full[g % C::kStages], (g / C::kStages) & 1, limit_ns, st, 21);
+        if (!ok) break;
+        tc_fence_after();
+        {
+          const uint32_t kaddr = smem_u32(smem + C::kKOff + (g % C::kStages) * C::kKVBytes);
+          for (int t = 0; t < 2; ++t) {
+            if (nkv_t[t] > 0) {
+              issue_qk<D, BN>(tbase + t * 256, smem_u32(smem + C::kQOff + t * C::kQBytes), kaddr);
+              mma_commit(&bars.s_full[t]);
+            }
+            if (nkv_t[t] <= 1) mma_commit(&bars.q_empty[t]);
+          }
+          issued = true;
+          mma_commit(&bars.k_empty[g % C::kStages]);
+        }
+        for (int j = 0; j < nkv && ok; ++j) {
+          const uint32_t gj = g + j, gn = g + j + 1;
+          bool v_ready = false, k_ready = false;
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (j >= nkv_t[t]) continue;
+            ok = mbar_wait(&bars.p_full[t], np[t] & 1, limit_ns, st, 22);
+            ++np[t];
+            if (ok && !v_ready) ok = mbar_wait(&bars.v_full[gj % C::kStages], (gj / C::kStages) & 1, limit_ns, st, 23);
+            if (!ok) break;
+            v_ready = true;
+            tc_fence_after();
+            issue_pv<D, BN>(tbase + t * 256 + 128, tbase + t * 256,
+                            smem_u32(smem + C::kVOff + (gj % C::kStages) * C::kKVBytes), j > 0);
+            if (j == nkv_t[t] - 1) mma_commit(&bars.o_done[t]);
+            if (j + 1 < nkv_t[t]) {
+              if (!k_ready) {
+                ok = mbar_wait(&bars.k_full[gn % C::kStages], (gn / C::kStages) & 1, limit_ns, st, 21);
+                if (!ok) break;
+                k_ready = true;
+                tc_fence_after();
+              }
+              issue_qk<D, BN>(tbase + t * 256, smem_u32(smem + C::kQOff + t * C::kQBytes),
+                              smem_u32(smem + C::kKOff + (gn % C::kStages) * C::kKVBytes));
+              mma_commit(&bars.s_full[t]);
+              if (j + 1 == nkv_t[t] - 1) mma_commit(&bars.q_empty[t]);
+            }
+          }
+          if (!ok) break;
+          mma_commit(&bars.v_empty[gj % C::kStages]);
+          if (k_ready) mma_commit(&bars.k_empty[gn % C::kStages]);
+        }
+        g += nkv;
+      }
+      if (!ok) *abort_flag = 1;
+      if (issued) {
+        mma_commit(&bars.drain);
+        mbar_wait(&bars.drain, 0, limit_ns, st, 24);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warpgroups
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsSoftmax));
+    const int t = warp / 4;                       // Q tile of this warpgroup
+    const int r = threadIdx.x - t * 128;          // query row within the tile = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t s_taddr = tbase + lane_base + t * 256;
+    const uint32_t o_taddr = s_taddr + 128;
+    float* sks = sks_all + t * 2 * BN;
+    const float qk_scale = kLog2e * rsqrtf(static_cast<float>(D));
+    uint32_t ns = 0, no = 0;   // S tiles consumed, items finished (this tile)
+    bool bad = false;
+    // first item in which this warpgroup's tile exists
+    int64_t item = blockIdx.x;
+    Item w{};
+    while (item < n_items) {
+      w = decode_item(a, item, group);
+      if (tile_nkv<BN>(2 * w.it + t, w.L, causal) > 0) break;
+      item += gridDim.x;
+    }
+    float qs_next = 0.0f, ks_next = 0.0f;
+    int ve_next = 0;
+    if (item < n_items) {
+      qs_next = a.q_scales[static_cast<int64_t>(w.hq) * a.t_pad_max + w.pstart + (2 * w.it + t) * kQTile + r];
+      if (a.v_exp) ve_next = a.v_exp[static_cast<int64_t>(w.s) * a.Hkv + w.hkv];
+      ks_next = a.k_scales[static_cast<int64_t>(w.hkv) * a.t_pad_max + w.pstart + r];
+    }
+    while (item < n_items) {
+      const int qt = 2 * w.it + t;
+      const int nkv = tile_nkv<BN>(qt, w.L, causal);
+      const int row_abs = qt * kQTile + r;
+      const float alpha = fmaxf(qs_next * qk_scale, FLT_MIN);
+      const float v_unscale = __int_as_float((127 + ve_next) << 23);
+      // the next item in which this warpgroup's tile exists
+      int64_t item_n = item + gridDim.x;
+      Item wn{};
+      while (item_n < n_items) {
+        wn = decode_item(a, item_n, group);
+        if (tile_nkv<BN>(2 * wn.it + t, wn.L, causal) > 0) break;
+        item_n += gridDim.x;
+      }
+      float m = -INFINITY, l = 0.0f;
+      for (int j = 0; j < nkv; ++j, ++ns) {
+        const uint32_t buf = ns & 1;
+        sks[buf * BN + r] = ks_next;
+        if (j + 1 < nkv) {
+          ks_next = a.k_scales[static_cast<int64_t>(w.hkv) * a.t_pad_max + w.pstart + (j + 1) * BN + r];
+        } else if (item_n < n_items) {
+          ks_next = a.k_scales[static_cast<int64_t>(wn.hkv) * a.t_pad_max + wn.pstart + r];
+          qs_next = a.q_scales[static_cast<int64_t>(wn.hq) * a.t_pad_max + wn.pstart + (2 * wn.it + t) * kQTile + r];
+          if (a.v_exp) ve_next = a.v_exp[static_cast<int64_t>(wn.s) * a.Hkv + wn.hkv];
+        }
+        if (wg_any(bad || *abort_flag, 1 + t)) {
+          bad = true;
+          break;
+        }
+        if (!warp_wait(&bars.s_full[t], ns & 1, limit_ns, st, 30)) {
+          bad = true;
+          continue;
+        }
+        tc_fence_after();
+        const int key0 = j * BN;
+        if constexpr (kLogits) {
+          logits_step<BN>(s_taddr, a, w, row_abs, key0);
+        } else {
+          const bool need_mask = (causal && key0 + BN - 1 > qt * kQTile) || (key0 + BN > w.L);
+          // O_t is safe to touch: S_t(j) was issued after PV_t(j-1), and its commit covers it
+          if (!softmax_step<BN, D>(s_taddr, o_taddr, sks + buf * BN, alpha, need_mask, key0, row_abs, w.L, causal,
+                                   j == 0, m, l, nullptr, 0, limit_ns, st)) {
+            bad = true;
+            continue;
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&bars.p_full[t]);
+      }
+      if (wg_any(bad || *abort_flag, 1 + t)) {
+        bad = true;
+        break;
+      }
+      if (!warp_wait(&bars.o_done[t], no & 1, limit_ns, st, 32)) {
+        bad = true;
+      } else {
+        tc_fence_after();
+        if constexpr (!kLogits) store_row<D>(o_taddr, a, w, row_abs, m, l, v_unscale);
+      }
+      ++no;
+      item = item_n;
+      w = wn;
+    }
+    if (bad) *abort_flag = 1;
+  }
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) tmem_dealloc(tbase, C::kTmemCols);
+}
+
+// ==================================================================== d = 256: one Q tile per CTA
+template <int D>
+struct SingleCfg {
+  static constexpr int BN = 64;
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kQBytes = kQTile * D * 2;
+  static constexpr int kKVBytes = BN * D * 2;
+  static constexpr int kStages = 2;
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + kQBytes;
+  static constexpr int kVOff = kKOff + kStages * kKVBytes;
+  static constexpr int kScaleOff = kVOff + kStages * kKVBytes;  // [2 buf][BN] floats
+  static constexpr int kBarOff = kScaleOff + 2 * BN * 4;
+  static constexpr int kUsed = kBarOff + 256 + 1024;
+  static constexpr int kSmemBytes = kUsed > 118784 ? kUsed : 118784;
+  static constexpr int kThreads = 192;  // warps 0-3 softmax; 4 TMA; 5 MMA
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kOCol = 2 * BN;
+  static_assert(kOCol + D <= kTmemCols, "TMEM budget");
+  static_assert(kSmemBytes <= 232448, "smem budget");
+};
+
+struct SingleBars {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int D, bool kLogits>
+__global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
+    prefill_single_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                          const __grid_constant__ CUtensorMap map_v, const PrefillArgs a, DeviceStatus* st,
+                          uint64_t limit_ns) {
+  using C = SingleCfg<D>;
+  constexpr int BN = C::BN;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  SingleBars& bars = *reinterpret_cast<SingleBars*>(smem + C::kBarOff);
+  float* sks = reinterpret_cast<float*>(smem + C::kScaleOff);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+  const bool causal = kLogits ? false : a.causal;
+  const int group = a.Hq / a.Hkv;
+  const int64_t n_items = static_cast<int64_t>(a.table.counts[0]) * a.Hq;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars.q_full, 1);
+    mbar_init(&bars.q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.k_full[i], 1);
+      mbar_init(&bars.k_empty[i], 1);
+      mbar_init(&bars.v_full[i], 1);
+      mbar_init(&bars.v_empty[i], 1);
+      mbar_init(&bars.s_full[i], 1);
+      mbar_init(&bars.p_full[i], 128);
+      mbar_init(&bars.o_done[i], 1);
+    }
+    mbar_init(&bars.drain, 1);
+    bars.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) {
     tmem_alloc(&bars.tmem_base, C::kTmemCols);
     tmem_relinquish();
   }
@@ -155,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const uint32_t tbase = bars.tmem_base;
   volatile int* abort_flag = &bars.abort;
 
-  if (warp == 0) {
+  if (warp == 4) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       prefetch_tensormap(&map_q);
@@ -163,355 +696,237 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       prefetch_tensormap(&map_v);
       uint32_t g = 0, it = 0;
       bool ok = true;
-      for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
-        const Item w = decode_item<D>(a, item, group, causal);
-        const uint32_t qs = it % C::kQStages;
-        if (it >= C::kQStages) ok = mbar_wait(&bars.q_empty[qs], ((it / C::kQStages) - 1) & 1, limit_ns, st, 10);
-        if (!ok || *abort_flag) break;
-        uint8_t* qdst = smem + C::kQOff + qs * C::kQBytes;
-        mbar_arrive_expect_tx(&bars.q_full[qs], C::kQBytes);
-        for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d(qdst + b * (kQTile * 128), &map_q, &bars.q_full[qs], b * 64, w.pstart + w.qt * kQTile, w.hq);
-        for (int j = 0; j < w.nkv; ++j, ++g) {
+      for (int64_t item = blockIdx.x; item < n_items && ok && !*abort_flag; item += gridDim.x, ++it) {
+        const Item w = decode_item(a, item, group);
+        const int nkv = tile_nkv<BN>(w.it, w.L, causal);
+        if (it >= 1) ok = mbar_wait(&bars.q_empty, (it - 1) & 1, limit_ns, st, 10);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bars.q_full, C::kQBytes);
+        load_q_tile(smem + C::kQOff, &map_q, &bars.q_full, C::kBoxes, w.pstart + w.it * kQTile, w.hq);
+        for (int j = 0; j < nkv && ok; ++j, ++g) {
           const uint32_t stg = g % C::kStages, n = g / C::kStages;
           if (g >= C::kStages) ok = mbar_wait(&bars.k_empty[stg], (n - 1) & 1, limit_ns, st, 11);
           if (!ok || *abort_flag) break;
-          uint8_t* kdst = smem + C::kKOff + stg * C::kKBytes;
-          mbar_arrive_expect_tx(&bars.k_full[stg], C::kKBytes);
-          for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_3d(kdst + b * (BN * 128), &map_k, &bars.k_full[stg], b * 64, w.pstart + j * BN, w.hkv);
-          if (g >= C::kStages) ok = mbar_wait(&bars.v_empty[stg], (n - 1) & 1, limit_ns, st, 12);
-          if (!ok || *abort_flag) break;
-          uint8_t* vdst = smem + C::kVOff + stg * C::kVBytes;
-          mbar_arrive_expect_tx(&bars.v_full[stg], C::kVBytes);
-          for (int b = 0; b < C::kBoxes; ++b) {
-            if (a.v16)
-              tma_load_3d(vdst + b * (BN * 128), &map_v, &bars.v_full[stg], b * 64, w.pstart + j * BN, w.hkv);
-            else if (a.varlen)
-              tma_load_3d(vdst + b * (BN * 128), &map_v, &bars.v_full[stg], b * 64, w.hkv, w.tok0 + j * BN);
-            else
-              tma_load_3d(vdst + b * (BN * 128), &map_v, &bars.v_full[stg], b * 64, j * BN, w.s * a.Hkv + w.hkv);
-          }
+          load_kv_tile<BN>(smem + C::kKOff + stg * C::kKVBytes, smem + C::kVOff + stg * C::kKVBytes, &map_k, &map_v,
+                           &bars.k_full[stg], &bars.v_full[stg], C::kBoxes, a, w, j, C::kKVBytes, &bars.v_empty[stg],
+                           (n - 1) & 1, g >= C::kStages, limit_ns, st, &ok);
         }
       }
       if (!ok) *abort_flag = 1;
     }
-  } else if (warp == 1) {
+  } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
+    // S tiles run one ahead of P.V: S_{g+1} is issued before PV_g (two S buffers).
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_f16(kQTile, BN, true, false, false);
-      constexpr uint32_t idesc_o = idesc_f16(kQTile, D, false, false, true);  // fp16 P x fp16 V
-      // S stream state
-      int64_t item_s = blockIdx.x;
-      uint32_t it_s = 0;
-      int j_s = 0;
-      Item ws{};
-      if (item_s < n_items) ws = decode_item<D>(a, item_s, group, causal);
-      uint32_t gs = 0;
-      // PV stream state
-      int64_t item_p = blockIdx.x;
-      int j_p = 0;
-      Item wp{};
-      if (item_p < n_items) wp = decode_item<D>(a, item_p, group, causal);
-      uint32_t gp = 0;
-      bool ok = true;
-      bool issued_any = false;
+      int64_t item_s = blockIdx.x, item_p = blockIdx.x;
+      uint32_t it_s = 0, gs = 0, gp = 0;
+      int j_s = 0, j_p = 0;
+      int nkv_s = 0, nkv_p = 0;
+      if (item_s < n_items) {
+        const Item ws = decode_item(a, item_s, group);
+        nkv_s = tile_nkv<BN>(ws.it, ws.L, causal);
+        nkv_p = nkv_s;
+      }
+      bool ok = true, issued = false;
       while (ok && item_p < n_items && !*abort_flag) {
-        // issue S tiles up to gp + 1
         while (ok && item_s < n_items && gs <= gp + 1) {
-          const uint32_t qs = it_s % C::kQStages;
-          if (j_s == 0) ok = mbar_wait(&bars.q_full[qs], (it_s / C::kQStages) & 1, limit_ns, st, 20);
+          if (j_s == 0) ok = mbar_wait(&bars.q_full, it_s & 1, limit_ns, st, 20);
           const uint32_t stg = gs % C::kStages;
           if (ok) ok = mbar_wait(&bars.k_full[stg], (gs / C::kStages) & 1, limit_ns, st, 21);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t qaddr = smem_u32(smem + C::kQOff + qs * C::kQBytes);
-          const uint32_t kaddr = smem_u32(smem + C::kKOff + stg * C::kKBytes);
-          const uint32_t dcol = tbase + (gs & 1) * BN;
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint64_t da = desc_sw128(qaddr + (k / 4) * (kQTile * 128) + (k % 4) * 32, 16, 1024);
-            const uint64_t db = desc_sw128(kaddr + (k / 4) * (BN * 128) + (k % 4) * 32, 16, 1024);
-            mma_ss(dcol, da, db, idesc_s, k > 0 ? 1u : 0u);
-          }
-          issued_any = true;
+          issue_qk<D, BN>(tbase + (gs & 1) * BN, smem_u32(smem + C::kQOff),
+                          smem_u32(smem + C::kKOff + stg * C::kKVBytes));
+          issued = true;
           mma_commit(&bars.s_full[gs & 1]);
           mma_commit(&bars.k_empty[stg]);
           ++gs;
-          if (++j_s == ws.nkv) {
-            mma_commit(&bars.q_empty[qs]);
+          if (++j_s == nkv_s) {
+            mma_commit(&bars.q_empty);
             j_s = 0;
             ++it_s;
             item_s += gridDim.x;
-            if (item_s < n_items) ws = decode_item<D>(a, item_s, group, causal);
+            if (item_s < n_items) {
+              const Item ws = decode_item(a, item_s, group);
+              nkv_s = tile_nkv<BN>(ws.it, ws.L, causal);
+            }
           }
         }
         if (!ok) break;
-        // O += P V for tile gp
         ok = mbar_wait(&bars.p_full[gp & 1], (gp >> 1) & 1, limit_ns, st, 22);
         const uint32_t stg = gp % C::kStages;
         if (ok) ok = mbar_wait(&bars.v_full[stg], (gp / C::kStages) & 1, limit_ns, st, 23);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t vaddr = smem_u32(smem + C::kVOff + stg * C::kVBytes);
-        const uint32_t pcol = tbase + (gp & 1) * BN;
-#pragma unroll
-        for (int k = 0; k < BN / 16; ++k) {
-          const uint64_t db = desc_sw128(vaddr + k * 2048, BN * 128, 1024);
-          mma_ts(tbase + C::kOCol, pcol + k * 8, db, idesc_o, (j_p > 0 || k > 0) ? 1u : 0u);
-        }
+        issue_pv<D, BN>(tbase + C::kOCol, tbase + (gp & 1) * BN, smem_u32(smem + C::kVOff + stg * C::kKVBytes),
+                        j_p > 0);
         mma_commit(&bars.o_done[gp & 1]);
         mma_commit(&bars.v_empty[stg]);
         ++gp;
-        if (++j_p == wp.nkv) {
+        if (++j_p == nkv_p) {
           j_p = 0;
           item_p += gridDim.x;
-          if (item_p < n_items) wp = decode_item<D>(a, item_p, group, causal);
+          if (item_p < n_items) {
+            const Item wp = decode_item(a, item_p, group);
+            nkv_p = tile_nkv<BN>(wp.it, wp.L, causal);
+          }
         }
       }
       if (!ok) *abort_flag = 1;
-      if (issued_any) {
-        // make sure every MMA this thread issued has finished before TMEM is released
+      if (issued) {
         mma_commit(&bars.drain);
         mbar_wait(&bars.drain, 0, limit_ns, st, 24);
       }
     }
-  } else if (warp >= kSoftmaxWarp0) {
-    // ------------------------------------------------------------ softmax / epilogue
-    // Control flow here is uniform across the 128 threads: every wait result is made
-    // warp-uniform with __all_sync and every exit decision group-uniform with a
-    // reducing named barrier, so no thread is ever left waiting at a barrier.
-    const int r = threadIdx.x - kSoftmaxWarp0 * 32;        // query row within the tile = TMEM lane
-    const uint32_t lane_base = static_cast<uint32_t>((warp - kSoftmaxWarp0) * 32) << 16;
-    const float qk_scale = 1.4426950408889634f / sqrtf(static_cast<float>(D));  // log2(e) / sqrt(d)
-    const bool out_bf16 = a.out_dtype == SL8_BF16, out_f32 = a.out_dtype == SL8_F32;
+  } else {
+    // ------------------------------------------------------------ softmax warpgroup (warps 0-3)
+    const int r = threadIdx.x;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const float qk_scale = kLog2e * rsqrtf(static_cast<float>(D));
     int64_t item = blockIdx.x;
     Item w{};
-    if (item < n_items) w = decode_item<D>(a, item, group, causal);
     uint32_t g = 0;
-    // prefetched per-row Q scale and per-tile K scale
     float qs_next = 0.0f, ks_next = 0.0f;
     int ve_next = 0;
     if (item < n_items) {
-      qs_next = a.q_scales[static_cast<int64_t>(w.hq) * a.t_pad_max + w.pstart + w.qt * kQTile + r];
+      w = decode_item(a, item, group);
+      qs_next = a.q_scales[static_cast<int64_t>(w.hq) * a.t_pad_max + w.pstart + w.it * kQTile + r];
       if (a.v_exp) ve_next = a.v_exp[static_cast<int64_t>(w.s) * a.Hkv + w.hkv];
       if (r < BN) ks_next = a.k_scales[static_cast<int64_t>(w.hkv) * a.t_pad_max + w.pstart + r];
     }
     bool bad = false;
     while (item < n_items) {
-      const int row_abs = w.qt * kQTile + r;
-      const float alpha = qs_next * qk_scale;
-      const float v_unscale = __int_as_float((127 + ve_next) << 23);  // 2^e undoes V's fp16 scaling
+      const int nkv = tile_nkv<BN>(w.it, w.L, causal);
+      const int row_abs = w.it * kQTile + r;
+      const float alpha = fmaxf(qs_next * qk_scale, FLT_MIN);
+      const float v_unscale = __int_as_float((127 + ve_next) << 23);
+      const int64_t item_n = item + gridDim.x;
+      Item wn{};
+      if (item_n < n_items) wn = decode_item(a, item_n, group);
       float m = -INFINITY, l = 0.0f;
-      for (int j = 0; j < w.nkv; ++j, ++g) {
+      for (int j = 0; j < nkv; ++j, ++g) {
         const uint32_t buf = g & 1;
         if (r < BN) sks[buf * BN + r] = ks_next;
-        // prefetch the scales of the next tile (possibly of the next item)
-        {
-          int jn = j + 1;
-          int64_t in = item;
-          Item wn = w;
-          if (jn == w.nkv) {
-            jn = 0;
-            in = item + gridDim.x;
-            if (in < n_items) wn = decode_item<D>(a, in, group, causal);
-          }
-          if (in < n_items) {
-            if (r < BN) ks_next = a.k_scales[static_cast<int64_t>(wn.hkv) * a.t_pad_max + wn.pstart + jn * BN + r];
-            if (jn == 0) {
-              qs_next = a.q_scales[static_cast<int64_t>(wn.hq) * a.t_pad_max + wn.pstart + wn.qt * kQTile + r];
-              if (a.v_exp) ve_next = a.v_exp[static_cast<int64_t>(wn.s) * a.Hkv + wn.hkv];
-            }
-          }
+        if (j + 1 < nkv) {
+          if (r < BN) ks_next = a.k_scales[static_cast<int64_t>(w.hkv) * a.t_pad_max + w.pstart + (j + 1) * BN + r];
+        } else if (item_n < n_items) {
+          if (r < BN) ks_next = a.k_scales[static_cast<int64_t>(wn.hkv) * a.t_pad_max + wn.pstart + r];
+          qs_next = a.q_scales[static_cast<int64_t>(wn.hq) * a.t_pad_max + wn.pstart + wn.it * kQTile + r];
+          if (a.v_exp) ve_next = a.v_exp[static_cast<int64_t>(wn.s) * a.Hkv + wn.hkv];
         }
-        if (wg_any(bad || *abort_flag)) { bad = true; break; }   // also publishes sks to the group
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars.s_full[buf], (g >> 1) & 1, limit_ns, st, 30))) {
+        if (wg_any(bad || *abort_flag, 1)) {
+          bad = true;
+          break;
+        }
+        if (!warp_wait(&bars.s_full[buf], (g >> 1) & 1, limit_ns, st, 30)) {
           bad = true;
           continue;
         }
         tc_fence_after();
-        float x[BN];
-#pragma unroll
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(tbase + lane_base + buf * BN + c0, v);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) x[c0 + c] = __uint_as_float(v[c]);
-        }
-        tmem_wait_ld();
+        const uint32_t s_taddr = tbase + lane_base + buf * BN;
+        const int key0 = j * BN;
         if constexpr (kLogits) {
-          // debug: write the exact int32 logits of this row for keys < L
-          if (row_abs >= a.row_begin && row_abs < a.row_end && row_abs < w.L) {
-            int32_t* dst = a.logits + ((static_cast<int64_t>(w.s) * a.Hq + w.hq) * (a.row_end - a.row_begin) +
-                                       (row_abs - a.row_begin)) * a.N;
-#pragma unroll
-            for (int c = 0; c < BN; ++c) {
-              const int key = j * BN + c;
-              if (key < w.L) dst[key] = __float2int_rn(x[c]);
-            }
-          }
+          logits_step<BN>(s_taddr, a, w, row_abs, key0);
         } else {
-          const float* ks = sks + buf * BN;
-          const int key0 = j * BN;
-          const bool need_mask = (causal && key0 + BN - 1 > w.qt * kQTile) || (key0 + BN > w.L);
-          float tmax = -INFINITY;
-          if (need_mask) {
-#pragma unroll
-            for (int c = 0; c < BN; ++c) {
-              const int key = key0 + c;
-              const bool valid = key < w.L && (!causal || key <= row_abs);
-              x[c] = valid ? x[c] * ks[c] : -INFINITY;
-              tmax = fmaxf(tmax, x[c]);
-            }
-          } else {
-#pragma unroll
-            for (int c = 0; c < BN; ++c) {
-              x[c] = x[c] * ks[c];
-              tmax = fmaxf(tmax, x[c]);
-            }
-          }
-          const float m_tile = tmax == -INFINITY ? -INFINITY : tmax * alpha;
-          float o_scale = 1.0f;
-          bool rescale = false;
-          if (j == 0) {
-            m = m_tile;
-          } else if (m_tile > m + kRescaleThreshold) {
-            o_scale = exp2f(m - m_tile);
-            l *= o_scale;
-            m = m_tile;
-            rescale = true;
-          }
-          const float neg_m = m == -INFINITY ? 0.0f : -m;
-          float rowsum = 0.0f;
-          uint32_t p[BN / 2];
-#pragma unroll
-          for (int c = 0; c < BN; c += 2) {
-            const float p0 = x[c] == -INFINITY ? 0.0f : exp2f(fmaf(x[c], alpha, neg_m));
-            const float p1 = x[c + 1] == -INFINITY ? 0.0f : exp2f(fmaf(x[c + 1], alpha, neg_m));
-            rowsum += p0 + p1;
-            p[c / 2] = pack2(p0, p1, false);
-          }
-          l += rowsum;
-#pragma unroll
-          for (int c0 = 0; c0 < BN / 2; c0 += 16) {
-            uint32_t v[16];
-#pragma unroll
-            for (int c = 0; c < 16; ++c) v[c] = p[c0 + c];
-            tmem_st16(tbase + lane_base + buf * BN + c0, v);
-          }
-          if (__any_sync(0xffffffffu, rescale)) {
-            // O holds the sum up to tile g-1: wait for that PV, then scale it in place
-            const uint32_t gprev = g - 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&bars.o_done[gprev & 1], (gprev >> 1) & 1, limit_ns, st, 31))) {
-              bad = true;
-              continue;
-            }
-            tc_fence_after();
-#pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 16) {
-              uint32_t v[16];
-              tmem_ld16(tbase + lane_base + C::kOCol + c0, v);
-              tmem_wait_ld();
-#pragma unroll
-              for (int c = 0; c < 16; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * o_scale);
-              tmem_st16(tbase + lane_base + C::kOCol + c0, v);
-            }
+          const bool need_mask = (causal && key0 + BN - 1 > w.it * kQTile) || (key0 + BN > w.L);
+          // here S_g was issued after PV_{g-2} only: wait for PV_{g-1} before touching O
+          const uint32_t gprev = g - 1;
+          if (!softmax_step<BN, D>(s_taddr, tbase + lane_base + C::kOCol, sks + buf * BN, alpha, need_mask, key0,
+                                   row_abs, w.L, causal, j == 0, m, l, &bars.o_done[gprev & 1], (gprev >> 1) & 1,
+                                   limit_ns, st)) {
+            bad = true;
+            continue;
           }
         }
-        tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars.p_full[buf]);
       }
-      if (wg_any(bad || *abort_flag)) { bad = true; break; }
-      // ---- epilogue: O / l for this item
+      if (wg_any(bad || *abort_flag, 1)) {
+        bad = true;
+        break;
+      }
       const uint32_t glast = g - 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars.o_done[glast & 1], (glast >> 1) & 1, limit_ns, st, 32))) {
+      if (!warp_wait(&bars.o_done[glast & 1], (glast >> 1) & 1, limit_ns, st, 32)) {
         bad = true;
       } else {
         tc_fence_after();
-        if constexpr (!kLogits) {
-          const bool row_ok = row_abs < w.L;
-          const float inv_l = v_unscale / l;
-          const int64_t orow = a.varlen ? (static_cast<int64_t>(w.tok0) + row_abs) * a.Hq + w.hq
-                                        : (static_cast<int64_t>(w.s) * a.Hq + w.hq) * a.N + row_abs;
-#pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 16) {
-            uint32_t v[16];
-            tmem_ld16(tbase + lane_base + C::kOCol + c0, v);
-            tmem_wait_ld();
-            if (row_ok) {
-              if (out_f32) {
-                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow * D + c0);
-#pragma unroll
-                for (int c = 0; c < 16; c += 4)
-                  dst[c / 4] = make_float4(__uint_as_float(v[c]) * inv_l, __uint_as_float(v[c + 1]) * inv_l,
-                                           __uint_as_float(v[c + 2]) * inv_l, __uint_as_float(v[c + 3]) * inv_l);
-              } else {
-                uint32_t pk[8];
-#pragma unroll
-                for (int c = 0; c < 16; c += 2)
-                  pk[c / 2] = pack2(__uint_as_float(v[c]) * inv_l, __uint_as_float(v[c + 1]) * inv_l, out_bf16);
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow * D + c0);
-                dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-              }
-            }
-          }
-          if (row_ok && a.lse) a.lse[orow] = (m + log2f(l)) * 0.6931471805599453f;
-        }
+        if constexpr (!kLogits) store_row<D>(tbase + lane_base + C::kOCol, a, w, row_abs, m, l, v_unscale);
       }
-      item += gridDim.x;
-      if (item < n_items) w = decode_item<D>(a, item, group, causal);
+      item = item_n;
+      w = wn;
     }
     if (bad) *abort_flag = 1;
   }
-  // ------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tbase, C::kTmemCols);
+  if (warp == 5) tmem_dealloc(tbase, C::kTmemCols);
 }
 
-}  // namespace
-
-template <int D, bool kLogits>
-static cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t s) {
-  using C = Cfg<D>;
+// ------------------------------------------------------------------ host side
+template <int BN>
+static bool make_maps(const PrefillArgs& a, int D, CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv) {
   bool ok = true;
-  const CUtensorMap mq = make_tmap_3d(a.q_codes, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, a.t_pad_max, a.Hq, D * 2ull,
-                                      a.t_pad_max * D * 2ull, 64, kQTile, 1, &ok);
-  const CUtensorMap mk = make_tmap_3d(a.k_codes, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, a.t_pad_max, a.Hkv, D * 2ull,
-                                      a.t_pad_max * D * 2ull, 64, C::BN, 1, &ok);
+  *mq = make_tmap_3d(a.q_codes, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, a.t_pad_max, a.Hq, D * 2ull,
+                     a.t_pad_max * D * 2ull, 64, kQTile, 1, &ok);
+  *mk = make_tmap_3d(a.k_codes, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, a.t_pad_max, a.Hkv, D * 2ull,
+                     a.t_pad_max * D * 2ull, 64, BN, 1, &ok);
   // P.V runs in fp16: V is either the caller's fp16 tensor or the fp16 copy of a bf16 V
   // in the padded workspace layout (same coordinates as K)
-  CUtensorMap mv;
   if (a.v16)
-    mv = make_tmap_3d(a.v16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, D, a.t_pad_max, a.Hkv, D * 2ull, a.t_pad_max * D * 2ull,
-                      64, C::BN, 1, &ok);
+    *mv = make_tmap_3d(a.v16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, D, a.t_pad_max, a.Hkv, D * 2ull, a.t_pad_max * D * 2ull,
+                       64, BN, 1, &ok);
   else if (a.varlen)  // [T, Hkv, d]: dims (d, Hkv, T)
-    mv = make_tmap_3d(a.v, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, D, a.Hkv, a.total_tokens, D * 2ull,
-                      static_cast<uint64_t>(a.Hkv) * D * 2ull, 64, 1, C::BN, &ok);
+    *mv = make_tmap_3d(a.v, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, D, a.Hkv, a.total_tokens, D * 2ull,
+                       static_cast<uint64_t>(a.Hkv) * D * 2ull, 64, 1, BN, &ok);
   else  // [nseq, Hkv, N, d]: dims (d, N, nseq*Hkv)
-    mv = make_tmap_3d(a.v, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, D, a.N, static_cast<uint64_t>(a.nseq) * a.Hkv, D * 2ull,
-                      static_cast<uint64_t>(a.N) * D * 2ull, 64, C::BN, 1, &ok);
-  if (!ok) return cudaErrorInvalidValue;
-  auto kern = prefill_kernel<D, kLogits>;
+    *mv = make_tmap_3d(a.v, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, D, a.N, static_cast<uint64_t>(a.nseq) * a.Hkv, D * 2ull,
+                       static_cast<uint64_t>(a.N) * D * 2ull, 64, BN, 1, &ok);
+  return ok;
+}
+
+template <int D, bool kLogits>
+static cudaError_t launch_pair(const PrefillArgs& a, cudaStream_t s) {
+  using C = PairCfg<D>;
+  CUtensorMap mq, mk, mv;
+  if (!make_maps<C::BN>(a, D, &mq, &mk, &mv)) return cudaErrorInvalidValue;
+  auto kern = prefill_pair_kernel<D, kLogits>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int64_t max_items = a.max_pairs * a.Hq;
   const int grid = static_cast<int>(max_items < num_sms() ? max_items : num_sms());
   if (grid <= 0) return cudaSuccess;
   TraceScope tr(kLogits ? "prefill_logits" : "prefill_attn", s);
-  kern<<<grid, kThreads, C::kSmemBytes, s>>>(mq, mk, mv, a, device_status_ptr(), spin_limit_ns());
+  kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(mq, mk, mv, a, device_status_ptr(), spin_limit_ns());
   return cudaGetLastError();
 }
+
+template <int D, bool kLogits>
+static cudaError_t launch_single(const PrefillArgs& a, cudaStream_t s) {
+  using C = SingleCfg<D>;
+  CUtensorMap mq, mk, mv;
+  if (!make_maps<C::BN>(a, D, &mq, &mk, &mv)) return cudaErrorInvalidValue;
+  auto kern = prefill_single_kernel<D, kLogits>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int64_t max_items = a.max_pairs * a.Hq;
+  const int grid = static_cast<int>(max_items < num_sms() ? max_items : num_sms());
+  if (grid <= 0) return cudaSuccess;
+  TraceScope tr(kLogits ? "prefill_logits" : "prefill_attn", s);
+  kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(mq, mk, mv, a, device_status_ptr(), spin_limit_ns());
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int prefill_item_rows(int d) { return d <= 128 ? 2 * kQTile : kQTile; }
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   const bool logits = a.logits != nullptr;
   switch (a.d) {
-    case 64: return logits ? launch_prefill_d<64, true>(a, s) : launch_prefill_d<64, false>(a, s);
-    case 128: return logits ? launch_prefill_d<128, true>(a, s) : launch_prefill_d<128, false>(a, s);
-    case 256: return logits ? launch_prefill_d<256, true>(a, s) : launch_prefill_d<256, false>(a, s);
+    case 64: return logits ? launch_pair<64, true>(a, s) : launch_pair<64, false>(a, s);
+    case 128: return logits ? launch_pair<128, true>(a, s) : launch_pair<128, false>(a, s);
+    case 256: return logits ? launch_single<256, true>(a, s) : launch_single<256, false>(a, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -73,18 +73,45 @@ __device__ __forceinline__ uint16_t code_to_bf16_bits(int c) {
 }
 
 // ---------------------------------------------------------------- scheduler
-// One CTA.  Fills the per-sequence table (length, first token, first padded row)
-// and the work list of (sequence, q-tile) pairs, ordered by q-tile index from the
-// largest down (under a causal mask the tile with the largest index has the most
-// key tiles), sequences with more tiles first within a level.
+// Exclusive prefix sum of v over the 1024 threads of the block; *total gets the sum.
+__device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* s_warp, int32_t* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int32_t inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t n = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += n;
+  }
+  if (lane == 31) s_warp[wid] = inc;
+  __syncthreads();
+  if (wid == 0) {
+    int32_t w = s_warp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += n;
+    }
+    s_warp[lane] = w;
+  }
+  __syncthreads();
+  *total = s_warp[31];
+  return inc - v + (wid > 0 ? s_warp[wid - 1] : 0);
+}
+
+// One CTA of 1024 threads.  Fills the per-sequence table (length, first token, first
+// padded row; sequences start on 128-row boundaries of the code workspace) and the work
+// list of (sequence, item) pairs, an item being `item_rows` consecutive query rows.
+// Order: by item index from the largest down (under a causal mask the last item of a
+// sequence has the most key tiles), sequences with more items first within a level.
 __global__ void __launch_bounds__(1024) schedule_kernel(const int32_t* __restrict__ cu, int32_t nseq, int32_t N,
                                                         int64_t total_tokens, int64_t t_pad_max, SeqTable t,
-                                                        int32_t max_tiles, DeviceStatus* st) {
-  __shared__ int32_t s_acc[1024];
+                                                        int32_t max_items, int32_t item_rows, DeviceStatus* st) {
+  __shared__ int32_t s_warp[32];
+  __shared__ int32_t s_fits;
   const int tid = threadIdx.x, nt = blockDim.x;
-  const int H = max_tiles + 2;
-  int32_t* bucket = t.hist;          // [H] counts, then bucket starts
-  int32_t* fill = t.hist + H;        // [H]
+  const int H = max_items + 2;
+  int32_t* bucket = t.hist;             // [H] counts, then bucket starts
+  int32_t* fill = t.hist + H;           // [H]
   int32_t* level_off = t.hist + 2 * H;  // [H]
   for (int i = tid; i < 3 * H; i += nt) t.hist[i] = 0;
   __syncthreads();
@@ -102,61 +129,53 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int32_t* __restric
     }
     t.len[s] = L;
     t.tok0[s] = tok0;
-    atomicAdd(&bucket[(L + kQTile - 1) / kQTile], 1);
+    atomicAdd(&bucket[(L + item_rows - 1) / item_rows], 1);
   }
   __syncthreads();
-  // padded row starts: exclusive scan of tiles * 128 in sequence order
+  // padded row starts: exclusive scan of ceil(L / 128) * 128 in sequence order
   const int per = (nseq + nt - 1) / nt;
   const int b = tid * per, e = min(b + per, nseq);
   int32_t acc = 0;
   for (int s = b; s < e; ++s) acc += ((t.len[s] + kQTile - 1) / kQTile) * kPadRows;
-  s_acc[tid] = acc;
-  __syncthreads();
-  if (tid == 0) {
-    int32_t run = 0;
-    for (int i = 0; i < nt; ++i) {
-      int32_t v = s_acc[i];
-      s_acc[i] = run;
-      run += v;
-    }
-    t.counts[1] = run;
-    const bool fits = run <= t_pad_max;  // overlapping sequences could overflow the workspace
-    if (!fits) record_status(st, kStatusBadArg, 902);
-    // buckets in descending tile count: start of bucket n = number of sequences with more than n tiles
-    int32_t r = 0;
-    for (int n = max_tiles; n >= 0; --n) {
-      int32_t c = bucket[n];
-      bucket[n] = r;
-      r += c;
-    }
-    // pairs of level qt are the bucket[qt] sequences with more than qt tiles; levels run from
-    // the largest qt down
-    int32_t o = 0;
-    for (int qt = max_tiles - 1; qt >= 0; --qt) {
-      level_off[qt] = o;
-      o += bucket[qt];
-    }
-    t.counts[0] = fits ? o : 0;
-    if (!fits) t.counts[1] = 0;
-  }
-  __syncthreads();
-  acc = s_acc[tid];
+  int32_t rows_total = 0;
+  acc = block_exclusive_scan(acc, s_warp, &rows_total);
   for (int s = b; s < e; ++s) {
     t.pstart[s] = acc;
     acc += ((t.len[s] + kQTile - 1) / kQTile) * kPadRows;
   }
-  for (int s = tid; s < nseq; s += nt) {
-    const int ntl = (t.len[s] + kQTile - 1) / kQTile;
-    const int slot = atomicAdd(&fill[ntl], 1);
-    t.sorted[bucket[ntl] + slot] = s;
+  if (tid == 0) {
+    const bool fits = rows_total <= t_pad_max;  // overlapping sequences could overflow the workspace
+    if (!fits) record_status(st, kStatusBadArg, 902);
+    s_fits = fits;
+    t.counts[1] = fits ? rows_total : 0;
+    // buckets in descending item count: start of bucket n = number of sequences with more than n items
+    int32_t r = 0;
+    for (int n = max_items; n >= 0; --n) {
+      const int32_t c = bucket[n];
+      bucket[n] = r;
+      r += c;
+    }
+    // level it holds the bucket[it] sequences with more than it items; levels run from the
+    // largest item index down
+    int32_t o = 0;
+    for (int it = max_items - 1; it >= 0; --it) {
+      level_off[it] = o;
+      o += bucket[it];
+    }
+    t.counts[0] = fits ? o : 0;
   }
   __syncthreads();
-  const int32_t P = t.counts[0];
+  for (int s = tid; s < nseq; s += nt) {
+    const int nit = (t.len[s] + item_rows - 1) / item_rows;
+    const int slot = atomicAdd(&fill[nit], 1);
+    t.sorted[bucket[nit] + slot] = s;
+  }
+  __syncthreads();
+  const int32_t P = s_fits ? t.counts[0] : 0;
   for (int32_t p = tid; p < P; p += nt) {
-    // level qt holds pairs [level_off[qt], level_off[qt] + bucket[qt]); level_off does not
-    // increase with qt and only empty levels share an offset with the next lower one,
-    // so p belongs to the smallest qt with level_off[qt] <= p
-    int lo = 0, hi = max_tiles - 1;
+    // level_off does not increase with the item index and only empty levels share an
+    // offset with the next lower one, so p belongs to the smallest level whose offset <= p
+    int lo = 0, hi = max_items - 1;
     while (lo < hi) {
       const int mid = (lo + hi) / 2;
       if (level_off[mid] <= p) hi = mid; else lo = mid + 1;
@@ -167,9 +186,10 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int32_t* __restric
 }
 
 cudaError_t launch_schedule(const int32_t* cu_seqlens, int32_t nseq, int32_t N, int64_t total_tokens,
-                            int64_t t_pad_max, const SeqTable& t, int32_t max_tiles, cudaStream_t s) {
+                            int64_t t_pad_max, const SeqTable& t, int32_t item_rows, cudaStream_t s) {
   TraceScope tr("schedule", s);
-  schedule_kernel<<<1, 1024, 0, s>>>(cu_seqlens, nseq, N, total_tokens, t_pad_max, t, max_tiles,
+  const int32_t max_items = (N + item_rows - 1) / item_rows;
+  schedule_kernel<<<1, 1024, 0, s>>>(cu_seqlens, nseq, N, total_tokens, t_pad_max, t, max_items, item_rows,
                                      device_status_ptr());
   return cudaGetLastError();
 }

@@ -57,8 +57,11 @@ struct TraceScope {
 // cu_seqlens (nullable = dense) must describe sequences inside [0, total_tokens) whose
 // padded rows fit in t_pad_max; violations are recorded as a device-side argument
 // error and the affected work is dropped.
+// Work-list items are `item_rows` (a multiple of 128) consecutive query rows.
 cudaError_t launch_schedule(const int32_t* cu_seqlens, int32_t nseq, int32_t N, int64_t total_tokens,
-                            int64_t t_pad_max, const SeqTable& t, int32_t max_tiles, cudaStream_t s);
+                            int64_t t_pad_max, const SeqTable& t, int32_t item_rows, cudaStream_t s);
+// Query rows per work-list item of the prefill kernel for head dim d.
+int prefill_item_rows(int d);
 // K chunk sums (k_partials, nullable) and V chunk abs-max (v_partials, nullable; V bf16),
 // then the K mean [nseq][Hkv][d] and the V power-of-two exponent [nseq][Hkv].
 cudaError_t launch_kv_stats(const void* k, sl8_dtype dt, const void* v, bool varlen, int32_t nseq, int32_t Hkv,
