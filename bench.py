@@ -223,7 +223,7 @@ def run_ours(args, world, rank, local):
             c[b, :, :L], s[b, :, :L] = cc, sc
     qdec = W.decode_query(wd).to(dev)
     seq = torch.from_numpy(lens.astype(np.int32)).to(dev)
-    S = sl8.decode_num_splits(wd.lmax, wd.d, 0)
+    S = sl8.decode_num_splits(wd.B, wd.Hkv, wd.lmax, wd.d, 0)
     o_part = torch.empty((wd.B, wd.Hq, S, wd.d), dtype=torch.float32, device=dev)
     l_part = torch.empty((wd.B, wd.Hq, S), dtype=torch.float32, device=dev)
     dout = torch.empty((wd.B, wd.Hq, wd.d), dtype=torch.bfloat16, device=dev)

@@ -152,17 +152,19 @@ SL8_API int sl8_attn_int8_qk_logits_debug(const void* q, const void* k, int qk_d
  *   k_cache, v_cache   device, [B][Hkv][Lmax][d] int8 codes.
  *   k_scale, v_scale   device, [B][Hkv][Lmax] fp32 per-token scales.
  *   seqlens            device, [B] int32, 0 <= L_b <= Lmax.
- *   num_splits         requested number of contiguous key splits (0 = automatic: one
- *                      split per 32 KB of K codes).  The effective count is
- *                      S = sl8_attn_decode_num_splits(Lmax, d, num_splits) (the request,
- *                      capped at Lmax), and split s covers tokens
- *                      [s * split_size, (s + 1) * split_size), split_size = ceil(Lmax / S).
- *   o_partial          device, [B][Hq][S][d] fp32; each split's normalised partial.
+ *   num_splits         requested number of contiguous key splits (0 = automatic: about
+ *                      16 (split, sequence, kv head) work slots per SM of the current
+ *                      device).  Split s covers tokens [s * split_size, (s + 1) * split_size)
+ *                      with split_size = ceil(Lmax / S) rounded up to a multiple of 16; the
+ *                      effective count S = sl8_attn_decode_num_splits(B, Hkv, Lmax, d,
+ *                      num_splits) can be below the request after that rounding.
+ *   o_partial          device, [B][Hq][S][d] fp32; each non-empty split's normalised partial
+ *                      (the O of an empty split is not written).
  *   lse_partial        device, [B][Hq][S] fp32 log-sum-exp per split (-inf if empty).
  * Hq / Hkv must be at most 8 (SL8_ERR_UNSUPPORTED otherwise).
  */
-SL8_API int32_t sl8_attn_decode_num_splits(int32_t Lmax, int32_t d, int32_t num_splits);
-SL8_API int32_t sl8_attn_decode_split_size(int32_t Lmax, int32_t d, int32_t num_splits);
+SL8_API int32_t sl8_attn_decode_num_splits(int32_t B, int32_t Hkv, int32_t Lmax, int32_t d, int32_t num_splits);
+SL8_API int32_t sl8_attn_decode_split_size(int32_t B, int32_t Hkv, int32_t Lmax, int32_t d, int32_t num_splits);
 SL8_API int sl8_attn_int8_decode_splitkv(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale,
                                  const int8_t* v_cache, const float* v_scale, const int32_t* seqlens, int32_t B,
                                  int32_t Hq, int32_t Hkv, int32_t Lmax, int32_t d, int32_t num_splits,
@@ -175,7 +177,7 @@ SL8_API int sl8_attn_int8_decode_splitkv(const void* q, int q_dtype, const int8_
  *   out      device, [B][Hq][d] of out_dtype (F16, BF16 or F32).
  *   lse_out  device, nullable, [B][Hq] fp32.
  *   num_splits must be the effective count S of the split call (same Lmax); the split
- *   size is ceil(Lmax / S) as there.
+ *   size is ceil(Lmax / S) rounded up to a multiple of 16, as there.
  */
 SL8_API int sl8_attn_decode_combine(const float* o_partial, const float* lse_partial, const int32_t* seqlens, int32_t B,
                             int32_t Hq, int32_t Lmax, int32_t d, int32_t num_splits, void* out, int out_dtype,
@@ -183,7 +185,8 @@ SL8_API int sl8_attn_decode_combine(const float* o_partial, const float* lse_par
 
 /*
  * Debug view of the decode's q quantisation and int32 logits (same kernel as the
- * split call, with num_splits automatic).
+ * split call, with num_splits automatic: o_partial/lse_partial sized for
+ * S = sl8_attn_decode_num_splits(B, Hkv, Lmax, d, 0)).
  *   logits_out  device, [B][Hq][Lmax] int32: entry t < L_b is int32(q_i8 . k_i8[t]);
  *               entries t >= L_b are left untouched.
  *   q_codes/q_scales  device, nullable, [B][Hq][d] int8 / [B][Hq] fp32.

@@ -104,7 +104,9 @@ def test_decode_partials_match_oracle_splits():
     seq = torch.from_numpy(lens_np.astype(np.int32)).to(DEV)
     op, lp = sl8.attn_int8_decode_splitkv(q.to(DEV), g["k"], gs["k"], g["v"], gs["v"], seq, num_splits=3)
     torch.cuda.synchronize()
-    ref = oracle.attn_decode(q.float().numpy(), o["k"], os_["k"], o["v"], os_["v"], lens_np, split_size=200)
+    split_size = sl8.lib().sl8_attn_decode_split_size(2, 2, 600, 128, 3)   # 200 -> 256: whole stages
+    assert split_size == 256 and op.shape[2] == 3
+    ref = oracle.attn_decode(q.float().numpy(), o["k"], os_["k"], o["v"], os_["v"], lens_np, split_size=split_size)
     lpn = to_np32(lp)
     live = np.isfinite(ref["lse_partial"])
     np.testing.assert_array_equal(np.isneginf(lpn), ~live)

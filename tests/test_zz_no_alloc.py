@@ -62,13 +62,14 @@ def test_noalloc_decode_matches_regular_entry_points():
         # two calls in a row: different caches, lengths and shapes
         (7001, 4, 8, 2, 128, [300, 1, 0, 700], 700),
         (7002, 3, 4, 4, 64, [513, 129, 20], 600),
-        # B * Hq * (d + 1) * 4 bytes * 16 automatic splits exceeds the array: splits are lowered
-        (7003, 128, 32, 8, 128, [4096] + [int(x) for x in np.random.default_rng(3).integers(1, 300, 127)], 4096),
+        # B * Hq * (d + 1) * 4 bytes times the automatic split count exceeds the array: the
+        # split count is lowered to fit
+        (7003, 8, 64, 8, 256, [8192, 77, 300, 1, 5, 999, 2048, 17], 8192),
     ]
     for wid, B, Hq, Hkv, d, lens, lmax in cases:
         q, kc, ks, vc, vs, seq = _cache(wid, B, Hq, Hkv, d, lens, lmax)
         if wid == 7003:
-            assert B * Hq * (d + 1) * 4 * sl8.decode_num_splits(lmax, d, 0) > SCRATCH_BYTES
+            assert B * Hq * (d + 1) * 4 * sl8.decode_num_splits(B, Hkv, lmax, d, 0) > SCRATCH_BYTES
         ref = sl8.attn_int8_decode(q, kc, ks, vc, vs, seq, out_dtype=torch.float32)
         out = torch.full((B, Hq, d), float("nan"), dtype=torch.float32, device=DEV)
         rc = _noalloc(q, kc, ks, vc, vs, seq, out)

@@ -62,8 +62,8 @@ _SIGNATURES = {
                                  _INT, _P, _P, _SZ, _P]),
     "sl8_attn_int8_qk_logits_debug": (_INT, [_P, _P, _INT, _I32, _I32, _I32, _I32, _I32, _INT, _I32, _I32, _P, _P,
                                              _P, _P, _P, _P, _SZ, _P]),
-    "sl8_attn_decode_num_splits": (_I32, [_I32, _I32, _I32]),
-    "sl8_attn_decode_split_size": (_I32, [_I32, _I32, _I32]),
+    "sl8_attn_decode_num_splits": (_I32, [_I32, _I32, _I32, _I32, _I32]),
+    "sl8_attn_decode_split_size": (_I32, [_I32, _I32, _I32, _I32, _I32]),
     "sl8_attn_int8_decode_splitkv": (_INT, [_P, _INT, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P,
                                             _P, _P]),
     "sl8_attn_decode_combine": (_INT, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _INT, _P, _P]),
@@ -250,8 +250,9 @@ def attn_int8_qk_logits_debug(q, k, smooth_k=True, row_begin=0, row_end=None, wa
 
 # ------------------------------------------------------------------ decode
 
-def decode_num_splits(Lmax: int, d: int, num_splits: int = 0) -> int:
-    return int(lib().sl8_attn_decode_num_splits(Lmax, d, num_splits))
+def decode_num_splits(B: int, Hkv: int, Lmax: int, d: int, num_splits: int = 0) -> int:
+    """Effective split count of the decode for this shape (0 = automatic)."""
+    return int(lib().sl8_attn_decode_num_splits(B, Hkv, Lmax, d, num_splits))
 
 
 def attn_int8_decode_splitkv(q, k_cache, k_scale, v_cache, v_scale, seqlens, num_splits=0, o_partial=None,
@@ -260,7 +261,7 @@ def attn_int8_decode_splitkv(q, k_cache, k_scale, v_cache, v_scale, seqlens, num
     _need_cuda(q, k_cache, k_scale, v_cache, v_scale, seqlens)
     B, Hq, d = q.shape
     _, Hkv, Lmax, _ = k_cache.shape
-    S = decode_num_splits(Lmax, d, num_splits)
+    S = decode_num_splits(B, Hkv, Lmax, d, num_splits)
     if o_partial is None:
         o_partial = torch.empty((B, Hq, max(S, 1), d), dtype=torch.float32, device=q.device)
     if lse_partial is None:
@@ -298,7 +299,7 @@ def attn_int8_decode_logits_debug(q, k_cache, k_scale, v_cache, v_scale, seqlens
     B, Hq, d = q.shape
     _, Hkv, Lmax, _ = k_cache.shape
     dev = q.device
-    S = decode_num_splits(Lmax, d, 0)
+    S = decode_num_splits(B, Hkv, Lmax, d, 0)
     logits = torch.zeros((B, Hq, Lmax), dtype=torch.int32, device=dev)
     q_codes = torch.empty((B, Hq, d), dtype=torch.int8, device=dev)
     q_scales = torch.empty((B, Hq), dtype=torch.float32, device=dev)

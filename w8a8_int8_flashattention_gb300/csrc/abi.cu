@@ -70,10 +70,10 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 3-D tiled map with 128-byte swizzle and zero fill out of bounds.
+// 3-D tiled map with zero fill out of bounds, 128-byte swizzle or none.
 CUtensorMap make_tmap_3d(const void* base, CUtensorMapDataType dt, uint64_t d0, uint64_t d1, uint64_t d2,
                          uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2,
-                         bool* ok) {
+                         bool* ok, bool swizzle128) {
   CUtensorMap m;
   memset(&m, 0, sizeof(m));
   auto fn = encode_fn();
@@ -86,7 +86,8 @@ CUtensorMap make_tmap_3d(const void* base, CUtensorMapDataType dt, uint64_t d0, 
   cuuint32_t box[3] = {b0, b1, b2};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = fn(&m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) *ok = false;
   return m;
 }
@@ -431,18 +432,38 @@ int sl8_attn_int8_qk_logits_debug(const void* q, const void* k, int qk_dtype, in
   return SL8_OK;
 }
 
-// The split plan: S = num_splits (or ceil(Lmax / chunk) when 0), capped at Lmax; every
-// split but possibly the last covers split_size = ceil(Lmax / S) tokens.  Both the split
-// kernel and the combine derive split_size from (Lmax, S) with this one formula.
-int32_t sl8_attn_decode_num_splits(int32_t Lmax, int32_t d, int32_t num_splits) {
-  if (Lmax <= 0 || !head_dim_ok(d) || num_splits < 0) return 0;
-  int32_t n = num_splits > 0 ? num_splits : (Lmax + decode_chunk_tokens(d) - 1) / decode_chunk_tokens(d);
-  return n < Lmax ? n : Lmax;
+// The split plan.  split_size_for(Lmax, S) = ceil(Lmax / S) rounded up to a whole number
+// of the decode kernel's 128-token stages (to 16 tokens below one stage): every stage of
+// the cache then starts on a 16-byte boundary of the scale rows, and only a sequence's
+// last split ends in a partial stage.  A request n (0: about 16 work slots per SM over
+// the B x Hkv pairs, at most one per stage) becomes S = ceil(Lmax /
+// split_size_for(Lmax, n)) splits; the split kernel and the combine both use
+// split_size_for(Lmax, S).
+static int32_t split_size_for(int32_t Lmax, int32_t S) {
+  const int32_t per = (Lmax + S - 1) / S;
+  const int32_t step = per >= 128 ? 128 : 16;
+  return (per + step - 1) / step * step;
 }
 
-int32_t sl8_attn_decode_split_size(int32_t Lmax, int32_t d, int32_t num_splits) {
-  const int32_t S = sl8_attn_decode_num_splits(Lmax, d, num_splits);
-  return S > 0 ? (Lmax + S - 1) / S : 0;
+int32_t sl8_attn_decode_num_splits(int32_t B, int32_t Hkv, int32_t Lmax, int32_t d, int32_t num_splits) {
+  if (B <= 0 || Hkv <= 0 || Lmax <= 0 || !head_dim_ok(d) || num_splits < 0) return 0;
+  int64_t n = num_splits;
+  if (n == 0) {
+    const int64_t pairs = static_cast<int64_t>(B) * Hkv;
+    n = (16ll * num_sms() + pairs - 1) / pairs;
+    const int64_t chunks = (Lmax + decode_chunk_tokens(d) - 1) / decode_chunk_tokens(d);
+    if (n > chunks) n = chunks;
+  }
+  const int64_t cap = (Lmax + 15) / 16;
+  if (n > cap) n = cap;
+  if (n < 1) n = 1;
+  const int32_t ss = split_size_for(Lmax, static_cast<int32_t>(n));
+  return (Lmax + ss - 1) / ss;
+}
+
+int32_t sl8_attn_decode_split_size(int32_t B, int32_t Hkv, int32_t Lmax, int32_t d, int32_t num_splits) {
+  const int32_t S = sl8_attn_decode_num_splits(B, Hkv, Lmax, d, num_splits);
+  return S > 0 ? split_size_for(Lmax, S) : 0;
 }
 
 static int decode_validate(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale,
@@ -456,6 +477,8 @@ static int decode_validate(const void* q, int q_dtype, const int8_t* k_cache, co
   SL8_CHECK(head_dim_ok(d), SL8_ERR_UNSUPPORTED);
   SL8_CHECK(Hq / Hkv <= 8, SL8_ERR_UNSUPPORTED);
   SL8_CHECK(B <= 65535 && Hkv <= 65535, SL8_ERR_UNSUPPORTED);
+  // the caches are addressed as [B * Hkv * Lmax] rows with 32-bit row coordinates
+  SL8_CHECK(static_cast<int64_t>(B) * Hkv * Lmax < (int64_t(1) << 31), SL8_ERR_UNSUPPORTED);
   return SL8_OK;
 }
 
@@ -480,8 +503,8 @@ static int decode_launch(const void* q, int q_dtype, const int8_t* k_cache, cons
   a.Hkv = Hkv;
   a.Lmax = Lmax;
   a.d = d;
-  a.split_size = sl8_attn_decode_split_size(Lmax, d, num_splits);
-  a.num_splits = sl8_attn_decode_num_splits(Lmax, d, num_splits);
+  a.split_size = sl8_attn_decode_split_size(B, Hkv, Lmax, d, num_splits);
+  a.num_splits = sl8_attn_decode_num_splits(B, Hkv, Lmax, d, num_splits);
   SL8_CHECK(a.num_splits > 0 && a.num_splits <= 65535, SL8_ERR_UNSUPPORTED);
   a.o_partial = o_partial;
   a.lse_partial = lse_partial;
@@ -509,7 +532,7 @@ int sl8_attn_decode_combine(const float* o_partial, const float* lse_partial, co
   SL8_CHECK(head_dim_ok(d), SL8_ERR_UNSUPPORTED);
   if (B == 0) return SL8_OK;
   SL8_CHECK(num_splits <= (Lmax > 0 ? Lmax : 1), SL8_ERR_INVALID_ARG);
-  const int32_t split_size = Lmax > 0 ? (Lmax + num_splits - 1) / num_splits : 1;
+  const int32_t split_size = Lmax > 0 ? split_size_for(Lmax, num_splits) : 16;
   SL8_LAUNCH(launch_decode_combine(o_partial, lse_partial, seqlens, B, Hq, d, num_splits, split_size, out,
                                    static_cast<sl8_dtype>(out_dtype), lse_out, static_cast<cudaStream_t>(stream)));
   return SL8_OK;

@@ -10,14 +10,28 @@
 //   O = sum_t p_t * s_v[t] * v_i8[t].
 // The key range is cut into contiguous splits of split_size tokens.  Each split
 // writes its normalised partial O and its log-sum-exp (natural log; -inf for an
-// empty split); the combine kernel merges the partials of a row with weights
-// exp(lse_s - max lse).
+// empty split, whose O is left unwritten); the combine kernel merges the partials
+// of a row with weights exp(lse_s - max lse).
 //
-// GB300 design: HBM streaming is the bound.  One CTA per (split, kv head, batch):
-// the split's K and V codes are contiguous in the cache, so each is fetched with
-// one bulk async copy (TMA, cp.async.bulk) into shared memory; the G query rows
-// of the kv group are quantised in the CTA and the int32 dots run on dp4a with
-// 8 threads (16 bytes each) per key row, conflict-free shared-memory reads.
+// GB300 design.  The kernel streams the cache once, so HBM is the bound; the work
+// per byte must stay small enough that eight warps per SM keep up with it.
+//  * A persistent CTA per SM walks the (split, b, kv head) work slots.  Warp 0 loads
+//    each split's K and V codes with tiled TMA copies (128-byte swizzle for d >= 128)
+//    in 128-token stages, with their scales and the group's q rows, into a shared-
+//    memory ring that runs ahead across splits.
+//  * Each of the eight compute warps takes 16 tokens of every stage and keeps its own
+//    online-softmax state; the warps' states are merged once per split.
+//  * Both contractions run on the tensor cores as m16n8k16 fp16 MMAs with fp32
+//    accumulation (the int8 tensor rate of this part is low).  Codes become fp16
+//    exactly (|c| <= 127), so q.k is the exact integer dot (|sum| < 2^24).
+//      S^T[16 tokens x 8 q] = K[16 x d] . Q^T    (the G <= 8 query rows of the group)
+//      O^T[d x 8 q]        += V^T[d x 16] . P'^T  (P' = p * s_v * 2^-E, fp16)
+//    Putting tokens and head dims on the M side keeps the padded query columns
+//    cheap and gives every lane the same two query columns in S^T and O^T, so the
+//    rescales of the online softmax stay inside the lane.
+//  * Rescaling is lazy: the running max moves only when a tile exceeds it by more
+//    than 2^8 (p then stays below 256), and the power-of-two V range E only when a
+//    token's V scale exceeds 2^E; both keep P' inside the fp16 range.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -27,292 +41,586 @@ namespace sl8 {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kComputeWarps = 8;
+constexpr int kComputeThreads = kComputeWarps * 32;
+constexpr int kThreads = kComputeThreads + 32;  // + the producer warp
+constexpr int kUnit = 16;                       // tokens per compute warp per stage
+constexpr int kChunk = kComputeWarps * kUnit;   // tokens per stage
+constexpr int kQSlots = 2;                      // q-row buffers (one per split in flight)
+constexpr float kLazy = 8.0f;                   // log2 headroom of the lazy max
 
 template <int D>
 struct DCfg {
-  static constexpr int kChunk = 32768 / D;  // tokens per sub-chunk (32 KB of K codes)
-  static constexpr int kTPR = D / 16;       // threads per key row (16 codes each)
-  static constexpr int kRowsPerPass = kThreads / kTPR;
+  static constexpr int kBW = D < 128 ? D : 128;  // bytes in one row of a TMA box
+  static constexpr int kBoxes = D / kBW;
+  static constexpr bool kSwz = D >= 128;         // 128-byte swizzled tiles
+  static constexpr int kTile = kChunk * D;       // one stage of K (or V) codes
+  static constexpr int kStages = D == 64 ? 8 : (D == 128 ? 5 : 2);
+  static constexpr int kSK = 0;
+  static constexpr int kSV = kTile;
+  static constexpr int kSKs = 2 * kTile;
+  static constexpr int kSVs = kSKs + kChunk * 4;
+  static constexpr int kStageBytes = kSVs + kChunk * 4;
+  static constexpr int kQBytes = 8 * D * 4;                    // 8 raw q rows, fp32 at most
+  static constexpr int kQ = kStages * kStageBytes;
+  static constexpr int kRed = kQ + kQSlots * kQBytes;          // [warp][d][8 q] floats
+  static constexpr int kP = kRed + kComputeWarps * D * 8 * 4;  // [warp][8 q][8 token pairs] fp16x2
+  static constexpr int kStat = kP + kComputeWarps * 256;       // [warp][8 q][4] floats
+  static constexpr int kBar = kStat + kComputeWarps * 8 * 16;
+  static constexpr int kNumBars = 2 * kStages + 2 * kQSlots;
+  static constexpr int kBytes = kBar + kNumBars * 8 + 1024;    // + alignment slack
+  static_assert(kStageBytes % 1024 == 0 && kTile % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+  static_assert(kBytes <= 232448, "smem budget");
 };
 
-template <int D, int GT>
-struct DSmem {
-  static constexpr int kK = 0;
-  static constexpr int kV = kK + DCfg<D>::kChunk * D;
-  static constexpr int kKs = kV + DCfg<D>::kChunk * D;
-  static constexpr int kVs = kKs + DCfg<D>::kChunk * 4;
-  static constexpr int kScore = kVs + DCfg<D>::kChunk * 4;          // [GT][chunk] floats
-  static constexpr int kQ = kScore + GT * DCfg<D>::kChunk * 4;      // [GT][D] int8
-  static constexpr int kQs = kQ + GT * D;                           // [GT] floats
-  static constexpr int kRowStat = kQs + GT * 4 + 16;                // [GT][2] floats (m, l of the sub-chunk)
-  // [8 warps][GT][D] floats for the final P.V reduction: reuses the K chunk once it
-  // is consumed when it fits there
-  static constexpr bool kRedInK = 8 * GT * D * 4 <= DCfg<D>::kChunk * D;
-  static constexpr int kTail = (kRowStat + GT * 8 + 127) / 128 * 128;
-  static constexpr int kRed = kRedInK ? kK : kTail;
-  static constexpr int kBar = kRedInK ? kTail : kTail + 8 * GT * D * 4;
-  static constexpr int kBytes = kBar + 64 + 128;
-};
+// Byte offset of (row r, 16-byte chunk c of the row) in a stage tile made of kBoxes
+// boxes of kChunk rows x kBW bytes, with the 128-byte swizzle when it applies.
+template <int D>
+__device__ __forceinline__ uint32_t tile_off(int r, int c) {
+  using C = DCfg<D>;
+  constexpr int cpb = C::kBW / 16;
+  const int b = c / cpb, cc = c % cpb;
+  return static_cast<uint32_t>(b * (kChunk * C::kBW) + r * C::kBW + 16 * (C::kSwz ? (cc ^ (r & 7)) : cc));
+}
 
 __device__ __forceinline__ float bf16_bits(uint32_t b) { return __uint_as_float(b << 16); }
-__device__ __forceinline__ float f16_bits(uint32_t b) { return __half2float(__ushort_as_half(static_cast<unsigned short>(b))); }
-
+__device__ __forceinline__ float f16_bits(uint32_t b) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(b)));
+}
 __device__ __forceinline__ float warp_max_f(float a) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
   return a;
 }
-__device__ __forceinline__ float warp_sum_f(float a) {
+// max / sum over the 8 lanes of one thread-in-group column (lanes t, t+4, ..., t+28)
+__device__ __forceinline__ float col_max(float a) {
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
+  return fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 16));
+}
+__device__ __forceinline__ float col_sum(float a) {
+  a += __shfl_xor_sync(0xffffffffu, a, 4);
+  a += __shfl_xor_sync(0xffffffffu, a, 8);
+  return a + __shfl_xor_sync(0xffffffffu, a, 16);
+}
+// Barrier over the 256 compute threads (named barrier 1).
+__device__ __forceinline__ void compute_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kComputeThreads) : "memory");
+}
+// The same barrier, returning the AND of v over the compute threads.
+__device__ __forceinline__ bool compute_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, 1, %2, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "n"(kComputeThreads)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns, DeviceStatus* st,
+                                          int site) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, limit_ns, st, site));
+}
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// 2^n as a float for -126 <= n <= 127, 0 below.
+__device__ __forceinline__ float pow2i(int n) {
+  return n < -126 ? 0.0f : __uint_as_float(static_cast<uint32_t>(n + 127) << 23);
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+// Two int8 codes, already offset by 128 (byte ^ 0x80), picked from ub by sel (0x4140:
+// bytes 0 and 1; 0x4342: bytes 2 and 3) and widened exactly to an fp16 pair: each byte
+// u becomes the mantissa of 1024 + u, and subtracting 1152 leaves u - 128.
+__device__ __forceinline__ uint32_t codes_f16x2(uint32_t ub, uint32_t sel) {
+  const uint32_t h = prmt(ub, 0x64646464u, sel);
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
+  return r;
+}
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Quantise one q row of D values (f16/bf16/f32) held by a warp, D / 32 per lane.
+template <int D>
+__device__ __forceinline__ float quant_row_warp(const float (&v)[D / 32], int8_t (&code)[D / 32]) {
+  float amax = 0.0f;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-  return a;
-}
-
-// int8 byte k of w (sign-extended) as float
-__device__ __forceinline__ float i8_to_f(uint32_t w, int k) {
-  return static_cast<float>(static_cast<int8_t>((w >> (8 * k)) & 0xFFu));
-}
-
-// An empty split: lse = -inf and a zero partial O for the G rows of the group.
-__device__ __forceinline__ void write_empty_split(const DecodeArgs& a, int64_t part_row0, int split, int G, int D) {
-  for (int i = threadIdx.x; i < G * D; i += kThreads) {
-    const int g = i / D, c = i % D;
-    a.o_partial[((part_row0 + g) * a.num_splits + split) * D + c] = 0.0f;
+  for (int e = 0; e < D / 32; ++e) amax = fmaxf(amax, fabsf(v[e]));
+  amax = warp_max_f(amax);
+  const float sc = __fdiv_rn(amax, 127.0f);
+#pragma unroll
+  for (int e = 0; e < D / 32; ++e) {
+    int c = 0;
+    if (sc != 0.0f) {
+      c = __float2int_rn(__fdiv_rn(v[e], sc));
+      c = c > 127 ? 127 : (c < -127 ? -127 : c);
+    }
+    code[e] = static_cast<int8_t>(c);
   }
-  if (threadIdx.x < G) a.lse_partial[(part_row0 + threadIdx.x) * a.num_splits + split] = -INFINITY;
+  return sc;
 }
 
-template <int D, int GT>
-__global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodeArgs a, DeviceStatus* st, uint64_t limit_ns) {
-  using C = DCfg<D>;
-  using S = DSmem<D, GT>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  int8_t* sk = reinterpret_cast<int8_t*>(smem + S::kK);
-  int8_t* sv = reinterpret_cast<int8_t*>(smem + S::kV);
-  float* sks = reinterpret_cast<float*>(smem + S::kKs);
-  float* svs = reinterpret_cast<float*>(smem + S::kVs);
-  float* score = reinterpret_cast<float*>(smem + S::kScore);
-  int8_t* sq = reinterpret_cast<int8_t*>(smem + S::kQ);
-  float* sqs = reinterpret_cast<float*>(smem + S::kQs);
-  float* red = reinterpret_cast<float*>(smem + S::kRed);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + S::kBar);
+__device__ __forceinline__ float load_q_elem(const void* base, sl8_dtype dt, int64_t idx) {
+  return dt == SL8_BF16 ? bf16_bits(static_cast<const uint16_t*>(base)[idx])
+       : dt == SL8_F16 ? f16_bits(static_cast<const uint16_t*>(base)[idx])
+                       : static_cast<const float*>(base)[idx];
+}
 
-  const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
-  const int G = a.Hq / a.Hkv;
-  int L = a.seqlens[b];
+// 16 consecutive q values of one row from shared memory.
+__device__ __forceinline__ void load_q16(const uint8_t* row, sl8_dtype dt, int e0, float (&v)[16]) {
+  if (dt == SL8_F32) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 f = *reinterpret_cast<const float4*>(row + (e0 + 4 * i) * 4);
+      v[4 * i] = f.x;
+      v[4 * i + 1] = f.y;
+      v[4 * i + 2] = f.z;
+      v[4 * i + 3] = f.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint4 u = *reinterpret_cast<const uint4*>(row + (e0 + 8 * i) * 2);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        v[8 * i + 2 * k] = dt == SL8_BF16 ? bf16_bits(w[k] & 0xffffu) : f16_bits(w[k] & 0xffffu);
+        v[8 * i + 2 * k + 1] = dt == SL8_BF16 ? bf16_bits(w[k] >> 16) : f16_bits(w[k] >> 16);
+      }
+    }
+  }
+}
+
+// Work slot -> (split, b, hkv); splits outermost so that every CTA gets a mix of
+// early (always non-empty) and late splits.
+struct Slot {
+  int split, b, hkv, t0, t1;
+};
+__device__ __forceinline__ Slot decode_slot(const DecodeArgs& a, int64_t i, DeviceStatus* st, bool report) {
+  Slot s;
+  const int64_t per = static_cast<int64_t>(a.B) * a.Hkv;
+  s.split = static_cast<int>(i / per);
+  const int64_t r = i - s.split * per;
+  s.b = static_cast<int>(r / a.Hkv);
+  s.hkv = static_cast<int>(r - static_cast<int64_t>(s.b) * a.Hkv);
+  int L = a.seqlens[s.b];
   if (L < 0 || L > a.Lmax) {
-    if (tid == 0) record_status(st, kStatusBadArg, 700);
+    if (report) record_status(st, kStatusBadArg, 700);
     L = L < 0 ? 0 : a.Lmax;
   }
-  const int t_begin = split * a.split_size;
-  const int t_end = min(t_begin + a.split_size, L);
-  const int64_t part_row0 = (static_cast<int64_t>(b) * a.Hq + hkv * G);  // first (b, hq) row of this group
-  const bool empty = t_begin >= t_end;
-  if (empty && !(split == 0 && a.q_codes)) {
-    write_empty_split(a, part_row0, split, G, D);
-    return;
-  }
+  s.t0 = s.split * a.split_size;
+  s.t1 = min(s.t0 + a.split_size, L);
+  return s;
+}
 
-  // ---- quantise the G query rows of this kv group (warp per row)
-  for (int g = warp; g < GT; g += kThreads / 32) {
-    float v[D / 32];
-    const int64_t qrow = (static_cast<int64_t>(b) * a.Hq + hkv * G + g) * D;
-#pragma unroll
-    for (int e = 0; e < D / 32; ++e) {
-      const int c = lane * (D / 32) + e;
-      float x = 0.0f;
-      if (g < G) {
-        if (a.q_dtype == SL8_BF16) x = bf16_bits(static_cast<const uint16_t*>(a.q)[qrow + c]);
-        else if (a.q_dtype == SL8_F16) x = f16_bits(static_cast<const uint16_t*>(a.q)[qrow + c]);
-        else x = static_cast<const float*>(a.q)[qrow + c];
-      }
-      v[e] = x;
-    }
-    float amax = 0.0f;
-#pragma unroll
-    for (int e = 0; e < D / 32; ++e) amax = fmaxf(amax, fabsf(v[e]));
-    amax = warp_max_f(amax);
-    const float s = __fdiv_rn(amax, 127.0f);
-#pragma unroll
-    for (int e = 0; e < D / 32; ++e) {
-      int code = 0;
-      if (s != 0.0f) {
-        code = __float2int_rn(__fdiv_rn(v[e], s));
-        code = code > 127 ? 127 : (code < -127 ? -127 : code);
-      }
-      sq[g * D + lane * (D / 32) + e] = static_cast<int8_t>(code);
-      if (split == 0 && g < G && a.q_codes) a.q_codes[qrow + lane * (D / 32) + e] = static_cast<int8_t>(code);
-    }
-    if (lane == 0) {
-      sqs[g] = s;
-      if (split == 0 && g < G && a.q_scales) a.q_scales[qrow / D] = s;
-    }
-  }
-  if (empty) {  // split 0 of an empty sequence: only the q codes were asked for
-    write_empty_split(a, part_row0, split, G, D);
-    return;
-  }
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap map_k,
+                        const __grid_constant__ CUtensorMap map_v, DeviceStatus* st, uint64_t limit_ns) {
+  using C = DCfg<D>;
+  constexpr int kStages = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBar);
+  uint64_t* empty = full + kStages;
+  uint64_t* q_full = empty + kStages;
+  uint64_t* q_empty = q_full + kQSlots;
 
-  // thread roles for the dot products and P.V: 8 threads (for d = 128) per key row
-  const int sub = tid % C::kTPR;           // 16-byte column slice of the row
-  const int rsub = tid / C::kTPR;          // row within a pass
-  const float log2e_over_sqrtd = 1.4426950408889634f / sqrtf(static_cast<float>(D));
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+  const int G = a.Hq / a.Hkv;
+  const int64_t n_slots = static_cast<int64_t>(a.num_splits) * a.B * a.Hkv;
+  const int q_elem = a.q_dtype == SL8_F32 ? 4 : 2;
+  // scales ride the bulk copies when every stage's range is 16-byte aligned
+  const bool scales_bulk = (a.Lmax % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.k_scale) |
+                                                  reinterpret_cast<uintptr_t>(a.v_scale)) & 15u) == 0;
 
-  if (tid == 0) {
-    mbar_init(bar, 1);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kComputeWarps);
+    }
+    for (int i = 0; i < kQSlots; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], kComputeWarps);
+    }
     fence_barrier_init();
   }
   __syncthreads();
 
-  // running statistics over the sub-chunks of this split (per q row g; every thread
-  // keeps the copy for all g, identical across threads)
-  float run_m[GT], run_l[GT];
-  float acc[GT][16];
-#pragma unroll
-  for (int g = 0; g < GT; ++g) {
-    run_m[g] = -INFINITY;
-    run_l[g] = 0.0f;
-#pragma unroll
-    for (int c = 0; c < 16; ++c) acc[g][c] = 0.0f;
-  }
-  // this thread's 16 q codes per row, as 4 words
-  uint32_t qw[GT][4];
-#pragma unroll
-  for (int g = 0; g < GT; ++g) {
-    const uint4 w = *reinterpret_cast<const uint4*>(sq + g * D + sub * 16);
-    qw[g][0] = w.x; qw[g][1] = w.y; qw[g][2] = w.z; qw[g][3] = w.w;
-  }
-  float qsc[GT];
-#pragma unroll
-  for (int g = 0; g < GT; ++g) qsc[g] = sqs[g] * log2e_over_sqrtd;
-
-  const int64_t cache_row0 = (static_cast<int64_t>(b) * a.Hkv + hkv) * a.Lmax;
-  uint32_t phase = 0;
-  bool ok = true;
-  for (int c0 = t_begin; c0 < t_end; c0 += C::kChunk) {
-    const int n = min(C::kChunk, t_end - c0);
-    if (tid == 0) {
-      const uint32_t bytes = static_cast<uint32_t>(n) * D;
-      mbar_arrive_expect_tx(bar, 2 * bytes);
-      bulk_load(sk, a.k_cache + (cache_row0 + c0) * D, bytes, bar);
-      bulk_load(sv, a.v_cache + (cache_row0 + c0) * D, bytes, bar);
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&map_k);
+      prefetch_tensormap(&map_v);
     }
-    for (int i = tid; i < n; i += kThreads) {
-      sks[i] = a.k_scale[cache_row0 + c0 + i];
-      svs[i] = a.v_scale[cache_row0 + c0 + i];
-    }
-    ok = mbar_wait(bar, phase, limit_ns, st, 40);
-    phase ^= 1;
-    if (!__syncthreads_and(ok)) break;  // also publishes the scales
-
-    // ---- scores: x2[g][t] = S * s_q * s_k[t] * log2(e) / sqrt(d)
-    for (int r0 = 0; r0 < n; r0 += C::kRowsPerPass) {
-      const int t = r0 + rsub;
-      uint4 kw = make_uint4(0, 0, 0, 0);
-      if (t < n) kw = *reinterpret_cast<const uint4*>(sk + t * D + sub * 16);
-      int dot[GT];
-#pragma unroll
-      for (int g = 0; g < GT; ++g) {
-        int s = 0;
-        s = __dp4a(static_cast<int>(kw.x), static_cast<int>(qw[g][0]), s);
-        s = __dp4a(static_cast<int>(kw.y), static_cast<int>(qw[g][1]), s);
-        s = __dp4a(static_cast<int>(kw.z), static_cast<int>(qw[g][2]), s);
-        s = __dp4a(static_cast<int>(kw.w), static_cast<int>(qw[g][3]), s);
-#pragma unroll
-        for (int o = 1; o < C::kTPR; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        dot[g] = s;
+    uint32_t k = 0, nq = 0;  // stages and q rows issued
+    bool ok = true;
+    for (int64_t i = blockIdx.x; i < n_slots && ok; i += gridDim.x) {
+      const Slot s = decode_slot(a, i, st, lane == 0);
+      if (s.t0 >= s.t1) continue;
+      const int64_t row0 = (static_cast<int64_t>(s.b) * a.Hkv + s.hkv) * a.Lmax;
+      {
+        const uint32_t qs = nq % kQSlots;
+        if (nq >= kQSlots) ok = warp_wait(&q_empty[qs], ((nq / kQSlots) - 1) & 1, limit_ns, st, 42);
+        if (!ok) break;
+        if (lane == 0) {
+          const uint32_t q_bytes = static_cast<uint32_t>(G * D * q_elem);
+          mbar_arrive_expect_tx(&q_full[qs], q_bytes);
+          bulk_load(smem + C::kQ + qs * C::kQBytes,
+                    static_cast<const uint8_t*>(a.q) + (static_cast<int64_t>(s.b) * a.Hq + s.hkv * G) * D * q_elem,
+                    q_bytes, &q_full[qs]);
+        }
+        ++nq;
       }
-      if (sub == 0 && t < n) {
-        const float kscale = sks[t];
+      for (int c0 = s.t0; c0 < s.t1 && ok; c0 += kChunk, ++k) {
+        const int n = min(kChunk, s.t1 - c0);
+        const uint32_t stg = k % kStages;
+        uint8_t* base = smem + stg * C::kStageBytes;
+        if (k >= kStages) ok = warp_wait(&empty[stg], ((k / kStages) - 1) & 1, limit_ns, st, 41);
+        if (!ok) break;
+        if (!scales_bulk) {
+          for (int j = lane; j < n; j += 32) {
+            reinterpret_cast<float*>(base + C::kSKs)[j] = a.k_scale[row0 + c0 + j];
+            reinterpret_cast<float*>(base + C::kSVs)[j] = a.v_scale[row0 + c0 + j];
+          }
+          __syncwarp();
+        }
+        if (lane == 0) {
+          const uint32_t sc_bytes = scales_bulk ? static_cast<uint32_t>((n + 3) / 4 * 16) : 0u;
+          mbar_arrive_expect_tx(&full[stg], 2 * C::kTile + 2 * sc_bytes);
+          const int y = static_cast<int>(row0 + c0);
 #pragma unroll
-        for (int g = 0; g < GT; ++g) {
-          if (a.logits && g < G)
-            a.logits[(part_row0 + g) * a.Lmax + c0 + t] = dot[g];
-          score[g * C::kChunk + t] = static_cast<float>(dot[g]) * kscale * qsc[g];
+          for (int b = 0; b < C::kBoxes; ++b) {
+            tma_load_3d(base + C::kSK + b * kChunk * C::kBW, &map_k, &full[stg], b * C::kBW, y, 0);
+            tma_load_3d(base + C::kSV + b * kChunk * C::kBW, &map_v, &full[stg], b * C::kBW, y, 0);
+          }
+          if (scales_bulk) {
+            bulk_load(base + C::kSKs, a.k_scale + row0 + c0, sc_bytes, &full[stg]);
+            bulk_load(base + C::kSVs, a.v_scale + row0 + c0, sc_bytes, &full[stg]);
+          }
         }
       }
     }
-    __syncthreads();
-
-    // ---- sub-chunk softmax statistics (warp per row g), weights w = p * s_v
-    float* rowstat = reinterpret_cast<float*>(smem + S::kRowStat);
-    for (int g = warp; g < GT; g += kThreads / 32) {
-      float mx = -INFINITY;
-      for (int t = lane; t < n; t += 32) mx = fmaxf(mx, score[g * C::kChunk + t]);
-      mx = warp_max_f(mx);
-      const float m_new = fmaxf(run_m[g], mx);
-      float sum = 0.0f;
-      for (int t = lane; t < n; t += 32) {
-        const float p = exp2f(score[g * C::kChunk + t] - m_new);
-        sum += p;
-        score[g * C::kChunk + t] = p * svs[t];
-      }
-      sum = warp_sum_f(sum);
-      if (lane == 0) {
-        rowstat[2 * g] = m_new;
-        rowstat[2 * g + 1] = sum;
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int g = 0; g < GT; ++g) {
-      const float m_new = rowstat[2 * g];
-      const float corr = run_m[g] == -INFINITY ? 0.0f : exp2f(run_m[g] - m_new);
-      run_l[g] = run_l[g] * corr + rowstat[2 * g + 1];
-      run_m[g] = m_new;
-#pragma unroll
-      for (int c = 0; c < 16; ++c) acc[g][c] *= corr;
-    }
-
-    // ---- P.V: each thread accumulates its 16 channels over rows t = rsub (mod rows per pass)
-    for (int t = rsub; t < n; t += C::kRowsPerPass) {
-      const uint4 vw = *reinterpret_cast<const uint4*>(sv + t * D + sub * 16);
-      float vf[16];
-      const uint32_t wds[4] = {vw.x, vw.y, vw.z, vw.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) vf[q * 4 + k] = i8_to_f(wds[q], k);
-#pragma unroll
-      for (int g = 0; g < GT; ++g) {
-        const float wt = score[g * C::kChunk + t];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) acc[g][c] = fmaf(wt, vf[c], acc[g][c]);
-      }
-    }
-    __syncthreads();  // score / sk / sv are rewritten by the next sub-chunk
+    return;  // the compute warps never wait on the producer beyond the rings
   }
 
-  if (!ok) return;
-  // ---- reduce acc over the row slots: within a warp (lanes with equal sub), then across warps
+  // ------------------------------------------------------------ compute warps
+  const int ct = threadIdx.x - 32;  // 0 .. 255
+  const int cw = ct / 32;           // compute warp 0 .. 7
+  const int g = lane >> 2, t = lane & 3;
+  // S^T rows of this lane: stage-local tokens u0 + pi and u0 + pi + 8 (a permutation of
+  // the unit's rows that keeps the swizzled K reads free of bank conflicts)
+  const int pi = C::kSwz ? (g >> 1) + 4 * (g & 1) : g;
+  // V^T rows of this lane: 16-byte chunk (8-byte piece for d = 64) of each V row
+  const int cg = C::kSwz ? (g >> 1) + 4 * (g & 1) : g;
+  const float log2e_over_sqrtd = 1.4426950408889634f / sqrtf(static_cast<float>(D));
+  float* stat = reinterpret_cast<float*>(smem + C::kStat);
+  float* red = reinterpret_cast<float*>(smem + C::kRed);
+  uint16_t* pw = reinterpret_cast<uint16_t*>(smem + C::kP + cw * 256);  // [8 q][8 pairs][2] fp16
+  const uint32_t* pw32 = reinterpret_cast<const uint32_t*>(pw);
+  uint32_t k = 0, nq = 0;
+  bool ok = true;
+  for (int64_t i = blockIdx.x; i < n_slots && ok; i += gridDim.x) {
+    const Slot s = decode_slot(a, i, st, false);
+    const int64_t part_row0 = static_cast<int64_t>(s.b) * a.Hq + s.hkv * G;  // first (b, hq) row
+    if (s.t0 >= s.t1) {
+      // an empty split: lse = -inf (its O is never read); split 0 of an empty sequence
+      // still exports the q codes when asked
+      if (ct < G) a.lse_partial[(part_row0 + ct) * a.num_splits + s.split] = -INFINITY;
+      if (s.split == 0 && a.q_codes && cw < G) {
+        float v[D / 32];
+        int8_t code[D / 32];
 #pragma unroll
-  for (int g = 0; g < GT; ++g)
+        for (int e = 0; e < D / 32; ++e) v[e] = load_q_elem(a.q, a.q_dtype, (part_row0 + cw) * D + lane * (D / 32) + e);
+        const float sc = quant_row_warp<D>(v, code);
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      float v = acc[g][c];
-#pragma unroll
-      for (int o = C::kTPR; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      acc[g][c] = v;
+        for (int e = 0; e < D / 32; ++e) a.q_codes[(part_row0 + cw) * D + lane * (D / 32) + e] = code[e];
+        if (lane == 0) a.q_scales[part_row0 + cw] = sc;
+      }
+      continue;
     }
-  if (lane < C::kTPR) {
+
+    // ---- the group's q rows: quantise row g (lanes of one group share it) straight
+    // into the B fragments; k-step 4h + j covers dims 64h + 16t + 4j + {0..3}
+    uint32_t qb[D / 16][2];
+    float qsa = 0.0f, qsb = 0.0f;  // dequantisation factors (log2 units) of query columns 2t, 2t+1
+    const uint32_t qs = nq % kQSlots;
+    ok = warp_wait(&q_full[qs], (nq / kQSlots) & 1, limit_ns, st, 43);
+    ++nq;
+    if (ok) {
+      const uint8_t* qrow = smem + C::kQ + qs * C::kQBytes + g * D * q_elem;
+      float qv[D / 64][16];
+      float amax = 0.0f;
 #pragma unroll
-    for (int g = 0; g < GT; ++g)
+      for (int h = 0; h < D / 64; ++h) {
+        if (g < G) {
+          load_q16(qrow, a.q_dtype, 64 * h + 16 * t, qv[h]);
+        } else {
 #pragma unroll
-      for (int c = 0; c < 16; ++c) red[(warp * GT + g) * D + sub * 16 + c] = acc[g][c];
-  }
-  __syncthreads();
-  for (int i = tid; i < G * D; i += kThreads) {
-    const int g = i / D, c = i % D;
-    float v = 0.0f;
+          for (int e = 0; e < 16; ++e) qv[h][e] = 0.0f;
+        }
 #pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) v += red[(w * GT + g) * D + c];
-    a.o_partial[((part_row0 + g) * a.num_splits + split) * D + c] = v / run_l[g];
-  }
-  if (tid < G) {
-    a.lse_partial[(part_row0 + tid) * a.num_splits + split] = (run_m[tid] + log2f(run_l[tid])) * 0.6931471805599453f;
+        for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(qv[h][e]));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_empty[qs]);
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      const float sc = __fdiv_rn(amax, 127.0f);
+      const bool export_q = a.q_codes && s.split == 0 && cw == 0 && g < G;
+#pragma unroll
+      for (int h = 0; h < D / 64; ++h) {
+        int c[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          c[e] = 0;
+          if (sc != 0.0f) {
+            c[e] = __float2int_rn(__fdiv_rn(qv[h][e], sc));
+            c[e] = c[e] > 127 ? 127 : (c[e] < -127 ? -127 : c[e]);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          qb[4 * h + j][0] = f16x2_of(static_cast<float>(c[4 * j]), static_cast<float>(c[4 * j + 1]));
+          qb[4 * h + j][1] = f16x2_of(static_cast<float>(c[4 * j + 2]), static_cast<float>(c[4 * j + 3]));
+        }
+        if (export_q) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) a.q_codes[(part_row0 + g) * D + 64 * h + 16 * t + e] = static_cast<int8_t>(c[e]);
+        }
+      }
+      if (export_q && t == 0) a.q_scales[part_row0 + g] = sc;
+      const float qf = sc * log2e_over_sqrtd;
+      qsa = __shfl_sync(0xffffffffu, qf, 8 * t);
+      qsb = __shfl_sync(0xffffffffu, qf, 8 * t + 4);
+    }
+
+    // ---- per-warp online softmax state for query columns qa = 2t, qb = 2t + 1
+    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.0f, l_b = 0.0f;
+    int E = -126;                    // P' carries s_v * 2^-E
+    float vlim = pow2i(-126), inv = __uint_as_float(253u << 23);  // 2^E, 2^-E
+    float o[D / 16][4];
+#pragma unroll
+    for (int j = 0; j < D / 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.0f;
+
+    for (int c0 = s.t0; c0 < s.t1 && ok; c0 += kChunk, ++k) {
+      const int n = min(kChunk, s.t1 - c0);
+      const uint32_t stg = k % kStages;
+      const uint8_t* base = smem + stg * C::kStageBytes;
+      if (!warp_wait(&full[stg], (k / kStages) & 1, limit_ns, st, 40)) {
+        ok = false;
+        break;
+      }
+      const int nv = n - kUnit * cw;  // valid tokens of this warp's unit
+      if (nv > 0) {
+        const int u0 = kUnit * cw;
+        const uint8_t* sk = base + C::kSK;
+        const uint8_t* sv = base + C::kSV;
+        const float* sks = reinterpret_cast<const float*>(base + C::kSKs);
+        const float* svs = reinterpret_cast<const float*>(base + C::kSVs);
+        const int rA = u0 + pi, rB = rA + 8;
+        // ---- S^T = K . Q^T (two accumulation chains)
+        float s0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+          const uint4 wa = *reinterpret_cast<const uint4*>(sk + tile_off<D>(rA, 4 * h + t));
+          const uint4 wb = *reinterpret_cast<const uint4*>(sk + tile_off<D>(rB, 4 * h + t));
+          const uint32_t A[4] = {wa.x, wa.y, wa.z, wa.w}, Bw[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t ua = A[j] ^ 0x80808080u, ub = Bw[j] ^ 0x80808080u;
+            mma_f16(j & 1 ? s1 : s0, codes_f16x2(ua, 0x4140), codes_f16x2(ub, 0x4140), codes_f16x2(ua, 0x4342),
+                    codes_f16x2(ub, 0x4342), qb[4 * h + j][0], qb[4 * h + j][1]);
+          }
+        }
+        const float d00 = s0[0] + s1[0], d01 = s0[1] + s1[1], d10 = s0[2] + s1[2], d11 = s0[3] + s1[3];
+        const bool vA = pi < nv, vB = pi + 8 < nv;
+        if (a.logits) {
+          int32_t* lg = a.logits + c0;
+          if (2 * t < G) {
+            if (vA) lg[(part_row0 + 2 * t) * a.Lmax + rA] = static_cast<int32_t>(d00);
+            if (vB) lg[(part_row0 + 2 * t) * a.Lmax + rB] = static_cast<int32_t>(d10);
+          }
+          if (2 * t + 1 < G) {
+            if (vA) lg[(part_row0 + 2 * t + 1) * a.Lmax + rA] = static_cast<int32_t>(d01);
+            if (vB) lg[(part_row0 + 2 * t + 1) * a.Lmax + rB] = static_cast<int32_t>(d11);
+          }
+        }
+        // ---- online softmax (log2 units), lazily rescaled
+        const float ksA = vA ? sks[rA] : 0.0f, ksB = vB ? sks[rB] : 0.0f;
+        const float vsA = vA ? svs[rA] : 0.0f, vsB = vB ? svs[rB] : 0.0f;
+        const float xa0 = vA ? d00 * ksA * qsa : -INFINITY, xa1 = vA ? d01 * ksA * qsb : -INFINITY;
+        const float xb0 = vB ? d10 * ksB * qsa : -INFINITY, xb1 = vB ? d11 * ksB * qsb : -INFINITY;
+        const float ma = col_max(fmaxf(xa0, xb0)), mb = col_max(fmaxf(xa1, xb1));
+        const float vm = col_max(fmaxf(vsA, vsB));
+        const bool grow_a = ma > m_a + kLazy, grow_b = mb > m_b + kLazy, grow_v = vm > vlim;
+        if (__any_sync(0xffffffffu, grow_a || grow_b || grow_v)) {
+          float fa = 1.0f, fb = 1.0f;
+          if (grow_a) {
+            fa = m_a == -INFINITY ? 0.0f : ex2(m_a - ma);
+            l_a *= fa;
+            m_a = ma;
+          }
+          if (grow_b) {
+            fb = m_b == -INFINITY ? 0.0f : ex2(m_b - mb);
+            l_b *= fb;
+            m_b = mb;
+          }
+          if (grow_v) {  // uniform: vm is the unit's max over all lanes
+            int e = static_cast<int>((__float_as_uint(vm) >> 23) & 0xffu) - 126;  // vm < 2^e
+            e = e > 126 ? 126 : e;
+            const float fe = pow2i(E - e);
+            fa *= fe;
+            fb *= fe;
+            E = e;
+            vlim = pow2i(e);
+            inv = pow2i(-e);
+          }
+#pragma unroll
+          for (int j = 0; j < D / 16; ++j) {
+            o[j][0] *= fa;
+            o[j][2] *= fa;
+            o[j][1] *= fb;
+            o[j][3] *= fb;
+          }
+        }
+        const float pa0 = ex2(xa0 - m_a), pa1 = ex2(xa1 - m_b), pb0 = ex2(xb0 - m_a), pb1 = ex2(xb1 - m_b);
+        l_a += pa0 + pb0;
+        l_b += pa1 + pb1;
+        const float wA = vsA * inv, wB = vsB * inv;
+        // ---- P'^T into the B-fragment order: pair u < 4 holds tokens (u, u + 4), pair
+        // 4 + u holds (u + 8, u + 12); this lane's tokens are pi and pi + 8
+        __syncwarp();
+        {
+          const int pr = pi & 3, hf = pi >> 2;
+          const __half h_a0 = __float2half_rn(pa0 * wA), h_a1 = __float2half_rn(pa1 * wA);
+          const __half h_b0 = __float2half_rn(pb0 * wB), h_b1 = __float2half_rn(pb1 * wB);
+          pw[((2 * t) * 8 + pr) * 2 + hf] = __half_as_ushort(h_a0);
+          pw[((2 * t + 1) * 8 + pr) * 2 + hf] = __half_as_ushort(h_a1);
+          pw[((2 * t) * 8 + 4 + pr) * 2 + hf] = __half_as_ushort(h_b0);
+          pw[((2 * t + 1) * 8 + 4 + pr) * 2 + hf] = __half_as_ushort(h_b1);
+        }
+        __syncwarp();
+        const uint32_t pb0r = pw32[g * 8 + t], pb1r = pw32[g * 8 + 4 + t];
+        // ---- O^T += V^T . P'^T; V rows u0 + t + 4c (c = 0..3) are the k columns
+        // 2t, 2t + 1, 2t + 8, 2t + 9
+        if constexpr (D == 64) {
+          uint2 w[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint2*>(sv + (u0 + t + 4 * c) * 64 + 8 * cg);
+#pragma unroll
+          for (int ii = 0; ii < 2; ++ii) {
+            const uint32_t w0 = ii ? w[0].y : w[0].x, w1 = ii ? w[1].y : w[1].x;
+            const uint32_t w2 = ii ? w[2].y : w[2].x, w3 = ii ? w[3].y : w[3].x;
+            const uint32_t x01 = prmt(w0, w1, 0x5140) ^ 0x80808080u, y01 = prmt(w0, w1, 0x7362) ^ 0x80808080u;
+            const uint32_t x23 = prmt(w2, w3, 0x5140) ^ 0x80808080u, y23 = prmt(w2, w3, 0x7362) ^ 0x80808080u;
+            mma_f16(o[2 * ii], codes_f16x2(x01, 0x4140), codes_f16x2(x01, 0x4342), codes_f16x2(x23, 0x4140),
+                    codes_f16x2(x23, 0x4342), pb0r, pb1r);
+            mma_f16(o[2 * ii + 1], codes_f16x2(y01, 0x4140), codes_f16x2(y01, 0x4342), codes_f16x2(y23, 0x4140),
+                    codes_f16x2(y23, 0x4342), pb0r, pb1r);
+          }
+        } else {
+#pragma unroll
+          for (int b = 0; b < C::kBoxes; ++b) {
+            uint4 w[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              w[c] = *reinterpret_cast<const uint4*>(sv + tile_off<D>(u0 + t + 4 * c, 8 * b + cg));
+#pragma unroll
+            for (int ii = 0; ii < 4; ++ii) {
+              const uint32_t w0 = ii == 0 ? w[0].x : ii == 1 ? w[0].y : ii == 2 ? w[0].z : w[0].w;
+              const uint32_t w1 = ii == 0 ? w[1].x : ii == 1 ? w[1].y : ii == 2 ? w[1].z : w[1].w;
+              const uint32_t w2 = ii == 0 ? w[2].x : ii == 1 ? w[2].y : ii == 2 ? w[2].z : w[2].w;
+              const uint32_t w3 = ii == 0 ? w[3].x : ii == 1 ? w[3].y : ii == 2 ? w[3].z : w[3].w;
+              const uint32_t x01 = prmt(w0, w1, 0x5140) ^ 0x80808080u, y01 = prmt(w0, w1, 0x7362) ^ 0x80808080u;
+              const uint32_t x23 = prmt(w2, w3, 0x5140) ^ 0x80808080u, y23 = prmt(w2, w3, 0x7362) ^ 0x80808080u;
+              mma_f16(o[8 * b + 2 * ii], codes_f16x2(x01, 0x4140), codes_f16x2(x01, 0x4342),
+                      codes_f16x2(x23, 0x4140), codes_f16x2(x23, 0x4342), pb0r, pb1r);
+              mma_f16(o[8 * b + 2 * ii + 1], codes_f16x2(y01, 0x4140), codes_f16x2(y01, 0x4342),
+                      codes_f16x2(y23, 0x4140), codes_f16x2(y23, 0x4342), pb0r, pb1r);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stg]);  // 8 arrivals (one per compute warp) free the stage
+    }
+    if (!compute_all(ok)) {
+      ok = false;
+      break;
+    }
+    // ---- merge the eight warps' states of this split
+    l_a = col_sum(l_a);
+    l_b = col_sum(l_b);
+    if (g == 0) {
+      float* sa = stat + (cw * 8 + 2 * t) * 4;
+      sa[0] = m_a;
+      sa[1] = l_a;
+      sa[4] = m_b;
+      sa[5] = l_b;
+    }
+    compute_sync();
+    float Ma = -INFINITY, Mb = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kComputeWarps; ++w) {
+      Ma = fmaxf(Ma, stat[(w * 8 + 2 * t) * 4]);
+      Mb = fmaxf(Mb, stat[(w * 8 + 2 * t + 1) * 4]);
+    }
+    float La = 0.0f, Lb = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kComputeWarps; ++w) {
+      const float* sa = stat + (w * 8 + 2 * t) * 4;
+      if (sa[0] != -INFINITY) La += sa[1] * ex2(sa[0] - Ma);
+      if (sa[4] != -INFINITY) Lb += sa[5] * ex2(sa[4] - Mb);
+    }
+    const float pe = pow2i(E);
+    const float fa = m_a == -INFINITY ? 0.0f : ex2(m_a - Ma) * pe / La;
+    const float fb = m_b == -INFINITY ? 0.0f : ex2(m_b - Mb) * pe / Lb;
+#pragma unroll
+    for (int j = 0; j < D / 16; ++j) {
+      // physical dims of rows g and g + 8 of m-tile j
+      int dim;
+      if constexpr (D == 64) {
+        dim = 8 * cg + 4 * (j >> 1) + 2 * (j & 1);
+      } else {
+        dim = 128 * (j >> 3) + 16 * cg + 4 * ((j & 7) >> 1) + 2 * (j & 1);
+      }
+      *reinterpret_cast<float2*>(red + (cw * D + dim) * 8 + 2 * t) = make_float2(o[j][0] * fa, o[j][1] * fb);
+      *reinterpret_cast<float2*>(red + (cw * D + dim + 1) * 8 + 2 * t) = make_float2(o[j][2] * fa, o[j][3] * fb);
+    }
+    if (cw == 0 && g == 0) {
+      if (2 * t < G)
+        a.lse_partial[(part_row0 + 2 * t) * a.num_splits + s.split] = (Ma + log2f(La)) * 0.6931471805599453f;
+      if (2 * t + 1 < G)
+        a.lse_partial[(part_row0 + 2 * t + 1) * a.num_splits + s.split] = (Mb + log2f(Lb)) * 0.6931471805599453f;
+    }
+    compute_sync();
+    for (int idx = ct; idx < D * 8; idx += kComputeThreads) {
+      const int q = idx & 7, dim = idx >> 3;
+      if (q >= G) continue;
+      float acc = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kComputeWarps; ++w) acc += red[(w * D + dim) * 8 + q];
+      a.o_partial[((part_row0 + q) * a.num_splits + s.split) * D + dim] = acc;
+    }
+    compute_sync();
   }
 }
 
@@ -370,30 +678,30 @@ __global__ void timeout_selftest_kernel(uint64_t limit_ns, DeviceStatus* st) {
   if (threadIdx.x == 0) mbar_wait(&bar, 0, limit_ns, st, 999);
 }
 
-template <int D, int GT>
-cudaError_t launch_split_dg(const DecodeArgs& a, cudaStream_t s) {
-  using S = DSmem<D, GT>;
-  auto kern = decode_split_kernel<D, GT>;
-  const int smem = S::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  dim3 grid(a.num_splits, a.Hkv, a.B);
-  kern<<<grid, kThreads, smem, s>>>(a, device_status_ptr(), spin_limit_ns());
-  return cudaGetLastError();
-}
-
 template <int D>
 cudaError_t launch_split_d(const DecodeArgs& a, cudaStream_t s) {
-  const int G = a.Hq / a.Hkv;
-  if (G <= 1) return launch_split_dg<D, 1>(a, s);
-  if (G <= 2) return launch_split_dg<D, 2>(a, s);
-  if (G <= 4) return launch_split_dg<D, 4>(a, s);
-  return launch_split_dg<D, 8>(a, s);
+  using C = DCfg<D>;
+  auto kern = decode_split_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
+  if (e != cudaSuccess) return e;
+  // each cache as a 2-D [B * Hkv * Lmax rows][d bytes] tensor, loaded in boxes of
+  // kChunk rows x kBW bytes
+  const uint64_t rows = static_cast<uint64_t>(a.B) * a.Hkv * a.Lmax;
+  bool ok = true;
+  const CUtensorMap mk = make_tmap_3d(a.k_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, D, rows, 1, D, rows * D, C::kBW,
+                                      kChunk, 1, &ok, C::kSwz);
+  const CUtensorMap mv = make_tmap_3d(a.v_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, D, rows, 1, D, rows * D, C::kBW,
+                                      kChunk, 1, &ok, C::kSwz);
+  if (!ok) return cudaErrorInvalidValue;
+  const int64_t slots = static_cast<int64_t>(a.num_splits) * a.B * a.Hkv;
+  const int grid = static_cast<int>(slots < num_sms() ? slots : num_sms());
+  kern<<<grid, kThreads, C::kBytes, s>>>(a, mk, mv, device_status_ptr(), spin_limit_ns());
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-int decode_chunk_tokens(int d) { return 32768 / d; }  // DCfg<d>::kChunk
+int decode_chunk_tokens(int) { return kChunk; }
 
 cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t s) {
   TraceScope tr("decode_split", s);

@@ -61,20 +61,22 @@ extern "C" int sl8_attn_int8_decode_noalloc(const void* q, int q_dtype, const in
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Lmax < 0 || Hq % Hkv != 0) return SL8_ERR_INVALID_ARG;
   if (d != 64 && d != 128 && d != 256) return SL8_ERR_UNSUPPORTED;
   if (Hq / Hkv > 8 || B > 65535 || Hkv > 65535) return SL8_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * Hkv * Lmax >= (int64_t(1) << 31)) return SL8_ERR_UNSUPPORTED;
   if (B == 0 || Lmax == 0) return SL8_OK;
 
   // Partials per split: [B][Hq][d] fp32 O and [B][Hq] fp32 lse.  Use the automatic split
   // count, lowered to what the fixed scratch holds; refuse if one split does not fit.
   const size_t per_split = static_cast<size_t>(B) * Hq * (static_cast<size_t>(d) + 1);
   if (per_split > kScratchFloats) return SL8_ERR_WORKSPACE;
-  int32_t S = sl8_attn_decode_num_splits(Lmax, d, 0);
+  int32_t S = sl8_attn_decode_num_splits(B, Hkv, Lmax, d, 0);
   const size_t fit = kScratchFloats / per_split;
   if (static_cast<size_t>(S) > fit) S = static_cast<int32_t>(fit);
 
   float* scratch = scratch_on_current_device();
   if (!scratch) return SL8_ERR_CUDA;
-  // Nothing here needs to start at zero: the split kernel writes every slot (o_partial and
-  // lse_partial of every split, empty ones included) before the combine reads any.
+  // Nothing here needs to start at zero: the split kernel writes the lse of every split and
+  // the O of every non-empty split before the combine reads them, and the combine reads no
+  // other slot.
   float* o_partial = scratch;
   float* lse_partial = scratch + static_cast<size_t>(B) * Hq * S * d;
 
@@ -91,8 +93,8 @@ extern "C" int sl8_attn_int8_decode_noalloc(const void* q, int q_dtype, const in
   a.Hkv = Hkv;
   a.Lmax = Lmax;
   a.d = d;
-  a.num_splits = sl8_attn_decode_num_splits(Lmax, d, S);
-  a.split_size = sl8_attn_decode_split_size(Lmax, d, S);
+  a.num_splits = sl8_attn_decode_num_splits(B, Hkv, Lmax, d, S);  // <= S: fits the array
+  a.split_size = sl8_attn_decode_split_size(B, Hkv, Lmax, d, S);
   a.o_partial = o_partial;
   a.lse_partial = lse_partial;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -125,12 +125,13 @@ cudaError_t launch_decode_combine(const float* o_partial, const float* lse_parti
                                   void* out, sl8_dtype out_dtype, float* lse_out, cudaStream_t s);
 cudaError_t launch_timeout_selftest(uint64_t limit_ns, cudaStream_t s);
 
-// tokens per decode sub-chunk for head dim d (the automatic split size)
+// tokens per stage of the decode kernel for head dim d
 int decode_chunk_tokens(int d);
 
-// 3-D tiled tensor map, 128-byte swizzle, zero fill out of bounds; *ok = false on failure.
+// 3-D tiled tensor map, zero fill out of bounds, 128-byte swizzle (or none); *ok = false
+// on failure.
 CUtensorMap make_tmap_3d(const void* base, CUtensorMapDataType dt, uint64_t d0, uint64_t d1, uint64_t d2,
                          uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2,
-                         bool* ok);
+                         bool* ok, bool swizzle128 = true);
 
 }  // namespace sl8
