@@ -33,6 +33,7 @@
 //    than 2^8 (p then stays below 256), and the power-of-two V range E only when a
 //    token's V scale exceeds 2^E; both keep P' inside the fp16 range.
 #include <cuda_bf16.h>
+#include <type_traits>
 #include <cuda_fp16.h>
 
 #include "sl8_internal.h"
@@ -66,7 +67,8 @@ struct DCfg {
   static constexpr int kRed = kQ + kQSlots * kQBytes;          // [warp][d][8 q] floats
   static constexpr int kP = kRed + kComputeWarps * D * 8 * 4;  // [warp][8 q][8 token pairs] fp16x2
   static constexpr int kStat = kP + kComputeWarps * 256;       // [warp][8 q][4] floats
-  static constexpr int kBar = kStat + kComputeWarps * 8 * 16;
+  static constexpr int kQc = kStat + kComputeWarps * 8 * 16;   // [8][D] q codes, [8] scales, [8] sums
+  static constexpr int kBar = kQc + 8 * D + 64;
   static constexpr int kNumBars = 2 * kStages + 2 * kQSlots;
   static constexpr int kBytes = kBar + kNumBars * 8 + 1024;    // + alignment slack
   static_assert(kStageBytes % 1024 == 0 && kTile % 1024 == 0, "swizzled tiles need 1024-byte alignment");
@@ -181,31 +183,6 @@ __device__ __forceinline__ float load_q_elem(const void* base, sl8_dtype dt, int
   return dt == SL8_BF16 ? bf16_bits(static_cast<const uint16_t*>(base)[idx])
        : dt == SL8_F16 ? f16_bits(static_cast<const uint16_t*>(base)[idx])
                        : static_cast<const float*>(base)[idx];
-}
-
-// 16 consecutive q values of one row from shared memory.
-__device__ __forceinline__ void load_q16(const uint8_t* row, sl8_dtype dt, int e0, float (&v)[16]) {
-  if (dt == SL8_F32) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 f = *reinterpret_cast<const float4*>(row + (e0 + 4 * i) * 4);
-      v[4 * i] = f.x;
-      v[4 * i + 1] = f.y;
-      v[4 * i + 2] = f.z;
-      v[4 * i + 3] = f.w;
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const uint4 u = *reinterpret_cast<const uint4*>(row + (e0 + 8 * i) * 2);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        v[8 * i + 2 * k] = dt == SL8_BF16 ? bf16_bits(w[k] & 0xffffu) : f16_bits(w[k] & 0xffffu);
-        v[8 * i + 2 * k + 1] = dt == SL8_BF16 ? bf16_bits(w[k] >> 16) : f16_bits(w[k] >> 16);
-      }
-    }
-  }
 }
 
 // Work slot -> (split, b, hkv); splits outermost so that every CTA gets a mix of
@@ -325,16 +302,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ct = threadIdx.x - 32;  // 0 .. 255
   const int cw = ct / 32;           // compute warp 0 .. 7
   const int g = lane >> 2, t = lane & 3;
-  // S^T rows of this lane: stage-local tokens u0 + pi and u0 + pi + 8 (a permutation of
-  // the unit's rows that keeps the swizzled K reads free of bank conflicts)
+  const int u0 = kUnit * cw;        // this warp's rows in every stage
+  // S^T rows of this lane: unit tokens pi and pi + 8.  The permutation keeps the
+  // swizzled K reads free of bank conflicts, and the two tokens form P' pair pi.
   const int pi = C::kSwz ? (g >> 1) + 4 * (g & 1) : g;
-  // V^T rows of this lane: 16-byte chunk (8-byte piece for d = 64) of each V row
-  const int cg = C::kSwz ? (g >> 1) + 4 * (g & 1) : g;
+  // V^T rows of this lane: 16-byte chunk (8-byte piece for d = 64) pi of each V row
+  const int cg = pi;
+  // stage-tile offsets of this lane's reads, the same for every stage
+  uint32_t offk[D / 64][2];
+#pragma unroll
+  for (int h = 0; h < D / 64; ++h) {
+    offk[h][0] = tile_off<D>(u0 + pi, 4 * h + t);
+    offk[h][1] = tile_off<D>(u0 + pi + 8, 4 * h + t);
+  }
+  // V rows: unit tokens t, t + 8, t + 4, t + 12 are the k columns 2t, 2t+1, 2t+8, 2t+9
+  uint32_t offv[C::kBoxes][4];
+#pragma unroll
+  for (int b = 0; b < C::kBoxes; ++b)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int row = u0 + t + (c == 1 ? 8 : c == 2 ? 4 : c == 3 ? 12 : 0);
+      offv[b][c] = D == 64 ? static_cast<uint32_t>(row * 64 + 8 * cg) : tile_off<D>(row, 8 * b + cg);
+    }
   const float log2e_over_sqrtd = 1.4426950408889634f / sqrtf(static_cast<float>(D));
   float* stat = reinterpret_cast<float*>(smem + C::kStat);
   float* red = reinterpret_cast<float*>(smem + C::kRed);
-  uint16_t* pw = reinterpret_cast<uint16_t*>(smem + C::kP + cw * 256);  // [8 q][8 pairs][2] fp16
-  const uint32_t* pw32 = reinterpret_cast<const uint32_t*>(pw);
+  uint32_t* pw = reinterpret_cast<uint32_t*>(smem + C::kP + cw * 256);  // [8 q][8 pairs] fp16x2
+  int8_t* qcodes = reinterpret_cast<int8_t*>(smem + C::kQc);             // [8][D]
+  float* qinfo = reinterpret_cast<float*>(smem + C::kQc + 8 * D);        // [8] scale, [8] code sum
   uint32_t k = 0, nq = 0;
   bool ok = true;
   for (int64_t i = blockIdx.x; i < n_slots && ok; i += gridDim.x) {
@@ -357,66 +352,73 @@ __global__ void __launch_bounds__(kThreads, 1)
       continue;
     }
 
-    // ---- the group's q rows: quantise row g (lanes of one group share it) straight
-    // into the B fragments; k-step 4h + j covers dims 64h + 16t + 4j + {0..3}
-    uint32_t qb[D / 16][2];
-    float qsa = 0.0f, qsb = 0.0f;  // dequantisation factors (log2 units) of query columns 2t, 2t+1
-    const uint32_t qs = nq % kQSlots;
-    ok = warp_wait(&q_full[qs], (nq / kQSlots) & 1, limit_ns, st, 43);
-    ++nq;
-    if (ok) {
-      const uint8_t* qrow = smem + C::kQ + qs * C::kQBytes + g * D * q_elem;
-      float qv[D / 64][16];
-      float amax = 0.0f;
+    // ---- the group's q rows: warp r quantises row r into shared memory
+    {
+      const uint32_t qs = nq % kQSlots;
+      ok = warp_wait(&q_full[qs], (nq / kQSlots) & 1, limit_ns, st, 43);
+      ++nq;
+      if (ok && cw < G) {
+        const uint8_t* raw = smem + C::kQ + qs * C::kQBytes + cw * D * q_elem;
+        float v[D / 32];
+        int8_t code[D / 32];
 #pragma unroll
-      for (int h = 0; h < D / 64; ++h) {
-        if (g < G) {
-          load_q16(qrow, a.q_dtype, 64 * h + 16 * t, qv[h]);
-        } else {
+        for (int e = 0; e < D / 32; ++e) {
+          const int idx = lane * (D / 32) + e;
+          v[e] = a.q_dtype == SL8_F32 ? reinterpret_cast<const float*>(raw)[idx]
+               : a.q_dtype == SL8_BF16 ? bf16_bits(reinterpret_cast<const uint16_t*>(raw)[idx])
+                                       : f16_bits(reinterpret_cast<const uint16_t*>(raw)[idx]);
+        }
+        const float sc = quant_row_warp<D>(v, code);
+        int csum = 0;
 #pragma unroll
-          for (int e = 0; e < 16; ++e) qv[h][e] = 0.0f;
+        for (int e = 0; e < D / 32; ++e) {
+          qcodes[cw * D + lane * (D / 32) + e] = code[e];
+          csum += code[e];
         }
 #pragma unroll
-        for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(qv[h][e]));
+        for (int o = 16; o > 0; o >>= 1) csum += __shfl_xor_sync(0xffffffffu, csum, o);
+        if (lane == 0) {
+          qinfo[cw] = sc;
+          qinfo[8 + cw] = static_cast<float>(csum);
+        }
+        if (a.q_codes && s.split == 0) {
+#pragma unroll
+          for (int e = 0; e < D / 32; ++e) a.q_codes[(part_row0 + cw) * D + lane * (D / 32) + e] = code[e];
+          if (lane == 0) a.q_scales[part_row0 + cw] = sc;
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&q_empty[qs]);
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-      const float sc = __fdiv_rn(amax, 127.0f);
-      const bool export_q = a.q_codes && s.split == 0 && cw == 0 && g < G;
-#pragma unroll
-      for (int h = 0; h < D / 64; ++h) {
-        int c[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          c[e] = 0;
-          if (sc != 0.0f) {
-            c[e] = __float2int_rn(__fdiv_rn(qv[h][e], sc));
-            c[e] = c[e] > 127 ? 127 : (c[e] < -127 ? -127 : c[e]);
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          qb[4 * h + j][0] = f16x2_of(static_cast<float>(c[4 * j]), static_cast<float>(c[4 * j + 1]));
-          qb[4 * h + j][1] = f16x2_of(static_cast<float>(c[4 * j + 2]), static_cast<float>(c[4 * j + 3]));
-        }
-        if (export_q) {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) a.q_codes[(part_row0 + g) * D + 64 * h + 16 * t + e] = static_cast<int8_t>(c[e]);
-        }
-      }
-      if (export_q && t == 0) a.q_scales[part_row0 + g] = sc;
-      const float qf = sc * log2e_over_sqrtd;
-      qsa = __shfl_sync(0xffffffffu, qf, 8 * t);
-      qsb = __shfl_sync(0xffffffffu, qf, 8 * t + 4);
+      compute_sync();
     }
+    // B fragments of Q^T: k-step 4h + j holds dims 64h + 16t + 4j + {0, 1} | {2, 3} of
+    // query row g (exact fp16 integers); zero rows past G
+    uint32_t qb[D / 16][2];
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h) {
+      uint4 w = make_uint4(0u, 0u, 0u, 0u);
+      if (g < G) w = *reinterpret_cast<const uint4*>(qcodes + g * D + 64 * h + 16 * t);
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t u = ww[j] ^ 0x80808080u;
+        qb[4 * h + j][0] = g < G ? codes_f16x2(u, 0x4140) : 0u;
+        qb[4 * h + j][1] = g < G ? codes_f16x2(u, 0x4342) : 0u;
+      }
+    }
+    // query columns qa = 2t, qb = 2t + 1: dequantisation factors (log2 units) and the
+    // offset of the biased K codes, -128 * sum(q codes)
+    const float qsa = 2 * t < G ? qinfo[2 * t] * log2e_over_sqrtd : 0.0f;
+    const float qsb = 2 * t + 1 < G ? qinfo[2 * t + 1] * log2e_over_sqrtd : 0.0f;
+    const float offa = 2 * t < G ? -128.0f * qinfo[8 + 2 * t] : 0.0f;
+    const float offb = 2 * t + 1 < G ? -128.0f * qinfo[8 + 2 * t + 1] : 0.0f;
 
-    // ---- per-warp online softmax state for query columns qa = 2t, qb = 2t + 1
+    // ---- per-warp online softmax state for the two query columns
     float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.0f, l_b = 0.0f;
-    int E = -126;                    // P' carries s_v * 2^-E
-    float vlim = pow2i(-126), inv = __uint_as_float(253u << 23);  // 2^E, 2^-E
-    float o[D / 16][4];
+    float tha = -INFINITY, thb = -INFINITY;  // m + lazy headroom
+    int E = -126;                            // P' carries s_v * 2^-E
+    float vlim = pow2i(-126), inv = pow2i(126);
+    float o[D / 16][4], osum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int j = 0; j < D / 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.0f;
 
@@ -428,30 +430,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
         break;
       }
-      const int nv = n - kUnit * cw;  // valid tokens of this warp's unit
-      if (nv > 0) {
-        const int u0 = kUnit * cw;
+      const int nv = n - u0;  // valid tokens of this warp's unit
+      auto unit = [&](auto full_tag) {
+        constexpr bool kFull = decltype(full_tag)::value;
         const uint8_t* sk = base + C::kSK;
         const uint8_t* sv = base + C::kSV;
         const float* sks = reinterpret_cast<const float*>(base + C::kSKs);
         const float* svs = reinterpret_cast<const float*>(base + C::kSVs);
-        const int rA = u0 + pi, rB = rA + 8;
-        // ---- S^T = K . Q^T (two accumulation chains)
+        // ---- S'^T = K_biased . Q^T: K codes + 128 enter as fp16 subnormals (u * 2^-24), so
+        // S = 2^24 S' - 128 sum(q) exactly (two accumulation chains)
         float s0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {
-          const uint4 wa = *reinterpret_cast<const uint4*>(sk + tile_off<D>(rA, 4 * h + t));
-          const uint4 wb = *reinterpret_cast<const uint4*>(sk + tile_off<D>(rB, 4 * h + t));
+          const uint4 wa = *reinterpret_cast<const uint4*>(sk + offk[h][0]);
+          const uint4 wb = *reinterpret_cast<const uint4*>(sk + offk[h][1]);
           const uint32_t A[4] = {wa.x, wa.y, wa.z, wa.w}, Bw[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint32_t ua = A[j] ^ 0x80808080u, ub = Bw[j] ^ 0x80808080u;
-            mma_f16(j & 1 ? s1 : s0, codes_f16x2(ua, 0x4140), codes_f16x2(ub, 0x4140), codes_f16x2(ua, 0x4342),
-                    codes_f16x2(ub, 0x4342), qb[4 * h + j][0], qb[4 * h + j][1]);
+            mma_f16(j & 1 ? s1 : s0, prmt(ua, 0u, 0x4140), prmt(ub, 0u, 0x4140), prmt(ua, 0u, 0x4342),
+                    prmt(ub, 0u, 0x4342), qb[4 * h + j][0], qb[4 * h + j][1]);
           }
         }
-        const float d00 = s0[0] + s1[0], d01 = s0[1] + s1[1], d10 = s0[2] + s1[2], d11 = s0[3] + s1[3];
-        const bool vA = pi < nv, vB = pi + 8 < nv;
+        constexpr float k2p24 = 16777216.0f;
+        const float d00 = fmaf(s0[0] + s1[0], k2p24, offa), d01 = fmaf(s0[1] + s1[1], k2p24, offb);
+        const float d10 = fmaf(s0[2] + s1[2], k2p24, offa), d11 = fmaf(s0[3] + s1[3], k2p24, offb);
+        const int rA = u0 + pi, rB = rA + 8;
+        const bool vA = kFull || pi < nv, vB = kFull || pi + 8 < nv;
         if (a.logits) {
           int32_t* lg = a.logits + c0;
           if (2 * t < G) {
@@ -466,24 +471,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- online softmax (log2 units), lazily rescaled
         const float ksA = vA ? sks[rA] : 0.0f, ksB = vB ? sks[rB] : 0.0f;
         const float vsA = vA ? svs[rA] : 0.0f, vsB = vB ? svs[rB] : 0.0f;
-        const float xa0 = vA ? d00 * ksA * qsa : -INFINITY, xa1 = vA ? d01 * ksA * qsb : -INFINITY;
-        const float xb0 = vB ? d10 * ksB * qsa : -INFINITY, xb1 = vB ? d11 * ksB * qsb : -INFINITY;
-        const float ma = col_max(fmaxf(xa0, xb0)), mb = col_max(fmaxf(xa1, xb1));
-        const float vm = col_max(fmaxf(vsA, vsB));
-        const bool grow_a = ma > m_a + kLazy, grow_b = mb > m_b + kLazy, grow_v = vm > vlim;
-        if (__any_sync(0xffffffffu, grow_a || grow_b || grow_v)) {
+        const float ka = ksA * qsa, kb = ksA * qsb, kc = ksB * qsa, kd = ksB * qsb;
+        const float xa0 = vA ? d00 * ka : -INFINITY, xa1 = vA ? d01 * kb : -INFINITY;
+        const float xb0 = vB ? d10 * kc : -INFINITY, xb1 = vB ? d11 * kd : -INFINITY;
+        const bool grow = (fmaxf(xa0, xb0) > tha) || (fmaxf(xa1, xb1) > thb) || (fmaxf(vsA, vsB) > vlim);
+        if (__any_sync(0xffffffffu, grow)) {
+          const float ma = col_max(fmaxf(xa0, xb0)), mb = col_max(fmaxf(xa1, xb1));
+          const float vm = col_max(fmaxf(vsA, vsB));
           float fa = 1.0f, fb = 1.0f;
-          if (grow_a) {
+          if (ma > tha) {
             fa = m_a == -INFINITY ? 0.0f : ex2(m_a - ma);
             l_a *= fa;
             m_a = ma;
+            tha = ma + kLazy;
           }
-          if (grow_b) {
+          if (mb > thb) {
             fb = m_b == -INFINITY ? 0.0f : ex2(m_b - mb);
             l_b *= fb;
             m_b = mb;
+            thb = mb + kLazy;
           }
-          if (grow_v) {  // uniform: vm is the unit's max over all lanes
+          if (vm > vlim) {  // uniform: vm is the unit's max over all lanes
             int e = static_cast<int>((__float_as_uint(vm) >> 23) & 0xffu) - 126;  // vm < 2^e
             e = e > 126 ? 126 : e;
             const float fe = pow2i(E - e);
@@ -500,49 +508,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             o[j][1] *= fb;
             o[j][3] *= fb;
           }
+          osum[0] *= fa;
+          osum[2] *= fa;
+          osum[1] *= fb;
+          osum[3] *= fb;
         }
         const float pa0 = ex2(xa0 - m_a), pa1 = ex2(xa1 - m_b), pb0 = ex2(xb0 - m_a), pb1 = ex2(xb1 - m_b);
         l_a += pa0 + pb0;
         l_b += pa1 + pb1;
         const float wA = vsA * inv, wB = vsB * inv;
-        // ---- P'^T into the B-fragment order: pair u < 4 holds tokens (u, u + 4), pair
-        // 4 + u holds (u + 8, u + 12); this lane's tokens are pi and pi + 8
+        // ---- P'^T in B-fragment order: pair tau holds tokens (tau, tau + 8) of one query
         __syncwarp();
-        {
-          const int pr = pi & 3, hf = pi >> 2;
-          const __half h_a0 = __float2half_rn(pa0 * wA), h_a1 = __float2half_rn(pa1 * wA);
-          const __half h_b0 = __float2half_rn(pb0 * wB), h_b1 = __float2half_rn(pb1 * wB);
-          pw[((2 * t) * 8 + pr) * 2 + hf] = __half_as_ushort(h_a0);
-          pw[((2 * t + 1) * 8 + pr) * 2 + hf] = __half_as_ushort(h_a1);
-          pw[((2 * t) * 8 + 4 + pr) * 2 + hf] = __half_as_ushort(h_b0);
-          pw[((2 * t + 1) * 8 + 4 + pr) * 2 + hf] = __half_as_ushort(h_b1);
-        }
+        pw[(2 * t) * 8 + pi] = f16x2_of(pa0 * wA, pb0 * wB);
+        pw[(2 * t + 1) * 8 + pi] = f16x2_of(pa1 * wA, pb1 * wB);
         __syncwarp();
-        const uint32_t pb0r = pw32[g * 8 + t], pb1r = pw32[g * 8 + 4 + t];
-        // ---- O^T += V^T . P'^T; V rows u0 + t + 4c (c = 0..3) are the k columns
-        // 2t, 2t + 1, 2t + 8, 2t + 9
+        const uint32_t pb0r = pw[g * 8 + t], pb1r = pw[g * 8 + 4 + t];
+        // ---- O'^T += V_biased^T . P'^T (V codes + 128 as fp16 subnormals), and the row
+        // sums of P' from an all-ones A for the offset
         if constexpr (D == 64) {
           uint2 w[4];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint2*>(sv + (u0 + t + 4 * c) * 64 + 8 * cg);
+          for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint2*>(sv + offv[0][c]);
 #pragma unroll
           for (int ii = 0; ii < 2; ++ii) {
             const uint32_t w0 = ii ? w[0].y : w[0].x, w1 = ii ? w[1].y : w[1].x;
             const uint32_t w2 = ii ? w[2].y : w[2].x, w3 = ii ? w[3].y : w[3].x;
             const uint32_t x01 = prmt(w0, w1, 0x5140) ^ 0x80808080u, y01 = prmt(w0, w1, 0x7362) ^ 0x80808080u;
             const uint32_t x23 = prmt(w2, w3, 0x5140) ^ 0x80808080u, y23 = prmt(w2, w3, 0x7362) ^ 0x80808080u;
-            mma_f16(o[2 * ii], codes_f16x2(x01, 0x4140), codes_f16x2(x01, 0x4342), codes_f16x2(x23, 0x4140),
-                    codes_f16x2(x23, 0x4342), pb0r, pb1r);
-            mma_f16(o[2 * ii + 1], codes_f16x2(y01, 0x4140), codes_f16x2(y01, 0x4342), codes_f16x2(y23, 0x4140),
-                    codes_f16x2(y23, 0x4342), pb0r, pb1r);
+            mma_f16(o[2 * ii], prmt(x01, 0u, 0x4140), prmt(x01, 0u, 0x4342), prmt(x23, 0u, 0x4140),
+                    prmt(x23, 0u, 0x4342), pb0r, pb1r);
+            mma_f16(o[2 * ii + 1], prmt(y01, 0u, 0x4140), prmt(y01, 0u, 0x4342), prmt(y23, 0u, 0x4140),
+                    prmt(y23, 0u, 0x4342), pb0r, pb1r);
           }
         } else {
 #pragma unroll
           for (int b = 0; b < C::kBoxes; ++b) {
             uint4 w[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-              w[c] = *reinterpret_cast<const uint4*>(sv + tile_off<D>(u0 + t + 4 * c, 8 * b + cg));
+            for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint4*>(sv + offv[b][c]);
 #pragma unroll
             for (int ii = 0; ii < 4; ++ii) {
               const uint32_t w0 = ii == 0 ? w[0].x : ii == 1 ? w[0].y : ii == 2 ? w[0].z : w[0].w;
@@ -551,20 +554,22 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t w3 = ii == 0 ? w[3].x : ii == 1 ? w[3].y : ii == 2 ? w[3].z : w[3].w;
               const uint32_t x01 = prmt(w0, w1, 0x5140) ^ 0x80808080u, y01 = prmt(w0, w1, 0x7362) ^ 0x80808080u;
               const uint32_t x23 = prmt(w2, w3, 0x5140) ^ 0x80808080u, y23 = prmt(w2, w3, 0x7362) ^ 0x80808080u;
-              mma_f16(o[8 * b + 2 * ii], codes_f16x2(x01, 0x4140), codes_f16x2(x01, 0x4342),
-                      codes_f16x2(x23, 0x4140), codes_f16x2(x23, 0x4342), pb0r, pb1r);
-              mma_f16(o[8 * b + 2 * ii + 1], codes_f16x2(y01, 0x4140), codes_f16x2(y01, 0x4342),
-                      codes_f16x2(y23, 0x4140), codes_f16x2(y23, 0x4342), pb0r, pb1r);
+              mma_f16(o[8 * b + 2 * ii], prmt(x01, 0u, 0x4140), prmt(x01, 0u, 0x4342), prmt(x23, 0u, 0x4140),
+                      prmt(x23, 0u, 0x4342), pb0r, pb1r);
+              mma_f16(o[8 * b + 2 * ii + 1], prmt(y01, 0u, 0x4140), prmt(y01, 0u, 0x4342),
+                      prmt(y23, 0u, 0x4140), prmt(y23, 0u, 0x4342), pb0r, pb1r);
             }
           }
         }
+        mma_f16(osum, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, pb0r, pb1r);
+      };
+      if (nv >= kUnit) {
+        unit(std::true_type{});
+      } else if (nv > 0) {
+        unit(std::false_type{});
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[stg]);  // 8 arrivals (one per compute warp) free the stage
-    }
-    if (!compute_all(ok)) {
-      ok = false;
-      break;
     }
     // ---- merge the eight warps' states of this split
     l_a = col_sum(l_a);
@@ -576,7 +581,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       sa[4] = m_b;
       sa[5] = l_b;
     }
-    compute_sync();
+    if (!compute_all(ok)) {
+      ok = false;
+      break;
+    }
     float Ma = -INFINITY, Mb = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kComputeWarps; ++w) {
@@ -590,9 +598,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (sa[0] != -INFINITY) La += sa[1] * ex2(sa[0] - Ma);
       if (sa[4] != -INFINITY) Lb += sa[5] * ex2(sa[4] - Mb);
     }
+    // O = (2^24 O' - 128 rowsum(P')) * 2^E * 2^(m - M) / L
     const float pe = pow2i(E);
     const float fa = m_a == -INFINITY ? 0.0f : ex2(m_a - Ma) * pe / La;
     const float fb = m_b == -INFINITY ? 0.0f : ex2(m_b - Mb) * pe / Lb;
+    constexpr float k2p24 = 16777216.0f;
+    const float ca = -128.0f * osum[0], cb = -128.0f * osum[1];
 #pragma unroll
     for (int j = 0; j < D / 16; ++j) {
       // physical dims of rows g and g + 8 of m-tile j
@@ -602,8 +613,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         dim = 128 * (j >> 3) + 16 * cg + 4 * ((j & 7) >> 1) + 2 * (j & 1);
       }
-      *reinterpret_cast<float2*>(red + (cw * D + dim) * 8 + 2 * t) = make_float2(o[j][0] * fa, o[j][1] * fb);
-      *reinterpret_cast<float2*>(red + (cw * D + dim + 1) * 8 + 2 * t) = make_float2(o[j][2] * fa, o[j][3] * fb);
+      *reinterpret_cast<float2*>(red + (cw * D + dim) * 8 + 2 * t) =
+          make_float2(fmaf(o[j][0], k2p24, ca) * fa, fmaf(o[j][1], k2p24, cb) * fb);
+      *reinterpret_cast<float2*>(red + (cw * D + dim + 1) * 8 + 2 * t) =
+          make_float2(fmaf(o[j][2], k2p24, ca) * fa, fmaf(o[j][3], k2p24, cb) * fb);
     }
     if (cw == 0 && g == 0) {
       if (2 * t < G)
@@ -612,6 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         a.lse_partial[(part_row0 + 2 * t + 1) * a.num_splits + s.split] = (Mb + log2f(Lb)) * 0.6931471805599453f;
     }
     compute_sync();
+    // every shared buffer read below is rewritten only after the next split's q barrier
     for (int idx = ct; idx < D * 8; idx += kComputeThreads) {
       const int q = idx & 7, dim = idx >> 3;
       if (q >= G) continue;
@@ -620,7 +634,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int w = 0; w < kComputeWarps; ++w) acc += red[(w * D + dim) * 8 + q];
       a.o_partial[((part_row0 + q) * a.num_splits + s.split) * D + dim] = acc;
     }
-    compute_sync();
   }
 }
 
