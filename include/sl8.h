@@ -64,6 +64,10 @@ typedef enum sl8_dtype { SL8_F16 = 0, SL8_BF16 = 1, SL8_F32 = 2, SL8_I8 = 3 } sl
 /* Human-readable name of a status code (static string). */
 SL8_API const char* sl8_status_string(int status);
 
+/* Text of the CUDA error behind the calling thread's most recent SL8_ERR_CUDA from a
+ * launch (a static string; "no CUDA error recorded" if there was none). */
+SL8_API const char* sl8_last_cuda_error_string(void);
+
 /* Library version, as major * 10000 + minor * 100 + patch. */
 SL8_API int sl8_version(void);
 
@@ -189,7 +193,7 @@ SL8_API int sl8_attn_decode_combine(const float* o_partial, const float* lse_par
  * S = sl8_attn_decode_num_splits(B, Hkv, Lmax, d, 0)).
  *   logits_out  device, [B][Hq][Lmax] int32: entry t < L_b is int32(q_i8 . k_i8[t]);
  *               entries t >= L_b are left untouched.
- *   q_codes/q_scales  device, nullable, [B][Hq][d] int8 / [B][Hq] fp32.
+ *   q_codes/q_scales  device, nullable, [B][Hq][d] int8 (4-byte aligned) / [B][Hq] fp32.
  *   o_partial/lse_partial  scratch as for the split call.
  */
 SL8_API int sl8_attn_int8_decode_logits_debug(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale,

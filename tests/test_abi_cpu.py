@@ -56,19 +56,22 @@ def test_workspace_sizes(lib):
 
 
 def test_decode_split_plan(lib):
-    # explicit requests: split size = ceil(Lmax / n) rounded up to whole 128-token stages
-    # (16 tokens below one stage)
+    # The decode kernel streams the cache in stages of 160 tokens for d = 128 (ten
+    # compute warps x 16 tokens).  Explicit requests: split size = ceil(Lmax / n) rounded
+    # up to whole stages (to 16 tokens below one stage).
+    stage = 160
     assert lib.sl8_attn_decode_num_splits(64, 8, 8192, 128, 5) == 5
-    assert lib.sl8_attn_decode_split_size(64, 8, 8192, 128, 5) == 1664
-    assert lib.sl8_attn_decode_split_size(2, 2, 600, 128, 3) == 256
+    assert lib.sl8_attn_decode_split_size(64, 8, 8192, 128, 5) == 1760
+    assert lib.sl8_attn_decode_split_size(2, 2, 600, 128, 4) == 160
+    assert lib.sl8_attn_decode_num_splits(2, 2, 600, 128, 3) == 2       # 200 -> 320 tokens
     assert lib.sl8_attn_decode_split_size(2, 2, 300, 128, 3) == 112
     assert lib.sl8_attn_decode_num_splits(64, 8, 8192, 128, 1) == 1
     assert lib.sl8_attn_decode_num_splits(1, 1, 10, 128, 64) == 1       # one 16-token split
     assert lib.sl8_attn_decode_num_splits(64, 8, 100, 32, 0) == 0       # unsupported head dim
     assert lib.sl8_attn_decode_num_splits(0, 8, 100, 128, 0) == 0
-    # every plan: 16-token aligned splits (whole stages from 128 tokens up), all non-empty
-    # at Lmax, covering Lmax, and the
-    # combine's split size (from Lmax and S alone) is the split kernel's
+    # every plan: 16-token aligned splits (whole stages from one stage up), all non-empty
+    # at Lmax, covering Lmax, and the combine's split size (from Lmax and S alone) is the
+    # split kernel's
     for B, Hkv in ((1, 1), (64, 8), (3, 2)):
         for lmax in range(1, 3000, 37):
             for n in (0, 1, 3, 40, 500):
@@ -76,10 +79,10 @@ def test_decode_split_plan(lib):
                 ss = lib.sl8_attn_decode_split_size(B, Hkv, lmax, 128, n)
                 assert S >= 1 and ss % 16 == 0 and ss * S >= lmax and (S - 1) * ss < lmax
                 per = -(-lmax // S)
-                step = 128 if per >= 128 else 16
+                step = stage if per >= stage else 16
                 assert ss == (per + step - 1) // step * step
                 if n == 0:
-                    assert S <= -(-lmax // 128)
+                    assert S <= -(-lmax // stage)
 
 
 def _host_buf(nbytes):

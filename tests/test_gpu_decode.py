@@ -102,10 +102,10 @@ def test_decode_partials_match_oracle_splits():
     lens_np, g, gs, o, os_ = build_cache(w, 600)
     q = W.decode_query(w)
     seq = torch.from_numpy(lens_np.astype(np.int32)).to(DEV)
-    op, lp = sl8.attn_int8_decode_splitkv(q.to(DEV), g["k"], gs["k"], g["v"], gs["v"], seq, num_splits=3)
+    op, lp = sl8.attn_int8_decode_splitkv(q.to(DEV), g["k"], gs["k"], g["v"], gs["v"], seq, num_splits=4)
     torch.cuda.synchronize()
-    split_size = sl8.lib().sl8_attn_decode_split_size(2, 2, 600, 128, 3)   # 200 -> 256: whole stages
-    assert split_size == 256 and op.shape[2] == 3
+    split_size = sl8.lib().sl8_attn_decode_split_size(2, 2, 600, 128, 4)   # one 160-token stage
+    assert split_size == 160 and op.shape[2] == 4
     ref = oracle.attn_decode(q.float().numpy(), o["k"], os_["k"], o["v"], os_["v"], lens_np, split_size=split_size)
     lpn = to_np32(lp)
     live = np.isfinite(ref["lse_partial"])

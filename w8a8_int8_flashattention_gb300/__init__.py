@@ -38,7 +38,13 @@ _TORCH_DTYPES = {v: k for k, v in _DTYPES.items()}
 class SL8Error(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        msg = f"{what}: {status_string(status)} (status {status})"
+        if status == SL8_ERR_CUDA:
+            try:
+                msg += ": " + lib().sl8_last_cuda_error_string().decode()
+            except Exception:  # noqa: BLE001 - used while formatting another error
+                pass
+        super().__init__(msg)
 
 
 _lock = threading.Lock()
@@ -53,6 +59,7 @@ _U64 = ctypes.c_uint64
 
 _SIGNATURES = {
     "sl8_status_string": (ctypes.c_char_p, [_INT]),
+    "sl8_last_cuda_error_string": (ctypes.c_char_p, []),
     "sl8_version": (_INT, []),
     "sl8_quant_rowwise": (_INT, [_P, _INT, _I64, _I32, _I64, _P, _I64, _P, _P, _P]),
     "sl8_k_channel_mean_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),

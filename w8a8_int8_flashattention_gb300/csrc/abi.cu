@@ -206,10 +206,15 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? SL8_OK : SL8_ERR_CUDA
     if (!(cond)) return (code); \
   } while (0)
 
+// The CUDA error behind the calling thread's last SL8_ERR_CUDA.
+static thread_local cudaError_t g_last_cuda_error = cudaSuccess;
 #define SL8_LAUNCH(expr)                     \
   do {                                       \
     cudaError_t e_ = (expr);                 \
-    if (e_ != cudaSuccess) return SL8_ERR_CUDA; \
+    if (e_ != cudaSuccess) {                 \
+      g_last_cuda_error = e_;                \
+      return SL8_ERR_CUDA;                   \
+    }                                        \
   } while (0)
 
 int validate_prefill(const void* q, const void* k, int qk_dtype, int32_t B, int32_t Hq, int32_t Hkv, int32_t N,
@@ -242,6 +247,10 @@ const char* sl8_status_string(int status) {
 }
 
 int sl8_version(void) { return 100; }
+
+const char* sl8_last_cuda_error_string(void) {
+  return g_last_cuda_error == cudaSuccess ? "no CUDA error recorded" : cudaGetErrorString(g_last_cuda_error);
+}
 
 int sl8_quant_rowwise(const void* x, int x_dtype, int64_t rows, int32_t cols, int64_t row_stride_elems,
                       const float* sub_mean, int64_t rows_per_group, int8_t* q_out, float* scale_out, void* stream) {
@@ -432,16 +441,17 @@ int sl8_attn_int8_qk_logits_debug(const void* q, const void* k, int qk_dtype, in
   return SL8_OK;
 }
 
-// The split plan.  split_size_for(Lmax, S) = ceil(Lmax / S) rounded up to a whole number
-// of the decode kernel's 128-token stages (to 16 tokens below one stage): every stage of
-// the cache then starts on a 16-byte boundary of the scale rows, and only a sequence's
-// last split ends in a partial stage.  A request n (0: about 16 work slots per SM over
-// the B x Hkv pairs, at most one per stage) becomes S = ceil(Lmax /
-// split_size_for(Lmax, n)) splits; the split kernel and the combine both use
-// split_size_for(Lmax, S).
-static int32_t split_size_for(int32_t Lmax, int32_t S) {
+// The split plan.  split_size_for(Lmax, S, d) = ceil(Lmax / S) rounded up to a whole
+// number of the decode kernel's stages (decode_chunk_tokens(d) tokens; to 16 tokens below
+// one stage): every stage of the cache then starts on a 16-byte boundary of the scale
+// rows, and only a sequence's last split ends in a partial stage.  A request n (0: about
+// 24 work slots per SM over the B x Hkv pairs, at most one per stage) becomes
+// S = ceil(Lmax / split_size_for(Lmax, n, d)) splits; the split kernel and the combine
+// both use split_size_for(Lmax, S, d).
+static int32_t split_size_for(int32_t Lmax, int32_t S, int32_t d) {
   const int32_t per = (Lmax + S - 1) / S;
-  const int32_t step = per >= 128 ? 128 : 16;
+  const int32_t chunk = decode_chunk_tokens(d);
+  const int32_t step = per >= chunk ? chunk : 16;
   return (per + step - 1) / step * step;
 }
 
@@ -450,20 +460,20 @@ int32_t sl8_attn_decode_num_splits(int32_t B, int32_t Hkv, int32_t Lmax, int32_t
   int64_t n = num_splits;
   if (n == 0) {
     const int64_t pairs = static_cast<int64_t>(B) * Hkv;
-    n = (16ll * num_sms() + pairs - 1) / pairs;
+    n = (24ll * num_sms() + pairs - 1) / pairs;
     const int64_t chunks = (Lmax + decode_chunk_tokens(d) - 1) / decode_chunk_tokens(d);
     if (n > chunks) n = chunks;
   }
   const int64_t cap = (Lmax + 15) / 16;
   if (n > cap) n = cap;
   if (n < 1) n = 1;
-  const int32_t ss = split_size_for(Lmax, static_cast<int32_t>(n));
+  const int32_t ss = split_size_for(Lmax, static_cast<int32_t>(n), d);
   return (Lmax + ss - 1) / ss;
 }
 
 int32_t sl8_attn_decode_split_size(int32_t B, int32_t Hkv, int32_t Lmax, int32_t d, int32_t num_splits) {
   const int32_t S = sl8_attn_decode_num_splits(B, Hkv, Lmax, d, num_splits);
-  return S > 0 ? split_size_for(Lmax, S) : 0;
+  return S > 0 ? split_size_for(Lmax, S, d) : 0;
 }
 
 static int decode_validate(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale,
@@ -532,7 +542,7 @@ int sl8_attn_decode_combine(const float* o_partial, const float* lse_partial, co
   SL8_CHECK(head_dim_ok(d), SL8_ERR_UNSUPPORTED);
   if (B == 0) return SL8_OK;
   SL8_CHECK(num_splits <= (Lmax > 0 ? Lmax : 1), SL8_ERR_INVALID_ARG);
-  const int32_t split_size = Lmax > 0 ? split_size_for(Lmax, num_splits) : 16;
+  const int32_t split_size = Lmax > 0 ? split_size_for(Lmax, num_splits, d) : 16;
   SL8_LAUNCH(launch_decode_combine(o_partial, lse_partial, seqlens, B, Hq, d, num_splits, split_size, out,
                                    static_cast<sl8_dtype>(out_dtype), lse_out, static_cast<cudaStream_t>(stream)));
   return SL8_OK;
@@ -545,6 +555,7 @@ int sl8_attn_int8_decode_logits_debug(const void* q, int q_dtype, const int8_t* 
                                       float* lse_partial, void* stream) {
   SL8_CHECK(logits_out, SL8_ERR_INVALID_ARG);
   SL8_CHECK(!q_codes == !q_scales, SL8_ERR_INVALID_ARG);
+  SL8_CHECK((reinterpret_cast<uintptr_t>(q_codes) & 3u) == 0, SL8_ERR_INVALID_ARG);  // written in 4-byte words
   return decode_launch(q, q_dtype, k_cache, k_scale, v_cache, v_scale, seqlens, B, Hq, Hkv, Lmax, d, 0, o_partial,
                        lse_partial, logits_out, q_codes, q_scales, stream);
 }

@@ -15,12 +15,14 @@
 //
 // GB300 design.  The kernel streams the cache once, so HBM is the bound; the work
 // per byte must stay small enough that eight warps per SM keep up with it.
-//  * A persistent CTA per SM walks the (split, b, kv head) work slots.  Warp 0 loads
-//    each split's K and V codes with tiled TMA copies (128-byte swizzle for d >= 128)
-//    in 128-token stages, with their scales and the group's q rows, into a shared-
-//    memory ring that runs ahead across splits.
+//  * A persistent CTA per SM walks a balanced list of (b, kv head, split) work slots.
+//    Warp 0 loads each split's K and V codes with tiled TMA copies (128-byte swizzle
+//    for d >= 128) in 128-token stages, with their scales and the group's q rows,
+//    into shared-memory rings that run ahead across splits.
 //  * Each of the eight compute warps takes 16 tokens of every stage and keeps its own
-//    online-softmax state; the warps' states are merged once per split.
+//    online-softmax state.  Warp 1 quantises the next split's q rows while they work
+//    and merges the eight warps' states of the previous split, so the compute warps
+//    never meet at a CTA barrier.
 //  * Both contractions run on the tensor cores as m16n8k16 fp16 MMAs with fp32
 //    accumulation (the int8 tensor rate of this part is low).  Codes become fp16
 //    exactly (|c| <= 127), so q.k is the exact integer dot (|sum| < 2^24).
@@ -42,34 +44,49 @@ namespace sl8 {
 
 namespace {
 
-constexpr int kComputeWarps = 8;
-constexpr int kComputeThreads = kComputeWarps * 32;
-constexpr int kThreads = kComputeThreads + 32;  // + the producer warp
+constexpr int kFirstCompute = 2;                // warp 0: loads, warp 1: merges
 constexpr int kUnit = 16;                       // tokens per compute warp per stage
-constexpr int kChunk = kComputeWarps * kUnit;   // tokens per stage
 constexpr int kQSlots = 2;                      // q-row buffers (one per split in flight)
 constexpr float kLazy = 8.0f;                   // log2 headroom of the lazy max
 
+constexpr int kSchedMaxB = 512;
+struct Sched {
+  int32_t len[kSchedMaxB];       // sequence lengths clamped to [0, Lmax]
+  int32_t pf[kSchedMaxB + 1];    // prefix over b of the full slots (full splits x Hkv)
+  uint32_t key[kSchedMaxB];      // sorted: (split_size - tail) << 16 | b, then 0xffffffff
+  int32_t n_full, n_tail;        // slots of each kind
+};
+static_assert(kSchedMaxB <= 65536, "b fits the key");
+
 template <int D>
 struct DCfg {
+  // ten compute warps (eight for d = 256, whose tiles and merge buffer are twice as
+  // large); registers are granted to the CTA in steps of four warps, so the loader and
+  // merging warps come free with them
+  static constexpr int kNW = D == 256 ? 8 : 10;
+  static constexpr int kCT = kNW * 32;
+  static constexpr int kThreads = kCT + 32 * kFirstCompute;
+  static constexpr int kChunk = kNW * kUnit;     // tokens per stage
   static constexpr int kBW = D < 128 ? D : 128;  // bytes in one row of a TMA box
   static constexpr int kBoxes = D / kBW;
   static constexpr bool kSwz = D >= 128;         // 128-byte swizzled tiles
   static constexpr int kTile = kChunk * D;       // one stage of K (or V) codes
-  static constexpr int kStages = D == 64 ? 8 : (D == 128 ? 5 : 2);
+  static constexpr int kStages = D == 64 ? 8 : (D == 128 ? 3 : 2);
   static constexpr int kSK = 0;
   static constexpr int kSV = kTile;
   static constexpr int kSKs = 2 * kTile;
   static constexpr int kSVs = kSKs + kChunk * 4;
-  static constexpr int kStageBytes = kSVs + kChunk * 4;
+  static constexpr int kStageBytes = (kSVs + kChunk * 4 + 1023) / 1024 * 1024;
   static constexpr int kQBytes = 8 * D * 4;                    // 8 raw q rows, fp32 at most
-  static constexpr int kQ = kStages * kStageBytes;
+  static constexpr int kQ = kStages * kStageBytes;             // [2] raw q rows
   static constexpr int kRed = kQ + kQSlots * kQBytes;          // [warp][d][8 q] floats
-  static constexpr int kP = kRed + kComputeWarps * D * 8 * 4;  // [warp][8 q][8 token pairs] fp16x2
-  static constexpr int kStat = kP + kComputeWarps * 256;       // [warp][8 q][4] floats
-  static constexpr int kQc = kStat + kComputeWarps * 8 * 16;   // [8][D] q codes, [8] scales, [8] sums
-  static constexpr int kBar = kQc + 8 * D + 64;
-  static constexpr int kNumBars = 2 * kStages + 2 * kQSlots;
+  static constexpr int kP = kRed + kNW * D * 8 * 4;            // [warp][8 q][8 token pairs] fp16x2
+  static constexpr int kStat = kP + kNW * 256;                 // [warp][8 q][4] floats
+  static constexpr int kQcBytes = 8 * D + 64;                  // 8 code rows, 8 scales, 8 code sums
+  static constexpr int kQc = kStat + kNW * 8 * 16;             // [2] quantised q rows
+  static constexpr int kSched = kQc + kQSlots * kQcBytes;      // Sched
+  static constexpr int kBar = (kSched + static_cast<int>(sizeof(Sched)) + 15) / 16 * 16;
+  static constexpr int kNumBars = 2 * kStages + 4 * kQSlots + 2;
   static constexpr int kBytes = kBar + kNumBars * 8 + 1024;    // + alignment slack
   static_assert(kStageBytes % 1024 == 0 && kTile % 1024 == 0, "swizzled tiles need 1024-byte alignment");
   static_assert(kBytes <= 232448, "smem budget");
@@ -82,7 +99,7 @@ __device__ __forceinline__ uint32_t tile_off(int r, int c) {
   using C = DCfg<D>;
   constexpr int cpb = C::kBW / 16;
   const int b = c / cpb, cc = c % cpb;
-  return static_cast<uint32_t>(b * (kChunk * C::kBW) + r * C::kBW + 16 * (C::kSwz ? (cc ^ (r & 7)) : cc));
+  return static_cast<uint32_t>(b * (C::kChunk * C::kBW) + r * C::kBW + 16 * (C::kSwz ? (cc ^ (r & 7)) : cc));
 }
 
 __device__ __forceinline__ float bf16_bits(uint32_t b) { return __uint_as_float(b << 16); }
@@ -104,20 +121,6 @@ __device__ __forceinline__ float col_sum(float a) {
   a += __shfl_xor_sync(0xffffffffu, a, 4);
   a += __shfl_xor_sync(0xffffffffu, a, 8);
   return a + __shfl_xor_sync(0xffffffffu, a, 16);
-}
-// Barrier over the 256 compute threads (named barrier 1).
-__device__ __forceinline__ void compute_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kComputeThreads) : "memory");
-}
-// The same barrier, returning the AND of v over the compute threads.
-__device__ __forceinline__ bool compute_all(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, 1, %2, q;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(v)), "n"(kComputeThreads)
-      : "memory");
-  return r != 0;
 }
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns, DeviceStatus* st,
                                           int site) {
@@ -185,44 +188,163 @@ __device__ __forceinline__ float load_q_elem(const void* base, sl8_dtype dt, int
                        : static_cast<const float*>(base)[idx];
 }
 
-// Work slot -> (split, b, hkv); splits outermost so that every CTA gets a mix of
-// early (always non-empty) and late splits.
+// ---- work schedule
+// A work slot is one (b, kv head, split).  With B <= kSchedMaxB every CTA builds the
+// same balanced schedule in shared memory: the full splits (split_size tokens) are
+// dealt round-robin, then the partial last splits of the sequences, longest first, in
+// snake order starting at the CTA after the last full one; empty splits are handled
+// up front and never scheduled.  Above kSchedMaxB the slots go round-robin in
+// split-major order (empty ones are skipped).
+
 struct Slot {
   int split, b, hkv, t0, t1;
 };
-__device__ __forceinline__ Slot decode_slot(const DecodeArgs& a, int64_t i, DeviceStatus* st, bool report) {
-  Slot s;
-  const int64_t per = static_cast<int64_t>(a.B) * a.Hkv;
-  s.split = static_cast<int>(i / per);
-  const int64_t r = i - s.split * per;
-  s.b = static_cast<int>(r / a.Hkv);
-  s.hkv = static_cast<int>(r - static_cast<int64_t>(s.b) * a.Hkv);
-  int L = a.seqlens[s.b];
+
+__device__ __forceinline__ int clamp_len(const DecodeArgs& a, int b, DeviceStatus* st, bool report) {
+  int L = a.seqlens[b];
   if (L < 0 || L > a.Lmax) {
     if (report) record_status(st, kStatusBadArg, 700);
     L = L < 0 ? 0 : a.Lmax;
   }
+  return L;
+}
+
+// Build the balanced schedule; one warp (the caller syncs the CTA afterwards).
+__device__ void build_sched_warp(const DecodeArgs& a, Sched* sc, DeviceStatus* st) {
+  const int lane = threadIdx.x & 31;
+  int n2 = 32;
+  while (n2 < a.B) n2 <<= 1;
+  // lane owns b = lane * per .. : lengths, tail keys, full-slot counts
+  const int per = (a.B + 31) / 32, b0 = lane * per, b1 = min(b0 + per, a.B);
+  int sum = 0, tails = 0;
+  for (int b = b0; b < b1; ++b) {
+    const int L = clamp_len(a, b, st, blockIdx.x == 0);
+    sc->len[b] = L;
+    const int nf = min(L / a.split_size, a.num_splits);
+    const int tail = L - nf * a.split_size;
+    sc->key[b] = tail > 0 ? (static_cast<uint32_t>(a.split_size - tail) << 16) | static_cast<uint32_t>(b) : 0xffffffffu;
+    sum += nf * a.Hkv;
+    tails += tail > 0;
+  }
+  for (int b = a.B + lane; b < n2; b += 32) sc->key[b] = 0xffffffffu;
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tails += __shfl_xor_sync(0xffffffffu, tails, o);
+  int run = incl - sum;
+  for (int b = b0; b < b1; ++b) {
+    sc->pf[b] = run;
+    run += min(sc->len[b] / a.split_size, a.num_splits) * a.Hkv;
+  }
+  if (lane == 31) {
+    sc->pf[a.B] = incl;
+    sc->n_full = incl;
+  }
+  if (lane == 0) sc->n_tail = tails * a.Hkv;
+  __syncwarp();
+  // bitonic sort of the tail keys, ascending
+  for (int size = 2; size <= n2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = lane; i < n2 / 2; i += 32) {
+        const int lo = (i / stride) * 2 * stride + (i % stride), hi = lo + stride;
+        const uint32_t x = sc->key[lo], y = sc->key[hi];
+        if ((x > y) == ((lo & size) == 0)) {
+          sc->key[lo] = y;
+          sc->key[hi] = x;
+        }
+      }
+      __syncwarp();
+    }
+  }
+}
+
+// Walks this CTA's non-empty slots.
+struct SlotIter {
+  int q = 0;
+  __device__ __forceinline__ bool next(const DecodeArgs& a, const Sched* sc, bool balanced, Slot& s);
+};
+
+// The q-th slot of this CTA; false when it has no more.  In the split-major order a
+// slot can be empty (t0 >= t1); the caller skips it.
+__device__ __forceinline__ bool next_slot(const DecodeArgs& a, const Sched* sc, bool balanced, int q, Slot& s) {
+  const int c = blockIdx.x, grid = gridDim.x;
+  if (!balanced) {
+    const int64_t i = c + static_cast<int64_t>(q) * grid;
+    const int64_t per = static_cast<int64_t>(a.B) * a.Hkv;
+    if (i >= per * a.num_splits) return false;
+    s.split = static_cast<int>(i / per);
+    const int64_t r = i - s.split * per;
+    s.b = static_cast<int>(r / a.Hkv);
+    s.hkv = static_cast<int>(r - static_cast<int64_t>(s.b) * a.Hkv);
+    int L = a.seqlens[s.b];
+    L = L < 0 ? 0 : (L > a.Lmax ? a.Lmax : L);
+    s.t0 = s.split * a.split_size;
+    s.t1 = min(s.t0 + a.split_size, L);
+    return true;
+  }
+  const int F = sc->n_full;
+  const int mine = F > c ? (F - 1 - c) / grid + 1 : 0;
+  if (q < mine) {
+    const int j = c + q * grid;
+    int lo = 0, hi = a.B;  // last b with pf[b] <= j
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (sc->pf[mid] <= j) lo = mid;
+      else hi = mid;
+    }
+    const int r = j - sc->pf[lo];
+    s.b = lo;
+    s.split = r / a.Hkv;
+    s.hkv = r - s.split * a.Hkv;
+    s.t0 = s.split * a.split_size;
+    s.t1 = s.t0 + a.split_size;
+    return true;
+  }
+  const int p = q - mine, pos = ((c - F % grid) % grid + grid) % grid;
+  const int i = p * grid + ((p & 1) ? grid - 1 - pos : pos);
+  if (i >= sc->n_tail) return false;
+  s.b = static_cast<int>(sc->key[i / a.Hkv] & 0xffffu);
+  s.hkv = i % a.Hkv;
+  const int L = sc->len[s.b];
+  s.split = min(L / a.split_size, a.num_splits);
   s.t0 = s.split * a.split_size;
-  s.t1 = min(s.t0 + a.split_size, L);
-  return s;
+  s.t1 = L;
+  return true;
+}
+
+__device__ __forceinline__ bool SlotIter::next(const DecodeArgs& a, const Sched* sc, bool balanced, Slot& s) {
+  while (next_slot(a, sc, balanced, q++, s))
+    if (s.t0 < s.t1) return true;
+  return false;
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(DCfg<D>::kThreads, 1)
     decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap map_k,
                         const __grid_constant__ CUtensorMap map_v, DeviceStatus* st, uint64_t limit_ns) {
   using C = DCfg<D>;
   constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBar);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBar);  // stage ring
   uint64_t* empty = full + kStages;
-  uint64_t* q_full = empty + kStages;
-  uint64_t* q_empty = q_full + kQSlots;
+  uint64_t* raw_full = empty + kStages;  // raw q rows (loader -> q warp)
+  uint64_t* raw_empty = raw_full + kQSlots;
+  uint64_t* qc_full = raw_empty + kQSlots;  // quantised q rows (q warp -> compute warps)
+  uint64_t* qc_empty = qc_full + kQSlots;
+  uint64_t* red_full = qc_empty + kQSlots;  // per-warp split states (compute warps -> q warp)
+  uint64_t* red_empty = red_full + 1;
+  Sched* sc = reinterpret_cast<Sched*>(smem + C::kSched);
+  float* stat = reinterpret_cast<float*>(smem + C::kStat);  // [warp][8 q][m, l, -, -]
+  float* red = reinterpret_cast<float*>(smem + C::kRed);    // [warp][d][8 q]
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const int G = a.Hq / a.Hkv;
-  const int64_t n_slots = static_cast<int64_t>(a.num_splits) * a.B * a.Hkv;
+  const bool balanced = a.B <= kSchedMaxB;
   const int q_elem = a.q_dtype == SL8_F32 ? 4 : 2;
   // scales ride the bulk copies when every stage's range is 16-byte aligned
   const bool scales_bulk = (a.Lmax % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.k_scale) |
@@ -231,62 +353,73 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kComputeWarps);
+      mbar_init(&empty[i], C::kNW);
     }
     for (int i = 0; i < kQSlots; ++i) {
-      mbar_init(&q_full[i], 1);
-      mbar_init(&q_empty[i], kComputeWarps);
+      mbar_init(&raw_full[i], 1);
+      mbar_init(&raw_empty[i], G);  // the warps quantising the rows
+      mbar_init(&qc_full[i], G);
+      mbar_init(&qc_empty[i], C::kNW);
     }
+    mbar_init(red_full, C::kNW);
+    mbar_init(red_empty, 1);
     fence_barrier_init();
   }
   __syncthreads();
+  if (balanced && warp == 0) build_sched_warp(a, sc, st);
+  __syncthreads();
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ loader
     if (lane == 0) {
       prefetch_tensormap(&map_k);
       prefetch_tensormap(&map_v);
     }
-    uint32_t k = 0, nq = 0;  // stages and q rows issued
+    // The q rows of split n + 1 are requested before the stages of split n, so that
+    // they are quantised while split n streams.
+    uint32_t k = 0, n = 0;  // stages issued, current split
     bool ok = true;
-    for (int64_t i = blockIdx.x; i < n_slots && ok; i += gridDim.x) {
-      const Slot s = decode_slot(a, i, st, lane == 0);
-      if (s.t0 >= s.t1) continue;
-      const int64_t row0 = (static_cast<int64_t>(s.b) * a.Hkv + s.hkv) * a.Lmax;
-      {
-        const uint32_t qs = nq % kQSlots;
-        if (nq >= kQSlots) ok = warp_wait(&q_empty[qs], ((nq / kQSlots) - 1) & 1, limit_ns, st, 42);
-        if (!ok) break;
-        if (lane == 0) {
-          const uint32_t q_bytes = static_cast<uint32_t>(G * D * q_elem);
-          mbar_arrive_expect_tx(&q_full[qs], q_bytes);
-          bulk_load(smem + C::kQ + qs * C::kQBytes,
-                    static_cast<const uint8_t*>(a.q) + (static_cast<int64_t>(s.b) * a.Hq + s.hkv * G) * D * q_elem,
-                    q_bytes, &q_full[qs]);
-        }
-        ++nq;
+    SlotIter it;
+    Slot cur, nxt;
+    auto load_q = [&](const Slot& x, uint32_t i) {
+      const uint32_t qs = i % kQSlots;
+      if (i >= kQSlots && !warp_wait(&raw_empty[qs], ((i / kQSlots) - 1) & 1, limit_ns, st, 42)) return false;
+      if (lane == 0) {
+        const uint32_t q_bytes = static_cast<uint32_t>(G * D * q_elem);
+        mbar_arrive_expect_tx(&raw_full[qs], q_bytes);
+        bulk_load(smem + C::kQ + qs * C::kQBytes,
+                  static_cast<const uint8_t*>(a.q) + (static_cast<int64_t>(x.b) * a.Hq + x.hkv * G) * D * q_elem,
+                  q_bytes, &raw_full[qs]);
       }
-      for (int c0 = s.t0; c0 < s.t1 && ok; c0 += kChunk, ++k) {
-        const int n = min(kChunk, s.t1 - c0);
+      return true;
+    };
+    bool has_cur = it.next(a, sc, balanced, cur);
+    if (has_cur) ok = load_q(cur, 0);
+    while (ok && has_cur) {
+      const bool has_nxt = it.next(a, sc, balanced, nxt);
+      if (has_nxt && !load_q(nxt, n + 1)) break;
+      const int64_t row0 = (static_cast<int64_t>(cur.b) * a.Hkv + cur.hkv) * a.Lmax;
+      for (int c0 = cur.t0; c0 < cur.t1 && ok; c0 += C::kChunk, ++k) {
+        const int nt = min(C::kChunk, cur.t1 - c0);
         const uint32_t stg = k % kStages;
         uint8_t* base = smem + stg * C::kStageBytes;
         if (k >= kStages) ok = warp_wait(&empty[stg], ((k / kStages) - 1) & 1, limit_ns, st, 41);
         if (!ok) break;
         if (!scales_bulk) {
-          for (int j = lane; j < n; j += 32) {
+          for (int j = lane; j < nt; j += 32) {
             reinterpret_cast<float*>(base + C::kSKs)[j] = a.k_scale[row0 + c0 + j];
             reinterpret_cast<float*>(base + C::kSVs)[j] = a.v_scale[row0 + c0 + j];
           }
           __syncwarp();
         }
         if (lane == 0) {
-          const uint32_t sc_bytes = scales_bulk ? static_cast<uint32_t>((n + 3) / 4 * 16) : 0u;
+          const uint32_t sc_bytes = scales_bulk ? static_cast<uint32_t>((nt + 3) / 4 * 16) : 0u;
           mbar_arrive_expect_tx(&full[stg], 2 * C::kTile + 2 * sc_bytes);
           const int y = static_cast<int>(row0 + c0);
 #pragma unroll
           for (int b = 0; b < C::kBoxes; ++b) {
-            tma_load_3d(base + C::kSK + b * kChunk * C::kBW, &map_k, &full[stg], b * C::kBW, y, 0);
-            tma_load_3d(base + C::kSV + b * kChunk * C::kBW, &map_v, &full[stg], b * C::kBW, y, 0);
+            tma_load_3d(base + C::kSK + b * C::kChunk * C::kBW, &map_k, &full[stg], b * C::kBW, y, 0);
+            tma_load_3d(base + C::kSV + b * C::kChunk * C::kBW, &map_v, &full[stg], b * C::kBW, y, 0);
           }
           if (scales_bulk) {
             bulk_load(base + C::kSKs, a.k_scale + row0 + c0, sc_bytes, &full[stg]);
@@ -294,15 +427,83 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      cur = nxt;
+      has_cur = has_nxt;
+      ++n;
     }
-    return;  // the compute warps never wait on the producer beyond the rings
+    return;  // nothing waits on the loader beyond the rings
+  }
+
+  if (warp == 1) {
+    // ------------------------------------------------------------ merges
+    bool ok = true;
+    uint32_t n = 0;
+    auto merge = [&](const Slot& m, uint32_t mi) {
+      if (!warp_wait(red_full, mi & 1, limit_ns, st, 45)) return false;
+      const int64_t row0 = static_cast<int64_t>(m.b) * a.Hq + m.hkv * G;
+      // lane q < G: the split's max and sum of query q over the warps
+      float M = -INFINITY, L = 0.0f;
+      if (lane < G) {
+#pragma unroll
+        for (int w = 0; w < C::kNW; ++w) M = fmaxf(M, stat[(w * 8 + lane) * 4]);
+#pragma unroll
+        for (int w = 0; w < C::kNW; ++w) {
+          const float mw = stat[(w * 8 + lane) * 4];
+          if (mw != -INFINITY) L += stat[(w * 8 + lane) * 4 + 1] * ex2(mw - M);
+        }
+        a.lse_partial[(row0 + lane) * a.num_splits + m.split] = (M + log2f(L)) * 0.6931471805599453f;
+      }
+      // weight of warp w's state for query q: 2^(m_w - M) / L
+      const int nq4 = G > 4 ? 2 : 1;  // float4 groups of query columns
+      const float rL = lane < G ? 1.0f / L : 0.0f;
+      float wt[C::kNW][8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float Mq = __shfl_sync(0xffffffffu, M, q), rLq = __shfl_sync(0xffffffffu, rL, q);
+#pragma unroll
+        for (int w = 0; w < C::kNW; ++w) {
+          const float mw = stat[(w * 8 + q) * 4];
+          wt[w][q] = mw == -INFINITY ? 0.0f : ex2(mw - Mq) * rLq;
+        }
+      }
+      // lane: dims lane + 32 i, all query columns of the group
+      for (int dim = lane; dim < D; dim += 32) {
+        float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int w = 0; w < C::kNW; ++w) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (h < nq4) {
+              const float4 r4 = *reinterpret_cast<const float4*>(red + (w * D + dim) * 8 + 4 * h);
+              acc[4 * h] = fmaf(r4.x, wt[w][4 * h], acc[4 * h]);
+              acc[4 * h + 1] = fmaf(r4.y, wt[w][4 * h + 1], acc[4 * h + 1]);
+              acc[4 * h + 2] = fmaf(r4.z, wt[w][4 * h + 2], acc[4 * h + 2]);
+              acc[4 * h + 3] = fmaf(r4.w, wt[w][4 * h + 3], acc[4 * h + 3]);
+            }
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (q < G) a.o_partial[((row0 + q) * a.num_splits + m.split) * D + dim] = acc[q];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(red_empty);
+      return true;
+    };
+    SlotIter it;
+    Slot cur;
+    while (ok && it.next(a, sc, balanced, cur)) {
+      ok = merge(cur, n);
+      ++n;
+    }
+    return;
   }
 
   // ------------------------------------------------------------ compute warps
-  const int ct = threadIdx.x - 32;  // 0 .. 255
-  const int cw = ct / 32;           // compute warp 0 .. 7
+  const int ct = threadIdx.x - 32 * kFirstCompute;  // 0 .. 255
+  const int cw = ct / 32;                            // compute warp 0 .. 7
   const int g = lane >> 2, t = lane & 3;
-  const int u0 = kUnit * cw;        // this warp's rows in every stage
+  const int u0 = kUnit * cw;  // this warp's rows in every stage
   // S^T rows of this lane: unit tokens pi and pi + 8.  The permutation keeps the
   // swizzled K reads free of bank conflicts, and the two tokens form P' pair pi.
   const int pi = C::kSwz ? (g >> 1) + 4 * (g & 1) : g;
@@ -325,79 +526,100 @@ __global__ void __launch_bounds__(kThreads, 1)
       offv[b][c] = D == 64 ? static_cast<uint32_t>(row * 64 + 8 * cg) : tile_off<D>(row, 8 * b + cg);
     }
   const float log2e_over_sqrtd = 1.4426950408889634f / sqrtf(static_cast<float>(D));
-  float* stat = reinterpret_cast<float*>(smem + C::kStat);
-  float* red = reinterpret_cast<float*>(smem + C::kRed);
   uint32_t* pw = reinterpret_cast<uint32_t*>(smem + C::kP + cw * 256);  // [8 q][8 pairs] fp16x2
-  int8_t* qcodes = reinterpret_cast<int8_t*>(smem + C::kQc);             // [8][D]
-  float* qinfo = reinterpret_cast<float*>(smem + C::kQc + 8 * D);        // [8] scale, [8] code sum
-  uint32_t k = 0, nq = 0;
-  bool ok = true;
-  for (int64_t i = blockIdx.x; i < n_slots && ok; i += gridDim.x) {
-    const Slot s = decode_slot(a, i, st, false);
-    const int64_t part_row0 = static_cast<int64_t>(s.b) * a.Hq + s.hkv * G;  // first (b, hq) row
-    if (s.t0 >= s.t1) {
-      // an empty split: lse = -inf (its O is never read); split 0 of an empty sequence
-      // still exports the q codes when asked
-      if (ct < G) a.lse_partial[(part_row0 + ct) * a.num_splits + s.split] = -INFINITY;
-      if (s.split == 0 && a.q_codes && cw < G) {
-        float v[D / 32];
-        int8_t code[D / 32];
-#pragma unroll
-        for (int e = 0; e < D / 32; ++e) v[e] = load_q_elem(a.q, a.q_dtype, (part_row0 + cw) * D + lane * (D / 32) + e);
-        const float sc = quant_row_warp<D>(v, code);
-#pragma unroll
-        for (int e = 0; e < D / 32; ++e) a.q_codes[(part_row0 + cw) * D + lane * (D / 32) + e] = code[e];
-        if (lane == 0) a.q_scales[part_row0 + cw] = sc;
-      }
-      continue;
-    }
 
-    // ---- the group's q rows: warp r quantises row r into shared memory
-    {
-      const uint32_t qs = nq % kQSlots;
-      ok = warp_wait(&q_full[qs], (nq / kQSlots) & 1, limit_ns, st, 43);
-      ++nq;
-      if (ok && cw < G) {
-        const uint8_t* raw = smem + C::kQ + qs * C::kQBytes + cw * D * q_elem;
+  // ---- empty splits, up front: lse = -inf (their O is never read), and the q codes of
+  // an empty sequence when asked; sequences b = blockIdx.x + k * gridDim.x
+  for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
+    const int L = clamp_len(a, b, st, !balanced && ct == 0);
+    const int ns = (L + a.split_size - 1) / a.split_size;
+    const int n_empty = (a.num_splits - ns) * a.Hq;
+    for (int e = ct; e < n_empty; e += C::kCT) {
+      const int split = ns + e / a.Hq, hq = e % a.Hq;
+      a.lse_partial[(static_cast<int64_t>(b) * a.Hq + hq) * a.num_splits + split] = -INFINITY;
+    }
+    if (L == 0 && a.q_codes) {
+      for (int hq = cw; hq < a.Hq; hq += C::kNW) {
+        const int64_t row = static_cast<int64_t>(b) * a.Hq + hq;
         float v[D / 32];
         int8_t code[D / 32];
 #pragma unroll
-        for (int e = 0; e < D / 32; ++e) {
-          const int idx = lane * (D / 32) + e;
-          v[e] = a.q_dtype == SL8_F32 ? reinterpret_cast<const float*>(raw)[idx]
-               : a.q_dtype == SL8_BF16 ? bf16_bits(reinterpret_cast<const uint16_t*>(raw)[idx])
-                                       : f16_bits(reinterpret_cast<const uint16_t*>(raw)[idx]);
-        }
-        const float sc = quant_row_warp<D>(v, code);
-        int csum = 0;
+        for (int e = 0; e < D / 32; ++e) v[e] = load_q_elem(a.q, a.q_dtype, row * D + lane * (D / 32) + e);
+        const float scq = quant_row_warp<D>(v, code);
 #pragma unroll
-        for (int e = 0; e < D / 32; ++e) {
-          qcodes[cw * D + lane * (D / 32) + e] = code[e];
-          csum += code[e];
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) csum += __shfl_xor_sync(0xffffffffu, csum, o);
-        if (lane == 0) {
-          qinfo[cw] = sc;
-          qinfo[8 + cw] = static_cast<float>(csum);
-        }
-        if (a.q_codes && s.split == 0) {
-#pragma unroll
-          for (int e = 0; e < D / 32; ++e) a.q_codes[(part_row0 + cw) * D + lane * (D / 32) + e] = code[e];
-          if (lane == 0) a.q_scales[part_row0 + cw] = sc;
-        }
+        for (int e = 0; e < D / 32; ++e) a.q_codes[row * D + lane * (D / 32) + e] = code[e];
+        if (lane == 0) a.q_scales[row] = scq;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&q_empty[qs]);
-      compute_sync();
     }
-    // B fragments of Q^T: k-step 4h + j holds dims 64h + 16t + 4j + {0, 1} | {2, 3} of
-    // query row g (exact fp16 integers); zero rows past G
+  }
+
+  // compute warp r < G quantises q row r of each split into qc[split % 2], one split
+  // ahead (split 0 before the loop)
+  auto quant_row = [&](const Slot& x, uint32_t i) {
+    const uint32_t qs = i % kQSlots;
+    if (!warp_wait(&raw_full[qs], (i / kQSlots) & 1, limit_ns, st, 43)) return false;
+    if (i >= kQSlots && !warp_wait(&qc_empty[qs], ((i / kQSlots) - 1) & 1, limit_ns, st, 44)) return false;
+    const uint8_t* raw = smem + C::kQ + qs * C::kQBytes + cw * D * q_elem;
+    int8_t* qc = reinterpret_cast<int8_t*>(smem + C::kQc + qs * C::kQcBytes);
+    float* qinfo = reinterpret_cast<float*>(qc + 8 * D);  // [8] scales, [8] code sums
+    float v[D / 32];
+    int8_t code[D / 32];
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) {
+      const int idx = lane * (D / 32) + e;
+      v[e] = a.q_dtype == SL8_F32 ? reinterpret_cast<const float*>(raw)[idx]
+           : a.q_dtype == SL8_BF16 ? bf16_bits(reinterpret_cast<const uint16_t*>(raw)[idx])
+                                   : f16_bits(reinterpret_cast<const uint16_t*>(raw)[idx]);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&raw_empty[qs]);
+    const float scq = quant_row_warp<D>(v, code);
+    int csum = 0;
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) {
+      qc[cw * D + lane * (D / 32) + e] = code[e];
+      csum += code[e];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) csum += __shfl_xor_sync(0xffffffffu, csum, o);
+    if (lane == 0) {
+      qinfo[cw] = scq;
+      qinfo[8 + cw] = static_cast<float>(csum);
+    }
+    if (a.q_codes && x.split == 0) {
+      const int64_t row = static_cast<int64_t>(x.b) * a.Hq + x.hkv * G + cw;
+#pragma unroll
+      for (int e = 0; e < D / 32; ++e) a.q_codes[row * D + lane * (D / 32) + e] = code[e];
+      if (lane == 0) a.q_scales[row] = scq;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&qc_full[qs]);
+    return true;
+  };
+
+  uint32_t k = 0, n = 0;
+  bool ok = true;
+  SlotIter it;
+  Slot s, s_next;
+  bool has_cur = it.next(a, sc, balanced, s);
+  if (has_cur && cw < G) ok = quant_row(s, 0);
+  while (ok && has_cur) {
+    const bool has_next = it.next(a, sc, balanced, s_next);
+    const int64_t part_row0 = static_cast<int64_t>(s.b) * a.Hq + s.hkv * G;  // first (b, hq) row
+    // ---- B fragments of Q^T from the quantised rows: k-step 4h + j holds dims
+    // 64h + 16t + 4j + {0, 1} | {2, 3} of query row g (exact fp16 integers); zero past G
+    const uint32_t qs = n % kQSlots;
+    if (!warp_wait(&qc_full[qs], (n / kQSlots) & 1, limit_ns, st, 46)) {
+      ok = false;
+      break;
+    }
+    const int8_t* qc = reinterpret_cast<const int8_t*>(smem + C::kQc + qs * C::kQcBytes);
+    const float* qinfo = reinterpret_cast<const float*>(qc + 8 * D);
     uint32_t qb[D / 16][2];
 #pragma unroll
     for (int h = 0; h < D / 64; ++h) {
       uint4 w = make_uint4(0u, 0u, 0u, 0u);
-      if (g < G) w = *reinterpret_cast<const uint4*>(qcodes + g * D + 64 * h + 16 * t);
+      if (g < G) w = *reinterpret_cast<const uint4*>(qc + g * D + 64 * h + 16 * t);
       const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -412,6 +634,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float qsb = 2 * t + 1 < G ? qinfo[2 * t + 1] * log2e_over_sqrtd : 0.0f;
     const float offa = 2 * t < G ? -128.0f * qinfo[8 + 2 * t] : 0.0f;
     const float offb = 2 * t + 1 < G ? -128.0f * qinfo[8 + 2 * t + 1] : 0.0f;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&qc_empty[qs]);
+    if (has_next && cw < G && !quant_row(s_next, n + 1)) {
+      ok = false;
+      break;
+    }
 
     // ---- per-warp online softmax state for the two query columns
     float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.0f, l_b = 0.0f;
@@ -421,16 +649,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     float o[D / 16][4], osum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int j = 0; j < D / 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.0f;
-
-    for (int c0 = s.t0; c0 < s.t1 && ok; c0 += kChunk, ++k) {
-      const int n = min(kChunk, s.t1 - c0);
+    for (int c0 = s.t0; c0 < s.t1 && ok; c0 += C::kChunk, ++k) {
+      const int ntok = min(C::kChunk, s.t1 - c0);
       const uint32_t stg = k % kStages;
       const uint8_t* base = smem + stg * C::kStageBytes;
       if (!warp_wait(&full[stg], (k / kStages) & 1, limit_ns, st, 40)) {
         ok = false;
         break;
       }
-      const int nv = n - u0;  // valid tokens of this warp's unit
+      const int nv = ntok - u0;  // valid tokens of this warp's unit
       auto unit = [&](auto full_tag) {
         constexpr bool kFull = decltype(full_tag)::value;
         const uint8_t* sk = base + C::kSK;
@@ -571,9 +798,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[stg]);  // 8 arrivals (one per compute warp) free the stage
     }
-    // ---- merge the eight warps' states of this split
+    if (!ok) break;
+    // ---- hand this warp's state to the merging warp: per query column its max and
+    // sum, and O = (2^24 O' - 128 rowsum(P')) * 2^E
     l_a = col_sum(l_a);
     l_b = col_sum(l_b);
+    if (n > 0 && !warp_wait(red_empty, (n - 1) & 1, limit_ns, st, 47)) {
+      ok = false;
+      break;
+    }
     if (g == 0) {
       float* sa = stat + (cw * 8 + 2 * t) * 4;
       sa[0] = m_a;
@@ -581,27 +814,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       sa[4] = m_b;
       sa[5] = l_b;
     }
-    if (!compute_all(ok)) {
-      ok = false;
-      break;
-    }
-    float Ma = -INFINITY, Mb = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kComputeWarps; ++w) {
-      Ma = fmaxf(Ma, stat[(w * 8 + 2 * t) * 4]);
-      Mb = fmaxf(Mb, stat[(w * 8 + 2 * t + 1) * 4]);
-    }
-    float La = 0.0f, Lb = 0.0f;
-#pragma unroll
-    for (int w = 0; w < kComputeWarps; ++w) {
-      const float* sa = stat + (w * 8 + 2 * t) * 4;
-      if (sa[0] != -INFINITY) La += sa[1] * ex2(sa[0] - Ma);
-      if (sa[4] != -INFINITY) Lb += sa[5] * ex2(sa[4] - Mb);
-    }
-    // O = (2^24 O' - 128 rowsum(P')) * 2^E * 2^(m - M) / L
     const float pe = pow2i(E);
-    const float fa = m_a == -INFINITY ? 0.0f : ex2(m_a - Ma) * pe / La;
-    const float fb = m_b == -INFINITY ? 0.0f : ex2(m_b - Mb) * pe / Lb;
     constexpr float k2p24 = 16777216.0f;
     const float ca = -128.0f * osum[0], cb = -128.0f * osum[1];
 #pragma unroll
@@ -614,26 +827,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         dim = 128 * (j >> 3) + 16 * cg + 4 * ((j & 7) >> 1) + 2 * (j & 1);
       }
       *reinterpret_cast<float2*>(red + (cw * D + dim) * 8 + 2 * t) =
-          make_float2(fmaf(o[j][0], k2p24, ca) * fa, fmaf(o[j][1], k2p24, cb) * fb);
+          make_float2(fmaf(o[j][0], k2p24, ca) * pe, fmaf(o[j][1], k2p24, cb) * pe);
       *reinterpret_cast<float2*>(red + (cw * D + dim + 1) * 8 + 2 * t) =
-          make_float2(fmaf(o[j][2], k2p24, ca) * fa, fmaf(o[j][3], k2p24, cb) * fb);
+          make_float2(fmaf(o[j][2], k2p24, ca) * pe, fmaf(o[j][3], k2p24, cb) * pe);
     }
-    if (cw == 0 && g == 0) {
-      if (2 * t < G)
-        a.lse_partial[(part_row0 + 2 * t) * a.num_splits + s.split] = (Ma + log2f(La)) * 0.6931471805599453f;
-      if (2 * t + 1 < G)
-        a.lse_partial[(part_row0 + 2 * t + 1) * a.num_splits + s.split] = (Mb + log2f(Lb)) * 0.6931471805599453f;
-    }
-    compute_sync();
-    // every shared buffer read below is rewritten only after the next split's q barrier
-    for (int idx = ct; idx < D * 8; idx += kComputeThreads) {
-      const int q = idx & 7, dim = idx >> 3;
-      if (q >= G) continue;
-      float acc = 0.0f;
-#pragma unroll
-      for (int w = 0; w < kComputeWarps; ++w) acc += red[(w * D + dim) * 8 + q];
-      a.o_partial[((part_row0 + q) * a.num_splits + s.split) * D + dim] = acc;
-    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(red_full);
+    ++n;
+    s = s_next;
+    has_cur = has_next;
   }
 }
 
@@ -698,23 +900,23 @@ cudaError_t launch_split_d(const DecodeArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
   if (e != cudaSuccess) return e;
   // each cache as a 2-D [B * Hkv * Lmax rows][d bytes] tensor, loaded in boxes of
-  // kChunk rows x kBW bytes
+  // C::kChunk rows x kBW bytes
   const uint64_t rows = static_cast<uint64_t>(a.B) * a.Hkv * a.Lmax;
   bool ok = true;
   const CUtensorMap mk = make_tmap_3d(a.k_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, D, rows, 1, D, rows * D, C::kBW,
-                                      kChunk, 1, &ok, C::kSwz);
+                                      C::kChunk, 1, &ok, C::kSwz);
   const CUtensorMap mv = make_tmap_3d(a.v_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, D, rows, 1, D, rows * D, C::kBW,
-                                      kChunk, 1, &ok, C::kSwz);
+                                      C::kChunk, 1, &ok, C::kSwz);
   if (!ok) return cudaErrorInvalidValue;
   const int64_t slots = static_cast<int64_t>(a.num_splits) * a.B * a.Hkv;
   const int grid = static_cast<int>(slots < num_sms() ? slots : num_sms());
-  kern<<<grid, kThreads, C::kBytes, s>>>(a, mk, mv, device_status_ptr(), spin_limit_ns());
+  kern<<<grid, C::kThreads, C::kBytes, s>>>(a, mk, mv, device_status_ptr(), spin_limit_ns());
   return cudaGetLastError();
 }
 
 }  // namespace
 
-int decode_chunk_tokens(int) { return kChunk; }
+int decode_chunk_tokens(int d) { return d == 256 ? DCfg<256>::kChunk : d == 128 ? DCfg<128>::kChunk : DCfg<64>::kChunk; }
 
 cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t s) {
   TraceScope tr("decode_split", s);
