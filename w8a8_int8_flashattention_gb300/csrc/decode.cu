@@ -35,6 +35,7 @@
 //    than 2^8 (p then stays below 256), and the power-of-two V range E only when a
 //    token's V scale exceeds 2^E; both keep P' inside the fp16 range.
 #include <cuda_bf16.h>
+#include <atomic>
 #include <type_traits>
 #include <cuda_fp16.h>
 
@@ -50,12 +51,25 @@ constexpr int kQSlots = 2;                      // q-row buffers (one per split 
 constexpr float kLazy = 8.0f;                   // log2 headroom of the lazy max
 
 constexpr int kSchedMaxB = 512;
+struct Slot {
+  int split, b, hkv, t0, t1;  // b < 0: no more slots
+};
+constexpr int kSlotRing = 8;   // slots announced by the loader ahead of the compute warps
 struct Sched {
   int32_t len[kSchedMaxB];       // sequence lengths clamped to [0, Lmax]
   int32_t pf[kSchedMaxB + 1];    // prefix over b of the full slots (full splits x Hkv)
   uint32_t key[kSchedMaxB];      // sorted: (split_size - tail) << 16 | b, then 0xffffffff
   int32_t n_full, n_tail;        // slots of each kind
+  Slot ring[kSlotRing];          // slot n of this CTA in ring[n % kSlotRing]
+  Slot merge;                    // the slot whose warp states wait in the merge buffer
 };
+// Dynamic claims: CTA c takes slot c first, then the next unclaimed slot from a
+// per-launch counter.  A launch uses counter pair g_claim[ticket] ([0] next slot - grid,
+// [1] CTAs done); the last CTA to finish zeroes the pair for the next launch that draws
+// the same ticket (tickets rotate over kTickets launches, so up to kTickets launches may
+// run at the same time).
+constexpr int kTickets = 64;
+__device__ uint32_t g_claim[kTickets][2];
 static_assert(kSchedMaxB <= 65536, "b fits the key");
 
 template <int D>
@@ -86,7 +100,7 @@ struct DCfg {
   static constexpr int kQc = kStat + kNW * 8 * 16;             // [2] quantised q rows
   static constexpr int kSched = kQc + kQSlots * kQcBytes;      // Sched
   static constexpr int kBar = (kSched + static_cast<int>(sizeof(Sched)) + 15) / 16 * 16;
-  static constexpr int kNumBars = 2 * kStages + 4 * kQSlots + 2;
+  static constexpr int kNumBars = 2 * kStages + 4 * kQSlots + 3;
   static constexpr int kBytes = kBar + kNumBars * 8 + 1024;    // + alignment slack
   static_assert(kStageBytes % 1024 == 0 && kTile % 1024 == 0, "swizzled tiles need 1024-byte alignment");
   static_assert(kBytes <= 232448, "smem budget");
@@ -189,16 +203,10 @@ __device__ __forceinline__ float load_q_elem(const void* base, sl8_dtype dt, int
 }
 
 // ---- work schedule
-// A work slot is one (b, kv head, split).  With B <= kSchedMaxB every CTA builds the
-// same balanced schedule in shared memory: the full splits (split_size tokens) are
-// dealt round-robin, then the partial last splits of the sequences, longest first, in
-// snake order starting at the CTA after the last full one; empty splits are handled
-// up front and never scheduled.  Above kSchedMaxB the slots go round-robin in
-// split-major order (empty ones are skipped).
-
-struct Slot {
-  int split, b, hkv, t0, t1;
-};
+// A work slot is one (b, kv head, split).  With B <= kSchedMaxB the launch's slot list
+// is: the full splits (split_size tokens), then the sequences' partial last splits,
+// longest first; empty splits are handled up front and never listed.  Above
+// kSchedMaxB the list is every slot in split-major order (empty ones are skipped).
 
 __device__ __forceinline__ int clamp_len(const DecodeArgs& a, int b, DeviceStatus* st, bool report) {
   int L = a.seqlens[b];
@@ -209,8 +217,8 @@ __device__ __forceinline__ int clamp_len(const DecodeArgs& a, int b, DeviceStatu
   return L;
 }
 
-// Build the balanced schedule; one warp (the caller syncs the CTA afterwards).
-__device__ void build_sched_warp(const DecodeArgs& a, Sched* sc, DeviceStatus* st) {
+// Lengths, tail keys (unsorted) and the prefix of the full slots; one warp.
+__device__ void sched_prefix_warp(const DecodeArgs& a, Sched* sc, DeviceStatus* st) {
   const int lane = threadIdx.x & 31;
   int n2 = 32;
   while (n2 < a.B) n2 <<= 1;
@@ -246,7 +254,13 @@ __device__ void build_sched_warp(const DecodeArgs& a, Sched* sc, DeviceStatus* s
   }
   if (lane == 0) sc->n_tail = tails * a.Hkv;
   __syncwarp();
-  // bitonic sort of the tail keys, ascending
+}
+
+// Bitonic sort of the tail keys, ascending (longest tail first); one warp.
+__device__ void sched_sort_warp(const DecodeArgs& a, Sched* sc) {
+  const int lane = threadIdx.x & 31;
+  int n2 = 32;
+  while (n2 < a.B) n2 <<= 1;
   for (int size = 2; size <= n2; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       for (int i = lane; i < n2 / 2; i += 32) {
@@ -262,41 +276,36 @@ __device__ void build_sched_warp(const DecodeArgs& a, Sched* sc, DeviceStatus* s
   }
 }
 
-// Walks this CTA's non-empty slots.
-struct SlotIter {
-  int q = 0;
-  __device__ __forceinline__ bool next(const DecodeArgs& a, const Sched* sc, bool balanced, Slot& s);
-};
+// Number of entries in the launch's slot list.
+__device__ __forceinline__ int64_t slot_count(const DecodeArgs& a, const Sched* sc, bool balanced) {
+  return balanced ? static_cast<int64_t>(sc->n_full) + sc->n_tail
+                  : static_cast<int64_t>(a.num_splits) * a.B * a.Hkv;
+}
 
-// The q-th slot of this CTA; false when it has no more.  In the split-major order a
-// slot can be empty (t0 >= t1); the caller skips it.
-__device__ __forceinline__ bool next_slot(const DecodeArgs& a, const Sched* sc, bool balanced, int q, Slot& s) {
-  const int c = blockIdx.x, grid = gridDim.x;
+// Entry j of the slot list; false if it is empty (split-major order only).  Tail
+// entries (j >= n_full) need the sorted keys.
+__device__ __forceinline__ bool slot_at(const DecodeArgs& a, const Sched* sc, bool balanced, int64_t j, Slot& s) {
   if (!balanced) {
-    const int64_t i = c + static_cast<int64_t>(q) * grid;
     const int64_t per = static_cast<int64_t>(a.B) * a.Hkv;
-    if (i >= per * a.num_splits) return false;
-    s.split = static_cast<int>(i / per);
-    const int64_t r = i - s.split * per;
+    s.split = static_cast<int>(j / per);
+    const int64_t r = j - s.split * per;
     s.b = static_cast<int>(r / a.Hkv);
     s.hkv = static_cast<int>(r - static_cast<int64_t>(s.b) * a.Hkv);
     int L = a.seqlens[s.b];
     L = L < 0 ? 0 : (L > a.Lmax ? a.Lmax : L);
     s.t0 = s.split * a.split_size;
     s.t1 = min(s.t0 + a.split_size, L);
-    return true;
+    return s.t0 < s.t1;
   }
-  const int F = sc->n_full;
-  const int mine = F > c ? (F - 1 - c) / grid + 1 : 0;
-  if (q < mine) {
-    const int j = c + q * grid;
+  if (j < sc->n_full) {
+    const int jj = static_cast<int>(j);
     int lo = 0, hi = a.B;  // last b with pf[b] <= j
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (sc->pf[mid] <= j) lo = mid;
+      if (sc->pf[mid] <= jj) lo = mid;
       else hi = mid;
     }
-    const int r = j - sc->pf[lo];
+    const int r = jj - sc->pf[lo];
     s.b = lo;
     s.split = r / a.Hkv;
     s.hkv = r - s.split * a.Hkv;
@@ -304,9 +313,7 @@ __device__ __forceinline__ bool next_slot(const DecodeArgs& a, const Sched* sc, 
     s.t1 = s.t0 + a.split_size;
     return true;
   }
-  const int p = q - mine, pos = ((c - F % grid) % grid + grid) % grid;
-  const int i = p * grid + ((p & 1) ? grid - 1 - pos : pos);
-  if (i >= sc->n_tail) return false;
+  const int i = static_cast<int>(j - sc->n_full);
   s.b = static_cast<int>(sc->key[i / a.Hkv] & 0xffffu);
   s.hkv = i % a.Hkv;
   const int L = sc->len[s.b];
@@ -316,16 +323,11 @@ __device__ __forceinline__ bool next_slot(const DecodeArgs& a, const Sched* sc, 
   return true;
 }
 
-__device__ __forceinline__ bool SlotIter::next(const DecodeArgs& a, const Sched* sc, bool balanced, Slot& s) {
-  while (next_slot(a, sc, balanced, q++, s))
-    if (s.t0 < s.t1) return true;
-  return false;
-}
-
 template <int D>
 __global__ void __launch_bounds__(DCfg<D>::kThreads, 1)
     decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap map_k,
-                        const __grid_constant__ CUtensorMap map_v, DeviceStatus* st, uint64_t limit_ns) {
+                        const __grid_constant__ CUtensorMap map_v, uint32_t ticket, DeviceStatus* st,
+                        uint64_t limit_ns) {
   using C = DCfg<D>;
   constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -336,8 +338,9 @@ __global__ void __launch_bounds__(DCfg<D>::kThreads, 1)
   uint64_t* raw_empty = raw_full + kQSlots;
   uint64_t* qc_full = raw_empty + kQSlots;  // quantised q rows (q warp -> compute warps)
   uint64_t* qc_empty = qc_full + kQSlots;
-  uint64_t* red_full = qc_empty + kQSlots;  // per-warp split states (compute warps -> q warp)
+  uint64_t* red_full = qc_empty + kQSlots;  // per-warp split states (compute warps -> merging warp)
   uint64_t* red_empty = red_full + 1;
+  uint64_t* sched_sorted = red_empty + 1;  // tail keys sorted (merging warp -> loader)
   Sched* sc = reinterpret_cast<Sched*>(smem + C::kSched);
   float* stat = reinterpret_cast<float*>(smem + C::kStat);  // [warp][8 q][m, l, -, -]
   float* red = reinterpret_cast<float*>(smem + C::kRed);    // [warp][d][8 q]
@@ -363,10 +366,12 @@ __global__ void __launch_bounds__(DCfg<D>::kThreads, 1)
     }
     mbar_init(red_full, C::kNW);
     mbar_init(red_empty, 1);
+    mbar_init(sched_sorted, 1);
     fence_barrier_init();
   }
-  __syncthreads();
-  if (balanced && warp == 0) build_sched_warp(a, sc, st);
+  // the loader's warp lays out the slot list before anyone uses it; the merging warp
+  // sorts the tail keys in the background
+  if (balanced && warp == 0) sched_prefix_warp(a, sc, st);
   __syncthreads();
 
   if (warp == 0) {
@@ -375,29 +380,75 @@ __global__ void __launch_bounds__(DCfg<D>::kThreads, 1)
       prefetch_tensormap(&map_k);
       prefetch_tensormap(&map_v);
     }
-    // The q rows of split n + 1 are requested before the stages of split n, so that
-    // they are quantised while split n streams.
-    uint32_t k = 0, n = 0;  // stages issued, current split
-    bool ok = true;
-    SlotIter it;
-    Slot cur, nxt;
-    auto load_q = [&](const Slot& x, uint32_t i) {
+    // Slot n + 1 is claimed (and its q rows requested) before the stages of slot n, so
+    // that its q rows are quantised while slot n streams; the claim of slot n + 2 is in
+    // flight meanwhile.
+    const int64_t total = slot_count(a, sc, balanced);
+    uint32_t* counter = &g_claim[ticket][0];
+    uint32_t k = 0, n = 0;  // stages issued, current slot
+    bool ok = true, sorted = !balanced;
+    // the next entry of the slot list for this CTA: entry blockIdx.x first, then claims
+    int64_t first = blockIdx.x;
+    uint32_t pending = 0;  // claim in flight (valid when claiming)
+    bool claiming = false, exhausted = static_cast<int64_t>(blockIdx.x) >= total;
+    auto next_entry = [&](Slot& x) {
+      while (!exhausted) {
+        int64_t j;
+        if (first >= 0) {
+          j = first;
+          first = -1;
+        } else {
+          if (!claiming) {
+            if (lane == 0) pending = atomicAdd(counter, 1u);
+            claiming = true;
+          }
+          j = static_cast<int64_t>(__shfl_sync(0xffffffffu, pending, 0)) + gridDim.x;
+          claiming = false;
+        }
+        if (j >= total) {
+          exhausted = true;
+          break;
+        }
+        // start the following claim now; its result is read at the next call
+        if (lane == 0) pending = atomicAdd(counter, 1u);
+        claiming = true;
+        if (balanced && j >= sc->n_full && !sorted) {
+          sorted = warp_wait(sched_sorted, 0, limit_ns, st, 48);
+          if (!sorted) {
+            ok = false;
+            exhausted = true;
+            break;
+          }
+        }
+        if (slot_at(a, sc, balanced, j, x)) return true;
+      }
+      x.b = -1;  // no more slots
+      return false;
+    };
+    // announce slot i (or the end) to the compute warps and request its q rows
+    auto announce = [&](const Slot& x, uint32_t i) {
       const uint32_t qs = i % kQSlots;
       if (i >= kQSlots && !warp_wait(&raw_empty[qs], ((i / kQSlots) - 1) & 1, limit_ns, st, 42)) return false;
       if (lane == 0) {
-        const uint32_t q_bytes = static_cast<uint32_t>(G * D * q_elem);
-        mbar_arrive_expect_tx(&raw_full[qs], q_bytes);
-        bulk_load(smem + C::kQ + qs * C::kQBytes,
-                  static_cast<const uint8_t*>(a.q) + (static_cast<int64_t>(x.b) * a.Hq + x.hkv * G) * D * q_elem,
-                  q_bytes, &raw_full[qs]);
+        sc->ring[i % kSlotRing] = x;
+        if (x.b >= 0) {
+          const uint32_t q_bytes = static_cast<uint32_t>(G * D * q_elem);
+          mbar_arrive_expect_tx(&raw_full[qs], q_bytes);
+          bulk_load(smem + C::kQ + qs * C::kQBytes,
+                    static_cast<const uint8_t*>(a.q) + (static_cast<int64_t>(x.b) * a.Hq + x.hkv * G) * D * q_elem,
+                    q_bytes, &raw_full[qs]);
+        } else {
+          mbar_arrive(&raw_full[qs]);
+        }
       }
       return true;
     };
-    bool has_cur = it.next(a, sc, balanced, cur);
-    if (has_cur) ok = load_q(cur, 0);
+    Slot cur, nxt;
+    bool has_cur = next_entry(cur);
+    ok = ok && announce(cur, 0);
     while (ok && has_cur) {
-      const bool has_nxt = it.next(a, sc, balanced, nxt);
-      if (has_nxt && !load_q(nxt, n + 1)) break;
+      const bool has_nxt = next_entry(nxt);
+      if (!ok || !announce(nxt, n + 1)) break;
       const int64_t row0 = (static_cast<int64_t>(cur.b) * a.Hkv + cur.hkv) * a.Lmax;
       for (int c0 = cur.t0; c0 < cur.t1 && ok; c0 += C::kChunk, ++k) {
         const int nt = min(C::kChunk, cur.t1 - c0);
@@ -431,6 +482,19 @@ __global__ void __launch_bounds__(DCfg<D>::kThreads, 1)
       has_cur = has_nxt;
       ++n;
     }
+    // This CTA claims no more; a claim still in flight is part of the count.  The last
+    // CTA of the launch resets the ticket's counters.
+    if (lane == 0) {
+      if (claiming) {
+        volatile uint32_t settled = pending;  // the claim in flight has completed
+        (void)settled;
+      }
+      __threadfence();
+      if (atomicAdd(&g_claim[ticket][1], 1u) == gridDim.x - 1) {
+        atomicExch(&g_claim[ticket][0], 0u);
+        atomicExch(&g_claim[ticket][1], 0u);
+      }
+    }
     return;  // nothing waits on the loader beyond the rings
   }
 
@@ -439,7 +503,6 @@ __global__ void __launch_bounds__(DCfg<D>::kThreads, 1)
     bool ok = true;
     uint32_t n = 0;
     auto merge = [&](const Slot& m, uint32_t mi) {
-      if (!warp_wait(red_full, mi & 1, limit_ns, st, 45)) return false;
       const int64_t row0 = static_cast<int64_t>(m.b) * a.Hq + m.hkv * G;
       // lane q < G: the split's max and sum of query q over the warps
       float M = -INFINITY, L = 0.0f;
@@ -490,10 +553,16 @@ __global__ void __launch_bounds__(DCfg<D>::kThreads, 1)
       if (lane == 0) mbar_arrive(red_empty);
       return true;
     };
-    SlotIter it;
-    Slot cur;
-    while (ok && it.next(a, sc, balanced, cur)) {
-      ok = merge(cur, n);
+    if (balanced) {
+      sched_sort_warp(a, sc);
+      if (lane == 0) mbar_arrive(sched_sorted);
+    }
+    // the compute warps hand over slot n with red_full; a slot with b < 0 ends the list
+    while (ok) {
+      if (!warp_wait(red_full, n & 1, limit_ns, st, 45)) break;
+      const Slot m = sc->merge;
+      if (m.b < 0) break;
+      ok = merge(m, n);
       ++n;
     }
     return;
@@ -555,10 +624,19 @@ __global__ void __launch_bounds__(DCfg<D>::kThreads, 1)
 
   // compute warp r < G quantises q row r of each split into qc[split % 2], one split
   // ahead (split 0 before the loop)
-  auto quant_row = [&](const Slot& x, uint32_t i) {
+  auto quant_row = [&](uint32_t i) {
     const uint32_t qs = i % kQSlots;
     if (!warp_wait(&raw_full[qs], (i / kQSlots) & 1, limit_ns, st, 43)) return false;
     if (i >= kQSlots && !warp_wait(&qc_empty[qs], ((i / kQSlots) - 1) & 1, limit_ns, st, 44)) return false;
+    const Slot x = sc->ring[i % kSlotRing];
+    if (x.b < 0) {  // the list has ended: nothing to quantise
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&raw_empty[qs]);
+        mbar_arrive(&qc_full[qs]);
+      }
+      return true;
+    }
     const uint8_t* raw = smem + C::kQ + qs * C::kQBytes + cw * D * q_elem;
     int8_t* qc = reinterpret_cast<int8_t*>(smem + C::kQc + qs * C::kQcBytes);
     float* qinfo = reinterpret_cast<float*>(qc + 8 * D);  // [8] scales, [8] code sums
@@ -599,20 +677,20 @@ __global__ void __launch_bounds__(DCfg<D>::kThreads, 1)
 
   uint32_t k = 0, n = 0;
   bool ok = true;
-  SlotIter it;
-  Slot s, s_next;
-  bool has_cur = it.next(a, sc, balanced, s);
-  if (has_cur && cw < G) ok = quant_row(s, 0);
-  while (ok && has_cur) {
-    const bool has_next = it.next(a, sc, balanced, s_next);
-    const int64_t part_row0 = static_cast<int64_t>(s.b) * a.Hq + s.hkv * G;  // first (b, hq) row
-    // ---- B fragments of Q^T from the quantised rows: k-step 4h + j holds dims
-    // 64h + 16t + 4j + {0, 1} | {2, 3} of query row g (exact fp16 integers); zero past G
+  Slot s;
+  if (cw < G) ok = quant_row(0);
+  while (ok) {
+    // ---- slot n, as announced by the loader (b < 0: the list has ended)
     const uint32_t qs = n % kQSlots;
     if (!warp_wait(&qc_full[qs], (n / kQSlots) & 1, limit_ns, st, 46)) {
       ok = false;
       break;
     }
+    s = sc->ring[n % kSlotRing];
+    if (s.b < 0) break;
+    const int64_t part_row0 = static_cast<int64_t>(s.b) * a.Hq + s.hkv * G;  // first (b, hq) row
+    // ---- B fragments of Q^T from the quantised rows: k-step 4h + j holds dims
+    // 64h + 16t + 4j + {0, 1} | {2, 3} of query row g (exact fp16 integers); zero past G
     const int8_t* qc = reinterpret_cast<const int8_t*>(smem + C::kQc + qs * C::kQcBytes);
     const float* qinfo = reinterpret_cast<const float*>(qc + 8 * D);
     uint32_t qb[D / 16][2];
@@ -636,7 +714,7 @@ __global__ void __launch_bounds__(DCfg<D>::kThreads, 1)
     const float offb = 2 * t + 1 < G ? -128.0f * qinfo[8 + 2 * t + 1] : 0.0f;
     __syncwarp();
     if (lane == 0) mbar_arrive(&qc_empty[qs]);
-    if (has_next && cw < G && !quant_row(s_next, n + 1)) {
+    if (cw < G && !quant_row(n + 1)) {
       ok = false;
       break;
     }
@@ -831,11 +909,17 @@ __global__ void __launch_bounds__(DCfg<D>::kThreads, 1)
       *reinterpret_cast<float2*>(red + (cw * D + dim + 1) * 8 + 2 * t) =
           make_float2(fmaf(o[j][2], k2p24, ca) * pe, fmaf(o[j][3], k2p24, cb) * pe);
     }
+    if (cw == 0 && lane == 0) sc->merge = s;
     __syncwarp();
     if (lane == 0) mbar_arrive(red_full);
     ++n;
-    s = s_next;
-    has_cur = has_next;
+  }
+  // hand the end of the list to the merging warp
+  if (ok && n > 0 && !warp_wait(red_empty, (n - 1) & 1, limit_ns, st, 47)) ok = false;
+  if (ok) {
+    if (cw == 0 && lane == 0) sc->merge.b = -1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(red_full);
   }
 }
 
@@ -910,7 +994,9 @@ cudaError_t launch_split_d(const DecodeArgs& a, cudaStream_t s) {
   if (!ok) return cudaErrorInvalidValue;
   const int64_t slots = static_cast<int64_t>(a.num_splits) * a.B * a.Hkv;
   const int grid = static_cast<int>(slots < num_sms() ? slots : num_sms());
-  kern<<<grid, C::kThreads, C::kBytes, s>>>(a, mk, mv, device_status_ptr(), spin_limit_ns());
+  static std::atomic<uint32_t> next_ticket{0};
+  const uint32_t ticket = next_ticket.fetch_add(1, std::memory_order_relaxed) % kTickets;
+  kern<<<grid, C::kThreads, C::kBytes, s>>>(a, mk, mv, ticket, device_status_ptr(), spin_limit_ns());
   return cudaGetLastError();
 }
 
