@@ -162,6 +162,7 @@ PrefillWorkspace plan_prefill_workspace(int32_t nseq, int32_t Hq, int32_t Hkv, i
   w.k_partials = take(static_cast<size_t>(nseq) * Hkv * w.max_chunks * d * 4);
   w.v_partials = take(static_cast<size_t>(nseq) * Hkv * w.max_chunks * 4);
   w.v_exp = take(static_cast<size_t>(nseq) * Hkv * 4);
+  w.kv_done = take(static_cast<size_t>(nseq) * Hkv * 4);
   w.pstart = take(static_cast<size_t>(nseq) * 4);
   w.len = take(static_cast<size_t>(nseq) * 4);
   w.tok0 = take(static_cast<size_t>(nseq) * 4);
@@ -288,11 +289,12 @@ int sl8_k_channel_mean(const void* k, int k_dtype, int32_t B, int32_t Hkv, int32
   uint8_t* base = static_cast<uint8_t*>(workspace) - p.k_mean;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const SeqTable t = table_at(base, p);
+  int32_t* kv_done = reinterpret_cast<int32_t*>(base + p.kv_done);
   SL8_LAUNCH(launch_schedule(cu_seqlens, B, N, cu_seqlens ? total_tokens : static_cast<int64_t>(B) * N,
-                             static_cast<int64_t>(B) * p.max_tiles * kPadRows, t, kQTile, s));
+                             static_cast<int64_t>(B) * p.max_tiles * kPadRows, t, kQTile, kv_done, B * Hkv, s));
   SL8_LAUNCH(launch_kv_stats(k, static_cast<sl8_dtype>(k_dtype), nullptr, cu_seqlens != nullptr, B, Hkv, N, d, t.len,
                              t.tok0, reinterpret_cast<float*>(base + p.k_partials), nullptr, p.max_chunks, mean_out,
-                             nullptr, s));
+                             nullptr, kv_done, s));
   return SL8_OK;
 }
 
@@ -315,22 +317,21 @@ static int prefill_prepare(const void* q, const void* k, const void* v, int qk_d
   const SeqTable t = table_at(ws, p);
   const int64_t tokens = varlen ? total_tokens : static_cast<int64_t>(B) * N;
   const bool convert_v = v && v_dtype == SL8_BF16;
-  SL8_LAUNCH(launch_schedule(cu_seqlens, B, N, tokens, p.t_pad_max, t, prefill_item_rows(d), s));
+  int32_t* kv_done = reinterpret_cast<int32_t*>(ws + p.kv_done);
+  SL8_LAUNCH(launch_schedule(cu_seqlens, B, N, tokens, p.t_pad_max, t, prefill_item_rows(d), kv_done, B * Hkv, s));
   float* mean = smooth_k ? reinterpret_cast<float*>(ws + p.k_mean) : nullptr;
   int32_t* v_exp = convert_v ? reinterpret_cast<int32_t*>(ws + p.v_exp) : nullptr;
   if (smooth_k || convert_v) {
     SL8_LAUNCH(launch_kv_stats(k, static_cast<sl8_dtype>(qk_dtype), convert_v ? v : nullptr, varlen, B, Hkv, N, d,
                                t.len, t.tok0, smooth_k ? reinterpret_cast<float*>(ws + p.k_partials) : nullptr,
                                convert_v ? reinterpret_cast<float*>(ws + p.v_partials) : nullptr, p.max_chunks, mean,
-                               v_exp, s));
+                               v_exp, kv_done, s));
   }
-  SL8_LAUNCH(launch_quant_codes(k, static_cast<sl8_dtype>(qk_dtype), varlen, B, Hkv, N, d, tokens, t, p.t_pad_max,
-                                mean, reinterpret_cast<uint16_t*>(ws + p.k_codes),
-                                reinterpret_cast<float*>(ws + p.k_scales), convert_v ? v : nullptr, v_exp,
-                                convert_v ? reinterpret_cast<uint16_t*>(ws + p.v16) : nullptr, true, s));
-  SL8_LAUNCH(launch_quant_codes(q, static_cast<sl8_dtype>(qk_dtype), varlen, B, Hq, N, d, tokens, t, p.t_pad_max,
-                                nullptr, reinterpret_cast<uint16_t*>(ws + p.q_codes),
-                                reinterpret_cast<float*>(ws + p.q_scales), nullptr, nullptr, nullptr, false, s));
+  SL8_LAUNCH(launch_quant_qk(q, k, static_cast<sl8_dtype>(qk_dtype), varlen, B, Hq, Hkv, N, d, tokens, t,
+                             p.t_pad_max, mean, reinterpret_cast<uint16_t*>(ws + p.q_codes),
+                             reinterpret_cast<float*>(ws + p.q_scales), reinterpret_cast<uint16_t*>(ws + p.k_codes),
+                             reinterpret_cast<float*>(ws + p.k_scales), convert_v ? v : nullptr, v_exp,
+                             convert_v ? reinterpret_cast<uint16_t*>(ws + p.v16) : nullptr, s));
   *plan = p;
   *table = t;
   return SL8_OK;

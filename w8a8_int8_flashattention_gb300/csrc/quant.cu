@@ -60,6 +60,25 @@ __device__ __forceinline__ int quant_code(float x, float s) {
   int c = __float2int_rn(__fdiv_rn(x, s));
   return c > 127 ? 127 : (c < -127 ? -127 : c);
 }
+// Round-half-even of |y| < 2^22 to an integer-valued float, in two additions.
+__device__ __forceinline__ float rint_add(float y) {
+  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: its ulp is 1
+  return __fsub_rn(__fadd_rn(y, kMagic), kMagic);
+}
+// The same code as an integer-valued float, from rs = RN(1 / s): for |x / s| <= 127.5 the
+// product x * rs lies within 3e-5 of the correctly rounded quotient, so both round to
+// the same integer unless the product is within 1e-4 of a half-integer; only then is
+// the quotient formed.
+__device__ __forceinline__ float quant_code_rcp(float x, float s, float rs) {
+  const float y = __fmul_rn(x, rs);
+  float r = rint_add(y);
+  if (fabsf(__fsub_rn(y, r)) > 0.4999f) r = rint_add(__fdiv_rn(x, s));
+  return fminf(fmaxf(r, -127.0f), 127.0f);
+}
+// bf16 bit pattern of an integer-valued float |c| <= 127 (exact: its low 16 bits are 0).
+__device__ __forceinline__ uint16_t code_f_to_bf16_bits(float c) {
+  return static_cast<uint16_t>(__float_as_uint(c) >> 16);
+}
 
 __device__ __forceinline__ float warp_max(float a) {
 #pragma unroll
@@ -103,17 +122,25 @@ __device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* s_wa
 // list of (sequence, item) pairs, an item being `item_rows` consecutive query rows.
 // Order: by item index from the largest down (under a causal mask the last item of a
 // sequence has the most key tiles), sequences with more items first within a level.
+// The histogram lives in shared memory when it fits (kSmemHist), else in t.hist.  It
+// also zeroes the n_done completion counters of the K/V statistics kernel.
+template <bool kSmemHist>
 __global__ void __launch_bounds__(1024) schedule_kernel(const int32_t* __restrict__ cu, int32_t nseq, int32_t N,
                                                         int64_t total_tokens, int64_t t_pad_max, SeqTable t,
-                                                        int32_t max_items, int32_t item_rows, DeviceStatus* st) {
+                                                        int32_t max_items, int32_t item_rows, int32_t* kv_done,
+                                                        int32_t n_done, DeviceStatus* st) {
+  extern __shared__ int32_t sh_hist[];
   __shared__ int32_t s_warp[32];
   __shared__ int32_t s_fits;
+  grid_dependency_wait();
   const int tid = threadIdx.x, nt = blockDim.x;
   const int H = max_items + 2;
-  int32_t* bucket = t.hist;             // [H] counts, then bucket starts
-  int32_t* fill = t.hist + H;           // [H]
-  int32_t* level_off = t.hist + 2 * H;  // [H]
-  for (int i = tid; i < 3 * H; i += nt) t.hist[i] = 0;
+  int32_t* hist = kSmemHist ? sh_hist : t.hist;
+  int32_t* bucket = hist;           // [H] counts, then bucket starts
+  int32_t* fill = hist + H;         // [H]
+  int32_t* level_off = hist + 2 * H;  // [H]
+  for (int i = tid; i < 3 * H; i += nt) hist[i] = 0;
+  for (int i = tid; i < n_done; i += nt) kv_done[i] = 0;
   __syncthreads();
   for (int s = tid; s < nseq; s += nt) {
     int32_t L = N, tok0 = s * N;
@@ -183,15 +210,20 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int32_t* __restric
     t.pair_seq[p] = t.sorted[p - level_off[lo]];
     t.pair_qt[p] = lo;
   }
+  grid_dependents_launch();
 }
 
 cudaError_t launch_schedule(const int32_t* cu_seqlens, int32_t nseq, int32_t N, int64_t total_tokens,
-                            int64_t t_pad_max, const SeqTable& t, int32_t item_rows, cudaStream_t s) {
+                            int64_t t_pad_max, const SeqTable& t, int32_t item_rows, int32_t* kv_done,
+                            int32_t n_done, cudaStream_t s) {
   TraceScope tr("schedule", s);
   const int32_t max_items = (N + item_rows - 1) / item_rows;
-  schedule_kernel<<<1, 1024, 0, s>>>(cu_seqlens, nseq, N, total_tokens, t_pad_max, t, max_items, item_rows,
-                                     device_status_ptr());
-  return cudaGetLastError();
+  const size_t hist_bytes = static_cast<size_t>(3) * (max_items + 2) * 4;
+  if (hist_bytes <= 32768)
+    return launch_pdl(schedule_kernel<true>, dim3(1), dim3(1024), hist_bytes, s, cu_seqlens, nseq, N, total_tokens,
+                      t_pad_max, t, max_items, item_rows, kv_done, n_done, device_status_ptr());
+  return launch_pdl(schedule_kernel<false>, dim3(1), dim3(1024), 0, s, cu_seqlens, nseq, N, total_tokens, t_pad_max,
+                    t, max_items, item_rows, kv_done, n_done, device_status_ptr());
 }
 
 // ---------------------------------------------------------------- K channel mean
@@ -204,31 +236,59 @@ __device__ __forceinline__ int64_t row_offset(bool varlen, int32_t s, int32_t h,
 // One CTA per (64-token chunk, kv head, sequence), one thread per channel:
 //   k_partials (nullable): fp32 sum of the chunk's K values per channel, in token order;
 //   v_partials (nullable): max |V| over the chunk (V is bf16 whenever this is asked for).
-template <sl8_dtype DT>
-__global__ void kv_stats_partial_kernel(const void* __restrict__ k, const void* __restrict__ v, bool varlen,
-                                        int32_t Hkv, int32_t N, int32_t d, const int32_t* __restrict__ len,
-                                        const int32_t* __restrict__ tok0, float* __restrict__ k_partials,
-                                        float* __restrict__ v_partials, int32_t max_chunks) {
+// The chunk's loads are issued kBatch at a time before they are summed in order.  The
+// last CTA of a (sequence, kv head) to finish (counted in done) then forms the K mean
+// = (chunk sums added in chunk order) / L, and the power-of-two exponent e >= 0 with
+// max|V| * 2^-e <= 2^15, so that V * 2^-e is exact in fp16 (up to fp16 subnormals)
+// and cannot overflow.
+template <sl8_dtype DT, int kMaxThreads>
+__global__ void __launch_bounds__(kMaxThreads) kv_stats_kernel(
+    const void* __restrict__ k, const void* __restrict__ v, bool varlen, int32_t Hkv, int32_t N, int32_t d,
+    const int32_t* __restrict__ len, const int32_t* __restrict__ tok0, float* __restrict__ k_partials,
+    float* __restrict__ v_partials, int32_t max_chunks, float* __restrict__ mean, int32_t* __restrict__ v_exp,
+    int32_t* __restrict__ done) {
+  constexpr int kBatch = kMaxThreads <= 256 ? 32 : 16;
   __shared__ float s_max[32];
+  __shared__ int s_last;
+  grid_dependency_wait();
   const int ch = blockIdx.x, h = blockIdx.y, s = blockIdx.z, c = threadIdx.x;
   const int L = len[s];
   const int t0 = ch * kMeanChunk;
   if (t0 >= L) return;
   const int t1 = min(t0 + kMeanChunk, L);
+  const int nch = (L + kMeanChunk - 1) / kMeanChunk;
   const int32_t base = varlen ? tok0[s] : 0;
   const bool active = c < d;
-  const int64_t slot = (static_cast<int64_t>(s) * Hkv + h) * max_chunks + ch;
+  const int64_t row = static_cast<int64_t>(s) * Hkv + h;
+  const int64_t slot = row * max_chunks + ch;
+  // element (t0 + i, c) sits at row_offset(t0) + c + i * stride
+  const int64_t e0 = row_offset(varlen, s, h, t0, Hkv, N, d, base) + c;
+  const int stride = varlen ? Hkv * d : d;
   if (k_partials && active) {
     float part = 0.0f;
-    for (int t = t0; t < t1; ++t)
-      part = __fadd_rn(part, load_elem<DT>(k, row_offset(varlen, s, h, t, Hkv, N, d, base) + c));
+    for (int tb = 0; tb < t1 - t0; tb += kBatch) {
+      float x[kBatch];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i)
+        x[i] = tb + i < t1 - t0 ? load_elem<DT>(k, e0 + static_cast<int64_t>((tb + i) * stride)) : 0.0f;
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i)
+        if (tb + i < t1 - t0) part = __fadd_rn(part, x[i]);
+    }
     k_partials[slot * d + c] = part;
   }
   if (v_partials) {
     float m = 0.0f;
-    if (active)
-      for (int t = t0; t < t1; ++t)
-        m = fmaxf(m, fabsf(load_elem<SL8_BF16>(v, row_offset(varlen, s, h, t, Hkv, N, d, base) + c)));
+    if (active) {
+      for (int tb = 0; tb < t1 - t0; tb += kBatch) {
+        float x[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i)
+          x[i] = tb + i < t1 - t0 ? load_elem<SL8_BF16>(v, e0 + static_cast<int64_t>((tb + i) * stride)) : 0.0f;
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) m = fmaxf(m, fabsf(x[i]));
+      }
+    }
     m = warp_max(m);
     if ((c & 31) == 0) s_max[c / 32] = m;
     __syncthreads();
@@ -237,174 +297,406 @@ __global__ void kv_stats_partial_kernel(const void* __restrict__ k, const void* 
       v_partials[slot] = m;
     }
   }
-}
-
-// One CTA per (kv head, sequence): K mean = (chunk sums added in chunk order) / L, and
-// the power-of-two exponent e >= 0 with max|V| * 2^-e <= 2^15, so that V * 2^-e is
-// exact in fp16 (up to fp16 subnormals) and cannot overflow.
-__global__ void kv_stats_finalize_kernel(const float* __restrict__ k_partials, const float* __restrict__ v_partials,
-                                         const int32_t* __restrict__ len, int32_t Hkv, int32_t d, int32_t max_chunks,
-                                         float* __restrict__ mean, int32_t* __restrict__ v_exp) {
-  const int h = blockIdx.x, s = blockIdx.y, c = threadIdx.x;
-  const int L = len[s];
-  const int nch = (L + kMeanChunk - 1) / kMeanChunk;
-  const int64_t row = static_cast<int64_t>(s) * Hkv + h;
-  if (k_partials && c < d) {
+  // ---- the last chunk of (s, h) finalises
+  __threadfence();
+  __syncthreads();
+  if (c == 0) s_last = atomicAdd(&done[row], 1) == nch - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (k_partials && active) {
     const float* p = k_partials + row * max_chunks * d + c;
     float total = 0.0f;
-    for (int ch = 0; ch < nch; ++ch) total = __fadd_rn(total, p[static_cast<int64_t>(ch) * d]);
-    mean[row * d + c] = L > 0 ? __fdiv_rn(total, static_cast<float>(L)) : 0.0f;
-  }
-  if (v_partials && c == 0) {
-    float m = 0.0f;
-    for (int ch = 0; ch < nch; ++ch) m = fmaxf(m, v_partials[row * max_chunks + ch]);
-    int e = 0;
-    if (m > 0.0f) {
-      int k2 = 0;
-      frexpf(m, &k2);  // m < 2^k2
-      e = k2 > 15 ? k2 - 15 : 0;
+    for (int cb = 0; cb < nch; cb += kBatch) {
+      float x[kBatch];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) x[i] = cb + i < nch ? p[static_cast<int64_t>(cb + i) * d] : 0.0f;
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i)
+        if (cb + i < nch) total = __fadd_rn(total, x[i]);
     }
-    v_exp[row] = e;
+    mean[row * d + c] = __fdiv_rn(total, static_cast<float>(L));
   }
+  if (v_partials) {
+    float m = 0.0f;
+    for (int cb = c; cb < nch; cb += blockDim.x) m = fmaxf(m, v_partials[row * max_chunks + cb]);
+    m = warp_max(m);
+    __syncthreads();
+    if ((c & 31) == 0) s_max[c / 32] = m;
+    __syncthreads();
+    if (c == 0) {
+      for (int w = 1; w < (static_cast<int>(blockDim.x) + 31) / 32; ++w) m = fmaxf(m, s_max[w]);
+      int e = 0;
+      if (m > 0.0f) {
+        int k2 = 0;
+        frexpf(m, &k2);  // m < 2^k2
+        e = k2 > 15 ? k2 - 15 : 0;
+      }
+      v_exp[row] = e;
+    }
+  }
+}
+
+// The same statistics with 16-byte loads: a thread owns VW consecutive channels of one
+// chunk (d / VW threads per chunk, 128 / (d / VW) chunks of one (sequence, kv head) per
+// CTA), so a CTA keeps 16 rows of 16-byte loads per thread in flight.  Each channel is
+// still summed in token order.  Requires d % VW == 0, d / VW <= 32 and V (if any) in
+// bf16 with K in a 16-bit type.
+template <sl8_dtype DT>
+__global__ void __launch_bounds__(128) kv_stats_vec_kernel(
+    const void* __restrict__ k, const void* __restrict__ v, bool varlen, int32_t Hkv, int32_t N, int32_t d,
+    const int32_t* __restrict__ len, const int32_t* __restrict__ tok0, float* __restrict__ k_partials,
+    float* __restrict__ v_partials, int32_t max_chunks, float* __restrict__ mean, int32_t* __restrict__ v_exp,
+    int32_t* __restrict__ done) {
+  constexpr int VW = DT == SL8_F32 ? 4 : 8;  // channels per 16-byte load
+  constexpr int kBatch = 16;
+  __shared__ float s_max[4];
+  __shared__ int s_last;
+  grid_dependency_wait();
+  const int tpi = d / VW, ipc = 128 / tpi;
+  const int h = blockIdx.y, s = blockIdx.z, tid = threadIdx.x;
+  const int item = tid / tpi, sub = tid % tpi;
+  const int L = len[s];
+  const int nch = (L + kMeanChunk - 1) / kMeanChunk;
+  const int n_cta = (nch + ipc - 1) / ipc;  // CTAs of (s, h) with work
+  if (static_cast<int>(blockIdx.x) >= n_cta) return;
+  const int ch = blockIdx.x * ipc + item;
+  const bool active = item < ipc && ch < nch;
+  const int64_t row = static_cast<int64_t>(s) * Hkv + h;
+  const int c0 = sub * VW;
+  float vmax = 0.0f;
+  if (active) {
+    const int t0 = ch * kMeanChunk, n = min(kMeanChunk, L - t0);
+    const int32_t base = varlen ? tok0[s] : 0;
+    const int64_t e0 = row_offset(varlen, s, h, t0, Hkv, N, d, base) + c0;
+    const int64_t stride = varlen ? static_cast<int64_t>(Hkv) * d : d;
+    const int64_t slot = row * max_chunks + ch;
+    if (k_partials) {
+      float part[VW];
+#pragma unroll
+      for (int e = 0; e < VW; ++e) part[e] = 0.0f;
+      for (int tb = 0; tb < n; tb += kBatch) {
+        uint4 w[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          w[i] = make_uint4(0u, 0u, 0u, 0u);
+          if (tb + i < n) {
+            const int64_t off = e0 + (tb + i) * stride;
+            w[i] = DT == SL8_F32 ? *reinterpret_cast<const uint4*>(static_cast<const float*>(k) + off)
+                                 : *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(k) + off);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          if (tb + i >= n) continue;
+          const uint32_t ww[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+          for (int e = 0; e < VW; ++e) {
+            float x;
+            if constexpr (DT == SL8_F32) x = __uint_as_float(ww[e]);
+            else {
+              const uint32_t b = (e & 1) ? ww[e / 2] >> 16 : ww[e / 2] & 0xffffu;
+              x = DT == SL8_BF16 ? bf16_bits_to_float(b) : f16_bits_to_float(b);
+            }
+            part[e] = __fadd_rn(part[e], x);
+          }
+        }
+      }
+      float* dst = k_partials + slot * d + c0;
+#pragma unroll
+      for (int e = 0; e < VW; e += 4) *reinterpret_cast<float4*>(dst + e) = make_float4(part[e], part[e + 1], part[e + 2], part[e + 3]);
+    }
+    if (v_partials) {
+      for (int tb = 0; tb < n; tb += kBatch) {
+        uint4 w[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i)
+          w[i] = tb + i < n ? *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(v) + e0 + (tb + i) * stride)
+                            : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          const uint32_t ww[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            vmax = fmaxf(vmax, fmaxf(fabsf(bf16_bits_to_float(ww[e] & 0xffffu)), fabsf(bf16_bits_to_float(ww[e] >> 16))));
+        }
+      }
+    }
+  }
+  if (v_partials) {
+    // max over the tpi threads of one chunk (aligned groups of lanes)
+    for (int o = tpi / 2; o > 0; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+    if (active && sub == 0) v_partials[row * max_chunks + ch] = vmax;
+  }
+  // ---- the last CTA of (s, h) finalises
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(&done[row], 1) == n_cta - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (k_partials) {
+    for (int c = tid; c < d; c += blockDim.x) {
+      const float* p = k_partials + row * max_chunks * d + c;
+      float total = 0.0f;
+      for (int cb = 0; cb < nch; cb += kBatch) {
+        float x[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) x[i] = cb + i < nch ? p[static_cast<int64_t>(cb + i) * d] : 0.0f;
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i)
+          if (cb + i < nch) total = __fadd_rn(total, x[i]);
+      }
+      mean[row * d + c] = __fdiv_rn(total, static_cast<float>(L));
+    }
+  }
+  if (v_partials) {
+    float m = 0.0f;
+    for (int cb = tid; cb < nch; cb += blockDim.x) m = fmaxf(m, v_partials[row * max_chunks + cb]);
+    m = warp_max(m);
+    if ((tid & 31) == 0) s_max[tid / 32] = m;
+    __syncthreads();
+    if (tid == 0) {
+      for (int w = 1; w < 4; ++w) m = fmaxf(m, s_max[w]);
+      int e = 0;
+      if (m > 0.0f) {
+        int k2 = 0;
+        frexpf(m, &k2);  // m < 2^k2
+        e = k2 > 15 ? k2 - 15 : 0;
+      }
+      v_exp[row] = e;
+    }
+  }
+}
+
+template <sl8_dtype DT>
+static cudaError_t launch_kv_stats_dt(const void* k, const void* v, bool varlen, int32_t nseq, int32_t Hkv, int32_t N,
+                                      int32_t d, const int32_t* len, const int32_t* tok0, float* k_partials,
+                                      float* v_partials, int32_t max_chunks, float* mean, int32_t* v_exp,
+                                      int32_t* done, cudaStream_t s) {
+  constexpr int VW = DT == SL8_F32 ? 4 : 8;
+  if (d % VW == 0 && d / VW <= 32 && (!v || DT != SL8_F32)) {
+    const int ipc = 128 / (d / VW);
+    return launch_pdl(kv_stats_vec_kernel<DT>, dim3((max_chunks + ipc - 1) / ipc, Hkv, nseq), dim3(128), 0, s, k, v,
+                      varlen, Hkv, N, d, len, tok0, k_partials, v_partials, max_chunks, mean, v_exp, done);
+  }
+  const dim3 grid(max_chunks, Hkv, nseq);
+  const int threads = (d + 31) / 32 * 32;
+  if (threads <= 256)
+    return launch_pdl(kv_stats_kernel<DT, 256>, grid, dim3(threads), 0, s, k, v, varlen, Hkv, N, d, len, tok0,
+                      k_partials, v_partials, max_chunks, mean, v_exp, done);
+  return launch_pdl(kv_stats_kernel<DT, 1024>, grid, dim3(threads), 0, s, k, v, varlen, Hkv, N, d, len, tok0,
+                    k_partials, v_partials, max_chunks, mean, v_exp, done);
 }
 
 cudaError_t launch_kv_stats(const void* k, sl8_dtype dt, const void* v, bool varlen, int32_t nseq, int32_t Hkv,
                             int32_t N, int32_t d, const int32_t* len, const int32_t* tok0, float* k_partials,
-                            float* v_partials, int32_t max_chunks, float* mean, int32_t* v_exp, cudaStream_t s) {
-  {
-    TraceScope tr("kv_stats_partial", s);
-    dim3 grid(max_chunks, Hkv, nseq);
-    const int threads = (d + 31) / 32 * 32;
-    switch (dt) {
-      case SL8_BF16: kv_stats_partial_kernel<SL8_BF16><<<grid, threads, 0, s>>>(k, v, varlen, Hkv, N, d, len, tok0, k_partials, v_partials, max_chunks); break;
-      case SL8_F16: kv_stats_partial_kernel<SL8_F16><<<grid, threads, 0, s>>>(k, v, varlen, Hkv, N, d, len, tok0, k_partials, v_partials, max_chunks); break;
-      default: kv_stats_partial_kernel<SL8_F32><<<grid, threads, 0, s>>>(k, v, varlen, Hkv, N, d, len, tok0, k_partials, v_partials, max_chunks); break;
-    }
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+                            float* v_partials, int32_t max_chunks, float* mean, int32_t* v_exp, int32_t* kv_done,
+                            cudaStream_t s) {
+  TraceScope tr("kv_stats", s);
+  switch (dt) {
+    case SL8_BF16: return launch_kv_stats_dt<SL8_BF16>(k, v, varlen, nseq, Hkv, N, d, len, tok0, k_partials, v_partials, max_chunks, mean, v_exp, kv_done, s);
+    case SL8_F16: return launch_kv_stats_dt<SL8_F16>(k, v, varlen, nseq, Hkv, N, d, len, tok0, k_partials, v_partials, max_chunks, mean, v_exp, kv_done, s);
+    default: return launch_kv_stats_dt<SL8_F32>(k, v, varlen, nseq, Hkv, N, d, len, tok0, k_partials, v_partials, max_chunks, mean, v_exp, kv_done, s);
   }
-  TraceScope tr("kv_stats_finalize", s);
-  kv_stats_finalize_kernel<<<dim3(Hkv, nseq), (d + 31) / 32 * 32, 0, s>>>(k_partials, v_partials, len, Hkv, d,
-                                                                           max_chunks, mean, v_exp);
-  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- prefill codes
-// One warp quantises one row of d = 32 * EPL values.  Rows live in the padded code
-// workspace [H][t_pad][d]; padded rows past a sequence's end are written as zeros.
+// Q and K rows in one launch (blockIdx.y < Hq: Q heads; the rest: K heads), each warp
+// quantising kQuantRowsPerWarp rows with all of their loads issued first.  Rows live in
+// the padded code workspace [H][t_pad][d]; padded rows past a sequence's end are
+// written as zeros.  For K rows with v16 set (V bf16), the warp also writes the same
+// row of V as fp16, scaled by the sequence/head's 2^-v_exp (exact), into v16
+// [Hkv][t_pad][d].
 constexpr int kQuantWarps = 8;
-constexpr int kQuantRowsPerWarp = 4;
+constexpr int kQuantRowsPerWarp = 8;
 
-// With v16 set (the K pass when V is bf16), each warp also writes the same row of V
-// as fp16, scaled by the sequence/head's 2^-v_exp (exact), into v16 [H][t_pad][d].
-template <sl8_dtype DT, int EPL>
-__global__ void __launch_bounds__(kQuantWarps * 32) quant_codes_kernel(
-    const void* __restrict__ x, bool varlen, int32_t nseq, int32_t H, int32_t N, int64_t total_tokens, SeqTable t,
-    int64_t t_pad_max, const float* __restrict__ mean, uint16_t* __restrict__ codes, float* __restrict__ scales,
-    const void* __restrict__ v, const int32_t* __restrict__ v_exp, uint16_t* __restrict__ v16, DeviceStatus* st) {
-  constexpr int D = 32 * EPL;
-  const int h = blockIdx.y;
+struct QuantQK {
+  const void* q;
+  const void* k;
+  bool varlen;
+  int32_t nseq, Hq, Hkv, N;
+  int64_t total_tokens;
+  SeqTable t;
+  int64_t t_pad_max;
+  const float* mean;        // [nseq][Hkv][d] K mean (nullable)
+  uint16_t* q_codes;
+  float* q_scales;
+  uint16_t* k_codes;
+  float* k_scales;
+  const void* v;            // bf16 V when v16 is set
+  const int32_t* v_exp;
+  uint16_t* v16;
+};
+
+template <int EPL>
+__device__ __forceinline__ void store_vec16(uint16_t* p, const uint16_t (&h)[EPL]) {
+  if constexpr (EPL == 8) {
+    uint4 w; memcpy(&w, h, 16); *reinterpret_cast<uint4*>(p) = w;
+  } else if constexpr (EPL == 4) {
+    uint2 w; memcpy(&w, h, 8); *reinterpret_cast<uint2*>(p) = w;
+  } else {
+    uint32_t w; memcpy(&w, h, 4); *reinterpret_cast<uint32_t*>(p) = w;
+  }
+}
+
+// Eight lanes per row (EPL = D / 8 values each, 16-byte accesses), four rows per warp
+// instruction.
+template <sl8_dtype DT, int D>
+__global__ void __launch_bounds__(kQuantWarps * 32) quant_qk_kernel(const QuantQK a, DeviceStatus* st) {
+  constexpr int LPR = 8, EPL = D / LPR, NV = EPL / 8, RPP = 32 / LPR, P = kQuantRowsPerWarp / RPP;
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const bool is_k = static_cast<int>(blockIdx.y) >= a.Hq;
+  const int h = is_k ? blockIdx.y - a.Hq : blockIdx.y;
+  const int H = is_k ? a.Hkv : a.Hq;
+  const void* x = is_k ? a.k : a.q;
+  uint16_t* codes = is_k ? a.k_codes : a.q_codes;
+  float* scales = is_k ? a.k_scales : a.q_scales;
+  const float* mean = is_k ? a.mean : nullptr;
+  uint16_t* v16 = is_k ? a.v16 : nullptr;
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-  const int32_t rows_used = t.counts[1];
+  const int rsub = lane / LPR, part = lane % LPR;
+  // dense input: sequence s owns padded rows [s * tiles * 128, ...) and the table is
+  // arithmetic; varlen: look the rows up in the scheduler's table
+  const int64_t seq_rows = static_cast<int64_t>((a.N + kQTile - 1) / kQTile) * kPadRows;
+  const int64_t rows_used = a.varlen ? a.t.counts[1] : a.nseq * seq_rows;
   const int64_t row0 = (static_cast<int64_t>(blockIdx.x) * kQuantWarps + warp) * kQuantRowsPerWarp;
-  for (int r = 0; r < kQuantRowsPerWarp; ++r) {
-    const int64_t pr = row0 + r;
-    if (pr >= rows_used || pr >= t_pad_max) return;
-    // sequence owning padded row pr: the last s with pstart[s] <= pr
-    int lo = 0, hi = nseq - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) / 2;
-      if (t.pstart[mid] <= pr) lo = mid; else hi = mid - 1;
-    }
-    const int s = lo;
-    const int32_t tt = static_cast<int32_t>(pr - t.pstart[s]);
-    const int32_t L = t.len[s];
-    uint16_t* crow = codes + (static_cast<int64_t>(h) * t_pad_max + pr) * D + lane * EPL;
-    float* srow = scales + static_cast<int64_t>(h) * t_pad_max + pr;
-    bool valid = tt < L;
-    if (valid && varlen && static_cast<int64_t>(t.tok0[s]) + tt >= total_tokens) {
-      if (lane == 0) record_status(st, kStatusBadArg, 901);
-      valid = false;
-    }
-    uint16_t out[EPL];
-    float scale = 0.0f;
-    if (valid) {
-      float v[EPL];
-      load_vec16<DT, EPL>(x, row_offset(varlen, s, h, tt, H, N, D, t.tok0[s]) + lane * EPL, v);
-      if (mean) {
-        const float* mu = mean + (static_cast<int64_t>(s) * H + h) * D + lane * EPL;
+  // this lane's rows (one per pass): owning sequence, position, validity; then all loads
+  int sq[P], tt[P];
+  bool live[P], valid[P];
+  uint4 xw[P][NV], vw[P][NV];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) v[e] = __fsub_rn(v[e], mu[e]);
+  for (int p = 0; p < P; ++p) {
+    const int64_t pr = row0 + p * RPP + rsub;
+    live[p] = pr < rows_used && pr < a.t_pad_max;
+    valid[p] = false;
+    sq[p] = 0;
+    tt[p] = 0;
+    int32_t tk = 0;
+    if (live[p]) {
+      if (!a.varlen) {
+        sq[p] = static_cast<int>(pr / seq_rows);
+        tt[p] = static_cast<int32_t>(pr - sq[p] * seq_rows);
+        valid[p] = tt[p] < a.N;
+      } else {
+        // sequence owning padded row pr: the last s with pstart[s] <= pr
+        int lo = 0, hi = a.nseq - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) / 2;
+          if (a.t.pstart[mid] <= pr) lo = mid; else hi = mid - 1;
+        }
+        sq[p] = lo;
+        tt[p] = static_cast<int32_t>(pr - a.t.pstart[lo]);
+        tk = a.t.tok0[lo];
+        valid[p] = tt[p] < a.t.len[lo];
+        if (valid[p] && static_cast<int64_t>(tk) + tt[p] >= a.total_tokens) {
+          record_status(st, kStatusBadArg, 901);
+          valid[p] = false;
+        }
       }
-      float a = 0.0f;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) a = fmaxf(a, fabsf(v[e]));
-      a = warp_max(a);
-      scale = __fdiv_rn(a, 127.0f);
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) out[e] = scale == 0.0f ? 0 : code_to_bf16_bits(quant_code(v[e], scale));
-    } else {
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) out[e] = 0;
     }
-    if constexpr (EPL == 8) {
-      uint4 w; memcpy(&w, out, 16); *reinterpret_cast<uint4*>(crow) = w;
-    } else if constexpr (EPL == 4) {
-      uint2 w; memcpy(&w, out, 8); *reinterpret_cast<uint2*>(crow) = w;
-    } else {
-      uint32_t w; memcpy(&w, out, 4); *reinterpret_cast<uint32_t*>(crow) = w;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      xw[p][j] = make_uint4(0u, 0u, 0u, 0u);
+      vw[p][j] = make_uint4(0u, 0u, 0u, 0u);
     }
-    if (lane == 0) *srow = scale;
+    if (valid[p]) {
+      const int64_t off = row_offset(a.varlen, sq[p], h, tt[p], H, a.N, D, tk) + part * EPL;
+#pragma unroll
+      for (int j = 0; j < NV; ++j) {
+        xw[p][j] = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + off + 8 * j);
+        if (v16) vw[p][j] = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.v) + off + 8 * j);
+      }
+    }
+  }
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+    const int64_t pr = row0 + p * RPP + rsub;
+    float v[EPL];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const uint32_t ww[4] = {xw[p][j].x, xw[p][j].y, xw[p][j].z, xw[p][j].w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t b = (e & 1) ? ww[e / 2] >> 16 : ww[e / 2] & 0xffffu;
+        v[8 * j + e] = DT == SL8_BF16 ? bf16_bits_to_float(b) : f16_bits_to_float(b);
+      }
+    }
+    if (mean && valid[p]) {
+      const float* mu = mean + (static_cast<int64_t>(sq[p]) * H + h) * D + part * EPL;
+#pragma unroll
+      for (int e = 0; e < EPL; e += 4) {
+        const float4 m4 = *reinterpret_cast<const float4*>(mu + e);
+        v[e] = __fsub_rn(v[e], m4.x);
+        v[e + 1] = __fsub_rn(v[e + 1], m4.y);
+        v[e + 2] = __fsub_rn(v[e + 2], m4.z);
+        v[e + 3] = __fsub_rn(v[e + 3], m4.w);
+      }
+    }
+    float am = 0.0f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) am = fmaxf(am, fabsf(v[e]));
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    if (!live[p]) continue;
+    const float scale = valid[p] ? __fdiv_rn(am, 127.0f) : 0.0f;
+    const float rs = scale == 0.0f ? 0.0f : __frcp_rn(scale);
+    uint16_t* crow = codes + (static_cast<int64_t>(h) * a.t_pad_max + pr) * D + part * EPL;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float c0 = scale == 0.0f ? 0.0f : quant_code_rcp(v[8 * j + 2 * e], scale, rs);
+        const float c1 = scale == 0.0f ? 0.0f : quant_code_rcp(v[8 * j + 2 * e + 1], scale, rs);
+        o[e] = (__float_as_uint(c0) >> 16) | (__float_as_uint(c1) & 0xffff0000u);
+      }
+      *reinterpret_cast<uint4*>(crow + 8 * j) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (part == 0) scales[static_cast<int64_t>(h) * a.t_pad_max + pr] = scale;
     if (v16) {
-      uint16_t vo[EPL];
-      if (valid) {
-        float vv[EPL];
-        load_vec16<SL8_BF16, EPL>(v, row_offset(varlen, s, h, tt, H, N, D, t.tok0[s]) + lane * EPL, vv);
-        const float vscale = __int_as_float((127 - v_exp[static_cast<int64_t>(s) * H + h]) << 23);  // 2^-e
+      const float vscale =
+          valid[p] ? __int_as_float((127 - a.v_exp[static_cast<int64_t>(sq[p]) * H + h]) << 23) : 0.0f;  // 2^-e
+      uint16_t* vrow = v16 + (static_cast<int64_t>(h) * a.t_pad_max + pr) * D + part * EPL;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) vo[e] = __half_as_ushort(__float2half_rn(__fmul_rn(vv[e], vscale)));
-      } else {
+      for (int j = 0; j < NV; ++j) {
+        const uint32_t ww[4] = {vw[p][j].x, vw[p][j].y, vw[p][j].z, vw[p][j].w};
+        uint32_t o[4];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) vo[e] = 0;
-      }
-      uint16_t* vrow = v16 + (static_cast<int64_t>(h) * t_pad_max + pr) * D + lane * EPL;
-      if constexpr (EPL == 8) {
-        uint4 w; memcpy(&w, vo, 16); *reinterpret_cast<uint4*>(vrow) = w;
-      } else if constexpr (EPL == 4) {
-        uint2 w; memcpy(&w, vo, 8); *reinterpret_cast<uint2*>(vrow) = w;
-      } else {
-        uint32_t w; memcpy(&w, vo, 4); *reinterpret_cast<uint32_t*>(vrow) = w;
+        for (int e = 0; e < 4; ++e) {
+          const __half2 h2 = __floats2half2_rn(__fmul_rn(bf16_bits_to_float(ww[e] & 0xffffu), vscale),
+                                               __fmul_rn(bf16_bits_to_float(ww[e] >> 16), vscale));
+          o[e] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        *reinterpret_cast<uint4*>(vrow + 8 * j) = make_uint4(o[0], o[1], o[2], o[3]);
       }
     }
   }
 }
 
 template <sl8_dtype DT>
-static cudaError_t launch_quant_codes_dt(const void* x, bool varlen, int32_t nseq, int32_t H, int32_t N, int32_t d,
-                                         int64_t total_tokens, const SeqTable& t, int64_t t_pad_max,
-                                         const float* mean, uint16_t* codes, float* scales, const void* v,
-                                         const int32_t* v_exp, uint16_t* v16, cudaStream_t s) {
+static cudaError_t launch_quant_qk_dt(const QuantQK& a, int32_t d, int32_t n_heads, cudaStream_t s) {
   const int64_t rows_per_cta = kQuantWarps * kQuantRowsPerWarp;
-  dim3 grid(static_cast<unsigned>((t_pad_max + rows_per_cta - 1) / rows_per_cta), H);
+  const dim3 grid(static_cast<unsigned>((a.t_pad_max + rows_per_cta - 1) / rows_per_cta), n_heads);
   DeviceStatus* st = device_status_ptr();
   switch (d) {
-    case 64: quant_codes_kernel<DT, 2><<<grid, kQuantWarps * 32, 0, s>>>(x, varlen, nseq, H, N, total_tokens, t, t_pad_max, mean, codes, scales, v, v_exp, v16, st); break;
-    case 128: quant_codes_kernel<DT, 4><<<grid, kQuantWarps * 32, 0, s>>>(x, varlen, nseq, H, N, total_tokens, t, t_pad_max, mean, codes, scales, v, v_exp, v16, st); break;
-    default: quant_codes_kernel<DT, 8><<<grid, kQuantWarps * 32, 0, s>>>(x, varlen, nseq, H, N, total_tokens, t, t_pad_max, mean, codes, scales, v, v_exp, v16, st); break;
+    case 64: return launch_pdl(quant_qk_kernel<DT, 64>, grid, dim3(kQuantWarps * 32), 0, s, a, st);
+    case 128: return launch_pdl(quant_qk_kernel<DT, 128>, grid, dim3(kQuantWarps * 32), 0, s, a, st);
+    default: return launch_pdl(quant_qk_kernel<DT, 256>, grid, dim3(kQuantWarps * 32), 0, s, a, st);
   }
-  return cudaGetLastError();
 }
 
-cudaError_t launch_quant_codes(const void* x, sl8_dtype dt, bool varlen, int32_t nseq, int32_t H, int32_t N, int32_t d,
-                               int64_t total_tokens, const SeqTable& t, int64_t t_pad_max, const float* mean,
-                               uint16_t* codes, float* scales, const void* v, const int32_t* v_exp, uint16_t* v16,
-                               bool is_k, cudaStream_t s) {
-  TraceScope tr(is_k ? "quant_k" : "quant_q", s);
-  if (dt == SL8_BF16)
-    return launch_quant_codes_dt<SL8_BF16>(x, varlen, nseq, H, N, d, total_tokens, t, t_pad_max, mean, codes, scales,
-                                           v, v_exp, v16, s);
-  return launch_quant_codes_dt<SL8_F16>(x, varlen, nseq, H, N, d, total_tokens, t, t_pad_max, mean, codes, scales, v,
-                                        v_exp, v16, s);
+cudaError_t launch_quant_qk(const void* q, const void* k, sl8_dtype dt, bool varlen, int32_t nseq, int32_t Hq,
+                            int32_t Hkv, int32_t N, int32_t d, int64_t total_tokens, const SeqTable& t,
+                            int64_t t_pad_max, const float* mean, uint16_t* q_codes, float* q_scales,
+                            uint16_t* k_codes, float* k_scales, const void* v, const int32_t* v_exp, uint16_t* v16,
+                            cudaStream_t s) {
+  QuantQK a{q, k, varlen, nseq, Hq, Hkv, N, total_tokens, t, t_pad_max, mean, q_codes, q_scales,
+            k_codes, k_scales, v, v_exp, v16};
+  TraceScope tr("quant_qk", s);
+  return dt == SL8_BF16 ? launch_quant_qk_dt<SL8_BF16>(a, d, Hq + Hkv, s)
+                        : launch_quant_qk_dt<SL8_F16>(a, d, Hq + Hkv, s);
 }
 
 // ---------------------------------------------------------------- generic rowwise int8
@@ -427,11 +719,12 @@ __global__ void __launch_bounds__(256) quant_rowwise_kernel(const void* __restri
   }
   a = warp_max(a);
   const float s = __fdiv_rn(a, 127.0f);
+  const float rs = s == 0.0f ? 0.0f : __frcp_rn(s);
   int8_t* q = q_out + row * cols;
   for (int c = lane; c < cols; c += 32) {
     float v = load_elem<DT>(x, base + c);
     if (mu) v = __fsub_rn(v, mu[c]);
-    q[c] = s == 0.0f ? 0 : static_cast<int8_t>(quant_code(v, s));
+    q[c] = s == 0.0f ? 0 : static_cast<int8_t>(static_cast<int>(quant_code_rcp(v, s, rs)));
   }
   if (lane == 0) scale_out[row] = s;
 }

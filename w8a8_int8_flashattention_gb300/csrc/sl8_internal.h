@@ -29,7 +29,7 @@ struct SeqTable {
 
 // Carve-up of the prefill workspace (byte offsets from its base).
 struct PrefillWorkspace {
-  size_t q_codes, q_scales, k_codes, k_scales, v16, k_mean, k_partials, v_partials, v_exp;
+  size_t q_codes, q_scales, k_codes, k_scales, v16, k_mean, k_partials, v_partials, v_exp, kv_done;
   size_t pstart, len, tok0, pair_seq, pair_qt, counts, hist, sorted;
   size_t total;
   int64_t t_pad_max;   // rows reserved per head in the code workspace
@@ -53,26 +53,49 @@ struct TraceScope {
   cudaStream_t stream;
 };
 
+// Launch with programmatic stream serialization: the kernel may start while the
+// previous kernel of the stream finishes, and must call grid_dependency_wait() before
+// it touches that kernel's results (every kernel launched this way does so first).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---- launchers (return a cudaError_t from the launch)
 // cu_seqlens (nullable = dense) must describe sequences inside [0, total_tokens) whose
 // padded rows fit in t_pad_max; violations are recorded as a device-side argument
 // error and the affected work is dropped.
 // Work-list items are `item_rows` (a multiple of 128) consecutive query rows.
+// kv_done [n_done] (the K/V statistics kernel's completion counters) is zeroed too.
 cudaError_t launch_schedule(const int32_t* cu_seqlens, int32_t nseq, int32_t N, int64_t total_tokens,
-                            int64_t t_pad_max, const SeqTable& t, int32_t item_rows, cudaStream_t s);
+                            int64_t t_pad_max, const SeqTable& t, int32_t item_rows, int32_t* kv_done,
+                            int32_t n_done, cudaStream_t s);
 // Query rows per work-list item of the prefill kernel for head dim d.
 int prefill_item_rows(int d);
-// K chunk sums (k_partials, nullable) and V chunk abs-max (v_partials, nullable; V bf16),
-// then the K mean [nseq][Hkv][d] and the V power-of-two exponent [nseq][Hkv].
+// K chunk sums (k_partials, nullable) and V chunk abs-max (v_partials, nullable; V bf16);
+// the last chunk of each (sequence, kv head) to finish forms the K mean [nseq][Hkv][d]
+// and the V power-of-two exponent [nseq][Hkv].  kv_done [nseq][Hkv] must be zero.
 cudaError_t launch_kv_stats(const void* k, sl8_dtype dt, const void* v, bool varlen, int32_t nseq, int32_t Hkv,
                             int32_t N, int32_t d, const int32_t* len, const int32_t* tok0, float* k_partials,
-                            float* v_partials, int32_t max_chunks, float* mean, int32_t* v_exp, cudaStream_t s);
-// Quantise Q or K rows of the caller's tensor into the padded bf16-code workspace; with
-// v16 set (K pass, V bf16) also write V as fp16 * 2^-v_exp into the padded layout.
-cudaError_t launch_quant_codes(const void* x, sl8_dtype dt, bool varlen, int32_t nseq, int32_t H, int32_t N,
-                               int32_t d, int64_t total_tokens, const SeqTable& t, int64_t t_pad_max,
-                               const float* mean, uint16_t* codes, float* scales, const void* v,
-                               const int32_t* v_exp, uint16_t* v16, bool is_k, cudaStream_t s);
+                            float* v_partials, int32_t max_chunks, float* mean, int32_t* v_exp, int32_t* kv_done,
+                            cudaStream_t s);
+// Q and K rows of prefill in one launch (K with the mean subtracted; V into v16 when set).
+cudaError_t launch_quant_qk(const void* q, const void* k, sl8_dtype dt, bool varlen, int32_t nseq, int32_t Hq,
+                            int32_t Hkv, int32_t N, int32_t d, int64_t total_tokens, const SeqTable& t,
+                            int64_t t_pad_max, const float* mean, uint16_t* q_codes, float* q_scales,
+                            uint16_t* k_codes, float* k_scales, const void* v, const int32_t* v_exp, uint16_t* v16,
+                            cudaStream_t s);
 cudaError_t launch_quant_rowwise(const void* x, sl8_dtype dt, int64_t rows, int32_t cols, int64_t row_stride,
                                  const float* sub_mean, int64_t rows_per_group, int8_t* q_out, float* scale_out,
                                  cudaStream_t s);
