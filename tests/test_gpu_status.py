@@ -66,5 +66,5 @@ def test_trace_records_kernels():
         rec = sl8.trace_collect()
     finally:
         sl8.trace_enable(False)
-    for name in ("schedule", "kv_stats", "quant_qk", "prefill_attn"):
+    for name in ("kv_partials", "quant_qk", "prefill_attn"):
         assert name in rec and rec[name][0] == 1 and rec[name][1] > 0

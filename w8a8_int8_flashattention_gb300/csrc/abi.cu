@@ -309,7 +309,7 @@ size_t sl8_attn_int8_fwd_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int3
 static int prefill_prepare(const void* q, const void* k, const void* v, int qk_dtype, int v_dtype, int32_t B,
                            int32_t Hq, int32_t Hkv, int32_t N, int32_t d, const int32_t* cu_seqlens,
                            int64_t total_tokens, int smooth_k, void* workspace, size_t workspace_bytes,
-                           cudaStream_t s, PrefillWorkspace* plan, SeqTable* table) {
+                           cudaStream_t s, bool want_table, PrefillWorkspace* plan, SeqTable* table) {
   const bool varlen = cu_seqlens != nullptr;
   const PrefillWorkspace p = plan_prefill_workspace(B, Hq, Hkv, N, d, varlen ? total_tokens : 0, varlen);
   SL8_CHECK(workspace && aligned16(workspace) && workspace_bytes >= p.total, SL8_ERR_WORKSPACE);
@@ -317,20 +317,21 @@ static int prefill_prepare(const void* q, const void* k, const void* v, int qk_d
   const SeqTable t = table_at(ws, p);
   const int64_t tokens = varlen ? total_tokens : static_cast<int64_t>(B) * N;
   const bool convert_v = v && v_dtype == SL8_BF16;
-  int32_t* kv_done = reinterpret_cast<int32_t*>(ws + p.kv_done);
-  SL8_LAUNCH(launch_schedule(cu_seqlens, B, N, tokens, p.t_pad_max, t, prefill_item_rows(d), kv_done, B * Hkv, s));
-  float* mean = smooth_k ? reinterpret_cast<float*>(ws + p.k_mean) : nullptr;
-  int32_t* v_exp = convert_v ? reinterpret_cast<int32_t*>(ws + p.v_exp) : nullptr;
-  if (smooth_k || convert_v) {
-    SL8_LAUNCH(launch_kv_stats(k, static_cast<sl8_dtype>(qk_dtype), convert_v ? v : nullptr, varlen, B, Hkv, N, d,
-                               t.len, t.tok0, smooth_k ? reinterpret_cast<float*>(ws + p.k_partials) : nullptr,
-                               convert_v ? reinterpret_cast<float*>(ws + p.v_partials) : nullptr, p.max_chunks, mean,
-                               v_exp, kv_done, s));
-  }
+  // the scheduler's table is needed for varlen input (and by the code export); dense
+  // input is laid out arithmetically
+  if (varlen || want_table)
+    SL8_LAUNCH(launch_schedule(cu_seqlens, B, N, tokens, p.t_pad_max, t, prefill_item_rows(d), nullptr, 0, s));
+  float* k_partials = smooth_k ? reinterpret_cast<float*>(ws + p.k_partials) : nullptr;
+  float* v_partials = convert_v ? reinterpret_cast<float*>(ws + p.v_partials) : nullptr;
+  if (smooth_k || convert_v)
+    SL8_LAUNCH(launch_kv_partials(k, static_cast<sl8_dtype>(qk_dtype), convert_v ? v : nullptr, varlen, B, Hkv, N, d,
+                                  varlen ? t.len : nullptr, varlen ? t.tok0 : nullptr, k_partials, v_partials,
+                                  p.max_chunks, s));
   SL8_LAUNCH(launch_quant_qk(q, k, static_cast<sl8_dtype>(qk_dtype), varlen, B, Hq, Hkv, N, d, tokens, t,
-                             p.t_pad_max, mean, reinterpret_cast<uint16_t*>(ws + p.q_codes),
-                             reinterpret_cast<float*>(ws + p.q_scales), reinterpret_cast<uint16_t*>(ws + p.k_codes),
-                             reinterpret_cast<float*>(ws + p.k_scales), convert_v ? v : nullptr, v_exp,
+                             p.t_pad_max, k_partials, v_partials, p.max_chunks,
+                             reinterpret_cast<uint16_t*>(ws + p.q_codes), reinterpret_cast<float*>(ws + p.q_scales),
+                             reinterpret_cast<uint16_t*>(ws + p.k_codes), reinterpret_cast<float*>(ws + p.k_scales),
+                             convert_v ? v : nullptr, convert_v ? reinterpret_cast<int32_t*>(ws + p.v_exp) : nullptr,
                              convert_v ? reinterpret_cast<uint16_t*>(ws + p.v16) : nullptr, s));
   *plan = p;
   *table = t;
@@ -354,7 +355,7 @@ int sl8_attn_int8_fwd(const void* q, const void* k, const void* v, int qk_dtype,
   PrefillWorkspace p;
   SeqTable t;
   rc = prefill_prepare(q, k, v, qk_dtype, v_dtype, B, Hq, Hkv, N, d, cu_seqlens, total_tokens, smooth_k, workspace,
-                       workspace_bytes, s, &p, &t);
+                       workspace_bytes, s, false, &p, &t);
   if (rc != SL8_OK) return rc;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   PrefillArgs a{};
@@ -377,6 +378,7 @@ int sl8_attn_int8_fwd(const void* q, const void* k, const void* v, int qk_dtype,
   a.total_tokens = a.varlen ? total_tokens : static_cast<int64_t>(B) * N;
   a.t_pad_max = p.t_pad_max;
   a.table = t;
+  a.dense_items = (N + prefill_item_rows(d) - 1) / prefill_item_rows(d);
   a.max_pairs = p.max_pairs;
   a.causal = causal != 0;
   a.out = out;
@@ -401,7 +403,7 @@ int sl8_attn_int8_qk_logits_debug(const void* q, const void* k, int qk_dtype, in
   PrefillWorkspace p;
   SeqTable t;
   rc = prefill_prepare(q, k, nullptr, qk_dtype, qk_dtype, B, Hq, Hkv, N, d, nullptr, 0, smooth_k, workspace,
-                       workspace_bytes, s, &p, &t);
+                       workspace_bytes, s, true, &p, &t);
   if (rc != SL8_OK) return rc;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   if (q_codes)
@@ -429,6 +431,7 @@ int sl8_attn_int8_qk_logits_debug(const void* q, const void* k, int qk_dtype, in
     a.total_tokens = static_cast<int64_t>(B) * N;
     a.t_pad_max = p.t_pad_max;
     a.table = t;
+    a.dense_items = (N + prefill_item_rows(d) - 1) / prefill_item_rows(d);
     a.max_pairs = p.max_pairs;
     a.causal = false;
     a.out = nullptr;

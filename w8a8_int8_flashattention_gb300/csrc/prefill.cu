@@ -113,17 +113,33 @@ struct Item {
   int32_t s, it, hq, hkv, L, pstart, tok0;
 };
 
+// Work item -> (sequence, item index, heads, extent).  Varlen input uses the scheduler's
+// longest-first list; dense input (every sequence N long) needs no table: pair p is item
+// index max_items - 1 - p / nseq of sequence p % nseq, which is the same order.
 __device__ __forceinline__ Item decode_item(const PrefillArgs& a, int64_t item, int group) {
   Item w;
   const int64_t pair = item / a.Hq;
   w.hq = static_cast<int32_t>(item - pair * a.Hq);
   w.hkv = w.hq / group;
-  w.s = a.table.pair_seq[pair];
-  w.it = a.table.pair_qt[pair];
-  w.L = a.table.len[w.s];
-  w.pstart = a.table.pstart[w.s];
-  w.tok0 = a.table.tok0[w.s];
+  if (a.varlen) {
+    w.s = a.table.pair_seq[pair];
+    w.it = a.table.pair_qt[pair];
+    w.L = a.table.len[w.s];
+    w.pstart = a.table.pstart[w.s];
+    w.tok0 = a.table.tok0[w.s];
+  } else {
+    const int64_t level = pair / a.nseq;
+    w.s = static_cast<int32_t>(pair - level * a.nseq);
+    w.it = a.dense_items - 1 - static_cast<int32_t>(level);
+    w.L = a.N;
+    w.pstart = w.s * ((a.N + kQTile - 1) / kQTile) * kPadRows;
+    w.tok0 = w.s * a.N;
+  }
   return w;
+}
+// Number of work items (pairs x query heads).
+__device__ __forceinline__ int64_t count_items(const PrefillArgs& a) {
+  return (a.varlen ? static_cast<int64_t>(a.table.counts[0]) : static_cast<int64_t>(a.nseq) * a.dense_items) * a.Hq;
 }
 
 // Key tiles of BN keys that Q tile qt (128 rows) visits; 0 if the tile is past the end.
@@ -391,7 +407,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const bool causal = kLogits ? false : a.causal;
   const int group = a.Hq / a.Hkv;
-  const int64_t n_items = static_cast<int64_t>(a.table.counts[0]) * a.Hq;
+  const int64_t n_items = count_items(a);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -661,7 +677,7 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const bool causal = kLogits ? false : a.causal;
   const int group = a.Hq / a.Hkv;
-  const int64_t n_items = static_cast<int64_t>(a.table.counts[0]) * a.Hq;
+  const int64_t n_items = count_items(a);
 
   if (threadIdx.x == 0) {
     mbar_init(&bars.q_full, 1);

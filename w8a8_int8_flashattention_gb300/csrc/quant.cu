@@ -501,6 +501,104 @@ cudaError_t launch_kv_stats(const void* k, sl8_dtype dt, const void* v, bool var
   }
 }
 
+// ---------------------------------------------------------------- prefill K/V partials
+// One CTA per (64-token chunk, kv head, sequence): the chunk's K rows (and V rows when
+// v_partials is set) are staged in shared memory with bulk copies, then thread c sums
+// channel c in token order into k_partials and the CTA takes max |V| into v_partials.
+// Dense input (len == nullptr): every sequence is N long.  The mean and the V exponent
+// are formed by the K quantisation CTAs.  d * sizeof(element) must be a multiple of 16.
+template <sl8_dtype DT>
+__global__ void kv_partials_kernel(const void* __restrict__ k, const void* __restrict__ v, bool varlen, int32_t Hkv,
+                                   int32_t N, int32_t d, const int32_t* __restrict__ len,
+                                   const int32_t* __restrict__ tok0, float* __restrict__ k_partials,
+                                   float* __restrict__ v_partials, int32_t max_chunks, uint64_t limit_ns,
+                                   DeviceStatus* st) {
+  extern __shared__ __align__(128) uint8_t stage[];
+  __shared__ uint64_t bar;
+  __shared__ float s_max[32];
+  constexpr int ES = DT == SL8_F32 ? 4 : 2;
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const int ch = blockIdx.x, h = blockIdx.y, s = blockIdx.z, c = threadIdx.x;
+  const int L = len ? len[s] : N;
+  const int t0 = ch * kMeanChunk;
+  if (t0 >= L) return;
+  const int n = min(kMeanChunk, L - t0);
+  const int32_t base = varlen ? tok0[s] : 0;
+  const uint32_t row_bytes = static_cast<uint32_t>(d) * ES;
+  uint8_t* sk = stage;
+  uint8_t* sv = stage + kMeanChunk * row_bytes;
+  if (c == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (c < 32) {
+    const uint32_t tx = static_cast<uint32_t>(n) * row_bytes * ((k_partials ? 1u : 0u) + (v_partials ? 1u : 0u));
+    if (c == 0) mbar_arrive_expect_tx(&bar, tx);
+    __syncwarp();
+    if (!varlen) {  // the chunk's rows are contiguous
+      if (c == 0) {
+        const int64_t e0 = row_offset(false, s, h, t0, Hkv, N, d, 0);
+        if (k_partials) bulk_load(sk, static_cast<const uint8_t*>(k) + e0 * ES, n * row_bytes, &bar);
+        if (v_partials) bulk_load(sv, static_cast<const uint8_t*>(v) + e0 * 2, n * row_bytes, &bar);
+      }
+    } else {
+      for (int i = c; i < n; i += 32) {
+        const int64_t e = row_offset(true, s, h, t0 + i, Hkv, N, d, base);
+        if (k_partials) bulk_load(sk + i * row_bytes, static_cast<const uint8_t*>(k) + e * ES, row_bytes, &bar);
+        if (v_partials) bulk_load(sv + i * row_bytes, static_cast<const uint8_t*>(v) + e * 2, row_bytes, &bar);
+      }
+    }
+  }
+  const bool ok = mbar_wait(&bar, 0, limit_ns, st, 903);
+  const int64_t slot = (static_cast<int64_t>(s) * Hkv + h) * max_chunks + ch;
+  if (k_partials && ok && c < d) {
+    float part = 0.0f;
+    for (int i = 0; i < n; ++i) {
+      const uint8_t* p = sk + i * row_bytes + c * ES;
+      const float x = DT == SL8_F32 ? *reinterpret_cast<const float*>(p)
+                    : DT == SL8_BF16 ? bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(p))
+                                     : f16_bits_to_float(*reinterpret_cast<const uint16_t*>(p));
+      part = __fadd_rn(part, x);
+    }
+    k_partials[slot * d + c] = part;
+  }
+  if (v_partials) {
+    float m = 0.0f;
+    if (ok && c < d)
+      for (int i = 0; i < n; ++i)
+        m = fmaxf(m, fabsf(bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(sv + i * row_bytes + c * 2))));
+    m = warp_max(m);
+    if ((c & 31) == 0) s_max[c / 32] = m;
+    __syncthreads();
+    if (c == 0) {
+      for (int w = 1; w < (static_cast<int>(blockDim.x) + 31) / 32; ++w) m = fmaxf(m, s_max[w]);
+      v_partials[slot] = m;
+    }
+  }
+}
+
+cudaError_t launch_kv_partials(const void* k, sl8_dtype dt, const void* v, bool varlen, int32_t nseq, int32_t Hkv,
+                               int32_t N, int32_t d, const int32_t* len, const int32_t* tok0, float* k_partials,
+                               float* v_partials, int32_t max_chunks, cudaStream_t s) {
+  TraceScope tr("kv_partials", s);
+  const int es = dt == SL8_F32 ? 4 : 2;
+  const size_t smem = static_cast<size_t>(kMeanChunk) * d * es * (v_partials ? 2 : 1);
+  const dim3 grid(max_chunks, Hkv, nseq), block((d + 31) / 32 * 32);
+  auto go = [&](auto kern) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    return launch_pdl(kern, grid, block, smem, s, k, v, varlen, Hkv, N, d, len, tok0, k_partials, v_partials,
+                      max_chunks, spin_limit_ns(), device_status_ptr());
+  };
+  switch (dt) {
+    case SL8_BF16: return go(kv_partials_kernel<SL8_BF16>);
+    case SL8_F16: return go(kv_partials_kernel<SL8_F16>);
+    default: return go(kv_partials_kernel<SL8_F32>);
+  }
+}
+
 // ---------------------------------------------------------------- prefill codes
 // Q and K rows in one launch (blockIdx.y < Hq: Q heads; the rest: K heads), each warp
 // quantising kQuantRowsPerWarp rows with all of their loads issued first.  Rows live in
@@ -519,13 +617,15 @@ struct QuantQK {
   int64_t total_tokens;
   SeqTable t;
   int64_t t_pad_max;
-  const float* mean;        // [nseq][Hkv][d] K mean (nullable)
+  const float* k_partials;  // [nseq][Hkv][max_chunks][d] K chunk sums (nullable: no smoothing)
+  const float* v_partials;  // [nseq][Hkv][max_chunks] V chunk abs-max (with v16)
+  int32_t max_chunks;
+  int32_t* v_exp_out;       // [nseq][Hkv] written by the first K CTA of each (s, h)
   uint16_t* q_codes;
   float* q_scales;
   uint16_t* k_codes;
   float* k_scales;
   const void* v;            // bf16 V when v16 is set
-  const int32_t* v_exp;
   uint16_t* v16;
 };
 
@@ -547,13 +647,16 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quant_qk_kernel(const QuantQ
   constexpr int LPR = 8, EPL = D / LPR, NV = EPL / 8, RPP = 32 / LPR, P = kQuantRowsPerWarp / RPP;
   grid_dependency_wait();
   grid_dependents_launch();
+  __shared__ __align__(16) float s_mean[D];
+  __shared__ float s_vm[kQuantWarps];
+  __shared__ int s_vexp;
   const bool is_k = static_cast<int>(blockIdx.y) >= a.Hq;
   const int h = is_k ? blockIdx.y - a.Hq : blockIdx.y;
   const int H = is_k ? a.Hkv : a.Hq;
   const void* x = is_k ? a.k : a.q;
   uint16_t* codes = is_k ? a.k_codes : a.q_codes;
   float* scales = is_k ? a.k_scales : a.q_scales;
-  const float* mean = is_k ? a.mean : nullptr;
+  const bool smooth = is_k && a.k_partials;
   uint16_t* v16 = is_k ? a.v16 : nullptr;
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const int rsub = lane / LPR, part = lane % LPR;
@@ -561,7 +664,64 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quant_qk_kernel(const QuantQ
   // arithmetic; varlen: look the rows up in the scheduler's table
   const int64_t seq_rows = static_cast<int64_t>((a.N + kQTile - 1) / kQTile) * kPadRows;
   const int64_t rows_used = a.varlen ? a.t.counts[1] : a.nseq * seq_rows;
-  const int64_t row0 = (static_cast<int64_t>(blockIdx.x) * kQuantWarps + warp) * kQuantRowsPerWarp;
+  const int64_t cta_row0 = static_cast<int64_t>(blockIdx.x) * kQuantWarps * kQuantRowsPerWarp;
+  const int64_t row0 = cta_row0 + static_cast<int64_t>(warp) * kQuantRowsPerWarp;
+  if (cta_row0 >= rows_used || cta_row0 >= a.t_pad_max) return;
+  // ---- K CTAs: the K mean of the CTA's sequence (its 64 rows never straddle two, as
+  // sequences start on 128-row boundaries) = chunk sums added in chunk order / L, and
+  // the V exponent e >= 0 with max|V| * 2^-e <= 2^15 (V * 2^-e exact in fp16)
+  if (is_k && (smooth || v16)) {
+    int s0 = 0, L0 = a.N;
+    if (!a.varlen) {
+      s0 = static_cast<int>(cta_row0 / seq_rows);
+    } else {
+      int lo = 0, hi = a.nseq - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (a.t.pstart[mid] <= cta_row0) lo = mid; else hi = mid - 1;
+      }
+      s0 = lo;
+      L0 = a.t.len[lo];
+    }
+    const int nch = (L0 + kMeanChunk - 1) / kMeanChunk;
+    const int64_t srow = static_cast<int64_t>(s0) * a.Hkv + h;
+    if (smooth) {
+      for (int c = threadIdx.x; c < D; c += blockDim.x) {
+        const float* p = a.k_partials + srow * a.max_chunks * D + c;
+        float total = 0.0f;
+        for (int cb = 0; cb < nch; cb += 16) {
+          float xx[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) xx[i] = cb + i < nch ? p[static_cast<int64_t>(cb + i) * D] : 0.0f;
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (cb + i < nch) total = __fadd_rn(total, xx[i]);
+        }
+        s_mean[c] = L0 > 0 ? __fdiv_rn(total, static_cast<float>(L0)) : 0.0f;
+      }
+    }
+    if (v16) {
+      float m = 0.0f;
+      for (int cb = threadIdx.x; cb < nch; cb += blockDim.x) m = fmaxf(m, a.v_partials[srow * a.max_chunks + cb]);
+      m = warp_max(m);
+      if (lane == 0) s_vm[warp] = m;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        for (int w = 1; w < kQuantWarps; ++w) m = fmaxf(m, s_vm[w]);
+        int e = 0;
+        if (m > 0.0f) {
+          int k2 = 0;
+          frexpf(m, &k2);  // m < 2^k2
+          e = k2 > 15 ? k2 - 15 : 0;
+        }
+        s_vexp = e;
+        // the CTA holding the sequence's first rows publishes it for the attention kernel
+        const int64_t first = a.varlen ? a.t.pstart[s0] : static_cast<int64_t>(s0) * seq_rows;
+        if (cta_row0 == first) a.v_exp_out[srow] = e;
+      }
+    }
+    __syncthreads();
+  }
   // this lane's rows (one per pass): owning sequence, position, validity; then all loads
   int sq[P], tt[P];
   bool live[P], valid[P];
@@ -623,8 +783,8 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quant_qk_kernel(const QuantQ
         v[8 * j + e] = DT == SL8_BF16 ? bf16_bits_to_float(b) : f16_bits_to_float(b);
       }
     }
-    if (mean && valid[p]) {
-      const float* mu = mean + (static_cast<int64_t>(sq[p]) * H + h) * D + part * EPL;
+    if (smooth && valid[p]) {
+      const float* mu = s_mean + part * EPL;
 #pragma unroll
       for (int e = 0; e < EPL; e += 4) {
         const float4 m4 = *reinterpret_cast<const float4*>(mu + e);
@@ -656,8 +816,7 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quant_qk_kernel(const QuantQ
     }
     if (part == 0) scales[static_cast<int64_t>(h) * a.t_pad_max + pr] = scale;
     if (v16) {
-      const float vscale =
-          valid[p] ? __int_as_float((127 - a.v_exp[static_cast<int64_t>(sq[p]) * H + h]) << 23) : 0.0f;  // 2^-e
+      const float vscale = valid[p] ? __int_as_float((127 - s_vexp) << 23) : 0.0f;  // 2^-e
       uint16_t* vrow = v16 + (static_cast<int64_t>(h) * a.t_pad_max + pr) * D + part * EPL;
 #pragma unroll
       for (int j = 0; j < NV; ++j) {
@@ -689,11 +848,11 @@ static cudaError_t launch_quant_qk_dt(const QuantQK& a, int32_t d, int32_t n_hea
 
 cudaError_t launch_quant_qk(const void* q, const void* k, sl8_dtype dt, bool varlen, int32_t nseq, int32_t Hq,
                             int32_t Hkv, int32_t N, int32_t d, int64_t total_tokens, const SeqTable& t,
-                            int64_t t_pad_max, const float* mean, uint16_t* q_codes, float* q_scales,
-                            uint16_t* k_codes, float* k_scales, const void* v, const int32_t* v_exp, uint16_t* v16,
-                            cudaStream_t s) {
-  QuantQK a{q, k, varlen, nseq, Hq, Hkv, N, total_tokens, t, t_pad_max, mean, q_codes, q_scales,
-            k_codes, k_scales, v, v_exp, v16};
+                            int64_t t_pad_max, const float* k_partials, const float* v_partials,
+                            int32_t max_chunks, uint16_t* q_codes, float* q_scales, uint16_t* k_codes,
+                            float* k_scales, const void* v, int32_t* v_exp, uint16_t* v16, cudaStream_t s) {
+  QuantQK a{q, k, varlen, nseq, Hq, Hkv, N, total_tokens, t, t_pad_max, k_partials, v_partials, max_chunks, v_exp,
+            q_codes, q_scales, k_codes, k_scales, v, v16};
   TraceScope tr("quant_qk", s);
   return dt == SL8_BF16 ? launch_quant_qk_dt<SL8_BF16>(a, d, Hq + Hkv, s)
                         : launch_quant_qk_dt<SL8_F16>(a, d, Hq + Hkv, s);

@@ -90,12 +90,19 @@ cudaError_t launch_kv_stats(const void* k, sl8_dtype dt, const void* v, bool var
                             int32_t N, int32_t d, const int32_t* len, const int32_t* tok0, float* k_partials,
                             float* v_partials, int32_t max_chunks, float* mean, int32_t* v_exp, int32_t* kv_done,
                             cudaStream_t s);
-// Q and K rows of prefill in one launch (K with the mean subtracted; V into v16 when set).
+// Prefill K chunk sums and V chunk abs-max (v_partials nullable), rows staged in shared
+// memory; len / tok0 nullable for dense input.
+cudaError_t launch_kv_partials(const void* k, sl8_dtype dt, const void* v, bool varlen, int32_t nseq, int32_t Hkv,
+                               int32_t N, int32_t d, const int32_t* len, const int32_t* tok0, float* k_partials,
+                               float* v_partials, int32_t max_chunks, cudaStream_t s);
+// Q and K rows of prefill in one launch.  K CTAs form the mean from k_partials (nullable:
+// no smoothing) and, with v16 set, the V exponent from v_partials (published in v_exp) and
+// write V as fp16 * 2^-v_exp.  t is read for varlen input only.
 cudaError_t launch_quant_qk(const void* q, const void* k, sl8_dtype dt, bool varlen, int32_t nseq, int32_t Hq,
                             int32_t Hkv, int32_t N, int32_t d, int64_t total_tokens, const SeqTable& t,
-                            int64_t t_pad_max, const float* mean, uint16_t* q_codes, float* q_scales,
-                            uint16_t* k_codes, float* k_scales, const void* v, const int32_t* v_exp, uint16_t* v16,
-                            cudaStream_t s);
+                            int64_t t_pad_max, const float* k_partials, const float* v_partials,
+                            int32_t max_chunks, uint16_t* q_codes, float* q_scales, uint16_t* k_codes,
+                            float* k_scales, const void* v, int32_t* v_exp, uint16_t* v16, cudaStream_t s);
 cudaError_t launch_quant_rowwise(const void* x, sl8_dtype dt, int64_t rows, int32_t cols, int64_t row_stride,
                                  const float* sub_mean, int64_t rows_per_group, int8_t* q_out, float* scale_out,
                                  cudaStream_t s);
@@ -116,7 +123,8 @@ struct PrefillArgs {
   int32_t nseq, Hq, Hkv, N, d;
   int64_t total_tokens;
   int64_t t_pad_max;
-  SeqTable table;
+  SeqTable table;            // varlen only: the dense layout is arithmetic
+  int32_t dense_items;       // items per sequence of a dense input (ceil(N / item rows))
   int64_t max_pairs;
   bool causal;
   void* out;                // caller's output
