@@ -151,99 +151,195 @@ __device__ __forceinline__ int tile_nkv(int qt, int L, bool causal) {
 }
 
 // ------------------------------------------------------------------ softmax step
-// One online-softmax step for this thread's query row over a BN-key S tile in TMEM:
-// dequantise (S * s_k[key], times alpha = s_q log2(e)/sqrt(d) folded into the
-// exponent), mask, update the running max m / sum l, write P (fp16) over the S
-// columns and, when the max grew by more than 2^8, scale the row's O in TMEM.
-// o_bar (nullable): barrier to wait on before touching O.  Returns false on timeout.
+// A softmax warp over TMEM lanes 32w..32w+31 works in the 16-lane fragment layout: its
+// thread (g = lane / 4, q = lane % 4) holds query rows 32w + {g, 8 + g, 16 + g, 24 + g}
+// (slot s = 2h + j: lane half h, low / high row j) and, of every 8-key group, keys 2q and
+// 2q + 1.  The quad (the four q of one g) together holds whole rows, so a row's max takes
+// two shuffles, and each thread needs only a quarter of the tile's K scales.
+struct QuadRows {
+  float m[4];      // running max, log2 units (times alpha)
+  float l[4];      // this thread's share of the running sum
+  float alpha[4];  // s_q log2(e) / sqrt(d)
+  int row[4];      // position of the row in its sequence
+};
+
+// Slot s of this thread: the row's offset within the warp's 32 lanes.
+__device__ __forceinline__ int quad_row(int s) {
+  return 16 * (s >> 1) + 8 * (s & 1) + ((threadIdx.x & 31) >> 2);
+}
+
+// Shared-memory position of key k's scale: thread q's scales (keys 8i + 2q + {0, 1}) are
+// 16-byte words (i / 2) * 4 + q, and the four q of one word index are adjacent.
+__device__ __forceinline__ int ks_slot(int k) {
+  const int i = k >> 3, q = (k >> 1) & 3;
+  return ((i >> 1) * 4 + q) * 4 + (i & 1) * 2 + (k & 1);
+}
+// ks[2i + e] = scale of key 8i + 2q + e.
+template <int BN>
+__device__ __forceinline__ void load_ks(const float* sks, float (&ks)[BN / 4]) {
+  const int q = threadIdx.x & 3;
+#pragma unroll
+  for (int w = 0; w < BN / 16; ++w) {
+    const float4 v = reinterpret_cast<const float4*>(sks)[w * 4 + q];
+    ks[4 * w] = v.x;
+    ks[4 * w + 1] = v.y;
+    ks[4 * w + 2] = v.z;
+    ks[4 * w + 3] = v.w;
+  }
+}
+
+// One online-softmax step over a BN-key S tile in TMEM (s_taddr: the warp's lane base and
+// the tile's first column): dequantise (S * s_k[key], alpha folded into the exponent),
+// mask, update each row's max m and sum l, write P (fp16) over the S columns and, when a
+// row's max grew by more than 2^8, scale the warp's O rows in TMEM.  o_bar (nullable):
+// barrier to wait on before touching O.  Returns false on timeout.
 template <int BN, int D>
-__device__ __forceinline__ bool softmax_step(uint32_t s_taddr, uint32_t o_taddr, const float* __restrict__ ks,
-                                             float alpha, bool need_mask, int key0, int row_abs, int L, bool causal,
-                                             bool first, float& m, float& l, uint64_t* o_bar, uint32_t o_parity,
-                                             uint64_t limit_ns, DeviceStatus* st) {
-  float x[BN];
+__device__ __forceinline__ bool softmax_step(uint32_t s_taddr, uint32_t o_taddr, const float (&ks)[BN / 4],
+                                             bool need_mask, int key0, int L, bool causal, bool first, QuadRows& rs,
+                                             uint64_t* o_bar, uint32_t o_parity, uint64_t limit_ns,
+                                             DeviceStatus* st) {
+  constexpr int G = BN / 8;  // 8-key groups
+  const int q = threadIdx.x & 3;
+  float x[2][4 * G];
 #pragma unroll
-  for (int c0 = 0; c0 < BN; c0 += 32) {
-    uint32_t v[32];
-    tmem_ld32(s_taddr + c0, v);
+  for (int h = 0; h < 2; ++h) {
 #pragma unroll
-    for (int c = 0; c < 32; ++c) x[c0 + c] = __uint_as_float(v[c]);
+    for (int c0 = 0; c0 < BN; c0 += 64) {
+      uint32_t v[32];
+      tmem_ld_q8(s_taddr + (static_cast<uint32_t>(16 * h) << 16) + c0, v);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) x[h][c0 / 2 + k] = __uint_as_float(v[k]);
+    }
   }
   tmem_wait_ld();
 #pragma unroll
-  for (int c = 0; c < BN; c += 4) {
-    const float4 k4 = *reinterpret_cast<const float4*>(ks + c);
-    upk2(mul2(pk2(x[c], x[c + 1]), pk2(k4.x, k4.y)), x[c], x[c + 1]);
-    upk2(mul2(pk2(x[c + 2], x[c + 3]), pk2(k4.z, k4.w)), x[c + 2], x[c + 3]);
+  for (int i = 0; i < G; ++i) {
+    const uint64_t k2 = pk2(ks[2 * i], ks[2 * i + 1]);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      upk2(mul2(pk2(x[h][4 * i], x[h][4 * i + 1]), k2), x[h][4 * i], x[h][4 * i + 1]);
+      upk2(mul2(pk2(x[h][4 * i + 2], x[h][4 * i + 3]), k2), x[h][4 * i + 2], x[h][4 * i + 3]);
+    }
   }
   if (need_mask) {
 #pragma unroll
-    for (int c = 0; c < BN; ++c) {
-      const int key = key0 + c;
-      if (!(key < L && (!causal || key <= row_abs))) x[c] = -INFINITY;
-    }
-  }
-  float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+    for (int h = 0; h < 2; ++h)
 #pragma unroll
-  for (int c = 0; c < BN; c += 8) {
-    m0 = max3(m0, x[c], x[c + 1]);
-    m1 = max3(m1, x[c + 2], x[c + 3]);
-    m2 = max3(m2, x[c + 4], x[c + 5]);
-    m3 = max3(m3, x[c + 6], x[c + 7]);
+      for (int i = 0; i < G; ++i)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int key = key0 + 8 * i + 2 * q + (c & 1), row = rs.row[2 * h + (c >> 1)];
+          if (!(key < L && (!causal || key <= row))) x[h][4 * i + c] = -INFINITY;
+        }
   }
-  const float m_tile = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * alpha;
-  float o_scale = 1.0f;
+  float mx[4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int h = s >> 1, j = s & 1;
+    float m0 = x[h][2 * j], m1 = x[h][2 * j + 1];
+#pragma unroll
+    for (int i = 1; i < G; i += 2) {
+      m0 = max3(m0, x[h][4 * i + 2 * j], x[h][4 * i + 2 * j + 1]);
+      if (i + 1 < G) m1 = max3(m1, x[h][4 * (i + 1) + 2 * j], x[h][4 * (i + 1) + 2 * j + 1]);
+    }
+    mx[s] = fmaxf(m0, m1);
+  }
+#pragma unroll
+  for (int s = 0; s < 4; ++s) mx[s] = fmaxf(mx[s], __shfl_xor_sync(0xffffffffu, mx[s], 1));
+#pragma unroll
+  for (int s = 0; s < 4; ++s) mx[s] = fmaxf(mx[s], __shfl_xor_sync(0xffffffffu, mx[s], 2));
+  float osc[4];
   bool rescale = false;
-  if (first) {
-    m = m_tile;
-  } else if (m_tile > m + kRescaleThreshold) {
-    o_scale = ex2(m - m_tile);
-    l *= o_scale;
-    m = m_tile;
-    rescale = true;
-  }
-  const uint64_t a2 = pk2(alpha, alpha), nm2 = pk2(-m, -m);
-  uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
-  for (int c0 = 0; c0 < BN; c0 += 32) {
-    uint32_t pw[16];
-#pragma unroll
-    for (int c = 0; c < 32; c += 2) {
-      float t0, t1;
-      upk2(fma2(pk2(x[c0 + c], x[c0 + c + 1]), a2, nm2), t0, t1);
-      const float e0 = ex2(t0), e1 = ex2(t1);
-      acc[(c / 2) & 3] = add2(acc[(c / 2) & 3], pk2(e0, e1));
-      pw[c / 2] = pack_half2(e0, e1);
+  for (int s = 0; s < 4; ++s) {
+    const float m_tile = mx[s] * rs.alpha[s];
+    osc[s] = 1.0f;
+    if (first) {
+      rs.m[s] = m_tile;
+    } else if (m_tile > rs.m[s] + kRescaleThreshold) {
+      osc[s] = ex2(rs.m[s] - m_tile);
+      rs.l[s] *= osc[s];
+      rs.m[s] = m_tile;
+      rescale = true;
     }
-    tmem_st16(s_taddr + c0 / 2, pw);
   }
-  float s0, s1, s2, s3, s4, s5, s6, s7;
-  upk2(acc[0], s0, s1);
-  upk2(acc[1], s2, s3);
-  upk2(acc[2], s4, s5);
-  upk2(acc[3], s6, s7);
-  l += ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+  uint64_t acc[4][2] = {{0, 0}, {0, 0}, {0, 0}, {0, 0}};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint64_t a_lo = pk2(rs.alpha[2 * h], rs.alpha[2 * h]), a_hi = pk2(rs.alpha[2 * h + 1], rs.alpha[2 * h + 1]);
+    const uint64_t n_lo = pk2(-rs.m[2 * h], -rs.m[2 * h]), n_hi = pk2(-rs.m[2 * h + 1], -rs.m[2 * h + 1]);
+#pragma unroll
+    for (int c0 = 0; c0 < BN; c0 += 64) {
+      uint32_t pw[16];
+#pragma unroll
+      for (int ii = 0; ii < 8; ++ii) {
+        const int i = c0 / 8 + ii;
+        float t0, t1, t2, t3;
+        upk2(fma2(pk2(x[h][4 * i], x[h][4 * i + 1]), a_lo, n_lo), t0, t1);
+        upk2(fma2(pk2(x[h][4 * i + 2], x[h][4 * i + 3]), a_hi, n_hi), t2, t3);
+        const float e0 = ex2(t0), e1 = ex2(t1), e2 = ex2(t2), e3 = ex2(t3);
+        acc[2 * h][ii & 1] = add2(acc[2 * h][ii & 1], pk2(e0, e1));
+        acc[2 * h + 1][ii & 1] = add2(acc[2 * h + 1][ii & 1], pk2(e2, e3));
+        pw[2 * ii] = pack_half2(e0, e1);
+        pw[2 * ii + 1] = pack_half2(e2, e3);
+      }
+      tmem_st_p8(s_taddr + (static_cast<uint32_t>(16 * h) << 16) + c0 / 2, pw);
+    }
+  }
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    float s0, s1, s2, s3;
+    upk2(acc[s][0], s0, s1);
+    upk2(acc[s][1], s2, s3);
+    rs.l[s] += (s0 + s1) + (s2 + s3);
+  }
   if (__any_sync(0xffffffffu, rescale)) {
     if (o_bar && !warp_wait(o_bar, o_parity, limit_ns, st, 31)) return false;
     tc_fence_after();
-    const uint64_t sc = pk2(o_scale, o_scale);
 #pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 16) {
-      uint32_t v[16];
-      tmem_ld16(o_taddr + c0, v);
-      tmem_wait_ld();
+    for (int h = 0; h < 2; ++h) {
+      const uint64_t sc_lo = pk2(osc[2 * h], osc[2 * h]), sc_hi = pk2(osc[2 * h + 1], osc[2 * h + 1]);
 #pragma unroll
-      for (int c = 0; c < 16; c += 2) {
-        float a, b;
-        upk2(mul2(pk2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), sc), a, b);
-        v[c] = __float_as_uint(a);
-        v[c + 1] = __float_as_uint(b);
+      for (int c0 = 0; c0 < D; c0 += 64) {
+        const uint32_t ta = o_taddr + (static_cast<uint32_t>(16 * h) << 16) + c0;
+        uint32_t v[32];
+        tmem_ld_q8(ta, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float a0, a1, a2, a3;
+          upk2(mul2(pk2(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1])), sc_lo), a0, a1);
+          upk2(mul2(pk2(__uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])), sc_hi), a2, a3);
+          v[4 * i] = __float_as_uint(a0);
+          v[4 * i + 1] = __float_as_uint(a1);
+          v[4 * i + 2] = __float_as_uint(a2);
+          v[4 * i + 3] = __float_as_uint(a3);
+        }
+        tmem_st_q8(ta, v);
       }
-      tmem_st16(o_taddr + c0, v);
     }
   }
   tmem_wait_st();
   return true;
+}
+
+// End of an item: complete each row's sum across its quad and give the thread on lane r
+// the max and sum of row 32w + r (the epilogue reads O one row per thread).
+__device__ __forceinline__ void quad_rows_to_lane(const QuadRows& rs, float& m, float& l) {
+  const int lane = threadIdx.x & 31, src = 4 * (lane & 7), slot = lane >> 3;
+  m = 0.0f;
+  l = 0.0f;
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    float ls = rs.l[s];
+    ls += __shfl_xor_sync(0xffffffffu, ls, 1);
+    ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+    const float mv = __shfl_sync(0xffffffffu, rs.m[s], src), lv = __shfl_sync(0xffffffffu, ls, src);
+    if (s == slot) {
+      m = mv;
+      l = lv;
+    }
+  }
 }
 
 // Debug: write this row's exact int32 logits (S of the tile) for keys < L.
@@ -466,8 +562,8 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
         }
       }
       if (!ok) *abort_flag = 1;
-    } else if (warp == 9 && lane == 0) {
-      // ---------------------------------------------------------- MMA issuer
+    } else if (warp == 9) {
+      // ---------------------------------------------------------- MMA issuer (whole warp, one lane issues)
       // Per key tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1): while one tile's softmax
       // runs, the tensor core works on the other tile.
       uint32_t g = 0, it = 0, np[2] = {0, 0};
@@ -476,9 +572,9 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
         const Item w = decode_item(a, item, group);
         const int nkv_t[2] = {tile_nkv<BN>(2 * w.it, w.L, causal), tile_nkv<BN>(2 * w.it + 1, w.L, causal)};
         const int nkv = max(nkv_t[0], nkv_t[1]);
-        ok = mbar_wait(&bars.q_full[0], it & 1, limit_ns, st, 20) &&
-             mbar_wait(&bars.q_full[1], it & 1, limit_ns, st, 20);
-        if (ok) ok = mbar_wait(&bars.k_full[g % C::kStages], (g / C::kStages) & 1, limit_ns, st, 21);
+        ok = warp_wait(&bars.q_full[0], it & 1, limit_ns, st, 20) &&
+             warp_wait(&bars.q_full[1], it & 1, limit_ns, st, 20);
+        if (ok) ok = warp_wait(&bars.k_full[g % C::kStages], (g / C::kStages) & 1, limit_ns, st, 21);
         if (!ok) break;
         tc_fence_after();
         {
@@ -498,9 +594,10 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
           bool v_ready = false, k_ready = false;
           for (int t = 0; t < 2 && ok; ++t) {
             if (j >= nkv_t[t]) continue;
-            ok = mbar_wait(&bars.p_full[t], np[t] & 1, limit_ns, st, 22);
+            ok = warp_wait(&bars.p_full[t], np[t] & 1, limit_ns, st, 22);
             ++np[t];
-            if (ok && !v_ready) ok = mbar_wait(&bars.v_full[gj % C::kStages], (gj / C::kStages) & 1, limit_ns, st, 23);
+            if (ok && !v_ready)
+              ok = warp_wait(&bars.v_full[gj % C::kStages], (gj / C::kStages) & 1, limit_ns, st, 23);
             if (!ok) break;
             v_ready = true;
             tc_fence_after();
@@ -509,7 +606,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
             if (j == nkv_t[t] - 1) mma_commit(&bars.o_done[t]);
             if (j + 1 < nkv_t[t]) {
               if (!k_ready) {
-                ok = mbar_wait(&bars.k_full[gn % C::kStages], (gn / C::kStages) & 1, limit_ns, st, 21);
+                ok = warp_wait(&bars.k_full[gn % C::kStages], (gn / C::kStages) & 1, limit_ns, st, 21);
                 if (!ok) break;
                 k_ready = true;
                 tc_fence_after();
@@ -529,15 +626,16 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
       if (!ok) *abort_flag = 1;
       if (issued) {
         mma_commit(&bars.drain);
-        mbar_wait(&bars.drain, 0, limit_ns, st, 24);
+        warp_wait(&bars.drain, 0, limit_ns, st, 24);
       }
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsSoftmax));
     const int t = warp / 4;                       // Q tile of this warpgroup
-    const int r = threadIdx.x - t * 128;          // query row within the tile = TMEM lane
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int r = threadIdx.x - t * 128;          // TMEM lane: the row this thread stores
+    const int wrow = (warp & 3) * 32;             // the warp's first row in the tile
+    const uint32_t lane_base = static_cast<uint32_t>(wrow) << 16;
     const uint32_t s_taddr = tbase + lane_base + t * 256;
     const uint32_t o_taddr = s_taddr + 128;
     float* sks = sks_all + t * 2 * BN;
@@ -552,10 +650,16 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
       if (tile_nkv<BN>(2 * w.it + t, w.L, causal) > 0) break;
       item += gridDim.x;
     }
-    float qs_next = 0.0f, ks_next = 0.0f;
+    // q scales of this thread's four softmax rows (the quad layout) for the next item
+    float qs_next[4] = {0.0f, 0.0f, 0.0f, 0.0f}, ks_next = 0.0f;
     int ve_next = 0;
+    auto load_qs = [&](const Item& x) {
+      const float* qs = a.q_scales + static_cast<int64_t>(x.hq) * a.t_pad_max + x.pstart + (2 * x.it + t) * kQTile;
+#pragma unroll
+      for (int s = 0; s < 4; ++s) qs_next[s] = qs[wrow + quad_row(s)];
+    };
     if (item < n_items) {
-      qs_next = a.q_scales[static_cast<int64_t>(w.hq) * a.t_pad_max + w.pstart + (2 * w.it + t) * kQTile + r];
+      load_qs(w);
       if (a.v_exp) ve_next = a.v_exp[static_cast<int64_t>(w.s) * a.Hkv + w.hkv];
       ks_next = a.k_scales[static_cast<int64_t>(w.hkv) * a.t_pad_max + w.pstart + r];
     }
@@ -563,7 +667,14 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
       const int qt = 2 * w.it + t;
       const int nkv = tile_nkv<BN>(qt, w.L, causal);
       const int row_abs = qt * kQTile + r;
-      const float alpha = fmaxf(qs_next * qk_scale, FLT_MIN);
+      QuadRows rs;
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        rs.m[s] = -INFINITY;
+        rs.l[s] = 0.0f;
+        rs.alpha[s] = fmaxf(qs_next[s] * qk_scale, FLT_MIN);
+        rs.row[s] = qt * kQTile + wrow + quad_row(s);
+      }
       const float v_unscale = __int_as_float((127 + ve_next) << 23);
       // the next item in which this warpgroup's tile exists
       int64_t item_n = item + gridDim.x;
@@ -573,21 +684,22 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
         if (tile_nkv<BN>(2 * wn.it + t, wn.L, causal) > 0) break;
         item_n += gridDim.x;
       }
-      float m = -INFINITY, l = 0.0f;
       for (int j = 0; j < nkv; ++j, ++ns) {
         const uint32_t buf = ns & 1;
-        sks[buf * BN + r] = ks_next;
+        sks[buf * BN + ks_slot(r)] = ks_next;
         if (j + 1 < nkv) {
           ks_next = a.k_scales[static_cast<int64_t>(w.hkv) * a.t_pad_max + w.pstart + (j + 1) * BN + r];
         } else if (item_n < n_items) {
           ks_next = a.k_scales[static_cast<int64_t>(wn.hkv) * a.t_pad_max + wn.pstart + r];
-          qs_next = a.q_scales[static_cast<int64_t>(wn.hq) * a.t_pad_max + wn.pstart + (2 * wn.it + t) * kQTile + r];
+          load_qs(wn);
           if (a.v_exp) ve_next = a.v_exp[static_cast<int64_t>(wn.s) * a.Hkv + wn.hkv];
         }
         if (wg_any(bad || *abort_flag, 1 + t)) {
           bad = true;
           break;
         }
+        float ks[BN / 4];
+        load_ks<BN>(sks + buf * BN, ks);
         if (!warp_wait(&bars.s_full[t], ns & 1, limit_ns, st, 30)) {
           bad = true;
           continue;
@@ -599,8 +711,8 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
         } else {
           const bool need_mask = (causal && key0 + BN - 1 > qt * kQTile) || (key0 + BN > w.L);
           // O_t is safe to touch: S_t(j) was issued after PV_t(j-1), and its commit covers it
-          if (!softmax_step<BN, D>(s_taddr, o_taddr, sks + buf * BN, alpha, need_mask, key0, row_abs, w.L, causal,
-                                   j == 0, m, l, nullptr, 0, limit_ns, st)) {
+          if (!softmax_step<BN, D>(s_taddr, o_taddr, ks, need_mask, key0, w.L, causal, j == 0, rs, nullptr, 0,
+                                   limit_ns, st)) {
             bad = true;
             continue;
           }
@@ -616,7 +728,11 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
         bad = true;
       } else {
         tc_fence_after();
-        if constexpr (!kLogits) store_row<D>(o_taddr, a, w, row_abs, m, l, v_unscale);
+        if constexpr (!kLogits) {
+          float m, l;
+          quad_rows_to_lane(rs, m, l);
+          store_row<D>(o_taddr, a, w, row_abs, m, l, v_unscale);
+        }
       }
       ++no;
       item = item_n;
@@ -732,8 +848,9 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
-    // S tiles run one ahead of P.V: S_{g+1} is issued before PV_g (two S buffers).
-    if (lane == 0) {
+    // S tiles run one ahead of P.V: S_{g+1} is issued before PV_g (two S buffers).  The
+    // whole warp runs this loop; one lane issues.
+    {
       int64_t item_s = blockIdx.x, item_p = blockIdx.x;
       uint32_t it_s = 0, gs = 0, gp = 0;
       int j_s = 0, j_p = 0;
@@ -746,9 +863,9 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
       bool ok = true, issued = false;
       while (ok && item_p < n_items && !*abort_flag) {
         while (ok && item_s < n_items && gs <= gp + 1) {
-          if (j_s == 0) ok = mbar_wait(&bars.q_full, it_s & 1, limit_ns, st, 20);
+          if (j_s == 0) ok = warp_wait(&bars.q_full, it_s & 1, limit_ns, st, 20);
           const uint32_t stg = gs % C::kStages;
-          if (ok) ok = mbar_wait(&bars.k_full[stg], (gs / C::kStages) & 1, limit_ns, st, 21);
+          if (ok) ok = warp_wait(&bars.k_full[stg], (gs / C::kStages) & 1, limit_ns, st, 21);
           if (!ok) break;
           tc_fence_after();
           issue_qk<D, BN>(tbase + (gs & 1) * BN, smem_u32(smem + C::kQOff),
@@ -769,9 +886,9 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
           }
         }
         if (!ok) break;
-        ok = mbar_wait(&bars.p_full[gp & 1], (gp >> 1) & 1, limit_ns, st, 22);
+        ok = warp_wait(&bars.p_full[gp & 1], (gp >> 1) & 1, limit_ns, st, 22);
         const uint32_t stg = gp % C::kStages;
-        if (ok) ok = mbar_wait(&bars.v_full[stg], (gp / C::kStages) & 1, limit_ns, st, 23);
+        if (ok) ok = warp_wait(&bars.v_full[stg], (gp / C::kStages) & 1, limit_ns, st, 23);
         if (!ok) break;
         tc_fence_after();
         issue_pv<D, BN>(tbase + C::kOCol, tbase + (gp & 1) * BN, smem_u32(smem + C::kVOff + stg * C::kKVBytes),
@@ -791,22 +908,29 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
       if (!ok) *abort_flag = 1;
       if (issued) {
         mma_commit(&bars.drain);
-        mbar_wait(&bars.drain, 0, limit_ns, st, 24);
+        warp_wait(&bars.drain, 0, limit_ns, st, 24);
       }
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroup (warps 0-3)
-    const int r = threadIdx.x;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int r = threadIdx.x;                    // TMEM lane: the row this thread stores
+    const int wrow = warp * 32;
+    const uint32_t lane_base = static_cast<uint32_t>(wrow) << 16;
     const float qk_scale = kLog2e * rsqrtf(static_cast<float>(D));
     int64_t item = blockIdx.x;
     Item w{};
     uint32_t g = 0;
-    float qs_next = 0.0f, ks_next = 0.0f;
+    // q scales of this thread's four softmax rows (the quad layout) for the next item
+    float qs_next[4] = {0.0f, 0.0f, 0.0f, 0.0f}, ks_next = 0.0f;
     int ve_next = 0;
+    auto load_qs = [&](const Item& x) {
+      const float* qs = a.q_scales + static_cast<int64_t>(x.hq) * a.t_pad_max + x.pstart + x.it * kQTile;
+#pragma unroll
+      for (int s = 0; s < 4; ++s) qs_next[s] = qs[wrow + quad_row(s)];
+    };
     if (item < n_items) {
       w = decode_item(a, item, group);
-      qs_next = a.q_scales[static_cast<int64_t>(w.hq) * a.t_pad_max + w.pstart + w.it * kQTile + r];
+      load_qs(w);
       if (a.v_exp) ve_next = a.v_exp[static_cast<int64_t>(w.s) * a.Hkv + w.hkv];
       if (r < BN) ks_next = a.k_scales[static_cast<int64_t>(w.hkv) * a.t_pad_max + w.pstart + r];
     }
@@ -814,26 +938,34 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
     while (item < n_items) {
       const int nkv = tile_nkv<BN>(w.it, w.L, causal);
       const int row_abs = w.it * kQTile + r;
-      const float alpha = fmaxf(qs_next * qk_scale, FLT_MIN);
+      QuadRows rs;
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        rs.m[s] = -INFINITY;
+        rs.l[s] = 0.0f;
+        rs.alpha[s] = fmaxf(qs_next[s] * qk_scale, FLT_MIN);
+        rs.row[s] = w.it * kQTile + wrow + quad_row(s);
+      }
       const float v_unscale = __int_as_float((127 + ve_next) << 23);
       const int64_t item_n = item + gridDim.x;
       Item wn{};
       if (item_n < n_items) wn = decode_item(a, item_n, group);
-      float m = -INFINITY, l = 0.0f;
       for (int j = 0; j < nkv; ++j, ++g) {
         const uint32_t buf = g & 1;
-        if (r < BN) sks[buf * BN + r] = ks_next;
+        if (r < BN) sks[buf * BN + ks_slot(r)] = ks_next;
         if (j + 1 < nkv) {
           if (r < BN) ks_next = a.k_scales[static_cast<int64_t>(w.hkv) * a.t_pad_max + w.pstart + (j + 1) * BN + r];
         } else if (item_n < n_items) {
           if (r < BN) ks_next = a.k_scales[static_cast<int64_t>(wn.hkv) * a.t_pad_max + wn.pstart + r];
-          qs_next = a.q_scales[static_cast<int64_t>(wn.hq) * a.t_pad_max + wn.pstart + wn.it * kQTile + r];
+          load_qs(wn);
           if (a.v_exp) ve_next = a.v_exp[static_cast<int64_t>(wn.s) * a.Hkv + wn.hkv];
         }
         if (wg_any(bad || *abort_flag, 1)) {
           bad = true;
           break;
         }
+        float ks[BN / 4];
+        load_ks<BN>(sks + buf * BN, ks);
         if (!warp_wait(&bars.s_full[buf], (g >> 1) & 1, limit_ns, st, 30)) {
           bad = true;
           continue;
@@ -847,9 +979,8 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
           const bool need_mask = (causal && key0 + BN - 1 > w.it * kQTile) || (key0 + BN > w.L);
           // here S_g was issued after PV_{g-2} only: wait for PV_{g-1} before touching O
           const uint32_t gprev = g - 1;
-          if (!softmax_step<BN, D>(s_taddr, tbase + lane_base + C::kOCol, sks + buf * BN, alpha, need_mask, key0,
-                                   row_abs, w.L, causal, j == 0, m, l, &bars.o_done[gprev & 1], (gprev >> 1) & 1,
-                                   limit_ns, st)) {
+          if (!softmax_step<BN, D>(s_taddr, tbase + lane_base + C::kOCol, ks, need_mask, key0, w.L, causal, j == 0,
+                                   rs, &bars.o_done[gprev & 1], (gprev >> 1) & 1, limit_ns, st)) {
             bad = true;
             continue;
           }
@@ -866,7 +997,11 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
         bad = true;
       } else {
         tc_fence_after();
-        if constexpr (!kLogits) store_row<D>(tbase + lane_base + C::kOCol, a, w, row_abs, m, l, v_unscale);
+        if constexpr (!kLogits) {
+          float m, l;
+          quad_rows_to_lane(rs, m, l);
+          store_row<D>(tbase + lane_base + C::kOCol, a, w, row_abs, m, l, v_unscale);
+        }
       }
       item = item_n;
       w = wn;
