@@ -479,14 +479,23 @@ struct PairCfg {
   static_assert(kSmemBytes <= 232448, "smem budget");
 };
 
+// Work items are claimed at run time (a counter in the workspace, after a first wave of
+// blockIdx.x): the TMA warp claims the next item when it is about to load it and hands
+// the index to the MMA warp and the softmax warps through a small ring.  Dense items are
+// numbered longest first, so the claims approximate longest-processing-time scheduling.
+constexpr int kItemRing = 4;
+
 struct PairBars {
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
   uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t item_full[kItemRing], item_empty[kItemRing];
   uint64_t drain;
+  int32_t item_idx[kItemRing];  // -1: no more items
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(PairBars) <= 256, "pair kernel barrier block");
 
 template <int D, bool kLogits>
 __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
@@ -517,6 +526,10 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
       mbar_init(&bars.p_full[i], 128);
       mbar_init(&bars.o_done[i], 1);
     }
+    for (int i = 0; i < kItemRing; ++i) {
+      mbar_init(&bars.item_full[i], 1);
+      mbar_init(&bars.item_empty[i], 9);  // the MMA warp and the 8 softmax warps
+    }
     mbar_init(&bars.drain, 1);
     bars.abort = 0;
     fence_barrier_init();
@@ -539,9 +552,17 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
       prefetch_tensormap(&map_q);
       prefetch_tensormap(&map_k);
       prefetch_tensormap(&map_v);
-      uint32_t g = 0, it = 0;
+      uint32_t g = 0;
       bool ok = true;
-      for (int64_t item = blockIdx.x; item < n_items && ok && !*abort_flag; item += gridDim.x, ++it) {
+      for (uint32_t it = 0;; ++it) {
+        // claim the next item and publish it (-1 ends every consumer's loop)
+        const uint32_t slot = it % kItemRing;
+        if (it >= kItemRing) ok = ok && mbar_wait(&bars.item_empty[slot], (it / kItemRing - 1) & 1, limit_ns, st, 13);
+        int64_t item = it == 0 ? blockIdx.x : gridDim.x + atomicAdd(a.table.counts + 2, 1);
+        if (item >= n_items || !ok || *abort_flag) item = -1;
+        bars.item_idx[slot] = static_cast<int32_t>(item);
+        mbar_arrive(&bars.item_full[slot]);
+        if (item < 0) break;
         const Item w = decode_item(a, item, group);
         const int nkv = max(tile_nkv<BN>(2 * w.it, w.L, causal), tile_nkv<BN>(2 * w.it + 1, w.L, causal));
         // both Q tiles are always loaded (a tile past the end reads rows no one uses)
@@ -566,9 +587,16 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
       // ---------------------------------------------------------- MMA issuer (whole warp, one lane issues)
       // Per key tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1): while one tile's softmax
       // runs, the tensor core works on the other tile.
-      uint32_t g = 0, it = 0, np[2] = {0, 0};
+      uint32_t g = 0, np[2] = {0, 0};
       bool ok = true, issued = false;
-      for (int64_t item = blockIdx.x; item < n_items && ok && !*abort_flag; item += gridDim.x, ++it) {
+      for (uint32_t it = 0; ok && !*abort_flag; ++it) {
+        const uint32_t slot = it % kItemRing;
+        ok = warp_wait(&bars.item_full[slot], (it / kItemRing) & 1, limit_ns, st, 25);
+        if (!ok) break;
+        const int32_t item = bars.item_idx[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.item_empty[slot]);
+        if (item < 0) break;
         const Item w = decode_item(a, item, group);
         const int nkv_t[2] = {tile_nkv<BN>(2 * w.it, w.L, causal), tile_nkv<BN>(2 * w.it + 1, w.L, causal)};
         const int nkv = max(nkv_t[0], nkv_t[1]);
@@ -642,58 +670,38 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
     const float qk_scale = kLog2e * rsqrtf(static_cast<float>(D));
     uint32_t ns = 0, no = 0;   // S tiles consumed, items finished (this tile)
     bool bad = false;
-    // first item in which this warpgroup's tile exists
-    int64_t item = blockIdx.x;
-    Item w{};
-    while (item < n_items) {
-      w = decode_item(a, item, group);
-      if (tile_nkv<BN>(2 * w.it + t, w.L, causal) > 0) break;
-      item += gridDim.x;
-    }
-    // q scales of this thread's four softmax rows (the quad layout) for the next item
-    float qs_next[4] = {0.0f, 0.0f, 0.0f, 0.0f}, ks_next = 0.0f;
-    int ve_next = 0;
-    auto load_qs = [&](const Item& x) {
-      const float* qs = a.q_scales + static_cast<int64_t>(x.hq) * a.t_pad_max + x.pstart + (2 * x.it + t) * kQTile;
-#pragma unroll
-      for (int s = 0; s < 4; ++s) qs_next[s] = qs[wrow + quad_row(s)];
-    };
-    if (item < n_items) {
-      load_qs(w);
-      if (a.v_exp) ve_next = a.v_exp[static_cast<int64_t>(w.s) * a.Hkv + w.hkv];
-      ks_next = a.k_scales[static_cast<int64_t>(w.hkv) * a.t_pad_max + w.pstart + r];
-    }
-    while (item < n_items) {
+    for (uint32_t it = 0; !bad; ++it) {
+      const uint32_t slot = it % kItemRing;
+      if (!warp_wait(&bars.item_full[slot], (it / kItemRing) & 1, limit_ns, st, 35)) {
+        bad = true;
+        break;
+      }
+      const int32_t item = bars.item_idx[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.item_empty[slot]);
+      if (item < 0) break;
+      const Item w = decode_item(a, item, group);
       const int qt = 2 * w.it + t;
       const int nkv = tile_nkv<BN>(qt, w.L, causal);
+      if (nkv == 0) continue;  // this tile lies past the sequence's end
       const int row_abs = qt * kQTile + r;
       QuadRows rs;
+      const float* qs = a.q_scales + static_cast<int64_t>(w.hq) * a.t_pad_max + w.pstart + qt * kQTile + wrow;
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
         rs.m[s] = -INFINITY;
         rs.l[s] = 0.0f;
-        rs.alpha[s] = fmaxf(qs_next[s] * qk_scale, FLT_MIN);
+        rs.alpha[s] = fmaxf(qs[quad_row(s)] * qk_scale, FLT_MIN);
         rs.row[s] = qt * kQTile + wrow + quad_row(s);
       }
-      const float v_unscale = __int_as_float((127 + ve_next) << 23);
-      // the next item in which this warpgroup's tile exists
-      int64_t item_n = item + gridDim.x;
-      Item wn{};
-      while (item_n < n_items) {
-        wn = decode_item(a, item_n, group);
-        if (tile_nkv<BN>(2 * wn.it + t, wn.L, causal) > 0) break;
-        item_n += gridDim.x;
-      }
+      const int ve = a.v_exp ? a.v_exp[static_cast<int64_t>(w.s) * a.Hkv + w.hkv] : 0;
+      const float v_unscale = __int_as_float((127 + ve) << 23);
+      const float* ksrc = a.k_scales + static_cast<int64_t>(w.hkv) * a.t_pad_max + w.pstart + r;
+      float ks_next = ksrc[0];
       for (int j = 0; j < nkv; ++j, ++ns) {
         const uint32_t buf = ns & 1;
         sks[buf * BN + ks_slot(r)] = ks_next;
-        if (j + 1 < nkv) {
-          ks_next = a.k_scales[static_cast<int64_t>(w.hkv) * a.t_pad_max + w.pstart + (j + 1) * BN + r];
-        } else if (item_n < n_items) {
-          ks_next = a.k_scales[static_cast<int64_t>(wn.hkv) * a.t_pad_max + wn.pstart + r];
-          load_qs(wn);
-          if (a.v_exp) ve_next = a.v_exp[static_cast<int64_t>(wn.s) * a.Hkv + wn.hkv];
-        }
+        if (j + 1 < nkv) ks_next = ksrc[(j + 1) * BN];
         if (wg_any(bad || *abort_flag, 1 + t)) {
           bad = true;
           break;
@@ -735,8 +743,6 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
         }
       }
       ++no;
-      item = item_n;
-      w = wn;
     }
     if (bad) *abort_flag = 1;
   }

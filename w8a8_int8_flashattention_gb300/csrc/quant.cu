@@ -647,6 +647,8 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quant_qk_kernel(const QuantQ
   constexpr int LPR = 8, EPL = D / LPR, NV = EPL / 8, RPP = 32 / LPR, P = kQuantRowsPerWarp / RPP;
   grid_dependency_wait();
   grid_dependents_launch();
+  // the attention kernel that follows claims work items from this counter
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) a.t.counts[2] = 0;
   __shared__ __align__(16) float s_mean[D];
   __shared__ float s_vm[kQuantWarps];
   __shared__ int s_vexp;

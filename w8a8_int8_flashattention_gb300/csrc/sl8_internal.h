@@ -22,7 +22,8 @@ struct SeqTable {
   int32_t* tok0;     // [nseq]  first token of the sequence in the caller's tensors (varlen: cu_seqlens[s])
   int32_t* pair_seq; // [max_pairs] work list: sequence of each (sequence, q-tile) pair
   int32_t* pair_qt;  // [max_pairs] q-tile index of each pair
-  int32_t* counts;   // [4]: 0 = number of pairs, 1 = total padded rows
+  int32_t* counts;   // [4]: 0 = number of pairs, 1 = total padded rows, 2 = attention items
+                     //      claimed past the first wave (zeroed by the quantiser)
   int32_t* hist;     // [max_tiles + 2] scratch for the scheduler
   int32_t* sorted;   // [nseq] scratch: sequences ordered by tile count, longest first
 };
