@@ -89,18 +89,6 @@ __device__ __forceinline__ uint32_t pack_out2(float lo, float hi, bool bf16) {
   return pack_half2(lo, hi);
 }
 
-// OR of a flag over the 128 threads of a softmax warpgroup (named barrier `id`); also
-// orders their shared-memory accesses like bar.sync.
-__device__ __forceinline__ bool wg_any(bool v, int id) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, %2, 128, q;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(v)), "r"(id)
-      : "memory");
-  return r != 0;
-}
-
 // Wait on an mbarrier phase with the result made uniform across the warp.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns, DeviceStatus* st,
                                           int site) {
@@ -168,23 +156,17 @@ __device__ __forceinline__ int quad_row(int s) {
   return 16 * (s >> 1) + 8 * (s & 1) + ((threadIdx.x & 31) >> 2);
 }
 
-// Shared-memory position of key k's scale: thread q's scales (keys 8i + 2q + {0, 1}) are
-// 16-byte words (i / 2) * 4 + q, and the four q of one word index are adjacent.
-__device__ __forceinline__ int ks_slot(int k) {
-  const int i = k >> 3, q = (k >> 1) & 3;
-  return ((i >> 1) * 4 + q) * 4 + (i & 1) * 2 + (k & 1);
-}
-// ks[2i + e] = scale of key 8i + 2q + e.
+// This thread's K scales of a key tile (tile_ks: the tile's first key): ks[2i + e] = scale
+// of key 8i + 2q + e.  Read through the read-only path: every warp of the CTA reads the
+// same 4 * BN bytes, so all but the first hit L1.
 template <int BN>
-__device__ __forceinline__ void load_ks(const float* sks, float (&ks)[BN / 4]) {
+__device__ __forceinline__ void load_ks(const float* tile_ks, float (&ks)[BN / 4]) {
   const int q = threadIdx.x & 3;
 #pragma unroll
-  for (int w = 0; w < BN / 16; ++w) {
-    const float4 v = reinterpret_cast<const float4*>(sks)[w * 4 + q];
-    ks[4 * w] = v.x;
-    ks[4 * w + 1] = v.y;
-    ks[4 * w + 2] = v.z;
-    ks[4 * w + 3] = v.w;
+  for (int i = 0; i < BN / 8; ++i) {
+    const float2 v = __ldg(reinterpret_cast<const float2*>(tile_ks + 8 * i + 2 * q));
+    ks[2 * i] = v.x;
+    ks[2 * i + 1] = v.y;
   }
 }
 
@@ -462,8 +444,7 @@ struct PairCfg {
   static constexpr int kQOff = 0;                                   // 2 Q tiles
   static constexpr int kKOff = kQOff + 2 * kQBytes;
   static constexpr int kVOff = kKOff + kStages * kKVBytes;
-  static constexpr int kScaleOff = kVOff + kStages * kKVBytes;     // [2 wg][2 buf][BN] floats
-  static constexpr int kBarOff = kScaleOff + 4 * BN * 4;
+  static constexpr int kBarOff = kVOff + kStages * kKVBytes;
   static constexpr int kUsed = kBarOff + 256 + 1024;
   // at least 116 KB so that a second CTA never shares the SM (each holds all 512 TMEM columns)
   static constexpr int kSmemBytes = kUsed > 118784 ? kUsed : 118784;
@@ -507,7 +488,6 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   PairBars& bars = *reinterpret_cast<PairBars*>(smem + C::kBarOff);
-  float* sks_all = reinterpret_cast<float*>(smem + C::kScaleOff);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const bool causal = kLogits ? false : a.causal;
@@ -666,7 +646,6 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(wrow) << 16;
     const uint32_t s_taddr = tbase + lane_base + t * 256;
     const uint32_t o_taddr = s_taddr + 128;
-    float* sks = sks_all + t * 2 * BN;
     const float qk_scale = kLog2e * rsqrtf(static_cast<float>(D));
     uint32_t ns = 0, no = 0;   // S tiles consumed, items finished (this tile)
     bool bad = false;
@@ -696,21 +675,17 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
       }
       const int ve = a.v_exp ? a.v_exp[static_cast<int64_t>(w.s) * a.Hkv + w.hkv] : 0;
       const float v_unscale = __int_as_float((127 + ve) << 23);
-      const float* ksrc = a.k_scales + static_cast<int64_t>(w.hkv) * a.t_pad_max + w.pstart + r;
-      float ks_next = ksrc[0];
+      const float* ksrc = a.k_scales + static_cast<int64_t>(w.hkv) * a.t_pad_max + w.pstart;
       for (int j = 0; j < nkv; ++j, ++ns) {
-        const uint32_t buf = ns & 1;
-        sks[buf * BN + ks_slot(r)] = ks_next;
-        if (j + 1 < nkv) ks_next = ksrc[(j + 1) * BN];
-        if (wg_any(bad || *abort_flag, 1 + t)) {
+        if (*abort_flag) {
           bad = true;
           break;
         }
         float ks[BN / 4];
-        load_ks<BN>(sks + buf * BN, ks);
+        load_ks<BN>(ksrc + j * BN, ks);
         if (!warp_wait(&bars.s_full[t], ns & 1, limit_ns, st, 30)) {
           bad = true;
-          continue;
+          break;
         }
         tc_fence_after();
         const int key0 = j * BN;
@@ -722,13 +697,13 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
           if (!softmax_step<BN, D>(s_taddr, o_taddr, ks, need_mask, key0, w.L, causal, j == 0, rs, nullptr, 0,
                                    limit_ns, st)) {
             bad = true;
-            continue;
+            break;
           }
         }
         tc_fence_before();
         mbar_arrive(&bars.p_full[t]);
       }
-      if (wg_any(bad || *abort_flag, 1 + t)) {
+      if (bad || *abort_flag) {
         bad = true;
         break;
       }
@@ -764,8 +739,7 @@ struct SingleCfg {
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + kQBytes;
   static constexpr int kVOff = kKOff + kStages * kKVBytes;
-  static constexpr int kScaleOff = kVOff + kStages * kKVBytes;  // [2 buf][BN] floats
-  static constexpr int kBarOff = kScaleOff + 2 * BN * 4;
+  static constexpr int kBarOff = kVOff + kStages * kKVBytes;
   static constexpr int kUsed = kBarOff + 256 + 1024;
   static constexpr int kSmemBytes = kUsed > 118784 ? kUsed : 118784;
   static constexpr int kThreads = 192;  // warps 0-3 softmax; 4 TMA; 5 MMA
@@ -794,7 +768,6 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   SingleBars& bars = *reinterpret_cast<SingleBars*>(smem + C::kBarOff);
-  float* sks = reinterpret_cast<float*>(smem + C::kScaleOff);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const bool causal = kLogits ? false : a.causal;
@@ -927,7 +900,7 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
     Item w{};
     uint32_t g = 0;
     // q scales of this thread's four softmax rows (the quad layout) for the next item
-    float qs_next[4] = {0.0f, 0.0f, 0.0f, 0.0f}, ks_next = 0.0f;
+    float qs_next[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     int ve_next = 0;
     auto load_qs = [&](const Item& x) {
       const float* qs = a.q_scales + static_cast<int64_t>(x.hq) * a.t_pad_max + x.pstart + x.it * kQTile;
@@ -938,7 +911,6 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
       w = decode_item(a, item, group);
       load_qs(w);
       if (a.v_exp) ve_next = a.v_exp[static_cast<int64_t>(w.s) * a.Hkv + w.hkv];
-      if (r < BN) ks_next = a.k_scales[static_cast<int64_t>(w.hkv) * a.t_pad_max + w.pstart + r];
     }
     bool bad = false;
     while (item < n_items) {
@@ -956,25 +928,22 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
       const int64_t item_n = item + gridDim.x;
       Item wn{};
       if (item_n < n_items) wn = decode_item(a, item_n, group);
+      const float* ksrc = a.k_scales + static_cast<int64_t>(w.hkv) * a.t_pad_max + w.pstart;
       for (int j = 0; j < nkv; ++j, ++g) {
         const uint32_t buf = g & 1;
-        if (r < BN) sks[buf * BN + ks_slot(r)] = ks_next;
-        if (j + 1 < nkv) {
-          if (r < BN) ks_next = a.k_scales[static_cast<int64_t>(w.hkv) * a.t_pad_max + w.pstart + (j + 1) * BN + r];
-        } else if (item_n < n_items) {
-          if (r < BN) ks_next = a.k_scales[static_cast<int64_t>(wn.hkv) * a.t_pad_max + wn.pstart + r];
+        if (j + 1 == nkv && item_n < n_items) {
           load_qs(wn);
           if (a.v_exp) ve_next = a.v_exp[static_cast<int64_t>(wn.s) * a.Hkv + wn.hkv];
         }
-        if (wg_any(bad || *abort_flag, 1)) {
+        if (*abort_flag) {
           bad = true;
           break;
         }
         float ks[BN / 4];
-        load_ks<BN>(sks + buf * BN, ks);
+        load_ks<BN>(ksrc + j * BN, ks);
         if (!warp_wait(&bars.s_full[buf], (g >> 1) & 1, limit_ns, st, 30)) {
           bad = true;
-          continue;
+          break;
         }
         tc_fence_after();
         const uint32_t s_taddr = tbase + lane_base + buf * BN;
@@ -988,13 +957,13 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
           if (!softmax_step<BN, D>(s_taddr, tbase + lane_base + C::kOCol, ks, need_mask, key0, w.L, causal, j == 0,
                                    rs, &bars.o_done[gprev & 1], (gprev >> 1) & 1, limit_ns, st)) {
             bad = true;
-            continue;
+            break;
           }
         }
         tc_fence_before();
         mbar_arrive(&bars.p_full[buf]);
       }
-      if (wg_any(bad || *abort_flag, 1)) {
+      if (bad || *abort_flag) {
         bad = true;
         break;
       }
