@@ -503,7 +503,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
       mbar_init(&bars.v_full[i], 1);
       mbar_init(&bars.v_empty[i], 1);
       mbar_init(&bars.s_full[i], 1);
-      mbar_init(&bars.p_full[i], 128);
+      mbar_init(&bars.p_full[i], 4);  // one arrival per softmax warp
       mbar_init(&bars.o_done[i], 1);
     }
     for (int i = 0; i < kItemRing; ++i) {
@@ -701,7 +701,8 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(&bars.p_full[t]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.p_full[t]);
       }
       if (bad || *abort_flag) {
         bad = true;
@@ -783,7 +784,7 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
       mbar_init(&bars.v_full[i], 1);
       mbar_init(&bars.v_empty[i], 1);
       mbar_init(&bars.s_full[i], 1);
-      mbar_init(&bars.p_full[i], 128);
+      mbar_init(&bars.p_full[i], 4);  // one arrival per softmax warp
       mbar_init(&bars.o_done[i], 1);
     }
     mbar_init(&bars.drain, 1);
@@ -961,7 +962,8 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(&bars.p_full[buf]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.p_full[buf]);
       }
       if (bad || *abort_flag) {
         bad = true;
