@@ -14,15 +14,18 @@
 // of a row with weights exp(lse_s - max lse).
 //
 // GB300 design.  The kernel streams the cache once, so HBM is the bound; the work
-// per byte must stay small enough that eight warps per SM keep up with it.
-//  * A persistent CTA per SM walks a balanced list of (b, kv head, split) work slots.
-//    Warp 0 loads each split's K and V codes with tiled TMA copies (128-byte swizzle
-//    for d >= 128) in 128-token stages, with their scales and the group's q rows,
-//    into shared-memory rings that run ahead across splits.
-//  * Each of the eight compute warps takes 16 tokens of every stage and keeps its own
-//    online-softmax state.  Warp 1 quantises the next split's q rows while they work
-//    and merges the eight warps' states of the previous split, so the compute warps
-//    never meet at a CTA barrier.
+// per byte must stay small enough that the compute warps of an SM keep up with it.
+//  * A persistent CTA per SM walks a balanced list of (b, kv head, split) work slots
+//    (full splits first, then the tails longest first), claiming each next slot from
+//    a per-launch counter.  Warp 0 loads each split's K and V codes with tiled TMA
+//    copies (128-byte swizzle for d >= 128) in stages of 16 tokens per compute warp,
+//    with their scales and the group's raw q rows, into shared-memory rings that run
+//    ahead across splits.
+//  * Each compute warp (ten for d <= 128, eight for d = 256) takes 16 tokens of every
+//    stage and keeps its own online-softmax state; compute warp r < G also quantises
+//    q row r of each split as its raw rows land.  Warp 1 merges the warps' states of
+//    the previous split into the split's partial O and LSE, so the compute warps never
+//    meet at a CTA barrier.
 //  * Both contractions run on the tensor cores as m16n8k16 fp16 MMAs with fp32
 //    accumulation (the int8 tensor rate of this part is low).  Codes become fp16
 //    exactly (|c| <= 127), so q.k is the exact integer dot (|sum| < 2^24).
