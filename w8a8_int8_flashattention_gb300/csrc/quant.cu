@@ -600,7 +600,7 @@ cudaError_t launch_kv_partials(const void* k, sl8_dtype dt, const void* v, bool 
 }
 
 // ---------------------------------------------------------------- prefill codes
-// Q and K rows in one launch (blockIdx.y < Hq: Q heads; the rest: K heads), each warp
+// Q and K rows in one launch (blockIdx.y < Hkv: K heads; the rest: Q heads), each warp
 // quantising kQuantRowsPerWarp rows with all of their loads issued first.  Rows live in
 // the padded code workspace [H][t_pad][d]; padded rows past a sequence's end are
 // written as zeros.  For K rows with v16 set (V bf16), the warp also writes the same
@@ -645,15 +645,21 @@ __device__ __forceinline__ void store_vec16(uint16_t* p, const uint16_t (&h)[EPL
 template <sl8_dtype DT, int D>
 __global__ void __launch_bounds__(kQuantWarps * 32) quant_qk_kernel(const QuantQK a, DeviceStatus* st) {
   constexpr int LPR = 8, EPL = D / LPR, NV = EPL / 8, RPP = 32 / LPR, P = kQuantRowsPerWarp / RPP;
-  grid_dependency_wait();
+  // K heads first: their CTAs also form the K mean and the V exponent, so they start
+  // in the first wave and the Q CTAs fill in behind them
+  const bool is_k = static_cast<int>(blockIdx.y) < a.Hkv;
+  const int h = is_k ? blockIdx.y : blockIdx.y - a.Hkv;
+  // When the K/V chunk kernel ran just before (k_partials or v_partials set), Q CTAs
+  // need none of its results: that kernel lets this grid start only after its own
+  // wait, so everything before it (the caller's Q, the schedule, the attention launch
+  // that last read this workspace) has completed, and Q runs alongside it.
+  if (is_k || (!a.k_partials && !a.v_partials)) grid_dependency_wait();
   grid_dependents_launch();
   // the attention kernel that follows claims work items from this counter
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) a.t.counts[2] = 0;
   __shared__ __align__(16) float s_mean[D];
   __shared__ float s_vm[kQuantWarps];
   __shared__ int s_vexp;
-  const bool is_k = static_cast<int>(blockIdx.y) >= a.Hq;
-  const int h = is_k ? blockIdx.y - a.Hq : blockIdx.y;
   const int H = is_k ? a.Hkv : a.Hq;
   const void* x = is_k ? a.k : a.q;
   uint16_t* codes = is_k ? a.k_codes : a.q_codes;
