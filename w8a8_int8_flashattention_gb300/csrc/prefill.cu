@@ -520,6 +520,9 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
   }
   __syncthreads();
   tc_fence_after();
+  // launched as a programmatic dependent of the quantiser: the set-up above overlaps
+  // its tail; everything below reads what it wrote
+  grid_dependency_wait();
   const uint32_t tbase = bars.tmem_base;
   volatile int* abort_flag = &bars.abort;
   static_assert(8 * 32 * C::kRegsSoftmax + 4 * 32 * C::kRegsOther <= C::kThreads * 168, "register split");
@@ -797,6 +800,9 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
   }
   __syncthreads();
   tc_fence_after();
+  // launched as a programmatic dependent of the quantiser: the set-up above overlaps
+  // its tail; everything below reads what it wrote
+  grid_dependency_wait();
   const uint32_t tbase = bars.tmem_base;
   volatile int* abort_flag = &bars.abort;
 
@@ -1025,8 +1031,8 @@ static cudaError_t launch_pair(const PrefillArgs& a, cudaStream_t s) {
   const int grid = static_cast<int>(max_items < num_sms() ? max_items : num_sms());
   if (grid <= 0) return cudaSuccess;
   TraceScope tr(kLogits ? "prefill_logits" : "prefill_attn", s);
-  kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(mq, mk, mv, a, device_status_ptr(), spin_limit_ns());
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, mq, mk, mv, a, device_status_ptr(),
+                    spin_limit_ns());
 }
 
 template <int D, bool kLogits>
@@ -1041,8 +1047,8 @@ static cudaError_t launch_single(const PrefillArgs& a, cudaStream_t s) {
   const int grid = static_cast<int>(max_items < num_sms() ? max_items : num_sms());
   if (grid <= 0) return cudaSuccess;
   TraceScope tr(kLogits ? "prefill_logits" : "prefill_attn", s);
-  kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(mq, mk, mv, a, device_status_ptr(), spin_limit_ns());
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, mq, mk, mv, a, device_status_ptr(),
+                    spin_limit_ns());
 }
 
 }  // namespace
