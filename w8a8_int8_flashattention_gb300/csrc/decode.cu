@@ -936,25 +936,43 @@ __global__ void decode_combine_kernel(const float* __restrict__ o_partial, const
   if (row >= B * Hq) return;
   const int b = row / Hq;
   const int L = max(0, seqlens[b]);
-  const int ns = min(num_splits, (L + split_size - 1) / split_size);
   const float* lse = lse_partial + static_cast<int64_t>(row) * num_splits;
-  float m = -INFINITY;
-  for (int s = lane; s < ns; s += 32) m = fmaxf(m, lse[s]);
-  m = warp_max_f(m);
-  constexpr int E = D / 32;
+  const float* op = o_partial + static_cast<int64_t>(row) * num_splits * D + lane * (D / 32);
+  constexpr int E = D / 32, K = 8;
   float o[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) o[e] = 0.0f;
-  float wsum = 0.0f;
-  if (m != -INFINITY) {
-    for (int s = 0; s < ns; ++s) {
-      const float ls = lse[s];
-      if (ls == -INFINITY) continue;
-      const float w = expf(ls - m);
-      wsum += w;
-      const float* op = o_partial + (static_cast<int64_t>(row) * num_splits + s) * D + lane * E;
+  float m = -INFINITY, wsum = 0.0f;
+  // K splits at a time: their LSEs (the same word for every lane) and partial rows are
+  // all loaded before any is used, together with the length.  An empty split (past the
+  // length, or lse = -inf) gets weight 0 and its unwritten row is never multiplied.
+  for (int s0 = 0; s0 < num_splits; s0 += K) {
+    float ls[K], pre[K][E];
 #pragma unroll
-      for (int e = 0; e < E; ++e) o[e] = fmaf(w, op[e], o[e]);
+    for (int k = 0; k < K; ++k) {
+      const bool in = s0 + k < num_splits;
+      ls[k] = in ? lse[s0 + k] : -INFINITY;
+#pragma unroll
+      for (int e = 0; e < E; ++e) pre[k][e] = in ? op[static_cast<int64_t>(s0 + k) * D + e] : 0.0f;
+    }
+    const int ns = min(num_splits, (L + split_size - 1) / split_size);
+    float m_new = m;
+#pragma unroll
+    for (int k = 0; k < K; ++k)
+      if (s0 + k < ns) m_new = fmaxf(m_new, ls[k]);
+    if (m_new == -INFINITY) continue;  // every split so far is empty
+    const float c = m == -INFINITY ? 0.0f : expf(m - m_new);
+    wsum *= c;
+#pragma unroll
+    for (int e = 0; e < E; ++e) o[e] *= c;
+    m = m_new;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const float w = (s0 + k < ns && ls[k] != -INFINITY) ? expf(ls[k] - m) : 0.0f;
+      if (w == 0.0f) continue;
+      wsum += w;
+#pragma unroll
+      for (int e = 0; e < E; ++e) o[e] = fmaf(w, pre[k][e], o[e]);
     }
   }
   const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
