@@ -157,11 +157,13 @@ SL8_API int sl8_attn_int8_qk_logits_debug(const void* q, const void* k, int qk_d
  *   k_scale, v_scale   device, [B][Hkv][Lmax] fp32 per-token scales.
  *   seqlens            device, [B] int32, 0 <= L_b <= Lmax.
  *   num_splits         requested number of contiguous key splits (0 = automatic: about
- *                      16 (split, sequence, kv head) work slots per SM of the current
+ *                      24 (split, sequence, kv head) work slots per SM of the current
  *                      device).  Split s covers tokens [s * split_size, (s + 1) * split_size)
- *                      with split_size = ceil(Lmax / S) rounded up to a multiple of 16; the
- *                      effective count S = sl8_attn_decode_num_splits(B, Hkv, Lmax, d,
- *                      num_splits) can be below the request after that rounding.
+ *                      with split_size = ceil(Lmax / S) rounded up to whole stages of the
+ *                      split kernel (160 tokens for d <= 128, 128 for d = 256; to 16 tokens
+ *                      below one stage); the effective count
+ *                      S = sl8_attn_decode_num_splits(B, Hkv, Lmax, d, num_splits) can be
+ *                      below the request after that rounding.
  *   o_partial          device, [B][Hq][S][d] fp32; each non-empty split's normalised partial
  *                      (the O of an empty split is not written).
  *   lse_partial        device, [B][Hq][S] fp32 log-sum-exp per split (-inf if empty).
@@ -181,7 +183,7 @@ SL8_API int sl8_attn_int8_decode_splitkv(const void* q, int q_dtype, const int8_
  *   out      device, [B][Hq][d] of out_dtype (F16, BF16 or F32).
  *   lse_out  device, nullable, [B][Hq] fp32.
  *   num_splits must be the effective count S of the split call (same Lmax); the split
- *   size is ceil(Lmax / S) rounded up to a multiple of 16, as there.
+ *   size is derived from Lmax and S as there.
  */
 SL8_API int sl8_attn_decode_combine(const float* o_partial, const float* lse_partial, const int32_t* seqlens, int32_t B,
                             int32_t Hq, int32_t Lmax, int32_t d, int32_t num_splits, void* out, int out_dtype,
