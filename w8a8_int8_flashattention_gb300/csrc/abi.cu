@@ -320,7 +320,8 @@ static int prefill_prepare(const void* q, const void* k, const void* v, int qk_d
   // the scheduler's table is needed for varlen input (and by the code export); dense
   // input is laid out arithmetically
   if (varlen || want_table)
-    SL8_LAUNCH(launch_schedule(cu_seqlens, B, N, tokens, p.t_pad_max, t, prefill_item_rows(d), nullptr, 0, s));
+    SL8_LAUNCH(launch_schedule(cu_seqlens, B, N, tokens, p.t_pad_max, t, prefill_item_rows(d, Hq / Hkv), nullptr, 0,
+                               s));
   float* k_partials = smooth_k ? reinterpret_cast<float*>(ws + p.k_partials) : nullptr;
   float* v_partials = convert_v ? reinterpret_cast<float*>(ws + p.v_partials) : nullptr;
   if (smooth_k || convert_v)
@@ -378,7 +379,8 @@ int sl8_attn_int8_fwd(const void* q, const void* k, const void* v, int qk_dtype,
   a.total_tokens = a.varlen ? total_tokens : static_cast<int64_t>(B) * N;
   a.t_pad_max = p.t_pad_max;
   a.table = t;
-  a.dense_items = (N + prefill_item_rows(d) - 1) / prefill_item_rows(d);
+  a.dense_items = (N + prefill_item_rows(d, Hq / Hkv) - 1) / prefill_item_rows(d, Hq / Hkv);
+  a.head_pairs = prefill_head_pairs(d, Hq / Hkv);
   a.max_pairs = p.max_pairs;
   a.causal = causal != 0;
   a.out = out;
@@ -431,7 +433,8 @@ int sl8_attn_int8_qk_logits_debug(const void* q, const void* k, int qk_dtype, in
     a.total_tokens = static_cast<int64_t>(B) * N;
     a.t_pad_max = p.t_pad_max;
     a.table = t;
-    a.dense_items = (N + prefill_item_rows(d) - 1) / prefill_item_rows(d);
+    a.dense_items = (N + prefill_item_rows(d, Hq / Hkv) - 1) / prefill_item_rows(d, Hq / Hkv);
+    a.head_pairs = prefill_head_pairs(d, Hq / Hkv);
     a.max_pairs = p.max_pairs;
     a.causal = false;
     a.out = nullptr;

@@ -96,18 +96,24 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
 }
 
 // ------------------------------------------------------------------ work items
-// An item is a block of consecutive 128-row Q tiles of one (sequence, query head).
+// An item is a block of consecutive 128-row Q tiles of one (sequence, query head), or
+// (head pairs) one Q tile of two query heads that share a kv head.
 struct Item {
   int32_t s, it, hq, hkv, L, pstart, tok0;
 };
 
+// Query heads handled per (sequence, row block) entry of the work list.
+__device__ __forceinline__ int item_heads(const PrefillArgs& a) { return a.head_pairs ? a.Hq / 2 : a.Hq; }
+
 // Work item -> (sequence, item index, heads, extent).  Varlen input uses the scheduler's
 // longest-first list; dense input (every sequence N long) needs no table: pair p is item
-// index max_items - 1 - p / nseq of sequence p % nseq, which is the same order.
+// index max_items - 1 - p / nseq of sequence p % nseq, which is the same order.  With
+// head pairs, w.hq is the first of the item's two query heads.
 __device__ __forceinline__ Item decode_item(const PrefillArgs& a, int64_t item, int group) {
   Item w;
-  const int64_t pair = item / a.Hq;
-  w.hq = static_cast<int32_t>(item - pair * a.Hq);
+  const int hh = item_heads(a);
+  const int64_t pair = item / hh;
+  w.hq = static_cast<int32_t>(item - pair * hh) * (a.head_pairs ? 2 : 1);
   w.hkv = w.hq / group;
   if (a.varlen) {
     w.s = a.table.pair_seq[pair];
@@ -125,9 +131,20 @@ __device__ __forceinline__ Item decode_item(const PrefillArgs& a, int64_t item, 
   }
   return w;
 }
-// Number of work items (pairs x query heads).
+// Number of work items (pairs x query heads, or x head pairs).
 __device__ __forceinline__ int64_t count_items(const PrefillArgs& a) {
-  return (a.varlen ? static_cast<int64_t>(a.table.counts[0]) : static_cast<int64_t>(a.nseq) * a.dense_items) * a.Hq;
+  return (a.varlen ? static_cast<int64_t>(a.table.counts[0]) : static_cast<int64_t>(a.nseq) * a.dense_items) *
+         item_heads(a);
+}
+
+// Q tile t (0, 1) of a two-tile item: its tile index in the sequence and its query head.
+__device__ __forceinline__ int tile_qt(const PrefillArgs& a, const Item& w, int t) {
+  return a.head_pairs ? w.it : 2 * w.it + t;
+}
+__device__ __forceinline__ Item tile_item(const PrefillArgs& a, const Item& w, int t) {
+  Item x = w;
+  if (a.head_pairs) x.hq = w.hq + t;
+  return x;
 }
 
 // Key tiles of BN keys that Q tile qt (128 rows) visits; 0 if the tile is past the end.
@@ -547,14 +564,14 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
         mbar_arrive(&bars.item_full[slot]);
         if (item < 0) break;
         const Item w = decode_item(a, item, group);
-        const int nkv = max(tile_nkv<BN>(2 * w.it, w.L, causal), tile_nkv<BN>(2 * w.it + 1, w.L, causal));
+        const int nkv = max(tile_nkv<BN>(tile_qt(a, w, 0), w.L, causal), tile_nkv<BN>(tile_qt(a, w, 1), w.L, causal));
         // both Q tiles are always loaded (a tile past the end reads rows no one uses)
         for (int t = 0; t < 2 && ok; ++t) {
           if (it >= 1) ok = mbar_wait(&bars.q_empty[t], (it - 1) & 1, limit_ns, st, 10);
           if (!ok) break;
           mbar_arrive_expect_tx(&bars.q_full[t], C::kQBytes);
           load_q_tile(smem + C::kQOff + t * C::kQBytes, &map_q, &bars.q_full[t], C::kBoxes,
-                      w.pstart + (2 * w.it + t) * kQTile, w.hq);
+                      w.pstart + tile_qt(a, w, t) * kQTile, tile_item(a, w, t).hq);
         }
         for (int j = 0; j < nkv && ok; ++j, ++g) {
           const uint32_t stg = g % C::kStages, n = g / C::kStages;
@@ -581,7 +598,8 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
         if (lane == 0) mbar_arrive(&bars.item_empty[slot]);
         if (item < 0) break;
         const Item w = decode_item(a, item, group);
-        const int nkv_t[2] = {tile_nkv<BN>(2 * w.it, w.L, causal), tile_nkv<BN>(2 * w.it + 1, w.L, causal)};
+        const int nkv_t[2] = {tile_nkv<BN>(tile_qt(a, w, 0), w.L, causal),
+                              tile_nkv<BN>(tile_qt(a, w, 1), w.L, causal)};
         const int nkv = max(nkv_t[0], nkv_t[1]);
         ok = warp_wait(&bars.q_full[0], it & 1, limit_ns, st, 20) &&
              warp_wait(&bars.q_full[1], it & 1, limit_ns, st, 20);
@@ -662,8 +680,8 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.item_empty[slot]);
       if (item < 0) break;
-      const Item w = decode_item(a, item, group);
-      const int qt = 2 * w.it + t;
+      const Item w = tile_item(a, decode_item(a, item, group), t);  // this warpgroup's Q tile
+      const int qt = tile_qt(a, w, t);
       const int nkv = tile_nkv<BN>(qt, w.L, causal);
       if (nkv == 0) continue;  // this tile lies past the sequence's end
       const int row_abs = qt * kQTile + r;
@@ -1053,7 +1071,8 @@ static cudaError_t launch_single(const PrefillArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-int prefill_item_rows(int d) { return d <= 128 ? 2 * kQTile : kQTile; }
+bool prefill_head_pairs(int d, int group) { return d <= 128 && group % 2 == 0; }
+int prefill_item_rows(int d, int group) { return d <= 128 && !prefill_head_pairs(d, group) ? 2 * kQTile : kQTile; }
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   const bool logits = a.logits != nullptr;

@@ -82,8 +82,11 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 cudaError_t launch_schedule(const int32_t* cu_seqlens, int32_t nseq, int32_t N, int64_t total_tokens,
                             int64_t t_pad_max, const SeqTable& t, int32_t item_rows, int32_t* kv_done,
                             int32_t n_done, cudaStream_t s);
-// Query rows per work-list item of the prefill kernel for head dim d.
-int prefill_item_rows(int d);
+// Query rows per work-list item of the prefill kernel for head dim d and group size
+// Hq / Hkv; prefill_head_pairs: whether an item of the two-tile kernel is one Q tile of
+// two query heads of the same kv head (else two Q tiles of one head).
+int prefill_item_rows(int d, int group);
+bool prefill_head_pairs(int d, int group);
 // K chunk sums (k_partials, nullable) and V chunk abs-max (v_partials, nullable; V bf16);
 // the last chunk of each (sequence, kv head) to finish forms the K mean [nseq][Hkv][d]
 // and the V power-of-two exponent [nseq][Hkv].  kv_done [nseq][Hkv] must be zero.
@@ -126,6 +129,7 @@ struct PrefillArgs {
   int64_t t_pad_max;
   SeqTable table;            // varlen only: the dense layout is arithmetic
   int32_t dense_items;       // items per sequence of a dense input (ceil(N / item rows))
+  bool head_pairs;           // see prefill_head_pairs
   int64_t max_pairs;
   bool causal;
   void* out;                // caller's output
