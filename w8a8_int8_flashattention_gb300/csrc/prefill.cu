@@ -372,26 +372,31 @@ __device__ __forceinline__ void store_row(uint32_t o_taddr, const PrefillArgs& a
   const bool out_f32 = a.out_dtype == SL8_F32, out_bf16 = a.out_dtype == SL8_BF16;
   const int64_t orow = a.varlen ? (static_cast<int64_t>(w.tok0) + row_abs) * a.Hq + w.hq
                                 : (static_cast<int64_t>(w.s) * a.Hq + w.hq) * a.N + row_abs;
+  // 64 columns per TMEM round trip
 #pragma unroll
-  for (int c0 = 0; c0 < D; c0 += 16) {
-    uint32_t v[16];
-    tmem_ld16(o_taddr + c0, v);
+  for (int c0 = 0; c0 < D; c0 += 64) {
+    uint32_t v[64];
+    tmem_ld32(o_taddr + c0, *reinterpret_cast<uint32_t(*)[32]>(v));
+    tmem_ld32(o_taddr + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
     tmem_wait_ld();
     if (row_ok) {
       if (out_f32) {
         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow * D + c0);
 #pragma unroll
-        for (int c = 0; c < 16; c += 4)
+        for (int c = 0; c < 64; c += 4)
           dst[c / 4] = make_float4(__uint_as_float(v[c]) * scale, __uint_as_float(v[c + 1]) * scale,
                                    __uint_as_float(v[c + 2]) * scale, __uint_as_float(v[c + 3]) * scale);
       } else {
-        uint32_t p[8];
-#pragma unroll
-        for (int c = 0; c < 16; c += 2)
-          p[c / 2] = pack_out2(__uint_as_float(v[c]) * scale, __uint_as_float(v[c + 1]) * scale, out_bf16);
         uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow * D + c0);
-        dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
-        dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+#pragma unroll
+        for (int c = 0; c < 64; c += 8) {
+          uint32_t p[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            p[e] = pack_out2(__uint_as_float(v[c + 2 * e]) * scale, __uint_as_float(v[c + 2 * e + 1]) * scale,
+                             out_bf16);
+          dst[c / 8] = make_uint4(p[0], p[1], p[2], p[3]);
+        }
       }
     }
   }
