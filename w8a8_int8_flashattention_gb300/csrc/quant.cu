@@ -65,6 +65,31 @@ __device__ __forceinline__ float rint_add(float y) {
   constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: its ulp is 1
   return __fsub_rn(__fadd_rn(y, kMagic), kMagic);
 }
+// Packed f32x2 arithmetic (two lanes per instruction, each rounded like its scalar op).
+__device__ __forceinline__ uint64_t q_pk2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void q_upk2(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t q_mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t q_add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t q_sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // The same code as an integer-valued float, from rs = RN(1 / s): for |x / s| <= 127.5 the
 // product x * rs lies within 3e-5 of the correctly rounded quotient, so both round to
 // the same integer unless the product is within 1e-4 of a half-integer; only then is
@@ -811,13 +836,24 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quant_qk_kernel(const QuantQ
     const float scale = valid[p] ? __fdiv_rn(am, 127.0f) : 0.0f;
     const float rs = scale == 0.0f ? 0.0f : __frcp_rn(scale);
     uint16_t* crow = codes + (static_cast<int64_t>(h) * a.t_pad_max + pr) * D + part * EPL;
+    // two elements per packed instruction: y = x * rs, c = RNE(y) (see quant_code_rcp;
+    // scale 0 gives rs = 0 and zero codes); a pair whose product lies near a
+    // half-integer takes the exact path
+    const uint64_t rs2 = q_pk2(rs, rs), mg2 = q_pk2(12582912.0f, 12582912.0f);
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
       uint32_t o[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float c0 = scale == 0.0f ? 0.0f : quant_code_rcp(v[8 * j + 2 * e], scale, rs);
-        const float c1 = scale == 0.0f ? 0.0f : quant_code_rcp(v[8 * j + 2 * e + 1], scale, rs);
+        const uint64_t y2 = q_mul2(q_pk2(v[8 * j + 2 * e], v[8 * j + 2 * e + 1]), rs2);
+        const uint64_t c2 = q_sub2(q_add2(y2, mg2), mg2);
+        float d0, d1, c0, c1;
+        q_upk2(q_sub2(y2, c2), d0, d1);
+        q_upk2(c2, c0, c1);
+        if (fmaxf(fabsf(d0), fabsf(d1)) > 0.4999f) {
+          c0 = quant_code_rcp(v[8 * j + 2 * e], scale, rs);
+          c1 = quant_code_rcp(v[8 * j + 2 * e + 1], scale, rs);
+        }
         o[e] = (__float_as_uint(c0) >> 16) | (__float_as_uint(c1) & 0xffff0000u);
       }
       *reinterpret_cast<uint4*>(crow + 8 * j) = make_uint4(o[0], o[1], o[2], o[3]);
