@@ -821,15 +821,13 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quant_qk_kernel(const QuantQ
 #pragma unroll
       for (int e = 0; e < EPL; e += 4) {
         const float4 m4 = *reinterpret_cast<const float4*>(mu + e);
-        v[e] = __fsub_rn(v[e], m4.x);
-        v[e + 1] = __fsub_rn(v[e + 1], m4.y);
-        v[e + 2] = __fsub_rn(v[e + 2], m4.z);
-        v[e + 3] = __fsub_rn(v[e + 3], m4.w);
+        q_upk2(q_sub2(q_pk2(v[e], v[e + 1]), q_pk2(m4.x, m4.y)), v[e], v[e + 1]);
+        q_upk2(q_sub2(q_pk2(v[e + 2], v[e + 3]), q_pk2(m4.z, m4.w)), v[e + 2], v[e + 3]);
       }
     }
     float am = 0.0f;
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) am = fmaxf(am, fabsf(v[e]));
+    for (int e = 0; e < EPL; e += 2) am = fmaxf(am, fmaxf(fabsf(v[e]), fabsf(v[e + 1])));
 #pragma unroll
     for (int o = LPR / 2; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
     if (!live[p]) continue;
