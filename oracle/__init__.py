@@ -11,7 +11,8 @@ it with gcc, lays out the per-(sequence, head) slices and loops over them.
 Sources: the "SuperL8" README (github.com/jajmangold/superl8) -- "Attention
 kernels" table (attn_int8_fwd: W8A8 FlashAttention-2, causal, GQA/MQA, head dims
 32/64/128/256; attn_varlen_fwd: ragged prefill; attn_decode: split-KV decode over
-an int8 KV cache, int8-V variant), "Supporting kernels" table (quant_rowwise:
+an int8 KV cache, int8-V variant; attn_paged_decode over a paged cache, with the
+"Engine" table's k8v8 format), "Supporting kernels" table (quant_rowwise:
 symmetric per-row int8), "Quantization" table (per-row int8 with K-smoothing) and
 the "Quick start" section (q [B,Hq,N,d], k/v [B,Hkv,N,d], quantises internally).
 The readings R1-R13 that fill what the pages leave open are restated in
@@ -255,14 +256,56 @@ def attn_decode(q, k_codes, k_scales, v_codes, v_scales, seqlens, num_splits=1, 
     rows: None, or an iterable of (b, hq).  Returns dict(out [B,Hq,d] f64, lse [B,Hq],
     q_codes, q_scales, o_partial [B,Hq,S,d], lse_partial [B,Hq,S], logits {(b,hq): int32 [L]}).
     """
-    q = _f32(q)
     k_codes = np.ascontiguousarray(k_codes, np.int8)
     v_codes = np.ascontiguousarray(v_codes, np.int8)
     k_scales = _f32(k_scales)
     v_scales = _f32(v_scales)
+
+    def rows_of(b, hkv, L):
+        return k_codes[b, hkv], k_scales[b, hkv], v_codes[b, hkv], v_scales[b, hkv]
+
+    return _decode(q, rows_of, k_codes.shape[1], k_codes.shape[2], seqlens, num_splits, split_size, rows,
+                   want_logits)
+
+
+def attn_paged_decode(q, k_pages, k_scale_pages, v_pages, v_scale_pages, block_table, seqlens, num_splits=1,
+                      split_size=None, rows=None, want_logits=False):
+    """Split-KV decode over a paged int8 (k8v8) cache, fp64 after the int32 dot.
+
+    Source: the "SuperL8" README, "Engine" table ("Paged KV cache" row: int8, k8v3 and
+    k8v8 cache formats) and "Attention kernels" table (attn_paged_decode row).  Reading
+    (the pages give no layout): a page holds page_size consecutive tokens of one
+    sequence for every kv head, k_pages / v_pages [num_pages, Hkv, page_size, d] int8
+    codes with per-token scales [num_pages, Hkv, page_size] float32 (k8v8: both K and V
+    int8, as in the int8-V decode); block_table [B, max_blocks] int32 names the page of
+    the logical block i = tokens [i * page_size, (i + 1) * page_size) of sequence b, so
+    token t is row t % page_size of page block_table[b, t // page_size].  The result is
+    attn_decode over those rows with Lmax = max_blocks * page_size (same split plan);
+    block-table entries past a sequence's last block are never read.
+    """
+    k_pages = np.ascontiguousarray(k_pages, np.int8)
+    v_pages = np.ascontiguousarray(v_pages, np.int8)
+    k_scale_pages = _f32(k_scale_pages)
+    v_scale_pages = _f32(v_scale_pages)
+    block_table = np.asarray(block_table, np.int64)
+    page = k_pages.shape[2]
+    lmax = block_table.shape[1] * page
+
+    def rows_of(b, hkv, L):
+        t = np.arange(L)
+        pg, off = block_table[b, t // page], t % page
+        return (np.ascontiguousarray(k_pages[pg, hkv, off]), np.ascontiguousarray(k_scale_pages[pg, hkv, off]),
+                np.ascontiguousarray(v_pages[pg, hkv, off]), np.ascontiguousarray(v_scale_pages[pg, hkv, off]))
+
+    return _decode(q, rows_of, k_pages.shape[1], lmax, seqlens, num_splits, split_size, rows, want_logits)
+
+
+def _decode(q, rows_of, hkv_n, lmax, seqlens, num_splits, split_size, rows, want_logits):
+    """The split loop shared by the decode oracles; rows_of(b, hkv, L) gives the kv head's
+    cache rows (k codes, k scales, v codes, v scales) for tokens 0 .. L-1 (at least)."""
+    q = _f32(q)
     seqlens = np.asarray(seqlens, np.int64)
     B, hq_n, d = q.shape
-    hkv_n, lmax = k_codes.shape[1], k_codes.shape[2]
     group = hq_n // hkv_n
     if split_size is None:
         split_size = max(1, -(-lmax // max(1, num_splits)))
@@ -275,11 +318,14 @@ def attn_decode(q, k_codes, k_scales, v_codes, v_scales, seqlens, num_splits=1, 
     l_part = np.full((B, hq_n, nsplit), np.nan, np.float64)
     logits = {}
     pairs = [(b, h) for b in range(B) for h in range(hq_n)] if rows is None else [(int(b), int(h)) for b, h in rows]
+    cached = {}
     for b, hq in pairs:
         hkv = hq // group
         L = int(seqlens[b])
-        kc, ksc = k_codes[b, hkv], k_scales[b, hkv]
-        vc, vsc = v_codes[b, hkv], v_scales[b, hkv]
+        if (b, hkv) not in cached:
+            cached.clear()
+            cached[(b, hkv)] = rows_of(b, hkv, L)
+        kc, ksc, vc, vsc = cached[(b, hkv)]
         for s in range(nsplit):
             o = np.zeros(d, np.float64)
             lv = np.zeros(1, np.float64)

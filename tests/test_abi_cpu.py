@@ -164,3 +164,25 @@ def test_oracle_builds_independently():
     assert "csrc" not in src and "sl8.h" not in src
     for f in os.listdir(os.path.join(ROOT, "w8a8_int8_flashattention_gb300", "csrc")):
         assert "oracle" not in open(os.path.join(ROOT, "w8a8_int8_flashattention_gb300", "csrc", f)).read().lower()
+
+
+def test_page_table_and_paginate_round_trip():
+    import workloads as W
+    w = W.custom(3301, kind="decode", B=4, Hq=4, Hkv=2, d=64, extra={"lengths": [0, 17, 64, 100]})
+    lens = W.seq_lengths(w)
+    table, num_pages = W.page_table(w, lens, 16, max_blocks=8, spare=2)
+    need = (lens + 15) // 16
+    assert num_pages == int(need.sum()) + 2
+    used = np.concatenate([table[b, :need[b]] for b in range(4)])
+    assert len(set(used.tolist())) == len(used) and used.min() >= 0 and used.max() < num_pages
+    assert all(np.all(table[b, need[b]:] == -1) for b in range(4))
+    rng = np.random.default_rng(5)
+    cache = rng.integers(-127, 128, size=(4, 2, 128, 64)).astype(np.int8)
+    scales = rng.uniform(0.01, 1.0, size=(4, 2, 128)).astype(np.float32)
+    pages, spages = W.paginate(cache, scales, table, lens, 16, num_pages)
+    for b in range(4):
+        for t in range(int(lens[b])):
+            np.testing.assert_array_equal(pages[table[b, t // 16], :, t % 16], cache[b, :, t])
+            np.testing.assert_array_equal(spages[table[b, t // 16], :, t % 16], scales[b, :, t])
+    shared, _ = W.page_table(w, lens, 16, max_blocks=8, shared_prefix=1)
+    assert shared[2, 0] == shared[0, 0] or lens[0] == 0

@@ -349,3 +349,110 @@ def test_combine_weights():
     out, l = oracle.decode_combine(o, lse)
     np.testing.assert_allclose(out[0], [(1 * 1 + 3 * 3) / 4, (2 * 1 + 4 * 3) / 4], rtol=0, atol=1e-15)
     np.testing.assert_allclose(l[0], math.log(4.0), rtol=0, atol=1e-15)
+
+
+# ---------------------------------------------------------------- paged (k8v8) decode
+
+def _contiguous_from_pages(pages, spages, table, lens, page):
+    """The contiguous cache [B, Hkv, max_blocks * page, d] that a paged cache stands for,
+    read token by token (t -> row t % page of page table[b, t // page])."""
+    B, lmax = table.shape[0], table.shape[1] * page
+    H, d = pages.shape[1], pages.shape[3]
+    c = np.zeros((B, H, lmax, d), pages.dtype)
+    s = np.zeros((B, H, lmax), spages.dtype)
+    for b in range(B):
+        for t in range(int(lens[b])):
+            c[b, :, t] = pages[table[b, t // page], :, t % page]
+            s[b, :, t] = spages[table[b, t // page], :, t % page]
+    return c, s
+
+
+def _assert_same_decode(a, b):
+    for key in ("out", "lse", "o_partial", "lse_partial", "q_codes", "q_scales"):
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+    assert a["logits"].keys() == b["logits"].keys()
+    for k in a["logits"]:
+        np.testing.assert_array_equal(a["logits"][k], b["logits"][k])
+
+
+def test_paged_decode_hand_layout():
+    # page size 2, one kv head, d 64: tokens 0,1 live in page 1 and token 2 in row 0 of
+    # page 0 (row 1 of page 0 holds junk that a length-3 sequence never reads)
+    rng = np.random.default_rng(40)
+    d = 64
+    tok_k = rng.integers(-127, 128, size=(3, d)).astype(np.int8)
+    tok_v = rng.integers(-127, 128, size=(3, d)).astype(np.int8)
+    tok_ks = np.array([0.01, 0.02, 0.03], np.float32)
+    tok_vs = np.array([0.5, 0.25, 0.125], np.float32)
+    kp = np.zeros((2, 1, 2, d), np.int8)
+    vp = np.zeros((2, 1, 2, d), np.int8)
+    ksp = np.zeros((2, 1, 2), np.float32)
+    vsp = np.zeros((2, 1, 2), np.float32)
+    kp[1, 0, 0], kp[1, 0, 1], kp[0, 0, 0] = tok_k
+    vp[1, 0, 0], vp[1, 0, 1], vp[0, 0, 0] = tok_v
+    ksp[1, 0, 0], ksp[1, 0, 1], ksp[0, 0, 0] = tok_ks
+    vsp[1, 0, 0], vsp[1, 0, 1], vsp[0, 0, 0] = tok_vs
+    kp[0, 0, 1] = 127
+    vp[0, 0, 1] = -127
+    ksp[0, 0, 1] = vsp[0, 0, 1] = 1e3
+    table = np.array([[1, 0]], np.int32)
+    q = rng.standard_normal((1, 2, d)).astype(np.float32)
+    paged = oracle.attn_paged_decode(q, kp, ksp, vp, vsp, table, [3], num_splits=2, want_logits=True)
+    kc = np.zeros((1, 1, 4, d), np.int8)
+    vc = np.zeros((1, 1, 4, d), np.int8)
+    kc[0, 0, :3], vc[0, 0, :3] = tok_k, tok_v
+    ks = np.zeros((1, 1, 4), np.float32)
+    vs = np.zeros((1, 1, 4), np.float32)
+    ks[0, 0, :3], vs[0, 0, :3] = tok_ks, tok_vs
+    flat = oracle.attn_decode(q, kc, ks, vc, vs, [3], num_splits=2, want_logits=True)
+    _assert_same_decode(paged, flat)
+    # and the logits are the plain int dots with the tokens in order
+    qc, _ = oracle.quant_rowwise(q)
+    np.testing.assert_array_equal(paged["logits"][(0, 1)], tok_k.astype(np.int64) @ qc[0, 1].astype(np.int64))
+
+
+@pytest.mark.parametrize("page", [16, 64])
+def test_paged_decode_equals_contiguous(page):
+    rng = np.random.default_rng(41 + page)
+    B, hq, hkv, d, max_blocks = 5, 8, 2, 64, 6
+    lens = np.array([0, 1, page - 1, page + 1, max_blocks * page])
+    need = (lens + page - 1) // page
+    num_pages = int(need.sum()) + 3                      # three pages nobody uses
+    perm = rng.permutation(num_pages)
+    table = np.full((B, max_blocks), -1, np.int32)
+    nxt = 0
+    for b in range(B):
+        table[b, :need[b]] = perm[nxt:nxt + need[b]]
+        nxt += need[b]
+    kp = rng.integers(-127, 128, size=(num_pages, hkv, page, d)).astype(np.int8)
+    vp = rng.integers(-127, 128, size=(num_pages, hkv, page, d)).astype(np.int8)
+    ksp = rng.uniform(0.001, 0.05, size=(num_pages, hkv, page)).astype(np.float32)
+    vsp = rng.uniform(0.001, 0.05, size=(num_pages, hkv, page)).astype(np.float32)
+    q = rng.standard_normal((B, hq, d)).astype(np.float32)
+    kc, ks = _contiguous_from_pages(kp, ksp, table, lens, page)
+    vc, vs = _contiguous_from_pages(vp, vsp, table, lens, page)
+    for ns in (1, 3):
+        paged = oracle.attn_paged_decode(q, kp, ksp, vp, vsp, table, lens, num_splits=ns, want_logits=True)
+        flat = oracle.attn_decode(q, kc, ks, vc, vs, lens, num_splits=ns, want_logits=True)
+        _assert_same_decode(paged, flat)
+
+
+def test_paged_decode_shared_prefix_pages():
+    # sequences 1 and 2 reuse sequence 0's first two pages (a common prompt prefix)
+    rng = np.random.default_rng(43)
+    page, d, hkv = 16, 64, 1
+    table = np.array([[3, 0, 5], [3, 0, 1], [3, 0, 4]], np.int32)
+    lens = np.array([40, 33, 48])
+    kp = rng.integers(-127, 128, size=(6, hkv, page, d)).astype(np.int8)
+    vp = rng.integers(-127, 128, size=(6, hkv, page, d)).astype(np.int8)
+    ksp = rng.uniform(0.001, 0.05, size=(6, hkv, page)).astype(np.float32)
+    vsp = rng.uniform(0.001, 0.05, size=(6, hkv, page)).astype(np.float32)
+    q = np.repeat(rng.standard_normal((1, 2, d)).astype(np.float32), 3, axis=0)
+    paged = oracle.attn_paged_decode(q, kp, ksp, vp, vsp, table, lens, num_splits=2)
+    kc, ks = _contiguous_from_pages(kp, ksp, table, lens, page)
+    vc, vs = _contiguous_from_pages(vp, vsp, table, lens, page)
+    flat = oracle.attn_decode(q, kc, ks, vc, vs, lens, num_splits=2)
+    _assert_same_decode(paged, flat)
+    # the shared prefix really is shared: the 32 common tokens are identical rows
+    np.testing.assert_array_equal(kc[0, :, :32], kc[1, :, :32])
+    np.testing.assert_array_equal(kc[0, :, :32], kc[2, :, :32])

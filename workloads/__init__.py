@@ -32,7 +32,7 @@ import torch
 SEED_BASE = 0x5EED0000
 
 # tensor tags (stream keys)
-TAG_Q, TAG_K, TAG_V, TAG_KBIAS, TAG_OUTLIER, TAG_LENS = 1, 2, 3, 4, 5, 6
+TAG_Q, TAG_K, TAG_V, TAG_KBIAS, TAG_OUTLIER, TAG_LENS, TAG_PAGES = 1, 2, 3, 4, 5, 6, 7
 
 
 @dataclass(frozen=True)
@@ -170,6 +170,60 @@ def decode_cache_values(w: Workload, b: int, which: str) -> np.ndarray:
     L = int(seq_lengths(w)[b])
     tag = TAG_K if which == "k" else TAG_V
     return _rng(w, tag, b).standard_normal((w.Hkv, L, w.d), dtype=np.float32)
+
+
+def page_table(w: Workload, lens, page_size: int, max_blocks: int | None = None, spare: int = 0,
+               shared_prefix: int = 0):
+    """A block table for a paged cache of the decode workload w.
+
+    Sequence b needs ceil(L_b / page_size) logical blocks.  The pages are a seeded
+    random permutation of 0 .. num_pages-1, where num_pages counts every block in use
+    plus `spare` pages nobody uses; entries past a sequence's last block are -1.  With
+    shared_prefix = n > 0, every sequence's first n blocks point at the pages of
+    sequence 0 (a shared prompt prefix).  Returns (block_table [B, max_blocks] int32,
+    num_pages)."""
+    lens = np.asarray(lens, np.int64)
+    need = (lens + page_size - 1) // page_size
+    if max_blocks is None:
+        max_blocks = int(max(1, need.max() if len(need) else 1))
+    own = [int(n) if b == 0 else max(0, int(n) - min(shared_prefix, int(need[0]), int(n)))
+           for b, n in enumerate(need)]
+    num_pages = int(sum(own)) + spare
+    perm = _rng(w, TAG_PAGES, page_size).permutation(max(num_pages, 1))
+    table = np.full((len(lens), max_blocks), -1, np.int32)
+    nxt = 0
+    for b, n in enumerate(need):
+        n = int(n)
+        share = 0 if b == 0 else min(shared_prefix, int(need[0]), n)
+        table[b, :share] = table[0, :share]
+        table[b, share:n] = perm[nxt:nxt + n - share]
+        nxt += n - share
+    return table, max(num_pages, 1)
+
+
+def paginate(cache, scales, block_table, lens, page_size: int, num_pages: int):
+    """Copy a contiguous cache [B, Hkv, Lmax, d] (+ scales [B, Hkv, Lmax]) into pages
+    [num_pages, Hkv, page_size, d] (+ [num_pages, Hkv, page_size]) following block_table:
+    token t of sequence b goes to row t % page_size of page block_table[b, t // page_size].
+    Works on numpy arrays or torch tensors (of any device); unused page rows are zero.
+    A page shared by several sequences receives each one's rows in turn (callers share
+    pages only between identical prefixes)."""
+    is_torch = isinstance(cache, torch.Tensor)
+    B, H, _, d = cache.shape
+    if is_torch:
+        pages = torch.zeros((num_pages, H, page_size, d), dtype=cache.dtype, device=cache.device)
+        spages = torch.zeros((num_pages, H, page_size), dtype=scales.dtype, device=scales.device)
+    else:
+        pages = np.zeros((num_pages, H, page_size, d), cache.dtype)
+        spages = np.zeros((num_pages, H, page_size), scales.dtype)
+    for b in range(B):
+        L = int(lens[b])
+        for i in range((L + page_size - 1) // page_size):
+            pg = int(block_table[b, i])
+            n = min(page_size, L - i * page_size)
+            pages[pg, :, :n] = cache[b, :, i * page_size:i * page_size + n]
+            spages[pg, :, :n] = scales[b, :, i * page_size:i * page_size + n]
+    return pages, spages
 
 
 def custom(wid: int, kind: str = "prefill", **fields) -> Workload:
