@@ -56,7 +56,7 @@ typedef enum sl8_status {
   SL8_ERR_WORKSPACE = 3,   /* workspace missing or smaller than the size query returned */
   SL8_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
   SL8_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up (see sl8_last_device_status) */
-  SL8_ERR_DEVICE_ARG = 6   /* the device found an out-of-range length (cu_seqlens / seqlens) */
+  SL8_ERR_DEVICE_ARG = 6   /* the device found an out-of-range length (cu_seqlens / seqlens) or page index */
 } sl8_status;
 
 typedef enum sl8_dtype { SL8_F16 = 0, SL8_BF16 = 1, SL8_F32 = 2, SL8_I8 = 3 } sl8_dtype;
@@ -175,6 +175,36 @@ SL8_API int sl8_attn_int8_decode_splitkv(const void* q, int q_dtype, const int8_
                                  const int8_t* v_cache, const float* v_scale, const int32_t* seqlens, int32_t B,
                                  int32_t Hq, int32_t Hkv, int32_t Lmax, int32_t d, int32_t num_splits,
                                  float* o_partial, float* lse_partial, void* stream);
+
+/*
+ * Split-KV decode over a paged int8 KV cache: the "Engine" table's "Paged KV cache" row
+ * (int8 / k8v3 / k8v8 cache formats) with the k8v8 format, and the "Attention kernels"
+ * table's attn_paged_decode row.  Same operation, split plan and outputs as
+ * sl8_attn_int8_decode_splitkv with Lmax = max_blocks * page_size; only the cache's
+ * storage differs (reading: the pages give no layout):
+ *   k_pages, v_pages            device, [num_pages][Hkv][page_size][d] int8 codes
+ *                               (16-byte aligned).
+ *   k_scale_pages, v_scale_pages device, [num_pages][Hkv][page_size] fp32 per-token
+ *                               scales (16-byte aligned).
+ *   block_table                 device, [B][max_blocks] int32: page of the logical block
+ *                               i = tokens [i * page_size, (i + 1) * page_size) of
+ *                               sequence b.  Token t of sequence b is row t % page_size
+ *                               of page block_table[b][t / page_size].  Entries past a
+ *                               sequence's last block are never read; pages may be
+ *                               shared between sequences (common prefixes).
+ *   page_size                   a multiple of 16 (SL8_ERR_UNSUPPORTED otherwise).
+ *   num_pages * Hkv * page_size must stay below 2^31.
+ * A block-table entry outside [0, num_pages) is reported as SL8_ERR_DEVICE_ARG by
+ * sl8_last_device_status and page 0 is read in its place.  The partials are merged
+ * with sl8_attn_decode_combine(..., Lmax = max_blocks * page_size, ...).
+ */
+SL8_API int sl8_attn_int8_paged_decode_splitkv(const void* q, int q_dtype, const int8_t* k_pages,
+                                               const float* k_scale_pages, const int8_t* v_pages,
+                                               const float* v_scale_pages, const int32_t* block_table,
+                                               int32_t max_blocks, int32_t page_size, int32_t num_pages,
+                                               const int32_t* seqlens, int32_t B, int32_t Hq, int32_t Hkv, int32_t d,
+                                               int32_t num_splits, float* o_partial, float* lse_partial,
+                                               void* stream);
 
 /*
  * Decode combine: merge the split partials of each (b, hq) row,

@@ -140,3 +140,82 @@ def test_full_size_decode_workload():
         np.testing.assert_array_equal(lg[b, h, :lens_np[b]], ref["logits"][(b, h)])
     for b in sample_b:
         np.testing.assert_array_equal(g["k"][b].cpu().numpy(), o["k"][b])
+
+
+# ---------------------------------------------------------------- paged (k8v8) cache
+
+PAGED = [
+    # wid, B, Hq, Hkv, d, lengths, page_size, max_blocks, shared prefix blocks
+    (3201, 5, 8, 2, 128, [1, 255, 256, 700, 0], 16, 44, 0),
+    (3202, 3, 4, 4, 64, [513, 17, 1024], 64, 16, 0),
+    (3203, 3, 8, 1, 256, [129, 300, 5], 32, 10, 0),
+    (3204, 4, 16, 2, 128, [2000, 77, 160, 161], 256, 8, 0),
+    (3205, 4, 8, 2, 128, [900, 640, 1000, 700], 128, 8, 5),
+]
+
+
+@pytest.mark.parametrize("case", PAGED, ids=[f"w{c[0]}_d{c[4]}_P{c[6]}" for c in PAGED])
+def test_paged_decode(case):
+    """Paged split-KV decode: parity with the oracle's paged decode, and the same bits as
+    the contiguous-cache kernel on the same tokens (same Lmax, same split plan)."""
+    wid, B, Hq, Hkv, d, lens, page, max_blocks, shared = case
+    lmax = page * max_blocks
+    w = W.custom(wid, kind="decode", B=B, Hq=Hq, Hkv=Hkv, d=d, dtype="bf16", extra={"lengths": lens})
+    lens_np, g, gs, o, os_ = build_cache(w, lmax)
+    if shared:
+        # sequences 1.. share sequence 0's first `shared` blocks: give them the same rows
+        n = shared * page
+        for b in range(1, B):
+            for src, dst in ((g, g), (gs, gs), (o, o), (os_, os_)):
+                for key in ("k", "v"):
+                    dst[key][b, :, :n] = src[key][0, :, :n]
+    table, num_pages = W.page_table(w, lens_np, page, max_blocks=max_blocks, spare=3, shared_prefix=shared)
+    gp, op_ = {}, {}
+    for key in ("k", "v"):
+        gp[key] = W.paginate(g[key], gs[key], table, lens_np, page, num_pages)
+        op_[key] = W.paginate(o[key], os_[key], table, lens_np, page, num_pages)
+    q = W.decode_query(w)
+    qd = q.to(DEV)
+    seq = torch.from_numpy(lens_np.astype(np.int32)).to(DEV)
+    tab = torch.from_numpy(table).to(DEV)
+    for ns in (0, 1, 3):
+        ref = oracle.attn_paged_decode(q.float().numpy(), op_["k"][0], op_["k"][1], op_["v"][0], op_["v"][1],
+                                       table, lens_np, split_size=sl8.lib().sl8_attn_decode_split_size(
+                                           B, Hkv, lmax, d, ns))
+        o32, lse = sl8.attn_int8_paged_decode(qd, gp["k"][0], gp["k"][1], gp["v"][0], gp["v"][1], tab, seq,
+                                              num_splits=ns, out_dtype=torch.float32, return_lse=True)
+        ob = sl8.attn_int8_paged_decode(qd, gp["k"][0], gp["k"][1], gp["v"][0], gp["v"][1], tab, seq,
+                                        num_splits=ns)
+        flat32 = sl8.attn_int8_decode(qd, g["k"], gs["k"], g["v"], gs["v"], seq, num_splits=ns,
+                                      out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        check_f32(to_np32(o32), ref["out"], f"w{wid} paged splits={ns} f32")
+        check_half(ob, ref["out"], f"w{wid} paged splits={ns} bf16")
+        ok = lens_np > 0
+        np.testing.assert_allclose(to_np32(lse)[ok], ref["lse"][ok], rtol=0, atol=1e-4)
+        assert np.all(np.isneginf(to_np32(lse)[~ok]))
+        assert torch.equal(o32, flat32), f"w{wid} splits={ns}: paged and contiguous kernels differ"
+    st, site = sl8.last_device_status()
+    assert st == sl8.SL8_OK, (st, site)
+
+
+def test_paged_decode_bad_page_is_reported():
+    """A block-table entry outside [0, num_pages) is reported on the device (and page 0 is
+    read instead); the context stays usable."""
+    w = W.custom(3206, kind="decode", B=2, Hq=4, Hkv=2, d=128, dtype="bf16", extra={"lengths": [100, 40]})
+    lens_np, g, gs, o, os_ = build_cache(w, 128)
+    table, num_pages = W.page_table(w, lens_np, 16, max_blocks=8)
+    pk = W.paginate(g["k"], gs["k"], table, lens_np, 16, num_pages)
+    pv = W.paginate(g["v"], gs["v"], table, lens_np, 16, num_pages)
+    bad = table.copy()
+    bad[0, 3] = num_pages + 7
+    q = W.decode_query(w).to(DEV)
+    seq = torch.from_numpy(lens_np.astype(np.int32)).to(DEV)
+    sl8.last_device_status()
+    sl8.attn_int8_paged_decode(q, pk[0], pk[1], pv[0], pv[1], torch.from_numpy(bad).to(DEV), seq)
+    st, site = sl8.last_device_status()
+    assert st == sl8.SL8_ERR_DEVICE_ARG, (st, site)
+    out = sl8.attn_int8_paged_decode(q, pk[0], pk[1], pv[0], pv[1], torch.from_numpy(table).to(DEV), seq)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()
+    assert sl8.last_device_status()[0] == sl8.SL8_OK

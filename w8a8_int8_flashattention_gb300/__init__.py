@@ -73,6 +73,8 @@ _SIGNATURES = {
     "sl8_attn_decode_split_size": (_I32, [_I32, _I32, _I32, _I32, _I32]),
     "sl8_attn_int8_decode_splitkv": (_INT, [_P, _INT, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P,
                                             _P, _P]),
+    "sl8_attn_int8_paged_decode_splitkv": (_INT, [_P, _INT, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _I32, _I32,
+                                                  _I32, _I32, _I32, _P, _P, _P]),
     "sl8_attn_decode_combine": (_INT, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _INT, _P, _P]),
     "sl8_attn_int8_decode_logits_debug": (_INT, [_P, _INT, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P,
                                                  _P, _P, _P, _P]),
@@ -298,6 +300,37 @@ def attn_int8_decode(q, k_cache, k_scale, v_cache, v_scale, seqlens, num_splits=
     o_p, l_p = attn_int8_decode_splitkv(q, k_cache, k_scale, v_cache, v_scale, seqlens, num_splits, o_partial,
                                         lse_partial)
     return attn_decode_combine(o_p, l_p, seqlens, k_cache.shape[2], out_dtype or q.dtype, return_lse, out)
+
+
+def attn_int8_paged_decode_splitkv(q, k_pages, k_scale_pages, v_pages, v_scale_pages, block_table, seqlens,
+                                   num_splits=0, o_partial=None, lse_partial=None):
+    """Split-KV partials over a paged k8v8 cache: pages [num_pages, Hkv, page_size, d] int8,
+    scales [num_pages, Hkv, page_size] fp32, block_table [B, max_blocks] int32."""
+    _need_cuda(q, k_pages, k_scale_pages, v_pages, v_scale_pages, block_table, seqlens)
+    B, Hq, d = q.shape
+    num_pages, Hkv, page_size, _ = k_pages.shape
+    max_blocks = block_table.shape[1]
+    S = decode_num_splits(B, Hkv, max_blocks * page_size, d, num_splits)
+    if o_partial is None:
+        o_partial = torch.empty((B, Hq, max(S, 1), d), dtype=torch.float32, device=q.device)
+    if lse_partial is None:
+        lse_partial = torch.empty((B, Hq, max(S, 1)), dtype=torch.float32, device=q.device)
+    _check(lib().sl8_attn_int8_paged_decode_splitkv(_ptr(q), _dt(q), _ptr(k_pages), _ptr(k_scale_pages),
+                                                    _ptr(v_pages), _ptr(v_scale_pages), _ptr(block_table),
+                                                    max_blocks, page_size, num_pages, _ptr(seqlens), B, Hq, Hkv, d,
+                                                    num_splits, _ptr(o_partial), _ptr(lse_partial),
+                                                    _stream(q.device)),
+           "sl8_attn_int8_paged_decode_splitkv")
+    return o_partial, lse_partial
+
+
+def attn_int8_paged_decode(q, k_pages, k_scale_pages, v_pages, v_scale_pages, block_table, seqlens, num_splits=0,
+                           out_dtype=None, return_lse=False, o_partial=None, lse_partial=None, out=None):
+    """Paged split-KV decode plus combine: out [B, Hq, d] (dtype q.dtype unless given)."""
+    o_p, l_p = attn_int8_paged_decode_splitkv(q, k_pages, k_scale_pages, v_pages, v_scale_pages, block_table,
+                                              seqlens, num_splits, o_partial, lse_partial)
+    lmax = block_table.shape[1] * k_pages.shape[2]
+    return attn_decode_combine(o_p, l_p, seqlens, lmax, out_dtype or q.dtype, return_lse, out)
 
 
 def attn_int8_decode_logits_debug(q, k_cache, k_scale, v_cache, v_scale, seqlens):

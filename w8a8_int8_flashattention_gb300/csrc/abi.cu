@@ -483,9 +483,15 @@ int32_t sl8_attn_decode_split_size(int32_t B, int32_t Hkv, int32_t Lmax, int32_t
   return S > 0 ? split_size_for(Lmax, S, d) : 0;
 }
 
+// A paged cache (see DecodeArgs): the block table and the page geometry.
+struct Paging {
+  const int32_t* table;
+  int32_t page_size, max_blocks, num_pages;
+};
+
 static int decode_validate(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale,
                            const int8_t* v_cache, const float* v_scale, const int32_t* seqlens, int32_t B, int32_t Hq,
-                           int32_t Hkv, int32_t Lmax, int32_t d) {
+                           int32_t Hkv, int32_t Lmax, int32_t d, const Paging* pg) {
   SL8_CHECK(q && k_cache && k_scale && v_cache && v_scale && seqlens, SL8_ERR_INVALID_ARG);
   SL8_CHECK(aligned16(q) && aligned16(k_cache) && aligned16(v_cache), SL8_ERR_INVALID_ARG);
   SL8_CHECK(q_dtype == SL8_F16 || q_dtype == SL8_BF16 || q_dtype == SL8_F32, SL8_ERR_INVALID_ARG);
@@ -494,16 +500,24 @@ static int decode_validate(const void* q, int q_dtype, const int8_t* k_cache, co
   SL8_CHECK(head_dim_ok(d), SL8_ERR_UNSUPPORTED);
   SL8_CHECK(Hq / Hkv <= 8, SL8_ERR_UNSUPPORTED);
   SL8_CHECK(B <= 65535 && Hkv <= 65535, SL8_ERR_UNSUPPORTED);
-  // the caches are addressed as [B * Hkv * Lmax] rows with 32-bit row coordinates
-  SL8_CHECK(static_cast<int64_t>(B) * Hkv * Lmax < (int64_t(1) << 31), SL8_ERR_UNSUPPORTED);
+  if (pg) {
+    // pages are loaded in 16-token units (TMA rows, 64-byte scale pieces)
+    SL8_CHECK(pg->table && pg->page_size > 0 && pg->max_blocks > 0 && pg->num_pages > 0, SL8_ERR_INVALID_ARG);
+    SL8_CHECK(pg->page_size % 16 == 0, SL8_ERR_UNSUPPORTED);
+    SL8_CHECK(aligned16(k_scale) && aligned16(v_scale), SL8_ERR_INVALID_ARG);
+    SL8_CHECK(static_cast<int64_t>(pg->num_pages) * Hkv * pg->page_size < (int64_t(1) << 31), SL8_ERR_UNSUPPORTED);
+  } else {
+    // the caches are addressed as [B * Hkv * Lmax] rows with 32-bit row coordinates
+    SL8_CHECK(static_cast<int64_t>(B) * Hkv * Lmax < (int64_t(1) << 31), SL8_ERR_UNSUPPORTED);
+  }
   return SL8_OK;
 }
 
 static int decode_launch(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale, const int8_t* v_cache,
                          const float* v_scale, const int32_t* seqlens, int32_t B, int32_t Hq, int32_t Hkv, int32_t Lmax,
                          int32_t d, int32_t num_splits, float* o_partial, float* lse_partial, int32_t* logits,
-                         int8_t* q_codes, float* q_scales, void* stream) {
-  int rc = decode_validate(q, q_dtype, k_cache, k_scale, v_cache, v_scale, seqlens, B, Hq, Hkv, Lmax, d);
+                         int8_t* q_codes, float* q_scales, void* stream, const Paging* pg = nullptr) {
+  int rc = decode_validate(q, q_dtype, k_cache, k_scale, v_cache, v_scale, seqlens, B, Hq, Hkv, Lmax, d, pg);
   if (rc != SL8_OK) return rc;
   SL8_CHECK(o_partial && lse_partial && num_splits >= 0, SL8_ERR_INVALID_ARG);
   if (B == 0 || Lmax == 0) return SL8_OK;
@@ -528,8 +542,28 @@ static int decode_launch(const void* q, int q_dtype, const int8_t* k_cache, cons
   a.logits = logits;
   a.q_codes = q_codes;
   a.q_scales = q_scales;
+  if (pg) {
+    a.block_table = pg->table;
+    a.page_size = pg->page_size;
+    a.max_blocks = pg->max_blocks;
+    a.num_pages = pg->num_pages;
+  }
   SL8_LAUNCH(launch_decode_split(a, static_cast<cudaStream_t>(stream)));
   return SL8_OK;
+}
+
+int sl8_attn_int8_paged_decode_splitkv(const void* q, int q_dtype, const int8_t* k_pages, const float* k_scale_pages,
+                                       const int8_t* v_pages, const float* v_scale_pages, const int32_t* block_table,
+                                       int32_t max_blocks, int32_t page_size, int32_t num_pages,
+                                       const int32_t* seqlens, int32_t B, int32_t Hq, int32_t Hkv, int32_t d,
+                                       int32_t num_splits, float* o_partial, float* lse_partial, void* stream) {
+  SL8_CHECK(max_blocks > 0 && page_size > 0, SL8_ERR_INVALID_ARG);
+  const int64_t lmax = static_cast<int64_t>(max_blocks) * page_size;
+  SL8_CHECK(lmax < (int64_t(1) << 31), SL8_ERR_UNSUPPORTED);
+  const Paging pg{block_table, page_size, max_blocks, num_pages};
+  return decode_launch(q, q_dtype, k_pages, k_scale_pages, v_pages, v_scale_pages, seqlens, B, Hq, Hkv,
+                       static_cast<int32_t>(lmax), d, num_splits, o_partial, lse_partial, nullptr, nullptr, nullptr,
+                       stream, &pg);
 }
 
 int sl8_attn_int8_decode_splitkv(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale,

@@ -459,6 +459,33 @@ __global__ void __launch_bounds__(DCfg<D>::kThreads, 1)
         uint8_t* base = smem + stg * C::kStageBytes;
         if (k >= kStages) ok = warp_wait(&empty[stg], ((k / kStages) - 1) & 1, limit_ns, st, 41);
         if (!ok) break;
+        if (a.block_table) {
+          // paged cache: one 16-token unit per lane, each inside one page (page_size is a
+          // multiple of 16); units past the split's end are not loaded (their compute
+          // warps skip them)
+          const int units = (nt + kUnit - 1) / kUnit;
+          if (lane == 0)
+            mbar_arrive_expect_tx(&full[stg], static_cast<uint32_t>(units * 2 * kUnit * (D + 4)));
+          __syncwarp();
+          if (lane < units) {
+            const int t = c0 + lane * kUnit;
+            int pg = a.block_table[static_cast<int64_t>(cur.b) * a.max_blocks + t / a.page_size];
+            if (pg < 0 || pg >= a.num_pages) {
+              record_status(st, kStatusBadArg, 49);
+              pg = 0;
+            }
+            const int64_t prow = (static_cast<int64_t>(pg) * a.Hkv + cur.hkv) * a.page_size + t % a.page_size;
+#pragma unroll
+            for (int b = 0; b < C::kBoxes; ++b) {
+              const uint32_t dst = static_cast<uint32_t>(b * C::kChunk * C::kBW + lane * kUnit * C::kBW);
+              tma_load_3d(base + C::kSK + dst, &map_k, &full[stg], b * C::kBW, static_cast<int>(prow), 0);
+              tma_load_3d(base + C::kSV + dst, &map_v, &full[stg], b * C::kBW, static_cast<int>(prow), 0);
+            }
+            bulk_load(base + C::kSKs + lane * kUnit * 4, a.k_scale + prow, kUnit * 4, &full[stg]);
+            bulk_load(base + C::kSVs + lane * kUnit * 4, a.v_scale + prow, kUnit * 4, &full[stg]);
+          }
+          continue;
+        }
         if (!scales_bulk) {
           for (int j = lane; j < nt; j += 32) {
             reinterpret_cast<float*>(base + C::kSKs)[j] = a.k_scale[row0 + c0 + j];
@@ -1005,13 +1032,17 @@ cudaError_t launch_split_d(const DecodeArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
   if (e != cudaSuccess) return e;
   // each cache as a 2-D [B * Hkv * Lmax rows][d bytes] tensor, loaded in boxes of
-  // C::kChunk rows x kBW bytes
-  const uint64_t rows = static_cast<uint64_t>(a.B) * a.Hkv * a.Lmax;
+  // C::kChunk rows x kBW bytes; a paged cache as [num_pages * Hkv * page_size rows][d],
+  // loaded in boxes of one 16-token unit
+  const bool paged = a.block_table != nullptr;
+  const uint64_t rows = paged ? static_cast<uint64_t>(a.num_pages) * a.Hkv * a.page_size
+                              : static_cast<uint64_t>(a.B) * a.Hkv * a.Lmax;
+  const uint32_t box_rows = paged ? kUnit : C::kChunk;
   bool ok = true;
   const CUtensorMap mk = make_tmap_3d(a.k_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, D, rows, 1, D, rows * D, C::kBW,
-                                      C::kChunk, 1, &ok, C::kSwz);
+                                      box_rows, 1, &ok, C::kSwz);
   const CUtensorMap mv = make_tmap_3d(a.v_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, D, rows, 1, D, rows * D, C::kBW,
-                                      C::kChunk, 1, &ok, C::kSwz);
+                                      box_rows, 1, &ok, C::kSwz);
   if (!ok) return cudaErrorInvalidValue;
   const int64_t slots = static_cast<int64_t>(a.num_splits) * a.B * a.Hkv;
   const int grid = static_cast<int>(slots < num_sms() ? slots : num_sms());

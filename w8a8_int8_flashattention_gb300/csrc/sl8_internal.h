@@ -154,6 +154,12 @@ struct DecodeArgs {
   int32_t* logits;   // debug: [B][Hq][Lmax] int32 (nullable)
   int8_t* q_codes;   // nullable
   float* q_scales;   // nullable
+  // paged cache (block_table non-null): k_cache / v_cache are pages [num_pages][Hkv]
+  // [page_size][d], the scales [num_pages][Hkv][page_size]; token t of sequence b is
+  // row t % page_size of page block_table[b * max_blocks + t / page_size]; Lmax is
+  // max_blocks * page_size
+  const int32_t* block_table;
+  int32_t page_size, max_blocks, num_pages;
 };
 cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_combine(const float* o_partial, const float* lse_partial, const int32_t* seqlens,

@@ -204,25 +204,42 @@ def page_table(w: Workload, lens, page_size: int, max_blocks: int | None = None,
 def paginate(cache, scales, block_table, lens, page_size: int, num_pages: int):
     """Copy a contiguous cache [B, Hkv, Lmax, d] (+ scales [B, Hkv, Lmax]) into pages
     [num_pages, Hkv, page_size, d] (+ [num_pages, Hkv, page_size]) following block_table:
-    token t of sequence b goes to row t % page_size of page block_table[b, t // page_size].
-    Works on numpy arrays or torch tensors (of any device); unused page rows are zero.
-    A page shared by several sequences receives each one's rows in turn (callers share
-    pages only between identical prefixes)."""
+    logical block i of sequence b (tokens [i * page_size, (i + 1) * page_size)) becomes
+    page block_table[b, i], for the blocks that hold tokens t < L_b.  Works on numpy
+    arrays or torch tensors (of any device); pages no block uses stay zero.  A page shared
+    by several sequences receives each one's block (callers share pages only between
+    identical prefixes)."""
     is_torch = isinstance(cache, torch.Tensor)
-    B, H, _, d = cache.shape
+    B, H, lmax, d = cache.shape
+    nb = block_table.shape[1]
+    lens = np.asarray(lens, np.int64)
+    need = (lens + page_size - 1) // page_size
+    table = np.asarray(block_table.cpu() if isinstance(block_table, torch.Tensor) else block_table, np.int64)
+    sel_b, sel_i = np.nonzero(np.arange(nb)[None, :] < need[:, None])
+    dst = table[sel_b, sel_i]
     if is_torch:
+        pad = nb * page_size - lmax
+        c = torch.nn.functional.pad(cache, (0, 0, 0, max(pad, 0)))[:, :, :nb * page_size]
+        sc = torch.nn.functional.pad(scales, (0, max(pad, 0)))[:, :, :nb * page_size]
+        blocks = c.reshape(B, H, nb, page_size, d).permute(0, 2, 1, 3, 4)
+        sblocks = sc.reshape(B, H, nb, page_size).permute(0, 2, 1, 3)
         pages = torch.zeros((num_pages, H, page_size, d), dtype=cache.dtype, device=cache.device)
         spages = torch.zeros((num_pages, H, page_size), dtype=scales.dtype, device=scales.device)
+        ib = torch.from_numpy(sel_b).to(cache.device)
+        ii = torch.from_numpy(sel_i).to(cache.device)
+        it = torch.from_numpy(dst).to(cache.device)
+        pages[it] = blocks[ib, ii]
+        spages[it] = sblocks[ib, ii]
     else:
+        pad = max(nb * page_size - lmax, 0)
+        c = np.pad(cache, ((0, 0), (0, 0), (0, pad), (0, 0)))[:, :, :nb * page_size]
+        sc = np.pad(scales, ((0, 0), (0, 0), (0, pad)))[:, :, :nb * page_size]
+        blocks = c.reshape(B, H, nb, page_size, d).transpose(0, 2, 1, 3, 4)
+        sblocks = sc.reshape(B, H, nb, page_size).transpose(0, 2, 1, 3)
         pages = np.zeros((num_pages, H, page_size, d), cache.dtype)
         spages = np.zeros((num_pages, H, page_size), scales.dtype)
-    for b in range(B):
-        L = int(lens[b])
-        for i in range((L + page_size - 1) // page_size):
-            pg = int(block_table[b, i])
-            n = min(page_size, L - i * page_size)
-            pages[pg, :, :n] = cache[b, :, i * page_size:i * page_size + n]
-            spages[pg, :, :n] = scales[b, :, i * page_size:i * page_size + n]
+        pages[dst] = blocks[sel_b, sel_i]
+        spages[dst] = sblocks[sel_b, sel_i]
     return pages, spages
 
 
