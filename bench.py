@@ -7,7 +7,9 @@ One step = one pass of the whole path over one batch of synthetic input:
   * decode: split-KV over an int8 KV cache, B64 Hq32 Hkv8 d128, context lengths
     uniform on [1024, 8192] (q quantisation, split kernel, combine).
 `value` is prefill TOPS (ops = 2 x 2 x d x causal pairs x heads, QK^T and P.V);
-the decode KV GB/s sits in `decode`.  Inputs are resident in HBM when the timed
+the decode KV GB/s sits in `decode`, and `paged_decode` repeats the decode over a
+paged k8v8 cache (64-token pages in a seeded random order) in a loop of its own after
+the timed steps.  Inputs are resident in HBM when the timed
 region starts; L2 is flushed before every step, outside the timed events (a 256 MB
 write, then a read of that buffer, so no dirty lines of the flush remain).  `e2e` repeats the prefill through the public API with pinned host
 inputs copied in and the output copied back every step.
@@ -301,6 +303,12 @@ def run_ours(args, world, rank, local):
                                           for n, (c, ms) in sorted(trace.items())}}), flush=True)
         return
 
+    # ---- the same decode over a paged k8v8 cache
+    pg_ms, pg_split_ms, pg_steps, pg_pages = measure_paged(sl8, W, wd, kc, ks, vc, vs, lens, qdec, seq, stream, flush,
+                                                           flush_sink, args.steps, args.warmup, world)
+    pg_gbs = dbytes * world / (pg_ms * 1e-3) / 1e9
+    pg_split_gbs = dbytes / (pg_split_ms * 1e-3) / 1e9
+
     # ---- e2e: public API with pinned host buffers, H2D inputs + D2H output every step
     qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
     oh = torch.empty(q.shape, dtype=q.dtype).pin_memory()
@@ -348,6 +356,12 @@ def run_ours(args, world, rank, local):
                                 "frac": split_gbs / peaks["hbm_gbs"],
                                 "traffic": traffic.get("decode_split"), "kernel": "decode_split",
                                 "peak_source": peaks["source"]}},
+        "paged_decode": {"value": pg_gbs, "unit": "GB/s", "ms": pg_ms, "steps": pg_steps,
+                         "config": f"the decode workload over a paged k8v8 cache, {PAGE_SIZE}-token pages in a "
+                                   f"seeded random order ({pg_pages} pages), L2 flushed before every step",
+                         "roofline": {"bound": "hbm", "achieved": pg_split_gbs, "peak": peaks["hbm_gbs"],
+                                      "unit": "GB/s", "frac": pg_split_gbs / peaks["hbm_gbs"], "traffic": None,
+                                      "kernel": "decode_split (paged)", "peak_source": peaks["source"]}},
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": attn_tflops / peaks["bf16_tflops"], "traffic": traffic.get("prefill_attn"),
                      "kernel": "prefill_attn", "launch_ms": attn_ms,
@@ -361,6 +375,51 @@ def run_ours(args, world, rank, local):
         "wall_s_timed": t_wall,
     }
     print(json.dumps(line), flush=True)
+
+
+PAGE_SIZE = 64
+
+
+def measure_paged(sl8, W, wd, kc, ks, vc, vs, lens, qdec, seq, stream, flush, flush_sink, steps, warmup, world):
+    """The same decode workload over a paged k8v8 cache (16-token pages in a seeded random
+    order): the step is the paged split kernel plus the combine, L2 flushed before each."""
+    import torch
+    table, num_pages = W.page_table(wd, lens, PAGE_SIZE, max_blocks=wd.lmax // PAGE_SIZE)
+    kp, ksp = W.paginate(kc, ks, table, lens, PAGE_SIZE, num_pages)
+    vp, vsp = W.paginate(vc, vs, table, lens, PAGE_SIZE, num_pages)
+    tab = torch.from_numpy(table).to(kc.device)
+    S = sl8.decode_num_splits(wd.B, wd.Hkv, wd.lmax, wd.d, 0)
+    o_part = torch.empty((wd.B, wd.Hq, S, wd.d), dtype=torch.float32, device=kc.device)
+    l_part = torch.empty((wd.B, wd.Hq, S), dtype=torch.float32, device=kc.device)
+    dout = torch.empty((wd.B, wd.Hq, wd.d), dtype=torch.bfloat16, device=kc.device)
+
+    def step(ev=None):
+        flush.zero_()
+        flush_sink.copy_(flush.view(torch.int64).sum())
+        if ev:
+            ev[0].record(stream)
+        sl8.attn_int8_paged_decode(qdec, kp, ksp, vp, vsp, tab, seq, o_partial=o_part, lse_partial=l_part, out=dout)
+        if ev:
+            ev[1].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(kc.device)
+    n = max(3, min(steps, 100))
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    sl8.trace_collect()
+    sl8.trace_enable(True)
+    for i in range(n):
+        step(events[i])
+    torch.cuda.synchronize(kc.device)
+    sl8.trace_enable(False)
+    trace = sl8.trace_collect()
+    st, site = sl8.last_device_status(kc.device)
+    if st != sl8.SL8_OK:
+        raise RuntimeError(f"device status {st} at {site} during the paged decode")
+    ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in events) / n, world)
+    c, split_ms = trace.get("decode_split", (0, 0.0))
+    return ms, (split_ms / c if c else float("nan")), n, num_pages
 
 
 def load_traffic():

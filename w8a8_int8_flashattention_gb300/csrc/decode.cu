@@ -326,11 +326,18 @@ __device__ __forceinline__ bool slot_at(const DecodeArgs& a, const Sched* sc, bo
   return true;
 }
 
+// Tensor maps of the two caches.  Contiguous cache: [0] only, boxes of one stage
+// (kChunk rows).  Paged cache: boxes of 16 << i rows (i < kPageBoxes), so that a stage's
+// rows inside one page go in a few large copies.
+constexpr int kPageBoxes = 4;
+struct CacheMaps {
+  CUtensorMap k[kPageBoxes], v[kPageBoxes];
+};
+
 template <int D>
 __global__ void __launch_bounds__(DCfg<D>::kThreads, 1)
-    decode_split_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap map_k,
-                        const __grid_constant__ CUtensorMap map_v, uint32_t ticket, DeviceStatus* st,
-                        uint64_t limit_ns) {
+    decode_split_kernel(const DecodeArgs a, const __grid_constant__ CacheMaps maps, uint32_t ticket,
+                        DeviceStatus* st, uint64_t limit_ns) {
   using C = DCfg<D>;
   constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -380,8 +387,10 @@ __global__ void __launch_bounds__(DCfg<D>::kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ loader
     if (lane == 0) {
-      prefetch_tensormap(&map_k);
-      prefetch_tensormap(&map_v);
+      for (int i = 0; i < (a.block_table ? kPageBoxes : 1); ++i) {
+        prefetch_tensormap(&maps.k[i]);
+        prefetch_tensormap(&maps.v[i]);
+      }
     }
     // Slot n + 1 is claimed (and its q rows requested) before the stages of slot n, so
     // that its q rows are quantised while slot n streams; the claim of slot n + 2 is in
@@ -457,32 +466,42 @@ __global__ void __launch_bounds__(DCfg<D>::kThreads, 1)
         const int nt = min(C::kChunk, cur.t1 - c0);
         const uint32_t stg = k % kStages;
         uint8_t* base = smem + stg * C::kStageBytes;
+        // paged cache: the page of this lane's unit, read before the wait for the stage
+        // so that the wait covers the load's latency
+        const int t = c0 + lane * kUnit;
+        const int units = (nt + kUnit - 1) / kUnit;
+        int pg = 0;
+        if (a.block_table && lane < units) pg = a.block_table[static_cast<int64_t>(cur.b) * a.max_blocks + t / a.page_size];
         if (k >= kStages) ok = warp_wait(&empty[stg], ((k / kStages) - 1) & 1, limit_ns, st, 41);
         if (!ok) break;
         if (a.block_table) {
-          // paged cache: one 16-token unit per lane, each inside one page (page_size is a
-          // multiple of 16); units past the split's end are not loaded (their compute
-          // warps skip them)
-          const int units = (nt + kUnit - 1) / kUnit;
+          // paged cache: the stage's 16-token units (page_size is a multiple of 16; units
+          // past the split's end are not loaded, their compute warps skip them) fall into
+          // pieces that each lie in one page; the lane of a piece's first unit loads the
+          // piece in boxes of 128/64/32/16 rows and its scales in one bulk copy each
           if (lane == 0)
             mbar_arrive_expect_tx(&full[stg], static_cast<uint32_t>(units * 2 * kUnit * (D + 4)));
           __syncwarp();
-          if (lane < units) {
-            const int t = c0 + lane * kUnit;
-            int pg = a.block_table[static_cast<int64_t>(cur.b) * a.max_blocks + t / a.page_size];
+          if (lane < units && (lane == 0 || t % a.page_size == 0)) {
+            const int rows = min(a.page_size - t % a.page_size, (units - lane) * kUnit);
             if (pg < 0 || pg >= a.num_pages) {
               record_status(st, kStatusBadArg, 49);
               pg = 0;
             }
             const int64_t prow = (static_cast<int64_t>(pg) * a.Hkv + cur.hkv) * a.page_size + t % a.page_size;
+            for (int r = 0; r < rows;) {
+              const int left = rows - r;
+              const int i = left >= 128 ? 3 : left >= 64 ? 2 : left >= 32 ? 1 : 0;
 #pragma unroll
-            for (int b = 0; b < C::kBoxes; ++b) {
-              const uint32_t dst = static_cast<uint32_t>(b * C::kChunk * C::kBW + lane * kUnit * C::kBW);
-              tma_load_3d(base + C::kSK + dst, &map_k, &full[stg], b * C::kBW, static_cast<int>(prow), 0);
-              tma_load_3d(base + C::kSV + dst, &map_v, &full[stg], b * C::kBW, static_cast<int>(prow), 0);
+              for (int b = 0; b < C::kBoxes; ++b) {
+                const uint32_t dst = static_cast<uint32_t>(b * C::kChunk * C::kBW + (lane * kUnit + r) * C::kBW);
+                tma_load_3d(base + C::kSK + dst, &maps.k[i], &full[stg], b * C::kBW, static_cast<int>(prow + r), 0);
+                tma_load_3d(base + C::kSV + dst, &maps.v[i], &full[stg], b * C::kBW, static_cast<int>(prow + r), 0);
+              }
+              r += kUnit << i;
             }
-            bulk_load(base + C::kSKs + lane * kUnit * 4, a.k_scale + prow, kUnit * 4, &full[stg]);
-            bulk_load(base + C::kSVs + lane * kUnit * 4, a.v_scale + prow, kUnit * 4, &full[stg]);
+            bulk_load(base + C::kSKs + lane * kUnit * 4, a.k_scale + prow, static_cast<uint32_t>(rows * 4), &full[stg]);
+            bulk_load(base + C::kSVs + lane * kUnit * 4, a.v_scale + prow, static_cast<uint32_t>(rows * 4), &full[stg]);
           }
           continue;
         }
@@ -499,8 +518,8 @@ __global__ void __launch_bounds__(DCfg<D>::kThreads, 1)
           const int y = static_cast<int>(row0 + c0);
 #pragma unroll
           for (int b = 0; b < C::kBoxes; ++b) {
-            tma_load_3d(base + C::kSK + b * C::kChunk * C::kBW, &map_k, &full[stg], b * C::kBW, y, 0);
-            tma_load_3d(base + C::kSV + b * C::kChunk * C::kBW, &map_v, &full[stg], b * C::kBW, y, 0);
+            tma_load_3d(base + C::kSK + b * C::kChunk * C::kBW, &maps.k[0], &full[stg], b * C::kBW, y, 0);
+            tma_load_3d(base + C::kSV + b * C::kChunk * C::kBW, &maps.v[0], &full[stg], b * C::kBW, y, 0);
           }
           if (scales_bulk) {
             bulk_load(base + C::kSKs, a.k_scale + row0 + c0, sc_bytes, &full[stg]);
@@ -1037,18 +1056,24 @@ cudaError_t launch_split_d(const DecodeArgs& a, cudaStream_t s) {
   const bool paged = a.block_table != nullptr;
   const uint64_t rows = paged ? static_cast<uint64_t>(a.num_pages) * a.Hkv * a.page_size
                               : static_cast<uint64_t>(a.B) * a.Hkv * a.Lmax;
-  const uint32_t box_rows = paged ? kUnit : C::kChunk;
   bool ok = true;
-  const CUtensorMap mk = make_tmap_3d(a.k_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, D, rows, 1, D, rows * D, C::kBW,
-                                      box_rows, 1, &ok, C::kSwz);
-  const CUtensorMap mv = make_tmap_3d(a.v_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, D, rows, 1, D, rows * D, C::kBW,
-                                      box_rows, 1, &ok, C::kSwz);
+  CacheMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  for (int i = 0; i < (paged ? kPageBoxes : 1); ++i) {
+    // a box taller than the whole pool is never used (a piece lies in one page)
+    const uint32_t box_rows = paged ? static_cast<uint32_t>(std::min<uint64_t>(static_cast<uint64_t>(kUnit) << i, rows / kUnit * kUnit))
+                                    : C::kChunk;
+    maps.k[i] = make_tmap_3d(a.k_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, D, rows, 1, D, rows * D, C::kBW, box_rows, 1,
+                             &ok, C::kSwz);
+    maps.v[i] = make_tmap_3d(a.v_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, D, rows, 1, D, rows * D, C::kBW, box_rows, 1,
+                             &ok, C::kSwz);
+  }
   if (!ok) return cudaErrorInvalidValue;
   const int64_t slots = static_cast<int64_t>(a.num_splits) * a.B * a.Hkv;
   const int grid = static_cast<int>(slots < num_sms() ? slots : num_sms());
   static std::atomic<uint32_t> next_ticket{0};
   const uint32_t ticket = next_ticket.fetch_add(1, std::memory_order_relaxed) % kTickets;
-  kern<<<grid, C::kThreads, C::kBytes, s>>>(a, mk, mv, ticket, device_status_ptr(), spin_limit_ns());
+  kern<<<grid, C::kThreads, C::kBytes, s>>>(a, maps, ticket, device_status_ptr(), spin_limit_ns());
   return cudaGetLastError();
 }
 
