@@ -11,7 +11,7 @@ it with gcc, lays out the per-(sequence, head) slices and loops over them.
 Sources: the "SuperL8" README (github.com/jajmangold/superl8) -- "Attention
 kernels" table (attn_int8_fwd: W8A8 FlashAttention-2, causal, GQA/MQA, head dims
 32/64/128/256; attn_varlen_fwd: ragged prefill; attn_decode: split-KV decode over
-an int8 KV cache, int8-V variant; attn_paged_decode over a paged cache, with the
+an int8 KV cache, int8-V and fp16-V variants; attn_paged_decode over a paged cache, with the
 "Engine" table's k8v8 format), "Supporting kernels" table (quant_rowwise:
 symmetric per-row int8), "Quantization" table (per-row int8 with K-smoothing) and
 the "Quick start" section (q [B,Hq,N,d], k/v [B,Hkv,N,d], quantises internally).
@@ -74,6 +74,10 @@ def _load():
             lib.oracle_decode_row.argtypes = [
                 _I8P, ctypes.c_float, _I8P, _F32P, _I8P, _F32P, ctypes.c_int64, ctypes.c_int64,
                 ctypes.c_int64, ctypes.c_int, _F64P, _F64P, ctypes.c_void_p]
+            lib.oracle_decode_row_fv.restype = ctypes.c_int
+            lib.oracle_decode_row_fv.argtypes = [
+                _I8P, ctypes.c_float, _I8P, _F32P, _F32P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                ctypes.c_int, _F64P, _F64P, ctypes.c_void_p]
             lib.oracle_decode_combine.argtypes = [_F64P, _F64P, ctypes.c_int, ctypes.c_int, _F64P, _F64P]
             _lib = lib
     return _lib
@@ -300,9 +304,33 @@ def attn_paged_decode(q, k_pages, k_scale_pages, v_pages, v_scale_pages, block_t
     return _decode(q, rows_of, k_pages.shape[1], lmax, seqlens, num_splits, split_size, rows, want_logits)
 
 
+def attn_decode_f16v(q, k_codes, k_scales, v, seqlens, num_splits=1, split_size=None, rows=None,
+                     want_logits=False):
+    """Split-KV decode with an int8 K cache and an fp16 V cache, fp64 after the int32 dot.
+
+    Source: the "SuperL8" README, "Attention kernels" table, attn_decode row (split-KV
+    decode with an int8 KV cache; its "fp16 V" variant).  Reading: K is the int8 cache
+    of attn_decode (codes [B,Hkv,Lmax,d] with per-token scales [B,Hkv,Lmax]); V is
+    [B,Hkv,Lmax,d] fp16 with no scale, O = sum_t p_t v[t] (R12 and R13 otherwise).
+    """
+    k_codes = np.ascontiguousarray(k_codes, np.int8)
+    k_scales = _f32(k_scales)
+    v = np.asarray(v)
+    if v.dtype != np.float16:
+        raise ValueError("v must be float16")
+    v = np.ascontiguousarray(v.astype(np.float32))   # exact widening
+
+    def rows_of(b, hkv, L):
+        return k_codes[b, hkv], k_scales[b, hkv], v[b, hkv], None
+
+    return _decode(q, rows_of, k_codes.shape[1], k_codes.shape[2], seqlens, num_splits, split_size, rows,
+                   want_logits)
+
+
 def _decode(q, rows_of, hkv_n, lmax, seqlens, num_splits, split_size, rows, want_logits):
     """The split loop shared by the decode oracles; rows_of(b, hkv, L) gives the kv head's
-    cache rows (k codes, k scales, v codes, v scales) for tokens 0 .. L-1 (at least)."""
+    cache rows (k codes, k scales, v codes, v scales) for tokens 0 .. L-1 (at least); v
+    scales None means V rows of fp16 values widened to fp32, without scales."""
     q = _f32(q)
     seqlens = np.asarray(seqlens, np.int64)
     B, hq_n, d = q.shape
@@ -326,11 +354,18 @@ def _decode(q, rows_of, hkv_n, lmax, seqlens, num_splits, split_size, rows, want
             cached.clear()
             cached[(b, hkv)] = rows_of(b, hkv, L)
         kc, ksc, vc, vsc = cached[(b, hkv)]
+
+        def row(t0, t1, o, lv, lg):
+            if vsc is None:
+                lib.oracle_decode_row_fv(q_codes[b, hq], float(q_scales[b, hq]), kc, ksc, vc, L, t0, t1, d, o, lv, lg)
+            else:
+                lib.oracle_decode_row(q_codes[b, hq], float(q_scales[b, hq]), kc, ksc, vc, vsc, L, t0, t1, d, o, lv,
+                                      lg)
+
         for s in range(nsplit):
             o = np.zeros(d, np.float64)
             lv = np.zeros(1, np.float64)
-            lib.oracle_decode_row(q_codes[b, hq], float(q_scales[b, hq]), kc, ksc, vc, vsc, L,
-                                  s * split_size, (s + 1) * split_size, d, o, lv, None)
+            row(s * split_size, (s + 1) * split_size, o, lv, None)
             o_part[b, hq, s], l_part[b, hq, s] = o, lv[0]
         o = np.zeros(d, np.float64)
         lv = np.zeros(1, np.float64)
@@ -341,8 +376,7 @@ def _decode(q, rows_of, hkv_n, lmax, seqlens, num_splits, split_size, rows, want
             lg = np.zeros(max(L, 1), np.int32)
             o2 = np.zeros(d, np.float64)
             l2 = np.zeros(1, np.float64)
-            lib.oracle_decode_row(q_codes[b, hq], float(q_scales[b, hq]), kc, ksc, vc, vsc, L, 0, L, d,
-                                  o2, l2, lg.ctypes.data)
+            row(0, L, o2, l2, lg.ctypes.data)
             logits[(b, hq)] = lg[:L].copy()
     return dict(out=out, lse=lse, q_codes=q_codes, q_scales=q_scales, o_partial=o_part,
                 lse_partial=l_part, logits=logits)

@@ -193,6 +193,21 @@ int oracle_decode_row(const int8_t* qc, float qs, const int8_t* kc, const float*
   return overflow;
 }
 
+/*
+ * Decode for one (b, hq) over a cache whose V is kept in fp16: the attn_decode "fp16 V"
+ * variant.  As oracle_decode_row, but the V rows v [L][d] are the fp16 values widened to
+ * fp32 (exact) and carry no per-token scale: O = sum_t p_t * v[t].
+ */
+int oracle_decode_row_fv(const int8_t* qc, float qs, const int8_t* kc, const float* ks, const float* v,
+                         int64_t L, int64_t t0, int64_t t1, int d, double* o, double* lse, int32_t* logits) {
+  if (t1 > L) t1 = L;
+  if (t0 < 0) t0 = 0;
+  int64_t n = t1 > t0 ? t1 - t0 : 0;
+  int overflow = 0;
+  attn_row(qc, qs, kc + t0 * (int64_t)d, ks + t0, v + t0 * (int64_t)d, NULL, n, d, o, lse, logits, &overflow);
+  return overflow;
+}
+
 /* Merge nsplit partials (o [nsplit][d] normalised, lse [nsplit]) into one row, R13. */
 void oracle_decode_combine(const double* o, const double* lse, int nsplit, int d, double* out,
                            double* lse_out) {

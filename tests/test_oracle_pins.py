@@ -456,3 +456,42 @@ def test_paged_decode_shared_prefix_pages():
     # the shared prefix really is shared: the 32 common tokens are identical rows
     np.testing.assert_array_equal(kc[0, :, :32], kc[1, :, :32])
     np.testing.assert_array_equal(kc[0, :, :32], kc[2, :, :32])
+
+
+# ---------------------------------------------------------------- decode with an fp16 V cache
+
+def test_decode_f16v_equals_textbook():
+    """fp16-V decode on quantisation-exact K and q rows: no quantisation error is left, so
+    it is fp64 softmax attention over the fp16 V values."""
+    rng = np.random.default_rng(50)
+    B, hq, hkv, lmax, d = 3, 4, 2, 300, 64
+    kf, kc, ks = exact_rows(rng, (B, hkv, lmax, d))
+    q, _, _ = exact_rows(rng, (B, hq, d))
+    v16 = rng.standard_normal((B, hkv, lmax, d)).astype(np.float16)
+    lens = np.array([1, 150, 300])
+    r = oracle.attn_decode_f16v(q, kc, ks, v16, lens, num_splits=3)
+    for b, L in enumerate(lens):
+        qq = q[b][:, None, :][None]
+        ref = textbook(qq, kf[b][None, :, :L], v16[b][None, :, :L].astype(np.float64), causal=False)[0, :, 0]
+        np.testing.assert_allclose(r["out"][b], ref, rtol=0, atol=1e-10)
+
+
+def test_decode_f16v_equals_int8v_on_exact_v():
+    """When every fp16 V value is s_v * code exactly (s_v = 2^-7), the fp16-V decode and the
+    int8-V decode are the same sum (up to the order of one fp64 product)."""
+    rng = np.random.default_rng(51)
+    B, hq, hkv, lmax, d = 2, 8, 2, 200, 128
+    q = rng.standard_normal((B, hq, d)).astype(np.float32)
+    kc = rng.integers(-127, 128, size=(B, hkv, lmax, d)).astype(np.int8)
+    ks = rng.uniform(0.001, 0.05, size=(B, hkv, lmax)).astype(np.float32)
+    vc = rng.integers(-127, 128, size=(B, hkv, lmax, d)).astype(np.int8)
+    vs = np.full((B, hkv, lmax), 2.0 ** -7, np.float32)
+    v16 = (vc.astype(np.float32) * np.float32(2.0 ** -7)).astype(np.float16)
+    assert np.array_equal(v16.astype(np.float32), vc.astype(np.float32) / 128)
+    lens = np.array([200, 37])
+    a = oracle.attn_decode_f16v(q, kc, ks, v16, lens, num_splits=2, want_logits=True)
+    b = oracle.attn_decode(q, kc, ks, vc, vs, lens, num_splits=2, want_logits=True)
+    np.testing.assert_allclose(a["out"], b["out"], rtol=1e-13, atol=1e-15)
+    np.testing.assert_array_equal(a["lse"], b["lse"])
+    for key in b["logits"]:
+        np.testing.assert_array_equal(a["logits"][key], b["logits"][key])
