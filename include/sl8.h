@@ -177,6 +177,20 @@ SL8_API int sl8_attn_int8_decode_splitkv(const void* q, int q_dtype, const int8_
                                  float* o_partial, float* lse_partial, void* stream);
 
 /*
+ * Split-KV decode with an int8 K cache and an fp16 V cache: the attn_decode row's
+ * "fp16 V" variant ("Attention kernels" table).  Same operation, split plan and outputs
+ * as sl8_attn_int8_decode_splitkv, with O = sum_t p_t * v[t] (V has no scale):
+ *   k_cache, k_scale  as there ([B][Hkv][Lmax][d] int8 codes, [B][Hkv][Lmax] fp32).
+ *   v_cache           device, [B][Hkv][Lmax][d] fp16 (16-byte aligned).
+ * d must be 64 or 128 (SL8_ERR_UNSUPPORTED for 256).  The partials are merged with
+ * sl8_attn_decode_combine.
+ */
+SL8_API int sl8_attn_int8_decode_splitkv_f16v(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale,
+                                              const void* v_cache, const int32_t* seqlens, int32_t B, int32_t Hq,
+                                              int32_t Hkv, int32_t Lmax, int32_t d, int32_t num_splits,
+                                              float* o_partial, float* lse_partial, void* stream);
+
+/*
  * Split-KV decode over a paged int8 KV cache: the "Engine" table's "Paged KV cache" row
  * (int8 / k8v3 / k8v8 cache formats) with the k8v8 format, and the "Attention kernels"
  * table's attn_paged_decode row.  Same operation, split plan and outputs as

@@ -219,3 +219,53 @@ def test_paged_decode_bad_page_is_reported():
     torch.cuda.synchronize()
     assert torch.isfinite(out.float()).all()
     assert sl8.last_device_status()[0] == sl8.SL8_OK
+
+
+# ---------------------------------------------------------------- fp16 V cache
+
+F16V = [
+    # wid, B, Hq, Hkv, d, lengths, lmax
+    (3401, 6, 8, 2, 128, [1, 255, 256, 257, 700, 0], 700),
+    (3402, 3, 4, 4, 64, [513, 1, 1024], 1024),
+    (3403, 2, 16, 2, 128, [2000, 77], 2000),
+    (3404, 3, 8, 8, 64, [160, 161, 3000], 3000),
+]
+
+
+@pytest.mark.parametrize("case", F16V, ids=[f"w{c[0]}_d{c[4]}_G{c[2] // c[3]}" for c in F16V])
+def test_decode_f16v(case):
+    """int8 K + fp16 V decode against the oracle's fp16-V decode."""
+    wid, B, Hq, Hkv, d, lens, lmax = case
+    w = W.custom(wid, kind="decode", B=B, Hq=Hq, Hkv=Hkv, d=d, dtype="bf16", extra={"lengths": lens})
+    lens_np, g, gs, o, os_ = build_cache(w, lmax)
+    v16 = torch.zeros((B, Hkv, lmax, d), dtype=torch.float16)
+    for b in range(B):
+        v16[b, :, :int(lens_np[b])] = torch.from_numpy(W.decode_cache_values(w, b, "v")).to(torch.float16)
+    vd = v16.to(DEV)
+    q = W.decode_query(w)
+    qd = q.to(DEV)
+    seq = torch.from_numpy(lens_np.astype(np.int32)).to(DEV)
+    for ns in (0, 1, 3):
+        ref = oracle.attn_decode_f16v(q.float().numpy(), o["k"], os_["k"], v16.numpy(), lens_np,
+                                      split_size=sl8.lib().sl8_attn_decode_split_size(B, Hkv, lmax, d, ns))
+        o32, lse = sl8.attn_int8_decode_f16v(qd, g["k"], gs["k"], vd, seq, num_splits=ns, out_dtype=torch.float32,
+                                             return_lse=True)
+        ob = sl8.attn_int8_decode_f16v(qd, g["k"], gs["k"], vd, seq, num_splits=ns)
+        torch.cuda.synchronize()
+        check_f32(to_np32(o32), ref["out"], f"w{wid} f16v splits={ns} f32")
+        check_half(ob, ref["out"], f"w{wid} f16v splits={ns} bf16")
+        ok = lens_np > 0
+        np.testing.assert_allclose(to_np32(lse)[ok], ref["lse"][ok], rtol=0, atol=1e-4)
+        assert np.all(np.isneginf(to_np32(lse)[~ok]))
+    st, site = sl8.last_device_status()
+    assert st == sl8.SL8_OK, (st, site)
+
+
+def test_decode_f16v_rejects_d256():
+    q = torch.zeros((1, 2, 256), dtype=torch.bfloat16, device=DEV)
+    kc = torch.zeros((1, 1, 64, 256), dtype=torch.int8, device=DEV)
+    ks = torch.ones((1, 1, 64), dtype=torch.float32, device=DEV)
+    v = torch.zeros((1, 1, 64, 256), dtype=torch.float16, device=DEV)
+    seq = torch.tensor([10], dtype=torch.int32, device=DEV)
+    with pytest.raises(sl8.SL8Error):
+        sl8.attn_int8_decode_splitkv_f16v(q, kc, ks, v, seq)

@@ -73,6 +73,8 @@ _SIGNATURES = {
     "sl8_attn_decode_split_size": (_I32, [_I32, _I32, _I32, _I32, _I32]),
     "sl8_attn_int8_decode_splitkv": (_INT, [_P, _INT, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P,
                                             _P, _P]),
+    "sl8_attn_int8_decode_splitkv_f16v": (_INT, [_P, _INT, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P,
+                                                 _P, _P]),
     "sl8_attn_int8_paged_decode_splitkv": (_INT, [_P, _INT, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _I32, _I32,
                                                   _I32, _I32, _I32, _P, _P, _P]),
     "sl8_attn_decode_combine": (_INT, [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _INT, _P, _P]),
@@ -299,6 +301,34 @@ def attn_int8_decode(q, k_cache, k_scale, v_cache, v_scale, seqlens, num_splits=
     """Split-KV decode plus combine: out [B, Hq, d] (dtype q.dtype unless given)."""
     o_p, l_p = attn_int8_decode_splitkv(q, k_cache, k_scale, v_cache, v_scale, seqlens, num_splits, o_partial,
                                         lse_partial)
+    return attn_decode_combine(o_p, l_p, seqlens, k_cache.shape[2], out_dtype or q.dtype, return_lse, out)
+
+
+def attn_int8_decode_splitkv_f16v(q, k_cache, k_scale, v_cache, seqlens, num_splits=0, o_partial=None,
+                                  lse_partial=None):
+    """Split-KV partials with an int8 K cache and an fp16 V cache [B, Hkv, Lmax, d]."""
+    _need_cuda(q, k_cache, k_scale, v_cache, seqlens)
+    if v_cache.dtype != torch.float16:
+        raise ValueError("v_cache must be float16")
+    B, Hq, d = q.shape
+    _, Hkv, Lmax, _ = k_cache.shape
+    S = decode_num_splits(B, Hkv, Lmax, d, num_splits)
+    if o_partial is None:
+        o_partial = torch.empty((B, Hq, max(S, 1), d), dtype=torch.float32, device=q.device)
+    if lse_partial is None:
+        lse_partial = torch.empty((B, Hq, max(S, 1)), dtype=torch.float32, device=q.device)
+    _check(lib().sl8_attn_int8_decode_splitkv_f16v(_ptr(q), _dt(q), _ptr(k_cache), _ptr(k_scale), _ptr(v_cache),
+                                                   _ptr(seqlens), B, Hq, Hkv, Lmax, d, num_splits, _ptr(o_partial),
+                                                   _ptr(lse_partial), _stream(q.device)),
+           "sl8_attn_int8_decode_splitkv_f16v")
+    return o_partial, lse_partial
+
+
+def attn_int8_decode_f16v(q, k_cache, k_scale, v_cache, seqlens, num_splits=0, out_dtype=None, return_lse=False,
+                          o_partial=None, lse_partial=None, out=None):
+    """Split-KV decode (int8 K, fp16 V) plus combine: out [B, Hq, d] (dtype q.dtype unless given)."""
+    o_p, l_p = attn_int8_decode_splitkv_f16v(q, k_cache, k_scale, v_cache, seqlens, num_splits, o_partial,
+                                             lse_partial)
     return attn_decode_combine(o_p, l_p, seqlens, k_cache.shape[2], out_dtype or q.dtype, return_lse, out)
 
 

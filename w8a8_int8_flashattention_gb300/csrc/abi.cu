@@ -489,10 +489,11 @@ struct Paging {
   int32_t page_size, max_blocks, num_pages;
 };
 
-static int decode_validate(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale,
-                           const int8_t* v_cache, const float* v_scale, const int32_t* seqlens, int32_t B, int32_t Hq,
-                           int32_t Hkv, int32_t Lmax, int32_t d, const Paging* pg) {
-  SL8_CHECK(q && k_cache && k_scale && v_cache && v_scale && seqlens, SL8_ERR_INVALID_ARG);
+static int decode_validate(const void* q, int q_dtype, const void* k_cache, const float* k_scale, const void* v_cache,
+                           const float* v_scale, const int32_t* seqlens, int32_t B, int32_t Hq, int32_t Hkv,
+                           int32_t Lmax, int32_t d, const Paging* pg, bool v16) {
+  SL8_CHECK(q && k_cache && k_scale && v_cache && (v_scale || v16) && seqlens, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(!v16 || (d <= 128 && !pg), SL8_ERR_UNSUPPORTED);
   SL8_CHECK(aligned16(q) && aligned16(k_cache) && aligned16(v_cache), SL8_ERR_INVALID_ARG);
   SL8_CHECK(q_dtype == SL8_F16 || q_dtype == SL8_BF16 || q_dtype == SL8_F32, SL8_ERR_INVALID_ARG);
   SL8_CHECK(B >= 0 && Hq > 0 && Hkv > 0 && Lmax >= 0 && d > 0, SL8_ERR_INVALID_ARG);
@@ -513,11 +514,12 @@ static int decode_validate(const void* q, int q_dtype, const int8_t* k_cache, co
   return SL8_OK;
 }
 
-static int decode_launch(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale, const int8_t* v_cache,
+static int decode_launch(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale, const void* v_cache,
                          const float* v_scale, const int32_t* seqlens, int32_t B, int32_t Hq, int32_t Hkv, int32_t Lmax,
                          int32_t d, int32_t num_splits, float* o_partial, float* lse_partial, int32_t* logits,
-                         int8_t* q_codes, float* q_scales, void* stream, const Paging* pg = nullptr) {
-  int rc = decode_validate(q, q_dtype, k_cache, k_scale, v_cache, v_scale, seqlens, B, Hq, Hkv, Lmax, d, pg);
+                         int8_t* q_codes, float* q_scales, void* stream, const Paging* pg = nullptr,
+                         bool v16 = false) {
+  int rc = decode_validate(q, q_dtype, k_cache, k_scale, v_cache, v_scale, seqlens, B, Hq, Hkv, Lmax, d, pg, v16);
   if (rc != SL8_OK) return rc;
   SL8_CHECK(o_partial && lse_partial && num_splits >= 0, SL8_ERR_INVALID_ARG);
   if (B == 0 || Lmax == 0) return SL8_OK;
@@ -526,8 +528,9 @@ static int decode_launch(const void* q, int q_dtype, const int8_t* k_cache, cons
   a.q_dtype = static_cast<sl8_dtype>(q_dtype);
   a.k_cache = k_cache;
   a.k_scale = k_scale;
-  a.v_cache = v_cache;
-  a.v_scale = v_scale;
+  a.v_cache = static_cast<const int8_t*>(v_cache);
+  a.v_scale = v16 ? nullptr : v_scale;
+  a.v16 = v16;
   a.seqlens = seqlens;
   a.B = B;
   a.Hq = Hq;
@@ -550,6 +553,14 @@ static int decode_launch(const void* q, int q_dtype, const int8_t* k_cache, cons
   }
   SL8_LAUNCH(launch_decode_split(a, static_cast<cudaStream_t>(stream)));
   return SL8_OK;
+}
+
+int sl8_attn_int8_decode_splitkv_f16v(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale,
+                                      const void* v_cache, const int32_t* seqlens, int32_t B, int32_t Hq,
+                                      int32_t Hkv, int32_t Lmax, int32_t d, int32_t num_splits, float* o_partial,
+                                      float* lse_partial, void* stream) {
+  return decode_launch(q, q_dtype, k_cache, k_scale, v_cache, nullptr, seqlens, B, Hq, Hkv, Lmax, d, num_splits,
+                       o_partial, lse_partial, nullptr, nullptr, nullptr, stream, nullptr, true);
 }
 
 int sl8_attn_int8_paged_decode_splitkv(const void* q, int q_dtype, const int8_t* k_pages, const float* k_scale_pages,

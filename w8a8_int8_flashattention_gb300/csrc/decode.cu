@@ -75,7 +75,7 @@ constexpr int kTickets = 64;
 __device__ uint32_t g_claim[kTickets][2];
 static_assert(kSchedMaxB <= 65536, "b fits the key");
 
-template <int D>
+template <int D, bool kV16 = false>
 struct DCfg {
   // ten compute warps (eight for d = 256, whose tiles and merge buffer are twice as
   // large); registers are granted to the CTA in steps of four warps, so the loader and
@@ -87,11 +87,14 @@ struct DCfg {
   static constexpr int kBW = D < 128 ? D : 128;  // bytes in one row of a TMA box
   static constexpr int kBoxes = D / kBW;
   static constexpr bool kSwz = D >= 128;         // 128-byte swizzled tiles
-  static constexpr int kTile = kChunk * D;       // one stage of K (or V) codes
-  static constexpr int kStages = D == 64 ? 8 : (D == 128 ? 3 : 2);
+  static constexpr int kTile = kChunk * D;       // one stage of K codes
+  // V: int8 codes like K, or (kV16) fp16 values in 128-byte rows of 64 dims
+  static constexpr int kTileV = kV16 ? 2 * kTile : kTile;
+  static constexpr int kBoxesV = kV16 ? D / 64 : kBoxes;
+  static constexpr int kStages = kV16 ? (D == 64 ? 4 : 2) : (D == 64 ? 8 : (D == 128 ? 3 : 2));
   static constexpr int kSK = 0;
   static constexpr int kSV = kTile;
-  static constexpr int kSKs = 2 * kTile;
+  static constexpr int kSKs = kTile + kTileV;
   static constexpr int kSVs = kSKs + kChunk * 4;
   static constexpr int kStageBytes = (kSVs + kChunk * 4 + 1023) / 1024 * 1024;
   static constexpr int kQBytes = 8 * D * 4;                    // 8 raw q rows, fp32 at most
@@ -106,6 +109,7 @@ struct DCfg {
   static constexpr int kNumBars = 2 * kStages + 4 * kQSlots + 3;
   static constexpr int kBytes = kBar + kNumBars * 8 + 1024;    // + alignment slack
   static_assert(kStageBytes % 1024 == 0 && kTile % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+  static_assert(!kV16 || D <= 128, "fp16 V: d <= 128");
   static_assert(kBytes <= 232448, "smem budget");
 };
 
@@ -173,6 +177,14 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// Four transposed 8x8 fp16 matrices from shared memory: lanes 8i .. 8i+7 give the row
+// addresses of matrix i; register i of thread T holds its rows 2 (T % 4) and 2 (T % 4) + 1
+// in column T / 4.
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
 }
 __device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
@@ -334,11 +346,11 @@ struct CacheMaps {
   CUtensorMap k[kPageBoxes], v[kPageBoxes];
 };
 
-template <int D>
-__global__ void __launch_bounds__(DCfg<D>::kThreads, 1)
+template <int D, bool kV16>
+__global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
     decode_split_kernel(const DecodeArgs a, const __grid_constant__ CacheMaps maps, uint32_t ticket,
                         DeviceStatus* st, uint64_t limit_ns) {
-  using C = DCfg<D>;
+  using C = DCfg<D, kV16>;
   constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -471,10 +483,10 @@ __global__ void __launch_bounds__(DCfg<D>::kThreads, 1)
         const int t = c0 + lane * kUnit;
         const int units = (nt + kUnit - 1) / kUnit;
         int pg = 0;
-        if (a.block_table && lane < units) pg = a.block_table[static_cast<int64_t>(cur.b) * a.max_blocks + t / a.page_size];
+        if (!kV16 && a.block_table && lane < units) pg = a.block_table[static_cast<int64_t>(cur.b) * a.max_blocks + t / a.page_size];
         if (k >= kStages) ok = warp_wait(&empty[stg], ((k / kStages) - 1) & 1, limit_ns, st, 41);
         if (!ok) break;
-        if (a.block_table) {
+        if (!kV16 && a.block_table) {
           // paged cache: the stage's 16-token units (page_size is a multiple of 16; units
           // past the split's end are not loaded, their compute warps skip them) fall into
           // pieces that each lie in one page; the lane of a piece's first unit loads the
@@ -508,22 +520,24 @@ __global__ void __launch_bounds__(DCfg<D>::kThreads, 1)
         if (!scales_bulk) {
           for (int j = lane; j < nt; j += 32) {
             reinterpret_cast<float*>(base + C::kSKs)[j] = a.k_scale[row0 + c0 + j];
-            reinterpret_cast<float*>(base + C::kSVs)[j] = a.v_scale[row0 + c0 + j];
+            if (!kV16) reinterpret_cast<float*>(base + C::kSVs)[j] = a.v_scale[row0 + c0 + j];
           }
           __syncwarp();
         }
         if (lane == 0) {
           const uint32_t sc_bytes = scales_bulk ? static_cast<uint32_t>((nt + 3) / 4 * 16) : 0u;
-          mbar_arrive_expect_tx(&full[stg], 2 * C::kTile + 2 * sc_bytes);
+          mbar_arrive_expect_tx(&full[stg], C::kTile + C::kTileV + (kV16 ? 1 : 2) * sc_bytes);
           const int y = static_cast<int>(row0 + c0);
 #pragma unroll
-          for (int b = 0; b < C::kBoxes; ++b) {
+          for (int b = 0; b < C::kBoxes; ++b)
             tma_load_3d(base + C::kSK + b * C::kChunk * C::kBW, &maps.k[0], &full[stg], b * C::kBW, y, 0);
-            tma_load_3d(base + C::kSV + b * C::kChunk * C::kBW, &maps.v[0], &full[stg], b * C::kBW, y, 0);
-          }
+#pragma unroll
+          for (int b = 0; b < C::kBoxesV; ++b)  // V16: boxes of 64 fp16 dims
+            tma_load_3d(base + C::kSV + b * C::kChunk * (kV16 ? 128 : C::kBW), &maps.v[0], &full[stg],
+                        b * (kV16 ? 64 : C::kBW), y, 0);
           if (scales_bulk) {
             bulk_load(base + C::kSKs, a.k_scale + row0 + c0, sc_bytes, &full[stg]);
-            bulk_load(base + C::kSVs, a.v_scale + row0 + c0, sc_bytes, &full[stg]);
+            if (!kV16) bulk_load(base + C::kSVs, a.v_scale + row0 + c0, sc_bytes, &full[stg]);
           }
         }
       }
@@ -643,6 +657,20 @@ __global__ void __launch_bounds__(DCfg<D>::kThreads, 1)
       const int row = u0 + t + (c == 1 ? 8 : c == 2 ? 4 : c == 3 ? 12 : 0);
       offv[b][c] = D == 64 ? static_cast<uint32_t>(row * 64 + 8 * cg) : tile_off<D>(row, 8 * b + cg);
     }
+  // fp16 V: this lane's ldmatrix row address for m-tile j (dims 16 j ..): it serves matrix
+  // i = lane / 8 (dims + 8 (i % 2); k columns 8 (i / 2) ..) and its row r = lane % 8, the
+  // token at k column 8 (i / 2) + r in the order of the P' pairs (k 2p -> token p,
+  // k 2p + 1 -> token p + 8 within each half of k)
+  uint32_t offv16[kV16 ? D / 16 : 1];
+  if constexpr (kV16) {
+    const int i = lane >> 3, r = lane & 7;
+    const int row = u0 + 4 * (i >> 1) + (r >> 1) + 8 * (r & 1);
+#pragma unroll
+    for (int j = 0; j < D / 16; ++j) {
+      const int chunk = 2 * j + (i & 1);
+      offv16[j] = static_cast<uint32_t>((chunk >> 3) * (C::kChunk * 128) + row * 128 + 16 * ((chunk & 7) ^ (row & 7)));
+    }
+  }
   const float log2e_over_sqrtd = 1.4426950408889634f / sqrtf(static_cast<float>(D));
   uint32_t* pw = reinterpret_cast<uint32_t*>(smem + C::kP + cw * 256);  // [8 q][8 pairs] fp16x2
 
@@ -824,7 +852,7 @@ __global__ void __launch_bounds__(DCfg<D>::kThreads, 1)
         }
         // ---- online softmax (log2 units), lazily rescaled
         const float ksA = vA ? sks[rA] : 0.0f, ksB = vB ? sks[rB] : 0.0f;
-        const float vsA = vA ? svs[rA] : 0.0f, vsB = vB ? svs[rB] : 0.0f;
+        const float vsA = vA ? (kV16 ? 1.0f : svs[rA]) : 0.0f, vsB = vB ? (kV16 ? 1.0f : svs[rB]) : 0.0f;
         const float ka = ksA * qsa, kb = ksA * qsb, kc = ksB * qsa, kd = ksB * qsb;
         const float xa0 = vA ? d00 * ka : -INFINITY, xa1 = vA ? d01 * kb : -INFINITY;
         const float xb0 = vB ? d10 * kc : -INFINITY, xb1 = vB ? d11 * kd : -INFINITY;
@@ -878,8 +906,17 @@ __global__ void __launch_bounds__(DCfg<D>::kThreads, 1)
         __syncwarp();
         const uint32_t pb0r = pw[g * 8 + t], pb1r = pw[g * 8 + 4 + t];
         // ---- O'^T += V_biased^T . P'^T (V codes + 128 as fp16 subnormals), and the row
-        // sums of P' from an all-ones A for the offset
-        if constexpr (D == 64) {
+        // sums of P' from an all-ones A for the offset; fp16 V: O'^T += V^T . P'^T with the
+        // A fragments read transposed from the [token][dim] tile
+        if constexpr (kV16) {
+          const uint32_t svb = smem_u32(sv);
+#pragma unroll
+          for (int j = 0; j < D / 16; ++j) {
+            uint32_t v0, v1, v2, v3;
+            ldsm_x4_t(svb + offv16[j], v0, v1, v2, v3);
+            mma_f16(o[j], v0, v1, v2, v3, pb0r, pb1r);
+          }
+        } else if constexpr (D == 64) {
           uint2 w[4];
 #pragma unroll
           for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint2*>(sv + offv[0][c]);
@@ -915,7 +952,7 @@ __global__ void __launch_bounds__(DCfg<D>::kThreads, 1)
             }
           }
         }
-        mma_f16(osum, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, pb0r, pb1r);
+        if constexpr (!kV16) mma_f16(osum, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, pb0r, pb1r);
       };
       if (nv >= kUnit) {
         unit(std::true_type{});
@@ -944,8 +981,17 @@ __global__ void __launch_bounds__(DCfg<D>::kThreads, 1)
     const float pe = pow2i(E);
     constexpr float k2p24 = 16777216.0f;
     const float ca = -128.0f * osum[0], cb = -128.0f * osum[1];
+    if constexpr (kV16) {
+      // fp16 V: O = O' 2^E; rows g and g + 8 of m-tile j are dims 16 j + g and 16 j + g + 8
 #pragma unroll
-    for (int j = 0; j < D / 16; ++j) {
+      for (int j = 0; j < D / 16; ++j) {
+        *reinterpret_cast<float2*>(red + (cw * D + 16 * j + g) * 8 + 2 * t) = make_float2(o[j][0] * pe, o[j][1] * pe);
+        *reinterpret_cast<float2*>(red + (cw * D + 16 * j + g + 8) * 8 + 2 * t) =
+            make_float2(o[j][2] * pe, o[j][3] * pe);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < (kV16 ? 0 : D / 16); ++j) {
       // physical dims of rows g and g + 8 of m-tile j
       int dim;
       if constexpr (D == 64) {
@@ -1044,10 +1090,10 @@ __global__ void timeout_selftest_kernel(uint64_t limit_ns, DeviceStatus* st) {
   if (threadIdx.x == 0) mbar_wait(&bar, 0, limit_ns, st, 999);
 }
 
-template <int D>
+template <int D, bool kV16>
 cudaError_t launch_split_d(const DecodeArgs& a, cudaStream_t s) {
-  using C = DCfg<D>;
-  auto kern = decode_split_kernel<D>;
+  using C = DCfg<D, kV16>;
+  auto kern = decode_split_kernel<D, kV16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
   if (e != cudaSuccess) return e;
   // each cache as a 2-D [B * Hkv * Lmax rows][d bytes] tensor, loaded in boxes of
@@ -1065,8 +1111,12 @@ cudaError_t launch_split_d(const DecodeArgs& a, cudaStream_t s) {
                                     : C::kChunk;
     maps.k[i] = make_tmap_3d(a.k_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, D, rows, 1, D, rows * D, C::kBW, box_rows, 1,
                              &ok, C::kSwz);
-    maps.v[i] = make_tmap_3d(a.v_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, D, rows, 1, D, rows * D, C::kBW, box_rows, 1,
-                             &ok, C::kSwz);
+    if (kV16)  // [rows][d] fp16, boxes of 64 dims (128 bytes, swizzled)
+      maps.v[i] = make_tmap_3d(a.v_cache, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, D, rows, 1, 2 * D, rows * D * 2, 64,
+                               box_rows, 1, &ok, true);
+    else
+      maps.v[i] = make_tmap_3d(a.v_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, D, rows, 1, D, rows * D, C::kBW, box_rows,
+                               1, &ok, C::kSwz);
   }
   if (!ok) return cudaErrorInvalidValue;
   const int64_t slots = static_cast<int64_t>(a.num_splits) * a.B * a.Hkv;
@@ -1083,10 +1133,17 @@ int decode_chunk_tokens(int d) { return d == 256 ? DCfg<256>::kChunk : d == 128 
 
 cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t s) {
   TraceScope tr("decode_split", s);
+  if (a.v16) {
+    switch (a.d) {
+      case 64: return launch_split_d<64, true>(a, s);
+      case 128: return launch_split_d<128, true>(a, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (a.d) {
-    case 64: return launch_split_d<64>(a, s);
-    case 128: return launch_split_d<128>(a, s);
-    case 256: return launch_split_d<256>(a, s);
+    case 64: return launch_split_d<64, false>(a, s);
+    case 128: return launch_split_d<128, false>(a, s);
+    case 256: return launch_split_d<256, false>(a, s);
     default: return cudaErrorInvalidValue;
   }
 }

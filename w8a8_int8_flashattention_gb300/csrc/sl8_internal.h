@@ -160,6 +160,9 @@ struct DecodeArgs {
   // max_blocks * page_size
   const int32_t* block_table;
   int32_t page_size, max_blocks, num_pages;
+  // fp16 V cache (v_cache holds [B][Hkv][Lmax][d] fp16 values, v_scale unused); d <= 128,
+  // contiguous caches only
+  bool v16;
 };
 cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_combine(const float* o_partial, const float* lse_partial, const int32_t* seqlens,
