@@ -9,7 +9,8 @@ One step = one pass of the whole path over one batch of synthetic input:
 `value` is prefill TOPS (ops = 2 x 2 x d x causal pairs x heads, QK^T and P.V);
 the decode KV GB/s sits in `decode`, and `paged_decode` repeats the decode over a
 paged k8v8 cache (64-token pages in a seeded random order) in a loop of its own after
-the timed steps.  Inputs are resident in HBM when the timed
+the timed steps, and `decode_f16v` the decode with an fp16 V cache (int8 K).  Inputs
+are resident in HBM when the timed
 region starts; L2 is flushed before every step, outside the timed events (a 256 MB
 write, then a read of that buffer, so no dirty lines of the flush remain).  `e2e` repeats the prefill through the public API with pinned host
 inputs copied in and the output copied back every step.
@@ -48,6 +49,12 @@ def prefill_ops(w) -> float:
 
 def decode_bytes(w, lens) -> float:
     kv = float(np.sum(lens)) * w.Hkv * (2 * w.d + 2 * 4)
+    return kv + w.B * w.Hq * w.d * 2 * 2
+
+
+def decode_bytes_f16v(w, lens) -> float:
+    """Algorithmic bytes of the fp16-V decode: int8 K codes + K scales + fp16 V, q and out."""
+    kv = float(np.sum(lens)) * w.Hkv * (w.d + 4 + 2 * w.d)
     return kv + w.B * w.Hq * w.d * 2 * 2
 
 
@@ -308,6 +315,12 @@ def run_ours(args, world, rank, local):
                                                            flush_sink, args.steps, args.warmup, world)
     pg_gbs = dbytes * world / (pg_ms * 1e-3) / 1e9
     pg_split_gbs = dbytes / (pg_split_ms * 1e-3) / 1e9
+    # ---- the same decode with an fp16 V cache
+    fv_ms, fv_split_ms, fv_steps = measure_f16v(sl8, W, wd, kc, ks, lens, qdec, seq, stream, flush, flush_sink,
+                                                args.steps, args.warmup, world)
+    fv_bytes = decode_bytes_f16v(wd, lens)
+    fv_gbs = fv_bytes * world / (fv_ms * 1e-3) / 1e9
+    fv_split_gbs = fv_bytes / (fv_split_ms * 1e-3) / 1e9
 
     # ---- e2e: public API with pinned host buffers, H2D inputs + D2H output every step
     qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
@@ -362,6 +375,12 @@ def run_ours(args, world, rank, local):
                          "roofline": {"bound": "hbm", "achieved": pg_split_gbs, "peak": peaks["hbm_gbs"],
                                       "unit": "GB/s", "frac": pg_split_gbs / peaks["hbm_gbs"], "traffic": None,
                                       "kernel": "decode_split (paged)", "peak_source": peaks["source"]}},
+        "decode_f16v": {"value": fv_gbs, "unit": "GB/s", "ms": fv_ms, "steps": fv_steps, "bytes": fv_bytes,
+                        "config": "the decode workload with int8 K and an fp16 V cache (attn_decode's fp16-V "
+                                  "variant), L2 flushed before every step",
+                        "roofline": {"bound": "hbm", "achieved": fv_split_gbs, "peak": peaks["hbm_gbs"],
+                                     "unit": "GB/s", "frac": fv_split_gbs / peaks["hbm_gbs"], "traffic": None,
+                                     "kernel": "decode_split (fp16 V)", "peak_source": peaks["source"]}},
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": attn_tflops / peaks["bf16_tflops"], "traffic": traffic.get("prefill_attn"),
                      "kernel": "prefill_attn", "launch_ms": attn_ms,
@@ -420,6 +439,49 @@ def measure_paged(sl8, W, wd, kc, ks, vc, vs, lens, qdec, seq, stream, flush, fl
     ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in events) / n, world)
     c, split_ms = trace.get("decode_split", (0, 0.0))
     return ms, (split_ms / c if c else float("nan")), n, num_pages
+
+
+def measure_f16v(sl8, W, wd, kc, ks, lens, qdec, seq, stream, flush, flush_sink, steps, warmup, world):
+    """The same decode workload with its V cache kept in fp16 (the V values cast to fp16;
+    K stays the int8 cache): split kernel plus combine, L2 flushed before each step."""
+    import torch
+    v16 = torch.zeros((wd.B, wd.Hkv, wd.lmax, wd.d), dtype=torch.float16, device=kc.device)
+    for b in range(wd.B):
+        L = int(lens[b])
+        v16[b, :, :L] = torch.from_numpy(W.decode_cache_values(wd, b, "v")).to(kc.device).to(torch.float16)
+    S = sl8.decode_num_splits(wd.B, wd.Hkv, wd.lmax, wd.d, 0)
+    o_part = torch.empty((wd.B, wd.Hq, S, wd.d), dtype=torch.float32, device=kc.device)
+    l_part = torch.empty((wd.B, wd.Hq, S), dtype=torch.float32, device=kc.device)
+    dout = torch.empty((wd.B, wd.Hq, wd.d), dtype=torch.bfloat16, device=kc.device)
+
+    def step(ev=None):
+        flush.zero_()
+        flush_sink.copy_(flush.view(torch.int64).sum())
+        if ev:
+            ev[0].record(stream)
+        sl8.attn_int8_decode_f16v(qdec, kc, ks, v16, seq, o_partial=o_part, lse_partial=l_part, out=dout)
+        if ev:
+            ev[1].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(kc.device)
+    n = max(3, min(steps, 100))
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    sl8.trace_collect()
+    sl8.trace_enable(True)
+    for i in range(n):
+        step(events[i])
+    torch.cuda.synchronize(kc.device)
+    sl8.trace_enable(False)
+    trace = sl8.trace_collect()
+    st, site = sl8.last_device_status(kc.device)
+    if st != sl8.SL8_OK:
+        raise RuntimeError(f"device status {st} at {site} during the fp16-V decode")
+    ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in events) / n, world)
+    c, split_ms = trace.get("decode_split", (0, 0.0))
+    del v16
+    return ms, (split_ms / c if c else float("nan")), n
 
 
 def load_traffic():
