@@ -69,7 +69,7 @@ def _load():
             lib.oracle_attn_prefill_head.restype = ctypes.c_int
             lib.oracle_attn_prefill_head.argtypes = [
                 _I8P, _F32P, _I8P, _F32P, _F32P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
-                ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, _F64P, _F64P, ctypes.c_void_p]
+                ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, _F64P, _F64P, ctypes.c_void_p]
             lib.oracle_decode_row.restype = ctypes.c_int
             lib.oracle_decode_row.argtypes = [
                 _I8P, ctypes.c_float, _I8P, _F32P, _I8P, _F32P, ctypes.c_int64, ctypes.c_int64,
@@ -148,7 +148,10 @@ def _seq_slices(q, k, v, cu_seqlens):
 def attn_prefill(q, k, v, causal=True, smooth_k=False, cu_seqlens=None, rows=None, want_logits=False):
     """W8A8 INT8 attention prefill, fp64 after the int32 dot.
 
-    Dense: q [B,Hq,N,d], k/v [B,Hkv,N,d].  Varlen (cu_seqlens int [nseq+1]):
+    Dense: q [B,Hq,N,d], k/v [B,Hkv,N,d], or a chunk of Nq <= Nk queries, q [B,Hq,Nq,d]
+    against k/v [B,Hkv,Nk,d]: the queries are the last Nq positions of the Nk-token
+    sequence, so causal query i sees keys j <= i + Nk - Nq (bottom-right alignment,
+    reading R19; the K mean runs over all Nk keys).  Varlen (cu_seqlens int [nseq+1]):
     q [T,Hq,d], k/v [T,Hkv,d] packed.  All inputs float32 (widened from fp16/bf16).
     rows: None for every query row, else an iterable of (seq, hq, i) with i the row
     index within its sequence.
@@ -184,8 +187,11 @@ def attn_prefill(q, k, v, causal=True, smooth_k=False, cu_seqlens=None, rows=Non
             want.setdefault((int(s), int(h)), []).append(int(i))
 
     cu = np.asarray(cu_seqlens, dtype=np.int64) if varlen else None
+    if not varlen and q.shape[2] > k.shape[2]:
+        raise ValueError("a query chunk cannot be longer than the keys")
     for s, qs, ks, vs in _seq_slices(q, k, v, cu_seqlens):
-        n = qs.shape[1]
+        nq, n = qs.shape[1], ks.shape[1]
+        q_off = n - nq
         # quantise this sequence's K (smoothed per kv head) and Q
         kc_seq = np.zeros((hkv_n, n, d), np.int8)
         ks_seq = np.zeros((hkv_n, n), np.float32)
@@ -201,8 +207,8 @@ def attn_prefill(q, k, v, causal=True, smooth_k=False, cu_seqlens=None, rows=Non
             a = int(cu[s])
             k_codes[a:a + n] = kc_seq.transpose(1, 0, 2)
             k_scales[a:a + n] = ks_seq.T
-            q_codes[a:a + n] = qc_seq.transpose(1, 0, 2)
-            q_scales[a:a + n] = qsc_seq.T
+            q_codes[a:a + nq] = qc_seq.transpose(1, 0, 2)
+            q_scales[a:a + nq] = qsc_seq.T
         else:
             k_codes[s], k_scales[s], q_codes[s], q_scales[s] = kc_seq, ks_seq, qc_seq, qsc_seq
 
@@ -216,8 +222,8 @@ def attn_prefill(q, k, v, causal=True, smooth_k=False, cu_seqlens=None, rows=Non
                 nrows = len(sel_arr)
                 rows_ptr = sel_arr.ctypes.data
             else:
-                sel_arr = np.arange(n, dtype=np.int64)
-                nrows = n
+                sel_arr = np.arange(nq, dtype=np.int64)
+                nrows = nq
                 rows_ptr = None
             if nrows == 0:
                 continue
@@ -228,7 +234,7 @@ def attn_prefill(q, k, v, causal=True, smooth_k=False, cu_seqlens=None, rows=Non
             ov = lib.oracle_attn_prefill_head(
                 np.ascontiguousarray(qc_seq[hq]), np.ascontiguousarray(qsc_seq[hq]),
                 np.ascontiguousarray(kc_seq[hkv]), np.ascontiguousarray(ks_seq[hkv]), vrows,
-                n, n, d, int(bool(causal)), rows_ptr, nrows, o_rows, l_rows,
+                nq, n, d, int(bool(causal)), q_off, rows_ptr, nrows, o_rows, l_rows,
                 None if lg is None else lg.ctypes.data)
             if ov:
                 raise OverflowError("int32 logit overflow")
@@ -241,7 +247,7 @@ def attn_prefill(q, k, v, causal=True, smooth_k=False, cu_seqlens=None, rows=Non
                 lse[s, hq, sel_arr] = l_rows
             if want_logits:
                 for r, i in enumerate(sel_arr):
-                    nn = min(int(i) + 1, n) if causal else n
+                    nn = min(int(i) + 1 + q_off, n) if causal else n
                     logits[(s, hq, int(i))] = lg[r, :nn].copy()
     return dict(out=out, lse=lse, q_codes=q_codes, q_scales=q_scales, k_codes=k_codes,
                 k_scales=k_scales, k_mean=k_mean, logits=logits)

@@ -145,15 +145,17 @@ static void attn_row(const int8_t* qc, float qs, const int8_t* kc, const float* 
 /*
  * Prefill attention for one (sequence, query head): nq query rows and nk key rows of
  * one kv head, all already quantised (codes [rows][d] int8, scales [rows]).  v is
- * [nk][d] fp32 (the widened bf16/fp16 input).  Query i (0-based within the sequence)
- * sees keys j < nk, and j <= i when causal (top-left, R9).
+ * [nk][d] fp32 (the widened bf16/fp16 input).  Query i (0-based within the query
+ * rows) sees keys j < nk, and j <= i + q_off when causal: q_off = 0 is the top-left
+ * alignment of a self-attention prefill (R9); q_off = nk - nq aligns the nq queries
+ * with the last nq keys (bottom-right, a chunk of a longer sequence, R19).
  * rows (nullable) lists the query rows to compute (nrows of them); NULL means all nq.
  * Outputs are per listed row: o [nrows][d], lse [nrows], logits [nrows][nk] (nullable;
  * entries for keys a row may not see are left untouched).
  * Returns 0, or 1 if some int32 dot overflowed (cannot happen for d <= 256).
  */
 int oracle_attn_prefill_head(const int8_t* qc, const float* qs, const int8_t* kc, const float* ks,
-                             const float* v, int64_t nq, int64_t nk, int d, int causal,
+                             const float* v, int64_t nq, int64_t nk, int d, int causal, int64_t q_off,
                              const int64_t* rows, int64_t nrows, double* o, double* lse,
                              int32_t* logits) {
   int overflow = 0;
@@ -162,7 +164,7 @@ int oracle_attn_prefill_head(const int8_t* qc, const float* qs, const int8_t* kc
   for (int64_t r = 0; r < nrows; ++r) {
     int64_t i = rows ? rows[r] : r;
     int64_t n = nk;
-    if (causal && i + 1 < n) n = i + 1;
+    if (causal && i + 1 + q_off < n) n = i + 1 + q_off;
     int ov = 0;
     attn_row(qc + i * (int64_t)d, qs[i], kc, ks, v, NULL, n, d, o + r * (int64_t)d, lse + r,
              logits ? logits + r * nk : NULL, &ov);

@@ -495,3 +495,42 @@ def test_decode_f16v_equals_int8v_on_exact_v():
     np.testing.assert_array_equal(a["lse"], b["lse"])
     for key in b["logits"]:
         np.testing.assert_array_equal(a["logits"][key], b["logits"][key])
+
+
+# ---------------------------------------------------------------- query chunks (Nq < Nk)
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_chunk_equals_tail_of_full_prefill(causal):
+    """A chunk of the last Nq queries against all Nk keys is the same computation as rows
+    Nk-Nq .. Nk-1 of the full prefill (bottom-right alignment; same K mean and codes)."""
+    rng = np.random.default_rng(60)
+    B, hq, hkv, nk, d = 2, 4, 2, 200, 64
+    qf = rng.standard_normal((B, hq, nk, d)).astype(np.float32)
+    k = (rng.standard_normal((B, hkv, nk, d)) + 3.0).astype(np.float32)
+    v = rng.standard_normal((B, hkv, nk, d)).astype(np.float32)
+    full = oracle.attn_prefill(qf, k, v, causal=causal, smooth_k=True, want_logits=True)
+    for nq in (1, 57, 200):
+        off = nk - nq
+        part = oracle.attn_prefill(qf[:, :, off:], k, v, causal=causal, smooth_k=True, want_logits=True)
+        np.testing.assert_array_equal(part["out"], full["out"][:, :, off:])
+        np.testing.assert_array_equal(part["lse"], full["lse"][:, :, off:])
+        np.testing.assert_array_equal(part["k_codes"], full["k_codes"])
+        for (s, h, i), lg in part["logits"].items():
+            np.testing.assert_array_equal(lg, full["logits"][(s, h, i + off)])
+
+
+def test_chunk_equals_textbook_bottom_right_mask():
+    rng = np.random.default_rng(61)
+    B, hq, hkv, nq, nk, d = 1, 4, 2, 40, 100, 64
+    qf, _, _ = exact_rows(rng, (B, hq, nq, d))
+    kf, _, _ = exact_rows(rng, (B, hkv, nk, d))
+    v = rng.standard_normal((B, hkv, nk, d)).astype(np.float32)
+    r = oracle.attn_prefill(qf, kf, v, causal=True, smooth_k=False)
+    g = hq // hkv
+    mask = torch.ones((nq, nk), dtype=torch.bool).tril(diagonal=nk - nq)   # j <= i + nk - nq
+    qt = torch.from_numpy(qf.astype(np.float64))
+    kt = torch.from_numpy(kf.astype(np.float64)).repeat_interleave(g, dim=1)
+    vt = torch.from_numpy(v.astype(np.float64)).repeat_interleave(g, dim=1)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask).numpy()
+    np.testing.assert_allclose(r["out"], ref, rtol=0, atol=1e-10)
+    assert mask[0].sum() == nk - nq + 1 and mask[-1].all()
