@@ -133,6 +133,22 @@ SL8_API int sl8_attn_int8_fwd(const void* q, const void* k, const void* v, int q
                       size_t workspace_bytes, void* stream);
 
 /*
+ * Prefill of a query chunk against a longer key sequence (the "Engine" table's chunked
+ * prefill onto keys already present; bottom-right alignment, reading: the pages give
+ * none): q [B][Hq][Nq][d] holds the last Nq positions of sequences whose keys and values
+ * k, v [B][Hkv][Nk][d] cover all Nk positions, 0 <= Nq <= Nk.  Query i is position
+ * i + Nk - Nq: causal, it sees keys j <= i + Nk - Nq.  K-smoothing, the K codes and the
+ * V range run over all Nk keys, so the result equals rows Nk-Nq .. Nk-1 of
+ * sl8_attn_int8_fwd on the full sequences.  out [B][Hq][Nq][d], lse_out [B][Hq][Nq].
+ * Dense input only; the workspace is sized by sl8_attn_int8_fwd_workspace_size(B, Hq,
+ * Hkv, Nk, d, 0).  Other arguments and errors as sl8_attn_int8_fwd.
+ */
+SL8_API int sl8_attn_int8_fwd_chunk(const void* q, const void* k, const void* v, int qk_dtype, int v_dtype, int32_t B,
+                                    int32_t Hq, int32_t Hkv, int32_t Nq, int32_t Nk, int32_t d, int causal,
+                                    int smooth_k, void* out, int out_dtype, float* lse_out, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+
+/*
  * Debug view of the prefill's quantisation and int32 logits (same kernels and
  * tensor-core path as sl8_attn_int8_fwd, without the mask).  Dense layout only.
  *   logits_out  device, nullable, [B][Hq][row_end - row_begin][N] int32:

@@ -226,3 +226,39 @@ def test_full_size_varlen_workload():
     ref = oracle.attn_prefill(_np(q), _np(k), _np(v), causal=True, smooth_k=True, cu_seqlens=cu.numpy(), rows=rows)
     check_f32(to_np32(o32), ref["out"], "varlen full f32")
     check_half(oh, ref["out"], "varlen full bf16")
+
+
+# ------------------------------------------------------------------ query chunks (Nq < Nk)
+
+CHUNK_CASES = [
+    # wid, B, Hq, Hkv, Nq, Nk, d, dtype, causal
+    (2601, 1, 4, 2, 100, 700, 64, "f16", True),
+    (2602, 2, 4, 1, 128, 300, 128, "bf16", True),
+    (2603, 1, 8, 4, 1, 513, 128, "bf16", True),
+    (2604, 1, 2, 2, 200, 200, 256, "bf16", True),
+    (2605, 1, 4, 2, 300, 777, 256, "bf16", True),
+    (2606, 1, 4, 4, 70, 400, 128, "bf16", False),
+    (2607, 2, 8, 2, 257, 1000, 128, "bf16", True),
+]
+
+
+@pytest.mark.parametrize("case", CHUNK_CASES, ids=[f"w{c[0]}_Nq{c[4]}_Nk{c[5]}_d{c[6]}" for c in CHUNK_CASES])
+def test_prefill_query_chunk(case):
+    """A chunk of the last Nq queries against Nk keys (bottom-right alignment) against the
+    oracle, and against the rows Nk-Nq.. of the full prefill computed by the same library."""
+    wid, B, Hq, Hkv, Nq, Nk, d, dt, causal = case
+    w = W.custom(wid, B=B, Hq=Hq, Hkv=Hkv, N=Nk, d=d, dtype=dt, k_bias_std=1.0)
+    q, k, v = W.prefill_dense(w)
+    qc = q[:, :, Nk - Nq:].contiguous()
+    o32, lse = sl8.attn_int8_fwd_chunk(qc.to(DEV), k.to(DEV), v.to(DEV), causal=causal, smooth_k=True,
+                                       out_dtype=torch.float32, return_lse=True)
+    oh = sl8.attn_int8_fwd_chunk(qc.to(DEV), k.to(DEV), v.to(DEV), causal=causal, smooth_k=True)
+    full = sl8.attn_int8_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, smooth_k=True, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    _status_ok()
+    ref = oracle.attn_prefill(_np(qc), _np(k), _np(v), causal=causal, smooth_k=True)
+    check_f32(to_np32(o32), ref["out"], f"w{wid} chunk f32")
+    check_half(oh, ref["out"], f"w{wid} chunk {dt}")
+    np.testing.assert_allclose(to_np32(lse), ref["lse"], rtol=0, atol=1e-4)
+    # the chunk's rows are the full prefill's last rows (same codes, same tiles of keys)
+    np.testing.assert_allclose(to_np32(o32), to_np32(full[:, :, Nk - Nq:]), rtol=0, atol=1e-6)

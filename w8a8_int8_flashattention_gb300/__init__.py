@@ -67,6 +67,8 @@ _SIGNATURES = {
     "sl8_attn_int8_fwd_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I64]),
     "sl8_attn_int8_fwd": (_INT, [_P, _P, _P, _INT, _INT, _I32, _I32, _I32, _I32, _I32, _P, _I64, _INT, _INT, _P,
                                  _INT, _P, _P, _SZ, _P]),
+    "sl8_attn_int8_fwd_chunk": (_INT, [_P, _P, _P, _INT, _INT, _I32, _I32, _I32, _I32, _I32, _I32, _INT, _INT, _P,
+                                       _INT, _P, _P, _SZ, _P]),
     "sl8_attn_int8_qk_logits_debug": (_INT, [_P, _P, _INT, _I32, _I32, _I32, _I32, _I32, _INT, _I32, _I32, _P, _P,
                                              _P, _P, _P, _P, _SZ, _P]),
     "sl8_attn_decode_num_splits": (_I32, [_I32, _I32, _I32, _I32, _I32]),
@@ -230,6 +232,29 @@ def attn_int8_fwd(q, k, v, causal=True, smooth_k=True, cu_seqlens=None, max_seql
                                    int(bool(causal)), int(bool(smooth_k)), _ptr(out), _dt(out),
                                    _ptr(lse) if return_lse else None, _ptr(workspace), workspace.numel(),
                                    _stream(q.device)), "sl8_attn_int8_fwd")
+    return (out, lse) if return_lse else out
+
+
+def attn_int8_fwd_chunk(q, k, v, causal=True, smooth_k=True, out_dtype=None, return_lse=False, workspace=None,
+                        out=None, lse=None):
+    """Prefill of a query chunk: q [B,Hq,Nq,d] holds the last Nq positions of sequences
+    whose keys/values k, v [B,Hkv,Nk,d] cover all Nk >= Nq positions (bottom-right causal
+    alignment).  Returns out [B,Hq,Nq,d] (and the fp32 LSE with return_lse)."""
+    _need_cuda(q, k, v, workspace)
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    out_dtype = out_dtype or v.dtype
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    if return_lse and lse is None:
+        lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    ws_bytes = prefill_workspace_bytes(B, Hq, Hkv, Nk, d, 0)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    _check(lib().sl8_attn_int8_fwd_chunk(_ptr(q), _ptr(k), _ptr(v), _dt(q), _dt(v), B, Hq, Hkv, Nq, Nk, d,
+                                         int(bool(causal)), int(bool(smooth_k)), _ptr(out), _dt(out),
+                                         _ptr(lse) if return_lse else None, _ptr(workspace), workspace.numel(),
+                                         _stream(q.device)), "sl8_attn_int8_fwd_chunk")
     return (out, lse) if return_lse else out
 
 

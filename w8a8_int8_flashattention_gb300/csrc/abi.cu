@@ -309,7 +309,8 @@ size_t sl8_attn_int8_fwd_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int3
 static int prefill_prepare(const void* q, const void* k, const void* v, int qk_dtype, int v_dtype, int32_t B,
                            int32_t Hq, int32_t Hkv, int32_t N, int32_t d, const int32_t* cu_seqlens,
                            int64_t total_tokens, int smooth_k, void* workspace, size_t workspace_bytes,
-                           cudaStream_t s, bool want_table, PrefillWorkspace* plan, SeqTable* table) {
+                           cudaStream_t s, bool want_table, PrefillWorkspace* plan, SeqTable* table,
+                           int32_t q_off = 0) {
   const bool varlen = cu_seqlens != nullptr;
   const PrefillWorkspace p = plan_prefill_workspace(B, Hq, Hkv, N, d, varlen ? total_tokens : 0, varlen);
   SL8_CHECK(workspace && aligned16(workspace) && workspace_bytes >= p.total, SL8_ERR_WORKSPACE);
@@ -333,16 +334,18 @@ static int prefill_prepare(const void* q, const void* k, const void* v, int qk_d
                              reinterpret_cast<uint16_t*>(ws + p.q_codes), reinterpret_cast<float*>(ws + p.q_scales),
                              reinterpret_cast<uint16_t*>(ws + p.k_codes), reinterpret_cast<float*>(ws + p.k_scales),
                              convert_v ? v : nullptr, convert_v ? reinterpret_cast<int32_t*>(ws + p.v_exp) : nullptr,
-                             convert_v ? reinterpret_cast<uint16_t*>(ws + p.v16) : nullptr, s));
+                             convert_v ? reinterpret_cast<uint16_t*>(ws + p.v16) : nullptr, s, q_off));
   *plan = p;
   *table = t;
   return SL8_OK;
 }
 
-int sl8_attn_int8_fwd(const void* q, const void* k, const void* v, int qk_dtype, int v_dtype, int32_t B, int32_t Hq,
-                      int32_t Hkv, int32_t N, int32_t d, const int32_t* cu_seqlens, int64_t total_tokens,
-                      int causal, int smooth_k, void* out, int out_dtype, float* lse_out, void* workspace,
-                      size_t workspace_bytes, void* stream) {
+// Prefill over N keys per sequence; q_off > 0 (dense only): a query chunk of the last
+// N - q_off positions, aligned bottom-right.
+static int prefill_run(const void* q, const void* k, const void* v, int qk_dtype, int v_dtype, int32_t B, int32_t Hq,
+                       int32_t Hkv, int32_t N, int32_t d, const int32_t* cu_seqlens, int64_t total_tokens, int causal,
+                       int smooth_k, void* out, int out_dtype, float* lse_out, void* workspace, size_t workspace_bytes,
+                       void* stream, int32_t q_off) {
   int rc = validate_prefill(q, k, qk_dtype, B, Hq, Hkv, N, d);
   if (rc != SL8_OK) return rc;
   SL8_CHECK(v && out && aligned16(v) && aligned16(out), SL8_ERR_INVALID_ARG);
@@ -356,10 +359,11 @@ int sl8_attn_int8_fwd(const void* q, const void* k, const void* v, int qk_dtype,
   PrefillWorkspace p;
   SeqTable t;
   rc = prefill_prepare(q, k, v, qk_dtype, v_dtype, B, Hq, Hkv, N, d, cu_seqlens, total_tokens, smooth_k, workspace,
-                       workspace_bytes, s, false, &p, &t);
+                       workspace_bytes, s, false, &p, &t, q_off);
   if (rc != SL8_OK) return rc;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   PrefillArgs a{};
+  a.q_off = q_off;
   a.q_codes = reinterpret_cast<const uint16_t*>(ws + p.q_codes);
   a.q_scales = reinterpret_cast<const float*>(ws + p.q_scales);
   a.k_codes = reinterpret_cast<const uint16_t*>(ws + p.k_codes);
@@ -379,7 +383,9 @@ int sl8_attn_int8_fwd(const void* q, const void* k, const void* v, int qk_dtype,
   a.total_tokens = a.varlen ? total_tokens : static_cast<int64_t>(B) * N;
   a.t_pad_max = p.t_pad_max;
   a.table = t;
-  a.dense_items = (N + prefill_item_rows(d, Hq / Hkv) - 1) / prefill_item_rows(d, Hq / Hkv);
+  const int32_t item_rows = prefill_item_rows(d, Hq / Hkv);
+  a.dense_first = q_off / item_rows;
+  a.dense_items = (N + item_rows - 1) / item_rows - a.dense_first;
   a.head_pairs = prefill_head_pairs(d, Hq / Hkv);
   a.max_pairs = p.max_pairs;
   a.causal = causal != 0;
@@ -389,6 +395,24 @@ int sl8_attn_int8_fwd(const void* q, const void* k, const void* v, int qk_dtype,
   a.logits = nullptr;
   SL8_LAUNCH(launch_prefill(a, s));
   return SL8_OK;
+}
+
+int sl8_attn_int8_fwd(const void* q, const void* k, const void* v, int qk_dtype, int v_dtype, int32_t B, int32_t Hq,
+                      int32_t Hkv, int32_t N, int32_t d, const int32_t* cu_seqlens, int64_t total_tokens,
+                      int causal, int smooth_k, void* out, int out_dtype, float* lse_out, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  return prefill_run(q, k, v, qk_dtype, v_dtype, B, Hq, Hkv, N, d, cu_seqlens, total_tokens, causal, smooth_k, out,
+                     out_dtype, lse_out, workspace, workspace_bytes, stream, 0);
+}
+
+int sl8_attn_int8_fwd_chunk(const void* q, const void* k, const void* v, int qk_dtype, int v_dtype, int32_t B,
+                            int32_t Hq, int32_t Hkv, int32_t Nq, int32_t Nk, int32_t d, int causal, int smooth_k,
+                            void* out, int out_dtype, float* lse_out, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  SL8_CHECK(Nq >= 0 && Nq <= Nk, SL8_ERR_INVALID_ARG);
+  if (Nq == 0) return SL8_OK;
+  return prefill_run(q, k, v, qk_dtype, v_dtype, B, Hq, Hkv, Nk, d, nullptr, 0, causal, smooth_k, out, out_dtype,
+                     lse_out, workspace, workspace_bytes, stream, Nk - Nq);
 }
 
 int sl8_attn_int8_qk_logits_debug(const void* q, const void* k, int qk_dtype, int32_t B, int32_t Hq, int32_t Hkv,

@@ -107,7 +107,8 @@ __device__ __forceinline__ int item_heads(const PrefillArgs& a) { return a.head_
 
 // Work item -> (sequence, item index, heads, extent).  Varlen input uses the scheduler's
 // longest-first list; dense input (every sequence N long) needs no table: pair p is item
-// index max_items - 1 - p / nseq of sequence p % nseq, which is the same order.  With
+// index max_items - 1 - p / nseq of sequence p % nseq, which is the same order (a query
+// chunk's items start at dense_first, the item holding its first position).  With
 // head pairs, w.hq is the first of the item's two query heads.
 __device__ __forceinline__ Item decode_item(const PrefillArgs& a, int64_t item, int group) {
   Item w;
@@ -124,7 +125,7 @@ __device__ __forceinline__ Item decode_item(const PrefillArgs& a, int64_t item, 
   } else {
     const int64_t level = pair / a.nseq;
     w.s = static_cast<int32_t>(pair - level * a.nseq);
-    w.it = a.dense_items - 1 - static_cast<int32_t>(level);
+    w.it = a.dense_first + a.dense_items - 1 - static_cast<int32_t>(level);
     w.L = a.N;
     w.pstart = w.s * ((a.N + kQTile - 1) / kQTile) * kPadRows;
     w.tok0 = w.s * a.N;
@@ -149,8 +150,9 @@ __device__ __forceinline__ Item tile_item(const PrefillArgs& a, const Item& w, i
 
 // Key tiles of BN keys that Q tile qt (128 rows) visits; 0 if the tile is past the end.
 template <int BN>
-__device__ __forceinline__ int tile_nkv(int qt, int L, bool causal) {
-  if (qt * kQTile >= L) return 0;
+__device__ __forceinline__ int tile_nkv(int qt, int L, bool causal, int q_off) {
+  // past the end, or (query chunk) wholly before its first position
+  if (qt * kQTile >= L || (qt + 1) * kQTile <= q_off) return 0;
   const int kend = causal ? min(L, (qt + 1) * kQTile) : L;
   return (kend + BN - 1) / BN;
 }
@@ -367,11 +369,12 @@ __device__ __forceinline__ void logits_step(uint32_t s_taddr, const PrefillArgs&
 template <int D>
 __device__ __forceinline__ void store_row(uint32_t o_taddr, const PrefillArgs& a, const Item& w, int row_abs, float m,
                                           float l, float v_unscale) {
-  const bool row_ok = row_abs < w.L;
+  const bool row_ok = row_abs < w.L && row_abs >= a.q_off;
   const float scale = v_unscale / l;
   const bool out_f32 = a.out_dtype == SL8_F32, out_bf16 = a.out_dtype == SL8_BF16;
+  // a query chunk's output holds positions q_off .. N-1
   const int64_t orow = a.varlen ? (static_cast<int64_t>(w.tok0) + row_abs) * a.Hq + w.hq
-                                : (static_cast<int64_t>(w.s) * a.Hq + w.hq) * a.N + row_abs;
+                                : (static_cast<int64_t>(w.s) * a.Hq + w.hq) * (a.N - a.q_off) + row_abs - a.q_off;
   // 64 columns per TMEM round trip
 #pragma unroll
   for (int c0 = 0; c0 < D; c0 += 64) {
@@ -571,7 +574,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
         mbar_arrive(&bars.item_full[slot]);
         if (item < 0) break;
         const Item w = decode_item(a, item, group);
-        const int nkv = max(tile_nkv<BN>(tile_qt(a, w, 0), w.L, causal), tile_nkv<BN>(tile_qt(a, w, 1), w.L, causal));
+        const int nkv = max(tile_nkv<BN>(tile_qt(a, w, 0), w.L, causal, a.q_off), tile_nkv<BN>(tile_qt(a, w, 1), w.L, causal, a.q_off));
         // both Q tiles are always loaded (a tile past the end reads rows no one uses)
         for (int t = 0; t < 2 && ok; ++t) {
           if (it >= 1) ok = mbar_wait(&bars.q_empty[t], (it - 1) & 1, limit_ns, st, 10);
@@ -605,8 +608,8 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
         if (lane == 0) mbar_arrive(&bars.item_empty[slot]);
         if (item < 0) break;
         const Item w = decode_item(a, item, group);
-        const int nkv_t[2] = {tile_nkv<BN>(tile_qt(a, w, 0), w.L, causal),
-                              tile_nkv<BN>(tile_qt(a, w, 1), w.L, causal)};
+        const int nkv_t[2] = {tile_nkv<BN>(tile_qt(a, w, 0), w.L, causal, a.q_off),
+                              tile_nkv<BN>(tile_qt(a, w, 1), w.L, causal, a.q_off)};
         const int nkv = max(nkv_t[0], nkv_t[1]);
         ok = warp_wait(&bars.q_full[0], it & 1, limit_ns, st, 20) &&
              warp_wait(&bars.q_full[1], it & 1, limit_ns, st, 20);
@@ -689,7 +692,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
       if (item < 0) break;
       const Item w = tile_item(a, decode_item(a, item, group), t);  // this warpgroup's Q tile
       const int qt = tile_qt(a, w, t);
-      const int nkv = tile_nkv<BN>(qt, w.L, causal);
+      const int nkv = tile_nkv<BN>(qt, w.L, causal, a.q_off);
       if (nkv == 0) continue;  // this tile lies past the sequence's end
       const int row_abs = qt * kQTile + r;
       QuadRows rs;
@@ -841,7 +844,7 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
       bool ok = true;
       for (int64_t item = blockIdx.x; item < n_items && ok && !*abort_flag; item += gridDim.x, ++it) {
         const Item w = decode_item(a, item, group);
-        const int nkv = tile_nkv<BN>(w.it, w.L, causal);
+        const int nkv = tile_nkv<BN>(w.it, w.L, causal, a.q_off);
         if (it >= 1) ok = mbar_wait(&bars.q_empty, (it - 1) & 1, limit_ns, st, 10);
         if (!ok) break;
         mbar_arrive_expect_tx(&bars.q_full, C::kQBytes);
@@ -868,7 +871,7 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
       int nkv_s = 0, nkv_p = 0;
       if (item_s < n_items) {
         const Item ws = decode_item(a, item_s, group);
-        nkv_s = tile_nkv<BN>(ws.it, ws.L, causal);
+        nkv_s = tile_nkv<BN>(ws.it, ws.L, causal, a.q_off);
         nkv_p = nkv_s;
       }
       bool ok = true, issued = false;
@@ -892,7 +895,7 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
             item_s += gridDim.x;
             if (item_s < n_items) {
               const Item ws = decode_item(a, item_s, group);
-              nkv_s = tile_nkv<BN>(ws.it, ws.L, causal);
+              nkv_s = tile_nkv<BN>(ws.it, ws.L, causal, a.q_off);
             }
           }
         }
@@ -912,7 +915,7 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
           item_p += gridDim.x;
           if (item_p < n_items) {
             const Item wp = decode_item(a, item_p, group);
-            nkv_p = tile_nkv<BN>(wp.it, wp.L, causal);
+            nkv_p = tile_nkv<BN>(wp.it, wp.L, causal, a.q_off);
           }
         }
       }
@@ -946,7 +949,7 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
     }
     bool bad = false;
     while (item < n_items) {
-      const int nkv = tile_nkv<BN>(w.it, w.L, causal);
+      const int nkv = tile_nkv<BN>(w.it, w.L, causal, a.q_off);
       const int row_abs = w.it * kQTile + r;
       QuadRows rs;
 #pragma unroll

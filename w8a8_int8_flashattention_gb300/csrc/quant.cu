@@ -639,6 +639,7 @@ struct QuantQK {
   const void* k;
   bool varlen;
   int32_t nseq, Hq, Hkv, N;
+  int32_t q_off;            // dense query chunk: q holds positions q_off .. N-1
   int64_t total_tokens;
   SeqTable t;
   int64_t t_pad_max;
@@ -771,7 +772,7 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quant_qk_kernel(const QuantQ
       if (!a.varlen) {
         sq[p] = static_cast<int>(pr / seq_rows);
         tt[p] = static_cast<int32_t>(pr - sq[p] * seq_rows);
-        valid[p] = tt[p] < a.N;
+        valid[p] = tt[p] < a.N && (is_k || tt[p] >= a.q_off);
       } else {
         // sequence owning padded row pr: the last s with pstart[s] <= pr
         int lo = 0, hi = a.nseq - 1;
@@ -795,7 +796,10 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quant_qk_kernel(const QuantQ
       vw[p][j] = make_uint4(0u, 0u, 0u, 0u);
     }
     if (valid[p]) {
-      const int64_t off = row_offset(a.varlen, sq[p], h, tt[p], H, a.N, D, tk) + part * EPL;
+      // a query chunk's rows: position t is row t - q_off of N - q_off
+      const int64_t off = (is_k ? row_offset(a.varlen, sq[p], h, tt[p], H, a.N, D, tk)
+                                : row_offset(a.varlen, sq[p], h, tt[p] - a.q_off, H, a.N - a.q_off, D, tk)) +
+                          part * EPL;
 #pragma unroll
       for (int j = 0; j < NV; ++j) {
         xw[p][j] = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + off + 8 * j);
@@ -892,8 +896,9 @@ cudaError_t launch_quant_qk(const void* q, const void* k, sl8_dtype dt, bool var
                             int32_t Hkv, int32_t N, int32_t d, int64_t total_tokens, const SeqTable& t,
                             int64_t t_pad_max, const float* k_partials, const float* v_partials,
                             int32_t max_chunks, uint16_t* q_codes, float* q_scales, uint16_t* k_codes,
-                            float* k_scales, const void* v, int32_t* v_exp, uint16_t* v16, cudaStream_t s) {
-  QuantQK a{q, k, varlen, nseq, Hq, Hkv, N, total_tokens, t, t_pad_max, k_partials, v_partials, max_chunks, v_exp,
+                            float* k_scales, const void* v, int32_t* v_exp, uint16_t* v16, cudaStream_t s,
+                            int32_t q_off) {
+  QuantQK a{q, k, varlen, nseq, Hq, Hkv, N, q_off, total_tokens, t, t_pad_max, k_partials, v_partials, max_chunks, v_exp,
             q_codes, q_scales, k_codes, k_scales, v, v16};
   TraceScope tr("quant_qk", s);
   return dt == SL8_BF16 ? launch_quant_qk_dt<SL8_BF16>(a, d, Hq + Hkv, s)

@@ -101,12 +101,15 @@ cudaError_t launch_kv_partials(const void* k, sl8_dtype dt, const void* v, bool 
                                float* v_partials, int32_t max_chunks, cudaStream_t s);
 // Q and K rows of prefill in one launch.  K CTAs form the mean from k_partials (nullable:
 // no smoothing) and, with v16 set, the V exponent from v_partials (published in v_exp) and
-// write V as fp16 * 2^-v_exp.  t is read for varlen input only.
+// write V as fp16 * 2^-v_exp.  t is read for varlen input only.  q_off > 0 (dense): q holds
+// N - q_off rows per (sequence, head), the positions q_off .. N-1; the code rows of the
+// positions before it are zero.
 cudaError_t launch_quant_qk(const void* q, const void* k, sl8_dtype dt, bool varlen, int32_t nseq, int32_t Hq,
                             int32_t Hkv, int32_t N, int32_t d, int64_t total_tokens, const SeqTable& t,
                             int64_t t_pad_max, const float* k_partials, const float* v_partials,
                             int32_t max_chunks, uint16_t* q_codes, float* q_scales, uint16_t* k_codes,
-                            float* k_scales, const void* v, int32_t* v_exp, uint16_t* v16, cudaStream_t s);
+                            float* k_scales, const void* v, int32_t* v_exp, uint16_t* v16, cudaStream_t s,
+                            int32_t q_off = 0);
 cudaError_t launch_quant_rowwise(const void* x, sl8_dtype dt, int64_t rows, int32_t cols, int64_t row_stride,
                                  const float* sub_mean, int64_t rows_per_group, int8_t* q_out, float* scale_out,
                                  cudaStream_t s);
@@ -125,10 +128,12 @@ struct PrefillArgs {
   const int32_t* v_exp;     // [nseq][Hkv] (nullable = 0)
   bool varlen;
   int32_t nseq, Hq, Hkv, N, d;
+  int32_t q_off;             // dense query chunk: q and out hold positions q_off .. N-1 (N keys)
   int64_t total_tokens;
   int64_t t_pad_max;
   SeqTable table;            // varlen only: the dense layout is arithmetic
-  int32_t dense_items;       // items per sequence of a dense input (ceil(N / item rows))
+  int32_t dense_items;       // items per sequence of a dense input (ceil(N / item rows) - dense_first)
+  int32_t dense_first;       // first item of a dense query chunk (q_off / item rows; 0 otherwise)
   bool head_pairs;           // see prefill_head_pairs
   int64_t max_pairs;
   bool causal;
