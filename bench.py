@@ -9,8 +9,9 @@ One step = one pass of the whole path over one batch of synthetic input:
 `value` is prefill TOPS (ops = 2 x 2 x d x causal pairs x heads, QK^T and P.V);
 the decode KV GB/s sits in `decode`, and `paged_decode` repeats the decode over a
 paged k8v8 cache (64-token pages in a seeded random order) in a loop of its own after
-the timed steps, and `decode_f16v` the decode with an fp16 V cache (int8 K).  Inputs
-are resident in HBM when the timed
+the timed steps, `decode_f16v` the decode with an fp16 V cache (int8 K), and
+`prefill_chunk` the prefill's last 1024 positions as a query chunk (chunked prefill,
+bottom-right causal).  Inputs are resident in HBM when the timed
 region starts; L2 is flushed before every step, outside the timed events (a 256 MB
 write, then a read of that buffer, so no dirty lines of the flush remain).  `e2e` repeats the prefill through the public API with pinned host
 inputs copied in and the output copied back every step.
@@ -44,6 +45,16 @@ METRIC = "W8A8 attn prefill TOPS & decode KV GB/s (1xGB300, % of INT8-TC / HBM r
 
 def prefill_ops(w) -> float:
     pairs = w.N * (w.N + 1) // 2 * w.Hq * w.B
+    return 2.0 * 2.0 * w.d * pairs
+
+
+CHUNK_Q = 1024   # query chunk of the chunked-prefill line: the last 1024 of the 4096 positions
+
+
+def chunk_ops(w, nq) -> float:
+    """QK^T + P.V ops of a causal query chunk of the last nq positions of N keys."""
+    off = w.N - nq
+    pairs = (nq * off + nq * (nq + 1) // 2) * w.Hq * w.B
     return 2.0 * 2.0 * w.d * pairs
 
 
@@ -315,6 +326,11 @@ def run_ours(args, world, rank, local):
                                                            flush_sink, args.steps, args.warmup, world)
     pg_gbs = dbytes * world / (pg_ms * 1e-3) / 1e9
     pg_split_gbs = dbytes / (pg_split_ms * 1e-3) / 1e9
+    # ---- the prefill's last positions as a query chunk
+    ch_ms, ch_attn_ms, ch_steps = measure_chunk(sl8, wp, qd, kd, vd, stream, flush, flush_sink, args.steps,
+                                                args.warmup, world)
+    ch_ops = chunk_ops(wp, CHUNK_Q)
+    ch_tflops = ch_ops / (ch_attn_ms * 1e-3) / 1e12
     # ---- the same decode with an fp16 V cache
     fv_ms, fv_split_ms, fv_steps = measure_f16v(sl8, W, wd, kc, ks, lens, qdec, seq, stream, flush, flush_sink,
                                                 args.steps, args.warmup, world)
@@ -375,6 +391,14 @@ def run_ours(args, world, rank, local):
                          "roofline": {"bound": "hbm", "achieved": pg_split_gbs, "peak": peaks["hbm_gbs"],
                                       "unit": "GB/s", "frac": pg_split_gbs / peaks["hbm_gbs"], "traffic": None,
                                       "kernel": "decode_split (paged)", "peak_source": peaks["source"]}},
+        "prefill_chunk": {"value": ch_ops * world / (ch_ms * 1e-3) / 1e12, "unit": "TOPS", "ms": ch_ms,
+                          "steps": ch_steps, "ops": ch_ops,
+                          "config": f"the prefill workload's last {CHUNK_Q} positions as a query chunk against "
+                                    f"all {wp.N} keys (bottom-right causal), quantisation included, L2 flushed "
+                                    "before every step",
+                          "roofline": {"bound": "tensor", "achieved": ch_tflops, "peak": peaks["bf16_tflops"],
+                                       "unit": "TFLOP/s", "frac": ch_tflops / peaks["bf16_tflops"], "traffic": None,
+                                       "kernel": "prefill_attn (chunk)", "peak_source": peaks["source"]}},
         "decode_f16v": {"value": fv_gbs, "unit": "GB/s", "ms": fv_ms, "steps": fv_steps, "bytes": fv_bytes,
                         "config": "the decode workload with int8 K and an fp16 V cache (attn_decode's fp16-V "
                                   "variant), L2 flushed before every step",
@@ -482,6 +506,44 @@ def measure_f16v(sl8, W, wd, kc, ks, lens, qdec, seq, stream, flush, flush_sink,
     c, split_ms = trace.get("decode_split", (0, 0.0))
     del v16
     return ms, (split_ms / c if c else float("nan")), n
+
+
+def measure_chunk(sl8, wp, qd, kd, vd, stream, flush, flush_sink, steps, warmup, world):
+    """The prefill workload's last CHUNK_Q positions as a query chunk against all N keys
+    (chunked prefill, bottom-right causal): quantisation and attention, L2 flushed before
+    each step."""
+    import torch
+    qc = qd[:, :, wp.N - CHUNK_Q:].contiguous()
+    ws = torch.empty(sl8.prefill_workspace_bytes(wp.B, wp.Hq, wp.Hkv, wp.N, wp.d), dtype=torch.uint8, device=qd.device)
+    out = torch.empty_like(qc)
+
+    def step(ev=None):
+        flush.zero_()
+        flush_sink.copy_(flush.view(torch.int64).sum())
+        if ev:
+            ev[0].record(stream)
+        sl8.attn_int8_fwd_chunk(qc, kd, vd, causal=True, smooth_k=True, workspace=ws, out=out)
+        if ev:
+            ev[1].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(qd.device)
+    n = max(3, min(steps, 100))
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    sl8.trace_collect()
+    sl8.trace_enable(True)
+    for i in range(n):
+        step(events[i])
+    torch.cuda.synchronize(qd.device)
+    sl8.trace_enable(False)
+    trace = sl8.trace_collect()
+    st, site = sl8.last_device_status(qd.device)
+    if st != sl8.SL8_OK:
+        raise RuntimeError(f"device status {st} at {site} during the chunked prefill")
+    ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in events) / n, world)
+    c, attn_ms = trace.get("prefill_attn", (0, 0.0))
+    return ms, (attn_ms / c if c else float("nan")), n
 
 
 def load_traffic():
