@@ -669,7 +669,7 @@ __device__ __forceinline__ void store_vec16(uint16_t* p, const uint16_t (&h)[EPL
 // Eight lanes per row (EPL = D / 8 values each, 16-byte accesses), four rows per warp
 // instruction.
 template <sl8_dtype DT, int D>
-__global__ void __launch_bounds__(kQuantWarps * 32) quant_qk_kernel(const QuantQK a, DeviceStatus* st) {
+__global__ void __launch_bounds__(kQuantWarps * 32, D == 256 ? 2 : 4) quant_qk_kernel(const QuantQK a, DeviceStatus* st) {
   constexpr int LPR = 8, EPL = D / LPR, NV = EPL / 8, RPP = 32 / LPR, P = kQuantRowsPerWarp / RPP;
   // K heads first: their CTAs also form the K mean and the V exponent, so they start
   // in the first wave and the Q CTAs fill in behind them
@@ -756,7 +756,28 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quant_qk_kernel(const QuantQ
     }
     __syncthreads();
   }
-  // this lane's rows (one per pass): owning sequence, position, validity; then all loads
+  // the CTA's rows all belong to one sequence (sequences start on 128-row boundaries and
+  // a CTA covers an aligned block of 64 rows): find it once
+  static_assert(kPadRows % (kQuantWarps * kQuantRowsPerWarp) == 0, "a CTA's rows lie in one sequence");
+  int cta_s = 0, cta_len = a.N;
+  int64_t cta_pstart = 0;
+  int32_t tk = 0;
+  if (!a.varlen) {
+    cta_s = static_cast<int>(cta_row0 / seq_rows);
+    cta_pstart = static_cast<int64_t>(cta_s) * seq_rows;
+  } else {
+    // the last s with pstart[s] <= cta_row0
+    int lo = 0, hi = a.nseq - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) / 2;
+      if (a.t.pstart[mid] <= cta_row0) lo = mid; else hi = mid - 1;
+    }
+    cta_s = lo;
+    cta_pstart = a.t.pstart[lo];
+    cta_len = a.t.len[lo];
+    tk = a.t.tok0[lo];
+  }
+  // this lane's rows (one per pass): position, validity; then all loads
   int sq[P], tt[P];
   bool live[P], valid[P];
   uint4 xw[P][NV], vw[P][NV];
@@ -765,25 +786,13 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quant_qk_kernel(const QuantQ
     const int64_t pr = row0 + p * RPP + rsub;
     live[p] = pr < rows_used && pr < a.t_pad_max;
     valid[p] = false;
-    sq[p] = 0;
-    tt[p] = 0;
-    int32_t tk = 0;
+    sq[p] = cta_s;
+    tt[p] = static_cast<int32_t>(pr - cta_pstart);
     if (live[p]) {
       if (!a.varlen) {
-        sq[p] = static_cast<int>(pr / seq_rows);
-        tt[p] = static_cast<int32_t>(pr - sq[p] * seq_rows);
         valid[p] = tt[p] < a.N && (is_k || tt[p] >= a.q_off);
       } else {
-        // sequence owning padded row pr: the last s with pstart[s] <= pr
-        int lo = 0, hi = a.nseq - 1;
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) / 2;
-          if (a.t.pstart[mid] <= pr) lo = mid; else hi = mid - 1;
-        }
-        sq[p] = lo;
-        tt[p] = static_cast<int32_t>(pr - a.t.pstart[lo]);
-        tk = a.t.tok0[lo];
-        valid[p] = tt[p] < a.t.len[lo];
+        valid[p] = tt[p] < cta_len;
         if (valid[p] && static_cast<int64_t>(tk) + tt[p] >= a.total_tokens) {
           record_status(st, kStatusBadArg, 901);
           valid[p] = false;
