@@ -333,6 +333,55 @@ def attn_decode_f16v(q, k_codes, k_scales, v, seqlens, num_splits=1, split_size=
                    want_logits)
 
 
+def attn_decode_verify(q, k_codes, k_scales, v_codes, v_scales, seqlens, tree_mask, rows=None):
+    """Speculative-decode verification over an int8 cache, fp64 after the int32 dot.
+
+    Source: the "SuperL8" README, "Attention kernels" table, attn_decode row (its
+    "verify mask" variant) and attn_tree_fwd row (tree-structured verification), with
+    the "Speculative decoding" table's drafters building chain or tree masks.  Reading
+    (R20): q [B, T, Hq, d] holds T draft queries per sequence; the cache (as attn_decode)
+    already holds the T draft tokens at positions L_b - T .. L_b - 1; query t sees every
+    position below L_b - T and draft token u (position L_b - T + u, when >= 0) iff bit u
+    of tree_mask[b, t] is set (uint32, T <= 32).  Each (b, t, hq) row is the attention of
+    its quantised query over exactly those positions.  Returns dict(out [B,T,Hq,d] f64,
+    lse [B,T,Hq], q_codes [B,T,Hq,d], q_scales [B,T,Hq]).
+    """
+    q = _f32(q)
+    k_codes = np.ascontiguousarray(k_codes, np.int8)
+    v_codes = np.ascontiguousarray(v_codes, np.int8)
+    k_scales = _f32(k_scales)
+    v_scales = _f32(v_scales)
+    seqlens = np.asarray(seqlens, np.int64)
+    tree_mask = np.asarray(tree_mask, np.uint64)
+    B, T, hq_n, d = q.shape
+    hkv_n = k_codes.shape[1]
+    group = hq_n // hkv_n
+    lib = _load()
+    q_codes, q_scales = quant_rowwise(q)
+    out = np.full((B, T, hq_n, d), np.nan, np.float64)
+    lse = np.full((B, T, hq_n), np.nan, np.float64)
+    triples = ([(b, t, h) for b in range(B) for t in range(T) for h in range(hq_n)] if rows is None
+               else [(int(b), int(t), int(h)) for b, t, h in rows])
+    for b, t, hq in triples:
+        hkv = hq // group
+        L = int(seqlens[b])
+        tail = L - T
+        pos = list(range(max(tail, 0)))
+        pos += [tail + u for u in range(T) if tail + u >= 0 and (int(tree_mask[b, t]) >> u) & 1]
+        pos = np.asarray(pos, np.int64)
+        n = len(pos)
+        kc = np.ascontiguousarray(k_codes[b, hkv][pos])
+        ksc = np.ascontiguousarray(k_scales[b, hkv][pos])
+        vc = np.ascontiguousarray(v_codes[b, hkv][pos])
+        vsc = np.ascontiguousarray(v_scales[b, hkv][pos])
+        o = np.zeros(d, np.float64)
+        lv = np.zeros(1, np.float64)
+        lib.oracle_decode_row(q_codes[b, t, hq], float(q_scales[b, t, hq]), kc, ksc, vc, vsc, n, 0, n, d, o, lv,
+                              None)
+        out[b, t, hq], lse[b, t, hq] = o, lv[0]
+    return dict(out=out, lse=lse, q_codes=q_codes, q_scales=q_scales)
+
+
 def _decode(q, rows_of, hkv_n, lmax, seqlens, num_splits, split_size, rows, want_logits):
     """The split loop shared by the decode oracles; rows_of(b, hkv, L) gives the kv head's
     cache rows (k codes, k scales, v codes, v scales) for tokens 0 .. L-1 (at least); v

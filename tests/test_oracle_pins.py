@@ -534,3 +534,55 @@ def test_chunk_equals_textbook_bottom_right_mask():
     ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask).numpy()
     np.testing.assert_allclose(r["out"], ref, rtol=0, atol=1e-10)
     assert mask[0].sum() == nk - nq + 1 and mask[-1].all()
+
+
+# ---------------------------------------------------------------- verify mask (speculative decoding)
+
+def _verify_case(rng, B=2, T=4, hq=4, hkv=2, lmax=64, d=64, lens=(40, 64)):
+    q = rng.standard_normal((B, T, hq, d)).astype(np.float32)
+    kc = rng.integers(-127, 128, size=(B, hkv, lmax, d)).astype(np.int8)
+    vc = rng.integers(-127, 128, size=(B, hkv, lmax, d)).astype(np.int8)
+    ks = rng.uniform(0.001, 0.05, size=(B, hkv, lmax)).astype(np.float32)
+    vs = rng.uniform(0.001, 0.05, size=(B, hkv, lmax)).astype(np.float32)
+    return q, kc, ks, vc, vs, np.array(lens)
+
+
+def test_verify_chain_mask_equals_decode_prefixes():
+    """A chain of drafts (query t sees drafts 0..t) is decode of query t at length
+    L - T + t + 1."""
+    rng = np.random.default_rng(70)
+    q, kc, ks, vc, vs, lens = _verify_case(rng)
+    T = q.shape[1]
+    chain = np.array([[(1 << (t + 1)) - 1 for t in range(T)]] * len(lens), np.uint32)
+    r = oracle.attn_decode_verify(q, kc, ks, vc, vs, lens, chain)
+    for t in range(T):
+        ref = oracle.attn_decode(q[:, t], kc, ks, vc, vs, lens - T + t + 1, num_splits=1)
+        np.testing.assert_allclose(r["out"][:, t], ref["out"], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(r["lse"][:, t], ref["lse"], rtol=0, atol=1e-13)
+
+
+def test_verify_full_mask_equals_decode():
+    rng = np.random.default_rng(71)
+    q, kc, ks, vc, vs, lens = _verify_case(rng)
+    T = q.shape[1]
+    full = np.full((len(lens), T), (1 << T) - 1, np.uint32)
+    r = oracle.attn_decode_verify(q, kc, ks, vc, vs, lens, full)
+    for t in range(T):
+        ref = oracle.attn_decode(q[:, t], kc, ks, vc, vs, lens, num_splits=1)
+        np.testing.assert_allclose(r["out"][:, t], ref["out"], rtol=0, atol=1e-13)
+
+
+def test_verify_tree_mask_drops_siblings():
+    """Two sibling drafts (each sees only itself): query 1 must not see draft 0, i.e. it
+    equals decode over a cache with draft 0's row removed."""
+    rng = np.random.default_rng(72)
+    q, kc, ks, vc, vs, lens = _verify_case(rng, B=1, T=2, lens=(30,))
+    mask = np.array([[0b01, 0b10]], np.uint32)
+    r = oracle.attn_decode_verify(q, kc, ks, vc, vs, lens, mask)
+    keep = [i for i in range(30) if i != 28]                      # draft 0 sits at position 28
+    kc2, ks2 = kc[:, :, keep], ks[:, :, keep]
+    vc2, vs2 = vc[:, :, keep], vs[:, :, keep]
+    ref = oracle.attn_decode(q[:, 1], kc2, ks2, vc2, vs2, [29], num_splits=1)
+    np.testing.assert_allclose(r["out"][:, 1], ref["out"], rtol=0, atol=1e-13)
+    ref0 = oracle.attn_decode(q[:, 0], kc, ks, vc, vs, [29], num_splits=1)   # draft 0 sees positions 0..28
+    np.testing.assert_allclose(r["out"][:, 0], ref0["out"], rtol=0, atol=1e-13)
