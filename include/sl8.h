@@ -193,6 +193,28 @@ SL8_API int sl8_attn_int8_decode_splitkv(const void* q, int q_dtype, const int8_
                                  float* o_partial, float* lse_partial, void* stream);
 
 /*
+ * Speculative-decode verification over the int8 cache: the attn_decode row's "verify
+ * mask" variant and the attn_tree_fwd row ("Attention kernels" table; tree or chain
+ * masks from the "Speculative decoding" table's drafters).  Reading (the pages give no
+ * layout): the cache (as sl8_attn_int8_decode_splitkv) already holds each sequence's T
+ * draft tokens at positions L_b - T .. L_b - 1, and
+ *   q          device, [B][T][Hq][d] (q_dtype F16, BF16 or F32): the drafts' queries.
+ *   tree_mask  device, [B][T] uint32: query t sees every position below L_b - T and
+ *              draft token u (position L_b - T + u, if >= 0) iff bit u is set.
+ *   T          1 .. 32 draft tokens per sequence; B * T <= 65535.
+ *   o_partial, lse_partial  scratch, [B * T][Hq][S][d] and [B * T][Hq][S] fp32 with
+ *              S = sl8_attn_decode_num_splits(B * T, Hkv, Lmax, d, num_splits).
+ *   out        device, [B][T][Hq][d] of out_dtype (F16, BF16 or F32); lse_out nullable
+ *              [B][T][Hq].
+ * Runs the split kernel (one pass over sequence b's cache per draft query) and the combine.
+ */
+SL8_API int sl8_attn_int8_decode_verify(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale,
+                                        const int8_t* v_cache, const float* v_scale, const int32_t* seqlens,
+                                        const uint32_t* tree_mask, int32_t T, int32_t B, int32_t Hq, int32_t Hkv,
+                                        int32_t Lmax, int32_t d, int32_t num_splits, float* o_partial,
+                                        float* lse_partial, void* out, int out_dtype, float* lse_out, void* stream);
+
+/*
  * Split-KV decode with an int8 K cache and an fp16 V cache: the attn_decode row's
  * "fp16 V" variant ("Attention kernels" table).  Same operation, split plan and outputs
  * as sl8_attn_int8_decode_splitkv, with O = sum_t p_t * v[t] (V has no scale):

@@ -269,3 +269,54 @@ def test_decode_f16v_rejects_d256():
     seq = torch.tensor([10], dtype=torch.int32, device=DEV)
     with pytest.raises(sl8.SL8Error):
         sl8.attn_int8_decode_splitkv_f16v(q, kc, ks, v, seq)
+
+
+# ---------------------------------------------------------------- speculative verify (tree mask)
+
+VERIFY = [
+    # wid, B, T, Hq, Hkv, d, lengths (draft tokens included), lmax
+    (3501, 3, 4, 8, 2, 128, [300, 4, 1000], 1000),
+    (3502, 2, 7, 4, 4, 64, [513, 160], 600),
+    (3503, 2, 16, 8, 1, 256, [200, 2000], 2000),
+    (3504, 4, 1, 8, 2, 128, [1, 17, 640, 641], 700),
+]
+
+
+@pytest.mark.parametrize("case", VERIFY, ids=[f"w{c[0]}_T{c[2]}_d{c[5]}" for c in VERIFY])
+def test_decode_verify(case):
+    wid, B, T, Hq, Hkv, d, lens, lmax = case
+    w = W.custom(wid, kind="decode", B=B, Hq=Hq, Hkv=Hkv, d=d, dtype="bf16", extra={"lengths": lens})
+    lens_np, g, gs, o, os_ = build_cache(w, lmax)
+    rng = np.random.default_rng(wid)
+    q = torch.from_numpy(rng.standard_normal((B, T, Hq, d)).astype(np.float32)).to(torch.bfloat16)
+    # row 0: a chain; other rows: random trees (every query sees itself and some earlier drafts)
+    mask = np.zeros((B, T), np.int64)
+    for b in range(B):
+        for t in range(T):
+            if b == 0:
+                mask[b, t] = (1 << (t + 1)) - 1
+            else:
+                anc = rng.integers(0, 2, size=t) if t else np.zeros(0, np.int64)
+                mask[b, t] = (1 << t) | int(sum(int(x) << i for i, x in enumerate(anc)))
+    mask32 = torch.from_numpy(mask.astype(np.uint32).view(np.int32)).to(DEV)
+    qd = q.to(DEV)
+    seq = torch.from_numpy(lens_np.astype(np.int32)).to(DEV)
+    ref = oracle.attn_decode_verify(q.float().numpy(), o["k"], os_["k"], o["v"], os_["v"], lens_np, mask)
+    for ns in (0, 3):
+        o32, lse = sl8.attn_int8_decode_verify(qd, g["k"], gs["k"], g["v"], gs["v"], seq, mask32, num_splits=ns,
+                                               out_dtype=torch.float32, return_lse=True)
+        ob = sl8.attn_int8_decode_verify(qd, g["k"], gs["k"], g["v"], gs["v"], seq, mask32, num_splits=ns)
+        torch.cuda.synchronize()
+        check_f32(to_np32(o32), ref["out"], f"w{wid} verify splits={ns} f32")
+        check_half(ob, ref["out"], f"w{wid} verify splits={ns} bf16")
+        np.testing.assert_allclose(to_np32(lse), ref["lse"], rtol=0, atol=1e-4)
+    if T == 1:
+        # one draft that sees itself is plain decode.  Not bit for bit: the masked tail unit
+        # may contract its arithmetic differently, and a last-bit change of p can move P'
+        # by one fp16 ulp (2^-11 relative)
+        plain = sl8.attn_int8_decode(qd[:, 0].contiguous(), g["k"], gs["k"], g["v"], gs["v"], seq,
+                                     out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        np.testing.assert_allclose(to_np32(o32[:, 0]), to_np32(plain), rtol=0, atol=5e-4)
+    st, site = sl8.last_device_status()
+    assert st == sl8.SL8_OK, (st, site)

@@ -75,6 +75,8 @@ _SIGNATURES = {
     "sl8_attn_decode_split_size": (_I32, [_I32, _I32, _I32, _I32, _I32]),
     "sl8_attn_int8_decode_splitkv": (_INT, [_P, _INT, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P,
                                             _P, _P]),
+    "sl8_attn_int8_decode_verify": (_INT, [_P, _INT, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
+                                           _I32, _P, _P, _P, _INT, _P, _P]),
     "sl8_attn_int8_decode_splitkv_f16v": (_INT, [_P, _INT, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P,
                                                  _P, _P]),
     "sl8_attn_int8_paged_decode_splitkv": (_INT, [_P, _INT, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _I32, _I32,
@@ -327,6 +329,31 @@ def attn_int8_decode(q, k_cache, k_scale, v_cache, v_scale, seqlens, num_splits=
     o_p, l_p = attn_int8_decode_splitkv(q, k_cache, k_scale, v_cache, v_scale, seqlens, num_splits, o_partial,
                                         lse_partial)
     return attn_decode_combine(o_p, l_p, seqlens, k_cache.shape[2], out_dtype or q.dtype, return_lse, out)
+
+
+def attn_int8_decode_verify(q, k_cache, k_scale, v_cache, v_scale, seqlens, tree_mask, num_splits=0, out_dtype=None,
+                            return_lse=False, o_partial=None, lse_partial=None, out=None):
+    """Speculative-decode verification: q [B, T, Hq, d] draft queries, tree_mask [B, T] int32
+    (bit u of row (b, t): query t sees draft token u, which sits at position L_b - T + u of
+    the cache).  Returns out [B, T, Hq, d] (and the LSE [B, T, Hq] with return_lse)."""
+    _need_cuda(q, k_cache, k_scale, v_cache, v_scale, seqlens, tree_mask)
+    if tree_mask.dtype != torch.int32:
+        raise TypeError("tree_mask must be int32 (bit u: draft token u is visible)")
+    B, T, Hq, d = q.shape
+    _, Hkv, Lmax, _ = k_cache.shape
+    S = decode_num_splits(B * T, Hkv, Lmax, d, num_splits)
+    if o_partial is None:
+        o_partial = torch.empty((B * T, Hq, max(S, 1), d), dtype=torch.float32, device=q.device)
+    if lse_partial is None:
+        lse_partial = torch.empty((B * T, Hq, max(S, 1)), dtype=torch.float32, device=q.device)
+    if out is None:
+        out = torch.empty((B, T, Hq, d), dtype=out_dtype or q.dtype, device=q.device)
+    lse = torch.empty((B, T, Hq), dtype=torch.float32, device=q.device) if return_lse else None
+    _check(lib().sl8_attn_int8_decode_verify(_ptr(q), _dt(q), _ptr(k_cache), _ptr(k_scale), _ptr(v_cache),
+                                             _ptr(v_scale), _ptr(seqlens), _ptr(tree_mask), T, B, Hq, Hkv, Lmax, d,
+                                             num_splits, _ptr(o_partial), _ptr(lse_partial), _ptr(out), _dt(out),
+                                             _ptr(lse), _stream(q.device)), "sl8_attn_int8_decode_verify")
+    return (out, lse) if return_lse else out
 
 
 def attn_int8_decode_splitkv_f16v(q, k_cache, k_scale, v_cache, seqlens, num_splits=0, o_partial=None,

@@ -542,7 +542,7 @@ static int decode_launch(const void* q, int q_dtype, const int8_t* k_cache, cons
                          const float* v_scale, const int32_t* seqlens, int32_t B, int32_t Hq, int32_t Hkv, int32_t Lmax,
                          int32_t d, int32_t num_splits, float* o_partial, float* lse_partial, int32_t* logits,
                          int8_t* q_codes, float* q_scales, void* stream, const Paging* pg = nullptr,
-                         bool v16 = false) {
+                         bool v16 = false, int32_t verify_T = 0, const uint32_t* tree_mask = nullptr) {
   int rc = decode_validate(q, q_dtype, k_cache, k_scale, v_cache, v_scale, seqlens, B, Hq, Hkv, Lmax, d, pg, v16);
   if (rc != SL8_OK) return rc;
   SL8_CHECK(o_partial && lse_partial && num_splits >= 0, SL8_ERR_INVALID_ARG);
@@ -555,6 +555,8 @@ static int decode_launch(const void* q, int q_dtype, const int8_t* k_cache, cons
   a.v_cache = static_cast<const int8_t*>(v_cache);
   a.v_scale = v16 ? nullptr : v_scale;
   a.v16 = v16;
+  a.verify_T = verify_T;
+  a.tree_mask = tree_mask;
   a.seqlens = seqlens;
   a.B = B;
   a.Hq = Hq;
@@ -576,6 +578,28 @@ static int decode_launch(const void* q, int q_dtype, const int8_t* k_cache, cons
     a.num_pages = pg->num_pages;
   }
   SL8_LAUNCH(launch_decode_split(a, static_cast<cudaStream_t>(stream)));
+  return SL8_OK;
+}
+
+int sl8_attn_int8_decode_verify(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale,
+                                 const int8_t* v_cache, const float* v_scale, const int32_t* seqlens,
+                                 const uint32_t* tree_mask, int32_t T, int32_t B, int32_t Hq, int32_t Hkv, int32_t Lmax,
+                                 int32_t d, int32_t num_splits, float* o_partial, float* lse_partial, void* out,
+                                 int out_dtype, float* lse_out, void* stream) {
+  SL8_CHECK(T >= 1 && T <= 32 && B >= 0, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(tree_mask && out, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(out_dtype == SL8_F16 || out_dtype == SL8_BF16 || out_dtype == SL8_F32, SL8_ERR_INVALID_ARG);
+  const int64_t bv = static_cast<int64_t>(B) * T;
+  SL8_CHECK(bv <= 65535, SL8_ERR_UNSUPPORTED);
+  if (B == 0 || Lmax == 0) return SL8_OK;
+  // the T queries of sequence b are the virtual sequences b * T + t (q [B][T][Hq][d])
+  const int32_t vb = static_cast<int32_t>(bv);
+  int rc = decode_launch(q, q_dtype, k_cache, k_scale, v_cache, v_scale, seqlens, vb, Hq, Hkv, Lmax, d, num_splits,
+                         o_partial, lse_partial, nullptr, nullptr, nullptr, stream, nullptr, false, T, tree_mask);
+  if (rc != SL8_OK) return rc;
+  const int32_t S = sl8_attn_decode_num_splits(vb, Hkv, Lmax, d, num_splits);
+  SL8_LAUNCH(launch_decode_combine(o_partial, lse_partial, seqlens, vb, Hq, d, S, split_size_for(Lmax, S, d), out,
+                                   static_cast<sl8_dtype>(out_dtype), lse_out, static_cast<cudaStream_t>(stream), T));
   return SL8_OK;
 }
 

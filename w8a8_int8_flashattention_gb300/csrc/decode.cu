@@ -223,8 +223,11 @@ __device__ __forceinline__ float load_q_elem(const void* base, sl8_dtype dt, int
 // longest first; empty splits are handled up front and never listed.  Above
 // kSchedMaxB the list is every slot in split-major order (empty ones are skipped).
 
+// The cache sequence of (virtual) sequence b: b itself, or b / verify_T when verifying.
+__device__ __forceinline__ int cache_seq(const DecodeArgs& a, int b) { return a.verify_T ? b / a.verify_T : b; }
+
 __device__ __forceinline__ int clamp_len(const DecodeArgs& a, int b, DeviceStatus* st, bool report) {
-  int L = a.seqlens[b];
+  int L = a.seqlens[cache_seq(a, b)];
   if (L < 0 || L > a.Lmax) {
     if (report) record_status(st, kStatusBadArg, 700);
     L = L < 0 ? 0 : a.Lmax;
@@ -306,7 +309,7 @@ __device__ __forceinline__ bool slot_at(const DecodeArgs& a, const Sched* sc, bo
     const int64_t r = j - s.split * per;
     s.b = static_cast<int>(r / a.Hkv);
     s.hkv = static_cast<int>(r - static_cast<int64_t>(s.b) * a.Hkv);
-    int L = a.seqlens[s.b];
+    int L = a.seqlens[cache_seq(a, s.b)];
     L = L < 0 ? 0 : (L > a.Lmax ? a.Lmax : L);
     s.t0 = s.split * a.split_size;
     s.t1 = min(s.t0 + a.split_size, L);
@@ -473,7 +476,7 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
     while (ok && has_cur) {
       const bool has_nxt = next_entry(nxt);
       if (!ok || !announce(nxt, n + 1)) break;
-      const int64_t row0 = (static_cast<int64_t>(cur.b) * a.Hkv + cur.hkv) * a.Lmax;
+      const int64_t row0 = (static_cast<int64_t>(cache_seq(a, cur.b)) * a.Hkv + cur.hkv) * a.Lmax;
       for (int c0 = cur.t0; c0 < cur.t1 && ok; c0 += C::kChunk, ++k) {
         const int nt = min(C::kChunk, cur.t1 - c0);
         const uint32_t stg = k % kStages;
@@ -804,6 +807,13 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
     float o[D / 16][4], osum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int j = 0; j < D / 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.0f;
+    // verify: the slot's draft tokens start at v_tail; v_mask says which it sees
+    int v_tail = 0;
+    uint32_t v_mask = 0;
+    if (a.verify_T) {
+      v_tail = (balanced ? sc->len[s.b] : clamp_len(a, s.b, st, false)) - a.verify_T;
+      v_mask = a.tree_mask[s.b];
+    }
     for (int c0 = s.t0; c0 < s.t1 && ok; c0 += C::kChunk, ++k) {
       const int ntok = min(C::kChunk, s.t1 - c0);
       const uint32_t stg = k % kStages;
@@ -838,7 +848,13 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
         const float d00 = fmaf(s0[0] + s1[0], k2p24, offa), d01 = fmaf(s0[1] + s1[1], k2p24, offb);
         const float d10 = fmaf(s0[2] + s1[2], k2p24, offa), d11 = fmaf(s0[3] + s1[3], k2p24, offb);
         const int rA = u0 + pi, rB = rA + 8;
-        const bool vA = kFull || pi < nv, vB = kFull || pi + 8 < nv;
+        bool vA = kFull || pi < nv, vB = kFull || pi + 8 < nv;
+        if (!kFull && a.verify_T) {
+          // verify: the draft tokens from v_tail on are visible as the slot's mask says
+          const int tA = c0 + rA, tB = c0 + rB;
+          vA = vA && (tA < v_tail || ((v_mask >> (tA - v_tail)) & 1u));
+          vB = vB && (tB < v_tail || ((v_mask >> (tB - v_tail)) & 1u));
+        }
         if (a.logits) {
           int32_t* lg = a.logits + c0;
           if (2 * t < G) {
@@ -895,7 +911,10 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
           osum[1] *= fb;
           osum[3] *= fb;
         }
-        const float pa0 = ex2(xa0 - m_a), pa1 = ex2(xa1 - m_b), pb0 = ex2(xb0 - m_a), pb1 = ex2(xb1 - m_b);
+        // a column with no visible token yet (verify masks can hide a warp's whole first
+        // unit) keeps m = -inf: its p must be 0, not exp(-inf - -inf)
+        const float ra = m_a == -INFINITY ? 0.0f : m_a, rb = m_b == -INFINITY ? 0.0f : m_b;
+        const float pa0 = ex2(xa0 - ra), pa1 = ex2(xa1 - rb), pb0 = ex2(xb0 - ra), pb1 = ex2(xb1 - rb);
         l_a += pa0 + pb0;
         l_b += pa1 + pb1;
         const float wA = vsA * inv, wB = vsB * inv;
@@ -954,7 +973,7 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
         }
         if constexpr (!kV16) mma_f16(osum, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, pb0r, pb1r);
       };
-      if (nv >= kUnit) {
+      if (nv >= kUnit && !(a.verify_T && c0 + u0 + kUnit > v_tail)) {
         unit(std::true_type{});
       } else if (nv > 0) {
         unit(std::false_type{});
@@ -1022,12 +1041,13 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
 template <int D>
 __global__ void decode_combine_kernel(const float* __restrict__ o_partial, const float* __restrict__ lse_partial,
                                       const int32_t* __restrict__ seqlens, int32_t B, int32_t Hq, int32_t num_splits,
-                                      int32_t split_size, void* out, sl8_dtype out_dtype, float* lse_out) {
+                                      int32_t split_size, void* out, sl8_dtype out_dtype, float* lse_out,
+                                      int32_t seq_div) {
   const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   if (row >= B * Hq) return;
   const int b = row / Hq;
-  const int L = max(0, seqlens[b]);
+  const int L = max(0, seqlens[b / seq_div]);
   const float* lse = lse_partial + static_cast<int64_t>(row) * num_splits;
   const float* op = o_partial + static_cast<int64_t>(row) * num_splits * D + lane * (D / 32);
   constexpr int E = D / 32, K = 8;
@@ -1150,14 +1170,14 @@ cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t s) {
 
 cudaError_t launch_decode_combine(const float* o_partial, const float* lse_partial, const int32_t* seqlens, int32_t B,
                                   int32_t Hq, int32_t d, int32_t num_splits, int32_t split_size, void* out,
-                                  sl8_dtype out_dtype, float* lse_out, cudaStream_t s) {
+                                  sl8_dtype out_dtype, float* lse_out, cudaStream_t s, int32_t seq_div) {
   TraceScope tr("decode_combine", s);
   const int rows = B * Hq;
   const int grid = (rows + 7) / 8;
   switch (d) {
-    case 64: decode_combine_kernel<64><<<grid, 256, 0, s>>>(o_partial, lse_partial, seqlens, B, Hq, num_splits, split_size, out, out_dtype, lse_out); break;
-    case 128: decode_combine_kernel<128><<<grid, 256, 0, s>>>(o_partial, lse_partial, seqlens, B, Hq, num_splits, split_size, out, out_dtype, lse_out); break;
-    case 256: decode_combine_kernel<256><<<grid, 256, 0, s>>>(o_partial, lse_partial, seqlens, B, Hq, num_splits, split_size, out, out_dtype, lse_out); break;
+    case 64: decode_combine_kernel<64><<<grid, 256, 0, s>>>(o_partial, lse_partial, seqlens, B, Hq, num_splits, split_size, out, out_dtype, lse_out, seq_div); break;
+    case 128: decode_combine_kernel<128><<<grid, 256, 0, s>>>(o_partial, lse_partial, seqlens, B, Hq, num_splits, split_size, out, out_dtype, lse_out, seq_div); break;
+    case 256: decode_combine_kernel<256><<<grid, 256, 0, s>>>(o_partial, lse_partial, seqlens, B, Hq, num_splits, split_size, out, out_dtype, lse_out, seq_div); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

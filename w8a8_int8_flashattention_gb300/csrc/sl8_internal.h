@@ -168,11 +168,18 @@ struct DecodeArgs {
   // fp16 V cache (v_cache holds [B][Hkv][Lmax][d] fp16 values, v_scale unused); d <= 128,
   // contiguous caches only
   bool v16;
+  // speculative verify (verify_T > 0): B counts B_cache * verify_T virtual sequences
+  // v = b * verify_T + t (query t of cache sequence b, q [B][Hq][d] = [B_cache][T][Hq][d]);
+  // seqlens and the caches are indexed by b = v / verify_T; the last verify_T positions of
+  // b are the draft tokens, of which v sees u iff bit u of tree_mask[v] is set
+  int32_t verify_T;
+  const uint32_t* tree_mask;
 };
 cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_combine(const float* o_partial, const float* lse_partial, const int32_t* seqlens,
                                   int32_t B, int32_t Hq, int32_t d, int32_t num_splits, int32_t split_size,
-                                  void* out, sl8_dtype out_dtype, float* lse_out, cudaStream_t s);
+                                  void* out, sl8_dtype out_dtype, float* lse_out, cudaStream_t s,
+                                  int32_t seq_div = 1);
 cudaError_t launch_timeout_selftest(uint64_t limit_ns, cudaStream_t s);
 
 // tokens per stage of the decode kernel for head dim d
