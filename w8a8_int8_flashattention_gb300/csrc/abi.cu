@@ -7,6 +7,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <map>
 #include <string>
 #include <vector>
 
@@ -56,6 +57,18 @@ int num_sms() {
 }
 
 uint64_t spin_limit_ns() { return g_spin_limit_ns.load(std::memory_order_relaxed); }
+
+cudaError_t ensure_smem(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> done;
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lk(mu);
+  int& have = done[{kernel, dev}];
+  if (have >= bytes) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) have = bytes;
+  return e;
+}
 
 // ---------------------------------------------------------------- tensor maps
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

@@ -1114,7 +1114,7 @@ template <int D, bool kV16>
 cudaError_t launch_split_d(const DecodeArgs& a, cudaStream_t s) {
   using C = DCfg<D, kV16>;
   auto kern = decode_split_kernel<D, kV16>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), C::kBytes);
   if (e != cudaSuccess) return e;
   // each cache as a 2-D [B * Hkv * Lmax rows][d bytes] tensor, loaded in boxes of
   // C::kChunk rows x kBW bytes; a paged cache as [num_pages * Hkv * page_size rows][d],

@@ -1053,7 +1053,7 @@ static cudaError_t launch_pair(const PrefillArgs& a, cudaStream_t s) {
   CUtensorMap mq, mk, mv;
   if (!make_maps<C::BN>(a, D, &mq, &mk, &mv)) return cudaErrorInvalidValue;
   auto kern = prefill_pair_kernel<D, kLogits>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int64_t max_items = a.max_pairs * a.Hq;
   const int grid = static_cast<int>(max_items < num_sms() ? max_items : num_sms());
@@ -1069,7 +1069,7 @@ static cudaError_t launch_single(const PrefillArgs& a, cudaStream_t s) {
   CUtensorMap mq, mk, mv;
   if (!make_maps<C::BN>(a, D, &mq, &mk, &mv)) return cudaErrorInvalidValue;
   auto kern = prefill_single_kernel<D, kLogits>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int64_t max_items = a.max_pairs * a.Hq;
   const int grid = static_cast<int>(max_items < num_sms() ? max_items : num_sms());

@@ -612,7 +612,7 @@ cudaError_t launch_kv_partials(const void* k, sl8_dtype dt, const void* v, bool 
   const size_t smem = static_cast<size_t>(kMeanChunk) * d * es * (v_partials ? 2 : 1);
   const dim3 grid(max_chunks, Hkv, nseq), block((d + 31) / 32 * 32);
   auto go = [&](auto kern) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, grid, block, smem, s, k, v, varlen, Hkv, N, d, len, tok0, k_partials, v_partials,
                       max_chunks, spin_limit_ns(), device_status_ptr());

@@ -45,6 +45,10 @@ PrefillWorkspace plan_prefill_workspace(int32_t nseq, int32_t Hq, int32_t Hkv, i
 DeviceStatus* device_status_ptr();
 uint64_t spin_limit_ns();
 int num_sms();
+// Raise a kernel's dynamic shared memory limit to at least `bytes` on the current device.
+// Each (kernel, device) is raised once, so the launches that follow (including those
+// recorded into a CUDA graph by stream capture) make no attribute call.
+cudaError_t ensure_smem(const void* kernel, int bytes);
 
 // ---- tracing (CUDA events around each launch when enabled)
 struct TraceScope {
