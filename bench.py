@@ -11,7 +11,8 @@ the decode KV GB/s sits in `decode`, and `paged_decode` repeats the decode over 
 paged k8v8 cache (64-token pages in a seeded random order) in a loop of its own after
 the timed steps, `decode_f16v` the decode with an fp16 V cache (int8 K), and
 `prefill_chunk` the prefill's last 1024 positions as a query chunk (chunked prefill,
-bottom-right causal).  Inputs are resident in HBM when the timed
+bottom-right causal), and `decode_verify` the decode with 4 chained draft queries per
+sequence (speculative verify).  Inputs are resident in HBM when the timed
 region starts; L2 is flushed before every step, outside the timed events (a 256 MB
 write, then a read of that buffer, so no dirty lines of the flush remain).  `e2e` repeats the prefill through the public API with pinned host
 inputs copied in and the output copied back every step.
@@ -326,6 +327,9 @@ def run_ours(args, world, rank, local):
                                                            flush_sink, args.steps, args.warmup, world)
     pg_gbs = dbytes * world / (pg_ms * 1e-3) / 1e9
     pg_split_gbs = dbytes / (pg_split_ms * 1e-3) / 1e9
+    # ---- speculative verify: VERIFY_T chained drafts per sequence
+    vf_ms, vf_steps = measure_verify(sl8, wd, kc, ks, vc, vs, lens, seq, stream, flush, flush_sink, args.steps,
+                                     args.warmup, world)
     # ---- the prefill's last positions as a query chunk
     ch_ms, ch_attn_ms, ch_steps = measure_chunk(sl8, wp, qd, kd, vd, stream, flush, flush_sink, args.steps,
                                                 args.warmup, world)
@@ -391,6 +395,11 @@ def run_ours(args, world, rank, local):
                          "roofline": {"bound": "hbm", "achieved": pg_split_gbs, "peak": peaks["hbm_gbs"],
                                       "unit": "GB/s", "frac": pg_split_gbs / peaks["hbm_gbs"], "traffic": None,
                                       "kernel": "decode_split (paged)", "peak_source": peaks["source"]}},
+        "decode_verify": {"value": dbytes * world / (vf_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": vf_ms,
+                          "steps": vf_steps, "draft_tokens": VERIFY_T,
+                          "config": f"the decode workload with {VERIFY_T} chained draft queries per sequence "
+                                    "(speculative verify), split kernel + combine; GB/s counts the cache once, "
+                                    f"the kernel reads it once per draft query ({VERIFY_T} times)"},
         "prefill_chunk": {"value": ch_ops * world / (ch_ms * 1e-3) / 1e12, "unit": "TOPS", "ms": ch_ms,
                           "steps": ch_steps, "ops": ch_ops,
                           "config": f"the prefill workload's last {CHUNK_Q} positions as a query chunk against "
@@ -544,6 +553,46 @@ def measure_chunk(sl8, wp, qd, kd, vd, stream, flush, flush_sink, steps, warmup,
     ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in events) / n, world)
     c, attn_ms = trace.get("prefill_attn", (0, 0.0))
     return ms, (attn_ms / c if c else float("nan")), n
+
+
+VERIFY_T = 4   # draft tokens per sequence of the verify line
+
+
+def measure_verify(sl8, wd, kc, ks, vc, vs, lens, seq, stream, flush, flush_sink, steps, warmup, world):
+    """Speculative verify on the decode workload: VERIFY_T chained draft queries per
+    sequence (the cache's last VERIFY_T tokens are the drafts), split kernel plus combine,
+    L2 flushed before each step."""
+    import torch
+    T = VERIFY_T
+    g = torch.Generator(device="cpu").manual_seed(0x5EED0000 + 7)
+    q = torch.randn((wd.B, T, wd.Hq, wd.d), generator=g).to(torch.bfloat16).to(kc.device)
+    mask = torch.tensor([[(1 << (t + 1)) - 1 for t in range(T)]] * wd.B, dtype=torch.int32, device=kc.device)
+    S = int(sl8.lib().sl8_attn_decode_verify_num_splits(wd.B, T, wd.Hq, wd.Hkv, wd.lmax, wd.d, 0))
+    o_part = torch.empty((wd.B * T, wd.Hq, S, wd.d), dtype=torch.float32, device=kc.device)
+    l_part = torch.empty((wd.B * T, wd.Hq, S), dtype=torch.float32, device=kc.device)
+    out = torch.empty((wd.B, T, wd.Hq, wd.d), dtype=torch.bfloat16, device=kc.device)
+
+    def step(ev=None):
+        flush.zero_()
+        flush_sink.copy_(flush.view(torch.int64).sum())
+        if ev:
+            ev[0].record(stream)
+        sl8.attn_int8_decode_verify(q, kc, ks, vc, vs, seq, mask, o_partial=o_part, lse_partial=l_part, out=out)
+        if ev:
+            ev[1].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(kc.device)
+    n = max(3, min(steps, 50))
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for i in range(n):
+        step(events[i])
+    torch.cuda.synchronize(kc.device)
+    st, site = sl8.last_device_status(kc.device)
+    if st != sl8.SL8_OK:
+        raise RuntimeError(f"device status {st} at {site} during the verify")
+    return max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in events) / n, world), n
 
 
 def load_traffic():

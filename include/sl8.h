@@ -203,11 +203,14 @@ SL8_API int sl8_attn_int8_decode_splitkv(const void* q, int q_dtype, const int8_
  *              draft token u (position L_b - T + u, if >= 0) iff bit u is set.
  *   T          1 .. 32 draft tokens per sequence; B * T <= 65535.
  *   o_partial, lse_partial  scratch, [B * T][Hq][S][d] and [B * T][Hq][S] fp32 with
- *              S = sl8_attn_decode_num_splits(B * T, Hkv, Lmax, d, num_splits).
+ *              S = sl8_attn_decode_verify_num_splits(B, T, Hq, Hkv, Lmax, d, num_splits).
  *   out        device, [B][T][Hq][d] of out_dtype (F16, BF16 or F32); lse_out nullable
  *              [B][T][Hq].
- * Runs the split kernel (one pass over sequence b's cache per draft query) and the combine.
+ * Runs the split kernel and the combine.  A work slot takes min(T, 8 / (Hq / Hkv)) draft
+ * queries beside their query heads, so sequence b's cache is read ceil(T / that) times.
  */
+SL8_API int32_t sl8_attn_decode_verify_num_splits(int32_t B, int32_t T, int32_t Hq, int32_t Hkv, int32_t Lmax,
+                                                  int32_t d, int32_t num_splits);
 SL8_API int sl8_attn_int8_decode_verify(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale,
                                         const int8_t* v_cache, const float* v_scale, const int32_t* seqlens,
                                         const uint32_t* tree_mask, int32_t T, int32_t B, int32_t Hq, int32_t Hkv,

@@ -75,6 +75,7 @@ _SIGNATURES = {
     "sl8_attn_decode_split_size": (_I32, [_I32, _I32, _I32, _I32, _I32]),
     "sl8_attn_int8_decode_splitkv": (_INT, [_P, _INT, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P,
                                             _P, _P]),
+    "sl8_attn_decode_verify_num_splits": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _I32]),
     "sl8_attn_int8_decode_verify": (_INT, [_P, _INT, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                            _I32, _P, _P, _P, _INT, _P, _P]),
     "sl8_attn_int8_decode_splitkv_f16v": (_INT, [_P, _INT, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P,
@@ -341,7 +342,7 @@ def attn_int8_decode_verify(q, k_cache, k_scale, v_cache, v_scale, seqlens, tree
         raise TypeError("tree_mask must be int32 (bit u: draft token u is visible)")
     B, T, Hq, d = q.shape
     _, Hkv, Lmax, _ = k_cache.shape
-    S = decode_num_splits(B * T, Hkv, Lmax, d, num_splits)
+    S = int(lib().sl8_attn_decode_verify_num_splits(B, T, Hq, Hkv, Lmax, d, num_splits))
     if o_partial is None:
         o_partial = torch.empty((B * T, Hq, max(S, 1), d), dtype=torch.float32, device=q.device)
     if lse_partial is None:

@@ -555,7 +555,8 @@ static int decode_launch(const void* q, int q_dtype, const int8_t* k_cache, cons
                          const float* v_scale, const int32_t* seqlens, int32_t B, int32_t Hq, int32_t Hkv, int32_t Lmax,
                          int32_t d, int32_t num_splits, float* o_partial, float* lse_partial, int32_t* logits,
                          int8_t* q_codes, float* q_scales, void* stream, const Paging* pg = nullptr,
-                         bool v16 = false, int32_t verify_T = 0, const uint32_t* tree_mask = nullptr) {
+                         bool v16 = false, int32_t verify_T = 0, const uint32_t* tree_mask = nullptr,
+                         int32_t verify_dps = 1) {
   int rc = decode_validate(q, q_dtype, k_cache, k_scale, v_cache, v_scale, seqlens, B, Hq, Hkv, Lmax, d, pg, v16);
   if (rc != SL8_OK) return rc;
   SL8_CHECK(o_partial && lse_partial && num_splits >= 0, SL8_ERR_INVALID_ARG);
@@ -570,6 +571,8 @@ static int decode_launch(const void* q, int q_dtype, const int8_t* k_cache, cons
   a.v16 = v16;
   a.verify_T = verify_T;
   a.tree_mask = tree_mask;
+  a.verify_dps = verify_dps;
+  a.verify_ng = verify_T ? (verify_T + verify_dps - 1) / verify_dps : 1;
   a.seqlens = seqlens;
   a.B = B;
   a.Hq = Hq;
@@ -594,6 +597,20 @@ static int decode_launch(const void* q, int q_dtype, const int8_t* k_cache, cons
   return SL8_OK;
 }
 
+// Drafts per slot of the verify: as many as fit the 8 query columns beside their G heads.
+static int32_t verify_dps(int32_t T, int32_t Hq, int32_t Hkv) {
+  const int32_t G = Hkv > 0 ? Hq / Hkv : 1;
+  const int32_t fit = G > 0 ? 8 / G : 1;
+  return std::max<int32_t>(1, std::min<int32_t>(T, fit));
+}
+
+int32_t sl8_attn_decode_verify_num_splits(int32_t B, int32_t T, int32_t Hq, int32_t Hkv, int32_t Lmax, int32_t d,
+                                          int32_t num_splits) {
+  if (T < 1 || T > 32 || Hkv <= 0 || Hq % Hkv) return 0;
+  const int32_t dps = verify_dps(T, Hq, Hkv);
+  return sl8_attn_decode_num_splits(B * ((T + dps - 1) / dps), Hkv, Lmax, d, num_splits);
+}
+
 int sl8_attn_int8_decode_verify(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale,
                                  const int8_t* v_cache, const float* v_scale, const int32_t* seqlens,
                                  const uint32_t* tree_mask, int32_t T, int32_t B, int32_t Hq, int32_t Hkv, int32_t Lmax,
@@ -602,16 +619,19 @@ int sl8_attn_int8_decode_verify(const void* q, int q_dtype, const int8_t* k_cach
   SL8_CHECK(T >= 1 && T <= 32 && B >= 0, SL8_ERR_INVALID_ARG);
   SL8_CHECK(tree_mask && out, SL8_ERR_INVALID_ARG);
   SL8_CHECK(out_dtype == SL8_F16 || out_dtype == SL8_BF16 || out_dtype == SL8_F32, SL8_ERR_INVALID_ARG);
-  const int64_t bv = static_cast<int64_t>(B) * T;
-  SL8_CHECK(bv <= 65535, SL8_ERR_UNSUPPORTED);
+  SL8_CHECK(Hkv > 0 && Hq % Hkv == 0, SL8_ERR_INVALID_ARG);
+  // the drafts of sequence b go dps at a time into one slot's query columns: virtual
+  // sequences b * ng + group (q [B][T][Hq][d])
+  const int32_t dps = verify_dps(T, Hq, Hkv), ng = (T + dps - 1) / dps;
+  const int64_t bv = static_cast<int64_t>(B) * ng;
+  SL8_CHECK(bv <= 65535 && static_cast<int64_t>(B) * T <= 65535, SL8_ERR_UNSUPPORTED);
   if (B == 0 || Lmax == 0) return SL8_OK;
-  // the T queries of sequence b are the virtual sequences b * T + t (q [B][T][Hq][d])
-  const int32_t vb = static_cast<int32_t>(bv);
-  int rc = decode_launch(q, q_dtype, k_cache, k_scale, v_cache, v_scale, seqlens, vb, Hq, Hkv, Lmax, d, num_splits,
-                         o_partial, lse_partial, nullptr, nullptr, nullptr, stream, nullptr, false, T, tree_mask);
+  int rc = decode_launch(q, q_dtype, k_cache, k_scale, v_cache, v_scale, seqlens, static_cast<int32_t>(bv), Hq, Hkv,
+                         Lmax, d, num_splits, o_partial, lse_partial, nullptr, nullptr, nullptr, stream, nullptr,
+                         false, T, tree_mask, dps);
   if (rc != SL8_OK) return rc;
-  const int32_t S = sl8_attn_decode_num_splits(vb, Hkv, Lmax, d, num_splits);
-  SL8_LAUNCH(launch_decode_combine(o_partial, lse_partial, seqlens, vb, Hq, d, S, split_size_for(Lmax, S, d), out,
+  const int32_t S = sl8_attn_decode_num_splits(static_cast<int32_t>(bv), Hkv, Lmax, d, num_splits);
+  SL8_LAUNCH(launch_decode_combine(o_partial, lse_partial, seqlens, B * T, Hq, d, S, split_size_for(Lmax, S, d), out,
                                    static_cast<sl8_dtype>(out_dtype), lse_out, static_cast<cudaStream_t>(stream), T));
   return SL8_OK;
 }

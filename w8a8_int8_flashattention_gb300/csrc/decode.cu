@@ -223,8 +223,22 @@ __device__ __forceinline__ float load_q_elem(const void* base, sl8_dtype dt, int
 // longest first; empty splits are handled up front and never listed.  Above
 // kSchedMaxB the list is every slot in split-major order (empty ones are skipped).
 
-// The cache sequence of (virtual) sequence b: b itself, or b / verify_T when verifying.
-__device__ __forceinline__ int cache_seq(const DecodeArgs& a, int b) { return a.verify_T ? b / a.verify_T : b; }
+// The cache sequence of (virtual) sequence b: b itself, or b / verify_ng when verifying.
+__device__ __forceinline__ int cache_seq(const DecodeArgs& a, int b) { return a.verify_T ? b / a.verify_ng : b; }
+
+// Query column c (< 8) of a slot of sequence v, kv head hkv: its (b, hq) row of the
+// partials and whether it holds a query (the G heads, or verify_dps drafts x G heads;
+// drafts past verify_T are dead columns).
+template <bool kVerify>
+__device__ __forceinline__ int64_t col_row(const DecodeArgs& a, int v, int hkv, int c, int G, bool& live) {
+  if constexpr (!kVerify) {
+    live = c < G;
+    return static_cast<int64_t>(v) * a.Hq + hkv * G + c;
+  }
+  const int t = (v % a.verify_ng) * a.verify_dps + c / G;
+  live = c < a.verify_dps * G && t < a.verify_T;
+  return (static_cast<int64_t>(v / a.verify_ng) * a.verify_T + t) * a.Hq + hkv * G + c % G;
+}
 
 __device__ __forceinline__ int clamp_len(const DecodeArgs& a, int b, DeviceStatus* st, bool report) {
   int L = a.seqlens[cache_seq(a, b)];
@@ -349,7 +363,9 @@ struct CacheMaps {
   CUtensorMap k[kPageBoxes], v[kPageBoxes];
 };
 
-template <int D, bool kV16>
+// kVerify: the speculative-verify form (a.verify_T > 0), built apart so that plain decode
+// carries none of its per-column masks.
+template <int D, bool kV16, bool kVerify>
 __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
     decode_split_kernel(const DecodeArgs a, const __grid_constant__ CacheMaps maps, uint32_t ticket,
                         DeviceStatus* st, uint64_t limit_ns) {
@@ -372,6 +388,7 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const int G = a.Hq / a.Hkv;
+  const int GC = kVerify ? a.verify_dps * G : G;  // query columns of a slot
   const bool balanced = a.B <= kSchedMaxB;
   const int q_elem = a.q_dtype == SL8_F32 ? 4 : 2;
   // scales ride the bulk copies when every stage's range is 16-byte aligned
@@ -385,8 +402,8 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
     }
     for (int i = 0; i < kQSlots; ++i) {
       mbar_init(&raw_full[i], 1);
-      mbar_init(&raw_empty[i], G);  // the warps quantising the rows
-      mbar_init(&qc_full[i], G);
+      mbar_init(&raw_empty[i], GC);  // the warps quantising the rows
+      mbar_init(&qc_full[i], GC);
       mbar_init(&qc_empty[i], C::kNW);
     }
     mbar_init(red_full, C::kNW);
@@ -459,11 +476,22 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
       if (lane == 0) {
         sc->ring[i % kSlotRing] = x;
         if (x.b >= 0) {
+          // the G rows of each live group of columns (one group unless verifying)
           const uint32_t q_bytes = static_cast<uint32_t>(G * D * q_elem);
-          mbar_arrive_expect_tx(&raw_full[qs], q_bytes);
-          bulk_load(smem + C::kQ + qs * C::kQBytes,
-                    static_cast<const uint8_t*>(a.q) + (static_cast<int64_t>(x.b) * a.Hq + x.hkv * G) * D * q_elem,
-                    q_bytes, &raw_full[qs]);
+          int groups = 0;
+          for (int c = 0; c < GC; c += G) {
+            bool live;
+            col_row<kVerify>(a, x.b, x.hkv, c, G, live);
+            groups += live ? 1 : 0;
+          }
+          mbar_arrive_expect_tx(&raw_full[qs], q_bytes * groups);
+          for (int c = 0; c < GC; c += G) {
+            bool live;
+            const int64_t row = col_row<kVerify>(a, x.b, x.hkv, c, G, live);
+            if (live)
+              bulk_load(smem + C::kQ + qs * C::kQBytes + c * D * q_elem,
+                        static_cast<const uint8_t*>(a.q) + row * D * q_elem, q_bytes, &raw_full[qs]);
+          }
         } else {
           mbar_arrive(&raw_full[qs]);
         }
@@ -569,10 +597,11 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
     bool ok = true;
     uint32_t n = 0;
     auto merge = [&](const Slot& m, uint32_t mi) {
-      const int64_t row0 = static_cast<int64_t>(m.b) * a.Hq + m.hkv * G;
-      // lane q < G: the split's max and sum of query q over the warps
+      // lane q < GC: the split's max and sum of query column q over the warps
+      bool lane_live;
+      const int64_t lane_row = col_row<kVerify>(a, m.b, m.hkv, lane & 7, G, lane_live);
       float M = -INFINITY, L = 0.0f;
-      if (lane < G) {
+      if (lane < GC) {
 #pragma unroll
         for (int w = 0; w < C::kNW; ++w) M = fmaxf(M, stat[(w * 8 + lane) * 4]);
 #pragma unroll
@@ -580,11 +609,11 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
           const float mw = stat[(w * 8 + lane) * 4];
           if (mw != -INFINITY) L += stat[(w * 8 + lane) * 4 + 1] * ex2(mw - M);
         }
-        a.lse_partial[(row0 + lane) * a.num_splits + m.split] = (M + log2f(L)) * 0.6931471805599453f;
+        if (lane_live) a.lse_partial[lane_row * a.num_splits + m.split] = (M + log2f(L)) * 0.6931471805599453f;
       }
       // weight of warp w's state for query q: 2^(m_w - M) / L
-      const int nq4 = G > 4 ? 2 : 1;  // float4 groups of query columns
-      const float rL = lane < G ? 1.0f / L : 0.0f;
+      const int nq4 = GC > 4 ? 2 : 1;  // float4 groups of query columns
+      const float rL = lane < GC ? 1.0f / L : 0.0f;
       float wt[C::kNW][8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
@@ -612,8 +641,11 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
           }
         }
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (q < G) a.o_partial[((row0 + q) * a.num_splits + m.split) * D + dim] = acc[q];
+        for (int q = 0; q < 8; ++q) {
+          bool live;
+          const int64_t row = col_row<kVerify>(a, m.b, m.hkv, q, G, live);
+          if (live) a.o_partial[(row * a.num_splits + m.split) * D + dim] = acc[q];
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(red_empty);
@@ -682,10 +714,15 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
   for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
     const int L = clamp_len(a, b, st, !balanced && ct == 0);
     const int ns = (L + a.split_size - 1) / a.split_size;
-    const int n_empty = (a.num_splits - ns) * a.Hq;
+    // the rows of sequence b: its Hq heads, or (verify) those of its drafts
+    const int nd = kVerify ? min(a.verify_dps, a.verify_T - (b % a.verify_ng) * a.verify_dps) : 1;
+    const int n_empty = (a.num_splits - ns) * nd * a.Hq;
     for (int e = ct; e < n_empty; e += C::kCT) {
-      const int split = ns + e / a.Hq, hq = e % a.Hq;
-      a.lse_partial[(static_cast<int64_t>(b) * a.Hq + hq) * a.num_splits + split] = -INFINITY;
+      const int split = ns + e / (nd * a.Hq), r = e % (nd * a.Hq);
+      const int64_t row = kVerify ? (static_cast<int64_t>(b / a.verify_ng) * a.verify_T +
+                                        (b % a.verify_ng) * a.verify_dps + r / a.Hq) * a.Hq + r % a.Hq
+                                     : static_cast<int64_t>(b) * a.Hq + r;
+      a.lse_partial[row * a.num_splits + split] = -INFINITY;
     }
     if (L == 0 && a.q_codes) {
       for (int hq = cw; hq < a.Hq; hq += C::kNW) {
@@ -718,6 +755,8 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
       return true;
     }
     const uint8_t* raw = smem + C::kQ + qs * C::kQBytes + cw * D * q_elem;
+    bool col_live;
+    col_row<kVerify>(a, x.b, x.hkv, cw, G, col_live);  // dead verify columns quantise zeros
     int8_t* qc = reinterpret_cast<int8_t*>(smem + C::kQc + qs * C::kQcBytes);
     float* qinfo = reinterpret_cast<float*>(qc + 8 * D);  // [8] scales, [8] code sums
     float v[D / 32];
@@ -725,7 +764,8 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
 #pragma unroll
     for (int e = 0; e < D / 32; ++e) {
       const int idx = lane * (D / 32) + e;
-      v[e] = a.q_dtype == SL8_F32 ? reinterpret_cast<const float*>(raw)[idx]
+      v[e] = !col_live ? 0.0f
+           : a.q_dtype == SL8_F32 ? reinterpret_cast<const float*>(raw)[idx]
            : a.q_dtype == SL8_BF16 ? bf16_bits(reinterpret_cast<const uint16_t*>(raw)[idx])
                                    : f16_bits(reinterpret_cast<const uint16_t*>(raw)[idx]);
     }
@@ -758,7 +798,7 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
   uint32_t k = 0, n = 0;
   bool ok = true;
   Slot s;
-  if (cw < G) ok = quant_row(0);
+  if (cw < GC) ok = quant_row(0);
   while (ok) {
     // ---- slot n, as announced by the loader (b < 0: the list has ended)
     const uint32_t qs = n % kQSlots;
@@ -777,24 +817,24 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
 #pragma unroll
     for (int h = 0; h < D / 64; ++h) {
       uint4 w = make_uint4(0u, 0u, 0u, 0u);
-      if (g < G) w = *reinterpret_cast<const uint4*>(qc + g * D + 64 * h + 16 * t);
+      if (g < GC) w = *reinterpret_cast<const uint4*>(qc + g * D + 64 * h + 16 * t);
       const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const uint32_t u = ww[j] ^ 0x80808080u;
-        qb[4 * h + j][0] = g < G ? codes_f16x2(u, 0x4140) : 0u;
-        qb[4 * h + j][1] = g < G ? codes_f16x2(u, 0x4342) : 0u;
+        qb[4 * h + j][0] = g < GC ? codes_f16x2(u, 0x4140) : 0u;
+        qb[4 * h + j][1] = g < GC ? codes_f16x2(u, 0x4342) : 0u;
       }
     }
     // query columns qa = 2t, qb = 2t + 1: dequantisation factors (log2 units) and the
     // offset of the biased K codes, -128 * sum(q codes)
-    const float qsa = 2 * t < G ? qinfo[2 * t] * log2e_over_sqrtd : 0.0f;
-    const float qsb = 2 * t + 1 < G ? qinfo[2 * t + 1] * log2e_over_sqrtd : 0.0f;
-    const float offa = 2 * t < G ? -128.0f * qinfo[8 + 2 * t] : 0.0f;
-    const float offb = 2 * t + 1 < G ? -128.0f * qinfo[8 + 2 * t + 1] : 0.0f;
+    const float qsa = 2 * t < GC ? qinfo[2 * t] * log2e_over_sqrtd : 0.0f;
+    const float qsb = 2 * t + 1 < GC ? qinfo[2 * t + 1] * log2e_over_sqrtd : 0.0f;
+    const float offa = 2 * t < GC ? -128.0f * qinfo[8 + 2 * t] : 0.0f;
+    const float offb = 2 * t + 1 < GC ? -128.0f * qinfo[8 + 2 * t + 1] : 0.0f;
     __syncwarp();
     if (lane == 0) mbar_arrive(&qc_empty[qs]);
-    if (cw < G && !quant_row(n + 1)) {
+    if (cw < GC && !quant_row(n + 1)) {
       ok = false;
       break;
     }
@@ -807,12 +847,16 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
     float o[D / 16][4], osum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int j = 0; j < D / 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.0f;
-    // verify: the slot's draft tokens start at v_tail; v_mask says which it sees
+    // verify: the slot's draft tokens start at v_tail; mask_a / mask_b say which of them
+    // the lane's query columns 2t and 2t + 1 see
     int v_tail = 0;
-    uint32_t v_mask = 0;
-    if (a.verify_T) {
+    uint32_t mask_a = 0, mask_b = 0;
+    if constexpr (kVerify) {
       v_tail = (balanced ? sc->len[s.b] : clamp_len(a, s.b, st, false)) - a.verify_T;
-      v_mask = a.tree_mask[s.b];
+      bool la, lb;
+      const int64_t ra_ = col_row<kVerify>(a, s.b, s.hkv, 2 * t, G, la), rb_ = col_row<kVerify>(a, s.b, s.hkv, 2 * t + 1, G, lb);
+      if (la) mask_a = a.tree_mask[ra_ / a.Hq];
+      if (lb) mask_b = a.tree_mask[rb_ / a.Hq];
     }
     for (int c0 = s.t0; c0 < s.t1 && ok; c0 += C::kChunk, ++k) {
       const int ntok = min(C::kChunk, s.t1 - c0);
@@ -848,12 +892,19 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
         const float d00 = fmaf(s0[0] + s1[0], k2p24, offa), d01 = fmaf(s0[1] + s1[1], k2p24, offb);
         const float d10 = fmaf(s0[2] + s1[2], k2p24, offa), d11 = fmaf(s0[3] + s1[3], k2p24, offb);
         const int rA = u0 + pi, rB = rA + 8;
-        bool vA = kFull || pi < nv, vB = kFull || pi + 8 < nv;
-        if (!kFull && a.verify_T) {
-          // verify: the draft tokens from v_tail on are visible as the slot's mask says
+        const bool vA = kFull || pi < nv, vB = kFull || pi + 8 < nv;
+        // per query column: verify shows the draft tokens from v_tail on as the masks say
+        bool vAa = vA, vAb = vA, vBa = vB, vBb = vB;
+        if (kVerify && !kFull) {
           const int tA = c0 + rA, tB = c0 + rB;
-          vA = vA && (tA < v_tail || ((v_mask >> (tA - v_tail)) & 1u));
-          vB = vB && (tB < v_tail || ((v_mask >> (tB - v_tail)) & 1u));
+          if (tA >= v_tail) {
+            vAa = vAa && ((mask_a >> (tA - v_tail)) & 1u);
+            vAb = vAb && ((mask_b >> (tA - v_tail)) & 1u);
+          }
+          if (tB >= v_tail) {
+            vBa = vBa && ((mask_a >> (tB - v_tail)) & 1u);
+            vBb = vBb && ((mask_b >> (tB - v_tail)) & 1u);
+          }
         }
         if (a.logits) {
           int32_t* lg = a.logits + c0;
@@ -870,8 +921,8 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
         const float ksA = vA ? sks[rA] : 0.0f, ksB = vB ? sks[rB] : 0.0f;
         const float vsA = vA ? (kV16 ? 1.0f : svs[rA]) : 0.0f, vsB = vB ? (kV16 ? 1.0f : svs[rB]) : 0.0f;
         const float ka = ksA * qsa, kb = ksA * qsb, kc = ksB * qsa, kd = ksB * qsb;
-        const float xa0 = vA ? d00 * ka : -INFINITY, xa1 = vA ? d01 * kb : -INFINITY;
-        const float xb0 = vB ? d10 * kc : -INFINITY, xb1 = vB ? d11 * kd : -INFINITY;
+        const float xa0 = vAa ? d00 * ka : -INFINITY, xa1 = vAb ? d01 * kb : -INFINITY;
+        const float xb0 = vBa ? d10 * kc : -INFINITY, xb1 = vBb ? d11 * kd : -INFINITY;
         const bool grow = (fmaxf(xa0, xb0) > tha) || (fmaxf(xa1, xb1) > thb) || (fmaxf(vsA, vsB) > vlim);
         if (__any_sync(0xffffffffu, grow)) {
           const float ma = col_max(fmaxf(xa0, xb0)), mb = col_max(fmaxf(xa1, xb1));
@@ -973,7 +1024,7 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
         }
         if constexpr (!kV16) mma_f16(osum, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, pb0r, pb1r);
       };
-      if (nv >= kUnit && !(a.verify_T && c0 + u0 + kUnit > v_tail)) {
+      if (nv >= kUnit && !(kVerify && c0 + u0 + kUnit > v_tail)) {
         unit(std::true_type{});
       } else if (nv > 0) {
         unit(std::false_type{});
@@ -1110,10 +1161,10 @@ __global__ void timeout_selftest_kernel(uint64_t limit_ns, DeviceStatus* st) {
   if (threadIdx.x == 0) mbar_wait(&bar, 0, limit_ns, st, 999);
 }
 
-template <int D, bool kV16>
+template <int D, bool kV16, bool kVerify = false>
 cudaError_t launch_split_d(const DecodeArgs& a, cudaStream_t s) {
   using C = DCfg<D, kV16>;
-  auto kern = decode_split_kernel<D, kV16>;
+  auto kern = decode_split_kernel<D, kV16, kVerify>;
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), C::kBytes);
   if (e != cudaSuccess) return e;
   // each cache as a 2-D [B * Hkv * Lmax rows][d bytes] tensor, loaded in boxes of
@@ -1153,6 +1204,14 @@ int decode_chunk_tokens(int d) { return d == 256 ? DCfg<256>::kChunk : d == 128 
 
 cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t s) {
   TraceScope tr("decode_split", s);
+  if (a.verify_T) {
+    switch (a.d) {
+      case 64: return launch_split_d<64, false, true>(a, s);
+      case 128: return launch_split_d<128, false, true>(a, s);
+      case 256: return launch_split_d<256, false, true>(a, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   if (a.v16) {
     switch (a.d) {
       case 64: return launch_split_d<64, true>(a, s);

@@ -172,11 +172,14 @@ struct DecodeArgs {
   // fp16 V cache (v_cache holds [B][Hkv][Lmax][d] fp16 values, v_scale unused); d <= 128,
   // contiguous caches only
   bool v16;
-  // speculative verify (verify_T > 0): B counts B_cache * verify_T virtual sequences
-  // v = b * verify_T + t (query t of cache sequence b, q [B][Hq][d] = [B_cache][T][Hq][d]);
-  // seqlens and the caches are indexed by b = v / verify_T; the last verify_T positions of
-  // b are the draft tokens, of which v sees u iff bit u of tree_mask[v] is set
-  int32_t verify_T;
+  // speculative verify (verify_T > 0): the verify_T draft queries of cache sequence b
+  // (q [B_cache][T][Hq][d]) go verify_dps at a time into the query columns of one slot
+  // (verify_dps * G <= 8): B counts B_cache * verify_ng virtual sequences v = b * verify_ng
+  // + group, group g holding drafts g * verify_dps ..; seqlens and the caches are indexed
+  // by b = v / verify_ng.  The last verify_T positions of b are the draft tokens: draft
+  // query t sees draft token u iff bit u of tree_mask[b * verify_T + t] is set.  The
+  // partials are [B_cache * T][Hq][S][d], row (b * T + t) * Hq + hq.
+  int32_t verify_T, verify_dps, verify_ng;
   const uint32_t* tree_mask;
 };
 cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t s);
