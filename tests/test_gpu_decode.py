@@ -320,3 +320,37 @@ def test_decode_verify(case):
         np.testing.assert_allclose(to_np32(o32[:, 0]), to_np32(plain), rtol=0, atol=5e-4)
     st, site = sl8.last_device_status()
     assert st == sl8.SL8_OK, (st, site)
+
+
+@pytest.mark.parametrize("qdt", ["f16", "f32"])
+def test_decode_query_dtypes(qdt):
+    """q in fp16 or fp32 (quantised inside the kernel like bf16): codes and logits bit-exact,
+    outputs within tolerance, for plain decode and for verify."""
+    B, Hq, Hkv, d, lens, lmax = 3, 8, 2, 128, [700, 33, 1], 700
+    w = W.custom(3601, kind="decode", B=B, Hq=Hq, Hkv=Hkv, d=d, dtype=qdt, extra={"lengths": lens})
+    lens_np, g, gs, o, os_ = build_cache(w, lmax)
+    q = W.decode_query(w)
+    qd = q.to(DEV)
+    seq = torch.from_numpy(lens_np.astype(np.int32)).to(DEV)
+    dbg = sl8.attn_int8_decode_logits_debug(qd, g["k"], gs["k"], g["v"], gs["v"], seq)
+    ref = oracle.attn_decode(q.float().numpy(), o["k"], os_["k"], o["v"], os_["v"], lens_np, want_logits=True)
+    np.testing.assert_array_equal(dbg["q_codes"].cpu().numpy(), ref["q_codes"])
+    np.testing.assert_array_equal(dbg["q_scales"].cpu().numpy(), ref["q_scales"])
+    lg = dbg["logits"].cpu().numpy()
+    for b in range(B):
+        for h in range(Hq):
+            np.testing.assert_array_equal(lg[b, h, :lens_np[b]], ref["logits"][(b, h)])
+    o32 = sl8.attn_int8_decode(qd, g["k"], gs["k"], g["v"], gs["v"], seq, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    check_f32(to_np32(o32), ref["out"], f"q {qdt} f32")
+    # verify with a 2-draft chain on the same cache
+    rng = np.random.default_rng(3602)
+    qv = torch.from_numpy(rng.standard_normal((B, 2, Hq, d)).astype(np.float32)).to(W.torch_dtype(qdt))
+    mask = np.array([[1, 3]] * B, np.int64)
+    refv = oracle.attn_decode_verify(qv.float().numpy(), o["k"], os_["k"], o["v"], os_["v"], lens_np, mask)
+    ov = sl8.attn_int8_decode_verify(qv.to(DEV), g["k"], gs["k"], g["v"], gs["v"], seq,
+                                     torch.from_numpy(mask.astype(np.int32)).to(DEV), out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    check_f32(to_np32(ov), refv["out"], f"q {qdt} verify f32")
+    st, site = sl8.last_device_status()
+    assert st == sl8.SL8_OK, (st, site)
