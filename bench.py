@@ -13,7 +13,9 @@ the timed steps, `decode_f16v` the decode with an fp16 V cache (int8 K), and
 `prefill_chunk` the prefill's last 1024 positions as a query chunk (chunked prefill,
 bottom-right causal), and `decode_verify` the decode with 4 chained draft queries per
 sequence (speculative verify).  Inputs are resident in HBM when the timed
-region starts; L2 is flushed before every step, outside the timed events (a 256 MB
+region starts (the timed steps carry no per-launch instrumentation: per-kernel times
+come from a separate traced pass); L2 is flushed before every step, outside the timed
+events (a 256 MB
 write, then a read of that buffer, so no dirty lines of the flush remain).  `e2e` repeats the prefill through the public API with pinned host
 inputs copied in and the output copied back every step.
 
@@ -279,8 +281,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    sl8.trace_collect()
-    sl8.trace_enable(True)
+    sl8.trace_enable(False)
     barrier(world)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
@@ -290,11 +291,20 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall
     barrier(world)
-    sl8.trace_enable(False)
-    trace = sl8.trace_collect()
     st, site = sl8.last_device_status(dev)
     if st != sl8.SL8_OK:
         raise RuntimeError(f"device status {st} at {site} during the timed steps")
+    # Per-kernel durations and launch counts come from the same steps run again with every
+    # launch bracketed by CUDA events.  Those events break the overlap of the
+    # programmatically dependent launches, so they stay out of the timed steps above.
+    trace_steps = min(args.steps, 100)
+    sl8.trace_collect()
+    sl8.trace_enable(True)
+    for _ in range(trace_steps):
+        step()
+    torch.cuda.synchronize(dev)
+    sl8.trace_enable(False)
+    trace = sl8.trace_collect()
 
     pre_ms = sum(e[0].elapsed_time(e[1]) for e in events) / args.steps
     dec_ms = sum(e[1].elapsed_time(e[2]) for e in events) / args.steps
@@ -313,7 +323,7 @@ def run_ours(args, world, rank, local):
     n_split, split_ms = kern("decode_split")
     attn_tflops = ops / (attn_ms * 1e-3) / 1e12
     split_gbs = dbytes / (split_ms * 1e-3) / 1e9
-    launches = sum(n for n, _ in trace.values())
+    launches = sum(n for n, _ in trace.values()) * args.steps // trace_steps  # launches in the timed steps
     traffic = load_traffic()
     if args.only != "all":
         if rank == 0:
@@ -429,6 +439,29 @@ def run_ours(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def timed_then_traced(sl8, step, device, steps, warmup):
+    """Run step(ev) warm-up times, then time up to 100 steps with events around each step
+    only; then a short pass with every launch traced, for the per-kernel durations.
+    Returns (steps timed, ms per step, trace)."""
+    import torch
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(device)
+    n = max(3, min(steps, 100))
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for i in range(n):
+        step(events[i])
+    torch.cuda.synchronize(device)
+    ms = sum(e[0].elapsed_time(e[1]) for e in events) / n
+    sl8.trace_collect()
+    sl8.trace_enable(True)
+    for _ in range(min(n, 20)):
+        step()
+    torch.cuda.synchronize(device)
+    sl8.trace_enable(False)
+    return n, ms, sl8.trace_collect()
+
+
 PAGE_SIZE = 64
 
 
@@ -454,22 +487,11 @@ def measure_paged(sl8, W, wd, kc, ks, vc, vs, lens, qdec, seq, stream, flush, fl
         if ev:
             ev[1].record(stream)
 
-    for _ in range(warmup):
-        step()
-    torch.cuda.synchronize(kc.device)
-    n = max(3, min(steps, 100))
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
-    sl8.trace_collect()
-    sl8.trace_enable(True)
-    for i in range(n):
-        step(events[i])
-    torch.cuda.synchronize(kc.device)
-    sl8.trace_enable(False)
-    trace = sl8.trace_collect()
+    n, ms, trace = timed_then_traced(sl8, step, kc.device, steps, warmup)
     st, site = sl8.last_device_status(kc.device)
     if st != sl8.SL8_OK:
         raise RuntimeError(f"device status {st} at {site} during the paged decode")
-    ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in events) / n, world)
+    ms = max_over_ranks(ms, world)
     c, split_ms = trace.get("decode_split", (0, 0.0))
     return ms, (split_ms / c if c else float("nan")), n, num_pages
 
@@ -496,22 +518,11 @@ def measure_f16v(sl8, W, wd, kc, ks, lens, qdec, seq, stream, flush, flush_sink,
         if ev:
             ev[1].record(stream)
 
-    for _ in range(warmup):
-        step()
-    torch.cuda.synchronize(kc.device)
-    n = max(3, min(steps, 100))
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
-    sl8.trace_collect()
-    sl8.trace_enable(True)
-    for i in range(n):
-        step(events[i])
-    torch.cuda.synchronize(kc.device)
-    sl8.trace_enable(False)
-    trace = sl8.trace_collect()
+    n, ms, trace = timed_then_traced(sl8, step, kc.device, steps, warmup)
     st, site = sl8.last_device_status(kc.device)
     if st != sl8.SL8_OK:
         raise RuntimeError(f"device status {st} at {site} during the fp16-V decode")
-    ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in events) / n, world)
+    ms = max_over_ranks(ms, world)
     c, split_ms = trace.get("decode_split", (0, 0.0))
     del v16
     return ms, (split_ms / c if c else float("nan")), n
@@ -535,22 +546,11 @@ def measure_chunk(sl8, wp, qd, kd, vd, stream, flush, flush_sink, steps, warmup,
         if ev:
             ev[1].record(stream)
 
-    for _ in range(warmup):
-        step()
-    torch.cuda.synchronize(qd.device)
-    n = max(3, min(steps, 100))
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
-    sl8.trace_collect()
-    sl8.trace_enable(True)
-    for i in range(n):
-        step(events[i])
-    torch.cuda.synchronize(qd.device)
-    sl8.trace_enable(False)
-    trace = sl8.trace_collect()
+    n, ms, trace = timed_then_traced(sl8, step, qd.device, steps, warmup)
     st, site = sl8.last_device_status(qd.device)
     if st != sl8.SL8_OK:
         raise RuntimeError(f"device status {st} at {site} during the chunked prefill")
-    ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in events) / n, world)
+    ms = max_over_ranks(ms, world)
     c, attn_ms = trace.get("prefill_attn", (0, 0.0))
     return ms, (attn_ms / c if c else float("nan")), n
 
