@@ -5,7 +5,8 @@
  *   - "Supporting kernels" table, quant_rowwise: symmetric per-row int8 quantisation;
  *   - "Quantization" table, "Per-row int8": symmetric, with K-smoothing;
  *   - "Attention kernels" table, attn_int8_fwd: W8A8 FlashAttention-2 forward,
- *     causal, GQA/MQA, head dims 32/64/128/256 (this library: 64, 128, 256);
+ *     causal, GQA/MQA, head dims 32/64/128/256 (this library: prefill all four, decode
+ *     64, 128, 256);
  *     attn_varlen_fwd: ragged variable-length prefill; attn_decode: split-KV decode
  *     with an int8 KV cache, int8-V variant;
  *   - "Quick start" section: q [B, Hq, N, d], k/v [B, Hkv, N, d],
@@ -112,7 +113,8 @@ SL8_API int sl8_k_channel_mean(const void* k, int k_dtype, int32_t B, int32_t Hk
  *               B = number of sequences, N = the longest sequence length (an upper
  *               bound every cu_seqlens length must respect).
  *   qk_dtype    F16 or BF16 (q and k); v_dtype F16 or BF16.
- *   d           64, 128 or 256.  Hq must be a multiple of Hkv.
+ *   d           32, 64, 128 or 256 (32 runs as 64 with zero channels past 32: exact, at the
+ *               cost of d = 64).  Hq must be a multiple of Hkv.
  *   causal      nonzero: key j is visible to query i iff j <= i (positions within the
  *               sequence).
  *   smooth_k    nonzero: subtract K's per-channel mean before quantising K.

@@ -45,6 +45,8 @@ CODE_CASES = [
     (2003, 1, 2, 2, 200, 256, "bf16", True, 0.0, 0.0),
     (2004, 1, 8, 8, 129, 128, "bf16", False, 0.0, 0.0),
     (2005, 1, 2, 1, 1, 64, "bf16", True, 1.0, 0.0),
+    (2006, 1, 4, 2, 200, 32, "bf16", True, 1.0, 0.0),
+    (2007, 2, 2, 1, 129, 32, "f16", False, 0.0, 0.0),
 ]
 
 
@@ -102,6 +104,9 @@ OUT_CASES = [
     (2109, 1, 2, 1, 128, 128, "bf16", True, True, 0.0),
     (2110, 1, 4, 1, 255, 128, "bf16", False, False, 0.0),
     (2111, 1, 2, 2, 384, 256, "f16", False, True, 1.0),
+    (2112, 1, 4, 2, 300, 32, "f16", True, True, 1.0),
+    (2113, 2, 8, 2, 129, 32, "bf16", True, True, 0.0),
+    (2114, 1, 2, 2, 200, 32, "bf16", False, False, 0.0),
 ]
 
 
@@ -153,6 +158,20 @@ def test_varlen_small():
     ref = oracle.attn_prefill(_np(q), _np(k), _np(v), causal=True, smooth_k=True, cu_seqlens=cu.numpy())
     check_f32(to_np32(o32), ref["out"], "varlen f32")
     check_half(oh, ref["out"], "varlen bf16")
+    np.testing.assert_allclose(to_np32(lse), ref["lse"], rtol=0, atol=1e-4)
+
+
+def test_varlen_head_dim_32():
+    """Head dim 32 (run as 64 with zero channels) on ragged sequences."""
+    w = W.custom(2202, kind="varlen", B=4, Hq=4, Hkv=2, d=32, dtype="bf16", k_bias_std=1.0,
+                 extra={"lengths": [1, 130, 77, 256]})
+    q, k, v, cu = W.prefill_varlen(w)
+    o32, lse = sl8.attn_int8_fwd(q.to(DEV), k.to(DEV), v.to(DEV), cu_seqlens=cu.to(DEV), max_seqlen=256,
+                                 out_dtype=torch.float32, return_lse=True)
+    torch.cuda.synchronize()
+    _status_ok()
+    ref = oracle.attn_prefill(_np(q), _np(k), _np(v), causal=True, smooth_k=True, cu_seqlens=cu.numpy())
+    check_f32(to_np32(o32), ref["out"], "varlen d32 f32")
     np.testing.assert_allclose(to_np32(lse), ref["lse"], rtol=0, atol=1e-4)
 
 
@@ -239,6 +258,7 @@ CHUNK_CASES = [
     (2605, 1, 4, 2, 300, 777, 256, "bf16", True),
     (2606, 1, 4, 4, 70, 400, 128, "bf16", False),
     (2607, 2, 8, 2, 257, 1000, 128, "bf16", True),
+    (2608, 1, 4, 2, 100, 333, 32, "f16", True),
 ]
 
 

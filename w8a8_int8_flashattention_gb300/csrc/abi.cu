@@ -147,6 +147,7 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 PrefillWorkspace plan_prefill_workspace(int32_t nseq, int32_t Hq, int32_t Hkv, int32_t N, int32_t d,
                                         int64_t total_tokens, bool varlen) {
+  if (d == 32) d = 64;  // head dim 32 runs as 64: code, V and partial rows of 64
   PrefillWorkspace w{};
   w.max_tiles = (N + kQTile - 1) / kQTile;
   w.max_chunks = (N + kMeanChunk - 1) / kMeanChunk;
@@ -212,6 +213,8 @@ namespace {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool is_half(int dt) { return dt == SL8_F16 || dt == SL8_BF16; }
 bool head_dim_ok(int32_t d) { return d == 64 || d == 128 || d == 256; }
+// Head dim the prefill kernels compute in: 32 runs as 64 (codes, V copy and O zero past 32).
+int32_t compute_dim(int32_t d) { return d == 32 ? 64 : d; }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? SL8_OK : SL8_ERR_CUDA; }
 
@@ -238,7 +241,7 @@ int validate_prefill(const void* q, const void* k, int qk_dtype, int32_t B, int3
   SL8_CHECK(is_half(qk_dtype), SL8_ERR_INVALID_ARG);
   SL8_CHECK(B >= 0 && N >= 0 && Hq > 0 && Hkv > 0 && d > 0, SL8_ERR_INVALID_ARG);
   SL8_CHECK(Hq % Hkv == 0, SL8_ERR_INVALID_ARG);
-  SL8_CHECK(head_dim_ok(d), SL8_ERR_UNSUPPORTED);
+  SL8_CHECK(d == 32 || head_dim_ok(d), SL8_ERR_UNSUPPORTED);  // head dim 32 runs as 64
   SL8_CHECK(N <= (1 << 24) && B <= (1 << 24), SL8_ERR_UNSUPPORTED);
   return SL8_OK;
 }
@@ -330,24 +333,28 @@ static int prefill_prepare(const void* q, const void* k, const void* v, int qk_d
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const SeqTable t = table_at(ws, p);
   const int64_t tokens = varlen ? total_tokens : static_cast<int64_t>(B) * N;
-  const bool convert_v = v && v_dtype == SL8_BF16;
+  // head dim 32 runs as 64 (zero channels past 32): V always goes through the padded copy
+  const int32_t dc = compute_dim(d);
+  const bool convert_v = v && (v_dtype == SL8_BF16 || dc != d);
+  const bool v_stats = v && v_dtype == SL8_BF16;
   // the scheduler's table is needed for varlen input (and by the code export); dense
   // input is laid out arithmetically
   if (varlen || want_table)
-    SL8_LAUNCH(launch_schedule(cu_seqlens, B, N, tokens, p.t_pad_max, t, prefill_item_rows(d, Hq / Hkv), nullptr, 0,
+    SL8_LAUNCH(launch_schedule(cu_seqlens, B, N, tokens, p.t_pad_max, t, prefill_item_rows(dc, Hq / Hkv), nullptr, 0,
                                s));
   float* k_partials = smooth_k ? reinterpret_cast<float*>(ws + p.k_partials) : nullptr;
-  float* v_partials = convert_v ? reinterpret_cast<float*>(ws + p.v_partials) : nullptr;
-  if (smooth_k || convert_v)
-    SL8_LAUNCH(launch_kv_partials(k, static_cast<sl8_dtype>(qk_dtype), convert_v ? v : nullptr, varlen, B, Hkv, N, d,
+  float* v_partials = v_stats ? reinterpret_cast<float*>(ws + p.v_partials) : nullptr;
+  if (smooth_k || v_stats)
+    SL8_LAUNCH(launch_kv_partials(k, static_cast<sl8_dtype>(qk_dtype), v_stats ? v : nullptr, varlen, B, Hkv, N, d,
                                   varlen ? t.len : nullptr, varlen ? t.tok0 : nullptr, k_partials, v_partials,
                                   p.max_chunks, s));
-  SL8_LAUNCH(launch_quant_qk(q, k, static_cast<sl8_dtype>(qk_dtype), varlen, B, Hq, Hkv, N, d, tokens, t,
+  SL8_LAUNCH(launch_quant_qk(q, k, static_cast<sl8_dtype>(qk_dtype), varlen, B, Hq, Hkv, N, dc, tokens, t,
                              p.t_pad_max, k_partials, v_partials, p.max_chunks,
                              reinterpret_cast<uint16_t*>(ws + p.q_codes), reinterpret_cast<float*>(ws + p.q_scales),
                              reinterpret_cast<uint16_t*>(ws + p.k_codes), reinterpret_cast<float*>(ws + p.k_scales),
                              convert_v ? v : nullptr, convert_v ? reinterpret_cast<int32_t*>(ws + p.v_exp) : nullptr,
-                             convert_v ? reinterpret_cast<uint16_t*>(ws + p.v16) : nullptr, s, q_off));
+                             convert_v ? reinterpret_cast<uint16_t*>(ws + p.v16) : nullptr, s, q_off, d,
+                             v_dtype == SL8_F16));
   *plan = p;
   *table = t;
   return SL8_OK;
@@ -377,13 +384,14 @@ static int prefill_run(const void* q, const void* k, const void* v, int qk_dtype
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   PrefillArgs a{};
   a.q_off = q_off;
+  const int32_t dc = compute_dim(d);
   a.q_codes = reinterpret_cast<const uint16_t*>(ws + p.q_codes);
   a.q_scales = reinterpret_cast<const float*>(ws + p.q_scales);
   a.k_codes = reinterpret_cast<const uint16_t*>(ws + p.k_codes);
   a.k_scales = reinterpret_cast<const float*>(ws + p.k_scales);
   a.v = v;
   a.v_dtype = static_cast<sl8_dtype>(v_dtype);
-  if (v_dtype == SL8_BF16) {
+  if (v_dtype == SL8_BF16 || dc != d) {  // the padded / rescaled fp16 copy of V
     a.v16 = reinterpret_cast<const uint16_t*>(ws + p.v16);
     a.v_exp = reinterpret_cast<const int32_t*>(ws + p.v_exp);
   }
@@ -392,14 +400,15 @@ static int prefill_run(const void* q, const void* k, const void* v, int qk_dtype
   a.Hq = Hq;
   a.Hkv = Hkv;
   a.N = N;
-  a.d = d;
+  a.d = dc;
+  a.d_io = d;
   a.total_tokens = a.varlen ? total_tokens : static_cast<int64_t>(B) * N;
   a.t_pad_max = p.t_pad_max;
   a.table = t;
-  const int32_t item_rows = prefill_item_rows(d, Hq / Hkv);
+  const int32_t item_rows = prefill_item_rows(dc, Hq / Hkv);
   a.dense_first = q_off / item_rows;
   a.dense_items = (N + item_rows - 1) / item_rows - a.dense_first;
-  a.head_pairs = prefill_head_pairs(d, Hq / Hkv);
+  a.head_pairs = prefill_head_pairs(dc, Hq / Hkv);
   a.max_pairs = p.max_pairs;
   a.causal = causal != 0;
   a.out = out;
@@ -445,33 +454,38 @@ int sl8_attn_int8_qk_logits_debug(const void* q, const void* k, int qk_dtype, in
                        workspace_bytes, s, true, &p, &t);
   if (rc != SL8_OK) return rc;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int32_t dc = compute_dim(d);
   if (q_codes)
     SL8_LAUNCH(launch_export_codes(reinterpret_cast<const uint16_t*>(ws + p.q_codes),
-                                   reinterpret_cast<const float*>(ws + p.q_scales), false, B, Hq, N, d, t, p.t_pad_max,
-                                   q_codes, q_scales, s));
+                                   reinterpret_cast<const float*>(ws + p.q_scales), false, B, Hq, N, dc, t,
+                                   p.t_pad_max, q_codes, q_scales, s, d));
   if (k_codes)
     SL8_LAUNCH(launch_export_codes(reinterpret_cast<const uint16_t*>(ws + p.k_codes),
-                                   reinterpret_cast<const float*>(ws + p.k_scales), false, B, Hkv, N, d, t,
-                                   p.t_pad_max, k_codes, k_scales, s));
+                                   reinterpret_cast<const float*>(ws + p.k_scales), false, B, Hkv, N, dc, t,
+                                   p.t_pad_max, k_codes, k_scales, s, d));
   if (logits_out && row_end > row_begin) {
     PrefillArgs a{};
     a.q_codes = reinterpret_cast<const uint16_t*>(ws + p.q_codes);
     a.q_scales = reinterpret_cast<const float*>(ws + p.q_scales);
     a.k_codes = reinterpret_cast<const uint16_t*>(ws + p.k_codes);
     a.k_scales = reinterpret_cast<const float*>(ws + p.k_scales);
-    a.v = q;  // V is not used for logits; any readable [B, Hkv, N, d] tensor keeps the map valid
+    // V is not used for logits; the V tiles are read from the Q code rows, a readable
+    // [Hq >= Hkv][t_pad][d] fp16-sized region of the workspace
+    a.v = nullptr;
     a.v_dtype = SL8_F16;
+    a.v16 = reinterpret_cast<const uint16_t*>(ws + p.q_codes);
     a.varlen = false;
     a.nseq = B;
     a.Hq = Hq;
     a.Hkv = Hkv;
     a.N = N;
-    a.d = d;
+    a.d = dc;
+    a.d_io = d;
     a.total_tokens = static_cast<int64_t>(B) * N;
     a.t_pad_max = p.t_pad_max;
     a.table = t;
-    a.dense_items = (N + prefill_item_rows(d, Hq / Hkv) - 1) / prefill_item_rows(d, Hq / Hkv);
-    a.head_pairs = prefill_head_pairs(d, Hq / Hkv);
+    a.dense_items = (N + prefill_item_rows(dc, Hq / Hkv) - 1) / prefill_item_rows(dc, Hq / Hkv);
+    a.head_pairs = prefill_head_pairs(dc, Hq / Hkv);
     a.max_pairs = p.max_pairs;
     a.causal = false;
     a.out = nullptr;

@@ -384,15 +384,18 @@ __device__ __forceinline__ void store_row(uint32_t o_taddr, const PrefillArgs& a
     tmem_wait_ld();
     if (row_ok) {
       if (out_f32) {
-        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow * D + c0);
+        // rows of the output hold d_io values (32 when head dim 32 runs as 64)
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow * a.d_io + c0);
 #pragma unroll
         for (int c = 0; c < 64; c += 4)
-          dst[c / 4] = make_float4(__uint_as_float(v[c]) * scale, __uint_as_float(v[c + 1]) * scale,
+          if (c0 + c < a.d_io)
+            dst[c / 4] = make_float4(__uint_as_float(v[c]) * scale, __uint_as_float(v[c + 1]) * scale,
                                    __uint_as_float(v[c + 2]) * scale, __uint_as_float(v[c + 3]) * scale);
       } else {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow * D + c0);
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow * a.d_io + c0);
 #pragma unroll
         for (int c = 0; c < 64; c += 8) {
+          if (c0 + c >= a.d_io) break;
           uint32_t p[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e)
@@ -677,7 +680,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(wrow) << 16;
     const uint32_t s_taddr = tbase + lane_base + t * 256;
     const uint32_t o_taddr = s_taddr + 128;
-    const float qk_scale = kLog2e * rsqrtf(static_cast<float>(D));
+    const float qk_scale = kLog2e * rsqrtf(static_cast<float>(a.d_io));  // the true head dim (32 runs as 64)
     uint32_t ns = 0, no = 0;   // S tiles consumed, items finished (this tile)
     bool bad = false;
     for (uint32_t it = 0; !bad; ++it) {
@@ -930,7 +933,7 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
     const int r = threadIdx.x;                    // TMEM lane: the row this thread stores
     const int wrow = warp * 32;
     const uint32_t lane_base = static_cast<uint32_t>(wrow) << 16;
-    const float qk_scale = kLog2e * rsqrtf(static_cast<float>(D));
+    const float qk_scale = kLog2e * rsqrtf(static_cast<float>(a.d_io));  // the true head dim (32 runs as 64)
     int64_t item = blockIdx.x;
     Item w{};
     uint32_t g = 0;

@@ -640,6 +640,8 @@ struct QuantQK {
   bool varlen;
   int32_t nseq, Hq, Hkv, N;
   int32_t q_off;            // dense query chunk: q holds positions q_off .. N-1
+  int32_t d_io;             // values per input row (<= D; the code rows are zero past them)
+  bool v_f16;               // V is fp16 (copied as is) rather than bf16
   int64_t total_tokens;
   SeqTable t;
   int64_t t_pad_max;
@@ -721,12 +723,13 @@ __global__ void __launch_bounds__(kQuantWarps * 32, D == 256 ? 2 : 4) quant_qk_k
     const int64_t srow = static_cast<int64_t>(s0) * a.Hkv + h;
     if (smooth) {
       for (int c = threadIdx.x; c < D; c += blockDim.x) {
-        const float* p = a.k_partials + srow * a.max_chunks * D + c;
+        // k_partials has d_io columns; the padded channels have mean 0
+        const float* p = a.k_partials + srow * a.max_chunks * a.d_io + c;
         float total = 0.0f;
-        for (int cb = 0; cb < nch; cb += 16) {
+        for (int cb = 0; cb < nch && c < a.d_io; cb += 16) {
           float xx[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) xx[i] = cb + i < nch ? p[static_cast<int64_t>(cb + i) * D] : 0.0f;
+          for (int i = 0; i < 16; ++i) xx[i] = cb + i < nch ? p[static_cast<int64_t>(cb + i) * a.d_io] : 0.0f;
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             if (cb + i < nch) total = __fadd_rn(total, xx[i]);
@@ -736,7 +739,8 @@ __global__ void __launch_bounds__(kQuantWarps * 32, D == 256 ? 2 : 4) quant_qk_k
     }
     if (v16) {
       float m = 0.0f;
-      for (int cb = threadIdx.x; cb < nch; cb += blockDim.x) m = fmaxf(m, a.v_partials[srow * a.max_chunks + cb]);
+      if (a.v_partials)  // fp16 V: exponent 0
+        for (int cb = threadIdx.x; cb < nch; cb += blockDim.x) m = fmaxf(m, a.v_partials[srow * a.max_chunks + cb]);
       m = warp_max(m);
       if (lane == 0) s_vm[warp] = m;
       __syncthreads();
@@ -804,10 +808,10 @@ __global__ void __launch_bounds__(kQuantWarps * 32, D == 256 ? 2 : 4) quant_qk_k
       xw[p][j] = make_uint4(0u, 0u, 0u, 0u);
       vw[p][j] = make_uint4(0u, 0u, 0u, 0u);
     }
-    if (valid[p]) {
-      // a query chunk's rows: position t is row t - q_off of N - q_off
-      const int64_t off = (is_k ? row_offset(a.varlen, sq[p], h, tt[p], H, a.N, D, tk)
-                                : row_offset(a.varlen, sq[p], h, tt[p] - a.q_off, H, a.N - a.q_off, D, tk)) +
+    if (valid[p] && part * EPL < a.d_io) {
+      // a query chunk's rows: position t is row t - q_off of N - q_off; rows hold d_io values
+      const int64_t off = (is_k ? row_offset(a.varlen, sq[p], h, tt[p], H, a.N, a.d_io, tk)
+                                : row_offset(a.varlen, sq[p], h, tt[p] - a.q_off, H, a.N - a.q_off, a.d_io, tk)) +
                           part * EPL;
 #pragma unroll
       for (int j = 0; j < NV; ++j) {
@@ -879,8 +883,9 @@ __global__ void __launch_bounds__(kQuantWarps * 32, D == 256 ? 2 : 4) quant_qk_k
         uint32_t o[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const __half2 h2 = __floats2half2_rn(__fmul_rn(bf16_bits_to_float(ww[e] & 0xffffu), vscale),
-                                               __fmul_rn(bf16_bits_to_float(ww[e] >> 16), vscale));
+          const float v0 = a.v_f16 ? f16_bits_to_float(ww[e] & 0xffffu) : bf16_bits_to_float(ww[e] & 0xffffu);
+          const float v1 = a.v_f16 ? f16_bits_to_float(ww[e] >> 16) : bf16_bits_to_float(ww[e] >> 16);
+          const __half2 h2 = __floats2half2_rn(__fmul_rn(v0, vscale), __fmul_rn(v1, vscale));
           o[e] = *reinterpret_cast<const uint32_t*>(&h2);
         }
         *reinterpret_cast<uint4*>(vrow + 8 * j) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -906,8 +911,9 @@ cudaError_t launch_quant_qk(const void* q, const void* k, sl8_dtype dt, bool var
                             int64_t t_pad_max, const float* k_partials, const float* v_partials,
                             int32_t max_chunks, uint16_t* q_codes, float* q_scales, uint16_t* k_codes,
                             float* k_scales, const void* v, int32_t* v_exp, uint16_t* v16, cudaStream_t s,
-                            int32_t q_off) {
-  QuantQK a{q, k, varlen, nseq, Hq, Hkv, N, q_off, total_tokens, t, t_pad_max, k_partials, v_partials, max_chunks, v_exp,
+                            int32_t q_off, int32_t d_io, bool v_f16) {
+  QuantQK a{q, k, varlen, nseq, Hq, Hkv, N, q_off, d_io > 0 ? d_io : d, v_f16, total_tokens, t, t_pad_max, k_partials,
+            v_partials, max_chunks, v_exp,
             q_codes, q_scales, k_codes, k_scales, v, v16};
   TraceScope tr("quant_qk", s);
   return dt == SL8_BF16 ? launch_quant_qk_dt<SL8_BF16>(a, d, Hq + Hkv, s)
@@ -961,8 +967,9 @@ cudaError_t launch_quant_rowwise(const void* x, sl8_dtype dt, int64_t rows, int3
 // Workspace bf16 codes [H][t_pad][d] -> caller's int8 layout (dense [nseq,H,N,d] or
 // packed [T,H,d]) and scales (dense [nseq,H,N] or packed [T,H]).
 __global__ void export_codes_kernel(const uint16_t* __restrict__ codes, const float* __restrict__ scales, bool varlen,
-                                    int32_t nseq, int32_t H, int32_t N, int32_t d, SeqTable t, int64_t t_pad_max,
-                                    int8_t* __restrict__ codes_out, float* __restrict__ scales_out) {
+                                    int32_t nseq, int32_t H, int32_t N, int32_t d, int32_t d_io, SeqTable t,
+                                    int64_t t_pad_max, int8_t* __restrict__ codes_out,
+                                    float* __restrict__ scales_out) {
   const int s = blockIdx.y, h = blockIdx.z;
   const int32_t L = t.len[s];
   const int32_t tok = blockIdx.x;
@@ -970,19 +977,19 @@ __global__ void export_codes_kernel(const uint16_t* __restrict__ codes, const fl
   const int64_t src = static_cast<int64_t>(h) * t_pad_max + t.pstart[s] + tok;
   const int64_t dst_row = varlen ? (static_cast<int64_t>(t.tok0[s]) + tok) * H + h
                                  : (static_cast<int64_t>(s) * H + h) * N + tok;
-  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+  for (int c = threadIdx.x; c < d_io; c += blockDim.x) {
     const float v = __bfloat162float(__ushort_as_bfloat16(codes[src * d + c]));
-    codes_out[dst_row * d + c] = static_cast<int8_t>(__float2int_rn(v));
+    codes_out[dst_row * d_io + c] = static_cast<int8_t>(__float2int_rn(v));
   }
   if (threadIdx.x == 0) scales_out[dst_row] = scales[src];
 }
 
 cudaError_t launch_export_codes(const uint16_t* codes, const float* scales, bool varlen, int32_t nseq, int32_t H,
                                 int32_t N, int32_t d, const SeqTable& t, int64_t t_pad_max, int8_t* codes_out,
-                                float* scales_out, cudaStream_t s) {
+                                float* scales_out, cudaStream_t s, int32_t d_io) {
   TraceScope tr("export_codes", s);
-  export_codes_kernel<<<dim3(N, nseq, H), 64, 0, s>>>(codes, scales, varlen, nseq, H, N, d, t, t_pad_max, codes_out,
-                                                       scales_out);
+  export_codes_kernel<<<dim3(N, nseq, H), 64, 0, s>>>(codes, scales, varlen, nseq, H, N, d, d_io > 0 ? d_io : d, t,
+                                                       t_pad_max, codes_out, scales_out);
   return cudaGetLastError();
 }
 

@@ -107,19 +107,21 @@ cudaError_t launch_kv_partials(const void* k, sl8_dtype dt, const void* v, bool 
 // no smoothing) and, with v16 set, the V exponent from v_partials (published in v_exp) and
 // write V as fp16 * 2^-v_exp.  t is read for varlen input only.  q_off > 0 (dense): q holds
 // N - q_off rows per (sequence, head), the positions q_off .. N-1; the code rows of the
-// positions before it are zero.
+// positions before it are zero.  d_io < d (head dim 32 run as 64): the inputs hold d_io
+// values per row and the code rows are zero past them; k_partials then has d_io columns;
+// v_f16: V is fp16 (copied, v_partials unused and the exponent 0), else bf16.
 cudaError_t launch_quant_qk(const void* q, const void* k, sl8_dtype dt, bool varlen, int32_t nseq, int32_t Hq,
                             int32_t Hkv, int32_t N, int32_t d, int64_t total_tokens, const SeqTable& t,
                             int64_t t_pad_max, const float* k_partials, const float* v_partials,
                             int32_t max_chunks, uint16_t* q_codes, float* q_scales, uint16_t* k_codes,
                             float* k_scales, const void* v, int32_t* v_exp, uint16_t* v16, cudaStream_t s,
-                            int32_t q_off = 0);
+                            int32_t q_off = 0, int32_t d_io = 0, bool v_f16 = false);
 cudaError_t launch_quant_rowwise(const void* x, sl8_dtype dt, int64_t rows, int32_t cols, int64_t row_stride,
                                  const float* sub_mean, int64_t rows_per_group, int8_t* q_out, float* scale_out,
                                  cudaStream_t s);
 cudaError_t launch_export_codes(const uint16_t* codes, const float* scales, bool varlen, int32_t nseq, int32_t H,
                                 int32_t N, int32_t d, const SeqTable& t, int64_t t_pad_max, int8_t* codes_out,
-                                float* scales_out, cudaStream_t s);
+                                float* scales_out, cudaStream_t s, int32_t d_io = 0);
 
 struct PrefillArgs {
   const uint16_t* q_codes;  // [Hq][t_pad][d] bf16 codes
@@ -132,6 +134,7 @@ struct PrefillArgs {
   const int32_t* v_exp;     // [nseq][Hkv] (nullable = 0)
   bool varlen;
   int32_t nseq, Hq, Hkv, N, d;
+  int32_t d_io;              // values per row of q, k, v and out (d, or 32 when head dim 32 runs as 64)
   int32_t q_off;             // dense query chunk: q and out hold positions q_off .. N-1 (N keys)
   int64_t total_tokens;
   int64_t t_pad_max;
