@@ -108,8 +108,9 @@ def test_prefill_argument_errors(lib):
     assert call(q=None) == sl8.SL8_ERR_INVALID_ARG
     assert call(q=p + 2) == sl8.SL8_ERR_INVALID_ARG           # misaligned
     assert call(Hkv=3) == sl8.SL8_ERR_INVALID_ARG             # Hq % Hkv != 0
-    assert call(d=32) == sl8.SL8_ERR_UNSUPPORTED
+    assert call(d=32) == sl8.SL8_ERR_WORKSPACE               # head dim 32 is accepted (runs as 64)
     assert call(d=96) == sl8.SL8_ERR_UNSUPPORTED
+    assert call(d=16) == sl8.SL8_ERR_UNSUPPORTED
     assert call(qk=sl8.SL8_F32) == sl8.SL8_ERR_INVALID_ARG
     assert call(odt=sl8.SL8_F16) == sl8.SL8_ERR_INVALID_ARG   # out must be V's dtype or F32
     assert call(ws=None) == sl8.SL8_ERR_WORKSPACE
