@@ -66,6 +66,8 @@ def _load():
             lib.oracle_quant_rows.argtypes = [_F32P, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
                                               ctypes.c_int64, _I8P, _F32P]
             lib.oracle_k_mean.argtypes = [_F32P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, _F32P]
+            lib.oracle_quant_groups.argtypes = [_F32P, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
+                                                ctypes.c_int64, ctypes.c_float, _I8P, _F32P, ctypes.c_void_p]
             lib.oracle_attn_prefill_head.restype = ctypes.c_int
             lib.oracle_attn_prefill_head.argtypes = [
                 _I8P, _F32P, _I8P, _F32P, _F32P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
@@ -122,6 +124,33 @@ def quant_rowwise(x, mu=None, rows_per_group=None):
     return codes, scales
 
 
+def quant_groups(x, group, tau=0.0, mu=None):
+    """Grouped symmetric int8 quantisation with outlier rows (reading R21).
+
+    x: float32 [n, d], the rows of one sequence and head in token order; mu: optional
+    float32 [d] subtracted first.  Rows form groups of ``group`` consecutive rows from
+    row 0 and share the scale max|x| / 127 over the group's non-outlier rows; with
+    tau > 0 a row whose max|x| exceeds tau times its group's lower median max|x| is an
+    outlier and keeps its own scale.  Returns (codes int8 [n, d], scales float32 [n],
+    outlier bool [n]).
+    """
+    x = _f32(x)
+    n, d = x.shape
+    if group < 1:
+        raise ValueError("group must be >= 1")
+    codes = np.zeros((n, d), np.int8)
+    scales = np.zeros(n, np.float32)
+    flags = np.zeros(n, np.uint8)
+    if n == 0:
+        return codes, scales, flags.astype(bool)
+    mu_ptr = None
+    if mu is not None:
+        mu = _f32(mu).reshape(d)
+        mu_ptr = mu.ctypes.data
+    _load().oracle_quant_groups(x, n, d, mu_ptr, int(group), float(tau), codes, scales, flags.ctypes.data)
+    return codes, scales, flags.astype(bool)
+
+
 def k_channel_mean(k):
     """Per-channel mean of token rows k [n, d] in the canonical fp32 order (reading R4)."""
     k = _f32(k)
@@ -145,7 +174,8 @@ def _seq_slices(q, k, v, cu_seqlens):
             yield s, q[a:e].transpose(1, 0, 2), k[a:e].transpose(1, 0, 2), v[a:e].transpose(1, 0, 2)
 
 
-def attn_prefill(q, k, v, causal=True, smooth_k=False, cu_seqlens=None, rows=None, want_logits=False):
+def attn_prefill(q, k, v, causal=True, smooth_k=False, cu_seqlens=None, rows=None, want_logits=False,
+                 q_group=1, k_group=1, q_outlier_ratio=0.0):
     """W8A8 INT8 attention prefill, fp64 after the int32 dot.
 
     Dense: q [B,Hq,N,d], k/v [B,Hkv,N,d], or a chunk of Nq <= Nk queries, q [B,Hq,Nq,d]
@@ -160,6 +190,9 @@ def attn_prefill(q, k, v, causal=True, smooth_k=False, cu_seqlens=None, rows=Non
       q_codes/q_scales, k_codes/k_scales (the quantised Q and smoothed K, full),
       k_mean [nseq, Hkv, d] float32 (zeros when smooth_k is off),
       logits: {(seq, hq, i): int32 [n_allowed]} when want_logits.
+    q_group / k_group > 1 or q_outlier_ratio > 0 select the grouped quantisation of
+    attn_w8a8_fwd (reading R21, ``quant_groups``) for Q and the smoothed K; the defaults
+    are the per-row quantiser.
     """
     q, k, v = _f32(q), _f32(k), _f32(v)
     lib = _load()
@@ -200,9 +233,18 @@ def attn_prefill(q, k, v, causal=True, smooth_k=False, cu_seqlens=None, rows=Non
             mu = k_channel_mean(krows) if (smooth_k and n > 0) else None
             if mu is not None:
                 k_mean[s, h] = mu
-            c, sc = quant_rowwise(krows, None if mu is None else mu[None, :], n)
+            if k_group > 1:
+                c, sc, _ = quant_groups(krows, k_group, 0.0, mu)
+            else:
+                c, sc = quant_rowwise(krows, None if mu is None else mu[None, :], n)
             kc_seq[h], ks_seq[h] = c, sc
-        qc_seq, qsc_seq = quant_rowwise(np.ascontiguousarray(qs))
+        if q_group > 1 or q_outlier_ratio > 0:
+            qc_seq = np.zeros(qs.shape, np.int8)
+            qsc_seq = np.zeros(qs.shape[:-1], np.float32)
+            for h in range(hq_n):
+                qc_seq[h], qsc_seq[h], _ = quant_groups(np.ascontiguousarray(qs[h]), q_group, q_outlier_ratio)
+        else:
+            qc_seq, qsc_seq = quant_rowwise(np.ascontiguousarray(qs))
         if varlen:
             a = int(cu[s])
             k_codes[a:a + n] = kc_seq.transpose(1, 0, 2)

@@ -23,6 +23,8 @@
  *   R9  causal is top-left aligned: key j is allowed for query i iff j <= i.
  *   R12 decode quantises q per (b, hq) row with R1/R3; V rows are s_v[t] * code.
  *   R13 split-KV uses contiguous chunks; an empty split has lse = -inf and weight 0.
+ *   R21 attn_w8a8_fwd: Q and K scales shared by groups of consecutive rows, Q outliers
+ *       keep their own scale (restated at oracle_quant_groups).
  * Everything after the int32 dot runs in fp64: logits, softmax, P.V and the LSE.
  *
  * Build: gcc -O2 -std=c11 -fopenmp -ffp-contract=off (no -ffast-math): every fp32
@@ -81,6 +83,70 @@ void oracle_quant_rows(const float* x, int64_t rows, int d, const float* mu, int
   for (int64_t r = 0; r < rows; ++r) {
     const float* m = mu ? mu + (r / rows_per_group) * (int64_t)d : NULL;
     quant_row(x + r * (int64_t)d, m, d, codes + r * (int64_t)d, scales + r);
+  }
+}
+
+/* ---------------------------------------------------------------- grouped quantisation */
+
+static int cmp_float(const void* a, const void* b) {
+  float x = *(const float*)a, y = *(const float*)b;
+  return (x > y) - (x < y);
+}
+
+/*
+ * "Attention kernels" table, attn_w8a8_fwd row ("W8A8 with per-warp quantization.
+ * Outlier-aware") and the "Quantization" table's "Q outlier detection"; the pages give
+ * no formula, so this is reading R21:
+ *   - the n rows (one sequence and head, in token order, optionally smoothed by mu)
+ *     form groups of `group` consecutive rows starting at row 0 (the last group may be
+ *     shorter); a = max|x| of each row (fp32, exact);
+ *   - with tau > 0 a row is an outlier when a > tau * med (one fp32 product), med the
+ *     lower median of its group's a values (element (cnt - 1) / 2 of the ascending
+ *     sort); an outlier keeps its own scale a / 127;
+ *   - every other row of the group takes s = (max a over the group's non-outliers) / 127,
+ *     an IEEE fp32 division, and its codes clamp(RNE(x / s), -127, 127) (R1, R3).
+ * group = 1 is the per-row quantiser.  outlier (nullable) receives one flag per row.
+ */
+void oracle_quant_groups(const float* x, int64_t n, int d, const float* mu, int64_t group, float tau,
+                         int8_t* codes, float* scales, uint8_t* outlier) {
+  for (int64_t g0 = 0; g0 < n; g0 += group) {
+    int64_t g1 = g0 + group < n ? g0 + group : n, cnt = g1 - g0;
+    float* a = (float*)malloc((size_t)cnt * sizeof(float));
+    float* sorted = (float*)malloc((size_t)cnt * sizeof(float));
+    uint8_t* out = (uint8_t*)calloc((size_t)cnt, 1);
+    for (int64_t r = g0; r < g1; ++r) {
+      float m = 0.0f;
+      for (int c = 0; c < d; ++c) {
+        float v = mu ? x[r * (int64_t)d + c] - mu[c] : x[r * (int64_t)d + c];
+        if (fabsf(v) > m) m = fabsf(v);
+      }
+      a[r - g0] = m;
+    }
+    if (tau > 0.0f) {
+      memcpy(sorted, a, (size_t)cnt * sizeof(float));
+      qsort(sorted, (size_t)cnt, sizeof(float), cmp_float);
+      float thr = tau * sorted[(cnt - 1) / 2];
+      for (int64_t i = 0; i < cnt; ++i) out[i] = a[i] > thr;
+    }
+    float inlier_max = 0.0f;
+    for (int64_t i = 0; i < cnt; ++i)
+      if (!out[i] && a[i] > inlier_max) inlier_max = a[i];
+    for (int64_t r = g0; r < g1; ++r) {
+      float s = (out[r - g0] ? a[r - g0] : inlier_max) / 127.0f;
+      scales[r] = s;
+      if (outlier) outlier[r] = out[r - g0];
+      for (int c = 0; c < d; ++c) {
+        float v = mu ? x[r * (int64_t)d + c] - mu[c] : x[r * (int64_t)d + c];
+        float t = s == 0.0f ? 0.0f : v / s;
+        float q = nearbyintf(t);
+        if (q > 127.0f) q = 127.0f;
+        if (q < -127.0f) q = -127.0f;
+        codes[r * (int64_t)d + c] = (int8_t)q;
+      }
+    }
+    free(a);
+    free(sorted);
+    free(out);
   }
 }
 
