@@ -151,6 +151,34 @@ SL8_API int sl8_attn_int8_fwd_chunk(const void* q, const void* k, const void* v,
                                     size_t workspace_bytes, void* stream);
 
 /*
+ * W8A8 prefill with grouped ("per-warp") scales and outlier-aware Q ("Attention
+ * kernels" table, attn_w8a8_fwd row: W8A8 with per-warp quantization, outlier-aware;
+ * "Quantization" table, per-row int8 row: Q outlier detection).  The pages give no
+ * formula; the reading implemented:
+ *   - the rows of each (sequence, head) form groups of G consecutive positions from
+ *     position 0 (q_group for Q, k_group for K after its channel mean); every row of a
+ *     group quantises with s = (max |x| over the group's non-outlier rows) / 127 (fp32
+ *     division) and codes RNE(x / s) clamped to +-127;
+ *   - a Q row is an outlier when max|x| > q_outlier_ratio * m (one fp32 product), m the
+ *     lower median of its group's row maxima (element (n - 1) / 2 of the ascending
+ *     sort); an outlier row keeps its own scale max|x| / 127.  q_outlier_ratio = 0
+ *     turns the test off.  K rows have no outlier test (K-smoothing handles K).
+ * q_group = k_group = 1 is sl8_attn_int8_fwd exactly.  The attention after the
+ * quantisation is that of sl8_attn_int8_fwd (exact int32 logits times the row
+ * scales), so the same kernel runs at the same speed.
+ *   q_group, k_group    powers of two, 1 .. 64 (SL8_ERR_INVALID_ARG otherwise); 32 are
+ *                       the rows one warp of the softmax covers.
+ *   q_outlier_ratio     finite, >= 0 (SL8_ERR_INVALID_ARG otherwise).
+ * Everything else (layouts, varlen, causal, head dims, dtypes, workspace from
+ * sl8_attn_int8_fwd_workspace_size, errors) as sl8_attn_int8_fwd.
+ */
+SL8_API int sl8_attn_w8a8_fwd(const void* q, const void* k, const void* v, int qk_dtype, int v_dtype, int32_t B,
+                              int32_t Hq, int32_t Hkv, int32_t N, int32_t d, const int32_t* cu_seqlens,
+                              int64_t total_tokens, int causal, int smooth_k, int32_t q_group, int32_t k_group,
+                              float q_outlier_ratio, void* out, int out_dtype, float* lse_out, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
  * Debug view of the prefill's quantisation and int32 logits (same kernels and
  * tensor-core path as sl8_attn_int8_fwd, without the mask).  Dense layout only.
  *   logits_out  device, nullable, [B][Hq][row_end - row_begin][N] int32:
@@ -165,6 +193,18 @@ SL8_API int sl8_attn_int8_qk_logits_debug(const void* q, const void* k, int qk_d
                                   int32_t N, int32_t d, int smooth_k, int32_t row_begin, int32_t row_end,
                                   int32_t* logits_out, int8_t* q_codes, float* q_scales, int8_t* k_codes,
                                   float* k_scales, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The same debug view for the grouped quantisation of sl8_attn_w8a8_fwd (q_group,
+ * k_group and q_outlier_ratio as there); the codes, scales and logits are those the
+ * sl8_attn_w8a8_fwd attention consumes.
+ */
+SL8_API int sl8_attn_w8a8_qk_logits_debug(const void* q, const void* k, int qk_dtype, int32_t B, int32_t Hq,
+                                          int32_t Hkv, int32_t N, int32_t d, int smooth_k, int32_t q_group,
+                                          int32_t k_group, float q_outlier_ratio, int32_t row_begin,
+                                          int32_t row_end, int32_t* logits_out, int8_t* q_codes, float* q_scales,
+                                          int8_t* k_codes, float* k_scales, void* workspace,
+                                          size_t workspace_bytes, void* stream);
 
 /*
  * Split-KV decode over an int8 KV cache ("Attention kernels" table, attn_decode,

@@ -119,6 +119,35 @@ def test_prefill_argument_errors(lib):
     assert call(N=0) == sl8.SL8_OK
 
 
+def test_w8a8_argument_errors(lib):
+    keep, p = _host_buf(1 << 12)
+    f = lib.sl8_attn_w8a8_fwd
+    # (..., causal, smooth, q_group, k_group, ratio, out, out_dtype, lse, ws, ws_bytes, stream)
+    base = [p, p, p, sl8.SL8_BF16, sl8.SL8_BF16, 1, 4, 2, 128, 128, None, 0, 1, 1, 32, 32, 4.0, p, sl8.SL8_BF16,
+            None, p, 16, None]
+
+    def call(**kw):
+        args = list(base)
+        idx = dict(gq=14, gk=15, tau=16, wsb=21)
+        for k, val in kw.items():
+            args[idx[k]] = val
+        return f(*args)
+
+    assert call() == sl8.SL8_ERR_WORKSPACE                    # valid groups reach the workspace check
+    for g in (0, 3, 48, 128, -32):
+        assert call(gq=g) == sl8.SL8_ERR_INVALID_ARG
+        assert call(gk=g) == sl8.SL8_ERR_INVALID_ARG
+    for g in (1, 2, 64):
+        assert call(gq=g, gk=g) == sl8.SL8_ERR_WORKSPACE
+    assert call(tau=-1.0) == sl8.SL8_ERR_INVALID_ARG
+    assert call(tau=float("nan")) == sl8.SL8_ERR_INVALID_ARG
+    assert call(tau=float("inf")) == sl8.SL8_ERR_INVALID_ARG
+    assert call(tau=0.0) == sl8.SL8_ERR_WORKSPACE
+    d = lib.sl8_attn_w8a8_qk_logits_debug
+    assert d(p, p, sl8.SL8_BF16, 1, 4, 2, 128, 128, 1, 5, 32, 4.0, 0, 1, p, None, None, None, None, p, 16,
+             None) == sl8.SL8_ERR_INVALID_ARG
+
+
 def test_decode_and_quant_argument_errors(lib):
     keep, p = _host_buf(1 << 12)
     f = lib.sl8_attn_int8_decode_splitkv

@@ -71,6 +71,10 @@ _SIGNATURES = {
                                        _INT, _P, _P, _SZ, _P]),
     "sl8_attn_int8_qk_logits_debug": (_INT, [_P, _P, _INT, _I32, _I32, _I32, _I32, _I32, _INT, _I32, _I32, _P, _P,
                                              _P, _P, _P, _P, _SZ, _P]),
+    "sl8_attn_w8a8_fwd": (_INT, [_P, _P, _P, _INT, _INT, _I32, _I32, _I32, _I32, _I32, _P, _I64, _INT, _INT, _I32,
+                                 _I32, ctypes.c_float, _P, _INT, _P, _P, _SZ, _P]),
+    "sl8_attn_w8a8_qk_logits_debug": (_INT, [_P, _P, _INT, _I32, _I32, _I32, _I32, _I32, _INT, _I32, _I32,
+                                             ctypes.c_float, _I32, _I32, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "sl8_attn_decode_num_splits": (_I32, [_I32, _I32, _I32, _I32, _I32]),
     "sl8_attn_decode_split_size": (_I32, [_I32, _I32, _I32, _I32, _I32]),
     "sl8_attn_int8_decode_splitkv": (_INT, [_P, _INT, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P,
@@ -209,6 +213,24 @@ def attn_int8_fwd(q, k, v, causal=True, smooth_k=True, cu_seqlens=None, max_seql
     cu_seqlens int32 [B+1] (CUDA) and max_seqlen (host int >= every length).
     Returns out (q's layout, dtype v.dtype or out_dtype=float32) and, with
     return_lse, the fp32 log-sum-exp per query row."""
+    return _prefill("sl8_attn_int8_fwd", (), q, k, v, causal, smooth_k, cu_seqlens, max_seqlen, out_dtype,
+                    return_lse, workspace, out, lse)
+
+
+def attn_w8a8_fwd(q, k, v, causal=True, smooth_k=True, q_group=32, k_group=32, q_outlier_ratio=4.0,
+                  cu_seqlens=None, max_seqlen=None, out_dtype=None, return_lse=False, workspace=None, out=None,
+                  lse=None):
+    """W8A8 prefill with grouped scales: rows of a (sequence, head) share one scale per
+    group of q_group (Q) / k_group (K) consecutive positions; a Q row above
+    q_outlier_ratio times its group's lower median row maximum keeps its own scale
+    (0 turns that off).  Groups are powers of two up to 64; q_group = k_group = 1 is
+    attn_int8_fwd.  Layouts and the rest as attn_int8_fwd."""
+    return _prefill("sl8_attn_w8a8_fwd", (int(q_group), int(k_group), float(q_outlier_ratio)), q, k, v, causal,
+                    smooth_k, cu_seqlens, max_seqlen, out_dtype, return_lse, workspace, out, lse)
+
+
+def _prefill(fn, extra, q, k, v, causal, smooth_k, cu_seqlens, max_seqlen, out_dtype, return_lse, workspace, out,
+             lse):
     _need_cuda(q, k, v, cu_seqlens, workspace)
     if cu_seqlens is None:
         B, Hq, N, d = q.shape
@@ -231,10 +253,10 @@ def attn_int8_fwd(q, k, v, causal=True, smooth_k=True, cu_seqlens=None, max_seql
     ws_bytes = prefill_workspace_bytes(B, Hq, Hkv, N, d, T)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
-    _check(lib().sl8_attn_int8_fwd(_ptr(q), _ptr(k), _ptr(v), _dt(q), _dt(v), B, Hq, Hkv, N, d, _ptr(cu_seqlens), T,
-                                   int(bool(causal)), int(bool(smooth_k)), _ptr(out), _dt(out),
-                                   _ptr(lse) if return_lse else None, _ptr(workspace), workspace.numel(),
-                                   _stream(q.device)), "sl8_attn_int8_fwd")
+    _check(getattr(lib(), fn)(_ptr(q), _ptr(k), _ptr(v), _dt(q), _dt(v), B, Hq, Hkv, N, d, _ptr(cu_seqlens), T,
+                              int(bool(causal)), int(bool(smooth_k)), *extra, _ptr(out), _dt(out),
+                              _ptr(lse) if return_lse else None, _ptr(workspace), workspace.numel(),
+                              _stream(q.device)), fn)
     return (out, lse) if return_lse else out
 
 
@@ -261,10 +283,11 @@ def attn_int8_fwd_chunk(q, k, v, causal=True, smooth_k=True, out_dtype=None, ret
     return (out, lse) if return_lse else out
 
 
-def attn_int8_qk_logits_debug(q, k, smooth_k=True, row_begin=0, row_end=None, want_codes=True):
+def attn_int8_qk_logits_debug(q, k, smooth_k=True, row_begin=0, row_end=None, want_codes=True, groups=None):
     """Exact int32 logits of the prefill tensor-core path for query rows
     [row_begin, row_end) against every key (dense only), plus the int8 codes and
-    fp32 scales of Q and (smoothed) K.  Returns a dict."""
+    fp32 scales of Q and (smoothed) K.  groups = (q_group, k_group, q_outlier_ratio)
+    selects the grouped quantisation of attn_w8a8_fwd.  Returns a dict."""
     _need_cuda(q, k)
     B, Hq, N, d = q.shape
     Hkv = k.shape[1]
@@ -279,11 +302,15 @@ def attn_int8_qk_logits_debug(q, k, smooth_k=True, row_begin=0, row_end=None, wa
                    k_scales=torch.empty((B, Hkv, N), dtype=torch.float32, device=dev))
     ws_bytes = prefill_workspace_bytes(B, Hq, Hkv, N, d, 0)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-    _check(lib().sl8_attn_int8_qk_logits_debug(_ptr(q), _ptr(k), _dt(q), B, Hq, Hkv, N, d, int(bool(smooth_k)),
-                                               row_begin, row_end, _ptr(logits), _ptr(res.get("q_codes")),
-                                               _ptr(res.get("q_scales")), _ptr(res.get("k_codes")),
-                                               _ptr(res.get("k_scales")), _ptr(ws), ws.numel(), _stream(dev)),
-           "sl8_attn_int8_qk_logits_debug")
+    tail = (row_begin, row_end, _ptr(logits), _ptr(res.get("q_codes")), _ptr(res.get("q_scales")),
+            _ptr(res.get("k_codes")), _ptr(res.get("k_scales")), _ptr(ws), ws.numel(), _stream(dev))
+    if groups is None:
+        _check(lib().sl8_attn_int8_qk_logits_debug(_ptr(q), _ptr(k), _dt(q), B, Hq, Hkv, N, d, int(bool(smooth_k)),
+                                                   *tail), "sl8_attn_int8_qk_logits_debug")
+    else:
+        g = (int(groups[0]), int(groups[1]), float(groups[2]))
+        _check(lib().sl8_attn_w8a8_qk_logits_debug(_ptr(q), _ptr(k), _dt(q), B, Hq, Hkv, N, d, int(bool(smooth_k)),
+                                                   *g, *tail), "sl8_attn_w8a8_qk_logits_debug")
     return res
 
 

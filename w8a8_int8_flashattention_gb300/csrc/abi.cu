@@ -326,7 +326,7 @@ static int prefill_prepare(const void* q, const void* k, const void* v, int qk_d
                            int32_t Hq, int32_t Hkv, int32_t N, int32_t d, const int32_t* cu_seqlens,
                            int64_t total_tokens, int smooth_k, void* workspace, size_t workspace_bytes,
                            cudaStream_t s, bool want_table, PrefillWorkspace* plan, SeqTable* table,
-                           int32_t q_off = 0) {
+                           int32_t q_off = 0, const QuantGroups& groups = QuantGroups()) {
   const bool varlen = cu_seqlens != nullptr;
   const PrefillWorkspace p = plan_prefill_workspace(B, Hq, Hkv, N, d, varlen ? total_tokens : 0, varlen);
   SL8_CHECK(workspace && aligned16(workspace) && workspace_bytes >= p.total, SL8_ERR_WORKSPACE);
@@ -354,7 +354,7 @@ static int prefill_prepare(const void* q, const void* k, const void* v, int qk_d
                              reinterpret_cast<uint16_t*>(ws + p.k_codes), reinterpret_cast<float*>(ws + p.k_scales),
                              convert_v ? v : nullptr, convert_v ? reinterpret_cast<int32_t*>(ws + p.v_exp) : nullptr,
                              convert_v ? reinterpret_cast<uint16_t*>(ws + p.v16) : nullptr, s, q_off, d,
-                             v_dtype == SL8_F16));
+                             v_dtype == SL8_F16, groups));
   *plan = p;
   *table = t;
   return SL8_OK;
@@ -365,7 +365,7 @@ static int prefill_prepare(const void* q, const void* k, const void* v, int qk_d
 static int prefill_run(const void* q, const void* k, const void* v, int qk_dtype, int v_dtype, int32_t B, int32_t Hq,
                        int32_t Hkv, int32_t N, int32_t d, const int32_t* cu_seqlens, int64_t total_tokens, int causal,
                        int smooth_k, void* out, int out_dtype, float* lse_out, void* workspace, size_t workspace_bytes,
-                       void* stream, int32_t q_off) {
+                       void* stream, int32_t q_off, const QuantGroups& groups = QuantGroups()) {
   int rc = validate_prefill(q, k, qk_dtype, B, Hq, Hkv, N, d);
   if (rc != SL8_OK) return rc;
   SL8_CHECK(v && out && aligned16(v) && aligned16(out), SL8_ERR_INVALID_ARG);
@@ -379,7 +379,7 @@ static int prefill_run(const void* q, const void* k, const void* v, int qk_dtype
   PrefillWorkspace p;
   SeqTable t;
   rc = prefill_prepare(q, k, v, qk_dtype, v_dtype, B, Hq, Hkv, N, d, cu_seqlens, total_tokens, smooth_k, workspace,
-                       workspace_bytes, s, false, &p, &t, q_off);
+                       workspace_bytes, s, false, &p, &t, q_off, groups);
   if (rc != SL8_OK) return rc;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   PrefillArgs a{};
@@ -437,10 +437,33 @@ int sl8_attn_int8_fwd_chunk(const void* q, const void* k, const void* v, int qk_
                      lse_out, workspace, workspace_bytes, stream, Nk - Nq);
 }
 
-int sl8_attn_int8_qk_logits_debug(const void* q, const void* k, int qk_dtype, int32_t B, int32_t Hq, int32_t Hkv,
-                                  int32_t N, int32_t d, int smooth_k, int32_t row_begin, int32_t row_end,
-                                  int32_t* logits_out, int8_t* q_codes, float* q_scales, int8_t* k_codes,
-                                  float* k_scales, void* workspace, size_t workspace_bytes, void* stream) {
+// Group sizes: powers of two from 1 to 64 (a group never leaves one 64-row CTA of the
+// quantiser); the outlier ratio: finite and >= 0.
+static int make_groups(int32_t q_group, int32_t k_group, float q_outlier_ratio, QuantGroups* g) {
+  auto pow2 = [](int32_t x) { return x >= 1 && x <= 64 && (x & (x - 1)) == 0; };
+  SL8_CHECK(pow2(q_group) && pow2(k_group), SL8_ERR_INVALID_ARG);
+  SL8_CHECK(q_outlier_ratio >= 0.0f && q_outlier_ratio <= 3.0e38f, SL8_ERR_INVALID_ARG);  // also rejects NaN
+  g->q_group = q_group;
+  g->k_group = k_group;
+  g->q_tau = q_outlier_ratio;
+  return SL8_OK;
+}
+
+int sl8_attn_w8a8_fwd(const void* q, const void* k, const void* v, int qk_dtype, int v_dtype, int32_t B, int32_t Hq,
+                      int32_t Hkv, int32_t N, int32_t d, const int32_t* cu_seqlens, int64_t total_tokens,
+                      int causal, int smooth_k, int32_t q_group, int32_t k_group, float q_outlier_ratio, void* out,
+                      int out_dtype, float* lse_out, void* workspace, size_t workspace_bytes, void* stream) {
+  QuantGroups g;
+  const int rc = make_groups(q_group, k_group, q_outlier_ratio, &g);
+  if (rc != SL8_OK) return rc;
+  return prefill_run(q, k, v, qk_dtype, v_dtype, B, Hq, Hkv, N, d, cu_seqlens, total_tokens, causal, smooth_k, out,
+                     out_dtype, lse_out, workspace, workspace_bytes, stream, 0, g);
+}
+
+static int qk_logits_debug(const void* q, const void* k, int qk_dtype, int32_t B, int32_t Hq, int32_t Hkv, int32_t N,
+                           int32_t d, int smooth_k, int32_t row_begin, int32_t row_end, int32_t* logits_out,
+                           int8_t* q_codes, float* q_scales, int8_t* k_codes, float* k_scales, void* workspace,
+                           size_t workspace_bytes, void* stream, const QuantGroups& groups) {
   int rc = validate_prefill(q, k, qk_dtype, B, Hq, Hkv, N, d);
   if (rc != SL8_OK) return rc;
   SL8_CHECK(0 <= row_begin && row_begin <= row_end && row_end <= N, SL8_ERR_INVALID_ARG);
@@ -451,7 +474,7 @@ int sl8_attn_int8_qk_logits_debug(const void* q, const void* k, int qk_dtype, in
   PrefillWorkspace p;
   SeqTable t;
   rc = prefill_prepare(q, k, nullptr, qk_dtype, qk_dtype, B, Hq, Hkv, N, d, nullptr, 0, smooth_k, workspace,
-                       workspace_bytes, s, true, &p, &t);
+                       workspace_bytes, s, true, &p, &t, 0, groups);
   if (rc != SL8_OK) return rc;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int32_t dc = compute_dim(d);
@@ -497,6 +520,26 @@ int sl8_attn_int8_qk_logits_debug(const void* q, const void* k, int qk_dtype, in
     SL8_LAUNCH(launch_prefill(a, s));
   }
   return SL8_OK;
+}
+
+int sl8_attn_int8_qk_logits_debug(const void* q, const void* k, int qk_dtype, int32_t B, int32_t Hq, int32_t Hkv,
+                                  int32_t N, int32_t d, int smooth_k, int32_t row_begin, int32_t row_end,
+                                  int32_t* logits_out, int8_t* q_codes, float* q_scales, int8_t* k_codes,
+                                  float* k_scales, void* workspace, size_t workspace_bytes, void* stream) {
+  return qk_logits_debug(q, k, qk_dtype, B, Hq, Hkv, N, d, smooth_k, row_begin, row_end, logits_out, q_codes,
+                         q_scales, k_codes, k_scales, workspace, workspace_bytes, stream, QuantGroups());
+}
+
+int sl8_attn_w8a8_qk_logits_debug(const void* q, const void* k, int qk_dtype, int32_t B, int32_t Hq, int32_t Hkv,
+                                  int32_t N, int32_t d, int smooth_k, int32_t q_group, int32_t k_group,
+                                  float q_outlier_ratio, int32_t row_begin, int32_t row_end, int32_t* logits_out,
+                                  int8_t* q_codes, float* q_scales, int8_t* k_codes, float* k_scales,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  QuantGroups g;
+  const int rc = make_groups(q_group, k_group, q_outlier_ratio, &g);
+  if (rc != SL8_OK) return rc;
+  return qk_logits_debug(q, k, qk_dtype, B, Hq, Hkv, N, d, smooth_k, row_begin, row_end, logits_out, q_codes,
+                         q_scales, k_codes, k_scales, workspace, workspace_bytes, stream, g);
 }
 
 // The split plan.  split_size_for(Lmax, S, d) = ceil(Lmax / S) rounded up to a whole

@@ -655,6 +655,11 @@ struct QuantQK {
   float* k_scales;
   const void* v;            // bf16 V when v16 is set
   uint16_t* v16;
+  // grouped scales (attn_w8a8_fwd): rows [g*G, (g+1)*G) of a sequence share one scale,
+  // G a power of two <= 64; Q rows above q_tau x their group's lower median max|x| keep
+  // their own (q_tau 0: no outlier test).  Only the kGroups instantiation reads these.
+  int32_t q_group, k_group;
+  float q_tau;
 };
 
 template <int EPL>
@@ -669,9 +674,11 @@ __device__ __forceinline__ void store_vec16(uint16_t* p, const uint16_t (&h)[EPL
 }
 
 // Eight lanes per row (EPL = D / 8 values each, 16-byte accesses), four rows per warp
-// instruction.
-template <sl8_dtype DT, int D>
-__global__ void __launch_bounds__(kQuantWarps * 32, D == 256 ? 2 : 4) quant_qk_kernel(const QuantQK a, DeviceStatus* st) {
+// instruction.  kGroups: scales shared by groups of rows (see QuantQK), formed in shared
+// memory from the CTA's 64 row maxima before any code is written.
+template <sl8_dtype DT, int D, bool kGroups>
+__global__ void __launch_bounds__(kQuantWarps * 32, D == 256 ? (kGroups ? 1 : 2) : (kGroups ? 3 : 4))
+    quant_qk_kernel(const QuantQK a, DeviceStatus* st) {
   constexpr int LPR = 8, EPL = D / LPR, NV = EPL / 8, RPP = 32 / LPR, P = kQuantRowsPerWarp / RPP;
   // K heads first: their CTAs also form the K mean and the V exponent, so they start
   // in the first wave and the Q CTAs fill in behind them
@@ -820,10 +827,8 @@ __global__ void __launch_bounds__(kQuantWarps * 32, D == 256 ? 2 : 4) quant_qk_k
       }
     }
   }
-#pragma unroll
-  for (int p = 0; p < P; ++p) {
-    const int64_t pr = row0 + p * RPP + rsub;
-    float v[EPL];
+  // the lane's EPL values of pass p's row, widened (and smoothed for K)
+  auto row_values = [&](int p, float (&v)[EPL]) {
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
       const uint32_t ww[4] = {xw[p][j].x, xw[p][j].y, xw[p][j].z, xw[p][j].w};
@@ -842,13 +847,85 @@ __global__ void __launch_bounds__(kQuantWarps * 32, D == 256 ? 2 : 4) quant_qk_k
         q_upk2(q_sub2(q_pk2(v[e + 2], v[e + 3]), q_pk2(m4.z, m4.w)), v[e + 2], v[e + 3]);
       }
     }
+  };
+  // max|x| of pass p's row, reduced over its eight lanes
+  auto row_absmax = [&](const float (&v)[EPL]) {
     float am = 0.0f;
 #pragma unroll
     for (int e = 0; e < EPL; e += 2) am = fmaxf(am, fmaxf(fabsf(v[e]), fabsf(v[e + 1])));
 #pragma unroll
     for (int o = LPR / 2; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-    if (!live[p]) continue;
-    const float scale = valid[p] ? __fdiv_rn(am, 127.0f) : 0.0f;
+    return am;
+  };
+  float grp_scale[P];
+  if constexpr (kGroups) {
+    // Row r of the CTA (0..63) is sequence position (cta_row0 - cta_pstart) + r, and
+    // cta_row0 - cta_pstart is a multiple of 64, so a group of G <= 64 rows is the
+    // CTA-local range [r & ~(G-1), +G).  Rows outside the sequence (or before a query
+    // chunk) take no part: a group's median and maximum run over its valid rows.
+    constexpr int kRows = kQuantWarps * kQuantRowsPerWarp;
+    __shared__ float s_am[kRows], s_med[kRows], s_sc[kRows];
+    __shared__ bool s_ok[kRows];
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      float v[EPL];
+      row_values(p, v);
+      const float am = row_absmax(v);
+      const int r = warp * kQuantRowsPerWarp + p * RPP + rsub;
+      if (part == 0) {
+        s_am[r] = valid[p] ? am : 0.0f;
+        s_ok[r] = valid[p];
+      }
+    }
+    __syncthreads();
+    const int G = is_k ? a.k_group : a.q_group;
+    const float tau = is_k ? 0.0f : a.q_tau;
+    const int r = threadIdx.x, g0 = r & ~(G - 1);
+    if (tau > 0.0f && r < kRows && s_ok[r]) {
+      // lower median: the valid row of rank (n - 1) / 2, ties broken by row index
+      const float m = s_am[r];
+      int n = 0, rank = 0;
+      for (int i = g0; i < g0 + G; ++i) {
+        if (!s_ok[i]) continue;
+        ++n;
+        const float mi = s_am[i];
+        rank += (mi < m || (mi == m && i < r)) ? 1 : 0;
+      }
+      if (rank == (n - 1) / 2) s_med[g0] = m;
+    }
+    __syncthreads();
+    if (r < kRows) {
+      float sc = 0.0f;
+      if (s_ok[r]) {
+        const float thr = tau > 0.0f ? __fmul_rn(tau, s_med[g0]) : INFINITY;
+        float top = s_am[r];
+        if (!(top > thr)) {  // an inlier: the largest inlier maximum of the group
+          top = 0.0f;
+          for (int i = g0; i < g0 + G; ++i)
+            if (s_ok[i] && !(s_am[i] > thr)) top = fmaxf(top, s_am[i]);
+        }
+        sc = __fdiv_rn(top, 127.0f);
+      }
+      s_sc[r] = sc;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int p = 0; p < P; ++p) grp_scale[p] = s_sc[warp * kQuantRowsPerWarp + p * RPP + rsub];
+  }
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+    const int64_t pr = row0 + p * RPP + rsub;
+    float v[EPL];
+    row_values(p, v);
+    float scale;
+    if constexpr (kGroups) {
+      if (!live[p]) continue;
+      scale = grp_scale[p];
+    } else {
+      const float am = row_absmax(v);
+      if (!live[p]) continue;
+      scale = valid[p] ? __fdiv_rn(am, 127.0f) : 0.0f;
+    }
     const float rs = scale == 0.0f ? 0.0f : __frcp_rn(scale);
     uint16_t* crow = codes + (static_cast<int64_t>(h) * a.t_pad_max + pr) * D + part * EPL;
     // two elements per packed instruction: y = x * rs, c = RNE(y) (see quant_code_rcp;
@@ -894,15 +971,15 @@ __global__ void __launch_bounds__(kQuantWarps * 32, D == 256 ? 2 : 4) quant_qk_k
   }
 }
 
-template <sl8_dtype DT>
+template <sl8_dtype DT, bool kGroups>
 static cudaError_t launch_quant_qk_dt(const QuantQK& a, int32_t d, int32_t n_heads, cudaStream_t s) {
   const int64_t rows_per_cta = kQuantWarps * kQuantRowsPerWarp;
   const dim3 grid(static_cast<unsigned>((a.t_pad_max + rows_per_cta - 1) / rows_per_cta), n_heads);
   DeviceStatus* st = device_status_ptr();
   switch (d) {
-    case 64: return launch_pdl(quant_qk_kernel<DT, 64>, grid, dim3(kQuantWarps * 32), 0, s, a, st);
-    case 128: return launch_pdl(quant_qk_kernel<DT, 128>, grid, dim3(kQuantWarps * 32), 0, s, a, st);
-    default: return launch_pdl(quant_qk_kernel<DT, 256>, grid, dim3(kQuantWarps * 32), 0, s, a, st);
+    case 64: return launch_pdl(quant_qk_kernel<DT, 64, kGroups>, grid, dim3(kQuantWarps * 32), 0, s, a, st);
+    case 128: return launch_pdl(quant_qk_kernel<DT, 128, kGroups>, grid, dim3(kQuantWarps * 32), 0, s, a, st);
+    default: return launch_pdl(quant_qk_kernel<DT, 256, kGroups>, grid, dim3(kQuantWarps * 32), 0, s, a, st);
   }
 }
 
@@ -911,13 +988,16 @@ cudaError_t launch_quant_qk(const void* q, const void* k, sl8_dtype dt, bool var
                             int64_t t_pad_max, const float* k_partials, const float* v_partials,
                             int32_t max_chunks, uint16_t* q_codes, float* q_scales, uint16_t* k_codes,
                             float* k_scales, const void* v, int32_t* v_exp, uint16_t* v16, cudaStream_t s,
-                            int32_t q_off, int32_t d_io, bool v_f16) {
+                            int32_t q_off, int32_t d_io, bool v_f16, const QuantGroups& groups) {
   QuantQK a{q, k, varlen, nseq, Hq, Hkv, N, q_off, d_io > 0 ? d_io : d, v_f16, total_tokens, t, t_pad_max, k_partials,
             v_partials, max_chunks, v_exp,
-            q_codes, q_scales, k_codes, k_scales, v, v16};
+            q_codes, q_scales, k_codes, k_scales, v, v16, groups.q_group, groups.k_group, groups.q_tau};
   TraceScope tr("quant_qk", s);
-  return dt == SL8_BF16 ? launch_quant_qk_dt<SL8_BF16>(a, d, Hq + Hkv, s)
-                        : launch_quant_qk_dt<SL8_F16>(a, d, Hq + Hkv, s);
+  if (groups.q_group > 1 || groups.k_group > 1 || groups.q_tau > 0.0f)
+    return dt == SL8_BF16 ? launch_quant_qk_dt<SL8_BF16, true>(a, d, Hq + Hkv, s)
+                          : launch_quant_qk_dt<SL8_F16, true>(a, d, Hq + Hkv, s);
+  return dt == SL8_BF16 ? launch_quant_qk_dt<SL8_BF16, false>(a, d, Hq + Hkv, s)
+                        : launch_quant_qk_dt<SL8_F16, false>(a, d, Hq + Hkv, s);
 }
 
 // ---------------------------------------------------------------- generic rowwise int8

@@ -110,12 +110,18 @@ cudaError_t launch_kv_partials(const void* k, sl8_dtype dt, const void* v, bool 
 // positions before it are zero.  d_io < d (head dim 32 run as 64): the inputs hold d_io
 // values per row and the code rows are zero past them; k_partials then has d_io columns;
 // v_f16: V is fp16 (copied, v_partials unused and the exponent 0), else bf16.
+// Grouped scales for attn_w8a8_fwd (all 1 / 0: per-row scales, the attn_int8_fwd path).
+struct QuantGroups {
+  int32_t q_group = 1, k_group = 1;  // rows per shared scale, powers of two <= 64
+  float q_tau = 0.0f;                // Q outlier ratio against the group's lower median; 0: none
+};
 cudaError_t launch_quant_qk(const void* q, const void* k, sl8_dtype dt, bool varlen, int32_t nseq, int32_t Hq,
                             int32_t Hkv, int32_t N, int32_t d, int64_t total_tokens, const SeqTable& t,
                             int64_t t_pad_max, const float* k_partials, const float* v_partials,
                             int32_t max_chunks, uint16_t* q_codes, float* q_scales, uint16_t* k_codes,
                             float* k_scales, const void* v, int32_t* v_exp, uint16_t* v16, cudaStream_t s,
-                            int32_t q_off = 0, int32_t d_io = 0, bool v_f16 = false);
+                            int32_t q_off = 0, int32_t d_io = 0, bool v_f16 = false,
+                            const QuantGroups& groups = QuantGroups());
 cudaError_t launch_quant_rowwise(const void* x, sl8_dtype dt, int64_t rows, int32_t cols, int64_t row_stride,
                                  const float* sub_mean, int64_t rows_per_group, int8_t* q_out, float* scale_out,
                                  cudaStream_t s);
