@@ -11,8 +11,9 @@ the decode KV GB/s sits in `decode`, and `paged_decode` repeats the decode over 
 paged k8v8 cache (64-token pages in a seeded random order) in a loop of its own after
 the timed steps, `decode_f16v` the decode with an fp16 V cache (int8 K), and
 `prefill_chunk` the prefill's last 1024 positions as a query chunk (chunked prefill,
-bottom-right causal), and `decode_verify` the decode with 4 chained draft queries per
-sequence (speculative verify).  Inputs are resident in HBM when the timed
+bottom-right causal), `prefill_w8a8` the prefill through attn_w8a8_fwd (scales per 32
+positions, outlier-aware Q), and `decode_verify` the decode with 4 chained draft
+queries per sequence (speculative verify).  Inputs are resident in HBM when the timed
 region starts (the timed steps carry no per-launch instrumentation: per-kernel times
 come from a separate traced pass); L2 is flushed before every step, outside the timed
 events (a 256 MB
@@ -345,6 +346,10 @@ def run_ours(args, world, rank, local):
                                                 args.warmup, world)
     ch_ops = chunk_ops(wp, CHUNK_Q)
     ch_tflops = ch_ops / (ch_attn_ms * 1e-3) / 1e12
+    # ---- the same prefill with grouped ("per-warp") scales and outlier-aware Q
+    w8_ms, w8_quant_ms, w8_attn_ms, w8_steps = measure_w8a8(sl8, wp, qd, kd, vd, stream, flush, flush_sink,
+                                                            args.steps, args.warmup, world)
+    w8_tflops = ops / (w8_attn_ms * 1e-3) / 1e12
     # ---- the same decode with an fp16 V cache
     fv_ms, fv_split_ms, fv_steps = measure_f16v(sl8, W, wd, kc, ks, lens, qdec, seq, stream, flush, flush_sink,
                                                 args.steps, args.warmup, world)
@@ -410,6 +415,14 @@ def run_ours(args, world, rank, local):
                           "config": f"the decode workload with {VERIFY_T} chained draft queries per sequence "
                                     "(speculative verify), split kernel + combine; GB/s counts the cache once, "
                                     f"the kernel reads it once per draft query ({VERIFY_T} times)"},
+        "prefill_w8a8": {"value": ops * world / (w8_ms * 1e-3) / 1e12, "unit": "TOPS", "ms": w8_ms,
+                         "steps": w8_steps, "quant_qk_ms": w8_quant_ms,
+                         "config": f"the prefill workload through attn_w8a8_fwd: Q and K scales per {W8A8_GROUP} "
+                                   f"positions, Q rows above {W8A8_RATIO} x their group's median maximum keep "
+                                   "their own, L2 flushed before every step",
+                         "roofline": {"bound": "tensor", "achieved": w8_tflops, "peak": peaks["bf16_tflops"],
+                                      "unit": "TFLOP/s", "frac": w8_tflops / peaks["bf16_tflops"], "traffic": None,
+                                      "kernel": "prefill_attn (w8a8)", "peak_source": peaks["source"]}},
         "prefill_chunk": {"value": ch_ops * world / (ch_ms * 1e-3) / 1e12, "unit": "TOPS", "ms": ch_ms,
                           "steps": ch_steps, "ops": ch_ops,
                           "config": f"the prefill workload's last {CHUNK_Q} positions as a query chunk against "
@@ -554,6 +567,38 @@ def measure_chunk(sl8, wp, qd, kd, vd, stream, flush, flush_sink, steps, warmup,
     c, attn_ms = trace.get("prefill_attn", (0, 0.0))
     return ms, (attn_ms / c if c else float("nan")), n
 
+
+def measure_w8a8(sl8, wp, qd, kd, vd, stream, flush, flush_sink, steps, warmup, world):
+    """The prefill workload through attn_w8a8_fwd (grouped scales, outlier-aware Q): the
+    whole step, and the quantiser and attention kernels from the traced pass."""
+    import torch
+    ws = torch.empty(sl8.prefill_workspace_bytes(wp.B, wp.Hq, wp.Hkv, wp.N, wp.d), dtype=torch.uint8, device=qd.device)
+    out = torch.empty_like(qd)
+
+    def step(ev=None):
+        flush.zero_()
+        flush_sink.copy_(flush.view(torch.int64).sum())
+        if ev:
+            ev[0].record(stream)
+        sl8.attn_w8a8_fwd(qd, kd, vd, causal=True, smooth_k=True, q_group=W8A8_GROUP, k_group=W8A8_GROUP,
+                          q_outlier_ratio=W8A8_RATIO, workspace=ws, out=out)
+        if ev:
+            ev[1].record(stream)
+
+    n, ms, trace = timed_then_traced(sl8, step, qd.device, steps, warmup)
+    st, site = sl8.last_device_status(qd.device)
+    if st != sl8.SL8_OK:
+        raise RuntimeError(f"device status {st} at {site} during the w8a8 prefill")
+    ms = max_over_ranks(ms, world)
+    per = {}
+    for name in ("quant_qk", "prefill_attn"):
+        c, t = trace.get(name, (0, 0.0))
+        per[name] = t / c if c else float("nan")
+    return ms, per["quant_qk"], per["prefill_attn"], n
+
+
+W8A8_GROUP = 32     # positions per shared scale in the w8a8 line (the rows of one softmax warp)
+W8A8_RATIO = 4.0    # its Q outlier ratio
 
 VERIFY_T = 4   # draft tokens per sequence of the verify line
 

@@ -864,50 +864,69 @@ __global__ void __launch_bounds__(kQuantWarps * 32, D == 256 ? (kGroups ? 1 : 2)
     // CTA-local range [r & ~(G-1), +G).  Rows outside the sequence (or before a query
     // chunk) take no part: a group's median and maximum run over its valid rows.
     constexpr int kRows = kQuantWarps * kQuantRowsPerWarp;
-    __shared__ float s_am[kRows], s_med[kRows], s_sc[kRows];
-    __shared__ bool s_ok[kRows];
+    static_assert(kRows * 4 == kQuantWarps * 32, "four threads per row in the group stage");
+    // s_am: max|x| of each row, -1 for rows that take no part
+    __shared__ __align__(16) float s_am[kRows];
+    __shared__ float s_med[kRows], s_sc[kRows];
 #pragma unroll
     for (int p = 0; p < P; ++p) {
       float v[EPL];
       row_values(p, v);
       const float am = row_absmax(v);
-      const int r = warp * kQuantRowsPerWarp + p * RPP + rsub;
-      if (part == 0) {
-        s_am[r] = valid[p] ? am : 0.0f;
-        s_ok[r] = valid[p];
-      }
+      if (part == 0) s_am[warp * kQuantRowsPerWarp + p * RPP + rsub] = valid[p] ? am : -1.0f;
     }
     __syncthreads();
     const int G = is_k ? a.k_group : a.q_group;
     const float tau = is_k ? 0.0f : a.q_tau;
-    const int r = threadIdx.x, g0 = r & ~(G - 1);
-    if (tau > 0.0f && r < kRows && s_ok[r]) {
-      // lower median: the valid row of rank (n - 1) / 2, ties broken by row index
-      const float m = s_am[r];
+    // four consecutive lanes per row r, each scanning 16 of the CTA's 64 rows (in r's
+    // group or not, decided per candidate), then combining over the four lanes
+    const int r = threadIdx.x >> 2, j = threadIdx.x & 3, g0 = r & ~(G - 1);
+    const float m = s_am[r];
+    // the lane's 16 candidates, four at a time
+    auto cands = [&](int i4, float (&c)[4]) {
+      const float4 c4 = *reinterpret_cast<const float4*>(s_am + 16 * j + 4 * i4);
+      c[0] = c4.x; c[1] = c4.y; c[2] = c4.z; c[3] = c4.w;
+    };
+    if (tau > 0.0f) {  // uniform over the CTA (Q heads only)
+      // lower median of the group's row maxima: the valid row of rank (n - 1) / 2, ties
+      // broken by row index
       int n = 0, rank = 0;
-      for (int i = g0; i < g0 + G; ++i) {
-        if (!s_ok[i]) continue;
-        ++n;
-        const float mi = s_am[i];
-        rank += (mi < m || (mi == m && i < r)) ? 1 : 0;
-      }
-      if (rank == (n - 1) / 2) s_med[g0] = m;
-    }
-    __syncthreads();
-    if (r < kRows) {
-      float sc = 0.0f;
-      if (s_ok[r]) {
-        const float thr = tau > 0.0f ? __fmul_rn(tau, s_med[g0]) : INFINITY;
-        float top = s_am[r];
-        if (!(top > thr)) {  // an inlier: the largest inlier maximum of the group
-          top = 0.0f;
-          for (int i = g0; i < g0 + G; ++i)
-            if (s_ok[i] && !(s_am[i] > thr)) top = fmaxf(top, s_am[i]);
+#pragma unroll
+      for (int i4 = 0; i4 < 4; ++i4) {
+        float c[4];
+        cands(i4, c);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int idx = 16 * j + 4 * i4 + e;
+          const bool in = (idx & ~(G - 1)) == g0 && c[e] >= 0.0f;
+          n += in ? 1 : 0;
+          rank += (in && (c[e] < m || (c[e] == m && idx < r))) ? 1 : 0;
         }
-        sc = __fdiv_rn(top, 127.0f);
       }
-      s_sc[r] = sc;
+#pragma unroll
+      for (int o = 1; o < 4; o <<= 1) {
+        n += __shfl_xor_sync(0xffffffffu, n, o);
+        rank += __shfl_xor_sync(0xffffffffu, rank, o);
+      }
+      if (j == 0 && m >= 0.0f && rank == (n - 1) / 2) s_med[g0] = m;
+      __syncthreads();
     }
+    // an outlier keeps its own maximum; the others take the group's largest inlier one
+    const float thr = tau > 0.0f ? __fmul_rn(tau, s_med[g0]) : INFINITY;
+    float top = 0.0f;
+#pragma unroll
+    for (int i4 = 0; i4 < 4; ++i4) {
+      float c[4];
+      cands(i4, c);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int idx = 16 * j + 4 * i4 + e;
+        if ((idx & ~(G - 1)) == g0 && c[e] >= 0.0f && !(c[e] > thr)) top = fmaxf(top, c[e]);
+      }
+    }
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1) top = fmaxf(top, __shfl_xor_sync(0xffffffffu, top, o));
+    if (j == 0) s_sc[r] = m < 0.0f ? 0.0f : __fdiv_rn(m > thr ? m : top, 127.0f);
     __syncthreads();
 #pragma unroll
     for (int p = 0; p < P; ++p) grp_scale[p] = s_sc[warp * kQuantRowsPerWarp + p * RPP + rsub];
