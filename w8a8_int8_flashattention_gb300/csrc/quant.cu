@@ -675,9 +675,11 @@ __device__ __forceinline__ void store_vec16(uint16_t* p, const uint16_t (&h)[EPL
 
 // Eight lanes per row (EPL = D / 8 values each, 16-byte accesses), four rows per warp
 // instruction.  kGroups: scales shared by groups of rows (see QuantQK), formed in shared
-// memory from the CTA's 64 row maxima before any code is written.
+// memory from the CTA's 64 row maxima before any code is written.  The per-row form runs
+// five CTAs per SM (48 registers at d <= 128): the loads in flight are what bound it, so
+// V, which only K CTAs convert, is read after the codes rather than held from the start.
 template <sl8_dtype DT, int D, bool kGroups>
-__global__ void __launch_bounds__(kQuantWarps * 32, D == 256 ? (kGroups ? 1 : 2) : (kGroups ? 3 : 4))
+__global__ void __launch_bounds__(kQuantWarps * 32, D == 256 ? (kGroups ? 1 : 2) : (kGroups ? 3 : 5))
     quant_qk_kernel(const QuantQK a, DeviceStatus* st) {
   constexpr int LPR = 8, EPL = D / LPR, NV = EPL / 8, RPP = 32 / LPR, P = kQuantRowsPerWarp / RPP;
   // K heads first: their CTAs also form the K mean and the V exponent, so they start
@@ -791,7 +793,8 @@ __global__ void __launch_bounds__(kQuantWarps * 32, D == 256 ? (kGroups ? 1 : 2)
   // this lane's rows (one per pass): position, validity; then all loads
   int sq[P], tt[P];
   bool live[P], valid[P];
-  uint4 xw[P][NV], vw[P][NV];
+  uint4 xw[P][NV];
+  int64_t voff[P];  // V row offset of each pass (-1: not loaded); V is read after the codes
 #pragma unroll
   for (int p = 0; p < P; ++p) {
     const int64_t pr = row0 + p * RPP + rsub;
@@ -813,8 +816,8 @@ __global__ void __launch_bounds__(kQuantWarps * 32, D == 256 ? (kGroups ? 1 : 2)
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
       xw[p][j] = make_uint4(0u, 0u, 0u, 0u);
-      vw[p][j] = make_uint4(0u, 0u, 0u, 0u);
     }
+    voff[p] = -1;
     if (valid[p] && part * EPL < a.d_io) {
       // a query chunk's rows: position t is row t - q_off of N - q_off; rows hold d_io values
       const int64_t off = (is_k ? row_offset(a.varlen, sq[p], h, tt[p], H, a.N, a.d_io, tk)
@@ -823,8 +826,8 @@ __global__ void __launch_bounds__(kQuantWarps * 32, D == 256 ? (kGroups ? 1 : 2)
 #pragma unroll
       for (int j = 0; j < NV; ++j) {
         xw[p][j] = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + off + 8 * j);
-        if (v16) vw[p][j] = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.v) + off + 8 * j);
       }
+      voff[p] = off;
     }
   }
   // the lane's EPL values of pass p's row, widened (and smoothed for K)
@@ -970,7 +973,20 @@ __global__ void __launch_bounds__(kQuantWarps * 32, D == 256 ? (kGroups ? 1 : 2)
       *reinterpret_cast<uint4*>(crow + 8 * j) = make_uint4(o[0], o[1], o[2], o[3]);
     }
     if (part == 0) scales[static_cast<int64_t>(h) * a.t_pad_max + pr] = scale;
-    if (v16) {
+  }
+  // K CTAs with a V to convert: V * 2^-e in fp16 for the P.V MMA, both passes' loads first
+  if (v16) {
+    uint4 vw[P][NV];
+#pragma unroll
+    for (int p = 0; p < P; ++p)
+#pragma unroll
+      for (int j = 0; j < NV; ++j)
+        vw[p][j] = voff[p] >= 0 ? *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.v) + voff[p] + 8 * j)
+                                : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      if (!live[p]) continue;
+      const int64_t pr = row0 + p * RPP + rsub;
       const float vscale = valid[p] ? __int_as_float((127 - s_vexp) << 23) : 0.0f;  // 2^-e
       uint16_t* vrow = v16 + (static_cast<int64_t>(h) * a.t_pad_max + pr) * D + part * EPL;
 #pragma unroll
