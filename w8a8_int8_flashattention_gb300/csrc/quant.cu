@@ -679,7 +679,7 @@ __device__ __forceinline__ void store_vec16(uint16_t* p, const uint16_t (&h)[EPL
 // five CTAs per SM (48 registers at d <= 128): the loads in flight are what bound it, so
 // V, which only K CTAs convert, is read after the codes rather than held from the start.
 template <sl8_dtype DT, int D, bool kGroups>
-__global__ void __launch_bounds__(kQuantWarps * 32, D == 256 ? (kGroups ? 1 : 2) : (kGroups ? 3 : 5))
+__global__ void __launch_bounds__(kQuantWarps * 32, D == 256 ? 2 : (kGroups ? 4 : 5))
     quant_qk_kernel(const QuantQK a, DeviceStatus* st) {
   constexpr int LPR = 8, EPL = D / LPR, NV = EPL / 8, RPP = 32 / LPR, P = kQuantRowsPerWarp / RPP;
   // K heads first: their CTAs also form the K mean and the V exponent, so they start
