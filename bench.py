@@ -232,7 +232,7 @@ def run_ours(args, world, rank, local):
 
     # ---- decode inputs: fp32 cache values quantised into the int8 cache by the library
     wd = W.get(DECODE)
-    if args.only == "prefill":
+    if args.only in ("prefill", "w8a8"):
         wd = W.get(DECODE, B=1, extra={"lengths": [1024]})
     lens = W.seq_lengths(wd)
     kc = torch.zeros((wd.B, wd.Hkv, wd.lmax, wd.d), dtype=torch.int8, device=dev)
@@ -268,11 +268,14 @@ def run_ours(args, world, rank, local):
         flush_sink.copy_(flush.view(torch.int64).sum())
         if ev:
             ev[0].record(stream)
-        if args.only != "decode":
+        if args.only == "w8a8":
+            sl8.attn_w8a8_fwd(qd, kd, vd, causal=True, smooth_k=True, q_group=W8A8_GROUP, k_group=W8A8_GROUP,
+                              q_outlier_ratio=W8A8_RATIO, workspace=ws, out=out)
+        elif args.only != "decode":
             sl8.attn_int8_fwd(qd, kd, vd, causal=True, smooth_k=True, workspace=ws, out=out)
         if ev:
             ev[1].record(stream)
-        if args.only != "prefill":
+        if args.only not in ("prefill", "w8a8"):
             sl8.attn_int8_decode(qdec, kc, ks, vc, vs, seq, o_partial=o_part, lse_partial=l_part, out=dout)
         if ev:
             ev[2].record(stream)
@@ -665,8 +668,9 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode"],
-                    help="time one half of the step only (profiling runs); no e2e or CPU leg")
+    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode", "w8a8"],
+                    help="time one half of the step only (profiling runs; w8a8: the prefill through "
+                         "attn_w8a8_fwd); no e2e or CPU leg")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup(args)
