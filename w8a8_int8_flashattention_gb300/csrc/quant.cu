@@ -881,31 +881,31 @@ __global__ void __launch_bounds__(kQuantWarps * 32, D == 256 ? 2 : (kGroups ? 4 
     __syncthreads();
     const int G = is_k ? a.k_group : a.q_group;
     const float tau = is_k ? 0.0f : a.q_tau;
-    // four consecutive lanes per row r, each scanning 16 of the CTA's 64 rows (in r's
-    // group or not, decided per candidate), then combining over the four lanes
+    // four consecutive lanes per row r, each scanning a quarter of r's group (rows
+    // [c0, c1)), then combining over the four lanes
     const int r = threadIdx.x >> 2, j = threadIdx.x & 3, g0 = r & ~(G - 1);
+    const int per = (G + 3) >> 2, c0 = g0 + j * per, c1 = min(c0 + per, g0 + G);
     const float m = s_am[r];
-    // the lane's 16 candidates, four at a time
-    auto cands = [&](int i4, float (&c)[4]) {
-      const float4 c4 = *reinterpret_cast<const float4*>(s_am + 16 * j + 4 * i4);
-      c[0] = c4.x; c[1] = c4.y; c[2] = c4.z; c[3] = c4.w;
+    // f(index, value) over the lane's rows: float4 reads when a quarter is 4-aligned (G >= 16)
+    auto scan = [&](auto&& f) {
+      if (per >= 4) {
+        for (int i = c0; i < c1; i += 4) {
+          const float4 c4 = *reinterpret_cast<const float4*>(s_am + i);
+          f(i, c4.x); f(i + 1, c4.y); f(i + 2, c4.z); f(i + 3, c4.w);
+        }
+      } else {
+        for (int i = c0; i < c1; ++i) f(i, s_am[i]);
+      }
     };
     if (tau > 0.0f) {  // uniform over the CTA (Q heads only)
       // lower median of the group's row maxima: the valid row of rank (n - 1) / 2, ties
       // broken by row index
       int n = 0, rank = 0;
-#pragma unroll
-      for (int i4 = 0; i4 < 4; ++i4) {
-        float c[4];
-        cands(i4, c);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int idx = 16 * j + 4 * i4 + e;
-          const bool in = (idx & ~(G - 1)) == g0 && c[e] >= 0.0f;
-          n += in ? 1 : 0;
-          rank += (in && (c[e] < m || (c[e] == m && idx < r))) ? 1 : 0;
-        }
-      }
+      scan([&](int idx, float c) {
+        const bool in = c >= 0.0f;
+        n += in ? 1 : 0;
+        rank += (in && (c < m || (c == m && idx < r))) ? 1 : 0;
+      });
 #pragma unroll
       for (int o = 1; o < 4; o <<= 1) {
         n += __shfl_xor_sync(0xffffffffu, n, o);
@@ -917,16 +917,9 @@ __global__ void __launch_bounds__(kQuantWarps * 32, D == 256 ? 2 : (kGroups ? 4 
     // an outlier keeps its own maximum; the others take the group's largest inlier one
     const float thr = tau > 0.0f ? __fmul_rn(tau, s_med[g0]) : INFINITY;
     float top = 0.0f;
-#pragma unroll
-    for (int i4 = 0; i4 < 4; ++i4) {
-      float c[4];
-      cands(i4, c);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int idx = 16 * j + 4 * i4 + e;
-        if ((idx & ~(G - 1)) == g0 && c[e] >= 0.0f && !(c[e] > thr)) top = fmaxf(top, c[e]);
-      }
-    }
+    scan([&](int, float c) {
+      if (c >= 0.0f && !(c > thr)) top = fmaxf(top, c);
+    });
 #pragma unroll
     for (int o = 1; o < 4; o <<= 1) top = fmaxf(top, __shfl_xor_sync(0xffffffffu, top, o));
     if (j == 0) s_sc[r] = m < 0.0f ? 0.0f : __fdiv_rn(m > thr ? m : top, 127.0f);
