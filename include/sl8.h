@@ -152,8 +152,9 @@ SL8_API int sl8_attn_int8_fwd_chunk(const void* q, const void* k, const void* v,
 
 /*
  * W8A8 prefill with grouped ("per-warp") scales and outlier-aware Q ("Attention
- * kernels" table, attn_w8a8_fwd row: W8A8 with per-warp quantization, outlier-aware;
- * "Quantization" table, per-row int8 row: Q outlier detection).  The pages give no
+ * kernels" table, attn_w8a8_fwd row: a W8A8 forward with scales set per warp that takes
+ * outliers into account; "Quantization" table, per-row int8 row, which lists outlier
+ * detection for Q).  The pages give no
  * formula; the reading implemented:
  *   - the rows of each (sequence, head) form groups of G consecutive positions from
  *     position 0 (q_group for Q, k_group for K after its channel mean); every row of a

@@ -94,9 +94,10 @@ static int cmp_float(const void* a, const void* b) {
 }
 
 /*
- * "Attention kernels" table, attn_w8a8_fwd row ("W8A8 with per-warp quantization.
- * Outlier-aware") and the "Quantization" table's "Q outlier detection"; the pages give
- * no formula, so this is reading R21:
+ * "Attention kernels" table, attn_w8a8_fwd row (a W8A8 forward whose scales are set per
+ * warp and which takes outliers into account), and the "Quantization" table's per-row
+ * int8 row, which lists outlier detection for Q.  The pages give no formula, so this is
+ * reading R21:
  *   - the n rows (one sequence and head, in token order, optionally smoothed by mu)
  *     form groups of `group` consecutive rows starting at row 0 (the last group may be
  *     shorter); a = max|x| of each row (fp32, exact);

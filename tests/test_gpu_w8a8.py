@@ -1,9 +1,9 @@
 """GPU parity of attn_w8a8_fwd (grouped "per-warp" scales, outlier-aware Q) against
 the CPU oracle, through the C ABI.
 
-Operation: the "SuperL8" README, "Attention kernels" table, attn_w8a8_fwd row (W8A8 with
-per-warp quantisation, outlier-aware) and the "Quantization" table's per-row int8 row
-(Q outlier detection).  Bit-exact: the int8 codes, the fp32 scales and the int32
+Operation: the "SuperL8" README, "Attention kernels" table, attn_w8a8_fwd row (a W8A8
+forward with scales set per warp that takes outliers into account) and the
+"Quantization" table's per-row int8 row (outlier detection for Q).  Bit-exact: the int8 codes, the fp32 scales and the int32
 logits; outputs within the tolerances of tests/_parity.py.
 """
 import numpy as np

@@ -1,8 +1,8 @@
 """Pins for the oracle's grouped quantiser and the attn_w8a8_fwd prefill built on it.
 
 Operation: "SuperL8" README (github.com/jajmangold/superl8), "Attention kernels" table,
-attn_w8a8_fwd row (W8A8 with per-warp quantisation, outlier-aware), and the
-"Quantization" table's per-row int8 row (Q outlier detection).  The reading (groups of
+attn_w8a8_fwd row (a W8A8 forward with scales set per warp that takes outliers into
+account), and the "Quantization" table's per-row int8 row (outlier detection for Q).  The reading (groups of
 G consecutive rows share the scale of their non-outlier rows; a row above tau times
 its group's lower median max|x| keeps its own scale) is restated in the oracle.
 
