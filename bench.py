@@ -84,70 +84,150 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples (SM clock, throttle reasons) during the timed region."""
+    """SM clock and throttle-reason samples while the bench runs.
 
+    Reads NVML directly (libnvidia-ml, read-only queries) every ``period`` seconds from a
+    thread, so that even a timed region of a few milliseconds holds samples; falls back
+    to ``nvidia-smi -lms 100`` where NVML cannot be loaded.  ``mark()`` brackets the timed
+    region; ``summary()`` reports the samples inside it and, separately, every sample
+    taken while the bench ran (the GPU under load)."""
+
+    # NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
-        self.index = index
-        self.proc = None
-        self.lines = []
+    def __init__(self, device_index: int, period: float = 0.002):
+        self.index = device_index
+        self.period = period
+        self.samples = []        # (t, sm_mhz, max_mhz, reasons set)
+        self.window = None
+        self.source = None
+        self._stop = threading.Event()
+        self._proc = None
+        self._thread = None
 
-    def __enter__(self):
-        try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
-            self.thread.start()
-        except OSError:
-            self.proc = None
-        return self
+    # ---- NVML
+    def _nvml_handle(self):
+        import ctypes
+        import torch
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        props = torch.cuda.get_device_properties(self.index)
+        bus = getattr(props, "pci_bus_id", None)
+        ok = False
+        if bus is not None:
+            dom, dev = getattr(props, "pci_domain_id", 0), getattr(props, "pci_device_id", 0)
+            for fmt in ("%08X:%02X:%02X.0", "%04X:%02X:%02X.0"):
+                if lib.nvmlDeviceGetHandleByPciBusId_v2((fmt % (dom, bus, dev)).encode(), ctypes.byref(h)) == 0:
+                    ok = True
+                    break
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(self.index, ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle")
+        reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return lib, h, reasons_fn
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
+    def _nvml_loop(self, lib, h, reasons_fn):
+        import ctypes
+        clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            t = time.perf_counter()
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:        # NVML_CLOCK_SM
+                lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+                reasons_fn(h, ctypes.byref(rs))
+                names = {n for bit, n in self.REASONS.items() if rs.value & bit}
+                self.samples.append((t, float(clk.value), float(mx.value), names))
+            self._stop.wait(self.period)
 
-    def __exit__(self, *exc):
-        if self.proc:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-
-    def summary(self):
-        sm, mx, reasons = [], 0.0, set()
+    # ---- nvidia-smi fallback
+    def _smi_loop(self):
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
+        for line in self._proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
             if len(parts) < 8:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx = max(mx, float(parts[1]))
+                sm, mx = float(parts[0]), float(parts[1])
             except ValueError:
                 continue
-            for n, val in zip(names, parts[4:8]):
-                if val.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+            rs = {n for n, val in zip(names, parts[4:8]) if val.lower().startswith("active")}
+            self.samples.append((time.perf_counter(), sm, mx, rs))
+
+    def __enter__(self):
+        try:
+            lib, h, fn = self._nvml_handle()
+            self._thread = threading.Thread(target=self._nvml_loop, args=(lib, h, fn), daemon=True)
+            self.source = f"NVML every {self.period * 1e3:.0f} ms"
+        except (OSError, AttributeError):
+            try:
+                self._proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                               "--format=csv,noheader,nounits", "-lms", "100"],
+                                              stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self._thread = threading.Thread(target=self._smi_loop, daemon=True)
+                self.source = "nvidia-smi -lms 100"
+            except OSError:
+                self._thread = None
+        if self._thread:
+            self._thread.start()
+        return self
+
+    def mark(self, t0: float, t1: float):
+        self.window = (t0, t1)
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self._proc:
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self._proc.kill()
+        if self._thread:
+            self._thread.join(timeout=5)
+
+    @staticmethod
+    def _stats(samples):
+        if not samples:
+            return None, None, [], 0
+        sm = [x[1] for x in samples]
+        return (statistics.median(sm), max(x[2] for x in samples), sorted(set().union(*(x[3] for x in samples))),
+                len(samples))
+
+    def summary(self):
+        timed = [x for x in self.samples if self.window and self.window[0] <= x[0] <= self.window[1]]
+        sm, mx, reasons, n = self._stats(timed)
+        asm, amx, areasons, an = self._stats(self.samples)
+        return {"sm_mhz": sm, "sm_max_mhz": mx, "reasons": reasons, "samples": n,
+                "run": {"sm_mhz": asm, "sm_max_mhz": amx, "reasons": areasons, "samples": an},
+                "source": self.source,
+                "note": "sm_mhz, reasons and samples: inside the timed steps; run: every sample while the bench ran"}
 
 
-def dist_setup(args):
+def dist_setup(args, backend=None):
+    """Process group of a torchrun launch (none for one rank).  The backend is nccl when a
+    GPU is visible, else gloo; ``backend`` or the SL8_DIST_BACKEND variable overrides it
+    (the CPU test of this host logic forces gloo so it never touches a GPU)."""
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        backend = backend or os.environ.get("SL8_DIST_BACKEND") or ("nccl" if torch.cuda.is_available() else "gloo")
+        if backend == "nccl":
+            torch.cuda.set_device(local)
         dist.init_process_group(backend)
     return world, rank, local
+
+
+def _reduce_device():
+    import torch.distributed as dist
+    return "cuda" if dist.get_backend() == "nccl" else "cpu"
 
 
 def max_over_ranks(x: float, world: int) -> float:
@@ -155,7 +235,7 @@ def max_over_ranks(x: float, world: int) -> float:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=_reduce_device())
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -168,7 +248,14 @@ def barrier(world: int):
 
 # ------------------------------------------------------------------ reference arm: the CPU oracle
 
+WORKLOAD_DESC = ("prefill B1 Hq32 Hkv8 N4096 d128 bf16 causal smooth_k (Qwen3-8B shape) + "
+                 "decode B64 Hq32 Hkv8 d128 int8 KV, L~U[1024,8192]")
+
+
 def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle as it stands, on the same workload as our arm.
+    A step is the whole prefill (every query row of every head) plus the whole decode
+    (every sequence and head over the int8 cache), run on the host cores."""
     if rank != 0:
         return
     import oracle
@@ -177,21 +264,40 @@ def run_reference(args, world, rank):
     q, k, v = W.prefill_dense(w)
     qn, kn, vn = q.float().numpy(), k.float().numpy(), v.float().numpy()
     rows = [(0, h, i) for h in range(w.Hq) for i in range(w.N)]
-    ops = 2.0 * 2.0 * w.d * sum(i + 1 for (_, _, i) in rows)
-    times = []
+    ops = prefill_ops(w)
+    # the decode cache, quantised by the oracle's own quantiser (set-up, not timed)
+    wd = W.get(DECODE)
+    lens = W.seq_lengths(wd)
+    caches = {}
+    for name in ("k", "v"):
+        c = np.zeros((wd.B, wd.Hkv, wd.lmax, wd.d), np.int8)
+        sc = np.zeros((wd.B, wd.Hkv, wd.lmax), np.float32)
+        for b in range(wd.B):
+            L = int(lens[b])
+            c[b, :, :L], sc[b, :, :L] = oracle.quant_rowwise(W.decode_cache_values(wd, b, name))
+        caches[name] = (c, sc)
+    qdec = W.decode_query(wd).float().numpy()
+    dbytes = decode_bytes(wd, lens)
+    pre, dec = [], []
     for it in range(args.warmup + args.steps):
         t0 = time.perf_counter()
         oracle.attn_prefill(qn, kn, vn, causal=True, smooth_k=True, rows=rows)
-        dt = time.perf_counter() - t0
+        t1 = time.perf_counter()
+        oracle.attn_decode(qdec, caches["k"][0], caches["k"][1], caches["v"][0], caches["v"][1], lens)
+        t2 = time.perf_counter()
         if it >= args.warmup:
-            times.append(dt)
-    sec = float(np.mean(times))
-    tops = ops / sec / 1e12
-    sample = f"the whole prefill workload, every query row of all {w.Hq} heads ({ops / 1e9:.1f} GOP per step)"
+            pre.append(t1 - t0)
+            dec.append(t2 - t1)
+    pre_s, dec_s = float(np.mean(pre)), float(np.mean(dec))
+    tops = ops / pre_s / 1e12
+    sample = (f"the whole workload every step: all {w.Hq} heads x {w.N} query rows of the prefill "
+              f"({ops / 1e9:.1f} GOP) and all {wd.B} x {wd.Hq} decode rows")
     line = {"impl": "reference", "metric": METRIC, "value": tops, "unit": "TOPS", "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{PREFILL} prefill sample (B1 Hq32 Hkv8 N4096 d128, causal, smooth_k)"},
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": (pre_s + dec_s) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC, "prefill_ms": pre_s * 1e3, "decode_ms": dec_s * 1e3},
+            "decode": {"value": dbytes / dec_s / 1e9, "unit": "GB/s", "ms": dec_s * 1e3},
+            "tokens_per_s": {"prefill": w.B * w.N / pre_s, "decode": wd.B / dec_s},
             "cpu_baseline": {"value": tops, "unit": "TOPS", "cores": oracle.num_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": tops, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -288,12 +394,15 @@ def run_ours(args, world, rank, local):
     sl8.trace_enable(False)
     barrier(world)
     torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clk:
-        t_wall = time.perf_counter()
-        for i in range(args.steps):
-            step(events[i])
-        torch.cuda.synchronize(dev)
-        t_wall = time.perf_counter() - t_wall
+    clk = ClockSampler(local).__enter__()
+    time.sleep(0.01)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(events[i])
+    torch.cuda.synchronize(dev)
+    t1 = time.perf_counter()
+    clk.mark(t0, t1)
+    t_wall = t1 - t0
     barrier(world)
     st, site = sl8.last_device_status(dev)
     if st != sl8.SL8_OK:
@@ -330,10 +439,12 @@ def run_ours(args, world, rank, local):
     launches = sum(n for n, _ in trace.values()) * args.steps // trace_steps  # launches in the timed steps
     traffic = load_traffic()
     if args.only != "all":
+        clk.__exit__(None, None, None)
         if rank == 0:
             print(json.dumps({"only": args.only, "prefill_ms": pre_ms, "decode_ms": dec_ms,
                               "kernels": {n: {"launches": c, "ms_per_launch": ms / c}
-                                          for n, (c, ms) in sorted(trace.items())}}), flush=True)
+                                          for n, (c, ms) in sorted(trace.items())},
+                              "clocks": clk.summary()}), flush=True)
         return
 
     # ---- the same decode over a paged k8v8 cache
@@ -360,35 +471,15 @@ def run_ours(args, world, rank, local):
     fv_gbs = fv_bytes * world / (fv_ms * 1e-3) / 1e9
     fv_split_gbs = fv_bytes / (fv_split_ms * 1e-3) / 1e9
 
+    # ---- the other prefill workloads: tiny latency case, Gemma3 shape at d = 256, ragged varlen
+    others = {name: measure_prefill_config(sl8, W, name, dev, stream, flush, flush_sink, args.steps, args.warmup,
+                                           world, peaks, rank)
+              for name in OTHER_PREFILL}
+
     # ---- e2e: public API with pinned host buffers, H2D inputs + D2H output every step
-    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
-    oh = torch.empty(q.shape, dtype=q.dtype).pin_memory()
-    qdh = W.decode_query(wd).pin_memory()
-    doh = torch.empty((wd.B, wd.Hq, wd.d), dtype=torch.bfloat16).pin_memory()
-    q2, k2, v2 = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
-    qdec2 = torch.empty_like(qdec)
+    e2e_ms, h2d, d2h, e_steps = measure_e2e(sl8, q, k, v, ws, dev, stream, args.steps, args.warmup, world)
 
-    def e2e_step():
-        q2.copy_(qh, non_blocking=True)
-        k2.copy_(kh, non_blocking=True)
-        v2.copy_(vh, non_blocking=True)
-        sl8.attn_int8_fwd(q2, k2, v2, causal=True, smooth_k=True, workspace=ws, out=out)
-        oh.copy_(out, non_blocking=True)
-
-    for _ in range(args.warmup):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    e_steps = max(3, args.steps // 4)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, world)
-    h2d = (q.numel() + k.numel() + v.numel()) * 2
-    d2h = out.numel() * 2
-
+    clk.__exit__(None, None, None)
     if rank != 0:
         return
     cpu = cpu_baseline_leg(wp, q.float().numpy(), k.float().numpy(), v.float().numpy())
@@ -397,12 +488,15 @@ def run_ours(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": pre_ms + dec_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "i8 codes on bf16 tensor cores (exact int32 QK^T), bf16 P.V, f32 softmax",
         "data": "synthetic",
-        "config": {"workload": "prefill B1 Hq32 Hkv8 N4096 d128 bf16 causal smooth_k (Qwen3-8B shape) + "
-                               "decode B64 Hq32 Hkv8 d128 int8 KV, L~U[1024,8192]",
+        "config": {"workload": WORKLOAD_DESC,
                    "prefill_ms": pre_ms, "decode_ms": dec_ms, "prefill_gops": ops / 1e9,
                    "decode_bytes": dbytes, "decode_splits": S,
                    "l2": "flushed before every step (256 MB write, then a read of it, outside the timed events)"},
-        "decode": {"value": gbs, "unit": "GB/s", "ms": dec_ms,
+        "tokens_per_s": {"prefill": wp.B * wp.N * world / (pre_ms * 1e-3),
+                         "decode": wd.B * world / (dec_ms * 1e-3),
+                         "note": "prefill: query tokens per second; decode: sequences advanced by one token per "
+                                 "second (one query token each)"},
+        "decode": {"value": gbs, "unit": "GB/s", "ms": dec_ms, "tokens_per_s": wd.B * world / (dec_ms * 1e-3),
                    "roofline": {"bound": "hbm", "achieved": split_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                 "frac": split_gbs / peaks["hbm_gbs"],
                                 "traffic": traffic.get("decode_split"), "kernel": "decode_split",
@@ -444,15 +538,150 @@ def run_ours(args, world, rank, local):
                      "frac": attn_tflops / peaks["bf16_tflops"], "traffic": traffic.get("prefill_attn"),
                      "kernel": "prefill_attn", "launch_ms": attn_ms,
                      "peak_source": peaks["source"] + " bf16 burst (QK^T and P.V both run on the bf16 pipe)"},
+        "prefill_configs": others,
         "kernels": {n: {"launches": c, "ms_per_launch": ms / c} for n, (c, ms) in sorted(trace.items())},
         "cpu_baseline": cpu,
         "e2e": {"value": ops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TOPS", "ms_per_step": e2e_ms,
+                "steps": e_steps,
+                "how": "sl8.attn_int8_fwd on device copies of pinned host q/k/v, output read back to pinned "
+                       "host memory, every step; double-buffered: step i+1's H2D (own stream) and step i-1's D2H "
+                       "(own stream) overlap step i's kernels; timed from the first H2D to the last D2H",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "wall_s_timed": t_wall,
     }
     print(json.dumps(line), flush=True)
+
+
+OTHER_PREFILL = ("tiny", "gemma3_d256", "varlen")
+OTHER_SAMPLE_STRIDE = {"tiny": 1, "gemma3_d256": 16, "varlen": 16}   # CPU baseline: every k-th query row
+
+
+def _causal_ops(lens, Hq, d) -> float:
+    return 2.0 * 2.0 * d * Hq * float(sum(int(L) * (int(L) + 1) // 2 for L in lens))
+
+
+def measure_prefill_config(sl8, W, name, dev, stream, flush, flush_sink, steps, warmup, world, peaks, rank):
+    """One more prefill workload (attn_int8_fwd, causal, K-smoothing): the step time with
+    L2 flushed before each step, the attention kernel's roofline from the traced pass,
+    tokens/s, and the oracle on a bounded sample of the same inputs (rank 0)."""
+    import torch
+    w = W.get(name)
+    if w.kind == "varlen":
+        q, k, v, cu = W.prefill_varlen(w)
+        lens = [int(x) for x in np.diff(cu.numpy())]
+        N = max(lens)
+        cud = cu.to(dev)
+        desc = (f"varlen causal prefill, {w.B} sequences, lengths U[{w.len_lo},{w.len_hi}] (seeded T = {sum(lens)}), "
+                f"Hq{w.Hq} Hkv{w.Hkv} d{w.d} {w.dtype}, smooth_k")
+    else:
+        q, k, v = W.prefill_dense(w)
+        lens = [w.N] * w.B
+        N, cu, cud = w.N, None, None
+        desc = f"causal prefill B{w.B} Hq{w.Hq} Hkv{w.Hkv} N{w.N} d{w.d} {w.dtype}, smooth_k={w.smooth_k}"
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    ws = torch.empty(sl8.prefill_workspace_bytes(len(lens), w.Hq, w.Hkv, N, w.d, sum(lens) if cu is not None else 0),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty_like(qd)
+
+    def step(ev=None):
+        flush.zero_()
+        flush_sink.copy_(flush.view(torch.int64).sum())
+        if ev:
+            ev[0].record(stream)
+        sl8.attn_int8_fwd(qd, kd, vd, causal=True, smooth_k=w.smooth_k, cu_seqlens=cud,
+                          max_seqlen=N if cud is not None else None, workspace=ws, out=out)
+        if ev:
+            ev[1].record(stream)
+
+    n, ms, trace = timed_then_traced(sl8, step, dev, steps, warmup)
+    st, site = sl8.last_device_status(dev)
+    if st != sl8.SL8_OK:
+        raise RuntimeError(f"device status {st} at {site} during the {name} prefill")
+    ms = max_over_ranks(ms, world)
+    ops = _causal_ops(lens, w.Hq, w.d)
+    c, attn_ms = trace.get("prefill_attn", (0, 0.0))
+    attn_ms = attn_ms / c if c else float("nan")
+    tflops = ops / (attn_ms * 1e-3) / 1e12
+    res = {"workload": desc, "value": ops * world / (ms * 1e-3) / 1e12, "unit": "TOPS", "ms": ms, "steps": n,
+           "ops": ops, "tokens_per_s": sum(lens) * world / (ms * 1e-3),
+           "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                        "frac": tflops / peaks["bf16_tflops"], "traffic": load_traffic().get(f"prefill_attn:{name}"),
+                        "kernel": "prefill_attn", "launch_ms": attn_ms,
+                        "peak_source": peaks["source"] + " bf16 burst"},
+           "kernels": {nm: {"launches": cc, "ms_per_launch": t / cc} for nm, (cc, t) in sorted(trace.items())},
+           "l2": "flushed before every step"}
+    del qd, kd, vd, ws, out
+    if rank == 0:
+        res["cpu_baseline"] = cpu_sample_leg(w, q, k, v, cu, lens, OTHER_SAMPLE_STRIDE[name])
+    return res
+
+
+def cpu_sample_leg(w, q, k, v, cu, lens, stride):
+    """The oracle as it stands on every stride-th query row of every head (all of them at
+    stride 1); the rate counts the causal (query, key) pairs of the rows it ran."""
+    import oracle
+    rows = [(s, h, i) for s, L in enumerate(lens) for h in range(w.Hq) for i in range(0, L, stride)]
+    ops = 2.0 * 2.0 * w.d * float(sum(i + 1 for (_, _, i) in rows))
+    qn, kn, vn = q.float().numpy(), k.float().numpy(), v.float().numpy()
+    t0 = time.perf_counter()
+    oracle.attn_prefill(qn, kn, vn, causal=True, smooth_k=w.smooth_k, rows=rows,
+                        cu_seqlens=None if cu is None else cu.numpy())
+    sec = time.perf_counter() - t0
+    return {"value": ops / sec / 1e12, "unit": "TOPS", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"every {stride}. query row of all {w.Hq} heads ({len(rows)} rows, {ops / 1e9:.2f} GOP, "
+                      f"quantisation of the whole input included), {sec:.2f} s"}
+
+
+def measure_e2e(sl8, q, k, v, ws, dev, stream, steps, warmup, world):
+    """The prefill end to end through the public API: every step copies its q, k, v from
+    pinned host memory and reads its output back into pinned host memory.  The steps run
+    as a pipeline over two device buffer sets: H2D on one stream, the library call on the
+    compute stream, D2H on a third, ordered by events (step i+1's inputs land while step
+    i computes and step i-1's output drains).  Returns (ms per step, H2D bytes per step,
+    D2H bytes per step, steps timed)."""
+    import torch
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    oh = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    bufs = [tuple(torch.empty(t.shape, dtype=t.dtype, device=dev) for t in (q, k, v)) for _ in range(2)]
+    outs = [torch.empty(q.shape, dtype=q.dtype, device=dev) for _ in range(2)]
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def run(n):
+        ev = lambda: torch.cuda.Event(enable_timing=False)  # noqa: E731
+        h2d_done = [ev() for _ in range(n)]
+        comp_done = [ev() for _ in range(n)]
+        d2h_done = [ev() for _ in range(n)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(up)
+        for i in range(n):
+            qb, kb, vb = bufs[i % 2]
+            if i >= 2:
+                up.wait_event(comp_done[i - 2])      # step i-2 has finished reading this buffer set
+            with torch.cuda.stream(up):
+                qb.copy_(qh, non_blocking=True)
+                kb.copy_(kh, non_blocking=True)
+                vb.copy_(vh, non_blocking=True)
+                h2d_done[i].record(up)
+            stream.wait_event(h2d_done[i])
+            if i >= 2:
+                stream.wait_event(d2h_done[i - 2])   # step i-2's output has left this buffer
+            sl8.attn_int8_fwd(qb, kb, vb, causal=True, smooth_k=True, workspace=ws, out=outs[i % 2])
+            comp_done[i].record(stream)
+            down.wait_event(comp_done[i])
+            with torch.cuda.stream(down):
+                oh.copy_(outs[i % 2], non_blocking=True)
+                d2h_done[i].record(down)
+        down.wait_event(d2h_done[n - 1])
+        t1.record(down)
+        torch.cuda.synchronize(dev)
+        return t0.elapsed_time(t1) / n
+
+    run(max(warmup, 3))
+    n = max(8, steps)
+    ms = max_over_ranks(run(n), world)
+    return ms, (q.numel() + k.numel() + v.numel()) * q.element_size(), q.numel() * q.element_size(), n
 
 
 def timed_then_traced(sl8, step, device, steps, warmup):
@@ -676,8 +905,10 @@ def main():
     world, rank, local = dist_setup(args)
     try:
         if args.impl == "reference":
-            if args.steps > 20:
-                args.steps = 3  # each step is seconds of CPU work; keep the run within minutes
+            # each step is seconds of CPU work (the whole prefill and decode on the host cores):
+            # at most 5 timed steps after one warm-up keep the run within a couple of minutes
+            args.steps = max(1, min(args.steps, 5))
+            args.warmup = 1
             run_reference(args, world, rank)
         else:
             run_ours(args, world, rank, local)

@@ -181,19 +181,25 @@ SL8_API int sl8_attn_w8a8_fwd(const void* q, const void* k, const void* v, int q
 
 /*
  * Debug view of the prefill's quantisation and int32 logits (same kernels and
- * tensor-core path as sl8_attn_int8_fwd, without the mask).  Dense layout only.
+ * tensor-core path as sl8_attn_int8_fwd, without the mask).  q, k, qk_dtype, B, Hq,
+ * Hkv, N, d, cu_seqlens and total_tokens as for sl8_attn_int8_fwd (dense or varlen).
  *   logits_out  device, nullable, [B][Hq][row_end - row_begin][N] int32:
- *               logits_out[b][h][i - row_begin][j] = int32(q_i8[b,h,i] . k_i8[b,hkv,j])
- *               for every key j < N, 0 <= row_begin <= i < row_end <= N.
- *   q_codes/q_scales    device, nullable, [B][Hq][N][d] int8 / [B][Hq][N] fp32.
- *   k_codes/k_scales    device, nullable, [B][Hkv][N][d] int8 / [B][Hkv][N] fp32
- *                       (after smoothing when smooth_k is set).
+ *               logits_out[s][h][i - row_begin][j] = int32(q_i8[s,h,i] . k_i8[s,hkv,j])
+ *               for every key j < L_s of sequence s (L_s = N dense, else its
+ *               cu_seqlens length) and every row row_begin <= i < min(row_end, L_s);
+ *               other entries are left untouched.  0 <= row_begin <= row_end <= N.
+ *   q_codes/q_scales    device, nullable: dense [B][Hq][N][d] int8 / [B][Hq][N] fp32,
+ *                       varlen [total_tokens][Hq][d] / [total_tokens][Hq].
+ *   k_codes/k_scales    device, nullable: dense [B][Hkv][N][d] int8 / [B][Hkv][N] fp32,
+ *                       varlen [total_tokens][Hkv][d] / [total_tokens][Hkv] (after
+ *                       smoothing when smooth_k is set).
  *   workspace   as for sl8_attn_int8_fwd (same size query).
  */
 SL8_API int sl8_attn_int8_qk_logits_debug(const void* q, const void* k, int qk_dtype, int32_t B, int32_t Hq, int32_t Hkv,
-                                  int32_t N, int32_t d, int smooth_k, int32_t row_begin, int32_t row_end,
-                                  int32_t* logits_out, int8_t* q_codes, float* q_scales, int8_t* k_codes,
-                                  float* k_scales, void* workspace, size_t workspace_bytes, void* stream);
+                                  int32_t N, int32_t d, const int32_t* cu_seqlens, int64_t total_tokens,
+                                  int smooth_k, int32_t row_begin, int32_t row_end, int32_t* logits_out,
+                                  int8_t* q_codes, float* q_scales, int8_t* k_codes, float* k_scales,
+                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * The same debug view for the grouped quantisation of sl8_attn_w8a8_fwd (q_group,
@@ -201,11 +207,11 @@ SL8_API int sl8_attn_int8_qk_logits_debug(const void* q, const void* k, int qk_d
  * sl8_attn_w8a8_fwd attention consumes.
  */
 SL8_API int sl8_attn_w8a8_qk_logits_debug(const void* q, const void* k, int qk_dtype, int32_t B, int32_t Hq,
-                                          int32_t Hkv, int32_t N, int32_t d, int smooth_k, int32_t q_group,
-                                          int32_t k_group, float q_outlier_ratio, int32_t row_begin,
-                                          int32_t row_end, int32_t* logits_out, int8_t* q_codes, float* q_scales,
-                                          int8_t* k_codes, float* k_scales, void* workspace,
-                                          size_t workspace_bytes, void* stream);
+                                          int32_t Hkv, int32_t N, int32_t d, const int32_t* cu_seqlens,
+                                          int64_t total_tokens, int smooth_k, int32_t q_group, int32_t k_group,
+                                          float q_outlier_ratio, int32_t row_begin, int32_t row_end,
+                                          int32_t* logits_out, int8_t* q_codes, float* q_scales, int8_t* k_codes,
+                                          float* k_scales, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Split-KV decode over an int8 KV cache ("Attention kernels" table, attn_decode,
@@ -230,6 +236,23 @@ SL8_API int sl8_attn_w8a8_qk_logits_debug(const void* q, const void* k, int qk_d
  */
 SL8_API int32_t sl8_attn_decode_num_splits(int32_t B, int32_t Hkv, int32_t Lmax, int32_t d, int32_t num_splits);
 SL8_API int32_t sl8_attn_decode_split_size(int32_t B, int32_t Hkv, int32_t Lmax, int32_t d, int32_t num_splits);
+
+/*
+ * Scratch of the split-KV decode ("Attention kernels" table, attn_decode: the partials
+ * that a split-KV decode merges): the bytes of o_partial and lse_partial for the
+ * effective split count S = sl8_attn_decode_num_splits(B, Hkv, Lmax, d, num_splits),
+ * laid out in one caller-owned buffer as
+ *   o_partial   at byte 0:                          [B][Hq][S][d] fp32;
+ *   lse_partial at sl8_attn_decode_lse_offset(...):  [B][Hq][S] fp32
+ * (the offset is B * Hq * S * d * 4 rounded up to 256 bytes).  Returns 0 for an
+ * invalid or unsupported shape (as sl8_attn_decode_num_splits, or Hq not a multiple
+ * of Hkv).  Pure host arithmetic: no device is touched except for the SM count that
+ * the automatic split count (num_splits = 0) uses.
+ */
+SL8_API size_t sl8_attn_decode_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t Lmax, int32_t d,
+                                              int32_t num_splits);
+SL8_API size_t sl8_attn_decode_lse_offset(int32_t B, int32_t Hq, int32_t Hkv, int32_t Lmax, int32_t d,
+                                          int32_t num_splits);
 SL8_API int sl8_attn_int8_decode_splitkv(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale,
                                  const int8_t* v_cache, const float* v_scale, const int32_t* seqlens, int32_t B,
                                  int32_t Hq, int32_t Hkv, int32_t Lmax, int32_t d, int32_t num_splits,
@@ -345,7 +368,10 @@ SL8_API int sl8_attn_int8_decode_logits_debug(const void* q, int q_dtype, const 
  *     single split needs more than the array (B * Hq * (d + 1) * 4 bytes >
  *     SL8_NOALLOC_SCRATCH_BYTES) is refused with SL8_ERR_WORKSPACE before any launch.
  *   - The first call on each device looks up the array's device address (with that
- *     device current); make that first call before any stream capture.
+ *     device current); make that first call before any stream capture.  The address is
+ *     kept for the life of the process: it does not survive cudaDeviceReset() or any
+ *     other teardown of the device's primary context, after which this entry point
+ *     must not be called again in the same process.
  *   - Every call uses the same array: calls whose work overlaps on the GPU (other
  *     streams, other threads) race on it and must be serialised by the caller.
  *   - Calls no cudaMalloc, cudaFree or allocating library routine.
@@ -357,7 +383,9 @@ SL8_API int sl8_attn_int8_decode_noalloc(const void* q, int q_dtype, const int8_
                                          int out_dtype, void* stream);
 
 /*
- * Synchronises `stream`, then reads and clears the current device's status word:
+ * Synchronises `stream`, then reads and clears the current device's status word (its
+ * address is looked up once per device and, like the no-allocation scratch above, is
+ * not valid after cudaDeviceReset()):
  * SL8_OK, SL8_ERR_TIMEOUT (a bounded wait gave up; *site names the wait) or
  * SL8_ERR_DEVICE_ARG (an out-of-range device-side length).  site may be NULL.
  */

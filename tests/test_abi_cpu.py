@@ -144,7 +144,7 @@ def test_w8a8_argument_errors(lib):
     assert call(tau=float("inf")) == sl8.SL8_ERR_INVALID_ARG
     assert call(tau=0.0) == sl8.SL8_ERR_WORKSPACE
     d = lib.sl8_attn_w8a8_qk_logits_debug
-    assert d(p, p, sl8.SL8_BF16, 1, 4, 2, 128, 128, 1, 5, 32, 4.0, 0, 1, p, None, None, None, None, p, 16,
+    assert d(p, p, sl8.SL8_BF16, 1, 4, 2, 128, 128, None, 0, 1, 5, 32, 4.0, 0, 1, p, None, None, None, None, p, 16,
              None) == sl8.SL8_ERR_INVALID_ARG
 
 
@@ -216,3 +216,22 @@ def test_page_table_and_paginate_round_trip():
             np.testing.assert_array_equal(spages[table[b, t // 16], :, t % 16], scales[b, :, t])
     shared, _ = W.page_table(w, lens, 16, max_blocks=8, shared_prefix=1)
     assert shared[2, 0] == shared[0, 0] or lens[0] == 0
+
+
+def test_decode_workspace_size(lib):
+    """The decode scratch query: o_partial [B,Hq,S,d] fp32 at 0, lse_partial [B,Hq,S] fp32
+    at a 256-byte aligned offset after it, for the effective split count S."""
+    for B, Hq, Hkv, lmax, d, n in ((64, 32, 8, 8192, 128, 0), (64, 32, 8, 8192, 128, 5), (3, 4, 4, 1024, 64, 7),
+                                   (2, 16, 2, 2000, 256, 0), (1, 1, 1, 10, 128, 64)):
+        S = lib.sl8_attn_decode_num_splits(B, Hkv, lmax, d, n)
+        assert S >= 1
+        off = lib.sl8_attn_decode_lse_offset(B, Hq, Hkv, lmax, d, n)
+        size = lib.sl8_attn_decode_workspace_size(B, Hq, Hkv, lmax, d, n)
+        o_bytes = B * Hq * S * d * 4
+        assert off % 256 == 0 and o_bytes <= off < o_bytes + 256
+        assert size == off + B * Hq * S * 4
+    # invalid or unsupported shapes size to 0
+    assert lib.sl8_attn_decode_workspace_size(64, 30, 8, 8192, 128, 0) == 0   # Hq % Hkv != 0
+    assert lib.sl8_attn_decode_workspace_size(64, 32, 8, 8192, 96, 0) == 0    # head dim
+    assert lib.sl8_attn_decode_workspace_size(0, 32, 8, 8192, 128, 0) == 0
+    assert lib.sl8_attn_decode_workspace_size(4, 32, 8, 0, 128, 0) == 0

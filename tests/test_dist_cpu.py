@@ -22,12 +22,14 @@ def _free_port():
 
 
 def _rank_main(rank, world, port, out):
+    # CPU only wherever it runs: no GPU is visible to the ranks and the backend is gloo
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), WORLD_SIZE=str(world), RANK=str(rank),
-                      LOCAL_RANK=str(rank))
+                      LOCAL_RANK=str(rank), CUDA_VISIBLE_DEVICES="", SL8_DIST_BACKEND="gloo")
     sys.path.insert(0, ROOT)
     import torch.distributed as dist
     import bench
     w, r, local = bench.dist_setup(None)
+    assert dist.get_backend() == "gloo"
     assert (w, r, local) == (world, rank, rank)
     # a per-rank step time: the job's time is the slowest rank's
     got = bench.max_over_ranks(1.5 + 2.0 * rank, w)

@@ -115,31 +115,33 @@ def test_decode_partials_match_oracle_splits():
 
 
 def test_full_size_decode_workload():
+    """The benchmark decode (B64 Hq32 Hkv8 d128, L ~ U[1024, 8192]) in the bench's launch
+    configuration (automatic split count): every sequence and head against the oracle,
+    the int8 caches byte for byte, q codes, scales and every int32 logit bit for bit."""
     w = W.get("decode")
-    sample_b = [0, 1, 17, 63]
-    lens_np, g, gs, o, os_ = build_cache(w, w.lmax, batches=set(sample_b))
+    lens_np, g, gs, o, os_ = build_cache(w, w.lmax)
     q = W.decode_query(w)
     seq = torch.from_numpy(lens_np.astype(np.int32)).to(DEV)
-    o32 = sl8.attn_int8_decode(q.to(DEV), g["k"], gs["k"], g["v"], gs["v"], seq, out_dtype=torch.float32)
+    o32, lse = sl8.attn_int8_decode(q.to(DEV), g["k"], gs["k"], g["v"], gs["v"], seq, out_dtype=torch.float32,
+                                    return_lse=True)
     ob = sl8.attn_int8_decode(q.to(DEV), g["k"], gs["k"], g["v"], gs["v"], seq)
     dbg = sl8.attn_int8_decode_logits_debug(q.to(DEV), g["k"], gs["k"], g["v"], gs["v"], seq)
     torch.cuda.synchronize()
     st, site = sl8.last_device_status()
     assert st == sl8.SL8_OK, (st, site)
-    rows = [(b, h) for b in sample_b for h in range(w.Hq)]
-    ref = oracle.attn_decode(q.float().numpy(), o["k"], os_["k"], o["v"], os_["v"], lens_np, rows=rows,
-                             want_logits=True)
-    sel = np.zeros((w.B, w.Hq), bool)
-    for b, h in rows:
-        sel[b, h] = True
-    refo = np.where(sel[..., None], ref["out"], np.nan)
-    check_f32(to_np32(o32), refo, "decode full f32")
-    check_half(ob, refo, "decode full bf16")
+    for n in ("k", "v"):
+        np.testing.assert_array_equal(g[n].cpu().numpy(), o[n])
+        np.testing.assert_array_equal(gs[n].cpu().numpy(), os_[n])
+    ref = oracle.attn_decode(q.float().numpy(), o["k"], os_["k"], o["v"], os_["v"], lens_np, want_logits=True)
+    np.testing.assert_array_equal(dbg["q_codes"].cpu().numpy(), ref["q_codes"])
+    np.testing.assert_array_equal(dbg["q_scales"].cpu().numpy(), ref["q_scales"])
+    check_f32(to_np32(o32), ref["out"], "decode full f32, every sequence and head")
+    check_half(ob, ref["out"], "decode full bf16, every sequence and head")
+    np.testing.assert_allclose(to_np32(lse), ref["lse"], rtol=0, atol=1e-4)
     lg = dbg["logits"].cpu().numpy()
-    for (b, h) in rows:
-        np.testing.assert_array_equal(lg[b, h, :lens_np[b]], ref["logits"][(b, h)])
-    for b in sample_b:
-        np.testing.assert_array_equal(g["k"][b].cpu().numpy(), o["k"][b])
+    for b in range(w.B):
+        for h in range(w.Hq):
+            np.testing.assert_array_equal(lg[b, h, :lens_np[b]], ref["logits"][(b, h)], err_msg=f"logits {(b, h)}")
 
 
 # ---------------------------------------------------------------- paged (k8v8) cache

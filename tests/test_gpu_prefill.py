@@ -196,55 +196,139 @@ def test_guard_canaries_untouched():
     assert torch.all(buf[:1024] == 12345) and torch.all(buf[1024 + n:] == 12345)
 
 
-# ------------------------------------------------------------------ full-size workloads (sampled rows)
+# ------------------------------------------------------------------ full-size workloads (every row)
+#
+# At the benchmark sizes every output row is compared with the oracle (fp32 and bf16
+# outputs, LSE), the codes and scales of every Q and K row bit for bit, and the exact
+# int32 logits on a seeded sample: for every head the first and the last 128-row tile
+# and 64 random rows (whole rows, every key of the sequence), and for two heads every
+# diagonal 128 x 128 tile (the tiles the causal mask cuts).  Only these launches reach
+# late causal rows, run-time item claiming across all SMs, head pairs at G = 4 and the
+# d = 256 kernel's double S buffer.
+
+LOGIT_RANDOM_ROWS = 64
+TILE = 128
+
+
+def _logit_sample(rng, lens, Hq, diag_heads, packed=False):
+    """({(s, h): rows} whole-row sample, {(s, h): rows} diagonal-tile rows), rows being
+    indices within sequence s.  Per head: the first and the last 128-row tile and 64
+    random rows of every sequence (dense), or of the packed token stream (packed=True:
+    varlen input, whose first and last tiles then lie in its first and last sequences)."""
+    lens = [int(x) for x in lens]
+    starts = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    spans = [(0, int(starts[-1]))] if packed else [(int(starts[s]), int(starts[s + 1])) for s in range(len(lens))]
+    whole = {}
+    for h in range(Hq):
+        for a, e in spans:
+            picks = set(range(a, min(a + TILE, e))) | set(range(max(a, e - TILE), e))
+            picks |= set(int(t) for t in rng.integers(a, e, size=LOGIT_RANDOM_ROWS))
+            for t in picks:
+                s = int(np.searchsorted(starts, t, side="right") - 1)
+                whole.setdefault((s, h), set()).add(t - int(starts[s]))
+    diag = {(s, h): set(range(lens[s])) for (s, h) in diag_heads}
+    return ({k: sorted(v) for k, v in whole.items()}, {k: sorted(v) for k, v in diag.items()})
+
+
+def _gpu_logits(qd, kd, smooth, lens, N, whole, diag, cu=None, chunk=1024):
+    """Run the debug view in row chunks and keep, per (s, h), the whole rows of `whole`
+    ({(s, h, i): int32 [L_s]}) and, of `diag`, each row's diagonal tile
+    ({(s, h, i): int32 [tile width]})."""
+    got_whole, got_diag = {}, {}
+    ws = torch.empty(max(sl8.prefill_workspace_bytes(len(lens), qd.shape[-3] if cu is None else qd.shape[-2],
+                                                     kd.shape[1] if cu is None else kd.shape[-2], N, qd.shape[-1],
+                                                     0 if cu is None else qd.shape[0]), 16),
+                     dtype=torch.uint8, device=DEV)
+    for r0 in range(0, N, chunk):
+        r1 = min(N, r0 + chunk)
+        res = sl8.attn_int8_qk_logits_debug(qd, kd, smooth_k=smooth, row_begin=r0, row_end=r1, want_codes=False,
+                                            cu_seqlens=cu, max_seqlen=None if cu is None else N, workspace=ws)
+        lg = res["logits"]
+        for (s, h), rows in whole.items():
+            sel = [i for i in rows if r0 <= i < r1]
+            if sel:
+                block = lg[s, h, torch.tensor(sel, device=DEV) - r0, :lens[s]].cpu().numpy()
+                for i, row in zip(sel, block):
+                    got_whole[(s, h, i)] = row
+        for (s, h), rows in diag.items():
+            lo, hi = r0, min(r1, lens[s])
+            for t0 in range(lo, hi, TILE):
+                t1 = min(t0 + TILE, hi)
+                blk = lg[s, h, t0 - r0:t1 - r0, t0:min(t0 + TILE, lens[s])].cpu().numpy()
+                for i in range(t0, t1):
+                    got_diag[(s, h, i)] = blk[i - t0]
+        del res, lg
+    return got_whole, got_diag
+
+
+def _check_logits(q, k, v, smooth, got_whole, got_diag, whole, diag, lens, cu=None):
+    rows = [(s, h, i) for (s, h), rr in whole.items() for i in rr]
+    ref = oracle.attn_prefill(q, k, v, causal=False, smooth_k=smooth, rows=rows, want_logits=True,
+                              cu_seqlens=cu)
+    for key in rows:
+        np.testing.assert_array_equal(got_whole[key], ref["logits"][key], err_msg=f"logits row {key}")
+    del ref
+    for (s, h), rr in diag.items():
+        ref = oracle.attn_prefill(q, k, v, causal=False, smooth_k=smooth, rows=[(s, h, i) for i in rr],
+                                  want_logits=True, cu_seqlens=cu)
+        for i in rr:
+            t0 = i // TILE * TILE
+            want = ref["logits"][(s, h, i)][t0:min(t0 + TILE, lens[s])]
+            np.testing.assert_array_equal(got_diag[(s, h, i)], want, err_msg=f"diagonal tile row {(s, h, i)}")
+        del ref
+
 
 @pytest.mark.parametrize("name", ["qwen3_8b", "gemma3_d256"])
 def test_full_size_dense_workload(name):
     w = W.get(name)
     q, k, v = W.prefill_dense(w)
     qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
-    o32 = sl8.attn_int8_fwd(qd, kd, vd, causal=True, smooth_k=w.smooth_k, out_dtype=torch.float32)
+    o32, lse = sl8.attn_int8_fwd(qd, kd, vd, causal=True, smooth_k=w.smooth_k, out_dtype=torch.float32,
+                                 return_lse=True)
     oh = sl8.attn_int8_fwd(qd, kd, vd, causal=True, smooth_k=w.smooth_k)
-    dbg = sl8.attn_int8_qk_logits_debug(qd, kd, smooth_k=w.smooth_k, row_begin=w.N - 64, row_end=w.N)
+    codes = sl8.attn_int8_qk_logits_debug(qd, kd, smooth_k=w.smooth_k, row_begin=0, row_end=0, want_logits=False)
     torch.cuda.synchronize()
     _status_ok()
-    rng = np.random.default_rng(7)
-    rows = sample_rows(rng, [w.N] * w.B, w.Hq, per_head=6)
-    logit_rows = [(b, h, i) for b in range(w.B) for h in range(0, w.Hq, max(1, w.Hq // 4))
-                  for i in range(w.N - 64, w.N, 16)]
-    ref = oracle.attn_prefill(_np(q), _np(k), _np(v), causal=True, smooth_k=w.smooth_k, rows=rows)
-    np.testing.assert_array_equal(dbg["q_codes"].cpu().numpy(), ref["q_codes"])
-    np.testing.assert_array_equal(dbg["k_codes"].cpu().numpy(), ref["k_codes"])
-    np.testing.assert_array_equal(dbg["q_scales"].cpu().numpy(), ref["q_scales"])
-    np.testing.assert_array_equal(dbg["k_scales"].cpu().numpy(), ref["k_scales"])
-    sel = np.zeros(q.shape[:-1], bool)
-    for (b, h, i) in rows:
-        sel[b, h, i] = True
-    refo = np.where(sel[..., None], ref["out"], np.nan)
-    check_f32(to_np32(o32), refo, f"{name} f32")
-    check_half(oh, refo, f"{name} bf16")
-    lref = oracle.attn_prefill(_np(q), _np(k), _np(v), causal=False, smooth_k=w.smooth_k, rows=logit_rows,
-                               want_logits=True)
-    lg = dbg["logits"].cpu().numpy()
-    for (b, h, i) in logit_rows:
-        np.testing.assert_array_equal(lg[b, h, i - (w.N - 64)], lref["logits"][(b, h, i)])
+    qn, kn, vn = _np(q), _np(k), _np(v)
+    ref = oracle.attn_prefill(qn, kn, vn, causal=True, smooth_k=w.smooth_k)
+    for c in ("q_codes", "q_scales", "k_codes", "k_scales"):
+        np.testing.assert_array_equal(codes[c].cpu().numpy(), ref[c], err_msg=c)
+    check_f32(to_np32(o32), ref["out"], f"{name} f32, every row")
+    check_half(oh, ref["out"], f"{name} bf16, every row")
+    np.testing.assert_allclose(to_np32(lse), ref["lse"], rtol=0, atol=1e-4)
+    del ref, o32, oh, lse
+    whole, diag = _logit_sample(np.random.default_rng(7), [w.N] * w.B, w.Hq, [(0, 0), (w.B - 1, w.Hq - 1)])
+    got_whole, got_diag = _gpu_logits(qd, kd, w.smooth_k, [w.N] * w.B, w.N, whole, diag)
+    _status_ok()
+    _check_logits(qn, kn, vn, w.smooth_k, got_whole, got_diag, whole, diag, [w.N] * w.B)
 
 
 def test_full_size_varlen_workload():
     w = W.get("varlen")
     q, k, v, cu = W.prefill_varlen(w)
-    lens = np.diff(cu.numpy())
-    o32 = sl8.attn_int8_fwd(q.to(DEV), k.to(DEV), v.to(DEV), cu_seqlens=cu.to(DEV), max_seqlen=int(lens.max()),
-                            out_dtype=torch.float32)
-    oh = sl8.attn_int8_fwd(q.to(DEV), k.to(DEV), v.to(DEV), cu_seqlens=cu.to(DEV), max_seqlen=int(lens.max()))
+    lens = [int(x) for x in np.diff(cu.numpy())]
+    N = max(lens)
+    qd, kd, vd, cud = q.to(DEV), k.to(DEV), v.to(DEV), cu.to(DEV)
+    o32, lse = sl8.attn_int8_fwd(qd, kd, vd, cu_seqlens=cud, max_seqlen=N, out_dtype=torch.float32,
+                                 return_lse=True)
+    oh = sl8.attn_int8_fwd(qd, kd, vd, cu_seqlens=cud, max_seqlen=N)
+    codes = sl8.attn_int8_qk_logits_debug(qd, kd, smooth_k=True, row_begin=0, row_end=0, want_logits=False,
+                                          cu_seqlens=cud, max_seqlen=N)
     torch.cuda.synchronize()
     _status_ok()
-    rng = np.random.default_rng(8)
-    rows = sample_rows(rng, lens, w.Hq, per_head=2, edge=False)
-    rows += [(s, h, i) for s in (0, len(lens) - 1) for h in (0, w.Hq - 1) for i in range(min(3, lens[s]))]
-    ref = oracle.attn_prefill(_np(q), _np(k), _np(v), causal=True, smooth_k=True, cu_seqlens=cu.numpy(), rows=rows)
-    check_f32(to_np32(o32), ref["out"], "varlen full f32")
-    check_half(oh, ref["out"], "varlen full bf16")
+    qn, kn, vn = _np(q), _np(k), _np(v)
+    ref = oracle.attn_prefill(qn, kn, vn, causal=True, smooth_k=True, cu_seqlens=cu.numpy())
+    for c in ("q_codes", "q_scales", "k_codes", "k_scales"):
+        np.testing.assert_array_equal(codes[c].cpu().numpy(), ref[c], err_msg=c)
+    check_f32(to_np32(o32), ref["out"], "varlen f32, every row")
+    check_half(oh, ref["out"], "varlen bf16, every row")
+    np.testing.assert_allclose(to_np32(lse), ref["lse"], rtol=0, atol=1e-4)
+    del ref, o32, oh, lse
+    whole, diag = _logit_sample(np.random.default_rng(8), lens, w.Hq, [(0, 0), (len(lens) - 1, w.Hq - 1)],
+                                packed=True)
+    got_whole, got_diag = _gpu_logits(qd, kd, True, lens, N, whole, diag, cu=cud, chunk=256)
+    _status_ok()
+    _check_logits(qn, kn, vn, True, got_whole, got_diag, whole, diag, lens, cu=cu.numpy())
 
 
 # ------------------------------------------------------------------ query chunks (Nq < Nk)

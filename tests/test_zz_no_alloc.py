@@ -6,9 +6,10 @@ framework, a C caller without an allocator).  It keeps its split partials in a
 fixed array inside the library instead of caller scratch.  Its output must match
 the regular split + combine entry points within the tests' tolerance, on two calls
 in a row with different inputs (so stale scratch from the first call cannot leak
-into the second), including the largest case (d = 256, eight query heads per kv
-head), whose partials come closest to the array (the split count is lowered to fit
-it only on parts with more SMs than this one).
+into the second), including the largest ordinary case (d = 256, eight query heads
+per kv head) and a shape whose automatic split count asks for more partials than the
+array holds, so that the entry point has to lower it.  One call is also checked
+against the oracle directly.
 
 This file is named to be collected last; it also runs on its own in a fresh process.
 """
@@ -18,9 +19,10 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as W
 import w8a8_int8_flashattention_gb300 as sl8
-from _parity import check_f32, to_np32
+from _parity import check_f32, check_half, to_np32
 
 pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
@@ -56,7 +58,28 @@ def _noalloc(q, kc, ks, vc, vs, seq, out):
     _, Hkv, Lmax, _ = kc.shape
     return sl8.lib().sl8_attn_int8_decode_noalloc(
         q.data_ptr(), sl8.SL8_BF16, kc.data_ptr(), ks.data_ptr(), vc.data_ptr(), vs.data_ptr(), seq.data_ptr(),
-        B, Hq, Hkv, Lmax, d, out.data_ptr(), sl8.SL8_F32, torch.cuda.current_stream().cuda_stream)
+        B, Hq, Hkv, Lmax, d, out.data_ptr(), sl8._DTYPES[out.dtype], torch.cuda.current_stream().cuda_stream)
+
+
+def test_noalloc_decode_matches_oracle():
+    """fp32 and bf16 outputs of the no-allocation decode against the CPU oracle."""
+    wid, B, Hq, Hkv, d, lens, lmax = 7101, 3, 8, 2, 128, [900, 1, 333], 900
+    q, kc, ks, vc, vs, seq = _cache(wid, B, Hq, Hkv, d, lens, lmax)
+    w = W.custom(wid, kind="decode", B=B, Hq=Hq, Hkv=Hkv, d=d, dtype="bf16", extra={"lengths": lens})
+    ok = {n: np.zeros((B, Hkv, lmax, d), np.int8) for n in ("k", "v")}
+    os_ = {n: np.zeros((B, Hkv, lmax), np.float32) for n in ("k", "v")}
+    for b, L in enumerate(lens):
+        for n in ("k", "v"):
+            ok[n][b, :, :L], os_[n][b, :, :L] = oracle.quant_rowwise(W.decode_cache_values(w, b, n))
+    ref = oracle.attn_decode(q.float().cpu().numpy(), ok["k"], os_["k"], ok["v"], os_["v"], np.asarray(lens))
+    o32 = torch.full((B, Hq, d), float("nan"), dtype=torch.float32, device=DEV)
+    ob = torch.zeros((B, Hq, d), dtype=torch.bfloat16, device=DEV)
+    for out in (o32, ob):
+        rc = _noalloc(q, kc, ks, vc, vs, seq, out)
+        assert rc == sl8.SL8_OK, sl8.status_string(rc)
+    torch.cuda.synchronize()
+    check_f32(to_np32(o32), ref["out"], "noalloc vs oracle f32")
+    check_half(ob, ref["out"], "noalloc vs oracle bf16")
 
 
 def test_noalloc_decode_matches_regular_entry_points():
@@ -77,6 +100,36 @@ def test_noalloc_decode_matches_regular_entry_points():
         check_f32(to_np32(out), to_np32(ref).astype(np.float64), f"noalloc w{wid}")
         st, site = sl8.last_device_status()
         assert st == sl8.SL8_OK, (st, site)
+
+
+def test_noalloc_lowers_the_split_count_to_the_array():
+    """A shape whose automatic split count needs more partials than the array holds:
+    many sequences of one kv head, d = 256, Lmax just above 16 stages of 128 tokens.
+    The entry point lowers the count to fit and must still agree with the regular path
+    (which uses the full automatic count)."""
+    Hq, Hkv, d, lmax = 8, 1, 256, 2200
+    floats = SCRATCH_BYTES // 4
+    pick = None
+    for B in range(150, 400):
+        S = sl8.decode_num_splits(B, Hkv, lmax, d, 0)
+        if S > floats // (B * Hq * (d + 1)):
+            pick = B
+            break
+    assert pick is not None, "no shape in the searched range needs lowering on this part"
+    B = pick
+    rng = np.random.default_rng(7201)
+    lens = [int(x) for x in rng.integers(1, lmax + 1, size=B)]
+    lens[:4] = [lmax, 2100, 2049, 2150]
+    q, kc, ks, vc, vs, seq = _cache(7201, B, Hq, Hkv, d, lens, lmax)
+    ref = sl8.attn_int8_decode(q, kc, ks, vc, vs, seq, out_dtype=torch.float32)
+    for _ in range(2):
+        out = torch.full((B, Hq, d), float("nan"), dtype=torch.float32, device=DEV)
+        rc = _noalloc(q, kc, ks, vc, vs, seq, out)
+        assert rc == sl8.SL8_OK, sl8.status_string(rc)
+        torch.cuda.synchronize()
+        check_f32(to_np32(out), to_np32(ref).astype(np.float64), f"noalloc lowered B={B}")
+    st, site = sl8.last_device_status()
+    assert st == sl8.SL8_OK, (st, site)
 
 
 def test_noalloc_refuses_problems_beyond_the_array():

@@ -69,14 +69,16 @@ _SIGNATURES = {
                                  _INT, _P, _P, _SZ, _P]),
     "sl8_attn_int8_fwd_chunk": (_INT, [_P, _P, _P, _INT, _INT, _I32, _I32, _I32, _I32, _I32, _I32, _INT, _INT, _P,
                                        _INT, _P, _P, _SZ, _P]),
-    "sl8_attn_int8_qk_logits_debug": (_INT, [_P, _P, _INT, _I32, _I32, _I32, _I32, _I32, _INT, _I32, _I32, _P, _P,
-                                             _P, _P, _P, _P, _SZ, _P]),
+    "sl8_attn_int8_qk_logits_debug": (_INT, [_P, _P, _INT, _I32, _I32, _I32, _I32, _I32, _P, _I64, _INT, _I32, _I32,
+                                             _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "sl8_attn_w8a8_fwd": (_INT, [_P, _P, _P, _INT, _INT, _I32, _I32, _I32, _I32, _I32, _P, _I64, _INT, _INT, _I32,
                                  _I32, ctypes.c_float, _P, _INT, _P, _P, _SZ, _P]),
-    "sl8_attn_w8a8_qk_logits_debug": (_INT, [_P, _P, _INT, _I32, _I32, _I32, _I32, _I32, _INT, _I32, _I32,
-                                             ctypes.c_float, _I32, _I32, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "sl8_attn_w8a8_qk_logits_debug": (_INT, [_P, _P, _INT, _I32, _I32, _I32, _I32, _I32, _P, _I64, _INT, _I32,
+                                             _I32, ctypes.c_float, _I32, _I32, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "sl8_attn_decode_num_splits": (_I32, [_I32, _I32, _I32, _I32, _I32]),
     "sl8_attn_decode_split_size": (_I32, [_I32, _I32, _I32, _I32, _I32]),
+    "sl8_attn_decode_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
+    "sl8_attn_decode_lse_offset": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
     "sl8_attn_int8_decode_splitkv": (_INT, [_P, _INT, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P,
                                             _P, _P]),
     "sl8_attn_decode_verify_num_splits": (_I32, [_I32, _I32, _I32, _I32, _I32, _I32, _I32]),
@@ -283,34 +285,47 @@ def attn_int8_fwd_chunk(q, k, v, causal=True, smooth_k=True, out_dtype=None, ret
     return (out, lse) if return_lse else out
 
 
-def attn_int8_qk_logits_debug(q, k, smooth_k=True, row_begin=0, row_end=None, want_codes=True, groups=None):
+def attn_int8_qk_logits_debug(q, k, smooth_k=True, row_begin=0, row_end=None, want_codes=True, groups=None,
+                              cu_seqlens=None, max_seqlen=None, want_logits=True, workspace=None):
     """Exact int32 logits of the prefill tensor-core path for query rows
-    [row_begin, row_end) against every key (dense only), plus the int8 codes and
-    fp32 scales of Q and (smoothed) K.  groups = (q_group, k_group, q_outlier_ratio)
-    selects the grouped quantisation of attn_w8a8_fwd.  Returns a dict."""
-    _need_cuda(q, k)
-    B, Hq, N, d = q.shape
-    Hkv = k.shape[1]
+    [row_begin, row_end) of every sequence against every key of that sequence, plus the
+    int8 codes and fp32 scales of Q and (smoothed) K.  Dense q [B,Hq,N,d], k [B,Hkv,N,d],
+    or varlen q [T,Hq,d], k [T,Hkv,d] with cu_seqlens and max_seqlen; logits are
+    [B,Hq,row_end-row_begin,N] (entries past a sequence's length stay 0).
+    groups = (q_group, k_group, q_outlier_ratio) selects the grouped quantisation of
+    attn_w8a8_fwd.  Returns a dict."""
+    _need_cuda(q, k, cu_seqlens, workspace)
+    if cu_seqlens is None:
+        B, Hq, N, d = q.shape
+        T = 0
+        code_shape = lambda H: (B, H, N)  # noqa: E731
+    else:
+        T, Hq, d = q.shape
+        B = cu_seqlens.numel() - 1
+        if max_seqlen is None:
+            raise ValueError("varlen logits need max_seqlen")
+        N = int(max_seqlen)
+        code_shape = lambda H: (T, H)  # noqa: E731
+    Hkv = k.shape[-2] if cu_seqlens is not None else k.shape[1]
     row_end = N if row_end is None else row_end
     dev = q.device
-    logits = torch.zeros((B, Hq, row_end - row_begin, N), dtype=torch.int32, device=dev)
+    logits = (torch.zeros((B, Hq, row_end - row_begin, N), dtype=torch.int32, device=dev) if want_logits else None)
     res = dict(logits=logits)
     if want_codes:
-        res.update(q_codes=torch.empty((B, Hq, N, d), dtype=torch.int8, device=dev),
-                   q_scales=torch.empty((B, Hq, N), dtype=torch.float32, device=dev),
-                   k_codes=torch.empty((B, Hkv, N, d), dtype=torch.int8, device=dev),
-                   k_scales=torch.empty((B, Hkv, N), dtype=torch.float32, device=dev))
-    ws_bytes = prefill_workspace_bytes(B, Hq, Hkv, N, d, 0)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+        res.update(q_codes=torch.empty((*code_shape(Hq), d), dtype=torch.int8, device=dev),
+                   q_scales=torch.empty(code_shape(Hq), dtype=torch.float32, device=dev),
+                   k_codes=torch.empty((*code_shape(Hkv), d), dtype=torch.int8, device=dev),
+                   k_scales=torch.empty(code_shape(Hkv), dtype=torch.float32, device=dev))
+    ws_bytes = prefill_workspace_bytes(B, Hq, Hkv, N, d, T)
+    ws = workspace if workspace is not None else torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    head = (_ptr(q), _ptr(k), _dt(q), B, Hq, Hkv, N, d, _ptr(cu_seqlens), T, int(bool(smooth_k)))
     tail = (row_begin, row_end, _ptr(logits), _ptr(res.get("q_codes")), _ptr(res.get("q_scales")),
             _ptr(res.get("k_codes")), _ptr(res.get("k_scales")), _ptr(ws), ws.numel(), _stream(dev))
     if groups is None:
-        _check(lib().sl8_attn_int8_qk_logits_debug(_ptr(q), _ptr(k), _dt(q), B, Hq, Hkv, N, d, int(bool(smooth_k)),
-                                                   *tail), "sl8_attn_int8_qk_logits_debug")
+        _check(lib().sl8_attn_int8_qk_logits_debug(*head, *tail), "sl8_attn_int8_qk_logits_debug")
     else:
         g = (int(groups[0]), int(groups[1]), float(groups[2]))
-        _check(lib().sl8_attn_w8a8_qk_logits_debug(_ptr(q), _ptr(k), _dt(q), B, Hq, Hkv, N, d, int(bool(smooth_k)),
-                                                   *g, *tail), "sl8_attn_w8a8_qk_logits_debug")
+        _check(lib().sl8_attn_w8a8_qk_logits_debug(*head, *g, *tail), "sl8_attn_w8a8_qk_logits_debug")
     return res
 
 
@@ -321,6 +336,21 @@ def decode_num_splits(B: int, Hkv: int, Lmax: int, d: int, num_splits: int = 0) 
     return int(lib().sl8_attn_decode_num_splits(B, Hkv, Lmax, d, num_splits))
 
 
+def decode_workspace(B: int, Hq: int, Hkv: int, Lmax: int, d: int, num_splits: int = 0, device=None):
+    """The decode's split partials carved from one buffer of
+    sl8_attn_decode_workspace_size bytes: (o_partial [B,Hq,S,d], lse_partial [B,Hq,S])
+    fp32 views, at the offsets the header states."""
+    S = decode_num_splits(B, Hkv, Lmax, d, num_splits)
+    nbytes = int(lib().sl8_attn_decode_workspace_size(B, Hq, Hkv, Lmax, d, num_splits))
+    off = int(lib().sl8_attn_decode_lse_offset(B, Hq, Hkv, Lmax, d, num_splits))
+    if S <= 0 or nbytes == 0:
+        raise SL8Error(SL8_ERR_UNSUPPORTED, "sl8_attn_decode_workspace_size")
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    o_partial = ws[:B * Hq * S * d * 4].view(torch.float32).view(B, Hq, S, d)
+    lse_partial = ws[off:off + B * Hq * S * 4].view(torch.float32).view(B, Hq, S)
+    return o_partial, lse_partial
+
+
 def attn_int8_decode_splitkv(q, k_cache, k_scale, v_cache, v_scale, seqlens, num_splits=0, o_partial=None,
                              lse_partial=None):
     """Split-KV partials (normalised O [B,Hq,S,d] fp32, lse [B,Hq,S] fp32)."""
@@ -328,6 +358,8 @@ def attn_int8_decode_splitkv(q, k_cache, k_scale, v_cache, v_scale, seqlens, num
     B, Hq, d = q.shape
     _, Hkv, Lmax, _ = k_cache.shape
     S = decode_num_splits(B, Hkv, Lmax, d, num_splits)
+    if o_partial is None and lse_partial is None and S > 0:
+        o_partial, lse_partial = decode_workspace(B, Hq, Hkv, Lmax, d, num_splits, q.device)
     if o_partial is None:
         o_partial = torch.empty((B, Hq, max(S, 1), d), dtype=torch.float32, device=q.device)
     if lse_partial is None:

@@ -461,30 +461,34 @@ int sl8_attn_w8a8_fwd(const void* q, const void* k, const void* v, int qk_dtype,
 }
 
 static int qk_logits_debug(const void* q, const void* k, int qk_dtype, int32_t B, int32_t Hq, int32_t Hkv, int32_t N,
-                           int32_t d, int smooth_k, int32_t row_begin, int32_t row_end, int32_t* logits_out,
-                           int8_t* q_codes, float* q_scales, int8_t* k_codes, float* k_scales, void* workspace,
-                           size_t workspace_bytes, void* stream, const QuantGroups& groups) {
+                           int32_t d, const int32_t* cu_seqlens, int64_t total_tokens, int smooth_k,
+                           int32_t row_begin, int32_t row_end, int32_t* logits_out, int8_t* q_codes, float* q_scales,
+                           int8_t* k_codes, float* k_scales, void* workspace, size_t workspace_bytes, void* stream,
+                           const QuantGroups& groups) {
   int rc = validate_prefill(q, k, qk_dtype, B, Hq, Hkv, N, d);
   if (rc != SL8_OK) return rc;
+  const bool varlen = cu_seqlens != nullptr;
   SL8_CHECK(0 <= row_begin && row_begin <= row_end && row_end <= N, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(!varlen || total_tokens >= 0, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(!varlen || total_tokens < (1ll << 31), SL8_ERR_UNSUPPORTED);
   SL8_CHECK(static_cast<int64_t>(B) * N < (1ll << 31), SL8_ERR_UNSUPPORTED);
   SL8_CHECK(!q_codes == !q_scales && !k_codes == !k_scales, SL8_ERR_INVALID_ARG);
-  if (B == 0 || N == 0) return SL8_OK;
+  if (B == 0 || N == 0 || (varlen && total_tokens == 0)) return SL8_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   PrefillWorkspace p;
   SeqTable t;
-  rc = prefill_prepare(q, k, nullptr, qk_dtype, qk_dtype, B, Hq, Hkv, N, d, nullptr, 0, smooth_k, workspace,
-                       workspace_bytes, s, true, &p, &t, 0, groups);
+  rc = prefill_prepare(q, k, nullptr, qk_dtype, qk_dtype, B, Hq, Hkv, N, d, cu_seqlens, total_tokens, smooth_k,
+                       workspace, workspace_bytes, s, true, &p, &t, 0, groups);
   if (rc != SL8_OK) return rc;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int32_t dc = compute_dim(d);
   if (q_codes)
     SL8_LAUNCH(launch_export_codes(reinterpret_cast<const uint16_t*>(ws + p.q_codes),
-                                   reinterpret_cast<const float*>(ws + p.q_scales), false, B, Hq, N, dc, t,
+                                   reinterpret_cast<const float*>(ws + p.q_scales), varlen, B, Hq, N, dc, t,
                                    p.t_pad_max, q_codes, q_scales, s, d));
   if (k_codes)
     SL8_LAUNCH(launch_export_codes(reinterpret_cast<const uint16_t*>(ws + p.k_codes),
-                                   reinterpret_cast<const float*>(ws + p.k_scales), false, B, Hkv, N, dc, t,
+                                   reinterpret_cast<const float*>(ws + p.k_scales), varlen, B, Hkv, N, dc, t,
                                    p.t_pad_max, k_codes, k_scales, s, d));
   if (logits_out && row_end > row_begin) {
     PrefillArgs a{};
@@ -497,14 +501,14 @@ static int qk_logits_debug(const void* q, const void* k, int qk_dtype, int32_t B
     a.v = nullptr;
     a.v_dtype = SL8_F16;
     a.v16 = reinterpret_cast<const uint16_t*>(ws + p.q_codes);
-    a.varlen = false;
+    a.varlen = varlen;
     a.nseq = B;
     a.Hq = Hq;
     a.Hkv = Hkv;
     a.N = N;
     a.d = dc;
     a.d_io = d;
-    a.total_tokens = static_cast<int64_t>(B) * N;
+    a.total_tokens = varlen ? total_tokens : static_cast<int64_t>(B) * N;
     a.t_pad_max = p.t_pad_max;
     a.table = t;
     a.dense_items = (N + prefill_item_rows(dc, Hq / Hkv) - 1) / prefill_item_rows(dc, Hq / Hkv);
@@ -523,23 +527,26 @@ static int qk_logits_debug(const void* q, const void* k, int qk_dtype, int32_t B
 }
 
 int sl8_attn_int8_qk_logits_debug(const void* q, const void* k, int qk_dtype, int32_t B, int32_t Hq, int32_t Hkv,
-                                  int32_t N, int32_t d, int smooth_k, int32_t row_begin, int32_t row_end,
-                                  int32_t* logits_out, int8_t* q_codes, float* q_scales, int8_t* k_codes,
-                                  float* k_scales, void* workspace, size_t workspace_bytes, void* stream) {
-  return qk_logits_debug(q, k, qk_dtype, B, Hq, Hkv, N, d, smooth_k, row_begin, row_end, logits_out, q_codes,
-                         q_scales, k_codes, k_scales, workspace, workspace_bytes, stream, QuantGroups());
+                                  int32_t N, int32_t d, const int32_t* cu_seqlens, int64_t total_tokens, int smooth_k,
+                                  int32_t row_begin, int32_t row_end, int32_t* logits_out, int8_t* q_codes,
+                                  float* q_scales, int8_t* k_codes, float* k_scales, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  return qk_logits_debug(q, k, qk_dtype, B, Hq, Hkv, N, d, cu_seqlens, total_tokens, smooth_k, row_begin, row_end,
+                         logits_out, q_codes, q_scales, k_codes, k_scales, workspace, workspace_bytes, stream,
+                         QuantGroups());
 }
 
 int sl8_attn_w8a8_qk_logits_debug(const void* q, const void* k, int qk_dtype, int32_t B, int32_t Hq, int32_t Hkv,
-                                  int32_t N, int32_t d, int smooth_k, int32_t q_group, int32_t k_group,
-                                  float q_outlier_ratio, int32_t row_begin, int32_t row_end, int32_t* logits_out,
-                                  int8_t* q_codes, float* q_scales, int8_t* k_codes, float* k_scales,
-                                  void* workspace, size_t workspace_bytes, void* stream) {
+                                  int32_t N, int32_t d, const int32_t* cu_seqlens, int64_t total_tokens, int smooth_k,
+                                  int32_t q_group, int32_t k_group, float q_outlier_ratio, int32_t row_begin,
+                                  int32_t row_end, int32_t* logits_out, int8_t* q_codes, float* q_scales,
+                                  int8_t* k_codes, float* k_scales, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
   QuantGroups g;
   const int rc = make_groups(q_group, k_group, q_outlier_ratio, &g);
   if (rc != SL8_OK) return rc;
-  return qk_logits_debug(q, k, qk_dtype, B, Hq, Hkv, N, d, smooth_k, row_begin, row_end, logits_out, q_codes,
-                         q_scales, k_codes, k_scales, workspace, workspace_bytes, stream, g);
+  return qk_logits_debug(q, k, qk_dtype, B, Hq, Hkv, N, d, cu_seqlens, total_tokens, smooth_k, row_begin, row_end,
+                         logits_out, q_codes, q_scales, k_codes, k_scales, workspace, workspace_bytes, stream, g);
 }
 
 // The split plan.  split_size_for(Lmax, S, d) = ceil(Lmax / S) rounded up to a whole
@@ -575,6 +582,21 @@ int32_t sl8_attn_decode_num_splits(int32_t B, int32_t Hkv, int32_t Lmax, int32_t
 int32_t sl8_attn_decode_split_size(int32_t B, int32_t Hkv, int32_t Lmax, int32_t d, int32_t num_splits) {
   const int32_t S = sl8_attn_decode_num_splits(B, Hkv, Lmax, d, num_splits);
   return S > 0 ? split_size_for(Lmax, S, d) : 0;
+}
+
+size_t sl8_attn_decode_lse_offset(int32_t B, int32_t Hq, int32_t Hkv, int32_t Lmax, int32_t d, int32_t num_splits) {
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv) return 0;
+  const int32_t S = sl8_attn_decode_num_splits(B, Hkv, Lmax, d, num_splits);
+  if (S <= 0) return 0;
+  return align_up(static_cast<size_t>(B) * Hq * S * d * sizeof(float), 256);
+}
+
+size_t sl8_attn_decode_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t Lmax, int32_t d,
+                                      int32_t num_splits) {
+  const size_t off = sl8_attn_decode_lse_offset(B, Hq, Hkv, Lmax, d, num_splits);
+  if (!off) return 0;
+  const int32_t S = sl8_attn_decode_num_splits(B, Hkv, Lmax, d, num_splits);
+  return off + static_cast<size_t>(B) * Hq * S * sizeof(float);
 }
 
 // A paged cache (see DecodeArgs): the block table and the page geometry.
