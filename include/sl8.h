@@ -53,7 +53,7 @@ extern "C" {
 typedef enum sl8_status {
   SL8_OK = 0,
   SL8_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad shape or dtype, Hq % Hkv != 0 */
-  SL8_ERR_UNSUPPORTED = 2, /* valid but not implemented here (e.g. d = 32, Hq/Hkv > 8 in decode) */
+  SL8_ERR_UNSUPPORTED = 2, /* valid but not implemented here (e.g. d = 32 in decode) */
   SL8_ERR_WORKSPACE = 3,   /* workspace missing or smaller than the size query returned */
   SL8_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
   SL8_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up (see sl8_last_device_status) */
@@ -232,7 +232,10 @@ SL8_API int sl8_attn_w8a8_qk_logits_debug(const void* q, const void* k, int qk_d
  *   o_partial          device, [B][Hq][S][d] fp32; each non-empty split's normalised partial
  *                      (the O of an empty split is not written).
  *   lse_partial        device, [B][Hq][S] fp32 log-sum-exp per split (-inf if empty).
- * Hq / Hkv must be at most 8 (SL8_ERR_UNSUPPORTED otherwise).
+ * GQA and MQA: any Hq that is a multiple of Hkv.  A work slot of the split kernel holds at
+ * most 8 query heads, so with G = Hq / Hkv > 8 each kv head's G query heads are cut into
+ * the fewest equal groups of at most 8 (G = 16: 2 groups of 8; G = 32: 4; G = 12: 2 of 6)
+ * and each group streams that kv head's cache: the cache is read once per group.
  */
 SL8_API int32_t sl8_attn_decode_num_splits(int32_t B, int32_t Hkv, int32_t Lmax, int32_t d, int32_t num_splits);
 SL8_API int32_t sl8_attn_decode_split_size(int32_t B, int32_t Hkv, int32_t Lmax, int32_t d, int32_t num_splits);
@@ -273,7 +276,8 @@ SL8_API int sl8_attn_int8_decode_splitkv(const void* q, int q_dtype, const int8_
  *   out        device, [B][T][Hq][d] of out_dtype (F16, BF16 or F32); lse_out nullable
  *              [B][T][Hq].
  * Runs the split kernel and the combine.  A work slot takes min(T, 8 / (Hq / Hkv)) draft
- * queries beside their query heads, so sequence b's cache is read ceil(T / that) times.
+ * queries beside their query heads, so sequence b's cache is read ceil(T / that) times;
+ * Hq / Hkv must be at most 8 (SL8_ERR_UNSUPPORTED otherwise).
  */
 SL8_API int32_t sl8_attn_decode_verify_num_splits(int32_t B, int32_t T, int32_t Hq, int32_t Hkv, int32_t Lmax,
                                                   int32_t d, int32_t num_splits);

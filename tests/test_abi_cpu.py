@@ -154,8 +154,11 @@ def test_decode_and_quant_argument_errors(lib):
     ok_args = [p, sl8.SL8_BF16, p, p, p, p, p, 64, 32, 8, 8192, 128, 0, p, p, None]
     a = list(ok_args); a[0] = None
     assert f(*a) == sl8.SL8_ERR_INVALID_ARG
-    a = list(ok_args); a[8] = 64; a[9] = 4                   # Hq/Hkv = 16 > 8
-    assert f(*a) == sl8.SL8_ERR_UNSUPPORTED
+    a = list(ok_args); a[8] = 30; a[9] = 4                   # Hq not a multiple of Hkv
+    assert f(*a) == sl8.SL8_ERR_INVALID_ARG
+    vf = lib.sl8_attn_int8_decode_verify                     # verify: Hq/Hkv = 16 > 8 is refused
+    assert vf(p, sl8.SL8_BF16, p, p, p, p, p, p, 4, 64, 64, 4, 8192, 128, 0, p, p, p, sl8.SL8_BF16, None,
+              None) == sl8.SL8_ERR_UNSUPPORTED
     a = list(ok_args); a[11] = 80
     assert f(*a) == sl8.SL8_ERR_UNSUPPORTED
     a = list(ok_args); a[7] = 0

@@ -57,6 +57,10 @@ CASES = [
     (3002, 3, 4, 4, 64, [513, 1, 1024], 1024),
     (3003, 3, 8, 1, 256, [129, 300, 5], 300),
     (3004, 2, 16, 2, 128, [2000, 77], 2000),
+    # MQA beyond 8 query heads per kv head: virtual kv heads of <= 8 query heads each
+    (3005, 3, 32, 1, 128, [900, 1, 333], 900),          # G = 32: four groups of 8
+    (3006, 2, 64, 4, 64, [700, 129], 700),               # G = 16: two groups of 8
+    (3007, 2, 12, 1, 256, [300, 17], 300),               # G = 12: two groups of 6
 ]
 
 
@@ -153,6 +157,7 @@ PAGED = [
     (3203, 3, 8, 1, 256, [129, 300, 5], 32, 10, 0),
     (3204, 4, 16, 2, 128, [2000, 77, 160, 161], 256, 8, 0),
     (3205, 4, 8, 2, 128, [900, 640, 1000, 700], 128, 8, 5),
+    (3206, 3, 32, 2, 128, [700, 33, 1000], 64, 16, 0),   # G = 16 over a paged cache
 ]
 
 
@@ -231,6 +236,7 @@ F16V = [
     (3402, 3, 4, 4, 64, [513, 1, 1024], 1024),
     (3403, 2, 16, 2, 128, [2000, 77], 2000),
     (3404, 3, 8, 8, 64, [160, 161, 3000], 3000),
+    (3405, 2, 32, 1, 128, [1500, 200], 1500),           # G = 32 with an fp16 V cache
 ]
 
 

@@ -344,17 +344,21 @@ static int prefill_prepare(const void* q, const void* k, const void* v, int qk_d
                                s));
   float* k_partials = smooth_k ? reinterpret_cast<float*>(ws + p.k_partials) : nullptr;
   float* v_partials = v_stats ? reinterpret_cast<float*>(ws + p.v_partials) : nullptr;
-  if (smooth_k || v_stats)
+  if (smooth_k || v_stats) {
     SL8_LAUNCH(launch_kv_partials(k, static_cast<sl8_dtype>(qk_dtype), v_stats ? v : nullptr, varlen, B, Hkv, N, d,
                                   varlen ? t.len : nullptr, varlen ? t.tok0 : nullptr, k_partials, v_partials,
                                   p.max_chunks, s));
+    SL8_LAUNCH(launch_kv_finalize(varlen, B, Hkv, N, d, varlen ? t.len : nullptr, k_partials, v_partials, p.max_chunks,
+                                  reinterpret_cast<float*>(ws + p.k_mean), reinterpret_cast<int32_t*>(ws + p.v_exp),
+                                  s));
+  }
   SL8_LAUNCH(launch_quant_qk(q, k, static_cast<sl8_dtype>(qk_dtype), varlen, B, Hq, Hkv, N, dc, tokens, t,
                              p.t_pad_max, k_partials, v_partials, p.max_chunks,
                              reinterpret_cast<uint16_t*>(ws + p.q_codes), reinterpret_cast<float*>(ws + p.q_scales),
                              reinterpret_cast<uint16_t*>(ws + p.k_codes), reinterpret_cast<float*>(ws + p.k_scales),
                              convert_v ? v : nullptr, convert_v ? reinterpret_cast<int32_t*>(ws + p.v_exp) : nullptr,
                              convert_v ? reinterpret_cast<uint16_t*>(ws + p.v16) : nullptr, s, q_off, d,
-                             v_dtype == SL8_F16, groups));
+                             v_dtype == SL8_F16, groups, smooth_k ? reinterpret_cast<float*>(ws + p.k_mean) : nullptr));
   *plan = p;
   *table = t;
   return SL8_OK;
@@ -605,6 +609,17 @@ struct Paging {
   int32_t page_size, max_blocks, num_pages;
 };
 
+// Virtual kv heads per cache kv head: a work slot of the split kernel holds at most 8 query
+// heads, so a kv head with G = Hq / Hkv > 8 query heads is split into the fewest equal
+// groups of <= 8 (the smallest divisor ng of G with G / ng <= 8); each group streams the
+// kv head's cache once.  1 for G <= 8.
+static int32_t decode_kv_groups(int32_t Hq, int32_t Hkv) {
+  const int32_t G = Hkv > 0 ? Hq / Hkv : 1;
+  int32_t ng = (G + 7) / 8;
+  while (ng < G && G % ng) ++ng;
+  return ng < 1 ? 1 : ng;
+}
+
 static int decode_validate(const void* q, int q_dtype, const void* k_cache, const float* k_scale, const void* v_cache,
                            const float* v_scale, const int32_t* seqlens, int32_t B, int32_t Hq, int32_t Hkv,
                            int32_t Lmax, int32_t d, const Paging* pg, bool v16) {
@@ -615,8 +630,7 @@ static int decode_validate(const void* q, int q_dtype, const void* k_cache, cons
   SL8_CHECK(B >= 0 && Hq > 0 && Hkv > 0 && Lmax >= 0 && d > 0, SL8_ERR_INVALID_ARG);
   SL8_CHECK(Hq % Hkv == 0, SL8_ERR_INVALID_ARG);
   SL8_CHECK(head_dim_ok(d), SL8_ERR_UNSUPPORTED);
-  SL8_CHECK(Hq / Hkv <= 8, SL8_ERR_UNSUPPORTED);
-  SL8_CHECK(B <= 65535 && Hkv <= 65535, SL8_ERR_UNSUPPORTED);
+  SL8_CHECK(B <= 65535 && static_cast<int64_t>(Hkv) * decode_kv_groups(Hq, Hkv) <= 65535, SL8_ERR_UNSUPPORTED);
   if (pg) {
     // pages are loaded in 16-token units (TMA rows, 64-byte scale pieces)
     SL8_CHECK(pg->table && pg->page_size > 0 && pg->max_blocks > 0 && pg->num_pages > 0, SL8_ERR_INVALID_ARG);
@@ -661,6 +675,10 @@ static int decode_launch(const void* q, int q_dtype, const int8_t* k_cache, cons
   a.split_size = sl8_attn_decode_split_size(B, Hkv, Lmax, d, num_splits);
   a.num_splits = sl8_attn_decode_num_splits(B, Hkv, Lmax, d, num_splits);
   SL8_CHECK(a.num_splits > 0 && a.num_splits <= 65535, SL8_ERR_UNSUPPORTED);
+  // MQA beyond 8 query heads per kv head: virtual kv heads (the split plan above stays that
+  // of the caller's Hkv, so the partials keep the size the queries report)
+  a.kv_groups = decode_kv_groups(Hq, Hkv);
+  a.Hkv = Hkv * a.kv_groups;
   a.o_partial = o_partial;
   a.lse_partial = lse_partial;
   a.logits = logits;
@@ -699,6 +717,7 @@ int sl8_attn_int8_decode_verify(const void* q, int q_dtype, const int8_t* k_cach
   SL8_CHECK(tree_mask && out, SL8_ERR_INVALID_ARG);
   SL8_CHECK(out_dtype == SL8_F16 || out_dtype == SL8_BF16 || out_dtype == SL8_F32, SL8_ERR_INVALID_ARG);
   SL8_CHECK(Hkv > 0 && Hq % Hkv == 0, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(Hq / Hkv <= 8, SL8_ERR_UNSUPPORTED);  // drafts share a slot's 8 query columns with their heads
   // the drafts of sequence b go dps at a time into one slot's query columns: virtual
   // sequences b * ng + group (q [B][T][Hq][d])
   const int32_t dps = verify_dps(T, Hq, Hkv), ng = (T + dps - 1) / dps;

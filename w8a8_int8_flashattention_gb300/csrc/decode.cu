@@ -504,7 +504,8 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
     while (ok && has_cur) {
       const bool has_nxt = next_entry(nxt);
       if (!ok || !announce(nxt, n + 1)) break;
-      const int64_t row0 = (static_cast<int64_t>(cache_seq(a, cur.b)) * a.Hkv + cur.hkv) * a.Lmax;
+      const int64_t row0 = (static_cast<int64_t>(cache_seq(a, cur.b)) * (a.Hkv / a.kv_groups) + cur.hkv / a.kv_groups) *
+                           a.Lmax;
       for (int c0 = cur.t0; c0 < cur.t1 && ok; c0 += C::kChunk, ++k) {
         const int nt = min(C::kChunk, cur.t1 - c0);
         const uint32_t stg = k % kStages;
@@ -531,7 +532,8 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
               record_status(st, kStatusBadArg, 49);
               pg = 0;
             }
-            const int64_t prow = (static_cast<int64_t>(pg) * a.Hkv + cur.hkv) * a.page_size + t % a.page_size;
+            const int64_t prow = (static_cast<int64_t>(pg) * (a.Hkv / a.kv_groups) + cur.hkv / a.kv_groups) * a.page_size +
+                                 t % a.page_size;
             for (int r = 0; r < rows;) {
               const int left = rows - r;
               const int i = left >= 128 ? 3 : left >= 64 ? 2 : left >= 32 ? 1 : 0;
@@ -1171,8 +1173,9 @@ cudaError_t launch_split_d(const DecodeArgs& a, cudaStream_t s) {
   // C::kChunk rows x kBW bytes; a paged cache as [num_pages * Hkv * page_size rows][d],
   // loaded in boxes of one 16-token unit
   const bool paged = a.block_table != nullptr;
-  const uint64_t rows = paged ? static_cast<uint64_t>(a.num_pages) * a.Hkv * a.page_size
-                              : static_cast<uint64_t>(a.B) * a.Hkv * a.Lmax;
+  const uint64_t hkv_cache = static_cast<uint64_t>(a.Hkv / a.kv_groups);  // kv heads the cache holds
+  const uint64_t rows = paged ? static_cast<uint64_t>(a.num_pages) * hkv_cache * a.page_size
+                              : static_cast<uint64_t>(a.B) * hkv_cache * a.Lmax;
   bool ok = true;
   CacheMaps maps;
   memset(&maps, 0, sizeof(maps));

@@ -95,6 +95,7 @@ extern "C" int sl8_attn_int8_decode_noalloc(const void* q, int q_dtype, const in
   a.d = d;
   a.num_splits = sl8_attn_decode_num_splits(B, Hkv, Lmax, d, S);  // <= S: fits the array
   a.split_size = sl8_attn_decode_split_size(B, Hkv, Lmax, d, S);
+  a.kv_groups = 1;
   a.o_partial = o_partial;
   a.lse_partial = lse_partial;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -999,6 +999,432 @@ __global__ void __launch_bounds__(kQuantWarps * 32, D == 256 ? 2 : (kGroups ? 4 
   }
 }
 
+// ---------------------------------------------------------------- K mean and V exponent
+// One CTA per (sequence, kv head): the K mean = (the chunk sums of k_partials added in
+// chunk order) / L per channel, and the V exponent e >= 0 with max|V| * 2^-e <= 2^15
+// from the chunk maxima of v_partials (e = 0 without them).  Both are read by the K units
+// of the quantiser and v_exp by the attention kernel.
+__global__ void __launch_bounds__(128) kv_finalize_kernel(bool varlen, int32_t Hkv, int32_t N, int32_t d_io,
+                                                          const int32_t* __restrict__ len,
+                                                          const float* __restrict__ k_partials,
+                                                          const float* __restrict__ v_partials, int32_t max_chunks,
+                                                          float* __restrict__ mean, int32_t* __restrict__ v_exp) {
+  __shared__ float s_max[4];
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const int h = blockIdx.x, s = blockIdx.y, tid = threadIdx.x;
+  const int L = varlen ? len[s] : N;
+  const int nch = (L + kMeanChunk - 1) / kMeanChunk;
+  const int64_t row = static_cast<int64_t>(s) * Hkv + h;
+  if (k_partials) {
+    for (int c = tid; c < d_io; c += blockDim.x) {
+      const float* p = k_partials + row * max_chunks * d_io + c;
+      float total = 0.0f;
+      // 64 chunk sums in flight per round trip (a 4096-token sequence in one), added in order
+      for (int cb = 0; cb < nch; cb += 64) {
+        float x[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) x[i] = cb + i < nch ? p[static_cast<int64_t>(cb + i) * d_io] : 0.0f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          if (cb + i < nch) total = __fadd_rn(total, x[i]);
+      }
+      mean[row * d_io + c] = L > 0 ? __fdiv_rn(total, static_cast<float>(L)) : 0.0f;
+    }
+  }
+  float m = 0.0f;
+  if (v_partials)
+    for (int cb = tid; cb < nch; cb += blockDim.x) m = fmaxf(m, v_partials[row * max_chunks + cb]);
+  m = warp_max(m);
+  if ((tid & 31) == 0) s_max[tid / 32] = m;
+  __syncthreads();
+  if (tid == 0) {
+    for (int w = 1; w < 4; ++w) m = fmaxf(m, s_max[w]);
+    int e = 0;
+    if (m > 0.0f) {
+      int k2 = 0;
+      frexpf(m, &k2);  // m < 2^k2
+      e = k2 > 15 ? k2 - 15 : 0;
+    }
+    v_exp[row] = e;
+  }
+}
+
+// ---------------------------------------------------------------- prefill codes, pipelined
+// Persistent CTAs walk the 64-row blocks ("units") of the code workspace: first those of
+// every Q head, then those of every K head.  A producer warp stages each unit's input rows
+// (and, for a K unit whose V is converted, the same rows of V) in shared memory with bulk
+// copies, kStages units ahead; eight consumer warps turn a staged unit into codes and
+// scales (and fp16 V), eight lanes per row, while the next units load.  K units read the
+// K mean and the V exponent that kv_finalize_kernel wrote (they wait for it, and through
+// it for the K/V chunk kernel, before their first unit), so Q units overlap those kernels.
+// The arithmetic is that of the per-row reading: s = max|x| / 127 (IEEE division), codes
+// RNE(x / s) formed as x * (1/s) and checked against the half-integer boundaries (the
+// exact quotient is formed for the few values near one), smoothed K = K - mean in fp32.
+constexpr int kQpRows = 64;       // rows per unit (a unit never straddles two sequences)
+constexpr int kQpConsumers = 8;   // consumer warps: 8 rows each, two passes of four
+
+// The unit's place, decoded once by the producer and handed to the consumers in the
+// unit's shared-memory stage.
+struct QpUnit {
+  int32_t is_k, h, s, L, tk, t0, vexp, pad;
+  int64_t row0;
+};
+
+template <int D>
+struct QpCfg {
+  static constexpr int kUnitBytes = kQpRows * D * 2;       // staged rows of <= D 16-bit values
+  static constexpr int kStages = D == 256 ? 2 : (D == 128 ? 3 : 4);
+  static constexpr int kMeanOff = 2 * kUnitBytes;          // input rows, V rows, K mean row
+  static constexpr int kInfoOff = kMeanOff + D * 4;
+  static constexpr int kStageBytes = kInfoOff + 128;
+  static constexpr int kSmem = kStages * kStageBytes + 128;
+  static constexpr int kThreads = (kQpConsumers + 1) * 32;
+  static constexpr int kCtasPerSm = D == 256 ? 1 : 2;
+  static_assert(kCtasPerSm * (kSmem + 1024) <= 232448, "quantiser shared memory");
+  static_assert(kStageBytes % 16 == 0 && sizeof(QpUnit) <= 128, "stage layout");
+};
+
+template <sl8_dtype DT, int D, bool kGroups>
+__global__ void __launch_bounds__(QpCfg<D>::kThreads, QpCfg<D>::kCtasPerSm)
+    quant_qk_pipe_kernel(const QuantQK a, const float* __restrict__ k_mean, DeviceStatus* st, uint64_t limit_ns) {
+  using C = QpCfg<D>;
+  constexpr int LPR = 8, NV = D / 64, RPP = 32 / LPR, P = kQpRows / kQpConsumers / RPP;
+  extern __shared__ __align__(128) uint8_t qp_smem[];
+  __shared__ uint64_t full[C::kStages], empty[C::kStages];
+  __shared__ __align__(16) float s_am[kQpRows];
+  __shared__ float s_med[kQpRows], s_sc[kQpRows];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+  // without the K/V chunk kernels before it, this kernel is the first to touch the
+  // workspace after the previous attention launch read it: every unit waits
+  const bool chained = a.k_partials || a.v_partials;
+  if (!chained) grid_dependency_wait();
+  grid_dependents_launch();
+  if (blockIdx.x == 0 && threadIdx.x == 0) a.t.counts[2] = 0;  // the attention kernel's item counter
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kQpConsumers);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const int32_t seq_rows = (a.N + kQTile - 1) / kQTile * kPadRows;
+  const int64_t rows_all = a.varlen ? static_cast<int64_t>(a.t.counts[1]) : static_cast<int64_t>(a.nseq) * seq_rows;
+  const int64_t rows_used = rows_all < a.t_pad_max ? rows_all : a.t_pad_max;
+  const int32_t nblk = static_cast<int32_t>((rows_used + kQpRows - 1) / kQpRows);
+  const int32_t n_q_units = a.Hq * nblk;
+  const int32_t n_units = n_q_units + a.Hkv * nblk;
+  const uint32_t row_bytes = static_cast<uint32_t>(a.d_io) * 2;
+  const bool convert_v = a.v16 != nullptr;
+
+  if (warp == kQpConsumers) {
+    // ------------------------------------------------------------ producer
+    bool ok = true, waited = !chained;
+    int stg = 0;
+    uint32_t phase = 0;
+    for (int32_t u = blockIdx.x, i = 0; u < n_units; u += gridDim.x, ++i) {
+      if (i >= C::kStages)
+        ok = __all_sync(0xffffffffu, mbar_wait(&empty[stg], phase ^ 1u, limit_ns, st, 911));
+      if (!ok) break;
+      QpUnit x;
+      x.pad = 0;
+      x.is_k = u >= n_q_units;
+      const int32_t v = x.is_k ? u - n_q_units : u;
+      x.h = v / nblk;
+      x.row0 = static_cast<int64_t>(v - x.h * nblk) * kQpRows;
+      int64_t pstart;
+      if (!a.varlen) {
+        x.s = static_cast<int32_t>(x.row0 / seq_rows);
+        pstart = static_cast<int64_t>(x.s) * seq_rows;
+        x.L = a.N;
+        x.tk = 0;
+      } else {
+        int lo = 0, hi = a.nseq - 1;  // the last s with pstart[s] <= row0
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) / 2;
+          if (a.t.pstart[mid] <= x.row0) lo = mid; else hi = mid - 1;
+        }
+        x.s = lo;
+        pstart = a.t.pstart[lo];
+        x.L = a.t.len[lo];
+        x.tk = a.t.tok0[lo];
+      }
+      x.t0 = static_cast<int32_t>(x.row0 - pstart);
+      const bool smooth = x.is_k && a.k_partials;
+      const bool with_v = x.is_k && convert_v;
+      const int64_t srow = static_cast<int64_t>(x.s) * a.Hkv + x.h;
+      if (x.is_k && !waited) {
+        grid_dependency_wait();  // the K mean and the V exponent of kv_finalize_kernel
+        waited = true;
+      }
+      // the V exponent: from kv_finalize_kernel when the chunk kernels ran (bf16 V), else 0,
+      // published here for the attention kernel by the unit holding the sequence's first rows
+      x.vexp = 0;
+      if (with_v) {
+        if (chained) x.vexp = a.v_exp_out[srow];
+        else if (x.t0 == 0 && lane == 0) a.v_exp_out[srow] = 0;
+      }
+      // the unit's rows with input: positions [ta, tb) (a query chunk's before q_off have none)
+      int tb = min(x.t0 + kQpRows, x.L);
+      if (a.varlen && static_cast<int64_t>(x.tk) + tb > a.total_tokens) {  // a length past the tensors
+        if (lane == 0) record_status(st, kStatusBadArg, 901);
+        tb = static_cast<int>(a.total_tokens - x.tk > x.t0 ? a.total_tokens - x.tk : x.t0);
+        x.L = tb;  // rows past the tensors count as past the sequence
+      }
+      const int ta = max(x.t0, x.is_k ? 0 : a.q_off);
+      const int n = max(0, tb - ta);
+      uint8_t* sx = qp_smem + stg * C::kStageBytes;
+      uint8_t* sv = sx + C::kUnitBytes;
+      const int H = x.is_k ? a.Hkv : a.Hq;
+      const void* src = x.is_k ? a.k : a.q;
+      if (lane == 0) {
+        *reinterpret_cast<QpUnit*>(sx + C::kInfoOff) = x;
+        const uint32_t bytes = static_cast<uint32_t>(n) * row_bytes * (with_v ? 2u : 1u) +
+                               (smooth ? static_cast<uint32_t>(a.d_io) * 4u : 0u);
+        if (bytes) mbar_arrive_expect_tx(&full[stg], bytes); else mbar_arrive(&full[stg]);
+        if (smooth) bulk_load(sx + C::kMeanOff, k_mean + srow * a.d_io, a.d_io * 4, &full[stg]);
+      }
+      __syncwarp();
+      if (n > 0) {
+        if (!a.varlen) {
+          if (lane == 0) {
+            const int64_t e0 = x.is_k ? row_offset(false, x.s, x.h, ta, H, a.N, a.d_io, 0)
+                                      : row_offset(false, x.s, x.h, ta - a.q_off, H, a.N - a.q_off, a.d_io, 0);
+            bulk_load(sx + (ta - x.t0) * row_bytes, static_cast<const uint16_t*>(src) + e0, n * row_bytes, &full[stg]);
+            if (with_v)
+              bulk_load(sv + (ta - x.t0) * row_bytes, static_cast<const uint16_t*>(a.v) + e0, n * row_bytes,
+                        &full[stg]);
+          }
+        } else {
+          for (int t = ta + lane; t < tb; t += 32) {
+            const int64_t e = row_offset(true, x.s, x.h, t, H, a.N, a.d_io, x.tk);
+            bulk_load(sx + (t - x.t0) * row_bytes, static_cast<const uint16_t*>(src) + e, row_bytes, &full[stg]);
+            if (with_v)
+              bulk_load(sv + (t - x.t0) * row_bytes, static_cast<const uint16_t*>(a.v) + e, row_bytes, &full[stg]);
+          }
+        }
+      }
+      if (++stg == C::kStages) {
+        stg = 0;
+        phase ^= 1u;
+      }
+    }
+    return;
+  }
+  // ------------------------------------------------------------ consumers
+  const int rsub = lane / LPR, part = lane % LPR;
+  int stg = 0;
+  uint32_t phase = 0;
+  for (int32_t u = blockIdx.x; u < n_units; u += gridDim.x) {
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[stg], phase, limit_ns, st, 912));
+    if (!ok) break;
+    const uint8_t* sx = qp_smem + stg * C::kStageBytes;
+    const uint8_t* sv = sx + C::kUnitBytes;
+    const QpUnit x = *reinterpret_cast<const QpUnit*>(sx + C::kInfoOff);
+    const bool smooth = x.is_k && a.k_partials;
+    const bool with_v = x.is_k && convert_v;
+    uint16_t* codes = x.is_k ? a.k_codes : a.q_codes;
+    float* scales = x.is_k ? a.k_scales : a.q_scales;
+    // the lane's values of each pass: widened, smoothed; validity of the pass's row.  The
+    // lane's channels are vectors part + 8 j (8 values each) of the row, so that the eight
+    // lanes of a row read 128 consecutive bytes of shared memory.
+    float v[P][NV][8];
+    bool valid[P];
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      const int r = warp * (kQpRows / kQpConsumers) + p * RPP + rsub;
+      const int t = x.t0 + r;
+      valid[p] = t < x.L && (x.is_k || t >= a.q_off);
+#pragma unroll
+      for (int j = 0; j < NV; ++j) {
+        const int c = 8 * (part + 8 * j);
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (valid[p] && c < a.d_io) w = *reinterpret_cast<const uint4*>(sx + r * row_bytes + c * 2);
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if constexpr (DT == SL8_BF16) {
+            v[p][j][2 * e] = __uint_as_float(ww[e] << 16);
+            v[p][j][2 * e + 1] = __uint_as_float(ww[e] & 0xffff0000u);
+          } else {
+            v[p][j][2 * e] = f16_bits_to_float(ww[e] & 0xffffu);
+            v[p][j][2 * e + 1] = f16_bits_to_float(ww[e] >> 16);
+          }
+        }
+        if (smooth && valid[p] && c < a.d_io) {
+          const float4 m0 = *reinterpret_cast<const float4*>(sx + C::kMeanOff + c * 4);
+          const float4 m1 = *reinterpret_cast<const float4*>(sx + C::kMeanOff + c * 4 + 16);
+          const float mu[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+          for (int e = 0; e < 8; e += 2)
+            q_upk2(q_sub2(q_pk2(v[p][j][e], v[p][j][e + 1]), q_pk2(mu[e], mu[e + 1])), v[p][j][e],
+                   v[p][j][e + 1]);
+        }
+      }
+    }
+    // per-row max |x| over the row's eight lanes
+    float am[P];
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      float m = 0.0f;
+#pragma unroll
+      for (int j = 0; j < NV; ++j)
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) m = fmaxf(m, fmaxf(fabsf(v[p][j][e]), fabsf(v[p][j][e + 1])));
+#pragma unroll
+      for (int o = LPR / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      am[p] = m;
+    }
+    float scale[P];
+    if constexpr (kGroups) {
+      // grouped scales: rows [g0, g0 + G) of the unit share one (see QuantQK); the unit's 64
+      // rows are positions t0 .. t0 + 63 and t0 is a multiple of 64, so groups are
+      // unit-local.  Rows that take no part hold -1.
+#pragma unroll
+      for (int p = 0; p < P; ++p)
+        if (part == 0) s_am[warp * (kQpRows / kQpConsumers) + p * RPP + rsub] = valid[p] ? am[p] : -1.0f;
+      named_bar_sync(1, kQpConsumers * 32);
+      const int G = x.is_k ? a.k_group : a.q_group;
+      const float tau = x.is_k ? 0.0f : a.q_tau;
+      // four consecutive threads per row r, each scanning a quarter of r's group
+      const int r = threadIdx.x >> 2, jq = threadIdx.x & 3, g0 = r & ~(G - 1);
+      const int per = (G + 3) >> 2, c0 = g0 + jq * per, c1 = min(c0 + per, g0 + G);
+      const float m = s_am[r];
+      if (tau > 0.0f) {
+        int n = 0, rank = 0;
+        for (int i2 = c0; i2 < c1; ++i2) {
+          const float c = s_am[i2];
+          const bool in = c >= 0.0f;
+          n += in ? 1 : 0;
+          rank += (in && (c < m || (c == m && i2 < r))) ? 1 : 0;
+        }
+#pragma unroll
+        for (int o = 1; o < 4; o <<= 1) {
+          n += __shfl_xor_sync(0xffffffffu, n, o);
+          rank += __shfl_xor_sync(0xffffffffu, rank, o);
+        }
+        if (jq == 0 && m >= 0.0f && rank == (n - 1) / 2) s_med[g0] = m;
+        named_bar_sync(1, kQpConsumers * 32);
+      }
+      const float thr = tau > 0.0f ? __fmul_rn(tau, s_med[g0]) : INFINITY;
+      float top = 0.0f;
+      for (int i2 = c0; i2 < c1; ++i2) {
+        const float c = s_am[i2];
+        if (c >= 0.0f && !(c > thr)) top = fmaxf(top, c);
+      }
+#pragma unroll
+      for (int o = 1; o < 4; o <<= 1) top = fmaxf(top, __shfl_xor_sync(0xffffffffu, top, o));
+      if (jq == 0) s_sc[r] = m < 0.0f ? 0.0f : __fdiv_rn(m > thr ? m : top, 127.0f);
+      named_bar_sync(1, kQpConsumers * 32);
+#pragma unroll
+      for (int p = 0; p < P; ++p) scale[p] = s_sc[warp * (kQpRows / kQpConsumers) + p * RPP + rsub];
+      // the shared arrays are rewritten by the next unit only after every consumer has
+      // passed this unit's last barrier
+      named_bar_sync(1, kQpConsumers * 32);
+    } else {
+#pragma unroll
+      for (int p = 0; p < P; ++p) scale[p] = valid[p] ? __fdiv_rn(am[p], 127.0f) : 0.0f;
+    }
+    // codes: y = x * (1/s) (an approximate reciprocal is close enough: y is within 2e-5 of the
+    // correctly rounded quotient), rounded half-even by the 1.5 * 2^23 addition; a value whose
+    // y lies within 1e-4 of a half-integer takes the IEEE quotient
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      const int r = warp * (kQpRows / kQpConsumers) + p * RPP + rsub;
+      const int64_t pr = x.row0 + r;
+      const float rs = scale[p] == 0.0f ? 0.0f : (scale[p] >= 1.0e-37f ? rcp_approx(scale[p]) : __frcp_rn(scale[p]));
+      const uint64_t rs2 = q_pk2(rs, rs), mg2 = q_pk2(12582912.0f, 12582912.0f);
+      uint16_t* crow = codes + (static_cast<int64_t>(x.h) * a.t_pad_max + pr) * D;
+#pragma unroll
+      for (int j = 0; j < NV; ++j) {
+        float cf[8];
+        float dev = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          const uint64_t y2 = q_mul2(q_pk2(v[p][j][e], v[p][j][e + 1]), rs2);
+          const uint64_t c2 = q_sub2(q_add2(y2, mg2), mg2);
+          float d0, d1;
+          q_upk2(q_sub2(y2, c2), d0, d1);
+          q_upk2(c2, cf[e], cf[e + 1]);
+          dev = fmaxf(dev, fmaxf(fabsf(d0), fabsf(d1)));
+        }
+        if (dev > 0.4999f) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) cf[e] = quant_code_rcp(v[p][j][e], scale[p], rs);
+        }
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          o[e] = (__float_as_uint(cf[2 * e]) >> 16) | (__float_as_uint(cf[2 * e + 1]) & 0xffff0000u);
+        *reinterpret_cast<uint4*>(crow + 8 * (part + 8 * j)) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      if (part == 0) scales[static_cast<int64_t>(x.h) * a.t_pad_max + pr] = scale[p];
+    }
+    // fp16 V * 2^-e of the same rows (zeros past the sequence and past d_io)
+    if (with_v) {
+#pragma unroll
+      for (int p = 0; p < P; ++p) {
+        const int r = warp * (kQpRows / kQpConsumers) + p * RPP + rsub;
+        const float vscale = valid[p] ? __int_as_float((127 - x.vexp) << 23) : 0.0f;
+        uint16_t* vrow = a.v16 + (static_cast<int64_t>(x.h) * a.t_pad_max + x.row0 + r) * D;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+          const int c = 8 * (part + 8 * j);
+          uint4 w = make_uint4(0u, 0u, 0u, 0u);
+          if (valid[p] && c < a.d_io) w = *reinterpret_cast<const uint4*>(sv + r * row_bytes + c * 2);
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float v0 = a.v_f16 ? f16_bits_to_float(ww[e] & 0xffffu) : bf16_bits_to_float(ww[e] & 0xffffu);
+            const float v1 = a.v_f16 ? f16_bits_to_float(ww[e] >> 16) : bf16_bits_to_float(ww[e] >> 16);
+            const __half2 h2 = __floats2half2_rn(__fmul_rn(v0, vscale), __fmul_rn(v1, vscale));
+            o[e] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+          *reinterpret_cast<uint4*>(vrow + c) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stg]);
+    if (++stg == C::kStages) {
+      stg = 0;
+      phase ^= 1u;
+    }
+  }
+}
+
+template <sl8_dtype DT, int D, bool kGroups>
+static cudaError_t launch_quant_pipe(const QuantQK& a, const float* k_mean, cudaStream_t s) {
+  using C = QpCfg<D>;
+  auto kern = quant_qk_pipe_kernel<DT, D, kGroups>;
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), C::kSmem);
+  if (e != cudaSuccess) return e;
+  const int64_t units = static_cast<int64_t>(a.Hq + a.Hkv) * ((a.t_pad_max + kQpRows - 1) / kQpRows);
+  const int64_t slots = static_cast<int64_t>(num_sms()) * C::kCtasPerSm;
+  const int grid = static_cast<int>(units < slots ? units : slots);
+  if (grid <= 0) return cudaSuccess;
+  return launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmem, s, a, k_mean, device_status_ptr(), spin_limit_ns());
+}
+
+template <sl8_dtype DT, bool kGroups>
+static cudaError_t launch_quant_pipe_dt(const QuantQK& a, const float* k_mean, int32_t d, cudaStream_t s) {
+  switch (d) {
+    case 64: return launch_quant_pipe<DT, 64, kGroups>(a, k_mean, s);
+    case 128: return launch_quant_pipe<DT, 128, kGroups>(a, k_mean, s);
+    default: return launch_quant_pipe<DT, 256, kGroups>(a, k_mean, s);
+  }
+}
+
+cudaError_t launch_kv_finalize(bool varlen, int32_t nseq, int32_t Hkv, int32_t N, int32_t d_io, const int32_t* len,
+                               const float* k_partials, const float* v_partials, int32_t max_chunks, float* mean,
+                               int32_t* v_exp, cudaStream_t s) {
+  TraceScope tr("kv_finalize", s);
+  return launch_pdl(kv_finalize_kernel, dim3(Hkv, nseq), dim3(128), 0, s, varlen, Hkv, N, d_io, len, k_partials,
+                    v_partials, max_chunks, mean, v_exp);
+}
+
 template <sl8_dtype DT, bool kGroups>
 static cudaError_t launch_quant_qk_dt(const QuantQK& a, int32_t d, int32_t n_heads, cudaStream_t s) {
   const int64_t rows_per_cta = kQuantWarps * kQuantRowsPerWarp;
@@ -1016,16 +1442,17 @@ cudaError_t launch_quant_qk(const void* q, const void* k, sl8_dtype dt, bool var
                             int64_t t_pad_max, const float* k_partials, const float* v_partials,
                             int32_t max_chunks, uint16_t* q_codes, float* q_scales, uint16_t* k_codes,
                             float* k_scales, const void* v, int32_t* v_exp, uint16_t* v16, cudaStream_t s,
-                            int32_t q_off, int32_t d_io, bool v_f16, const QuantGroups& groups) {
+                            int32_t q_off, int32_t d_io, bool v_f16, const QuantGroups& groups,
+                            const float* k_mean) {
   QuantQK a{q, k, varlen, nseq, Hq, Hkv, N, q_off, d_io > 0 ? d_io : d, v_f16, total_tokens, t, t_pad_max, k_partials,
             v_partials, max_chunks, v_exp,
             q_codes, q_scales, k_codes, k_scales, v, v16, groups.q_group, groups.k_group, groups.q_tau};
   TraceScope tr("quant_qk", s);
   if (groups.q_group > 1 || groups.k_group > 1 || groups.q_tau > 0.0f)
-    return dt == SL8_BF16 ? launch_quant_qk_dt<SL8_BF16, true>(a, d, Hq + Hkv, s)
-                          : launch_quant_qk_dt<SL8_F16, true>(a, d, Hq + Hkv, s);
-  return dt == SL8_BF16 ? launch_quant_qk_dt<SL8_BF16, false>(a, d, Hq + Hkv, s)
-                        : launch_quant_qk_dt<SL8_F16, false>(a, d, Hq + Hkv, s);
+    return dt == SL8_BF16 ? launch_quant_pipe_dt<SL8_BF16, true>(a, k_mean, d, s)
+                          : launch_quant_pipe_dt<SL8_F16, true>(a, k_mean, d, s);
+  return dt == SL8_BF16 ? launch_quant_pipe_dt<SL8_BF16, false>(a, k_mean, d, s)
+                        : launch_quant_pipe_dt<SL8_F16, false>(a, k_mean, d, s);
 }
 
 // ---------------------------------------------------------------- generic rowwise int8

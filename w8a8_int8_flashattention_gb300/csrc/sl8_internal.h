@@ -103,9 +103,16 @@ cudaError_t launch_kv_stats(const void* k, sl8_dtype dt, const void* v, bool var
 cudaError_t launch_kv_partials(const void* k, sl8_dtype dt, const void* v, bool varlen, int32_t nseq, int32_t Hkv,
                                int32_t N, int32_t d, const int32_t* len, const int32_t* tok0, float* k_partials,
                                float* v_partials, int32_t max_chunks, cudaStream_t s);
-// Q and K rows of prefill in one launch.  K CTAs form the mean from k_partials (nullable:
-// no smoothing) and, with v16 set, the V exponent from v_partials (published in v_exp) and
-// write V as fp16 * 2^-v_exp.  t is read for varlen input only.  q_off > 0 (dense): q holds
+// From the chunk results of launch_kv_partials (either nullable): the K mean
+// [nseq][Hkv][d_io] and the V exponent [nseq][Hkv] (0 without v_partials); one CTA per
+// (sequence, kv head); len nullable for dense input (every sequence N long).
+cudaError_t launch_kv_finalize(bool varlen, int32_t nseq, int32_t Hkv, int32_t N, int32_t d_io, const int32_t* len,
+                               const float* k_partials, const float* v_partials, int32_t max_chunks, float* mean,
+                               int32_t* v_exp, cudaStream_t s);
+// Q and K rows of prefill in one launch.  With k_partials or v_partials set, the chunk
+// kernels and launch_kv_finalize ran just before: K rows are smoothed with k_mean (set
+// iff k_partials is) and, with v16 set, V is written as fp16 * 2^-v_exp with the exponent
+// kv_finalize left in v_exp; otherwise the exponent is 0 and is written to v_exp here.  t is read for varlen input only.  q_off > 0 (dense): q holds
 // N - q_off rows per (sequence, head), the positions q_off .. N-1; the code rows of the
 // positions before it are zero.  d_io < d (head dim 32 run as 64): the inputs hold d_io
 // values per row and the code rows are zero past them; k_partials then has d_io columns;
@@ -121,7 +128,7 @@ cudaError_t launch_quant_qk(const void* q, const void* k, sl8_dtype dt, bool var
                             int32_t max_chunks, uint16_t* q_codes, float* q_scales, uint16_t* k_codes,
                             float* k_scales, const void* v, int32_t* v_exp, uint16_t* v16, cudaStream_t s,
                             int32_t q_off = 0, int32_t d_io = 0, bool v_f16 = false,
-                            const QuantGroups& groups = QuantGroups());
+                            const QuantGroups& groups = QuantGroups(), const float* k_mean = nullptr);
 cudaError_t launch_quant_rowwise(const void* x, sl8_dtype dt, int64_t rows, int32_t cols, int64_t row_stride,
                                  const float* sub_mean, int64_t rows_per_group, int8_t* q_out, float* scale_out,
                                  cudaStream_t s);
@@ -190,6 +197,12 @@ struct DecodeArgs {
   // partials are [B_cache * T][Hq][S][d], row (b * T + t) * Hq + hq.
   int32_t verify_T, verify_dps, verify_ng;
   const uint32_t* tree_mask;
+  // query heads per kv head above 8 (MQA): each cache kv head serves kv_groups virtual kv
+  // heads of Hq / Hkv <= 8 query heads each.  Hkv here counts the virtual heads (the
+  // cache holds Hkv / kv_groups), so virtual head hv reads cache head hv / kv_groups and
+  // its query columns are heads hv * (Hq / Hkv) + c, i.e. consecutive groups of the cache
+  // head's query heads.  1 otherwise.
+  int32_t kv_groups;
 };
 cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_combine(const float* o_partial, const float* lse_partial, const int32_t* seqlens,
