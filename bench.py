@@ -328,6 +328,14 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     peaks = load_peaks()
+    if args.only in OTHER_PREFILL:
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        flush_sink = torch.empty((), dtype=torch.int64, device=dev)
+        res = measure_prefill_config(sl8, W, args.only, dev, torch.cuda.current_stream(dev), flush, flush_sink,
+                                     args.steps, args.warmup, world, peaks, rank=1)  # no CPU leg
+        if rank == 0:
+            print(json.dumps({"only": args.only, **res}), flush=True)
+        return
 
     # ---- prefill inputs (HBM resident)
     wp = W.get(PREFILL)
@@ -897,9 +905,9 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode", "w8a8"],
-                    help="time one half of the step only (profiling runs; w8a8: the prefill through "
-                         "attn_w8a8_fwd); no e2e or CPU leg")
+    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode", "w8a8", *OTHER_PREFILL],
+                    help="time one part only (profiling runs): the prefill or decode half of the step, the "
+                         "prefill through attn_w8a8_fwd, or one of the other prefill workloads; no e2e or CPU leg")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup(args)

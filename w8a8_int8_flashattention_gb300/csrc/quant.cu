@@ -90,6 +90,13 @@ __device__ __forceinline__ uint64_t q_sub2(uint64_t a, uint64_t b) {
   return d;
 }
 
+// Three-input max (one instruction).
+__device__ __forceinline__ float q_max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // The same code as an integer-valued float, from rs = RN(1 / s): for |x / s| <= 127.5 the
 // product x * rs lies within 3e-5 of the correctly rounded quotient, so both round to
 // the same integer unless the product is within 1e-4 of a half-integer; only then is
@@ -625,14 +632,10 @@ cudaError_t launch_kv_partials(const void* k, sl8_dtype dt, const void* v, bool 
 }
 
 // ---------------------------------------------------------------- prefill codes
-// Q and K rows in one launch (blockIdx.y < Hkv: K heads; the rest: Q heads), each warp
-// quantising kQuantRowsPerWarp rows with all of their loads issued first.  Rows live in
-// the padded code workspace [H][t_pad][d]; padded rows past a sequence's end are
-// written as zeros.  For K rows with v16 set (V bf16), the warp also writes the same
-// row of V as fp16, scaled by the sequence/head's 2^-v_exp (exact), into v16
-// [Hkv][t_pad][d].
-constexpr int kQuantWarps = 8;
-constexpr int kQuantRowsPerWarp = 8;
+// Arguments of the prefill quantiser (Q and K rows in one launch).  Rows live in the padded
+// code workspace [H][t_pad][d]; padded rows past a sequence's end are written as zeros.
+// For K rows with v16 set (V bf16, or head dim 32 run as 64), the same rows of V are
+// written as fp16 scaled by the sequence/head's 2^-v_exp (exact) into v16 [Hkv][t_pad][d].
 
 struct QuantQK {
   const void* q;
@@ -661,343 +664,6 @@ struct QuantQK {
   int32_t q_group, k_group;
   float q_tau;
 };
-
-template <int EPL>
-__device__ __forceinline__ void store_vec16(uint16_t* p, const uint16_t (&h)[EPL]) {
-  if constexpr (EPL == 8) {
-    uint4 w; memcpy(&w, h, 16); *reinterpret_cast<uint4*>(p) = w;
-  } else if constexpr (EPL == 4) {
-    uint2 w; memcpy(&w, h, 8); *reinterpret_cast<uint2*>(p) = w;
-  } else {
-    uint32_t w; memcpy(&w, h, 4); *reinterpret_cast<uint32_t*>(p) = w;
-  }
-}
-
-// Eight lanes per row (EPL = D / 8 values each, 16-byte accesses), four rows per warp
-// instruction.  kGroups: scales shared by groups of rows (see QuantQK), formed in shared
-// memory from the CTA's 64 row maxima before any code is written.  The per-row form runs
-// five CTAs per SM (48 registers at d <= 128): the loads in flight are what bound it, so
-// V, which only K CTAs convert, is read after the codes rather than held from the start.
-template <sl8_dtype DT, int D, bool kGroups>
-__global__ void __launch_bounds__(kQuantWarps * 32, D == 256 ? 2 : (kGroups ? 4 : 5))
-    quant_qk_kernel(const QuantQK a, DeviceStatus* st) {
-  constexpr int LPR = 8, EPL = D / LPR, NV = EPL / 8, RPP = 32 / LPR, P = kQuantRowsPerWarp / RPP;
-  // K heads first: their CTAs also form the K mean and the V exponent, so they start
-  // in the first wave and the Q CTAs fill in behind them
-  const bool is_k = static_cast<int>(blockIdx.y) < a.Hkv;
-  const int h = is_k ? blockIdx.y : blockIdx.y - a.Hkv;
-  // When the K/V chunk kernel ran just before (k_partials or v_partials set), Q CTAs
-  // need none of its results: that kernel lets this grid start only after its own
-  // wait, so everything before it (the caller's Q, the schedule, the attention launch
-  // that last read this workspace) has completed, and Q runs alongside it.
-  if (is_k || (!a.k_partials && !a.v_partials)) grid_dependency_wait();
-  grid_dependents_launch();
-  // the attention kernel that follows claims work items from this counter
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) a.t.counts[2] = 0;
-  __shared__ __align__(16) float s_mean[D];
-  __shared__ float s_vm[kQuantWarps];
-  __shared__ int s_vexp;
-  const int H = is_k ? a.Hkv : a.Hq;
-  const void* x = is_k ? a.k : a.q;
-  uint16_t* codes = is_k ? a.k_codes : a.q_codes;
-  float* scales = is_k ? a.k_scales : a.q_scales;
-  const bool smooth = is_k && a.k_partials;
-  uint16_t* v16 = is_k ? a.v16 : nullptr;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-  const int rsub = lane / LPR, part = lane % LPR;
-  // dense input: sequence s owns padded rows [s * tiles * 128, ...) and the table is
-  // arithmetic; varlen: look the rows up in the scheduler's table
-  const int64_t seq_rows = static_cast<int64_t>((a.N + kQTile - 1) / kQTile) * kPadRows;
-  const int64_t rows_used = a.varlen ? a.t.counts[1] : a.nseq * seq_rows;
-  const int64_t cta_row0 = static_cast<int64_t>(blockIdx.x) * kQuantWarps * kQuantRowsPerWarp;
-  const int64_t row0 = cta_row0 + static_cast<int64_t>(warp) * kQuantRowsPerWarp;
-  if (cta_row0 >= rows_used || cta_row0 >= a.t_pad_max) return;
-  // ---- K CTAs: the K mean of the CTA's sequence (its 64 rows never straddle two, as
-  // sequences start on 128-row boundaries) = chunk sums added in chunk order / L, and
-  // the V exponent e >= 0 with max|V| * 2^-e <= 2^15 (V * 2^-e exact in fp16)
-  if (is_k && (smooth || v16)) {
-    int s0 = 0, L0 = a.N;
-    if (!a.varlen) {
-      s0 = static_cast<int>(cta_row0 / seq_rows);
-    } else {
-      int lo = 0, hi = a.nseq - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) / 2;
-        if (a.t.pstart[mid] <= cta_row0) lo = mid; else hi = mid - 1;
-      }
-      s0 = lo;
-      L0 = a.t.len[lo];
-    }
-    const int nch = (L0 + kMeanChunk - 1) / kMeanChunk;
-    const int64_t srow = static_cast<int64_t>(s0) * a.Hkv + h;
-    if (smooth) {
-      for (int c = threadIdx.x; c < D; c += blockDim.x) {
-        // k_partials has d_io columns; the padded channels have mean 0
-        const float* p = a.k_partials + srow * a.max_chunks * a.d_io + c;
-        float total = 0.0f;
-        for (int cb = 0; cb < nch && c < a.d_io; cb += 16) {
-          float xx[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) xx[i] = cb + i < nch ? p[static_cast<int64_t>(cb + i) * a.d_io] : 0.0f;
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (cb + i < nch) total = __fadd_rn(total, xx[i]);
-        }
-        s_mean[c] = L0 > 0 ? __fdiv_rn(total, static_cast<float>(L0)) : 0.0f;
-      }
-    }
-    if (v16) {
-      float m = 0.0f;
-      if (a.v_partials)  // fp16 V: exponent 0
-        for (int cb = threadIdx.x; cb < nch; cb += blockDim.x) m = fmaxf(m, a.v_partials[srow * a.max_chunks + cb]);
-      m = warp_max(m);
-      if (lane == 0) s_vm[warp] = m;
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        for (int w = 1; w < kQuantWarps; ++w) m = fmaxf(m, s_vm[w]);
-        int e = 0;
-        if (m > 0.0f) {
-          int k2 = 0;
-          frexpf(m, &k2);  // m < 2^k2
-          e = k2 > 15 ? k2 - 15 : 0;
-        }
-        s_vexp = e;
-        // the CTA holding the sequence's first rows publishes it for the attention kernel
-        const int64_t first = a.varlen ? a.t.pstart[s0] : static_cast<int64_t>(s0) * seq_rows;
-        if (cta_row0 == first) a.v_exp_out[srow] = e;
-      }
-    }
-    __syncthreads();
-  }
-  // the CTA's rows all belong to one sequence (sequences start on 128-row boundaries and
-  // a CTA covers an aligned block of 64 rows): find it once
-  static_assert(kPadRows % (kQuantWarps * kQuantRowsPerWarp) == 0, "a CTA's rows lie in one sequence");
-  int cta_s = 0, cta_len = a.N;
-  int64_t cta_pstart = 0;
-  int32_t tk = 0;
-  if (!a.varlen) {
-    cta_s = static_cast<int>(cta_row0 / seq_rows);
-    cta_pstart = static_cast<int64_t>(cta_s) * seq_rows;
-  } else {
-    // the last s with pstart[s] <= cta_row0
-    int lo = 0, hi = a.nseq - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) / 2;
-      if (a.t.pstart[mid] <= cta_row0) lo = mid; else hi = mid - 1;
-    }
-    cta_s = lo;
-    cta_pstart = a.t.pstart[lo];
-    cta_len = a.t.len[lo];
-    tk = a.t.tok0[lo];
-  }
-  // this lane's rows (one per pass): position, validity; then all loads
-  int sq[P], tt[P];
-  bool live[P], valid[P];
-  uint4 xw[P][NV];
-  int64_t voff[P];  // V row offset of each pass (-1: not loaded); V is read after the codes
-#pragma unroll
-  for (int p = 0; p < P; ++p) {
-    const int64_t pr = row0 + p * RPP + rsub;
-    live[p] = pr < rows_used && pr < a.t_pad_max;
-    valid[p] = false;
-    sq[p] = cta_s;
-    tt[p] = static_cast<int32_t>(pr - cta_pstart);
-    if (live[p]) {
-      if (!a.varlen) {
-        valid[p] = tt[p] < a.N && (is_k || tt[p] >= a.q_off);
-      } else {
-        valid[p] = tt[p] < cta_len;
-        if (valid[p] && static_cast<int64_t>(tk) + tt[p] >= a.total_tokens) {
-          record_status(st, kStatusBadArg, 901);
-          valid[p] = false;
-        }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {
-      xw[p][j] = make_uint4(0u, 0u, 0u, 0u);
-    }
-    voff[p] = -1;
-    if (valid[p] && part * EPL < a.d_io) {
-      // a query chunk's rows: position t is row t - q_off of N - q_off; rows hold d_io values
-      const int64_t off = (is_k ? row_offset(a.varlen, sq[p], h, tt[p], H, a.N, a.d_io, tk)
-                                : row_offset(a.varlen, sq[p], h, tt[p] - a.q_off, H, a.N - a.q_off, a.d_io, tk)) +
-                          part * EPL;
-#pragma unroll
-      for (int j = 0; j < NV; ++j) {
-        xw[p][j] = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + off + 8 * j);
-      }
-      voff[p] = off;
-    }
-  }
-  // the lane's EPL values of pass p's row, widened (and smoothed for K)
-  auto row_values = [&](int p, float (&v)[EPL]) {
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {
-      const uint32_t ww[4] = {xw[p][j].x, xw[p][j].y, xw[p][j].z, xw[p][j].w};
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const uint32_t b = (e & 1) ? ww[e / 2] >> 16 : ww[e / 2] & 0xffffu;
-        v[8 * j + e] = DT == SL8_BF16 ? bf16_bits_to_float(b) : f16_bits_to_float(b);
-      }
-    }
-    if (smooth && valid[p]) {
-      const float* mu = s_mean + part * EPL;
-#pragma unroll
-      for (int e = 0; e < EPL; e += 4) {
-        const float4 m4 = *reinterpret_cast<const float4*>(mu + e);
-        q_upk2(q_sub2(q_pk2(v[e], v[e + 1]), q_pk2(m4.x, m4.y)), v[e], v[e + 1]);
-        q_upk2(q_sub2(q_pk2(v[e + 2], v[e + 3]), q_pk2(m4.z, m4.w)), v[e + 2], v[e + 3]);
-      }
-    }
-  };
-  // max|x| of pass p's row, reduced over its eight lanes
-  auto row_absmax = [&](const float (&v)[EPL]) {
-    float am = 0.0f;
-#pragma unroll
-    for (int e = 0; e < EPL; e += 2) am = fmaxf(am, fmaxf(fabsf(v[e]), fabsf(v[e + 1])));
-#pragma unroll
-    for (int o = LPR / 2; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-    return am;
-  };
-  float grp_scale[P];
-  if constexpr (kGroups) {
-    // Row r of the CTA (0..63) is sequence position (cta_row0 - cta_pstart) + r, and
-    // cta_row0 - cta_pstart is a multiple of 64, so a group of G <= 64 rows is the
-    // CTA-local range [r & ~(G-1), +G).  Rows outside the sequence (or before a query
-    // chunk) take no part: a group's median and maximum run over its valid rows.
-    constexpr int kRows = kQuantWarps * kQuantRowsPerWarp;
-    static_assert(kRows * 4 == kQuantWarps * 32, "four threads per row in the group stage");
-    // s_am: max|x| of each row, -1 for rows that take no part
-    __shared__ __align__(16) float s_am[kRows];
-    __shared__ float s_med[kRows], s_sc[kRows];
-#pragma unroll
-    for (int p = 0; p < P; ++p) {
-      float v[EPL];
-      row_values(p, v);
-      const float am = row_absmax(v);
-      if (part == 0) s_am[warp * kQuantRowsPerWarp + p * RPP + rsub] = valid[p] ? am : -1.0f;
-    }
-    __syncthreads();
-    const int G = is_k ? a.k_group : a.q_group;
-    const float tau = is_k ? 0.0f : a.q_tau;
-    // four consecutive lanes per row r, each scanning a quarter of r's group (rows
-    // [c0, c1)), then combining over the four lanes
-    const int r = threadIdx.x >> 2, j = threadIdx.x & 3, g0 = r & ~(G - 1);
-    const int per = (G + 3) >> 2, c0 = g0 + j * per, c1 = min(c0 + per, g0 + G);
-    const float m = s_am[r];
-    // f(index, value) over the lane's rows: float4 reads when a quarter is 4-aligned (G >= 16)
-    auto scan = [&](auto&& f) {
-      if (per >= 4) {
-        for (int i = c0; i < c1; i += 4) {
-          const float4 c4 = *reinterpret_cast<const float4*>(s_am + i);
-          f(i, c4.x); f(i + 1, c4.y); f(i + 2, c4.z); f(i + 3, c4.w);
-        }
-      } else {
-        for (int i = c0; i < c1; ++i) f(i, s_am[i]);
-      }
-    };
-    if (tau > 0.0f) {  // uniform over the CTA (Q heads only)
-      // lower median of the group's row maxima: the valid row of rank (n - 1) / 2, ties
-      // broken by row index
-      int n = 0, rank = 0;
-      scan([&](int idx, float c) {
-        const bool in = c >= 0.0f;
-        n += in ? 1 : 0;
-        rank += (in && (c < m || (c == m && idx < r))) ? 1 : 0;
-      });
-#pragma unroll
-      for (int o = 1; o < 4; o <<= 1) {
-        n += __shfl_xor_sync(0xffffffffu, n, o);
-        rank += __shfl_xor_sync(0xffffffffu, rank, o);
-      }
-      if (j == 0 && m >= 0.0f && rank == (n - 1) / 2) s_med[g0] = m;
-      __syncthreads();
-    }
-    // an outlier keeps its own maximum; the others take the group's largest inlier one
-    const float thr = tau > 0.0f ? __fmul_rn(tau, s_med[g0]) : INFINITY;
-    float top = 0.0f;
-    scan([&](int, float c) {
-      if (c >= 0.0f && !(c > thr)) top = fmaxf(top, c);
-    });
-#pragma unroll
-    for (int o = 1; o < 4; o <<= 1) top = fmaxf(top, __shfl_xor_sync(0xffffffffu, top, o));
-    if (j == 0) s_sc[r] = m < 0.0f ? 0.0f : __fdiv_rn(m > thr ? m : top, 127.0f);
-    __syncthreads();
-#pragma unroll
-    for (int p = 0; p < P; ++p) grp_scale[p] = s_sc[warp * kQuantRowsPerWarp + p * RPP + rsub];
-  }
-#pragma unroll
-  for (int p = 0; p < P; ++p) {
-    const int64_t pr = row0 + p * RPP + rsub;
-    float v[EPL];
-    row_values(p, v);
-    float scale;
-    if constexpr (kGroups) {
-      if (!live[p]) continue;
-      scale = grp_scale[p];
-    } else {
-      const float am = row_absmax(v);
-      if (!live[p]) continue;
-      scale = valid[p] ? __fdiv_rn(am, 127.0f) : 0.0f;
-    }
-    const float rs = scale == 0.0f ? 0.0f : __frcp_rn(scale);
-    uint16_t* crow = codes + (static_cast<int64_t>(h) * a.t_pad_max + pr) * D + part * EPL;
-    // two elements per packed instruction: y = x * rs, c = RNE(y) (see quant_code_rcp;
-    // scale 0 gives rs = 0 and zero codes); a pair whose product lies near a
-    // half-integer takes the exact path
-    const uint64_t rs2 = q_pk2(rs, rs), mg2 = q_pk2(12582912.0f, 12582912.0f);
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {
-      uint32_t o[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint64_t y2 = q_mul2(q_pk2(v[8 * j + 2 * e], v[8 * j + 2 * e + 1]), rs2);
-        const uint64_t c2 = q_sub2(q_add2(y2, mg2), mg2);
-        float d0, d1, c0, c1;
-        q_upk2(q_sub2(y2, c2), d0, d1);
-        q_upk2(c2, c0, c1);
-        if (fmaxf(fabsf(d0), fabsf(d1)) > 0.4999f) {
-          c0 = quant_code_rcp(v[8 * j + 2 * e], scale, rs);
-          c1 = quant_code_rcp(v[8 * j + 2 * e + 1], scale, rs);
-        }
-        o[e] = (__float_as_uint(c0) >> 16) | (__float_as_uint(c1) & 0xffff0000u);
-      }
-      *reinterpret_cast<uint4*>(crow + 8 * j) = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-    if (part == 0) scales[static_cast<int64_t>(h) * a.t_pad_max + pr] = scale;
-  }
-  // K CTAs with a V to convert: V * 2^-e in fp16 for the P.V MMA, both passes' loads first
-  if (v16) {
-    uint4 vw[P][NV];
-#pragma unroll
-    for (int p = 0; p < P; ++p)
-#pragma unroll
-      for (int j = 0; j < NV; ++j)
-        vw[p][j] = voff[p] >= 0 ? *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.v) + voff[p] + 8 * j)
-                                : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-    for (int p = 0; p < P; ++p) {
-      if (!live[p]) continue;
-      const int64_t pr = row0 + p * RPP + rsub;
-      const float vscale = valid[p] ? __int_as_float((127 - s_vexp) << 23) : 0.0f;  // 2^-e
-      uint16_t* vrow = v16 + (static_cast<int64_t>(h) * a.t_pad_max + pr) * D + part * EPL;
-#pragma unroll
-      for (int j = 0; j < NV; ++j) {
-        const uint32_t ww[4] = {vw[p][j].x, vw[p][j].y, vw[p][j].z, vw[p][j].w};
-        uint32_t o[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float v0 = a.v_f16 ? f16_bits_to_float(ww[e] & 0xffffu) : bf16_bits_to_float(ww[e] & 0xffffu);
-          const float v1 = a.v_f16 ? f16_bits_to_float(ww[e] >> 16) : bf16_bits_to_float(ww[e] >> 16);
-          const __half2 h2 = __floats2half2_rn(__fmul_rn(v0, vscale), __fmul_rn(v1, vscale));
-          o[e] = *reinterpret_cast<const uint32_t*>(&h2);
-        }
-        *reinterpret_cast<uint4*>(vrow + 8 * j) = make_uint4(o[0], o[1], o[2], o[3]);
-      }
-    }
-  }
-}
 
 // ---------------------------------------------------------------- K mean and V exponent
 // One CTA per (sequence, kv head): the K mean = (the chunk sums of k_partials added in
@@ -1074,13 +740,13 @@ struct QpUnit {
 template <int D>
 struct QpCfg {
   static constexpr int kUnitBytes = kQpRows * D * 2;       // staged rows of <= D 16-bit values
-  static constexpr int kStages = D == 256 ? 2 : (D == 128 ? 3 : 4);
+  static constexpr int kStages = D == 256 ? 2 : (D == 128 ? 2 : 4);
   static constexpr int kMeanOff = 2 * kUnitBytes;          // input rows, V rows, K mean row
   static constexpr int kInfoOff = kMeanOff + D * 4;
   static constexpr int kStageBytes = kInfoOff + 128;
   static constexpr int kSmem = kStages * kStageBytes + 128;
   static constexpr int kThreads = (kQpConsumers + 1) * 32;
-  static constexpr int kCtasPerSm = D == 256 ? 1 : 2;
+  static constexpr int kCtasPerSm = D == 256 ? 1 : 3;
   static_assert(kCtasPerSm * (kSmem + 1024) <= 232448, "quantiser shared memory");
   static_assert(kStageBytes % 16 == 0 && sizeof(QpUnit) <= 128, "stage layout");
 };
@@ -1271,7 +937,7 @@ __global__ void __launch_bounds__(QpCfg<D>::kThreads, QpCfg<D>::kCtasPerSm)
 #pragma unroll
       for (int j = 0; j < NV; ++j)
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) m = fmaxf(m, fmaxf(fabsf(v[p][j][e]), fabsf(v[p][j][e + 1])));
+        for (int e = 0; e < 8; e += 2) m = q_max3(m, fabsf(v[p][j][e]), fabsf(v[p][j][e + 1]));
 #pragma unroll
       for (int o = LPR / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
       am[p] = m;
@@ -1347,7 +1013,7 @@ __global__ void __launch_bounds__(QpCfg<D>::kThreads, QpCfg<D>::kCtasPerSm)
           float d0, d1;
           q_upk2(q_sub2(y2, c2), d0, d1);
           q_upk2(c2, cf[e], cf[e + 1]);
-          dev = fmaxf(dev, fmaxf(fabsf(d0), fabsf(d1)));
+          dev = q_max3(dev, fabsf(d0), fabsf(d1));
         }
         if (dev > 0.4999f) {
 #pragma unroll
@@ -1423,18 +1089,6 @@ cudaError_t launch_kv_finalize(bool varlen, int32_t nseq, int32_t Hkv, int32_t N
   TraceScope tr("kv_finalize", s);
   return launch_pdl(kv_finalize_kernel, dim3(Hkv, nseq), dim3(128), 0, s, varlen, Hkv, N, d_io, len, k_partials,
                     v_partials, max_chunks, mean, v_exp);
-}
-
-template <sl8_dtype DT, bool kGroups>
-static cudaError_t launch_quant_qk_dt(const QuantQK& a, int32_t d, int32_t n_heads, cudaStream_t s) {
-  const int64_t rows_per_cta = kQuantWarps * kQuantRowsPerWarp;
-  const dim3 grid(static_cast<unsigned>((a.t_pad_max + rows_per_cta - 1) / rows_per_cta), n_heads);
-  DeviceStatus* st = device_status_ptr();
-  switch (d) {
-    case 64: return launch_pdl(quant_qk_kernel<DT, 64, kGroups>, grid, dim3(kQuantWarps * 32), 0, s, a, st);
-    case 128: return launch_pdl(quant_qk_kernel<DT, 128, kGroups>, grid, dim3(kQuantWarps * 32), 0, s, a, st);
-    default: return launch_pdl(quant_qk_kernel<DT, 256, kGroups>, grid, dim3(kQuantWarps * 32), 0, s, a, st);
-  }
 }
 
 cudaError_t launch_quant_qk(const void* q, const void* k, sl8_dtype dt, bool varlen, int32_t nseq, int32_t Hq,
