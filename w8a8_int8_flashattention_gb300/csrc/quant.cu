@@ -13,6 +13,8 @@
 // 64-token chunks in ascending token order, then the chunk sums in ascending
 // order, then divides by the token count.  This file is built without fast-math
 // and spells every rounding step as an explicit _rn intrinsic.
+#include <atomic>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -535,10 +537,12 @@ cudaError_t launch_kv_stats(const void* k, sl8_dtype dt, const void* v, bool var
 
 // ---------------------------------------------------------------- prefill K/V partials
 // One CTA per (64-token chunk, kv head, sequence): the chunk's K rows (and V rows when
-// v_partials is set) are staged in shared memory with bulk copies, then thread c sums
-// channel c in token order into k_partials and the CTA takes max |V| into v_partials.
-// Dense input (len == nullptr): every sequence is N long.  The mean and the V exponent
-// are formed by the K quantisation CTAs.  d * sizeof(element) must be a multiple of 16.
+// v_partials is set) are staged in shared memory with bulk copies; then thread c < d sums
+// channel c of K in token order into k_partials, while the second half of the CTA (with
+// V) takes max |V| of the chunk into v_partials.  Dense input (len == nullptr): every
+// sequence is N long.  kv_finalize_kernel forms the mean and the V exponent from these.
+// d * sizeof(element) must be a multiple of 16; the block is 2 * ceil32(d) threads with V,
+// ceil32(d) without.
 template <sl8_dtype DT>
 __global__ void kv_partials_kernel(const void* __restrict__ k, const void* __restrict__ v, bool varlen, int32_t Hkv,
                                    int32_t N, int32_t d, const int32_t* __restrict__ len,
@@ -551,7 +555,10 @@ __global__ void kv_partials_kernel(const void* __restrict__ k, const void* __res
   constexpr int ES = DT == SL8_F32 ? 4 : 2;
   grid_dependency_wait();
   grid_dependents_launch();
-  const int ch = blockIdx.x, h = blockIdx.y, s = blockIdx.z, c = threadIdx.x;
+  const int ch = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+  const int half = (d + 31) / 32 * 32;  // threads per role
+  const bool v_role = v_partials && static_cast<int>(threadIdx.x) >= half;
+  const int c = v_role ? threadIdx.x - half : threadIdx.x;
   const int L = len ? len[s] : N;
   const int t0 = ch * kMeanChunk;
   if (t0 >= L) return;
@@ -560,23 +567,24 @@ __global__ void kv_partials_kernel(const void* __restrict__ k, const void* __res
   const uint32_t row_bytes = static_cast<uint32_t>(d) * ES;
   uint8_t* sk = stage;
   uint8_t* sv = stage + kMeanChunk * row_bytes;
-  if (c == 0) {
+  if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
     fence_barrier_init();
   }
   __syncthreads();
-  if (c < 32) {
+  if (threadIdx.x < 32) {
+    const int l = threadIdx.x;
     const uint32_t tx = static_cast<uint32_t>(n) * row_bytes * ((k_partials ? 1u : 0u) + (v_partials ? 1u : 0u));
-    if (c == 0) mbar_arrive_expect_tx(&bar, tx);
+    if (l == 0) mbar_arrive_expect_tx(&bar, tx);
     __syncwarp();
     if (!varlen) {  // the chunk's rows are contiguous
-      if (c == 0) {
+      if (l == 0) {
         const int64_t e0 = row_offset(false, s, h, t0, Hkv, N, d, 0);
         if (k_partials) bulk_load(sk, static_cast<const uint8_t*>(k) + e0 * ES, n * row_bytes, &bar);
         if (v_partials) bulk_load(sv, static_cast<const uint8_t*>(v) + e0 * 2, n * row_bytes, &bar);
       }
     } else {
-      for (int i = c; i < n; i += 32) {
+      for (int i = l; i < n; i += 32) {
         const int64_t e = row_offset(true, s, h, t0 + i, Hkv, N, d, base);
         if (k_partials) bulk_load(sk + i * row_bytes, static_cast<const uint8_t*>(k) + e * ES, row_bytes, &bar);
         if (v_partials) bulk_load(sv + i * row_bytes, static_cast<const uint8_t*>(v) + e * 2, row_bytes, &bar);
@@ -585,27 +593,39 @@ __global__ void kv_partials_kernel(const void* __restrict__ k, const void* __res
   }
   const bool ok = mbar_wait(&bar, 0, limit_ns, st, 903);
   const int64_t slot = (static_cast<int64_t>(s) * Hkv + h) * max_chunks + ch;
-  if (k_partials && ok && c < d) {
-    float part = 0.0f;
-    for (int i = 0; i < n; ++i) {
-      const uint8_t* p = sk + i * row_bytes + c * ES;
-      const float x = DT == SL8_F32 ? *reinterpret_cast<const float*>(p)
-                    : DT == SL8_BF16 ? bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(p))
-                                     : f16_bits_to_float(*reinterpret_cast<const uint16_t*>(p));
-      part = __fadd_rn(part, x);
+  if (!v_role) {
+    // channel c of K, summed in token order (16 rows' loads in flight at a time)
+    if (k_partials && ok && c < d) {
+      float part = 0.0f;
+      for (int i0 = 0; i0 < n; i0 += 16) {
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          x[i] = 0.0f;
+          if (i0 + i < n) {
+            const uint8_t* p = sk + (i0 + i) * row_bytes + c * ES;
+            x[i] = DT == SL8_F32 ? *reinterpret_cast<const float*>(p)
+                 : DT == SL8_BF16 ? bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(p))
+                                  : f16_bits_to_float(*reinterpret_cast<const uint16_t*>(p));
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (i0 + i < n) part = __fadd_rn(part, x[i]);
+      }
+      k_partials[slot * d + c] = part;
     }
-    k_partials[slot * d + c] = part;
-  }
-  if (v_partials) {
+  } else {
+    // max |V| of the chunk: channel c of every row, then over the role's threads
     float m = 0.0f;
     if (ok && c < d)
       for (int i = 0; i < n; ++i)
         m = fmaxf(m, fabsf(bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(sv + i * row_bytes + c * 2))));
     m = warp_max(m);
     if ((c & 31) == 0) s_max[c / 32] = m;
-    __syncthreads();
+    named_bar_sync(1, half);
     if (c == 0) {
-      for (int w = 1; w < (static_cast<int>(blockDim.x) + 31) / 32; ++w) m = fmaxf(m, s_max[w]);
+      for (int w = 1; w < half / 32; ++w) m = fmaxf(m, s_max[w]);
       v_partials[slot] = m;
     }
   }
@@ -617,7 +637,8 @@ cudaError_t launch_kv_partials(const void* k, sl8_dtype dt, const void* v, bool 
   TraceScope tr("kv_partials", s);
   const int es = dt == SL8_F32 ? 4 : 2;
   const size_t smem = static_cast<size_t>(kMeanChunk) * d * es * (v_partials ? 2 : 1);
-  const dim3 grid(max_chunks, Hkv, nseq), block((d + 31) / 32 * 32);
+  const int half = (d + 31) / 32 * 32;
+  const dim3 grid(max_chunks, Hkv, nseq), block(v_partials ? 2 * half : half);
   auto go = [&](auto kern) {
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -730,8 +751,15 @@ __global__ void __launch_bounds__(128) kv_finalize_kernel(bool varlen, int32_t H
 constexpr int kQpRows = 64;       // rows per unit (a unit never straddles two sequences)
 constexpr int kQpConsumers = 8;   // consumer warps: 8 rows each, two passes of four
 
+// Run-time claiming: CTA c takes unit c first, then the next unclaimed unit from a
+// per-launch counter.  A launch uses the counter pair g_qp_claim[ticket] ([0] next unit -
+// grid, [1] CTAs done); the last CTA to finish zeroes the pair for the next launch that
+// draws the same ticket (tickets rotate over kQpTickets launches).
+constexpr int kQpTickets = 64;
+__device__ uint32_t g_qp_claim[kQpTickets][2];
+
 // The unit's place, decoded once by the producer and handed to the consumers in the
-// unit's shared-memory stage.
+// unit's shared-memory stage (is_k < 0: no more units).
 struct QpUnit {
   int32_t is_k, h, s, L, tk, t0, vexp, pad;
   int64_t row0;
@@ -753,7 +781,8 @@ struct QpCfg {
 
 template <sl8_dtype DT, int D, bool kGroups>
 __global__ void __launch_bounds__(QpCfg<D>::kThreads, QpCfg<D>::kCtasPerSm)
-    quant_qk_pipe_kernel(const QuantQK a, const float* __restrict__ k_mean, DeviceStatus* st, uint64_t limit_ns) {
+    quant_qk_pipe_kernel(const QuantQK a, const float* __restrict__ k_mean, uint32_t ticket, DeviceStatus* st,
+                         uint64_t limit_ns) {
   using C = QpCfg<D>;
   constexpr int LPR = 8, NV = D / 64, RPP = 32 / LPR, P = kQpRows / kQpConsumers / RPP;
   extern __shared__ __align__(128) uint8_t qp_smem[];
@@ -789,10 +818,24 @@ __global__ void __launch_bounds__(QpCfg<D>::kThreads, QpCfg<D>::kCtasPerSm)
     bool ok = true, waited = !chained;
     int stg = 0;
     uint32_t phase = 0;
-    for (int32_t u = blockIdx.x, i = 0; u < n_units; u += gridDim.x, ++i) {
+    for (int32_t i = 0;; ++i) {
       if (i >= C::kStages)
         ok = __all_sync(0xffffffffu, mbar_wait(&empty[stg], phase ^ 1u, limit_ns, st, 911));
       if (!ok) break;
+      int32_t u = static_cast<int32_t>(blockIdx.x);
+      if (i > 0) {
+        uint32_t c = 0;
+        if (lane == 0) c = atomicAdd(&g_qp_claim[ticket][0], 1u);
+        u = static_cast<int32_t>(gridDim.x + __shfl_sync(0xffffffffu, c, 0));
+      }
+      if (u >= n_units) {
+        // no more units: tell the consumers through the stage
+        if (lane == 0) {
+          reinterpret_cast<QpUnit*>(qp_smem + stg * C::kStageBytes + C::kInfoOff)->is_k = -1;
+          mbar_arrive(&full[stg]);
+        }
+        break;
+      }
       QpUnit x;
       x.pad = 0;
       x.is_k = u >= n_q_units;
@@ -876,18 +919,27 @@ __global__ void __launch_bounds__(QpCfg<D>::kThreads, QpCfg<D>::kCtasPerSm)
         phase ^= 1u;
       }
     }
+    // this CTA claims no more; the last CTA of the launch resets the ticket's counters
+    if (lane == 0) {
+      __threadfence();
+      if (atomicAdd(&g_qp_claim[ticket][1], 1u) == gridDim.x - 1) {
+        atomicExch(&g_qp_claim[ticket][0], 0u);
+        atomicExch(&g_qp_claim[ticket][1], 0u);
+      }
+    }
     return;
   }
   // ------------------------------------------------------------ consumers
   const int rsub = lane / LPR, part = lane % LPR;
   int stg = 0;
   uint32_t phase = 0;
-  for (int32_t u = blockIdx.x; u < n_units; u += gridDim.x) {
+  for (;;) {
     const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[stg], phase, limit_ns, st, 912));
     if (!ok) break;
     const uint8_t* sx = qp_smem + stg * C::kStageBytes;
     const uint8_t* sv = sx + C::kUnitBytes;
     const QpUnit x = *reinterpret_cast<const QpUnit*>(sx + C::kInfoOff);
+    if (x.is_k < 0) break;
     const bool smooth = x.is_k && a.k_partials;
     const bool with_v = x.is_k && convert_v;
     uint16_t* codes = x.is_k ? a.k_codes : a.q_codes;
@@ -1071,7 +1123,10 @@ static cudaError_t launch_quant_pipe(const QuantQK& a, const float* k_mean, cuda
   const int64_t slots = static_cast<int64_t>(num_sms()) * C::kCtasPerSm;
   const int grid = static_cast<int>(units < slots ? units : slots);
   if (grid <= 0) return cudaSuccess;
-  return launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmem, s, a, k_mean, device_status_ptr(), spin_limit_ns());
+  static std::atomic<uint32_t> next_ticket{0};
+  const uint32_t ticket = next_ticket.fetch_add(1, std::memory_order_relaxed) % kQpTickets;
+  return launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmem, s, a, k_mean, ticket, device_status_ptr(),
+                    spin_limit_ns());
 }
 
 template <sl8_dtype DT, bool kGroups>
