@@ -53,6 +53,7 @@ def prefill_ops(w) -> float:
 
 
 CHUNK_Q = 1024   # query chunk of the chunked-prefill line: the last 1024 of the 4096 positions
+CHUNK_Q_SMALL = 128  # a short chunk (16 items for the SMs): the line on which keys are split across CTAs
 
 
 def chunk_ops(w, nq) -> float:
@@ -373,6 +374,15 @@ def run_ours(args, world, rank, local):
         raise RuntimeError(f"device status {st} at {site} after set-up")
 
     stream = torch.cuda.current_stream(dev)
+    if args.only == "paged":
+        pg_ms, pg_split_ms, pg_steps, pg_pages = measure_paged(sl8, W, wd, kc, ks, vc, vs, lens, qdec, seq, stream,
+                                                               flush, flush_sink, args.steps, args.warmup, world)
+        dbytes = decode_bytes(wd, lens)
+        if rank == 0:
+            print(json.dumps({"only": "paged", "ms": pg_ms, "split_ms": pg_split_ms, "pages": pg_pages,
+                              "split_gbs": dbytes / (pg_split_ms * 1e-3) / 1e9,
+                              "frac": dbytes / (pg_split_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}), flush=True)
+        return
 
     def step(ev=None):
         # L2 flush outside the timed events: write a buffer twice the size of L2, then
@@ -464,10 +474,14 @@ def run_ours(args, world, rank, local):
     vf_ms, vf_steps = measure_verify(sl8, wd, kc, ks, vc, vs, lens, seq, stream, flush, flush_sink, args.steps,
                                      args.warmup, world)
     # ---- the prefill's last positions as a query chunk
-    ch_ms, ch_attn_ms, ch_steps = measure_chunk(sl8, wp, qd, kd, vd, stream, flush, flush_sink, args.steps,
-                                                args.warmup, world)
+    ch_ms, ch_attn_ms, ch_steps, ch_kernels = measure_chunk(sl8, wp, qd, kd, vd, stream, flush, flush_sink,
+                                                            args.steps, args.warmup, world)
     ch_ops = chunk_ops(wp, CHUNK_Q)
     ch_tflops = ch_ops / (ch_attn_ms * 1e-3) / 1e12
+    cs_ms, cs_attn_ms, cs_steps, cs_kernels = measure_chunk(sl8, wp, qd, kd, vd, stream, flush, flush_sink,
+                                                            args.steps, args.warmup, world, nq=CHUNK_Q_SMALL)
+    cs_ops = chunk_ops(wp, CHUNK_Q_SMALL)
+    cs_tflops = cs_ops / (cs_attn_ms * 1e-3) / 1e12
     # ---- the same prefill with grouped ("per-warp") scales and outlier-aware Q
     w8_ms, w8_quant_ms, w8_attn_ms, w8_steps = measure_w8a8(sl8, wp, qd, kd, vd, stream, flush, flush_sink,
                                                             args.steps, args.warmup, world)
@@ -529,13 +543,23 @@ def run_ours(args, world, rank, local):
                                       "unit": "TFLOP/s", "frac": w8_tflops / peaks["bf16_tflops"], "traffic": None,
                                       "kernel": "prefill_attn (w8a8)", "peak_source": peaks["source"]}},
         "prefill_chunk": {"value": ch_ops * world / (ch_ms * 1e-3) / 1e12, "unit": "TOPS", "ms": ch_ms,
-                          "steps": ch_steps, "ops": ch_ops,
+                          "steps": ch_steps, "ops": ch_ops, "kernels_ms": ch_kernels,
                           "config": f"the prefill workload's last {CHUNK_Q} positions as a query chunk against "
                                     f"all {wp.N} keys (bottom-right causal), quantisation included, L2 flushed "
                                     "before every step",
                           "roofline": {"bound": "tensor", "achieved": ch_tflops, "peak": peaks["bf16_tflops"],
                                        "unit": "TFLOP/s", "frac": ch_tflops / peaks["bf16_tflops"], "traffic": None,
                                        "kernel": "prefill_attn (chunk)", "peak_source": peaks["source"]}},
+        "prefill_chunk_small": {"value": cs_ops * world / (cs_ms * 1e-3) / 1e12, "unit": "TOPS", "ms": cs_ms,
+                                "steps": cs_steps, "ops": cs_ops, "kernels_ms": cs_kernels,
+                                "config": f"the prefill workload's last {CHUNK_Q_SMALL} positions as a query chunk "
+                                          f"against all {wp.N} keys: keys split across CTAs and merged "
+                                          "(prefill_combine), quantisation of all keys included, L2 flushed "
+                                          "before every step",
+                                "roofline": {"bound": "tensor", "achieved": cs_tflops, "peak": peaks["bf16_tflops"],
+                                             "unit": "TFLOP/s", "frac": cs_tflops / peaks["bf16_tflops"],
+                                             "traffic": None, "kernel": "prefill_attn (split chunk)",
+                                             "peak_source": peaks["source"]}},
         "decode_f16v": {"value": fv_gbs, "unit": "GB/s", "ms": fv_ms, "steps": fv_steps, "bytes": fv_bytes,
                         "config": "the decode workload with int8 K and an fp16 V cache (attn_decode's fp16-V "
                                   "variant), L2 flushed before every step",
@@ -719,7 +743,7 @@ PAGE_SIZE = 64
 
 
 def measure_paged(sl8, W, wd, kc, ks, vc, vs, lens, qdec, seq, stream, flush, flush_sink, steps, warmup, world):
-    """The same decode workload over a paged k8v8 cache (16-token pages in a seeded random
+    """The same decode workload over a paged k8v8 cache (PAGE_SIZE-token pages in a seeded random
     order): the step is the paged split kernel plus the combine, L2 flushed before each."""
     import torch
     table, num_pages = W.page_table(wd, lens, PAGE_SIZE, max_blocks=wd.lmax // PAGE_SIZE)
@@ -781,13 +805,15 @@ def measure_f16v(sl8, W, wd, kc, ks, lens, qdec, seq, stream, flush, flush_sink,
     return ms, (split_ms / c if c else float("nan")), n
 
 
-def measure_chunk(sl8, wp, qd, kd, vd, stream, flush, flush_sink, steps, warmup, world):
-    """The prefill workload's last CHUNK_Q positions as a query chunk against all N keys
+def measure_chunk(sl8, wp, qd, kd, vd, stream, flush, flush_sink, steps, warmup, world, nq=CHUNK_Q):
+    """The prefill workload's last nq positions as a query chunk against all N keys
     (chunked prefill, bottom-right causal): quantisation and attention, L2 flushed before
     each step."""
     import torch
-    qc = qd[:, :, wp.N - CHUNK_Q:].contiguous()
-    ws = torch.empty(sl8.prefill_workspace_bytes(wp.B, wp.Hq, wp.Hkv, wp.N, wp.d), dtype=torch.uint8, device=qd.device)
+    qc = qd[:, :, wp.N - nq:].contiguous()
+    # the chunk workspace: room for the key-split partials the library uses on a small chunk
+    ws = torch.empty(int(sl8.lib().sl8_attn_int8_fwd_chunk_workspace_size(wp.B, wp.Hq, wp.Hkv, nq, wp.N, wp.d)),
+                     dtype=torch.uint8, device=qd.device)
     out = torch.empty_like(qc)
 
     def step(ev=None):
@@ -805,7 +831,7 @@ def measure_chunk(sl8, wp, qd, kd, vd, stream, flush, flush_sink, steps, warmup,
         raise RuntimeError(f"device status {st} at {site} during the chunked prefill")
     ms = max_over_ranks(ms, world)
     c, attn_ms = trace.get("prefill_attn", (0, 0.0))
-    return ms, (attn_ms / c if c else float("nan")), n
+    return ms, (attn_ms / c if c else float("nan")), n, {nm: t / cc for nm, (cc, t) in trace.items() if cc}
 
 
 def measure_w8a8(sl8, wp, qd, kd, vd, stream, flush, flush_sink, steps, warmup, world):
@@ -905,9 +931,10 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode", "w8a8", *OTHER_PREFILL],
+    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode", "paged", "w8a8", *OTHER_PREFILL],
                     help="time one part only (profiling runs): the prefill or decode half of the step, the "
-                         "prefill through attn_w8a8_fwd, or one of the other prefill workloads; no e2e or CPU leg")
+                         "decode over the paged cache, the prefill through attn_w8a8_fwd, or one of the other "
+                         "prefill workloads; no e2e or CPU leg")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup(args)

@@ -142,9 +142,18 @@ SL8_API int sl8_attn_int8_fwd(const void* q, const void* k, const void* v, int q
  * i + Nk - Nq: causal, it sees keys j <= i + Nk - Nq.  K-smoothing, the K codes and the
  * V range run over all Nk keys, so the result equals rows Nk-Nq .. Nk-1 of
  * sl8_attn_int8_fwd on the full sequences.  out [B][Hq][Nq][d], lse_out [B][Hq][Nq].
- * Dense input only; the workspace is sized by sl8_attn_int8_fwd_workspace_size(B, Hq,
- * Hkv, Nk, d, 0).  Other arguments and errors as sl8_attn_int8_fwd.
+ * Dense input only.  The workspace is at least sl8_attn_int8_fwd_workspace_size(B, Hq,
+ * Hkv, Nk, d, 0) bytes.  Given sl8_attn_int8_fwd_chunk_workspace_size(B, Hq, Hkv, Nq, Nk,
+ * d) bytes, a chunk whose (query tile, head) items fill at most half the current
+ * device's SMs (d <= 128) also splits each item's keys into up to 8 parts, so that the
+ * parts run as one wave.  Each part writes a normalised fp32 partial and its log-sum-exp
+ * into the workspace, and a merge step (weights e^(lse - max lse), as the split-KV
+ * decode's combine) forms out and lse_out: the same attention, with P rounded to fp16
+ * against each part's own running maximum.  Other arguments and errors as
+ * sl8_attn_int8_fwd.
  */
+SL8_API size_t sl8_attn_int8_fwd_chunk_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t Nq, int32_t Nk,
+                                                      int32_t d);
 SL8_API int sl8_attn_int8_fwd_chunk(const void* q, const void* k, const void* v, int qk_dtype, int v_dtype, int32_t B,
                                     int32_t Hq, int32_t Hkv, int32_t Nq, int32_t Nk, int32_t d, int causal,
                                     int smooth_k, void* out, int out_dtype, float* lse_out, void* workspace,

@@ -89,6 +89,25 @@ def test_k_mean_bit_exact_dense_and_varlen():
             np.testing.assert_array_equal(muv[s, h], oracle.k_channel_mean(_np(kv[c[s]:c[s + 1], h])))
 
 
+def test_k_mean_bit_exact_f32_keys():
+    """fp32 keys (rows twice as wide as the half-precision ones), dense and ragged."""
+    w = W.custom(2012, B=1, Hq=2, Hkv=2, N=200, d=256, dtype="bf16", k_bias_std=2.0)
+    _, k, _ = W.prefill_dense(w)
+    k32 = k.float() * 1.0009765625  # off the bf16 grid
+    mu = sl8.k_channel_mean(k32.to(DEV)).cpu().numpy()
+    for h in range(2):
+        np.testing.assert_array_equal(mu[0, h], oracle.k_channel_mean(k32[0, h].numpy()))
+    wv = W.custom(2013, kind="varlen", B=3, Hq=2, Hkv=2, d=128, dtype="bf16", k_bias_std=1.0,
+                  extra={"lengths": [65, 1, 190]})
+    _, kv, _, cu = W.prefill_varlen(wv)
+    kv32 = kv.float() * 1.0009765625
+    muv = sl8.k_channel_mean(kv32.to(DEV), cu.to(DEV), max_seqlen=190).cpu().numpy()
+    c = cu.numpy()
+    for s in range(3):
+        for h in range(2):
+            np.testing.assert_array_equal(muv[s, h], oracle.k_channel_mean(kv32[c[s]:c[s + 1], h].numpy()))
+
+
 # ------------------------------------------------------------------ outputs, small shapes
 
 OUT_CASES = [
@@ -343,6 +362,7 @@ CHUNK_CASES = [
     (2606, 1, 4, 4, 70, 400, 128, "bf16", False),
     (2607, 2, 8, 2, 257, 1000, 128, "bf16", True),
     (2608, 1, 4, 2, 100, 333, 32, "f16", True),
+    (2609, 1, 4, 2, 100, 2100, 64, "f16", True),  # 4 items: keys split into 8 parts
 ]
 
 
@@ -364,5 +384,43 @@ def test_prefill_query_chunk(case):
     check_f32(to_np32(o32), ref["out"], f"w{wid} chunk f32")
     check_half(oh, ref["out"], f"w{wid} chunk {dt}")
     np.testing.assert_allclose(to_np32(lse), ref["lse"], rtol=0, atol=1e-4)
-    # the chunk's rows are the full prefill's last rows (same codes, same tiles of keys)
-    np.testing.assert_allclose(to_np32(o32), to_np32(full[:, :, Nk - Nq:]), rtol=0, atol=1e-6)
+    # the default workspace lets a small chunk split its keys across CTAs and merge the
+    # parts: the same attention, with P rounded to fp16 against each part's own running max
+    # (so within that rounding of the unsplit rows; the oracle checks above are the bar)
+    np.testing.assert_allclose(to_np32(o32), to_np32(full[:, :, Nk - Nq:]), rtol=0, atol=2e-4)
+    # with only the plain prefill workspace the chunk is not split: its rows are the full
+    # prefill's last rows (same codes, same tiles of keys, same order)
+    base_ws = torch.empty(sl8.prefill_workspace_bytes(B, Hq, Hkv, Nk, d), dtype=torch.uint8, device=DEV)
+    o32b, lseb = sl8.attn_int8_fwd_chunk(qc.to(DEV), k.to(DEV), v.to(DEV), causal=causal, smooth_k=True,
+                                         out_dtype=torch.float32, return_lse=True, workspace=base_ws)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(to_np32(o32b), to_np32(full[:, :, Nk - Nq:]), rtol=0, atol=1e-6)
+    np.testing.assert_allclose(to_np32(lseb), to_np32(lse), rtol=0, atol=1e-4)
+    _status_ok()
+
+
+def test_chunk_key_split_is_used_and_matches():
+    """A 256-query chunk of the Qwen3-8B-shaped prefill: 32 (query tile, head pair) items
+    for the GPU's SMs, so the default workspace splits each item's keys.  The split form
+    and the unsplit form (plain workspace) agree with each other and with the oracle on
+    sampled rows.  The 1024-query chunk (128 items) is left unsplit."""
+    w = W.get("qwen3_8b")
+    q, k, v = W.prefill_dense(w)
+    small = sl8.prefill_workspace_bytes(w.B, w.Hq, w.Hkv, w.N, w.d)
+    assert sl8.lib().sl8_attn_int8_fwd_chunk_workspace_size(w.B, w.Hq, w.Hkv, 1024, w.N, w.d) == small
+    nq = 256
+    qc = q[:, :, w.N - nq:].contiguous()
+    qd, kd, vd = qc.to(DEV), k.to(DEV), v.to(DEV)
+    big = sl8.lib().sl8_attn_int8_fwd_chunk_workspace_size(w.B, w.Hq, w.Hkv, nq, w.N, w.d)
+    assert big > small
+    o_split, l_split = sl8.attn_int8_fwd_chunk(qd, kd, vd, out_dtype=torch.float32, return_lse=True)
+    o_one, l_one = sl8.attn_int8_fwd_chunk(qd, kd, vd, out_dtype=torch.float32, return_lse=True,
+                                           workspace=torch.empty(small, dtype=torch.uint8, device=DEV))
+    torch.cuda.synchronize()
+    _status_ok()
+    np.testing.assert_allclose(to_np32(o_split), to_np32(o_one), rtol=0, atol=2e-4)
+    np.testing.assert_allclose(to_np32(l_split), to_np32(l_one), rtol=0, atol=1e-4)
+    rng = np.random.default_rng(11)
+    rows = [(0, h, int(i)) for h in range(w.Hq) for i in rng.integers(0, nq, size=8)]
+    ref = oracle.attn_prefill(_np(qc), _np(k), _np(v), causal=True, smooth_k=True, rows=rows)
+    check_f32(to_np32(o_split), ref["out"], "chunk 256 split f32")

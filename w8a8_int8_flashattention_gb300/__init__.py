@@ -67,6 +67,7 @@ _SIGNATURES = {
     "sl8_attn_int8_fwd_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I64]),
     "sl8_attn_int8_fwd": (_INT, [_P, _P, _P, _INT, _INT, _I32, _I32, _I32, _I32, _I32, _P, _I64, _INT, _INT, _P,
                                  _INT, _P, _P, _SZ, _P]),
+    "sl8_attn_int8_fwd_chunk_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
     "sl8_attn_int8_fwd_chunk": (_INT, [_P, _P, _P, _INT, _INT, _I32, _I32, _I32, _I32, _I32, _I32, _INT, _INT, _P,
                                        _INT, _P, _P, _SZ, _P]),
     "sl8_attn_int8_qk_logits_debug": (_INT, [_P, _P, _INT, _I32, _I32, _I32, _I32, _I32, _P, _I64, _INT, _I32, _I32,
@@ -275,8 +276,9 @@ def attn_int8_fwd_chunk(q, k, v, causal=True, smooth_k=True, out_dtype=None, ret
         out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
     if return_lse and lse is None:
         lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
-    ws_bytes = prefill_workspace_bytes(B, Hq, Hkv, Nk, d, 0)
     if workspace is None:
+        # room for the key-split partials, which the library uses when the chunk is small
+        ws_bytes = int(lib().sl8_attn_int8_fwd_chunk_workspace_size(B, Hq, Hkv, Nq, Nk, d))
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
     _check(lib().sl8_attn_int8_fwd_chunk(_ptr(q), _ptr(k), _ptr(v), _dt(q), _dt(v), B, Hq, Hkv, Nq, Nk, d,
                                          int(bool(causal)), int(bool(smooth_k)), _ptr(out), _dt(out),

@@ -347,7 +347,7 @@ static int prefill_prepare(const void* q, const void* k, const void* v, int qk_d
   if (smooth_k || v_stats) {
     SL8_LAUNCH(launch_kv_partials(k, static_cast<sl8_dtype>(qk_dtype), v_stats ? v : nullptr, varlen, B, Hkv, N, d,
                                   varlen ? t.len : nullptr, varlen ? t.tok0 : nullptr, k_partials, v_partials,
-                                  p.max_chunks, s));
+                                  p.max_chunks, tokens, s));
     SL8_LAUNCH(launch_kv_finalize(varlen, B, Hkv, N, d, varlen ? t.len : nullptr, k_partials, v_partials, p.max_chunks,
                                   reinterpret_cast<float*>(ws + p.k_mean), reinterpret_cast<int32_t*>(ws + p.v_exp),
                                   s));
@@ -362,6 +362,43 @@ static int prefill_prepare(const void* q, const void* k, const void* v, int qk_d
   *plan = p;
   *table = t;
   return SL8_OK;
+}
+
+// Key splits of a dense query chunk (the attention kernel for d <= 128 only).  When the
+// chunk's (query tile, head) items number at most half the SMs, each item's keys are cut
+// into SMs / items parts (at most kMaxKeySplit, each keeping at least two key tiles of
+// the longest item), so that the parts run as one wave.  Larger chunks are not split: a
+// part costs about one key tile's time to fill and drain the tile pipeline, and the merge
+// reads every partial once more, which outweighs rebalancing a wave that is mostly full.
+static int32_t chunk_kv_split(int32_t B, int32_t Hq, int32_t Hkv, int32_t Nk, int32_t Nq, int32_t d) {
+  const int32_t dc = compute_dim(d);
+  if (dc > 128 || Nq <= 0 || B <= 0) return 1;
+  const int32_t item_rows = prefill_item_rows(dc, Hq / Hkv);
+  const int64_t per_seq = (Nk + item_rows - 1) / item_rows - (Nk - Nq) / item_rows;
+  const int64_t items = static_cast<int64_t>(B) * per_seq * (prefill_head_pairs(dc, Hq / Hkv) ? Hq / 2 : Hq);
+  const int64_t sms = num_sms();
+  if (2 * items > sms) return 1;
+  int64_t split = sms / items;
+  const int64_t max_tiles = (Nk + kQTile - 1) / kQTile;
+  if (split > max_tiles / 2) split = max_tiles / 2;
+  if (split > kMaxKeySplit) split = kMaxKeySplit;
+  return split < 1 ? 1 : static_cast<int32_t>(split);
+}
+
+// Bytes of the key-split partials of a chunk split into `split` parts: O [split][B * Hq *
+// Nq][d] fp32, then (256-byte aligned) the LSE [split][B * Hq * Nq].
+static size_t chunk_partial_o_bytes(int32_t split, int64_t rows, int32_t d) {
+  return align_up(static_cast<size_t>(split) * rows * d * sizeof(float), 256);
+}
+
+// Workspace of a query chunk: the prefill plan over Nk keys, then the key-split partials
+// when the chunk is split on this device.
+static size_t chunk_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t Nq, int32_t Nk, int32_t d) {
+  const PrefillWorkspace p = plan_prefill_workspace(B, Hq, Hkv, Nk, d, 0, false);
+  const int32_t split = chunk_kv_split(B, Hq, Hkv, Nk, Nq, d);
+  if (split <= 1) return p.total;
+  const int64_t rows = static_cast<int64_t>(B) * Hq * Nq;
+  return p.total + chunk_partial_o_bytes(split, rows, d) + static_cast<size_t>(split) * rows * sizeof(float);
 }
 
 // Prefill over N keys per sequence; q_off > 0 (dense only): a query chunk of the last
@@ -419,6 +456,22 @@ static int prefill_run(const void* q, const void* k, const void* v, int qk_dtype
   a.out_dtype = static_cast<sl8_dtype>(out_dtype);
   a.lse = lse_out;
   a.logits = nullptr;
+  a.kv_split = 1;
+  // A query chunk on few items: split each item's keys so that the parts fill the GPU,
+  // when the caller's workspace holds the partials (sl8_attn_int8_fwd_chunk_workspace_size).
+  const int32_t split = q_off > 0 ? chunk_kv_split(B, Hq, Hkv, N, N - q_off, d) : 1;
+  if (split > 1 && workspace_bytes >= chunk_workspace_bytes(B, Hq, Hkv, N - q_off, N, d)) {
+    const int64_t rows = static_cast<int64_t>(B) * Hq * (N - q_off);
+    a.kv_split = split;
+    a.o_part = reinterpret_cast<float*>(ws + p.total);
+    a.lse_part = reinterpret_cast<float*>(ws + p.total + chunk_partial_o_bytes(split, rows, d));
+    a.out = nullptr;
+    a.lse = nullptr;
+    SL8_LAUNCH(launch_prefill(a, s));
+    SL8_LAUNCH(launch_prefill_combine(a.o_part, a.lse_part, rows, d, split, out, static_cast<sl8_dtype>(out_dtype),
+                                      lse_out, s));
+    return SL8_OK;
+  }
   SL8_LAUNCH(launch_prefill(a, s));
   return SL8_OK;
 }
@@ -429,6 +482,11 @@ int sl8_attn_int8_fwd(const void* q, const void* k, const void* v, int qk_dtype,
                       size_t workspace_bytes, void* stream) {
   return prefill_run(q, k, v, qk_dtype, v_dtype, B, Hq, Hkv, N, d, cu_seqlens, total_tokens, causal, smooth_k, out,
                      out_dtype, lse_out, workspace, workspace_bytes, stream, 0);
+}
+
+size_t sl8_attn_int8_fwd_chunk_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t Nq, int32_t Nk, int32_t d) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || Nk < Nq || d <= 0) return 0;
+  return chunk_workspace_bytes(B, Hq, Hkv, Nq, Nk, d);
 }
 
 int sl8_attn_int8_fwd_chunk(const void* q, const void* k, const void* v, int qk_dtype, int v_dtype, int32_t B,

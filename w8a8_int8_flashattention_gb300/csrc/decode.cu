@@ -100,8 +100,7 @@ struct DCfg {
   static constexpr int kQBytes = 8 * D * 4;                    // 8 raw q rows, fp32 at most
   static constexpr int kQ = kStages * kStageBytes;             // [2] raw q rows
   static constexpr int kRed = kQ + kQSlots * kQBytes;          // [warp][d][8 q] floats
-  static constexpr int kP = kRed + kNW * D * 8 * 4;            // [warp][8 q][8 token pairs] fp16x2
-  static constexpr int kStat = kP + kNW * 256;                 // [warp][8 q][4] floats
+  static constexpr int kStat = kRed + kNW * D * 8 * 4;         // [warp][8 q][4] floats
   static constexpr int kQcBytes = 8 * D + 64;                  // 8 code rows, 8 scales, 8 code sums
   static constexpr int kQc = kStat + kNW * 8 * 16;             // [2] quantised q rows
   static constexpr int kSched = kQc + kQSlots * kQcBytes;      // Sched
@@ -185,6 +184,13 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
+}
+// Transpose of an 8x8 fp16 matrix held one register per lane (lane l: row l / 4,
+// columns 2 (l % 4) and 2 (l % 4) + 1), into the same layout.
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
 }
 __device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
@@ -498,27 +504,45 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
       }
       return true;
     };
+    // paged cache: the block-table entry of this lane's unit in the stage of slot x that
+    // starts at token c0 (0 when the lane has no unit there)
+    const bool paged = !kV16 && a.block_table != nullptr;
+    auto page_of = [&](const Slot& x, int c0) {
+      const int t = c0 + lane * kUnit;
+      return paged && x.b >= 0 && t < x.t1 ? a.block_table[static_cast<int64_t>(x.b) * a.max_blocks + t / a.page_size]
+                                          : 0;
+    };
+    // and an L2 prefetch of the entries a slot will read, issued a slot ahead
+    auto prefetch_pages = [&](const Slot& x) {
+      if (!paged || x.b < 0) return;
+      const int p0 = x.t0 / a.page_size, p1 = (x.t1 - 1) / a.page_size;
+      const int32_t* row = a.block_table + static_cast<int64_t>(x.b) * a.max_blocks;
+      for (int e = (p0 & ~7) + 8 * lane; e <= p1; e += 8 * 32) prefetch_l2(row + (e < p0 ? p0 : e));
+    };
     Slot cur, nxt;
     bool has_cur = next_entry(cur);
     ok = ok && announce(cur, 0);
+    // the page of this lane's unit in the next stage to issue, loaded one stage early
+    int pg_ahead = has_cur ? page_of(cur, cur.t0) : 0;
     while (ok && has_cur) {
       const bool has_nxt = next_entry(nxt);
       if (!ok || !announce(nxt, n + 1)) break;
+      prefetch_pages(nxt);
       const int64_t row0 = (static_cast<int64_t>(cache_seq(a, cur.b)) * (a.Hkv / a.kv_groups) + cur.hkv / a.kv_groups) *
                            a.Lmax;
       for (int c0 = cur.t0; c0 < cur.t1 && ok; c0 += C::kChunk, ++k) {
         const int nt = min(C::kChunk, cur.t1 - c0);
         const uint32_t stg = k % kStages;
         uint8_t* base = smem + stg * C::kStageBytes;
-        // paged cache: the page of this lane's unit, read before the wait for the stage
-        // so that the wait covers the load's latency
+        // paged cache: the page of this lane's unit (loaded during the previous stage), and
+        // the load of the next stage's, whose latency this stage's wait and issue cover
         const int t = c0 + lane * kUnit;
         const int units = (nt + kUnit - 1) / kUnit;
-        int pg = 0;
-        if (!kV16 && a.block_table && lane < units) pg = a.block_table[static_cast<int64_t>(cur.b) * a.max_blocks + t / a.page_size];
+        int pg = pg_ahead;
+        if (paged) pg_ahead = c0 + C::kChunk < cur.t1 ? page_of(cur, c0 + C::kChunk) : has_nxt ? page_of(nxt, nxt.t0) : 0;
         if (k >= kStages) ok = warp_wait(&empty[stg], ((k / kStages) - 1) & 1, limit_ns, st, 41);
         if (!ok) break;
-        if (!kV16 && a.block_table) {
+        if (paged) {
           // paged cache: the stage's 16-token units (page_size is a multiple of 16; units
           // past the split's end are not loaded, their compute warps skip them) fall into
           // pieces that each lie in one page; the lane of a piece's first unit loads the
@@ -673,9 +697,13 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
   const int cw = ct / 32;                            // compute warp 0 .. 7
   const int g = lane >> 2, t = lane & 3;
   const int u0 = kUnit * cw;  // this warp's rows in every stage
-  // S^T rows of this lane: unit tokens pi and pi + 8.  The permutation keeps the
-  // swizzled K reads free of bank conflicts, and the two tokens form P' pair pi.
-  const int pi = C::kSwz ? (g >> 1) + 4 * (g & 1) : g;
+  // S^T row r (and r + 8) holds unit token tok(r) (and tok(r) + 8).  The permutation keeps
+  // the K reads (row tok(g), 16-byte chunk t) and the V reads (rows tok(2t), tok(2t + 1),
+  // + 8) free of bank conflicts, or at two ways for the 64-byte rows of d = 64.
+  auto tok = [](int r) {
+    return C::kSwz ? (r >> 1) + 4 * (r & 1) : ((r & 1) ? 4 + ((r >> 1) ^ 1) : (r >> 1));
+  };
+  const int pi = tok(g);
   // V^T rows of this lane: 16-byte chunk (8-byte piece for d = 64) pi of each V row
   const int cg = pi;
   // stage-tile offsets of this lane's reads, the same for every stage
@@ -685,23 +713,24 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
     offk[h][0] = tile_off<D>(u0 + pi, 4 * h + t);
     offk[h][1] = tile_off<D>(u0 + pi + 8, 4 * h + t);
   }
-  // V rows: unit tokens t, t + 8, t + 4, t + 12 are the k columns 2t, 2t+1, 2t+8, 2t+9
+  // V rows: the k columns 2t, 2t+1, 2t+8, 2t+9 of P'^T are the S^T rows 2t, 2t+1 of the
+  // two 8-row halves (movm_t transposes each half), i.e. unit tokens tok(2t), tok(2t+1)
+  // and the same + 8
   uint32_t offv[C::kBoxes][4];
 #pragma unroll
   for (int b = 0; b < C::kBoxes; ++b)
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const int row = u0 + t + (c == 1 ? 8 : c == 2 ? 4 : c == 3 ? 12 : 0);
+      const int row = u0 + tok(2 * t + (c & 1)) + 8 * (c >> 1);
       offv[b][c] = D == 64 ? static_cast<uint32_t>(row * 64 + 8 * cg) : tile_off<D>(row, 8 * b + cg);
     }
   // fp16 V: this lane's ldmatrix row address for m-tile j (dims 16 j ..): it serves matrix
   // i = lane / 8 (dims + 8 (i % 2); k columns 8 (i / 2) ..) and its row r = lane % 8, the
-  // token at k column 8 (i / 2) + r in the order of the P' pairs (k 2p -> token p,
-  // k 2p + 1 -> token p + 8 within each half of k)
+  // token at k column 8 (i / 2) + r: tok(r) + 8 (i / 2)
   uint32_t offv16[kV16 ? D / 16 : 1];
   if constexpr (kV16) {
     const int i = lane >> 3, r = lane & 7;
-    const int row = u0 + 4 * (i >> 1) + (r >> 1) + 8 * (r & 1);
+    const int row = u0 + 8 * (i >> 1) + tok(r);
 #pragma unroll
     for (int j = 0; j < D / 16; ++j) {
       const int chunk = 2 * j + (i & 1);
@@ -709,7 +738,6 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
     }
   }
   const float log2e_over_sqrtd = 1.4426950408889634f / sqrtf(static_cast<float>(D));
-  uint32_t* pw = reinterpret_cast<uint32_t*>(smem + C::kP + cw * 256);  // [8 q][8 pairs] fp16x2
 
   // ---- empty splits, up front: lse = -inf (their O is never read), and the q codes of
   // an empty sequence when asked; sequences b = blockIdx.x + k * gridDim.x
@@ -971,12 +999,9 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
         l_a += pa0 + pb0;
         l_b += pa1 + pb1;
         const float wA = vsA * inv, wB = vsB * inv;
-        // ---- P'^T in B-fragment order: pair tau holds tokens (tau, tau + 8) of one query
-        __syncwarp();
-        pw[(2 * t) * 8 + pi] = f16x2_of(pa0 * wA, pb0 * wB);
-        pw[(2 * t + 1) * 8 + pi] = f16x2_of(pa1 * wA, pb1 * wB);
-        __syncwarp();
-        const uint32_t pb0r = pw[g * 8 + t], pb1r = pw[g * 8 + 4 + t];
+        // ---- P'^T as B fragments: the fp16 S^T layout of P', each 8-row half transposed
+        const uint32_t pb0r = movm_t(f16x2_of(pa0 * wA, pa1 * wA));
+        const uint32_t pb1r = movm_t(f16x2_of(pb0 * wB, pb1 * wB));
         // ---- O'^T += V_biased^T . P'^T (V codes + 128 as fp16 subnormals), and the row
         // sums of P' from an all-ones A for the offset; fp16 V: O'^T += V^T . P'^T with the
         // A fragments read transposed from the [token][dim] tile

@@ -100,6 +100,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
 // (head pairs) one Q tile of two query heads that share a kv head.
 struct Item {
   int32_t s, it, hq, hkv, L, pstart, tok0;
+  int32_t part;  // key split of the item (PrefillArgs::kv_split), 0 without splits
 };
 
 // Query heads handled per (sequence, row block) entry of the work list.
@@ -110,8 +111,16 @@ __device__ __forceinline__ int item_heads(const PrefillArgs& a) { return a.head_
 // index max_items - 1 - p / nseq of sequence p % nseq, which is the same order (a query
 // chunk's items start at dense_first, the item holding its first position).  With
 // head pairs, w.hq is the first of the item's two query heads.
+// kSplit = false: the launch has no key splits (kv_split <= 1), known at compile time.
+template <bool kSplit = false>
 __device__ __forceinline__ Item decode_item(const PrefillArgs& a, int64_t item, int group) {
   Item w;
+  w.part = 0;
+  if (kSplit && a.kv_split > 1) {  // the parts of one item are consecutive items
+    const int64_t base = item / a.kv_split;
+    w.part = static_cast<int32_t>(item - base * a.kv_split);
+    item = base;
+  }
   const int hh = item_heads(a);
   const int64_t pair = item / hh;
   w.hq = static_cast<int32_t>(item - pair * hh) * (a.head_pairs ? 2 : 1);
@@ -132,10 +141,28 @@ __device__ __forceinline__ Item decode_item(const PrefillArgs& a, int64_t item, 
   }
   return w;
 }
-// Number of work items (pairs x query heads, or x head pairs).
+// Number of work items (pairs x query heads, or x head pairs, x key splits).
+template <bool kSplit = false>
 __device__ __forceinline__ int64_t count_items(const PrefillArgs& a) {
   return (a.varlen ? static_cast<int64_t>(a.table.counts[0]) : static_cast<int64_t>(a.nseq) * a.dense_items) *
-         item_heads(a);
+         item_heads(a) * (kSplit && a.kv_split > 1 ? a.kv_split : 1);
+}
+
+// Key tiles [jb, je) a Q tile with nkv_t key tiles visits in item part w.part: all of them
+// without splits, else part w.part of the item's longest range (nkv_max tiles) cut into
+// kv_split equal parts (je <= jb: none).
+template <bool kSplit>
+__device__ __forceinline__ void part_range(const PrefillArgs& a, const Item& w, int nkv_t, int nkv_max, int& jb,
+                                           int& je) {
+  if (!kSplit || a.kv_split <= 1) {
+    jb = 0;
+    je = nkv_t;
+    return;
+  }
+  const int per = (nkv_max + a.kv_split - 1) / a.kv_split;
+  jb = w.part * per;
+  je = min(jb + per, nkv_t);
+  if (je < jb) je = jb;
 }
 
 // Q tile t (0, 1) of a two-tile item: its tile index in the sequence and its query head.
@@ -365,16 +392,53 @@ __device__ __forceinline__ void logits_step(uint32_t s_taddr, const PrefillArgs&
   }
 }
 
-// Normalised output row (and LSE) from O in TMEM.
-template <int D>
+// Output row index of position row_abs of item w's head (dense or varlen; a query chunk's
+// output holds positions q_off .. N-1).
+__device__ __forceinline__ int64_t out_row(const PrefillArgs& a, const Item& w, int row_abs) {
+  return a.varlen ? (static_cast<int64_t>(w.tok0) + row_abs) * a.Hq + w.hq
+                  : (static_cast<int64_t>(w.s) * a.Hq + w.hq) * (a.N - a.q_off) + row_abs - a.q_off;
+}
+
+// A key-split part with no keys for this row: log-sum-exp -inf (its O is never read).
+__device__ __forceinline__ void store_empty_part(const PrefillArgs& a, const Item& w, int row_abs) {
+  if (row_abs < w.L && row_abs >= a.q_off) {
+    const int64_t rows = static_cast<int64_t>(a.nseq) * a.Hq * (a.N - a.q_off);
+    a.lse_part[w.part * rows + out_row(a, w, row_abs)] = -INFINITY;
+  }
+}
+
+// Normalised output row (and LSE) from O in TMEM; with key splits, the part's normalised
+// fp32 row and log-sum-exp into the partials.
+template <int D, bool kSplit = false>
 __device__ __forceinline__ void store_row(uint32_t o_taddr, const PrefillArgs& a, const Item& w, int row_abs, float m,
                                           float l, float v_unscale) {
   const bool row_ok = row_abs < w.L && row_abs >= a.q_off;
+  if (kSplit && a.kv_split > 1) {
+    const int64_t rows = static_cast<int64_t>(a.nseq) * a.Hq * (a.N - a.q_off);
+    const int64_t prow = w.part * rows + out_row(a, w, row_abs);
+    const float sc = v_unscale / l;
+#pragma unroll
+    for (int c0 = 0; c0 < D; c0 += 64) {
+      uint32_t v[64];
+      tmem_ld32(o_taddr + c0, *reinterpret_cast<uint32_t(*)[32]>(v));
+      tmem_ld32(o_taddr + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      tmem_wait_ld();
+      if (row_ok) {
+        float4* dst = reinterpret_cast<float4*>(a.o_part + prow * a.d_io + c0);
+#pragma unroll
+        for (int c = 0; c < 64; c += 4)
+          if (c0 + c < a.d_io)
+            dst[c / 4] = make_float4(__uint_as_float(v[c]) * sc, __uint_as_float(v[c + 1]) * sc,
+                                     __uint_as_float(v[c + 2]) * sc, __uint_as_float(v[c + 3]) * sc);
+      }
+    }
+    if (row_ok) a.lse_part[prow] = (m + __log2f(l)) * kLn2;
+    return;
+  }
   const float scale = v_unscale / l;
   const bool out_f32 = a.out_dtype == SL8_F32, out_bf16 = a.out_dtype == SL8_BF16;
   // a query chunk's output holds positions q_off .. N-1
-  const int64_t orow = a.varlen ? (static_cast<int64_t>(w.tok0) + row_abs) * a.Hq + w.hq
-                                : (static_cast<int64_t>(w.s) * a.Hq + w.hq) * (a.N - a.q_off) + row_abs - a.q_off;
+  const int64_t orow = out_row(a, w, row_abs);
   // 64 columns per TMEM round trip
 #pragma unroll
   for (int c0 = 0; c0 < D; c0 += 64) {
@@ -508,7 +572,7 @@ struct PairBars {
 };
 static_assert(sizeof(PairBars) <= 256, "pair kernel barrier block");
 
-template <int D, bool kLogits>
+template <int D, bool kLogits, bool kSplit>
 __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                         const __grid_constant__ CUtensorMap map_v, const PrefillArgs a, DeviceStatus* st,
@@ -522,7 +586,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const bool causal = kLogits ? false : a.causal;
   const int group = a.Hq / a.Hkv;
-  const int64_t n_items = count_items(a);
+  const int64_t n_items = count_items<kSplit>(a);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -576,8 +640,13 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
         bars.item_idx[slot] = static_cast<int32_t>(item);
         mbar_arrive(&bars.item_full[slot]);
         if (item < 0) break;
-        const Item w = decode_item(a, item, group);
-        const int nkv = max(tile_nkv<BN>(tile_qt(a, w, 0), w.L, causal, a.q_off), tile_nkv<BN>(tile_qt(a, w, 1), w.L, causal, a.q_off));
+        const Item w = decode_item<kSplit>(a, item, group);
+        const int nkv0 = tile_nkv<BN>(tile_qt(a, w, 0), w.L, causal, a.q_off);
+        const int nkv1 = tile_nkv<BN>(tile_qt(a, w, 1), w.L, causal, a.q_off);
+        int jb, je0, je1;
+        part_range<kSplit>(a, w, nkv0, max(nkv0, nkv1), jb, je0);
+        part_range<kSplit>(a, w, nkv1, max(nkv0, nkv1), jb, je1);
+        const int je = max(je0, je1);
         // both Q tiles are always loaded (a tile past the end reads rows no one uses)
         for (int t = 0; t < 2 && ok; ++t) {
           if (it >= 1) ok = mbar_wait(&bars.q_empty[t], (it - 1) & 1, limit_ns, st, 10);
@@ -586,7 +655,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
           load_q_tile(smem + C::kQOff + t * C::kQBytes, &map_q, &bars.q_full[t], C::kBoxes,
                       w.pstart + tile_qt(a, w, t) * kQTile, tile_item(a, w, t).hq);
         }
-        for (int j = 0; j < nkv && ok; ++j, ++g) {
+        for (int j = jb; j < je && ok; ++j, ++g) {
           const uint32_t stg = g % C::kStages, n = g / C::kStages;
           if (g >= C::kStages) ok = mbar_wait(&bars.k_empty[stg], (n - 1) & 1, limit_ns, st, 11);
           if (!ok || *abort_flag) break;
@@ -610,15 +679,27 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.item_empty[slot]);
         if (item < 0) break;
-        const Item w = decode_item(a, item, group);
-        const int nkv_t[2] = {tile_nkv<BN>(tile_qt(a, w, 0), w.L, causal, a.q_off),
-                              tile_nkv<BN>(tile_qt(a, w, 1), w.L, causal, a.q_off)};
+        const Item w = decode_item<kSplit>(a, item, group);
+        // key tiles of each Q tile in this item (part), counted from the part's first, jb
+        const int nkv0 = tile_nkv<BN>(tile_qt(a, w, 0), w.L, causal, a.q_off);
+        const int nkv1 = tile_nkv<BN>(tile_qt(a, w, 1), w.L, causal, a.q_off);
+        int jb, je0, je1;
+        part_range<kSplit>(a, w, nkv0, max(nkv0, nkv1), jb, je0);
+        part_range<kSplit>(a, w, nkv1, max(nkv0, nkv1), jb, je1);
+        const int nkv_t[2] = {je0 - jb, je1 - jb};
         const int nkv = max(nkv_t[0], nkv_t[1]);
         ok = warp_wait(&bars.q_full[0], it & 1, limit_ns, st, 20) &&
              warp_wait(&bars.q_full[1], it & 1, limit_ns, st, 20);
-        if (ok) ok = warp_wait(&bars.k_full[g % C::kStages], (g / C::kStages) & 1, limit_ns, st, 21);
+        if (ok && (!kSplit || nkv > 0)) ok = warp_wait(&bars.k_full[g % C::kStages], (g / C::kStages) & 1, limit_ns, st, 21);
         if (!ok) break;
         tc_fence_after();
+        if (kSplit && nkv == 0) {
+          // a key split with no key tiles for either Q tile: nothing to compute or load
+          mma_commit(&bars.q_empty[0]);
+          mma_commit(&bars.q_empty[1]);
+          issued = true;
+          continue;
+        }
         {
           const uint32_t kaddr = smem_u32(smem + C::kKOff + (g % C::kStages) * C::kKVBytes);
           for (int t = 0; t < 2; ++t) {
@@ -693,11 +774,17 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.item_empty[slot]);
       if (item < 0) break;
-      const Item w = tile_item(a, decode_item(a, item, group), t);  // this warpgroup's Q tile
+      const Item w = tile_item(a, decode_item<kSplit>(a, item, group), t);  // this warpgroup's Q tile
       const int qt = tile_qt(a, w, t);
-      const int nkv = tile_nkv<BN>(qt, w.L, causal, a.q_off);
-      if (nkv == 0) continue;  // this tile lies past the sequence's end
+      const int nkv_full = tile_nkv<BN>(qt, w.L, causal, a.q_off);
+      if (nkv_full == 0) continue;  // this tile lies past the sequence's end (or before a chunk)
       const int row_abs = qt * kQTile + r;
+      int jb, je;
+      part_range<kSplit>(a, w, nkv_full, max(nkv_full, tile_nkv<BN>(tile_qt(a, w, 1 - t), w.L, causal, a.q_off)), jb, je);
+      if (je <= jb) {  // a key split that reaches none of this tile's keys: an empty part
+        store_empty_part(a, w, row_abs);
+        continue;
+      }
       QuadRows rs;
       const float* qs = a.q_scales + static_cast<int64_t>(w.hq) * a.t_pad_max + w.pstart + qt * kQTile + wrow;
 #pragma unroll
@@ -710,7 +797,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
       const int ve = a.v_exp ? a.v_exp[static_cast<int64_t>(w.s) * a.Hkv + w.hkv] : 0;
       const float v_unscale = __int_as_float((127 + ve) << 23);
       const float* ksrc = a.k_scales + static_cast<int64_t>(w.hkv) * a.t_pad_max + w.pstart;
-      for (int j = 0; j < nkv; ++j, ++ns) {
+      for (int j = jb; j < je; ++j, ++ns) {
         if (*abort_flag) {
           bad = true;
           break;
@@ -728,7 +815,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
         } else {
           const bool need_mask = (causal && key0 + BN - 1 > qt * kQTile) || (key0 + BN > w.L);
           // O_t is safe to touch: S_t(j) was issued after PV_t(j-1), and its commit covers it
-          if (!softmax_step<BN, D>(s_taddr, o_taddr, ks, need_mask, key0, w.L, causal, j == 0, rs, nullptr, 0,
+          if (!softmax_step<BN, D>(s_taddr, o_taddr, ks, need_mask, key0, w.L, causal, j == jb, rs, nullptr, 0,
                                    limit_ns, st)) {
             bad = true;
             break;
@@ -749,7 +836,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
         if constexpr (!kLogits) {
           float m, l;
           quad_rows_to_lane(rs, m, l);
-          store_row<D>(o_taddr, a, w, row_abs, m, l, v_unscale);
+          store_row<D, kSplit>(o_taddr, a, w, row_abs, m, l, v_unscale);
         }
       }
       ++no;
@@ -1050,15 +1137,15 @@ static bool make_maps(const PrefillArgs& a, int D, CUtensorMap* mq, CUtensorMap*
   return ok;
 }
 
-template <int D, bool kLogits>
+template <int D, bool kLogits, bool kSplit = false>
 static cudaError_t launch_pair(const PrefillArgs& a, cudaStream_t s) {
   using C = PairCfg<D>;
   CUtensorMap mq, mk, mv;
   if (!make_maps<C::BN>(a, D, &mq, &mk, &mv)) return cudaErrorInvalidValue;
-  auto kern = prefill_pair_kernel<D, kLogits>;
+  auto kern = prefill_pair_kernel<D, kLogits, kSplit>;
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int64_t max_items = a.max_pairs * a.Hq;
+  const int64_t max_items = a.max_pairs * a.Hq * (kSplit ? a.kv_split : 1);
   const int grid = static_cast<int>(max_items < num_sms() ? max_items : num_sms());
   if (grid <= 0) return cudaSuccess;
   TraceScope tr(kLogits ? "prefill_logits" : "prefill_attn", s);
@@ -1084,14 +1171,76 @@ static cudaError_t launch_single(const PrefillArgs& a, cudaStream_t s) {
 
 }  // namespace
 
+// Merge of the key-split partials of a query chunk: one warp per output row; weights
+// e^(lse_p - max lse) over the parts that saw a key (lse -inf parts are skipped).  Every
+// part's LSE and row slice are loaded before any is used (at most kMaxKeySplit parts).
+template <int EPL>
+static __global__ void __launch_bounds__(256) prefill_combine_kernel(const float* __restrict__ o_part,
+                                                              const float* __restrict__ lse_part, int64_t rows,
+                                                              int d_io, int S, void* __restrict__ out,
+                                                              sl8_dtype out_dtype, float* __restrict__ lse) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+  if (row >= rows) return;
+  const int lane = threadIdx.x & 31;
+  float lp[kMaxKeySplit], x[kMaxKeySplit][EPL];
+#pragma unroll
+  for (int p = 0; p < kMaxKeySplit; ++p) {
+    lp[p] = p < S ? lse_part[p * rows + row] : -INFINITY;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) x[p][e] = p < S ? o_part[(p * rows + row) * d_io + lane * EPL + e] : 0.0f;
+  }
+  float M = -INFINITY;
+#pragma unroll
+  for (int p = 0; p < kMaxKeySplit; ++p) M = fmaxf(M, lp[p]);
+  float acc[EPL] = {};
+  float wsum = 0.0f;
+#pragma unroll
+  for (int p = 0; p < kMaxKeySplit; ++p) {
+    if (lp[p] == -INFINITY) continue;
+    const float w = expf(lp[p] - M);
+    wsum += w;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = fmaf(w, x[p][e], acc[e]);
+  }
+  const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
+  const int64_t o = row * d_io + lane * EPL;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    const float y = acc[e] * inv;
+    if (out_dtype == SL8_F32) static_cast<float*>(out)[o + e] = y;
+    else if (out_dtype == SL8_BF16) static_cast<__nv_bfloat16*>(out)[o + e] = __float2bfloat16_rn(y);
+    else static_cast<__half*>(out)[o + e] = __float2half_rn(y);
+  }
+  if (lse && lane == 0) lse[row] = wsum > 0.0f ? M + logf(wsum) : -INFINITY;
+}
+
+cudaError_t launch_prefill_combine(const float* o_part, const float* lse_part, int64_t rows, int32_t d_io,
+                                   int32_t kv_split, void* out, sl8_dtype out_dtype, float* lse, cudaStream_t s) {
+  TraceScope tr("prefill_combine", s);
+  if (rows <= 0) return cudaSuccess;
+  if (kv_split > kMaxKeySplit) return cudaErrorInvalidValue;
+  const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
+  switch (d_io) {
+    case 32: prefill_combine_kernel<1><<<grid, 256, 0, s>>>(o_part, lse_part, rows, d_io, kv_split, out, out_dtype, lse); break;
+    case 64: prefill_combine_kernel<2><<<grid, 256, 0, s>>>(o_part, lse_part, rows, d_io, kv_split, out, out_dtype, lse); break;
+    case 128: prefill_combine_kernel<4><<<grid, 256, 0, s>>>(o_part, lse_part, rows, d_io, kv_split, out, out_dtype, lse); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
 bool prefill_head_pairs(int d, int group) { return d <= 128 && group % 2 == 0; }
 int prefill_item_rows(int d, int group) { return d <= 128 && !prefill_head_pairs(d, group) ? 2 * kQTile : kQTile; }
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   const bool logits = a.logits != nullptr;
   switch (a.d) {
-    case 64: return logits ? launch_pair<64, true>(a, s) : launch_pair<64, false>(a, s);
-    case 128: return logits ? launch_pair<128, true>(a, s) : launch_pair<128, false>(a, s);
+    // key splits (query chunks only) have an instantiation of their own, so that the
+    // unsplit kernel compiles without the split bookkeeping
+    case 64: return logits ? launch_pair<64, true>(a, s)
+                           : (a.kv_split > 1 ? launch_pair<64, false, true>(a, s) : launch_pair<64, false>(a, s));
+    case 128: return logits ? launch_pair<128, true>(a, s)
+                            : (a.kv_split > 1 ? launch_pair<128, false, true>(a, s) : launch_pair<128, false>(a, s));
     case 256: return logits ? launch_single<256, true>(a, s) : launch_single<256, false>(a, s);
     default: return cudaErrorInvalidValue;
   }

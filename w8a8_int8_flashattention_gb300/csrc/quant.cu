@@ -14,6 +14,7 @@
 // order, then divides by the token count.  This file is built without fast-math
 // and spells every rounding step as an explicit _rn intrinsic.
 #include <atomic>
+#include <cstring>
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -537,7 +538,8 @@ cudaError_t launch_kv_stats(const void* k, sl8_dtype dt, const void* v, bool var
 
 // ---------------------------------------------------------------- prefill K/V partials
 // One CTA per (64-token chunk, kv head, sequence): the chunk's K rows (and V rows when
-// v_partials is set) are staged in shared memory with bulk copies; then thread c < d sums
+// v_partials is set) are staged in shared memory (dense: one bulk copy per tensor; varlen:
+// one tiled copy per tensor of the chunk's rows of head h); then thread c < d sums
 // channel c of K in token order into k_partials, while the second half of the CTA (with
 // V) takes max |V| of the chunk into v_partials.  Dense input (len == nullptr): every
 // sequence is N long.  kv_finalize_kernel forms the mean and the V exponent from these.
@@ -547,8 +549,9 @@ template <sl8_dtype DT>
 __global__ void kv_partials_kernel(const void* __restrict__ k, const void* __restrict__ v, bool varlen, int32_t Hkv,
                                    int32_t N, int32_t d, const int32_t* __restrict__ len,
                                    const int32_t* __restrict__ tok0, float* __restrict__ k_partials,
-                                   float* __restrict__ v_partials, int32_t max_chunks, uint64_t limit_ns,
-                                   DeviceStatus* st) {
+                                   float* __restrict__ v_partials, int32_t max_chunks,
+                                   const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                                   uint64_t limit_ns, DeviceStatus* st) {
   extern __shared__ __align__(128) uint8_t stage[];
   __shared__ uint64_t bar;
   __shared__ float s_max[32];
@@ -564,7 +567,8 @@ __global__ void kv_partials_kernel(const void* __restrict__ k, const void* __res
   if (t0 >= L) return;
   const int n = min(kMeanChunk, L - t0);
   const int32_t base = varlen ? tok0[s] : 0;
-  const uint32_t row_bytes = static_cast<uint32_t>(d) * ES;
+  const uint32_t row_bytes = static_cast<uint32_t>(d) * ES;  // K rows; V rows are bf16
+  const uint32_t v_row_bytes = static_cast<uint32_t>(d) * 2;
   uint8_t* sk = stage;
   uint8_t* sv = stage + kMeanChunk * row_bytes;
   if (threadIdx.x == 0) {
@@ -572,23 +576,20 @@ __global__ void kv_partials_kernel(const void* __restrict__ k, const void* __res
     fence_barrier_init();
   }
   __syncthreads();
-  if (threadIdx.x < 32) {
-    const int l = threadIdx.x;
-    const uint32_t tx = static_cast<uint32_t>(n) * row_bytes * ((k_partials ? 1u : 0u) + (v_partials ? 1u : 0u));
-    if (l == 0) mbar_arrive_expect_tx(&bar, tx);
-    __syncwarp();
-    if (!varlen) {  // the chunk's rows are contiguous
-      if (l == 0) {
-        const int64_t e0 = row_offset(false, s, h, t0, Hkv, N, d, 0);
-        if (k_partials) bulk_load(sk, static_cast<const uint8_t*>(k) + e0 * ES, n * row_bytes, &bar);
-        if (v_partials) bulk_load(sv, static_cast<const uint8_t*>(v) + e0 * 2, n * row_bytes, &bar);
-      }
+  if (threadIdx.x == 0) {
+    // dense: the chunk's rows are contiguous (one bulk copy); varlen: one tiled copy of the
+    // chunk's 64 token rows of head h (rows past the sequence are read and ignored, rows
+    // past the tensors zero-filled)
+    const uint32_t rows = varlen ? static_cast<uint32_t>(kMeanChunk) : static_cast<uint32_t>(n);
+    const uint32_t tx = rows * ((k_partials ? row_bytes : 0u) + (v_partials ? v_row_bytes : 0u));
+    mbar_arrive_expect_tx(&bar, tx);
+    if (!varlen) {
+      const int64_t e0 = row_offset(false, s, h, t0, Hkv, N, d, 0);
+      if (k_partials) bulk_load(sk, static_cast<const uint8_t*>(k) + e0 * ES, n * row_bytes, &bar);
+      if (v_partials) bulk_load(sv, static_cast<const uint8_t*>(v) + e0 * 2, n * v_row_bytes, &bar);
     } else {
-      for (int i = l; i < n; i += 32) {
-        const int64_t e = row_offset(true, s, h, t0 + i, Hkv, N, d, base);
-        if (k_partials) bulk_load(sk + i * row_bytes, static_cast<const uint8_t*>(k) + e * ES, row_bytes, &bar);
-        if (v_partials) bulk_load(sv + i * row_bytes, static_cast<const uint8_t*>(v) + e * 2, row_bytes, &bar);
-      }
+      if (k_partials) tma_load_3d(sk, &map_k, &bar, 0, h, base + t0);
+      if (v_partials) tma_load_3d(sv, &map_v, &bar, 0, h, base + t0);
     }
   }
   const bool ok = mbar_wait(&bar, 0, limit_ns, st, 903);
@@ -620,7 +621,7 @@ __global__ void kv_partials_kernel(const void* __restrict__ k, const void* __res
     float m = 0.0f;
     if (ok && c < d)
       for (int i = 0; i < n; ++i)
-        m = fmaxf(m, fabsf(bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(sv + i * row_bytes + c * 2))));
+        m = fmaxf(m, fabsf(bf16_bits_to_float(*reinterpret_cast<const uint16_t*>(sv + i * v_row_bytes + c * 2))));
     m = warp_max(m);
     if ((c & 31) == 0) s_max[c / 32] = m;
     named_bar_sync(1, half);
@@ -633,17 +634,30 @@ __global__ void kv_partials_kernel(const void* __restrict__ k, const void* __res
 
 cudaError_t launch_kv_partials(const void* k, sl8_dtype dt, const void* v, bool varlen, int32_t nseq, int32_t Hkv,
                                int32_t N, int32_t d, const int32_t* len, const int32_t* tok0, float* k_partials,
-                               float* v_partials, int32_t max_chunks, cudaStream_t s) {
+                               float* v_partials, int32_t max_chunks, int64_t total_tokens, cudaStream_t s) {
   TraceScope tr("kv_partials", s);
   const int es = dt == SL8_F32 ? 4 : 2;
   const size_t smem = static_cast<size_t>(kMeanChunk) * d * es * (v_partials ? 2 : 1);
   const int half = (d + 31) / 32 * 32;
   const dim3 grid(max_chunks, Hkv, nseq), block(v_partials ? 2 * half : half);
+  CUtensorMap mk, mv;
+  memset(&mk, 0, sizeof(mk));
+  memset(&mv, 0, sizeof(mv));
+  if (varlen) {  // [T][Hkv][d]: 64 token rows of one head per copy
+    bool ok = true;
+    const uint64_t T = static_cast<uint64_t>(total_tokens), dd = static_cast<uint64_t>(d);
+    const CUtensorMapDataType et = es == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+    if (k_partials) mk = make_tmap_3d(k, et, dd, Hkv, T, dd * es, dd * es * Hkv, d, 1, kMeanChunk, &ok, false);
+    if (v_partials)
+      mv = make_tmap_3d(v, CU_TENSOR_MAP_DATA_TYPE_UINT16, dd, Hkv, T, dd * 2, dd * 2 * Hkv, d, 1, kMeanChunk, &ok,
+                        false);
+    if (!ok) return cudaErrorInvalidValue;
+  }
   auto go = [&](auto kern) {
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, grid, block, smem, s, k, v, varlen, Hkv, N, d, len, tok0, k_partials, v_partials,
-                      max_chunks, spin_limit_ns(), device_status_ptr());
+                      max_chunks, mk, mv, spin_limit_ns(), device_status_ptr());
   };
   switch (dt) {
     case SL8_BF16: return go(kv_partials_kernel<SL8_BF16>);
@@ -781,8 +795,9 @@ struct QpCfg {
 
 template <sl8_dtype DT, int D, bool kGroups>
 __global__ void __launch_bounds__(QpCfg<D>::kThreads, QpCfg<D>::kCtasPerSm)
-    quant_qk_pipe_kernel(const QuantQK a, const float* __restrict__ k_mean, uint32_t ticket, DeviceStatus* st,
-                         uint64_t limit_ns) {
+    quant_qk_pipe_kernel(const QuantQK a, const float* __restrict__ k_mean, const __grid_constant__ CUtensorMap map_q,
+                         const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                         uint32_t ticket, DeviceStatus* st, uint64_t limit_ns) {
   using C = QpCfg<D>;
   constexpr int LPR = 8, NV = D / 64, RPP = 32 / LPR, P = kQpRows / kQpConsumers / RPP;
   extern __shared__ __align__(128) uint8_t qp_smem[];
@@ -887,9 +902,13 @@ __global__ void __launch_bounds__(QpCfg<D>::kThreads, QpCfg<D>::kCtasPerSm)
       uint8_t* sv = sx + C::kUnitBytes;
       const int H = x.is_k ? a.Hkv : a.Hq;
       const void* src = x.is_k ? a.k : a.q;
+      // varlen rows are one tiled copy of the unit's 64 token rows (rows past the sequence
+      // are read and ignored; past the tensors they are zero-filled), dense rows one bulk
+      // copy of the rows with input
+      const uint32_t rows_copied = n > 0 ? static_cast<uint32_t>(a.varlen ? kQpRows : n) : 0u;
       if (lane == 0) {
         *reinterpret_cast<QpUnit*>(sx + C::kInfoOff) = x;
-        const uint32_t bytes = static_cast<uint32_t>(n) * row_bytes * (with_v ? 2u : 1u) +
+        const uint32_t bytes = rows_copied * row_bytes * (with_v ? 2u : 1u) +
                                (smooth ? static_cast<uint32_t>(a.d_io) * 4u : 0u);
         if (bytes) mbar_arrive_expect_tx(&full[stg], bytes); else mbar_arrive(&full[stg]);
         if (smooth) bulk_load(sx + C::kMeanOff, k_mean + srow * a.d_io, a.d_io * 4, &full[stg]);
@@ -905,13 +924,9 @@ __global__ void __launch_bounds__(QpCfg<D>::kThreads, QpCfg<D>::kCtasPerSm)
               bulk_load(sv + (ta - x.t0) * row_bytes, static_cast<const uint16_t*>(a.v) + e0, n * row_bytes,
                         &full[stg]);
           }
-        } else {
-          for (int t = ta + lane; t < tb; t += 32) {
-            const int64_t e = row_offset(true, x.s, x.h, t, H, a.N, a.d_io, x.tk);
-            bulk_load(sx + (t - x.t0) * row_bytes, static_cast<const uint16_t*>(src) + e, row_bytes, &full[stg]);
-            if (with_v)
-              bulk_load(sv + (t - x.t0) * row_bytes, static_cast<const uint16_t*>(a.v) + e, row_bytes, &full[stg]);
-          }
+        } else if (lane == 0) {
+          tma_load_3d(sx, x.is_k ? &map_k : &map_q, &full[stg], 0, x.h, x.tk + x.t0);
+          if (with_v) tma_load_3d(sv, &map_v, &full[stg], 0, x.h, x.tk + x.t0);
         }
       }
       if (++stg == C::kStages) {
@@ -1123,10 +1138,27 @@ static cudaError_t launch_quant_pipe(const QuantQK& a, const float* k_mean, cuda
   const int64_t slots = static_cast<int64_t>(num_sms()) * C::kCtasPerSm;
   const int grid = static_cast<int>(units < slots ? units : slots);
   if (grid <= 0) return cudaSuccess;
+  // varlen input: each unit's 64 token rows of one head as a tiled copy of [T][H][d_io]
+  CUtensorMap mq, mk, mv;
+  memset(&mq, 0, sizeof(mq));
+  memset(&mk, 0, sizeof(mk));
+  memset(&mv, 0, sizeof(mv));
+  if (a.varlen) {
+    bool ok = true;
+    const uint64_t T = static_cast<uint64_t>(a.total_tokens), dio = static_cast<uint64_t>(a.d_io);
+    mq = make_tmap_3d(a.q, CU_TENSOR_MAP_DATA_TYPE_UINT16, dio, a.Hq, T, dio * 2, dio * 2 * a.Hq, a.d_io, 1, kQpRows,
+                      &ok, false);
+    mk = make_tmap_3d(a.k, CU_TENSOR_MAP_DATA_TYPE_UINT16, dio, a.Hkv, T, dio * 2, dio * 2 * a.Hkv, a.d_io, 1,
+                      kQpRows, &ok, false);
+    if (a.v16)
+      mv = make_tmap_3d(a.v, CU_TENSOR_MAP_DATA_TYPE_UINT16, dio, a.Hkv, T, dio * 2, dio * 2 * a.Hkv, a.d_io, 1,
+                        kQpRows, &ok, false);
+    if (!ok) return cudaErrorInvalidValue;
+  }
   static std::atomic<uint32_t> next_ticket{0};
   const uint32_t ticket = next_ticket.fetch_add(1, std::memory_order_relaxed) % kQpTickets;
-  return launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmem, s, a, k_mean, ticket, device_status_ptr(),
-                    spin_limit_ns());
+  return launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmem, s, a, k_mean, mq, mk, mv, ticket,
+                    device_status_ptr(), spin_limit_ns());
 }
 
 template <sl8_dtype DT, bool kGroups>

@@ -13,6 +13,7 @@ namespace sl8 {
 constexpr int kQTile = 128;      // query rows per prefill work item (MMA M)
 constexpr int kPadRows = 128;    // each sequence starts at a multiple of this in the code workspace
 constexpr int kMeanChunk = 64;   // K-smoothing summation chunk (tokens)
+constexpr int kMaxKeySplit = 8;  // key-split parts of a query chunk, merged by prefill_combine
 
 // Per-sequence table and work list written by the scheduler kernel into the
 // prefill workspace.  All arrays are int32.
@@ -99,10 +100,10 @@ cudaError_t launch_kv_stats(const void* k, sl8_dtype dt, const void* v, bool var
                             float* v_partials, int32_t max_chunks, float* mean, int32_t* v_exp, int32_t* kv_done,
                             cudaStream_t s);
 // Prefill K chunk sums and V chunk abs-max (v_partials nullable), rows staged in shared
-// memory; len / tok0 nullable for dense input.
+// memory; len / tok0 nullable for dense input; total_tokens: rows of a varlen K / V.
 cudaError_t launch_kv_partials(const void* k, sl8_dtype dt, const void* v, bool varlen, int32_t nseq, int32_t Hkv,
                                int32_t N, int32_t d, const int32_t* len, const int32_t* tok0, float* k_partials,
-                               float* v_partials, int32_t max_chunks, cudaStream_t s);
+                               float* v_partials, int32_t max_chunks, int64_t total_tokens, cudaStream_t s);
 // From the chunk results of launch_kv_partials (either nullable): the K mean
 // [nseq][Hkv][d_io] and the V exponent [nseq][Hkv] (0 without v_partials); one CTA per
 // (sequence, kv head); len nullable for dense input (every sequence N long).
@@ -112,11 +113,12 @@ cudaError_t launch_kv_finalize(bool varlen, int32_t nseq, int32_t Hkv, int32_t N
 // Q and K rows of prefill in one launch.  With k_partials or v_partials set, the chunk
 // kernels and launch_kv_finalize ran just before: K rows are smoothed with k_mean (set
 // iff k_partials is) and, with v16 set, V is written as fp16 * 2^-v_exp with the exponent
-// kv_finalize left in v_exp; otherwise the exponent is 0 and is written to v_exp here.  t is read for varlen input only.  q_off > 0 (dense): q holds
-// N - q_off rows per (sequence, head), the positions q_off .. N-1; the code rows of the
-// positions before it are zero.  d_io < d (head dim 32 run as 64): the inputs hold d_io
-// values per row and the code rows are zero past them; k_partials then has d_io columns;
-// v_f16: V is fp16 (copied, v_partials unused and the exponent 0), else bf16.
+// kv_finalize left in v_exp; otherwise the exponent is 0 and is written to v_exp here.
+// t is read for varlen input only.  q_off > 0 (dense): q holds N - q_off rows per
+// (sequence, head), the positions q_off .. N-1; the code rows of the positions before it
+// are zero.  d_io < d (head dim 32 run as 64): the inputs hold d_io values per row and the
+// code rows are zero past them; k_partials then has d_io columns; v_f16: V is fp16
+// (copied, v_partials unused and the exponent 0), else bf16.
 // Grouped scales for attn_w8a8_fwd (all 1 / 0: per-row scales, the attn_int8_fwd path).
 struct QuantGroups {
   int32_t q_group = 1, k_group = 1;  // rows per shared scale, powers of two <= 64
@@ -162,8 +164,20 @@ struct PrefillArgs {
   float* lse;               // nullable
   int32_t* logits;          // debug mode: [nseq][Hq][row_end-row_begin][N] int32 (dense only)
   int32_t row_begin, row_end;
+  // key splits (dense query chunks, d <= 128): each item's key tiles are cut into kv_split
+  // contiguous parts run as separate items; a part writes its normalised O (fp32) and its
+  // log-sum-exp (natural log, -inf for a part with no key) for the chunk's output rows
+  // r = (s * Hq + hq) * (N - q_off) + position - q_off to o_part [kv_split][rows][d_io] and
+  // lse_part [kv_split][rows], which launch_prefill_combine merges.  1: no split.
+  int32_t kv_split;
+  float* o_part;
+  float* lse_part;
 };
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
+// Merge the kv_split partials of `rows` output rows (layout as PrefillArgs::o_part) into
+// out [rows][d_io] of out_dtype and lse (nullable, fp32 natural log).
+cudaError_t launch_prefill_combine(const float* o_part, const float* lse_part, int64_t rows, int32_t d_io,
+                                   int32_t kv_split, void* out, sl8_dtype out_dtype, float* lse, cudaStream_t s);
 
 struct DecodeArgs {
   const void* q;
