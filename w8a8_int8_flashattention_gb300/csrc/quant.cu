@@ -711,8 +711,12 @@ __global__ void __launch_bounds__(128) kv_finalize_kernel(bool varlen, int32_t H
                                                           const float* __restrict__ v_partials, int32_t max_chunks,
                                                           float* __restrict__ mean, int32_t* __restrict__ v_exp) {
   __shared__ float s_max[4];
-  grid_dependency_wait();
+  // Let the quantiser launch at once, so that its Q blocks run alongside the chunk kernel.
+  // That is safe: this kernel starts only after the chunk kernel has passed its own wait,
+  // i.e. after every earlier kernel (the previous attention reading the code workspace)
+  // completed; and the quantiser waits for this kernel before it reads the mean.
   grid_dependents_launch();
+  grid_dependency_wait();
   const int h = blockIdx.x, s = blockIdx.y, tid = threadIdx.x;
   const int L = varlen ? len[s] : N;
   const int nch = (L + kMeanChunk - 1) / kMeanChunk;
