@@ -10,15 +10,16 @@ One step = one pass of the whole path over one batch of synthetic input:
 the decode KV GB/s sits in `decode`, and `paged_decode` repeats the decode over a
 paged k8v8 cache (64-token pages in a seeded random order) in a loop of its own after
 the timed steps, `decode_f16v` the decode with an fp16 V cache (int8 K), and
-`prefill_chunk` the prefill's last 1024 positions as a query chunk (chunked prefill,
-bottom-right causal), `prefill_w8a8` the prefill through attn_w8a8_fwd (scales per 32
-positions, outlier-aware Q), and `decode_verify` the decode with 4 chained draft
-queries per sequence (speculative verify).  Inputs are resident in HBM when the timed
-region starts (the timed steps carry no per-launch instrumentation: per-kernel times
-come from a separate traced pass); L2 is flushed before every step, outside the timed
-events (a 256 MB
-write, then a read of that buffer, so no dirty lines of the flush remain).  `e2e` repeats the prefill through the public API with pinned host
-inputs copied in and the output copied back every step.
+`prefill_chunk` / `prefill_chunk_small` the prefill's last 1024 / 128 positions as a
+query chunk (chunked prefill, bottom-right causal), `prefill_w8a8` the prefill through
+attn_w8a8_fwd (scales per 32 positions, outlier-aware Q), and `decode_verify` the
+decode with 4 chained draft queries per sequence (speculative verify).  Inputs are
+resident in HBM when the timed region starts (the timed steps carry no per-launch
+instrumentation: per-kernel times come from a separate traced pass).  L2 is flushed
+before the prefill and again before the decode of every step, outside the timed events
+(a 256 MB write, then a read of that buffer, so no dirty lines of the flush or of the
+prefill's outputs remain).  `e2e` repeats the prefill through the public API with
+pinned host inputs copied in and the output copied back every step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -384,12 +385,15 @@ def run_ours(args, world, rank, local):
                               "frac": dbytes / (pg_split_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}), flush=True)
         return
 
-    def step(ev=None):
-        # L2 flush outside the timed events: write a buffer twice the size of L2, then
-        # read it, so that the step starts with none of its inputs in L2 and no dirty
-        # lines left behind by the flush itself
+    def l2_flush():
+        # outside the timed events: write a buffer twice the size of L2, then read it, so
+        # that what follows starts with none of its inputs in L2 and no dirty lines (the
+        # flush's own, or those the prefill's outputs left) to write back
         flush.zero_()
         flush_sink.copy_(flush.view(torch.int64).sum())
+
+    def step(ev=None):
+        l2_flush()
         if ev:
             ev[0].record(stream)
         if args.only == "w8a8":
@@ -400,15 +404,20 @@ def run_ours(args, world, rank, local):
         if ev:
             ev[1].record(stream)
         if args.only not in ("prefill", "w8a8"):
+            l2_flush()
+            if ev:
+                ev[2].record(stream)
             sl8.attn_int8_decode(qdec, kc, ks, vc, vs, seq, o_partial=o_part, lse_partial=l_part, out=dout)
-        if ev:
+        elif ev:
             ev[2].record(stream)
+        if ev:
+            ev[3].record(stream)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     sl8.trace_enable(False)
     barrier(world)
     torch.cuda.synchronize(dev)
@@ -438,7 +447,7 @@ def run_ours(args, world, rank, local):
     trace = sl8.trace_collect()
 
     pre_ms = sum(e[0].elapsed_time(e[1]) for e in events) / args.steps
-    dec_ms = sum(e[1].elapsed_time(e[2]) for e in events) / args.steps
+    dec_ms = sum(e[2].elapsed_time(e[3]) for e in events) / args.steps
     pre_ms = max_over_ranks(pre_ms, world)
     dec_ms = max_over_ranks(dec_ms, world)
     ops = prefill_ops(wp)
@@ -513,7 +522,8 @@ def run_ours(args, world, rank, local):
         "config": {"workload": WORKLOAD_DESC,
                    "prefill_ms": pre_ms, "decode_ms": dec_ms, "prefill_gops": ops / 1e9,
                    "decode_bytes": dbytes, "decode_splits": S,
-                   "l2": "flushed before every step (256 MB write, then a read of it, outside the timed events)"},
+                   "l2": "flushed before the prefill and again before the decode of every step (256 MB write, then a "
+                         "read of it, outside the timed events)"},
         "tokens_per_s": {"prefill": wp.B * wp.N * world / (pre_ms * 1e-3),
                          "decode": wd.B * world / (dec_ms * 1e-3),
                          "note": "prefill: query tokens per second; decode: sequences advanced by one token per "
