@@ -504,42 +504,25 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
       }
       return true;
     };
-    // paged cache: the block-table entry of this lane's unit in the stage of slot x that
-    // starts at token c0 (0 when the lane has no unit there)
     const bool paged = !kV16 && a.block_table != nullptr;
-    auto page_of = [&](const Slot& x, int c0) {
-      const int t = c0 + lane * kUnit;
-      return paged && x.b >= 0 && t < x.t1 ? a.block_table[static_cast<int64_t>(x.b) * a.max_blocks + t / a.page_size]
-                                          : 0;
-    };
-    // and an L2 prefetch of the entries a slot will read, issued a slot ahead
-    auto prefetch_pages = [&](const Slot& x) {
-      if (!paged || x.b < 0) return;
-      const int p0 = x.t0 / a.page_size, p1 = (x.t1 - 1) / a.page_size;
-      const int32_t* row = a.block_table + static_cast<int64_t>(x.b) * a.max_blocks;
-      for (int e = (p0 & ~7) + 8 * lane; e <= p1; e += 8 * 32) prefetch_l2(row + (e < p0 ? p0 : e));
-    };
     Slot cur, nxt;
     bool has_cur = next_entry(cur);
     ok = ok && announce(cur, 0);
-    // the page of this lane's unit in the next stage to issue, loaded one stage early
-    int pg_ahead = has_cur ? page_of(cur, cur.t0) : 0;
     while (ok && has_cur) {
       const bool has_nxt = next_entry(nxt);
       if (!ok || !announce(nxt, n + 1)) break;
-      prefetch_pages(nxt);
       const int64_t row0 = (static_cast<int64_t>(cache_seq(a, cur.b)) * (a.Hkv / a.kv_groups) + cur.hkv / a.kv_groups) *
                            a.Lmax;
       for (int c0 = cur.t0; c0 < cur.t1 && ok; c0 += C::kChunk, ++k) {
         const int nt = min(C::kChunk, cur.t1 - c0);
         const uint32_t stg = k % kStages;
         uint8_t* base = smem + stg * C::kStageBytes;
-        // paged cache: the page of this lane's unit (loaded during the previous stage), and
-        // the load of the next stage's, whose latency this stage's wait and issue cover
+        // paged cache: the page of this lane's unit, read before the wait for the stage
+        // so that the wait covers the load's latency
         const int t = c0 + lane * kUnit;
         const int units = (nt + kUnit - 1) / kUnit;
-        int pg = pg_ahead;
-        if (paged) pg_ahead = c0 + C::kChunk < cur.t1 ? page_of(cur, c0 + C::kChunk) : has_nxt ? page_of(nxt, nxt.t0) : 0;
+        int pg = 0;
+        if (paged && lane < units) pg = a.block_table[static_cast<int64_t>(cur.b) * a.max_blocks + t / a.page_size];
         if (k >= kStages) ok = warp_wait(&empty[stg], ((k / kStages) - 1) & 1, limit_ns, st, 41);
         if (!ok) break;
         if (paged) {

@@ -130,10 +130,6 @@ __device__ __forceinline__ float rcp_approx(float x) {
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
-// Bring the line holding a global address into L2 (a hint: no data returns).
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
 
 // ------------------------------------------------------------------ tcgen05
 // Shared-memory matrix descriptor, 128-byte swizzle.  Start address, leading and
