@@ -475,12 +475,16 @@ __device__ __forceinline__ void store_row(uint32_t o_taddr, const PrefillArgs& a
 
 // Issue the D/16 MMAs of S = Q . K^T (M = 128, N = BN) into TMEM column d_col.
 template <int D, int BN>
+// The descriptors of a tile's K-steps differ only in the start-address field, which holds
+// address / 16 and cannot overflow its 14 bits for a shared-memory address: each is the
+// first one plus a constant, so the issuing warp spends one add per descriptor.
 __device__ __forceinline__ void issue_qk(uint32_t d_col, uint32_t qaddr, uint32_t kaddr) {
   constexpr uint32_t idesc = idesc_f16(kQTile, BN, true, false, false);
+  const uint64_t da0 = desc_sw128(qaddr, 16, 1024), db0 = desc_sw128(kaddr, 16, 1024);
 #pragma unroll
   for (int k = 0; k < D / 16; ++k) {
-    const uint64_t da = desc_sw128(qaddr + (k / 4) * (kQTile * 128) + (k % 4) * 32, 16, 1024);
-    const uint64_t db = desc_sw128(kaddr + (k / 4) * (BN * 128) + (k % 4) * 32, 16, 1024);
+    const uint64_t da = da0 + static_cast<uint64_t>(((k / 4) * (kQTile * 128) + (k % 4) * 32) >> 4);
+    const uint64_t db = db0 + static_cast<uint64_t>(((k / 4) * (BN * 128) + (k % 4) * 32) >> 4);
     mma_ss(d_col, da, db, idesc, k > 0 ? 1u : 0u);
   }
 }
@@ -489,11 +493,10 @@ __device__ __forceinline__ void issue_qk(uint32_t d_col, uint32_t qaddr, uint32_
 template <int D, int BN>
 __device__ __forceinline__ void issue_pv(uint32_t o_col, uint32_t p_col, uint32_t vaddr, bool accumulate) {
   constexpr uint32_t idesc = idesc_f16(kQTile, D, false, false, true);  // fp16 P x fp16 V (MN-major)
+  const uint64_t db0 = desc_sw128(vaddr, BN * 128, 1024);
 #pragma unroll
-  for (int k = 0; k < BN / 16; ++k) {
-    const uint64_t db = desc_sw128(vaddr + k * 2048, BN * 128, 1024);
-    mma_ts(o_col, p_col + k * 8, db, idesc, (accumulate || k > 0) ? 1u : 0u);
-  }
+  for (int k = 0; k < BN / 16; ++k)
+    mma_ts(o_col, p_col + k * 8, db0 + static_cast<uint64_t>(k * (2048 >> 4)), idesc, (accumulate || k > 0) ? 1u : 0u);
 }
 
 __device__ __forceinline__ void load_q_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int boxes, int row,
