@@ -5,8 +5,8 @@
  *   - "Supporting kernels" table, quant_rowwise: symmetric per-row int8 quantisation;
  *   - "Quantization" table, "Per-row int8": symmetric, with K-smoothing;
  *   - "Attention kernels" table, attn_int8_fwd: W8A8 FlashAttention-2 forward,
- *     causal, GQA/MQA, head dims 32/64/128/256 (this library: prefill all four, decode
- *     64, 128, 256);
+ *     causal, GQA/MQA, head dims 32/64/128/256 (this library: prefill and the int8-V
+ *     decode all four, the fp16-V decode 64 and 128);
  *     attn_varlen_fwd: ragged variable-length prefill; attn_decode: split-KV decode
  *     with an int8 KV cache, int8-V variant;
  *   - "Quick start" section: q [B, Hq, N, d], k/v [B, Hkv, N, d],
@@ -53,7 +53,7 @@ extern "C" {
 typedef enum sl8_status {
   SL8_OK = 0,
   SL8_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad shape or dtype, Hq % Hkv != 0 */
-  SL8_ERR_UNSUPPORTED = 2, /* valid but not implemented here (e.g. d = 32 in decode) */
+  SL8_ERR_UNSUPPORTED = 2, /* valid but not implemented here (e.g. the fp16-V decode at d = 256) */
   SL8_ERR_WORKSPACE = 3,   /* workspace missing or smaller than the size query returned */
   SL8_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
   SL8_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up (see sl8_last_device_status) */
@@ -123,7 +123,7 @@ SL8_API int sl8_k_channel_mean(const void* k, int k_dtype, int32_t B, int32_t Hk
  *               dense [B][Hq][N], varlen [total_tokens][Hq].
  *   workspace   device scratch of at least sl8_attn_int8_fwd_workspace_size() bytes
  *               (the quantised codes, scales, K means and the work list live there).
- * Errors: SL8_ERR_INVALID_ARG, SL8_ERR_UNSUPPORTED (d not in {64,128,256}),
+ * Errors: SL8_ERR_INVALID_ARG, SL8_ERR_UNSUPPORTED (d not in {32,64,128,256}),
  * SL8_ERR_WORKSPACE, SL8_ERR_CUDA.  Empty inputs (B, N or total_tokens 0) return
  * SL8_OK without launching.
  */
@@ -225,6 +225,7 @@ SL8_API int sl8_attn_w8a8_qk_logits_debug(const void* q, const void* k, int qk_d
 /*
  * Split-KV decode over an int8 KV cache ("Attention kernels" table, attn_decode,
  * int8-V variant): one query token per sequence against its cached keys t < L_b.
+ * d is 32, 64, 128 or 256.
  *   q                  device, [B][Hq][d] of q_dtype (F16, BF16 or F32); quantised
  *                      per row inside the kernel.
  *   k_cache, v_cache   device, [B][Hkv][Lmax][d] int8 codes.
@@ -302,7 +303,7 @@ SL8_API int sl8_attn_int8_decode_verify(const void* q, int q_dtype, const int8_t
  * as sl8_attn_int8_decode_splitkv, with O = sum_t p_t * v[t] (V has no scale):
  *   k_cache, k_scale  as there ([B][Hkv][Lmax][d] int8 codes, [B][Hkv][Lmax] fp32).
  *   v_cache           device, [B][Hkv][Lmax][d] fp16 (16-byte aligned).
- * d must be 64 or 128 (SL8_ERR_UNSUPPORTED for 256).  The partials are merged with
+ * d must be 64 or 128 (SL8_ERR_UNSUPPORTED for 32 and 256).  The partials are merged with
  * sl8_attn_decode_combine.
  */
 SL8_API int sl8_attn_int8_decode_splitkv_f16v(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale,

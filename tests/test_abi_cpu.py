@@ -67,7 +67,9 @@ def test_decode_split_plan(lib):
     assert lib.sl8_attn_decode_split_size(2, 2, 300, 128, 3) == 112
     assert lib.sl8_attn_decode_num_splits(64, 8, 8192, 128, 1) == 1
     assert lib.sl8_attn_decode_num_splits(1, 1, 10, 128, 64) == 1       # one 16-token split
-    assert lib.sl8_attn_decode_num_splits(64, 8, 100, 32, 0) == 0       # unsupported head dim
+    assert lib.sl8_attn_decode_num_splits(64, 8, 100, 96, 0) == 0       # unsupported head dim
+    # head dim 32: the same 160-token stages
+    assert lib.sl8_attn_decode_split_size(64, 8, 8192, 32, 5) == 1760
     assert lib.sl8_attn_decode_num_splits(0, 8, 100, 128, 0) == 0
     # every plan: 16-token aligned splits (whole stages from one stage up), all non-empty
     # at Lmax, covering Lmax, and the combine's split size (from Lmax and S alone) is the

@@ -61,6 +61,9 @@ CASES = [
     (3005, 3, 32, 1, 128, [900, 1, 333], 900),          # G = 32: four groups of 8
     (3006, 2, 64, 4, 64, [700, 129], 700),               # G = 16: two groups of 8
     (3007, 2, 12, 1, 256, [300, 17], 300),               # G = 12: two groups of 6
+    # head dim 32 (32-byte cache rows)
+    (3008, 4, 8, 2, 32, [1, 300, 0, 161], 320),
+    (3009, 2, 16, 1, 32, [500, 33], 500),                # G = 16 at d = 32
 ]
 
 
@@ -158,6 +161,7 @@ PAGED = [
     (3204, 4, 16, 2, 128, [2000, 77, 160, 161], 256, 8, 0),
     (3205, 4, 8, 2, 128, [900, 640, 1000, 700], 128, 8, 5),
     (3206, 3, 32, 2, 128, [700, 33, 1000], 64, 16, 0),   # G = 16 over a paged cache
+    (3207, 3, 8, 2, 32, [100, 17, 640], 32, 20, 0),      # d = 32 over a paged cache
 ]
 
 
@@ -269,11 +273,12 @@ def test_decode_f16v(case):
     assert st == sl8.SL8_OK, (st, site)
 
 
-def test_decode_f16v_rejects_d256():
-    q = torch.zeros((1, 2, 256), dtype=torch.bfloat16, device=DEV)
-    kc = torch.zeros((1, 1, 64, 256), dtype=torch.int8, device=DEV)
+@pytest.mark.parametrize("d", [32, 256])
+def test_decode_f16v_rejects_d32_d256(d):
+    q = torch.zeros((1, 2, d), dtype=torch.bfloat16, device=DEV)
+    kc = torch.zeros((1, 1, 64, d), dtype=torch.int8, device=DEV)
     ks = torch.ones((1, 1, 64), dtype=torch.float32, device=DEV)
-    v = torch.zeros((1, 1, 64, 256), dtype=torch.float16, device=DEV)
+    v = torch.zeros((1, 1, 64, d), dtype=torch.float16, device=DEV)
     seq = torch.tensor([10], dtype=torch.int32, device=DEV)
     with pytest.raises(sl8.SL8Error):
         sl8.attn_int8_decode_splitkv_f16v(q, kc, ks, v, seq)
@@ -287,6 +292,7 @@ VERIFY = [
     (3502, 2, 7, 4, 4, 64, [513, 160], 600),
     (3503, 2, 16, 8, 1, 256, [200, 2000], 2000),
     (3504, 4, 1, 8, 2, 128, [1, 17, 640, 641], 700),
+    (3505, 2, 4, 8, 2, 32, [300, 64], 400),
 ]
 
 

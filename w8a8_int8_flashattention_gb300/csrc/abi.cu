@@ -213,6 +213,8 @@ namespace {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool is_half(int dt) { return dt == SL8_F16 || dt == SL8_BF16; }
 bool head_dim_ok(int32_t d) { return d == 64 || d == 128 || d == 256; }
+// The decode kernels also take head dim 32 (int8 V only).
+static bool decode_head_dim_ok(int32_t d) { return d == 32 || head_dim_ok(d); }
 // Head dim the prefill kernels compute in: 32 runs as 64 (codes, V copy and O zero past 32).
 int32_t compute_dim(int32_t d) { return d == 32 ? 64 : d; }
 
@@ -626,7 +628,7 @@ static int32_t split_size_for(int32_t Lmax, int32_t S, int32_t d) {
 }
 
 int32_t sl8_attn_decode_num_splits(int32_t B, int32_t Hkv, int32_t Lmax, int32_t d, int32_t num_splits) {
-  if (B <= 0 || Hkv <= 0 || Lmax <= 0 || !head_dim_ok(d) || num_splits < 0) return 0;
+  if (B <= 0 || Hkv <= 0 || Lmax <= 0 || !decode_head_dim_ok(d) || num_splits < 0) return 0;
   int64_t n = num_splits;
   if (n == 0) {
     const int64_t pairs = static_cast<int64_t>(B) * Hkv;
@@ -682,12 +684,12 @@ static int decode_validate(const void* q, int q_dtype, const void* k_cache, cons
                            const float* v_scale, const int32_t* seqlens, int32_t B, int32_t Hq, int32_t Hkv,
                            int32_t Lmax, int32_t d, const Paging* pg, bool v16) {
   SL8_CHECK(q && k_cache && k_scale && v_cache && (v_scale || v16) && seqlens, SL8_ERR_INVALID_ARG);
-  SL8_CHECK(!v16 || (d <= 128 && !pg), SL8_ERR_UNSUPPORTED);
+  SL8_CHECK(!v16 || (d >= 64 && d <= 128 && !pg), SL8_ERR_UNSUPPORTED);
   SL8_CHECK(aligned16(q) && aligned16(k_cache) && aligned16(v_cache), SL8_ERR_INVALID_ARG);
   SL8_CHECK(q_dtype == SL8_F16 || q_dtype == SL8_BF16 || q_dtype == SL8_F32, SL8_ERR_INVALID_ARG);
   SL8_CHECK(B >= 0 && Hq > 0 && Hkv > 0 && Lmax >= 0 && d > 0, SL8_ERR_INVALID_ARG);
   SL8_CHECK(Hq % Hkv == 0, SL8_ERR_INVALID_ARG);
-  SL8_CHECK(head_dim_ok(d), SL8_ERR_UNSUPPORTED);
+  SL8_CHECK(decode_head_dim_ok(d), SL8_ERR_UNSUPPORTED);
   SL8_CHECK(B <= 65535 && static_cast<int64_t>(Hkv) * decode_kv_groups(Hq, Hkv) <= 65535, SL8_ERR_UNSUPPORTED);
   if (pg) {
     // pages are loaded in 16-token units (TMA rows, 64-byte scale pieces)
@@ -828,7 +830,7 @@ int sl8_attn_decode_combine(const float* o_partial, const float* lse_partial, co
   SL8_CHECK(o_partial && lse_partial && seqlens && out, SL8_ERR_INVALID_ARG);
   SL8_CHECK(out_dtype == SL8_F16 || out_dtype == SL8_BF16 || out_dtype == SL8_F32, SL8_ERR_INVALID_ARG);
   SL8_CHECK(B >= 0 && Hq > 0 && Lmax >= 0 && num_splits >= 1, SL8_ERR_INVALID_ARG);
-  SL8_CHECK(head_dim_ok(d), SL8_ERR_UNSUPPORTED);
+  SL8_CHECK(decode_head_dim_ok(d), SL8_ERR_UNSUPPORTED);
   if (B == 0) return SL8_OK;
   SL8_CHECK(num_splits <= (Lmax > 0 ? Lmax : 1), SL8_ERR_INVALID_ARG);
   const int32_t split_size = Lmax > 0 ? split_size_for(Lmax, num_splits, d) : 16;

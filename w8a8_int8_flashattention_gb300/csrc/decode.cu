@@ -91,7 +91,7 @@ struct DCfg {
   // V: int8 codes like K, or (kV16) fp16 values in 128-byte rows of 64 dims
   static constexpr int kTileV = kV16 ? 2 * kTile : kTile;
   static constexpr int kBoxesV = kV16 ? D / 64 : kBoxes;
-  static constexpr int kStages = kV16 ? (D == 64 ? 4 : 2) : (D == 64 ? 8 : (D == 128 ? 3 : 2));
+  static constexpr int kStages = kV16 ? (D == 64 ? 4 : 2) : (D <= 64 ? 8 : (D == 128 ? 3 : 2));
   static constexpr int kSK = 0;
   static constexpr int kSV = kTile;
   static constexpr int kSKs = kTile + kTileV;
@@ -108,7 +108,7 @@ struct DCfg {
   static constexpr int kNumBars = 2 * kStages + 4 * kQSlots + 3;
   static constexpr int kBytes = kBar + kNumBars * 8 + 1024;    // + alignment slack
   static_assert(kStageBytes % 1024 == 0 && kTile % 1024 == 0, "swizzled tiles need 1024-byte alignment");
-  static_assert(!kV16 || D <= 128, "fp16 V: d <= 128");
+  static_assert(!kV16 || (D >= 64 && D <= 128), "fp16 V: 64 <= d <= 128");
   static_assert(kBytes <= 232448, "smem budget");
 };
 
@@ -681,20 +681,29 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
   const int g = lane >> 2, t = lane & 3;
   const int u0 = kUnit * cw;  // this warp's rows in every stage
   // S^T row r (and r + 8) holds unit token tok(r) (and tok(r) + 8).  The permutation keeps
-  // the K reads (row tok(g), 16-byte chunk t) and the V reads (rows tok(2t), tok(2t + 1),
-  // + 8) free of bank conflicts, or at two ways for the 64-byte rows of d = 64.
+  // the K reads (row tok(g), 16-byte chunk t; 8-byte piece t at d = 32) and the V reads
+  // (rows tok(2t), tok(2t + 1), + 8) free of bank conflicts, or at two ways for the
+  // 64-byte rows of d = 64.
   auto tok = [](int r) {
-    return C::kSwz ? (r >> 1) + 4 * (r & 1) : ((r & 1) ? 4 + ((r >> 1) ^ 1) : (r >> 1));
+    if constexpr (C::kSwz) return (r >> 1) + 4 * (r & 1);
+    if constexpr (D == 32) return (r & 1) ? 4 + (((r >> 1) + 2) & 3) : (r >> 1);
+    return (r & 1) ? 4 + ((r >> 1) ^ 1) : (r >> 1);
   };
   const int pi = tok(g);
   // V^T rows of this lane: 16-byte chunk (8-byte piece for d = 64) pi of each V row
   const int cg = pi;
   // stage-tile offsets of this lane's reads, the same for every stage
-  uint32_t offk[D / 64][2];
+  constexpr int kKH = D >= 64 ? D / 64 : 1;  // 64-dim parts of a K row (d = 32: one 32-byte row)
+  uint32_t offk[kKH][2];
+  if constexpr (D == 32) {
+    offk[0][0] = static_cast<uint32_t>((u0 + pi) * 32 + 8 * t);
+    offk[0][1] = static_cast<uint32_t>((u0 + pi + 8) * 32 + 8 * t);
+  } else {
 #pragma unroll
-  for (int h = 0; h < D / 64; ++h) {
-    offk[h][0] = tile_off<D>(u0 + pi, 4 * h + t);
-    offk[h][1] = tile_off<D>(u0 + pi + 8, 4 * h + t);
+    for (int h = 0; h < D / 64; ++h) {
+      offk[h][0] = tile_off<D>(u0 + pi, 4 * h + t);
+      offk[h][1] = tile_off<D>(u0 + pi + 8, 4 * h + t);
+    }
   }
   // V rows: the k columns 2t, 2t+1, 2t+8, 2t+9 of P'^T are the S^T rows 2t, 2t+1 of the
   // two 8-row halves (movm_t transposes each half), i.e. unit tokens tok(2t), tok(2t+1)
@@ -705,7 +714,9 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const int row = u0 + tok(2 * t + (c & 1)) + 8 * (c >> 1);
-      offv[b][c] = D == 64 ? static_cast<uint32_t>(row * 64 + 8 * cg) : tile_off<D>(row, 8 * b + cg);
+      offv[b][c] = D == 32   ? static_cast<uint32_t>(row * 32 + 4 * cg)
+                 : D == 64 ? static_cast<uint32_t>(row * 64 + 8 * cg)
+                           : tile_off<D>(row, 8 * b + cg);
     }
   // fp16 V: this lane's ldmatrix row address for m-tile j (dims 16 j ..): it serves matrix
   // i = lane / 8 (dims + 8 (i % 2); k columns 8 (i / 2) ..) and its row r = lane % 8, the
@@ -827,6 +838,18 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
     const int8_t* qc = reinterpret_cast<const int8_t*>(smem + C::kQc + qs * C::kQcBytes);
     const float* qinfo = reinterpret_cast<const float*>(qc + 8 * D);
     uint32_t qb[D / 16][2];
+    if constexpr (D == 32) {
+      // k-step j holds dims 8t + 4j + {0, 1} | {2, 3}
+      uint2 w = make_uint2(0u, 0u);
+      if (g < GC) w = *reinterpret_cast<const uint2*>(qc + g * D + 8 * t);
+      const uint32_t ww[2] = {w.x, w.y};
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint32_t u = ww[j] ^ 0x80808080u;
+        qb[j][0] = g < GC ? codes_f16x2(u, 0x4140) : 0u;
+        qb[j][1] = g < GC ? codes_f16x2(u, 0x4342) : 0u;
+      }
+    }
 #pragma unroll
     for (int h = 0; h < D / 64; ++h) {
       uint4 w = make_uint4(0u, 0u, 0u, 0u);
@@ -889,6 +912,17 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
         // ---- S'^T = K_biased . Q^T: K codes + 128 enter as fp16 subnormals (u * 2^-24), so
         // S = 2^24 S' - 128 sum(q) exactly (two accumulation chains)
         float s0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if constexpr (D == 32) {
+          const uint2 wa = *reinterpret_cast<const uint2*>(sk + offk[0][0]);
+          const uint2 wb = *reinterpret_cast<const uint2*>(sk + offk[0][1]);
+          const uint32_t A[2] = {wa.x, wa.y}, Bw[2] = {wb.x, wb.y};
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const uint32_t ua = A[j] ^ 0x80808080u, ub = Bw[j] ^ 0x80808080u;
+            mma_f16(j & 1 ? s1 : s0, prmt(ua, 0u, 0x4140), prmt(ub, 0u, 0x4140), prmt(ua, 0u, 0x4342),
+                    prmt(ub, 0u, 0x4342), qb[j][0], qb[j][1]);
+          }
+        }
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {
           const uint4 wa = *reinterpret_cast<const uint4*>(sk + offk[h][0]);
@@ -996,6 +1030,17 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
             ldsm_x4_t(svb + offv16[j], v0, v1, v2, v3);
             mma_f16(o[j], v0, v1, v2, v3, pb0r, pb1r);
           }
+        } else if constexpr (D == 32) {
+          // one 4-byte piece (dims 4 cg .. 4 cg + 3) of each of the four V rows
+          uint32_t w[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint32_t*>(sv + offv[0][c]);
+          const uint32_t x01 = prmt(w[0], w[1], 0x5140) ^ 0x80808080u, y01 = prmt(w[0], w[1], 0x7362) ^ 0x80808080u;
+          const uint32_t x23 = prmt(w[2], w[3], 0x5140) ^ 0x80808080u, y23 = prmt(w[2], w[3], 0x7362) ^ 0x80808080u;
+          mma_f16(o[0], prmt(x01, 0u, 0x4140), prmt(x01, 0u, 0x4342), prmt(x23, 0u, 0x4140), prmt(x23, 0u, 0x4342),
+                  pb0r, pb1r);
+          mma_f16(o[1], prmt(y01, 0u, 0x4140), prmt(y01, 0u, 0x4342), prmt(y23, 0u, 0x4140), prmt(y23, 0u, 0x4342),
+                  pb0r, pb1r);
         } else if constexpr (D == 64) {
           uint2 w[4];
 #pragma unroll
@@ -1074,7 +1119,9 @@ __global__ void __launch_bounds__(DCfg<D, kV16>::kThreads, 1)
     for (int j = 0; j < (kV16 ? 0 : D / 16); ++j) {
       // physical dims of rows g and g + 8 of m-tile j
       int dim;
-      if constexpr (D == 64) {
+      if constexpr (D == 32) {
+        dim = 4 * cg + 2 * j;
+      } else if constexpr (D == 64) {
         dim = 8 * cg + 4 * (j >> 1) + 2 * (j & 1);
       } else {
         dim = 128 * (j >> 3) + 16 * cg + 4 * ((j & 7) >> 1) + 2 * (j & 1);
@@ -1211,12 +1258,15 @@ cudaError_t launch_split_d(const DecodeArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-int decode_chunk_tokens(int d) { return d == 256 ? DCfg<256>::kChunk : d == 128 ? DCfg<128>::kChunk : DCfg<64>::kChunk; }
+int decode_chunk_tokens(int d) {
+  return d == 256 ? DCfg<256>::kChunk : d == 128 ? DCfg<128>::kChunk : d == 64 ? DCfg<64>::kChunk : DCfg<32>::kChunk;
+}
 
 cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t s) {
   TraceScope tr("decode_split", s);
   if (a.verify_T) {
     switch (a.d) {
+      case 32: return launch_split_d<32, false, true>(a, s);
       case 64: return launch_split_d<64, false, true>(a, s);
       case 128: return launch_split_d<128, false, true>(a, s);
       case 256: return launch_split_d<256, false, true>(a, s);
@@ -1231,6 +1281,7 @@ cudaError_t launch_decode_split(const DecodeArgs& a, cudaStream_t s) {
     }
   }
   switch (a.d) {
+    case 32: return launch_split_d<32, false>(a, s);
     case 64: return launch_split_d<64, false>(a, s);
     case 128: return launch_split_d<128, false>(a, s);
     case 256: return launch_split_d<256, false>(a, s);
@@ -1245,6 +1296,7 @@ cudaError_t launch_decode_combine(const float* o_partial, const float* lse_parti
   const int rows = B * Hq;
   const int grid = (rows + 7) / 8;
   switch (d) {
+    case 32: decode_combine_kernel<32><<<grid, 256, 0, s>>>(o_partial, lse_partial, seqlens, B, Hq, num_splits, split_size, out, out_dtype, lse_out, seq_div); break;
     case 64: decode_combine_kernel<64><<<grid, 256, 0, s>>>(o_partial, lse_partial, seqlens, B, Hq, num_splits, split_size, out, out_dtype, lse_out, seq_div); break;
     case 128: decode_combine_kernel<128><<<grid, 256, 0, s>>>(o_partial, lse_partial, seqlens, B, Hq, num_splits, split_size, out, out_dtype, lse_out, seq_div); break;
     case 256: decode_combine_kernel<256><<<grid, 256, 0, s>>>(o_partial, lse_partial, seqlens, B, Hq, num_splits, split_size, out, out_dtype, lse_out, seq_div); break;
