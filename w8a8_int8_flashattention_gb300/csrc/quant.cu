@@ -757,12 +757,14 @@ __global__ void __launch_bounds__(128) kv_finalize_kernel(bool varlen, int32_t H
 
 // ---------------------------------------------------------------- prefill codes, pipelined
 // Persistent CTAs walk the 64-row blocks ("units") of the code workspace: first those of
-// every Q head, then those of every K head.  A producer warp stages each unit's input rows
-// (and, for a K unit whose V is converted, the same rows of V) in shared memory with bulk
-// copies, kStages units ahead; eight consumer warps turn a staged unit into codes and
-// scales (and fp16 V), eight lanes per row, while the next units load.  K units read the
-// K mean and the V exponent that kv_finalize_kernel wrote (they wait for it, and through
-// it for the K/V chunk kernel, before their first unit), so Q units overlap those kernels.
+// every Q head, then those of every kv head, a K unit followed by the V unit of the same
+// rows when V is converted.  A producer warp stages each unit's input rows in shared
+// memory with bulk copies, kStages units ahead; eight consumer warps turn a staged unit
+// into codes and scales (a V unit: into fp16 V), eight lanes per row, while the next
+// units load.  Every unit moves the same bytes, so the last units end together.  K and V
+// units read the K mean and the V exponent that kv_finalize_kernel wrote (they wait for
+// it, and through it for the K/V chunk kernel, before their first unit), so Q units
+// overlap those kernels.
 // The arithmetic is that of the per-row reading: s = max|x| / 127 (IEEE division), codes
 // RNE(x / s) formed as x * (1/s) and checked against the half-integer boundaries (the
 // exact quotient is formed for the few values near one), smoothed K = K - mean in fp32.
@@ -777,25 +779,208 @@ constexpr int kQpTickets = 64;
 __device__ uint32_t g_qp_claim[kQpTickets][2];
 
 // The unit's place, decoded once by the producer and handed to the consumers in the
-// unit's shared-memory stage (is_k < 0: no more units).
+// unit's shared-memory stage.
+constexpr int32_t kQpDone = -1, kQpQ = 0, kQpK = 1, kQpV = 2;  // QpUnit::kind
 struct QpUnit {
-  int32_t is_k, h, s, L, tk, t0, vexp, pad;
+  int32_t kind, h, s, L, tk, t0, vexp, pad;
   int64_t row0;
 };
 
 template <int D>
 struct QpCfg {
   static constexpr int kUnitBytes = kQpRows * D * 2;       // staged rows of <= D 16-bit values
-  static constexpr int kStages = D == 256 ? 2 : (D == 128 ? 2 : 4);
-  static constexpr int kMeanOff = 2 * kUnitBytes;          // input rows, V rows, K mean row
+  static constexpr int kStages = D == 256 ? 3 : (D == 128 ? 4 : 6);
+  static constexpr int kMeanOff = kUnitBytes;              // input rows, K mean row
   static constexpr int kInfoOff = kMeanOff + D * 4;
   static constexpr int kStageBytes = kInfoOff + 128;
   static constexpr int kSmem = kStages * kStageBytes + 128;
   static constexpr int kThreads = (kQpConsumers + 1) * 32;
-  static constexpr int kCtasPerSm = D == 256 ? 1 : 3;
+  static constexpr int kCtasPerSm = D == 256 ? 2 : 3;
   static_assert(kCtasPerSm * (kSmem + 1024) <= 232448, "quantiser shared memory");
   static_assert(kStageBytes % 16 == 0 && sizeof(QpUnit) <= 128, "stage layout");
 };
+
+// A Q or K unit's codes and scales (K smoothed by the staged mean): the eight lanes of a row
+// hold its vectors part + 8 j (8 values each), so that they read 128 consecutive bytes of
+// shared memory.  s_am, s_med, s_sc: the grouped scales' shared scratch (kGroups).
+template <sl8_dtype DT, int D, bool kGroups>
+__device__ __forceinline__ void qp_codes(const QuantQK& a, const QpUnit& x, const uint8_t* sx, uint32_t row_bytes,
+                                         int lane, float* s_am, float* s_med, float* s_sc) {
+  using C = QpCfg<D>;
+  constexpr int LPR = 8, NV = D / 64, RPP = 32 / LPR, P = kQpRows / kQpConsumers / RPP;
+  const int warp = threadIdx.x / 32, rsub = lane / LPR, part = lane % LPR;
+  const bool smooth = x.kind == kQpK && a.k_partials;
+  uint16_t* codes = x.kind == kQpK ? a.k_codes : a.q_codes;
+  float* scales = x.kind == kQpK ? a.k_scales : a.q_scales;
+  // the lane's values of each pass (widened, smoothed) and the validity of the pass's row
+  float v[P][NV][8];
+  bool valid[P];
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+    const int r = warp * (kQpRows / kQpConsumers) + p * RPP + rsub;
+    const int t = x.t0 + r;
+    valid[p] = t < x.L && (x.kind == kQpK || t >= a.q_off);
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int c = 8 * (part + 8 * j);
+      uint4 w = make_uint4(0u, 0u, 0u, 0u);
+      if (valid[p] && c < a.d_io) w = *reinterpret_cast<const uint4*>(sx + r * row_bytes + c * 2);
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if constexpr (DT == SL8_BF16) {
+          v[p][j][2 * e] = __uint_as_float(ww[e] << 16);
+          v[p][j][2 * e + 1] = __uint_as_float(ww[e] & 0xffff0000u);
+        } else {
+          v[p][j][2 * e] = f16_bits_to_float(ww[e] & 0xffffu);
+          v[p][j][2 * e + 1] = f16_bits_to_float(ww[e] >> 16);
+        }
+      }
+      if (smooth && valid[p] && c < a.d_io) {
+        const float4 m0 = *reinterpret_cast<const float4*>(sx + C::kMeanOff + c * 4);
+        const float4 m1 = *reinterpret_cast<const float4*>(sx + C::kMeanOff + c * 4 + 16);
+        const float mu[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+        for (int e = 0; e < 8; e += 2)
+          q_upk2(q_sub2(q_pk2(v[p][j][e], v[p][j][e + 1]), q_pk2(mu[e], mu[e + 1])), v[p][j][e],
+                 v[p][j][e + 1]);
+      }
+    }
+  }
+  // per-row max |x| over the row's eight lanes
+  float am[P];
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+    float m = 0.0f;
+#pragma unroll
+    for (int j = 0; j < NV; ++j)
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) m = q_max3(m, fabsf(v[p][j][e]), fabsf(v[p][j][e + 1]));
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    am[p] = m;
+  }
+  float scale[P];
+  if constexpr (kGroups) {
+    // grouped scales: rows [g0, g0 + G) of the unit share one (see QuantQK); the unit's 64
+    // rows are positions t0 .. t0 + 63 and t0 is a multiple of 64, so groups are
+    // unit-local.  Rows that take no part hold -1.
+#pragma unroll
+    for (int p = 0; p < P; ++p)
+      if (part == 0) s_am[warp * (kQpRows / kQpConsumers) + p * RPP + rsub] = valid[p] ? am[p] : -1.0f;
+    named_bar_sync(1, kQpConsumers * 32);
+    const int G = x.kind == kQpK ? a.k_group : a.q_group;
+    const float tau = x.kind == kQpK ? 0.0f : a.q_tau;
+    // four consecutive threads per row r, each scanning a quarter of r's group
+    const int r = threadIdx.x >> 2, jq = threadIdx.x & 3, g0 = r & ~(G - 1);
+    const int per = (G + 3) >> 2, c0 = g0 + jq * per, c1 = min(c0 + per, g0 + G);
+    const float m = s_am[r];
+    if (tau > 0.0f) {
+      int n = 0, rank = 0;
+      for (int i2 = c0; i2 < c1; ++i2) {
+        const float c = s_am[i2];
+        const bool in = c >= 0.0f;
+        n += in ? 1 : 0;
+        rank += (in && (c < m || (c == m && i2 < r))) ? 1 : 0;
+      }
+#pragma unroll
+      for (int o = 1; o < 4; o <<= 1) {
+        n += __shfl_xor_sync(0xffffffffu, n, o);
+        rank += __shfl_xor_sync(0xffffffffu, rank, o);
+      }
+      if (jq == 0 && m >= 0.0f && rank == (n - 1) / 2) s_med[g0] = m;
+      named_bar_sync(1, kQpConsumers * 32);
+    }
+    const float thr = tau > 0.0f ? __fmul_rn(tau, s_med[g0]) : INFINITY;
+    float top = 0.0f;
+    for (int i2 = c0; i2 < c1; ++i2) {
+      const float c = s_am[i2];
+      if (c >= 0.0f && !(c > thr)) top = fmaxf(top, c);
+    }
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1) top = fmaxf(top, __shfl_xor_sync(0xffffffffu, top, o));
+    if (jq == 0) s_sc[r] = m < 0.0f ? 0.0f : __fdiv_rn(m > thr ? m : top, 127.0f);
+    named_bar_sync(1, kQpConsumers * 32);
+#pragma unroll
+    for (int p = 0; p < P; ++p) scale[p] = s_sc[warp * (kQpRows / kQpConsumers) + p * RPP + rsub];
+    // the shared arrays are rewritten by the next unit only after every consumer has
+    // passed this unit's last barrier
+    named_bar_sync(1, kQpConsumers * 32);
+  } else {
+#pragma unroll
+    for (int p = 0; p < P; ++p) scale[p] = valid[p] ? __fdiv_rn(am[p], 127.0f) : 0.0f;
+  }
+  // codes: y = x * (1/s) (an approximate reciprocal is close enough: y is within 2e-5 of the
+  // correctly rounded quotient), rounded half-even by the 1.5 * 2^23 addition; a value whose
+  // y lies within 1e-4 of a half-integer takes the IEEE quotient
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+    const int r = warp * (kQpRows / kQpConsumers) + p * RPP + rsub;
+    const int64_t pr = x.row0 + r;
+    const float rs = scale[p] == 0.0f ? 0.0f : (scale[p] >= 1.0e-37f ? rcp_approx(scale[p]) : __frcp_rn(scale[p]));
+    const uint64_t rs2 = q_pk2(rs, rs), mg2 = q_pk2(12582912.0f, 12582912.0f);
+    uint16_t* crow = codes + (static_cast<int64_t>(x.h) * a.t_pad_max + pr) * D;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      float cf[8];
+      float dev = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        const uint64_t y2 = q_mul2(q_pk2(v[p][j][e], v[p][j][e + 1]), rs2);
+        const uint64_t c2 = q_sub2(q_add2(y2, mg2), mg2);
+        float d0, d1;
+        q_upk2(q_sub2(y2, c2), d0, d1);
+        q_upk2(c2, cf[e], cf[e + 1]);
+        dev = q_max3(dev, fabsf(d0), fabsf(d1));
+      }
+      if (dev > 0.4999f) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) cf[e] = quant_code_rcp(v[p][j][e], scale[p], rs);
+      }
+      // the codes are small integers: their bf16 bits are the float's upper half (one
+      // byte permute per pair)
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[e] = __byte_perm(__float_as_uint(cf[2 * e]), __float_as_uint(cf[2 * e + 1]), 0x7632);
+      *reinterpret_cast<uint4*>(crow + 8 * (part + 8 * j)) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (part == 0) scales[static_cast<int64_t>(x.h) * a.t_pad_max + pr] = scale[p];
+  }
+}
+
+// A V unit: fp16 V * 2^-e of its rows (zeros past the sequence and past d_io).
+template <int D>
+__device__ __forceinline__ void qp_convert_v(const QuantQK& a, const QpUnit& x, const uint8_t* sx, uint32_t row_bytes,
+                                             int lane) {
+  constexpr int LPR = 8, NV = D / 64, RPP = 32 / LPR, P = kQpRows / kQpConsumers / RPP;
+  const int warp = threadIdx.x / 32, rsub = lane / LPR, part = lane % LPR;
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+    const int r = warp * (kQpRows / kQpConsumers) + p * RPP + rsub;
+    const bool valid = x.t0 + r < x.L;
+    const float vscale = valid ? __int_as_float((127 - x.vexp) << 23) : 0.0f;
+    const uint64_t vs2 = q_pk2(vscale, vscale);
+    uint16_t* vrow = a.v16 + (static_cast<int64_t>(x.h) * a.t_pad_max + x.row0 + r) * D;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int c = 8 * (part + 8 * j);
+      uint4 w = make_uint4(0u, 0u, 0u, 0u);
+      if (valid && c < a.d_io) w = *reinterpret_cast<const uint4*>(sx + r * row_bytes + c * 2);
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float v0 = a.v_f16 ? f16_bits_to_float(ww[e] & 0xffffu) : bf16_bits_to_float(ww[e] & 0xffffu);
+        const float v1 = a.v_f16 ? f16_bits_to_float(ww[e] >> 16) : bf16_bits_to_float(ww[e] >> 16);
+        float s0, s1;
+        q_upk2(q_mul2(q_pk2(v0, v1), vs2), s0, s1);
+        const __half2 h2 = __floats2half2_rn(s0, s1);
+        o[e] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      *reinterpret_cast<uint4*>(vrow + c) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
 
 template <sl8_dtype DT, int D, bool kGroups>
 __global__ void __launch_bounds__(QpCfg<D>::kThreads, QpCfg<D>::kCtasPerSm)
@@ -803,7 +988,6 @@ __global__ void __launch_bounds__(QpCfg<D>::kThreads, QpCfg<D>::kCtasPerSm)
                          const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                          uint32_t ticket, DeviceStatus* st, uint64_t limit_ns) {
   using C = QpCfg<D>;
-  constexpr int LPR = 8, NV = D / 64, RPP = 32 / LPR, P = kQpRows / kQpConsumers / RPP;
   extern __shared__ __align__(128) uint8_t qp_smem[];
   __shared__ uint64_t full[C::kStages], empty[C::kStages];
   __shared__ __align__(16) float s_am[kQpRows];
@@ -827,10 +1011,10 @@ __global__ void __launch_bounds__(QpCfg<D>::kThreads, QpCfg<D>::kCtasPerSm)
   const int64_t rows_all = a.varlen ? static_cast<int64_t>(a.t.counts[1]) : static_cast<int64_t>(a.nseq) * seq_rows;
   const int64_t rows_used = rows_all < a.t_pad_max ? rows_all : a.t_pad_max;
   const int32_t nblk = static_cast<int32_t>((rows_used + kQpRows - 1) / kQpRows);
-  const int32_t n_q_units = a.Hq * nblk;
-  const int32_t n_units = n_q_units + a.Hkv * nblk;
-  const uint32_t row_bytes = static_cast<uint32_t>(a.d_io) * 2;
   const bool convert_v = a.v16 != nullptr;
+  const int32_t n_q_units = a.Hq * nblk;
+  const int32_t n_units = n_q_units + a.Hkv * nblk * (convert_v ? 2 : 1);
+  const uint32_t row_bytes = static_cast<uint32_t>(a.d_io) * 2;
 
   if (warp == kQpConsumers) {
     // ------------------------------------------------------------ producer
@@ -850,15 +1034,24 @@ __global__ void __launch_bounds__(QpCfg<D>::kThreads, QpCfg<D>::kCtasPerSm)
       if (u >= n_units) {
         // no more units: tell the consumers through the stage
         if (lane == 0) {
-          reinterpret_cast<QpUnit*>(qp_smem + stg * C::kStageBytes + C::kInfoOff)->is_k = -1;
+          reinterpret_cast<QpUnit*>(qp_smem + stg * C::kStageBytes + C::kInfoOff)->kind = kQpDone;
           mbar_arrive(&full[stg]);
         }
         break;
       }
       QpUnit x;
       x.pad = 0;
-      x.is_k = u >= n_q_units;
-      const int32_t v = x.is_k ? u - n_q_units : u;
+      int32_t v = u;
+      x.kind = kQpQ;
+      if (u >= n_q_units) {
+        v = u - n_q_units;
+        x.kind = kQpK;
+        if (convert_v) {
+          x.kind = (v & 1) ? kQpV : kQpK;
+          v >>= 1;
+        }
+      }
+      const bool kv = x.kind != kQpQ;
       x.h = v / nblk;
       x.row0 = static_cast<int64_t>(v - x.h * nblk) * kQpRows;
       int64_t pstart;
@@ -879,17 +1072,16 @@ __global__ void __launch_bounds__(QpCfg<D>::kThreads, QpCfg<D>::kCtasPerSm)
         x.tk = a.t.tok0[lo];
       }
       x.t0 = static_cast<int32_t>(x.row0 - pstart);
-      const bool smooth = x.is_k && a.k_partials;
-      const bool with_v = x.is_k && convert_v;
+      const bool smooth = x.kind == kQpK && a.k_partials;
       const int64_t srow = static_cast<int64_t>(x.s) * a.Hkv + x.h;
-      if (x.is_k && !waited) {
+      if (kv && !waited) {
         grid_dependency_wait();  // the K mean and the V exponent of kv_finalize_kernel
         waited = true;
       }
       // the V exponent: from kv_finalize_kernel when the chunk kernels ran (bf16 V), else 0,
       // published here for the attention kernel by the unit holding the sequence's first rows
       x.vexp = 0;
-      if (with_v) {
+      if (x.kind == kQpV) {
         if (chained) x.vexp = a.v_exp_out[srow];
         else if (x.t0 == 0 && lane == 0) a.v_exp_out[srow] = 0;
       }
@@ -900,20 +1092,18 @@ __global__ void __launch_bounds__(QpCfg<D>::kThreads, QpCfg<D>::kCtasPerSm)
         tb = static_cast<int>(a.total_tokens - x.tk > x.t0 ? a.total_tokens - x.tk : x.t0);
         x.L = tb;  // rows past the tensors count as past the sequence
       }
-      const int ta = max(x.t0, x.is_k ? 0 : a.q_off);
+      const int ta = max(x.t0, kv ? 0 : a.q_off);
       const int n = max(0, tb - ta);
       uint8_t* sx = qp_smem + stg * C::kStageBytes;
-      uint8_t* sv = sx + C::kUnitBytes;
-      const int H = x.is_k ? a.Hkv : a.Hq;
-      const void* src = x.is_k ? a.k : a.q;
+      const int H = kv ? a.Hkv : a.Hq;
+      const void* src = x.kind == kQpV ? a.v : (kv ? a.k : a.q);
       // varlen rows are one tiled copy of the unit's 64 token rows (rows past the sequence
       // are read and ignored; past the tensors they are zero-filled), dense rows one bulk
       // copy of the rows with input
       const uint32_t rows_copied = n > 0 ? static_cast<uint32_t>(a.varlen ? kQpRows : n) : 0u;
       if (lane == 0) {
         *reinterpret_cast<QpUnit*>(sx + C::kInfoOff) = x;
-        const uint32_t bytes = rows_copied * row_bytes * (with_v ? 2u : 1u) +
-                               (smooth ? static_cast<uint32_t>(a.d_io) * 4u : 0u);
+        const uint32_t bytes = rows_copied * row_bytes + (smooth ? static_cast<uint32_t>(a.d_io) * 4u : 0u);
         if (bytes) mbar_arrive_expect_tx(&full[stg], bytes); else mbar_arrive(&full[stg]);
         if (smooth) bulk_load(sx + C::kMeanOff, k_mean + srow * a.d_io, a.d_io * 4, &full[stg]);
       }
@@ -921,16 +1111,13 @@ __global__ void __launch_bounds__(QpCfg<D>::kThreads, QpCfg<D>::kCtasPerSm)
       if (n > 0) {
         if (!a.varlen) {
           if (lane == 0) {
-            const int64_t e0 = x.is_k ? row_offset(false, x.s, x.h, ta, H, a.N, a.d_io, 0)
-                                      : row_offset(false, x.s, x.h, ta - a.q_off, H, a.N - a.q_off, a.d_io, 0);
+            const int64_t e0 = kv ? row_offset(false, x.s, x.h, ta, H, a.N, a.d_io, 0)
+                                  : row_offset(false, x.s, x.h, ta - a.q_off, H, a.N - a.q_off, a.d_io, 0);
             bulk_load(sx + (ta - x.t0) * row_bytes, static_cast<const uint16_t*>(src) + e0, n * row_bytes, &full[stg]);
-            if (with_v)
-              bulk_load(sv + (ta - x.t0) * row_bytes, static_cast<const uint16_t*>(a.v) + e0, n * row_bytes,
-                        &full[stg]);
           }
         } else if (lane == 0) {
-          tma_load_3d(sx, x.is_k ? &map_k : &map_q, &full[stg], 0, x.h, x.tk + x.t0);
-          if (with_v) tma_load_3d(sv, &map_v, &full[stg], 0, x.h, x.tk + x.t0);
+          const CUtensorMap* map = x.kind == kQpV ? &map_v : (kv ? &map_k : &map_q);
+          tma_load_3d(sx, map, &full[stg], 0, x.h, x.tk + x.t0);
         }
       }
       if (++stg == C::kStages) {
@@ -949,179 +1136,18 @@ __global__ void __launch_bounds__(QpCfg<D>::kThreads, QpCfg<D>::kCtasPerSm)
     return;
   }
   // ------------------------------------------------------------ consumers
-  const int rsub = lane / LPR, part = lane % LPR;
   int stg = 0;
   uint32_t phase = 0;
   for (;;) {
     const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[stg], phase, limit_ns, st, 912));
     if (!ok) break;
     const uint8_t* sx = qp_smem + stg * C::kStageBytes;
-    const uint8_t* sv = sx + C::kUnitBytes;
     const QpUnit x = *reinterpret_cast<const QpUnit*>(sx + C::kInfoOff);
-    if (x.is_k < 0) break;
-    const bool smooth = x.is_k && a.k_partials;
-    const bool with_v = x.is_k && convert_v;
-    uint16_t* codes = x.is_k ? a.k_codes : a.q_codes;
-    float* scales = x.is_k ? a.k_scales : a.q_scales;
-    // the lane's values of each pass: widened, smoothed; validity of the pass's row.  The
-    // lane's channels are vectors part + 8 j (8 values each) of the row, so that the eight
-    // lanes of a row read 128 consecutive bytes of shared memory.
-    float v[P][NV][8];
-    bool valid[P];
-#pragma unroll
-    for (int p = 0; p < P; ++p) {
-      const int r = warp * (kQpRows / kQpConsumers) + p * RPP + rsub;
-      const int t = x.t0 + r;
-      valid[p] = t < x.L && (x.is_k || t >= a.q_off);
-#pragma unroll
-      for (int j = 0; j < NV; ++j) {
-        const int c = 8 * (part + 8 * j);
-        uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        if (valid[p] && c < a.d_io) w = *reinterpret_cast<const uint4*>(sx + r * row_bytes + c * 2);
-        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if constexpr (DT == SL8_BF16) {
-            v[p][j][2 * e] = __uint_as_float(ww[e] << 16);
-            v[p][j][2 * e + 1] = __uint_as_float(ww[e] & 0xffff0000u);
-          } else {
-            v[p][j][2 * e] = f16_bits_to_float(ww[e] & 0xffffu);
-            v[p][j][2 * e + 1] = f16_bits_to_float(ww[e] >> 16);
-          }
-        }
-        if (smooth && valid[p] && c < a.d_io) {
-          const float4 m0 = *reinterpret_cast<const float4*>(sx + C::kMeanOff + c * 4);
-          const float4 m1 = *reinterpret_cast<const float4*>(sx + C::kMeanOff + c * 4 + 16);
-          const float mu[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-#pragma unroll
-          for (int e = 0; e < 8; e += 2)
-            q_upk2(q_sub2(q_pk2(v[p][j][e], v[p][j][e + 1]), q_pk2(mu[e], mu[e + 1])), v[p][j][e],
-                   v[p][j][e + 1]);
-        }
-      }
-    }
-    // per-row max |x| over the row's eight lanes
-    float am[P];
-#pragma unroll
-    for (int p = 0; p < P; ++p) {
-      float m = 0.0f;
-#pragma unroll
-      for (int j = 0; j < NV; ++j)
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) m = q_max3(m, fabsf(v[p][j][e]), fabsf(v[p][j][e + 1]));
-#pragma unroll
-      for (int o = LPR / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      am[p] = m;
-    }
-    float scale[P];
-    if constexpr (kGroups) {
-      // grouped scales: rows [g0, g0 + G) of the unit share one (see QuantQK); the unit's 64
-      // rows are positions t0 .. t0 + 63 and t0 is a multiple of 64, so groups are
-      // unit-local.  Rows that take no part hold -1.
-#pragma unroll
-      for (int p = 0; p < P; ++p)
-        if (part == 0) s_am[warp * (kQpRows / kQpConsumers) + p * RPP + rsub] = valid[p] ? am[p] : -1.0f;
-      named_bar_sync(1, kQpConsumers * 32);
-      const int G = x.is_k ? a.k_group : a.q_group;
-      const float tau = x.is_k ? 0.0f : a.q_tau;
-      // four consecutive threads per row r, each scanning a quarter of r's group
-      const int r = threadIdx.x >> 2, jq = threadIdx.x & 3, g0 = r & ~(G - 1);
-      const int per = (G + 3) >> 2, c0 = g0 + jq * per, c1 = min(c0 + per, g0 + G);
-      const float m = s_am[r];
-      if (tau > 0.0f) {
-        int n = 0, rank = 0;
-        for (int i2 = c0; i2 < c1; ++i2) {
-          const float c = s_am[i2];
-          const bool in = c >= 0.0f;
-          n += in ? 1 : 0;
-          rank += (in && (c < m || (c == m && i2 < r))) ? 1 : 0;
-        }
-#pragma unroll
-        for (int o = 1; o < 4; o <<= 1) {
-          n += __shfl_xor_sync(0xffffffffu, n, o);
-          rank += __shfl_xor_sync(0xffffffffu, rank, o);
-        }
-        if (jq == 0 && m >= 0.0f && rank == (n - 1) / 2) s_med[g0] = m;
-        named_bar_sync(1, kQpConsumers * 32);
-      }
-      const float thr = tau > 0.0f ? __fmul_rn(tau, s_med[g0]) : INFINITY;
-      float top = 0.0f;
-      for (int i2 = c0; i2 < c1; ++i2) {
-        const float c = s_am[i2];
-        if (c >= 0.0f && !(c > thr)) top = fmaxf(top, c);
-      }
-#pragma unroll
-      for (int o = 1; o < 4; o <<= 1) top = fmaxf(top, __shfl_xor_sync(0xffffffffu, top, o));
-      if (jq == 0) s_sc[r] = m < 0.0f ? 0.0f : __fdiv_rn(m > thr ? m : top, 127.0f);
-      named_bar_sync(1, kQpConsumers * 32);
-#pragma unroll
-      for (int p = 0; p < P; ++p) scale[p] = s_sc[warp * (kQpRows / kQpConsumers) + p * RPP + rsub];
-      // the shared arrays are rewritten by the next unit only after every consumer has
-      // passed this unit's last barrier
-      named_bar_sync(1, kQpConsumers * 32);
+    if (x.kind == kQpDone) break;
+    if (x.kind == kQpV) {
+      qp_convert_v<D>(a, x, sx, row_bytes, lane);
     } else {
-#pragma unroll
-      for (int p = 0; p < P; ++p) scale[p] = valid[p] ? __fdiv_rn(am[p], 127.0f) : 0.0f;
-    }
-    // codes: y = x * (1/s) (an approximate reciprocal is close enough: y is within 2e-5 of the
-    // correctly rounded quotient), rounded half-even by the 1.5 * 2^23 addition; a value whose
-    // y lies within 1e-4 of a half-integer takes the IEEE quotient
-#pragma unroll
-    for (int p = 0; p < P; ++p) {
-      const int r = warp * (kQpRows / kQpConsumers) + p * RPP + rsub;
-      const int64_t pr = x.row0 + r;
-      const float rs = scale[p] == 0.0f ? 0.0f : (scale[p] >= 1.0e-37f ? rcp_approx(scale[p]) : __frcp_rn(scale[p]));
-      const uint64_t rs2 = q_pk2(rs, rs), mg2 = q_pk2(12582912.0f, 12582912.0f);
-      uint16_t* crow = codes + (static_cast<int64_t>(x.h) * a.t_pad_max + pr) * D;
-#pragma unroll
-      for (int j = 0; j < NV; ++j) {
-        float cf[8];
-        float dev = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          const uint64_t y2 = q_mul2(q_pk2(v[p][j][e], v[p][j][e + 1]), rs2);
-          const uint64_t c2 = q_sub2(q_add2(y2, mg2), mg2);
-          float d0, d1;
-          q_upk2(q_sub2(y2, c2), d0, d1);
-          q_upk2(c2, cf[e], cf[e + 1]);
-          dev = q_max3(dev, fabsf(d0), fabsf(d1));
-        }
-        if (dev > 0.4999f) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) cf[e] = quant_code_rcp(v[p][j][e], scale[p], rs);
-        }
-        uint32_t o[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          o[e] = (__float_as_uint(cf[2 * e]) >> 16) | (__float_as_uint(cf[2 * e + 1]) & 0xffff0000u);
-        *reinterpret_cast<uint4*>(crow + 8 * (part + 8 * j)) = make_uint4(o[0], o[1], o[2], o[3]);
-      }
-      if (part == 0) scales[static_cast<int64_t>(x.h) * a.t_pad_max + pr] = scale[p];
-    }
-    // fp16 V * 2^-e of the same rows (zeros past the sequence and past d_io)
-    if (with_v) {
-#pragma unroll
-      for (int p = 0; p < P; ++p) {
-        const int r = warp * (kQpRows / kQpConsumers) + p * RPP + rsub;
-        const float vscale = valid[p] ? __int_as_float((127 - x.vexp) << 23) : 0.0f;
-        uint16_t* vrow = a.v16 + (static_cast<int64_t>(x.h) * a.t_pad_max + x.row0 + r) * D;
-#pragma unroll
-        for (int j = 0; j < NV; ++j) {
-          const int c = 8 * (part + 8 * j);
-          uint4 w = make_uint4(0u, 0u, 0u, 0u);
-          if (valid[p] && c < a.d_io) w = *reinterpret_cast<const uint4*>(sv + r * row_bytes + c * 2);
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-          uint32_t o[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float v0 = a.v_f16 ? f16_bits_to_float(ww[e] & 0xffffu) : bf16_bits_to_float(ww[e] & 0xffffu);
-            const float v1 = a.v_f16 ? f16_bits_to_float(ww[e] >> 16) : bf16_bits_to_float(ww[e] >> 16);
-            const __half2 h2 = __floats2half2_rn(__fmul_rn(v0, vscale), __fmul_rn(v1, vscale));
-            o[e] = *reinterpret_cast<const uint32_t*>(&h2);
-          }
-          *reinterpret_cast<uint4*>(vrow + c) = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-      }
+      qp_codes<DT, D, kGroups>(a, x, sx, row_bytes, lane, s_am, s_med, s_sc);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stg]);
@@ -1138,7 +1164,8 @@ static cudaError_t launch_quant_pipe(const QuantQK& a, const float* k_mean, cuda
   auto kern = quant_qk_pipe_kernel<DT, D, kGroups>;
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), C::kSmem);
   if (e != cudaSuccess) return e;
-  const int64_t units = static_cast<int64_t>(a.Hq + a.Hkv) * ((a.t_pad_max + kQpRows - 1) / kQpRows);
+  const int64_t units =
+      static_cast<int64_t>(a.Hq + a.Hkv * (a.v16 ? 2 : 1)) * ((a.t_pad_max + kQpRows - 1) / kQpRows);
   const int64_t slots = static_cast<int64_t>(num_sms()) * C::kCtasPerSm;
   const int grid = static_cast<int>(units < slots ? units : slots);
   if (grid <= 0) return cudaSuccess;
