@@ -767,19 +767,34 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
     const float qk_scale = kLog2e * rsqrtf(static_cast<float>(a.d_io));  // the true head dim (32 runs as 64)
     uint32_t ns = 0, no = 0;   // S tiles consumed, items finished (this tile)
     bool bad = false;
-    for (uint32_t it = 0; !bad; ++it) {
+    // item index it from the ring (false on timeout)
+    auto fetch = [&](uint32_t it, int32_t& item) -> bool {
       const uint32_t slot = it % kItemRing;
-      if (!warp_wait(&bars.item_full[slot], (it / kItemRing) & 1, limit_ns, st, 35)) {
+      if (!warp_wait(&bars.item_full[slot], (it / kItemRing) & 1, limit_ns, st, 35)) return false;
+      item = bars.item_idx[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.item_empty[slot]);
+      return true;
+    };
+    // The next item is read from the ring, and its q scales and V exponent loaded, before
+    // this item's epilogue, so that their latency overlaps the epilogue.
+    int32_t next_item = -1;
+    bool have_next = false, have_scales = false;
+    float qs_next[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    int ve_next = 0;
+    for (uint32_t it = 0; !bad; ++it) {
+      int32_t item = next_item;
+      if (!have_next && !fetch(it, item)) {
         bad = true;
         break;
       }
-      const int32_t item = bars.item_idx[slot];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.item_empty[slot]);
+      have_next = false;
       if (item < 0) break;
       const Item w = tile_item(a, decode_item<kSplit>(a, item, group), t);  // this warpgroup's Q tile
       const int qt = tile_qt(a, w, t);
       const int nkv_full = tile_nkv<BN>(qt, w.L, causal, a.q_off);
+      const bool scales_ready = have_scales;
+      have_scales = false;
       if (nkv_full == 0) continue;  // this tile lies past the sequence's end (or before a chunk)
       const int row_abs = qt * kQTile + r;
       int jb, je;
@@ -794,10 +809,10 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
       for (int s = 0; s < 4; ++s) {
         rs.m[s] = -INFINITY;
         rs.l[s] = 0.0f;
-        rs.alpha[s] = fmaxf(qs[quad_row(s)] * qk_scale, FLT_MIN);
+        rs.alpha[s] = fmaxf((scales_ready ? qs_next[s] : qs[quad_row(s)]) * qk_scale, FLT_MIN);
         rs.row[s] = qt * kQTile + wrow + quad_row(s);
       }
-      const int ve = a.v_exp ? a.v_exp[static_cast<int64_t>(w.s) * a.Hkv + w.hkv] : 0;
+      const int ve = scales_ready ? ve_next : (a.v_exp ? a.v_exp[static_cast<int64_t>(w.s) * a.Hkv + w.hkv] : 0);
       const float v_unscale = __int_as_float((127 + ve) << 23);
       const float* ksrc = a.k_scales + static_cast<int64_t>(w.hkv) * a.t_pad_max + w.pstart;
       for (int j = jb; j < je; ++j, ++ns) {
@@ -832,6 +847,26 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
         bad = true;
         break;
       }
+      // only when the next item is already published: never wait for it here
+      const uint32_t nslot = (it + 1) % kItemRing;
+      if (__all_sync(0xffffffffu, mbar_try_wait(&bars.item_full[nslot], ((it + 1) / kItemRing) & 1))) {
+        if (!fetch(it + 1, next_item)) {
+          bad = true;
+          break;
+        }
+        have_next = true;
+      }
+      if (have_next && next_item >= 0) {
+        const Item wn = tile_item(a, decode_item<kSplit>(a, next_item, group), t);
+        const int qtn = tile_qt(a, wn, t);
+        if (tile_nkv<BN>(qtn, wn.L, causal, a.q_off) > 0) {
+          const float* qsn = a.q_scales + static_cast<int64_t>(wn.hq) * a.t_pad_max + wn.pstart + qtn * kQTile + wrow;
+#pragma unroll
+          for (int s = 0; s < 4; ++s) qs_next[s] = qsn[quad_row(s)];
+          ve_next = a.v_exp ? a.v_exp[static_cast<int64_t>(wn.s) * a.Hkv + wn.hkv] : 0;
+          have_scales = true;
+        }
+      }
       if (!warp_wait(&bars.o_done[t], no & 1, limit_ns, st, 32)) {
         bad = true;
       } else {
@@ -854,6 +889,15 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
 }
 
 // ==================================================================== d = 256: one Q tile per CTA
+// Item k of this CTA.  Items are numbered longest first; CTA c takes item c of every even
+// round of gridDim.x items and item gridDim.x - 1 - c of every odd round ("snake" order),
+// so that each CTA's long and short items even out (plain round robin gives CTA 0 the
+// longest item of every round).  Past the last item, every later k is past it too.
+__device__ __forceinline__ int64_t snake_item(int64_t k) {
+  const int64_t base = k * gridDim.x;
+  return (k & 1) ? base + gridDim.x - 1 - blockIdx.x : base + blockIdx.x;
+}
+
 template <int D>
 struct SingleCfg {
   static constexpr int BN = 64;
@@ -935,7 +979,7 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
       prefetch_tensormap(&map_v);
       uint32_t g = 0, it = 0;
       bool ok = true;
-      for (int64_t item = blockIdx.x; item < n_items && ok && !*abort_flag; item += gridDim.x, ++it) {
+      for (int64_t item = snake_item(0); item < n_items && ok && !*abort_flag; ++it, item = snake_item(it)) {
         const Item w = decode_item(a, item, group);
         const int nkv = tile_nkv<BN>(w.it, w.L, causal, a.q_off);
         if (it >= 1) ok = mbar_wait(&bars.q_empty, (it - 1) & 1, limit_ns, st, 10);
@@ -958,8 +1002,8 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
     // S tiles run one ahead of P.V: S_{g+1} is issued before PV_g (two S buffers).  The
     // whole warp runs this loop; one lane issues.
     {
-      int64_t item_s = blockIdx.x, item_p = blockIdx.x;
-      uint32_t it_s = 0, gs = 0, gp = 0;
+      int64_t item_s = snake_item(0), item_p = item_s;
+      uint32_t it_s = 0, it_p = 0, gs = 0, gp = 0;
       int j_s = 0, j_p = 0;
       int nkv_s = 0, nkv_p = 0;
       if (item_s < n_items) {
@@ -985,7 +1029,7 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
             mma_commit(&bars.q_empty);
             j_s = 0;
             ++it_s;
-            item_s += gridDim.x;
+            item_s = snake_item(it_s);
             if (item_s < n_items) {
               const Item ws = decode_item(a, item_s, group);
               nkv_s = tile_nkv<BN>(ws.it, ws.L, causal, a.q_off);
@@ -1005,7 +1049,7 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
         ++gp;
         if (++j_p == nkv_p) {
           j_p = 0;
-          item_p += gridDim.x;
+          item_p = snake_item(++it_p);
           if (item_p < n_items) {
             const Item wp = decode_item(a, item_p, group);
             nkv_p = tile_nkv<BN>(wp.it, wp.L, causal, a.q_off);
@@ -1024,7 +1068,7 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
     const int wrow = warp * 32;
     const uint32_t lane_base = static_cast<uint32_t>(wrow) << 16;
     const float qk_scale = kLog2e * rsqrtf(static_cast<float>(a.d_io));  // the true head dim (32 runs as 64)
-    int64_t item = blockIdx.x;
+    int64_t k_item = 0, item = snake_item(0);
     Item w{};
     uint32_t g = 0;
     // q scales of this thread's four softmax rows (the quad layout) for the next item
@@ -1053,7 +1097,7 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
         rs.row[s] = w.it * kQTile + wrow + quad_row(s);
       }
       const float v_unscale = __int_as_float((127 + ve_next) << 23);
-      const int64_t item_n = item + gridDim.x;
+      const int64_t item_n = snake_item(k_item + 1);
       Item wn{};
       if (item_n < n_items) wn = decode_item(a, item_n, group);
       const float* ksrc = a.k_scales + static_cast<int64_t>(w.hkv) * a.t_pad_max + w.pstart;
@@ -1108,6 +1152,7 @@ __global__ void __launch_bounds__(SingleCfg<D>::kThreads, 1)
         }
       }
       item = item_n;
+      ++k_item;
       w = wn;
     }
     if (bad) *abort_flag = 1;
