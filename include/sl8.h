@@ -160,6 +160,39 @@ SL8_API int sl8_attn_int8_fwd_chunk(const void* q, const void* k, const void* v,
                                     size_t workspace_bytes, void* stream);
 
 /*
+ * Prefill of a query chunk onto an int8 KV cache that already holds its keys (the
+ * "Engine" table's chunked prefill onto a paged/int8 KV cache, with the cache format of
+ * the "Attention kernels" table's attn_decode row; reading: the pages give no layout).
+ * Nothing is re-quantised but Q: the cache's K codes and scales enter the exact int32
+ * logits as they are, and V is dequantised (code * scale) into the fp16 operand of P.V.
+ *   q                   device, [B][Hq][Nq][d] of q_dtype (F16 or BF16): the queries of
+ *                       positions Nk - Nq .. Nk - 1 of every sequence, quantised per row
+ *                       as in sl8_attn_int8_fwd.
+ *   k_cache, v_cache    device, [B][Hkv][Lmax][d] int8 codes (16-byte aligned), as for
+ *                       sl8_attn_int8_decode_splitkv; every sequence holds Nk positions
+ *                       (rows 0 .. Nk-1, the chunk's own included), Nq <= Nk <= Lmax.
+ *   k_scale, v_scale    device, [B][Hkv][Lmax] fp32 per-token scales.
+ *   causal              nonzero: query i (position Nk - Nq + i) sees keys j <= Nk - Nq + i;
+ *                       zero: every query sees all Nk keys.
+ *   out                 device, [B][Hq][Nq][d] of out_dtype (F16, BF16 or F32).
+ *   lse_out             device, nullable, [B][Hq][Nq] fp32 (natural log).
+ *   workspace           at least sl8_attn_int8_fwd_chunk_workspace_size(B, Hq, Hkv, Nq,
+ *                       Nk, d) bytes (the same layout, key splits of small chunks
+ *                       included); sl8_attn_int8_fwd_workspace_size(B, Hq, Hkv, Nk, d, 0)
+ *                       bytes run without key splits.
+ * V enters P.V as fp16(code * scale * 2^-e), e >= 0 the least exponent with
+ * max(v_scale) < 2^(e + 8) over the (sequence, kv head), and O is scaled back by 2^e.
+ * Errors: SL8_ERR_INVALID_ARG (null or misaligned pointers, dtypes, shapes,
+ * Nq > Nk > Lmax), SL8_ERR_UNSUPPORTED (d not in {32, 64, 128, 256}, B * Nk >= 2^31),
+ * SL8_ERR_WORKSPACE, SL8_ERR_CUDA.  B or Nq 0: SL8_OK without launching.
+ */
+SL8_API int sl8_attn_int8_fwd_chunk_cache(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale,
+                                          const int8_t* v_cache, const float* v_scale, int32_t B, int32_t Hq,
+                                          int32_t Hkv, int32_t Nq, int32_t Nk, int32_t Lmax, int32_t d, int causal,
+                                          void* out, int out_dtype, float* lse_out, void* workspace,
+                                          size_t workspace_bytes, void* stream);
+
+/*
  * W8A8 prefill with grouped ("per-warp") scales and outlier-aware Q ("Attention
  * kernels" table, attn_w8a8_fwd row: a W8A8 forward with scales set per warp that takes
  * outliers into account; "Quantization" table, per-row int8 row, which lists outlier

@@ -424,6 +424,41 @@ def attn_decode_verify(q, k_codes, k_scales, v_codes, v_scales, seqlens, tree_ma
     return dict(out=out, lse=lse, q_codes=q_codes, q_scales=q_scales)
 
 
+def attn_chunk_cache(q, k_codes, k_scales, v_codes, v_scales, nk, causal=True, rows=None):
+    """A query chunk against an int8 cache that holds its keys, fp64 after the int32 dot.
+
+    Source: the "SuperL8-serve" README, "Engine" table (chunked prefill onto the KV
+    cache), with the cache of the "Attention kernels" table's attn_decode row (int8 codes,
+    per-token scales).  Reading (R21): q [B, Hq, Nq, d] holds the queries of positions
+    nk - Nq .. nk - 1; the caches [B, Hkv, Lmax, d] hold positions 0 .. nk - 1 of every
+    sequence.  Row (b, hq, i) is the decode of its quantised query over cache positions
+    0 .. nk - Nq + i (causal) or 0 .. nk - 1.  Returns dict(out [B,Hq,Nq,d] f64,
+    lse [B,Hq,Nq], q_codes, q_scales).
+    """
+    q = _f32(q)
+    k_codes = np.ascontiguousarray(k_codes, np.int8)
+    v_codes = np.ascontiguousarray(v_codes, np.int8)
+    k_scales = _f32(k_scales)
+    v_scales = _f32(v_scales)
+    B, hq_n, nq, d = q.shape
+    group = hq_n // k_codes.shape[1]
+    lib = _load()
+    q_codes, q_scales = quant_rowwise(q)
+    out = np.full((B, hq_n, nq, d), np.nan, np.float64)
+    lse = np.full((B, hq_n, nq), np.nan, np.float64)
+    triples = ([(b, h, i) for b in range(B) for h in range(hq_n) for i in range(nq)] if rows is None
+               else [(int(b), int(h), int(i)) for b, h, i in rows])
+    for b, hq, i in triples:
+        hkv = hq // group
+        L = nk - nq + i + 1 if causal else nk
+        o = np.zeros(d, np.float64)
+        lv = np.zeros(1, np.float64)
+        lib.oracle_decode_row(q_codes[b, hq, i], float(q_scales[b, hq, i]), k_codes[b, hkv], k_scales[b, hkv],
+                              v_codes[b, hkv], v_scales[b, hkv], L, 0, L, d, o, lv, None)
+        out[b, hq, i], lse[b, hq, i] = o, lv[0]
+    return dict(out=out, lse=lse, q_codes=q_codes, q_scales=q_scales)
+
+
 def _decode(q, rows_of, hkv_n, lmax, seqlens, num_splits, split_size, rows, want_logits):
     """The split loop shared by the decode oracles; rows_of(b, hkv, L) gives the kv head's
     cache rows (k codes, k scales, v codes, v scales) for tokens 0 .. L-1 (at least); v

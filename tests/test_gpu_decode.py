@@ -368,3 +368,45 @@ def test_decode_query_dtypes(qdt):
     check_f32(to_np32(ov), refv["out"], f"q {qdt} verify f32")
     st, site = sl8.last_device_status()
     assert st == sl8.SL8_OK, (st, site)
+
+
+CHUNK_CACHE_CASES = [
+    # wid, B, Hq, Hkv, d, Nq, Nk, Lmax, causal, q dtype
+    (4101, 2, 8, 2, 128, 200, 700, 760, True, "bf16"),
+    (4102, 1, 4, 4, 64, 96, 96, 128, True, "f16"),       # the chunk is the whole sequence
+    (4103, 1, 8, 1, 256, 130, 1000, 1000, True, "bf16"),  # MQA at d = 256
+    (4104, 1, 4, 2, 128, 64, 2048, 2048, True, "bf16"),   # two items: keys split 8 ways
+    (4105, 2, 4, 2, 32, 50, 300, 320, False, "f16"),      # head dim 32, not causal
+    (4106, 1, 8, 2, 128, 300, 300, 300, False, "bf16"),
+]
+
+
+@pytest.mark.parametrize("case", CHUNK_CACHE_CASES, ids=[f"w{c[0]}_d{c[4]}_nq{c[5]}" for c in CHUNK_CACHE_CASES])
+def test_chunk_onto_int8_cache(case):
+    """A query chunk against an int8 cache that already holds its keys, against the
+    oracle: every output row, in fp32 and in the query dtype, and the LSE."""
+    wid, B, Hq, Hkv, d, nq, nk, lmax, causal, qdt = case
+    w = W.custom(wid, kind="decode", B=B, Hq=Hq, Hkv=Hkv, d=d, dtype=qdt, extra={"lengths": [nk] * B})
+    _, g, gs, o, os_ = build_cache(w, lmax)
+    q = W.chunk_query(w, nq)
+    qd = q.to(DEV)
+    ref = oracle.attn_chunk_cache(q.float().numpy(), o["k"], os_["k"], o["v"], os_["v"], nk, causal=causal)
+    o32, lse = sl8.attn_int8_fwd_chunk_cache(qd, g["k"], gs["k"], g["v"], gs["v"], Nk=nk, causal=causal,
+                                             out_dtype=torch.float32, return_lse=True)
+    oh = sl8.attn_int8_fwd_chunk_cache(qd, g["k"], gs["k"], g["v"], gs["v"], Nk=nk, causal=causal)
+    torch.cuda.synchronize()
+    check_f32(to_np32(o32), ref["out"], f"w{wid} f32")
+    check_half(oh, ref["out"], f"w{wid} {qdt}")
+    np.testing.assert_allclose(to_np32(lse), ref["lse"], rtol=0, atol=1e-4)
+    st, site = sl8.last_device_status()
+    assert st == sl8.SL8_OK, (st, site)
+
+
+def test_chunk_onto_int8_cache_rejects_bad_shapes():
+    w = W.custom(4107, kind="decode", B=1, Hq=4, Hkv=2, d=64, dtype="bf16", extra={"lengths": [64]})
+    _, g, gs, _, _ = build_cache(w, 64)
+    q = W.chunk_query(w, 16).to(DEV)
+    with pytest.raises(RuntimeError):  # Nk > Lmax
+        sl8.attn_int8_fwd_chunk_cache(q, g["k"], gs["k"], g["v"], gs["v"], Nk=65)
+    with pytest.raises(RuntimeError):  # Nq > Nk
+        sl8.attn_int8_fwd_chunk_cache(q, g["k"], gs["k"], g["v"], gs["v"], Nk=8)

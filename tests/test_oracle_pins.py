@@ -586,3 +586,40 @@ def test_verify_tree_mask_drops_siblings():
     np.testing.assert_allclose(r["out"][:, 1], ref["out"], rtol=0, atol=1e-13)
     ref0 = oracle.attn_decode(q[:, 0], kc, ks, vc, vs, [29], num_splits=1)   # draft 0 sees positions 0..28
     np.testing.assert_allclose(r["out"][:, 0], ref0["out"], rtol=0, atol=1e-13)
+
+
+def _chunk_cache_case(rng, B=2, hq=4, hkv=2, nq=5, nk=40, lmax=48, d=64):
+    q = rng.standard_normal((B, hq, nq, d)).astype(np.float32)
+    kc = rng.integers(-127, 128, size=(B, hkv, lmax, d)).astype(np.int8)
+    # every key row reaches +-127, so that re-quantising code * scale gives the codes back
+    kc[..., 0] = np.where(rng.random((B, hkv, lmax)) < 0.5, 127, -127).astype(np.int8)
+    vc = rng.integers(-127, 128, size=(B, hkv, lmax, d)).astype(np.int8)
+    ks = rng.uniform(0.001, 0.05, size=(B, hkv, lmax)).astype(np.float32)
+    vs = rng.uniform(0.001, 0.05, size=(B, hkv, lmax)).astype(np.float32)
+    return q, kc, ks, vc, vs, nk
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_chunk_cache_equals_prefill_chunk_on_dequantised_cache(causal):
+    """The chunk against an int8 cache is the prefill chunk (bottom-right, no smoothing)
+    whose K and V are the cache's code * scale: the prefill's own per-row quantisation of
+    K returns the cache's codes (every row holds a +-127), up to fp32 rounding of the
+    products."""
+    rng = np.random.default_rng(80)
+    q, kc, ks, vc, vs, nk = _chunk_cache_case(rng)
+    r = oracle.attn_chunk_cache(q, kc, ks, vc, vs, nk, causal=causal)
+    kf = (kc[:, :, :nk].astype(np.float32) * ks[:, :, :nk, None]).astype(np.float32)
+    vf = (vc[:, :, :nk].astype(np.float32) * vs[:, :, :nk, None]).astype(np.float32)
+    ref = oracle.attn_prefill(q, kf, vf, causal=causal, smooth_k=False)
+    np.testing.assert_allclose(r["out"], ref["out"], rtol=0, atol=1e-6)
+    np.testing.assert_allclose(r["lse"], ref["lse"], rtol=0, atol=1e-6)
+
+
+def test_chunk_cache_single_query_is_decode():
+    """A one-query chunk is the decode of that query over the whole cache (length nk)."""
+    rng = np.random.default_rng(81)
+    q, kc, ks, vc, vs, nk = _chunk_cache_case(rng, nq=1)
+    r = oracle.attn_chunk_cache(q, kc, ks, vc, vs, nk)
+    ref = oracle.attn_decode(q[:, :, 0], kc, ks, vc, vs, np.full(q.shape[0], nk), num_splits=1)
+    np.testing.assert_allclose(r["out"][:, :, 0], ref["out"], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(r["lse"][:, :, 0], ref["lse"], rtol=0, atol=1e-13)

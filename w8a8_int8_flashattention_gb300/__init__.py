@@ -70,6 +70,8 @@ _SIGNATURES = {
     "sl8_attn_int8_fwd_chunk_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
     "sl8_attn_int8_fwd_chunk": (_INT, [_P, _P, _P, _INT, _INT, _I32, _I32, _I32, _I32, _I32, _I32, _INT, _INT, _P,
                                        _INT, _P, _P, _SZ, _P]),
+    "sl8_attn_int8_fwd_chunk_cache": (_INT, [_P, _INT, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _INT,
+                                             _P, _INT, _P, _P, _SZ, _P]),
     "sl8_attn_int8_qk_logits_debug": (_INT, [_P, _P, _INT, _I32, _I32, _I32, _I32, _I32, _P, _I64, _INT, _I32, _I32,
                                              _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "sl8_attn_w8a8_fwd": (_INT, [_P, _P, _P, _INT, _INT, _I32, _I32, _I32, _I32, _I32, _P, _I64, _INT, _INT, _I32,
@@ -284,6 +286,32 @@ def attn_int8_fwd_chunk(q, k, v, causal=True, smooth_k=True, out_dtype=None, ret
                                          int(bool(causal)), int(bool(smooth_k)), _ptr(out), _dt(out),
                                          _ptr(lse) if return_lse else None, _ptr(workspace), workspace.numel(),
                                          _stream(q.device)), "sl8_attn_int8_fwd_chunk")
+    return (out, lse) if return_lse else out
+
+
+def attn_int8_fwd_chunk_cache(q, k_cache, k_scale, v_cache, v_scale, Nk=None, causal=True, out_dtype=None,
+                              return_lse=False, workspace=None, out=None, lse=None):
+    """Prefill of a query chunk onto an int8 KV cache: q [B,Hq,Nq,d] (fp16/bf16) holds
+    positions Nk-Nq .. Nk-1; the caches k_cache, v_cache [B,Hkv,Lmax,d] int8 with scales
+    [B,Hkv,Lmax] fp32 hold Nk (default Lmax) positions of every sequence.  Returns out
+    [B,Hq,Nq,d] (and the fp32 LSE with return_lse)."""
+    _need_cuda(q, k_cache, k_scale, v_cache, v_scale, workspace)
+    B, Hq, Nq, d = q.shape
+    Hkv, Lmax = k_cache.shape[1], k_cache.shape[2]
+    Nk = Lmax if Nk is None else int(Nk)
+    out_dtype = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    if return_lse and lse is None:
+        lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    if workspace is None:
+        ws_bytes = int(lib().sl8_attn_int8_fwd_chunk_workspace_size(B, Hq, Hkv, Nq, Nk, d))
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    _check(lib().sl8_attn_int8_fwd_chunk_cache(_ptr(q), _dt(q), _ptr(k_cache), _ptr(k_scale), _ptr(v_cache),
+                                               _ptr(v_scale), B, Hq, Hkv, Nq, Nk, Lmax, d, int(bool(causal)),
+                                               _ptr(out), _dt(out), _ptr(lse) if return_lse else None,
+                                               _ptr(workspace), workspace.numel(), _stream(q.device)),
+           "sl8_attn_int8_fwd_chunk_cache")
     return (out, lse) if return_lse else out
 
 

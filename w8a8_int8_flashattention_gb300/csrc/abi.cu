@@ -403,27 +403,12 @@ static size_t chunk_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t 
   return p.total + chunk_partial_o_bytes(split, rows, d) + static_cast<size_t>(split) * rows * sizeof(float);
 }
 
-// Prefill over N keys per sequence; q_off > 0 (dense only): a query chunk of the last
-// N - q_off positions, aligned bottom-right.
-static int prefill_run(const void* q, const void* k, const void* v, int qk_dtype, int v_dtype, int32_t B, int32_t Hq,
-                       int32_t Hkv, int32_t N, int32_t d, const int32_t* cu_seqlens, int64_t total_tokens, int causal,
-                       int smooth_k, void* out, int out_dtype, float* lse_out, void* workspace, size_t workspace_bytes,
-                       void* stream, int32_t q_off, const QuantGroups& groups = QuantGroups()) {
-  int rc = validate_prefill(q, k, qk_dtype, B, Hq, Hkv, N, d);
-  if (rc != SL8_OK) return rc;
-  SL8_CHECK(v && out && aligned16(v) && aligned16(out), SL8_ERR_INVALID_ARG);
-  SL8_CHECK(is_half(v_dtype), SL8_ERR_INVALID_ARG);
-  SL8_CHECK(out_dtype == v_dtype || out_dtype == SL8_F32, SL8_ERR_INVALID_ARG);
-  SL8_CHECK(!cu_seqlens || total_tokens >= 0, SL8_ERR_INVALID_ARG);
-  SL8_CHECK(!cu_seqlens || total_tokens < (1ll << 31), SL8_ERR_UNSUPPORTED);
-  SL8_CHECK(static_cast<int64_t>(B) * N < (1ll << 31), SL8_ERR_UNSUPPORTED);
-  if (B == 0 || N == 0 || (cu_seqlens && total_tokens == 0)) return SL8_OK;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  PrefillWorkspace p;
-  SeqTable t;
-  rc = prefill_prepare(q, k, v, qk_dtype, v_dtype, B, Hq, Hkv, N, d, cu_seqlens, total_tokens, smooth_k, workspace,
-                       workspace_bytes, s, false, &p, &t, q_off, groups);
-  if (rc != SL8_OK) return rc;
+// The attention launch after the codes are in the workspace (plan p, table t): with use_v16
+// V is read from the workspace's fp16 copy and its exponents, else from v (fp16).
+static int prefill_attend(const PrefillWorkspace& p, const SeqTable& t, void* workspace, size_t workspace_bytes,
+                          const void* v, int v_dtype, bool use_v16, int32_t B, int32_t Hq, int32_t Hkv, int32_t N,
+                          int32_t d, const int32_t* cu_seqlens, int64_t total_tokens, int causal, void* out,
+                          int out_dtype, float* lse_out, cudaStream_t s, int32_t q_off) {
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   PrefillArgs a{};
   a.q_off = q_off;
@@ -434,7 +419,7 @@ static int prefill_run(const void* q, const void* k, const void* v, int qk_dtype
   a.k_scales = reinterpret_cast<const float*>(ws + p.k_scales);
   a.v = v;
   a.v_dtype = static_cast<sl8_dtype>(v_dtype);
-  if (v_dtype == SL8_BF16 || dc != d) {  // the padded / rescaled fp16 copy of V
+  if (use_v16) {  // the padded / rescaled fp16 copy of V
     a.v16 = reinterpret_cast<const uint16_t*>(ws + p.v16);
     a.v_exp = reinterpret_cast<const int32_t*>(ws + p.v_exp);
   }
@@ -478,6 +463,31 @@ static int prefill_run(const void* q, const void* k, const void* v, int qk_dtype
   return SL8_OK;
 }
 
+// Prefill over N keys per sequence; q_off > 0 (dense only): a query chunk of the last
+// N - q_off positions, aligned bottom-right.
+static int prefill_run(const void* q, const void* k, const void* v, int qk_dtype, int v_dtype, int32_t B, int32_t Hq,
+                       int32_t Hkv, int32_t N, int32_t d, const int32_t* cu_seqlens, int64_t total_tokens, int causal,
+                       int smooth_k, void* out, int out_dtype, float* lse_out, void* workspace, size_t workspace_bytes,
+                       void* stream, int32_t q_off, const QuantGroups& groups = QuantGroups()) {
+  int rc = validate_prefill(q, k, qk_dtype, B, Hq, Hkv, N, d);
+  if (rc != SL8_OK) return rc;
+  SL8_CHECK(v && out && aligned16(v) && aligned16(out), SL8_ERR_INVALID_ARG);
+  SL8_CHECK(is_half(v_dtype), SL8_ERR_INVALID_ARG);
+  SL8_CHECK(out_dtype == v_dtype || out_dtype == SL8_F32, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(!cu_seqlens || total_tokens >= 0, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(!cu_seqlens || total_tokens < (1ll << 31), SL8_ERR_UNSUPPORTED);
+  SL8_CHECK(static_cast<int64_t>(B) * N < (1ll << 31), SL8_ERR_UNSUPPORTED);
+  if (B == 0 || N == 0 || (cu_seqlens && total_tokens == 0)) return SL8_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PrefillWorkspace p;
+  SeqTable t;
+  rc = prefill_prepare(q, k, v, qk_dtype, v_dtype, B, Hq, Hkv, N, d, cu_seqlens, total_tokens, smooth_k, workspace,
+                       workspace_bytes, s, false, &p, &t, q_off, groups);
+  if (rc != SL8_OK) return rc;
+  return prefill_attend(p, t, workspace, workspace_bytes, v, v_dtype, v_dtype == SL8_BF16 || compute_dim(d) != d, B,
+                        Hq, Hkv, N, d, cu_seqlens, total_tokens, causal, out, out_dtype, lse_out, s, q_off);
+}
+
 int sl8_attn_int8_fwd(const void* q, const void* k, const void* v, int qk_dtype, int v_dtype, int32_t B, int32_t Hq,
                       int32_t Hkv, int32_t N, int32_t d, const int32_t* cu_seqlens, int64_t total_tokens,
                       int causal, int smooth_k, void* out, int out_dtype, float* lse_out, void* workspace,
@@ -499,6 +509,39 @@ int sl8_attn_int8_fwd_chunk(const void* q, const void* k, const void* v, int qk_
   if (Nq == 0) return SL8_OK;
   return prefill_run(q, k, v, qk_dtype, v_dtype, B, Hq, Hkv, Nk, d, nullptr, 0, causal, smooth_k, out, out_dtype,
                      lse_out, workspace, workspace_bytes, stream, Nk - Nq);
+}
+
+int sl8_attn_int8_fwd_chunk_cache(const void* q, int q_dtype, const int8_t* k_cache, const float* k_scale,
+                                  const int8_t* v_cache, const float* v_scale, int32_t B, int32_t Hq, int32_t Hkv,
+                                  int32_t Nq, int32_t Nk, int32_t Lmax, int32_t d, int causal, void* out,
+                                  int out_dtype, float* lse_out, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  SL8_CHECK(q && k_cache && k_scale && v_cache && v_scale && out, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(aligned16(q) && aligned16(k_cache) && aligned16(v_cache) && aligned16(out), SL8_ERR_INVALID_ARG);
+  SL8_CHECK(is_half(q_dtype) && (is_half(out_dtype) || out_dtype == SL8_F32), SL8_ERR_INVALID_ARG);
+  SL8_CHECK(B >= 0 && Hq > 0 && Hkv > 0 && d > 0 && Hq % Hkv == 0, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(Nq >= 0 && Nq <= Nk && Nk <= Lmax, SL8_ERR_INVALID_ARG);
+  SL8_CHECK(d == 32 || head_dim_ok(d), SL8_ERR_UNSUPPORTED);  // head dim 32 runs as 64
+  SL8_CHECK(Nk <= (1 << 24) && B <= (1 << 24) && static_cast<int64_t>(B) * Nk < (1ll << 31), SL8_ERR_UNSUPPORTED);
+  if (B == 0 || Nq == 0) return SL8_OK;
+  const PrefillWorkspace p = plan_prefill_workspace(B, Hq, Hkv, Nk, d, 0, false);
+  SL8_CHECK(workspace && aligned16(workspace) && workspace_bytes >= p.total, SL8_ERR_WORKSPACE);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const SeqTable t = table_at(ws, p);
+  const int32_t dc = compute_dim(d);
+  // K and V codes from the cache (a plain launch: it follows every earlier reader of the
+  // workspace in stream order), then the Q rows, then the attention
+  SL8_LAUNCH(launch_cache_codes(k_cache, k_scale, v_cache, v_scale, B, Hkv, Nk, Lmax, dc, d, p.t_pad_max,
+                                reinterpret_cast<uint16_t*>(ws + p.k_codes), reinterpret_cast<float*>(ws + p.k_scales),
+                                reinterpret_cast<uint16_t*>(ws + p.v16), reinterpret_cast<int32_t*>(ws + p.v_exp), s));
+  SL8_LAUNCH(launch_quant_qk(q, nullptr, static_cast<sl8_dtype>(q_dtype), false, B, Hq, Hkv, Nk, dc,
+                             static_cast<int64_t>(B) * Nk, t, p.t_pad_max, nullptr, nullptr, p.max_chunks,
+                             reinterpret_cast<uint16_t*>(ws + p.q_codes), reinterpret_cast<float*>(ws + p.q_scales),
+                             reinterpret_cast<uint16_t*>(ws + p.k_codes), reinterpret_cast<float*>(ws + p.k_scales),
+                             nullptr, nullptr, nullptr, s, Nk - Nq, d));
+  return prefill_attend(p, t, workspace, workspace_bytes, nullptr, SL8_F16, true, B, Hq, Hkv, Nk, d, nullptr, 0,
+                        causal, out, out_dtype, lse_out, s, Nk - Nq);
 }
 
 // Group sizes: powers of two from 1 to 64 (a group never leaves one 64-row CTA of the

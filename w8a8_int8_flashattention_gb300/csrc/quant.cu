@@ -1013,7 +1013,7 @@ __global__ void __launch_bounds__(QpCfg<D>::kThreads, QpCfg<D>::kCtasPerSm)
   const int32_t nblk = static_cast<int32_t>((rows_used + kQpRows - 1) / kQpRows);
   const bool convert_v = a.v16 != nullptr;
   const int32_t n_q_units = a.Hq * nblk;
-  const int32_t n_units = n_q_units + a.Hkv * nblk * (convert_v ? 2 : 1);
+  const int32_t n_units = n_q_units + (a.k ? a.Hkv * nblk * (convert_v ? 2 : 1) : 0);  // k null: Q rows only
   const uint32_t row_bytes = static_cast<uint32_t>(a.d_io) * 2;
 
   if (warp == kQpConsumers) {
@@ -1165,7 +1165,7 @@ static cudaError_t launch_quant_pipe(const QuantQK& a, const float* k_mean, cuda
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), C::kSmem);
   if (e != cudaSuccess) return e;
   const int64_t units =
-      static_cast<int64_t>(a.Hq + a.Hkv * (a.v16 ? 2 : 1)) * ((a.t_pad_max + kQpRows - 1) / kQpRows);
+      static_cast<int64_t>(a.Hq + (a.k ? a.Hkv * (a.v16 ? 2 : 1) : 0)) * ((a.t_pad_max + kQpRows - 1) / kQpRows);
   const int64_t slots = static_cast<int64_t>(num_sms()) * C::kCtasPerSm;
   const int grid = static_cast<int>(units < slots ? units : slots);
   if (grid <= 0) return cudaSuccess;
@@ -1179,8 +1179,9 @@ static cudaError_t launch_quant_pipe(const QuantQK& a, const float* k_mean, cuda
     const uint64_t T = static_cast<uint64_t>(a.total_tokens), dio = static_cast<uint64_t>(a.d_io);
     mq = make_tmap_3d(a.q, CU_TENSOR_MAP_DATA_TYPE_UINT16, dio, a.Hq, T, dio * 2, dio * 2 * a.Hq, a.d_io, 1, kQpRows,
                       &ok, false);
-    mk = make_tmap_3d(a.k, CU_TENSOR_MAP_DATA_TYPE_UINT16, dio, a.Hkv, T, dio * 2, dio * 2 * a.Hkv, a.d_io, 1,
-                      kQpRows, &ok, false);
+    if (a.k)
+      mk = make_tmap_3d(a.k, CU_TENSOR_MAP_DATA_TYPE_UINT16, dio, a.Hkv, T, dio * 2, dio * 2 * a.Hkv, a.d_io, 1,
+                        kQpRows, &ok, false);
     if (a.v16)
       mv = make_tmap_3d(a.v, CU_TENSOR_MAP_DATA_TYPE_UINT16, dio, a.Hkv, T, dio * 2, dio * 2 * a.Hkv, a.d_io, 1,
                         kQpRows, &ok, false);
@@ -1225,6 +1226,87 @@ cudaError_t launch_quant_qk(const void* q, const void* k, sl8_dtype dt, bool var
                           : launch_quant_pipe_dt<SL8_F16, true>(a, k_mean, d, s);
   return dt == SL8_BF16 ? launch_quant_pipe_dt<SL8_BF16, false>(a, k_mean, d, s)
                         : launch_quant_pipe_dt<SL8_F16, false>(a, k_mean, d, s);
+}
+
+// ---------------------------------------------------------------- codes from an int8 cache
+// One CTA per (64-row block of a sequence's padded rows, kv head, sequence); each thread
+// turns 16 codes of a row at a time.  The V exponent e >= 0 is the least with
+// max(v_scale) < 2^(e + 8): then |code * scale| <= 127 * max(v_scale) < 2^15 after the
+// 2^-e, so fp16 cannot overflow (the exponent the bf16-V path would choose, or one more).
+__global__ void __launch_bounds__(256) cache_codes_kernel(const int8_t* __restrict__ k_cache,
+                                                          const float* __restrict__ k_scale,
+                                                          const int8_t* __restrict__ v_cache,
+                                                          const float* __restrict__ v_scale, int32_t Hkv, int32_t N,
+                                                          int32_t Lmax, int32_t d, int32_t d_io, int32_t seq_rows,
+                                                          int64_t t_pad_max, uint16_t* __restrict__ k_codes,
+                                                          float* __restrict__ k_scales, uint16_t* __restrict__ v16,
+                                                          int32_t* __restrict__ v_exp) {
+  __shared__ float s_max[8];
+  const int h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+  const int64_t src_row0 = (static_cast<int64_t>(b) * Hkv + h) * Lmax;  // token 0 of (b, h) in the cache
+  // the V exponent of (b, h): every CTA of the pair forms it from all N scales
+  float m = 0.0f;
+  for (int t = tid; t < N; t += blockDim.x) m = fmaxf(m, v_scale[src_row0 + t]);
+  m = warp_max(m);
+  if ((tid & 31) == 0) s_max[tid >> 5] = m;
+  __syncthreads();
+  m = s_max[0];
+  for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) m = fmaxf(m, s_max[w]);
+  int e = 0;
+  if (m > 0.0f) {
+    int km = 0;
+    frexpf(m, &km);  // m < 2^km
+    e = km > 8 ? km - 8 : 0;
+  }
+  if (blockIdx.x == 0 && tid == 0) v_exp[static_cast<int64_t>(b) * Hkv + h] = e;
+  const float vmul = __int_as_float((127 - e) << 23);  // 2^-e
+  const int vec = d / 16;                              // 16-code vectors per code row
+  const int t0 = blockIdx.x * 64;
+  for (int i = tid; i < 64 * vec; i += blockDim.x) {
+    const int r = i / vec, c = (i - r * vec) * 16, t = t0 + r;
+    const int64_t dst = static_cast<int64_t>(h) * t_pad_max + static_cast<int64_t>(b) * seq_rows + t;
+    const bool valid = t < N && c < d_io;
+    uint4 kw = make_uint4(0u, 0u, 0u, 0u), vw = kw;
+    float vs = 0.0f;
+    if (valid) {
+      kw = *reinterpret_cast<const uint4*>(k_cache + (src_row0 + t) * d_io + c);
+      vw = *reinterpret_cast<const uint4*>(v_cache + (src_row0 + t) * d_io + c);
+      vs = __fmul_rn(v_scale[src_row0 + t], vmul);
+    }
+    const uint32_t kb[4] = {kw.x, kw.y, kw.z, kw.w}, vb[4] = {vw.x, vw.y, vw.z, vw.w};
+    uint32_t ko[8], vo[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      // codes 2j and 2j+1 of the vector, sign-extended from their bytes
+      const int c0 = static_cast<int8_t>((kb[j >> 1] >> (16 * (j & 1))) & 0xffu);
+      const int c1 = static_cast<int8_t>((kb[j >> 1] >> (16 * (j & 1) + 8)) & 0xffu);
+      ko[j] = (__float_as_uint(static_cast<float>(c0)) >> 16) | (__float_as_uint(static_cast<float>(c1)) & 0xffff0000u);
+      const int v0 = static_cast<int8_t>((vb[j >> 1] >> (16 * (j & 1))) & 0xffu);
+      const int v1 = static_cast<int8_t>((vb[j >> 1] >> (16 * (j & 1) + 8)) & 0xffu);
+      const __half2 h2 = __floats2half2_rn(__fmul_rn(static_cast<float>(v0), vs), __fmul_rn(static_cast<float>(v1), vs));
+      vo[j] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    uint4* kd = reinterpret_cast<uint4*>(k_codes + dst * d + c);
+    uint4* vd = reinterpret_cast<uint4*>(v16 + dst * d + c);
+    kd[0] = make_uint4(ko[0], ko[1], ko[2], ko[3]);
+    kd[1] = make_uint4(ko[4], ko[5], ko[6], ko[7]);
+    vd[0] = make_uint4(vo[0], vo[1], vo[2], vo[3]);
+    vd[1] = make_uint4(vo[4], vo[5], vo[6], vo[7]);
+    if (c == 0) k_scales[static_cast<int64_t>(h) * t_pad_max + static_cast<int64_t>(b) * seq_rows + t] =
+        t < N ? k_scale[src_row0 + t] : 0.0f;
+  }
+}
+
+cudaError_t launch_cache_codes(const int8_t* k_cache, const float* k_scale, const int8_t* v_cache,
+                               const float* v_scale, int32_t nseq, int32_t Hkv, int32_t N, int32_t Lmax, int32_t d,
+                               int32_t d_io, int64_t t_pad_max, uint16_t* k_codes, float* k_scales, uint16_t* v16,
+                               int32_t* v_exp, cudaStream_t s) {
+  TraceScope tr("cache_codes", s);
+  const int32_t seq_rows = (N + kQTile - 1) / kQTile * kPadRows;
+  const dim3 grid(seq_rows / 64, Hkv, nseq);
+  cache_codes_kernel<<<grid, 256, 0, s>>>(k_cache, k_scale, v_cache, v_scale, Hkv, N, Lmax, d, d_io, seq_rows,
+                                          t_pad_max, k_codes, k_scales, v16, v_exp);
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- generic rowwise int8

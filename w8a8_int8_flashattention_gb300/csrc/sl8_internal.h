@@ -131,6 +131,18 @@ cudaError_t launch_quant_qk(const void* q, const void* k, sl8_dtype dt, bool var
                             float* k_scales, const void* v, int32_t* v_exp, uint16_t* v16, cudaStream_t s,
                             int32_t q_off = 0, int32_t d_io = 0, bool v_f16 = false,
                             const QuantGroups& groups = QuantGroups(), const float* k_mean = nullptr);
+// k == nullptr: Q rows only (the K codes, K scales and V come from elsewhere, e.g.
+// launch_cache_codes).
+// K and V rows of a dense int8 cache (every sequence holding N positions, Lmax rows apart)
+// into the attention kernel's code workspace: K codes widened to bf16 with their scales;
+// V dequantised (code * scale) and stored as fp16 * 2^-v_exp, the exponent per (sequence,
+// kv head) from the largest V scale, written to v_exp.  Rows from N to the end of the
+// sequence's padded rows (and columns from d_io to d) are zero.  d: the code row width
+// (64 when head dim 32 runs as 64).
+cudaError_t launch_cache_codes(const int8_t* k_cache, const float* k_scale, const int8_t* v_cache,
+                               const float* v_scale, int32_t nseq, int32_t Hkv, int32_t N, int32_t Lmax, int32_t d,
+                               int32_t d_io, int64_t t_pad_max, uint16_t* k_codes, float* k_scales, uint16_t* v16,
+                               int32_t* v_exp, cudaStream_t s);
 cudaError_t launch_quant_rowwise(const void* x, sl8_dtype dt, int64_t rows, int32_t cols, int64_t row_stride,
                                  const float* sub_mean, int64_t rows_per_group, int8_t* q_out, float* scale_out,
                                  cudaStream_t s);

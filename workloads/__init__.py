@@ -163,6 +163,15 @@ def decode_query(w: Workload) -> torch.Tensor:
     return _cast(q, w.dtype)
 
 
+def chunk_query(w: Workload, nq: int) -> torch.Tensor:
+    """q [B, Hq, nq, d] of the workload dtype: the queries of a chunk of nq positions per
+    sequence (prefill onto a cache), N(0,1)."""
+    q = np.empty((w.B, w.Hq, nq, w.d), np.float32)
+    for b in range(w.B):
+        q[b] = _rng(w, TAG_Q, b, nq).standard_normal((w.Hq, nq, w.d), dtype=np.float32)
+    return _cast(q, w.dtype)
+
+
 def decode_cache_values(w: Workload, b: int, which: str) -> np.ndarray:
     """fp32 cache values [Hkv, L_b, d] for sequence b (which = "k" or "v"), N(0,1).
 
