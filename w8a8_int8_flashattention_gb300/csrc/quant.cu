@@ -678,6 +678,8 @@ struct QuantQK {
   bool varlen;
   int32_t nseq, Hq, Hkv, N;
   int32_t q_off;            // dense query chunk: q holds positions q_off .. N-1
+  int32_t q_row0;           // dense: the first position whose Q row the attention reads (a
+                            // multiple of 64 <= q_off); Q blocks before it are not written
   int32_t d_io;             // values per input row (<= D; the code rows are zero past them)
   bool v_f16;               // V is fp16 (copied as is) rather than bf16
   int64_t total_tokens;
@@ -1012,7 +1014,9 @@ __global__ void __launch_bounds__(QpCfg<D>::kThreads, QpCfg<D>::kCtasPerSm)
   const int64_t rows_used = rows_all < a.t_pad_max ? rows_all : a.t_pad_max;
   const int32_t nblk = static_cast<int32_t>((rows_used + kQpRows - 1) / kQpRows);
   const bool convert_v = a.v16 != nullptr;
-  const int32_t n_q_units = a.Hq * nblk;
+  // dense Q blocks: those of each sequence from row q_row0 on (varlen: every block)
+  const int32_t nqb = (seq_rows - a.q_row0) / kQpRows;
+  const int32_t n_q_units = a.varlen ? a.Hq * nblk : a.Hq * a.nseq * nqb;
   const int32_t n_units = n_q_units + (a.k ? a.Hkv * nblk * (convert_v ? 2 : 1) : 0);  // k null: Q rows only
   const uint32_t row_bytes = static_cast<uint32_t>(a.d_io) * 2;
 
@@ -1043,6 +1047,13 @@ __global__ void __launch_bounds__(QpCfg<D>::kThreads, QpCfg<D>::kCtasPerSm)
       x.pad = 0;
       int32_t v = u;
       x.kind = kQpQ;
+      x.h = -1;
+      if (u < n_q_units && !a.varlen) {
+        // dense Q block: head, sequence, block from row q_row0 of the sequence
+        x.h = v / (a.nseq * nqb);
+        const int32_t rem = v - x.h * (a.nseq * nqb), sq = rem / nqb;
+        x.row0 = static_cast<int64_t>(sq) * seq_rows + a.q_row0 + static_cast<int64_t>(rem - sq * nqb) * kQpRows;
+      }
       if (u >= n_q_units) {
         v = u - n_q_units;
         x.kind = kQpK;
@@ -1052,8 +1063,10 @@ __global__ void __launch_bounds__(QpCfg<D>::kThreads, QpCfg<D>::kCtasPerSm)
         }
       }
       const bool kv = x.kind != kQpQ;
-      x.h = v / nblk;
-      x.row0 = static_cast<int64_t>(v - x.h * nblk) * kQpRows;
+      if (x.h < 0) {  // varlen Q blocks and every K / V block: block v of the head's rows
+        x.h = v / nblk;
+        x.row0 = static_cast<int64_t>(v - x.h * nblk) * kQpRows;
+      }
       int64_t pstart;
       if (!a.varlen) {
         x.s = static_cast<int32_t>(x.row0 / seq_rows);
@@ -1217,7 +1230,11 @@ cudaError_t launch_quant_qk(const void* q, const void* k, sl8_dtype dt, bool var
                             float* k_scales, const void* v, int32_t* v_exp, uint16_t* v16, cudaStream_t s,
                             int32_t q_off, int32_t d_io, bool v_f16, const QuantGroups& groups,
                             const float* k_mean) {
-  QuantQK a{q, k, varlen, nseq, Hq, Hkv, N, q_off, d_io > 0 ? d_io : d, v_f16, total_tokens, t, t_pad_max, k_partials,
+  // a chunk's Q blocks start at the first row of the attention's first item
+  const int32_t item_rows = prefill_item_rows(d, Hq / Hkv);
+  const int32_t q_row0 = varlen ? 0 : q_off / item_rows * item_rows;
+  QuantQK a{q, k, varlen, nseq, Hq, Hkv, N, q_off, q_row0, d_io > 0 ? d_io : d, v_f16, total_tokens, t, t_pad_max,
+            k_partials,
             v_partials, max_chunks, v_exp,
             q_codes, q_scales, k_codes, k_scales, v, v16, groups.q_group, groups.k_group, groups.q_tau};
   TraceScope tr("quant_qk", s);
@@ -1229,10 +1246,45 @@ cudaError_t launch_quant_qk(const void* q, const void* k, sl8_dtype dt, bool var
 }
 
 // ---------------------------------------------------------------- codes from an int8 cache
-// One CTA per (64-row block of a sequence's padded rows, kv head, sequence); each thread
-// turns 16 codes of a row at a time.  The V exponent e >= 0 is the least with
-// max(v_scale) < 2^(e + 8): then |code * scale| <= 127 * max(v_scale) < 2^15 after the
-// 2^-e, so fp16 cannot overflow (the exponent the bf16-V path would choose, or one more).
+// The V exponent of each (sequence, kv head) of a dense int8 cache: e >= 0 the least with
+// max(v_scale) < 2^(e + 8), so that |code * scale| <= 127 * max(v_scale) < 2^15 after the
+// 2^-e and fp16 cannot overflow (the exponent the bf16-V path would choose, or one more).
+// One CTA per (kv head, sequence).
+__global__ void __launch_bounds__(256) cache_vexp_kernel(const float* __restrict__ v_scale, int32_t Hkv, int32_t N,
+                                                         int32_t Lmax, int32_t* __restrict__ v_exp) {
+  __shared__ float s_max[8];
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const float* vs = v_scale + (static_cast<int64_t>(b) * Hkv + h) * Lmax;
+  float m0 = 0.0f, m1 = 0.0f, m2 = 0.0f, m3 = 0.0f;
+  int t = tid;
+  for (; t + 768 < N; t += 1024) {  // four loads in flight per round
+    m0 = fmaxf(m0, vs[t]);
+    m1 = fmaxf(m1, vs[t + 256]);
+    m2 = fmaxf(m2, vs[t + 512]);
+    m3 = fmaxf(m3, vs[t + 768]);
+  }
+  for (; t < N; t += 256) m0 = fmaxf(m0, vs[t]);
+  float m = warp_max(fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)));
+  if ((tid & 31) == 0) s_max[tid >> 5] = m;
+  __syncthreads();
+  if (tid == 0) {
+    for (int w = 1; w < 8; ++w) m = fmaxf(m, s_max[w]);
+    int e = 0;
+    if (m > 0.0f) {
+      int km = 0;
+      frexpf(m, &km);  // m < 2^km
+      e = km > 8 ? km - 8 : 0;
+    }
+    v_exp[static_cast<int64_t>(b) * Hkv + h] = e;
+  }
+}
+
+// K and V rows of the cache into the code workspace: one CTA per (64-row block of a
+// sequence's padded rows, kv head, sequence); each thread turns 16 codes of a row of K
+// and of V at a time.  Launched as a programmatic dependent of cache_vexp_kernel, whose
+// exponent it reads.
 __global__ void __launch_bounds__(256) cache_codes_kernel(const int8_t* __restrict__ k_cache,
                                                           const float* __restrict__ k_scale,
                                                           const int8_t* __restrict__ v_cache,
@@ -1240,28 +1292,15 @@ __global__ void __launch_bounds__(256) cache_codes_kernel(const int8_t* __restri
                                                           int32_t Lmax, int32_t d, int32_t d_io, int32_t seq_rows,
                                                           int64_t t_pad_max, uint16_t* __restrict__ k_codes,
                                                           float* __restrict__ k_scales, uint16_t* __restrict__ v16,
-                                                          int32_t* __restrict__ v_exp) {
-  __shared__ float s_max[8];
+                                                          const int32_t* __restrict__ v_exp) {
   const int h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
   const int64_t src_row0 = (static_cast<int64_t>(b) * Hkv + h) * Lmax;  // token 0 of (b, h) in the cache
-  // the V exponent of (b, h): every CTA of the pair forms it from all N scales
-  float m = 0.0f;
-  for (int t = tid; t < N; t += blockDim.x) m = fmaxf(m, v_scale[src_row0 + t]);
-  m = warp_max(m);
-  if ((tid & 31) == 0) s_max[tid >> 5] = m;
-  __syncthreads();
-  m = s_max[0];
-  for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) m = fmaxf(m, s_max[w]);
-  int e = 0;
-  if (m > 0.0f) {
-    int km = 0;
-    frexpf(m, &km);  // m < 2^km
-    e = km > 8 ? km - 8 : 0;
-  }
-  if (blockIdx.x == 0 && tid == 0) v_exp[static_cast<int64_t>(b) * Hkv + h] = e;
-  const float vmul = __int_as_float((127 - e) << 23);  // 2^-e
-  const int vec = d / 16;                              // 16-code vectors per code row
+  const int vec = d / 16;                                               // 16-code vectors per code row
   const int t0 = blockIdx.x * 64;
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const int e = v_exp[static_cast<int64_t>(b) * Hkv + h];
+  const float vmul = __int_as_float((127 - e) << 23);  // 2^-e
   for (int i = tid; i < 64 * vec; i += blockDim.x) {
     const int r = i / vec, c = (i - r * vec) * 16, t = t0 + r;
     const int64_t dst = static_cast<int64_t>(h) * t_pad_max + static_cast<int64_t>(b) * seq_rows + t;
@@ -1303,10 +1342,11 @@ cudaError_t launch_cache_codes(const int8_t* k_cache, const float* k_scale, cons
                                int32_t* v_exp, cudaStream_t s) {
   TraceScope tr("cache_codes", s);
   const int32_t seq_rows = (N + kQTile - 1) / kQTile * kPadRows;
-  const dim3 grid(seq_rows / 64, Hkv, nseq);
-  cache_codes_kernel<<<grid, 256, 0, s>>>(k_cache, k_scale, v_cache, v_scale, Hkv, N, Lmax, d, d_io, seq_rows,
-                                          t_pad_max, k_codes, k_scales, v16, v_exp);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(cache_vexp_kernel, dim3(Hkv, nseq), dim3(256), 0, s, v_scale, Hkv, N, Lmax, v_exp);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(cache_codes_kernel, dim3(seq_rows / 64, Hkv, nseq), dim3(256), 0, s, k_cache, k_scale, v_cache,
+                    v_scale, Hkv, N, Lmax, d, d_io, seq_rows, t_pad_max, k_codes, k_scales, v16,
+                    static_cast<const int32_t*>(v_exp));
 }
 
 // ---------------------------------------------------------------- generic rowwise int8

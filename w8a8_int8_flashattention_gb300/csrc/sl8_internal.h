@@ -115,8 +115,8 @@ cudaError_t launch_kv_finalize(bool varlen, int32_t nseq, int32_t Hkv, int32_t N
 // iff k_partials is) and, with v16 set, V is written as fp16 * 2^-v_exp with the exponent
 // kv_finalize left in v_exp; otherwise the exponent is 0 and is written to v_exp here.
 // t is read for varlen input only.  q_off > 0 (dense): q holds N - q_off rows per
-// (sequence, head), the positions q_off .. N-1; the code rows of the positions before it
-// are zero.  d_io < d (head dim 32 run as 64): the inputs hold d_io values per row and the
+// (sequence, head), the positions q_off .. N-1; the Q code rows of the positions before it
+// in the attention's first item are zero, those of earlier items are not written.  d_io < d (head dim 32 run as 64): the inputs hold d_io values per row and the
 // code rows are zero past them; k_partials then has d_io columns; v_f16: V is fp16
 // (copied, v_partials unused and the exponent 0), else bf16.
 // Grouped scales for attn_w8a8_fwd (all 1 / 0: per-row scales, the attn_int8_fwd path).
