@@ -81,3 +81,30 @@ def test_decode_graph_replay():
         assert torch.equal(out, eager), step
     st, site = sl8.last_device_status()
     assert st == sl8.SL8_OK, (st, site)
+
+
+def test_chunk_onto_cache_graph_replay():
+    """A serving loop's prefill chunk onto the int8 cache, captured once: replays on new
+    queries and a grown cache give the bits of eager calls (the short chunk takes the
+    key-split path, so the merge launch is captured too)."""
+    B, Hq, Hkv, d, lmax, nq = 1, 8, 2, 128, 2048, 128
+    gen = torch.Generator(device="cpu").manual_seed(4)
+    kc = torch.randint(-127, 128, (B, Hkv, lmax, d), generator=gen, dtype=torch.int8).to(DEV)
+    vc = torch.randint(-127, 128, (B, Hkv, lmax, d), generator=gen, dtype=torch.int8).to(DEV)
+    ks = (torch.rand((B, Hkv, lmax), generator=gen) * 0.05 + 1e-3).to(DEV)
+    vs = (torch.rand((B, Hkv, lmax), generator=gen) * 0.05 + 1e-3).to(DEV)
+    q = torch.randn((B, Hq, nq, d), generator=gen).to(torch.bfloat16).to(DEV)
+    nk = 1500
+    ws = torch.empty(int(sl8.lib().sl8_attn_int8_fwd_chunk_workspace_size(B, Hq, Hkv, nq, nk, d)), dtype=torch.uint8,
+                     device=DEV)
+    out = torch.empty_like(q)
+    g = _capture(lambda: sl8.attn_int8_fwd_chunk_cache(q, kc, ks, vc, vs, Nk=nk, workspace=ws, out=out))
+    for step in range(2):
+        q.copy_(torch.randn(q.shape, generator=gen).to(torch.bfloat16))
+        vs.mul_(2.0 ** (8 * step + 6))             # V scales grow 2^6, then 2^14 more: a new V exponent
+        g.replay()
+        eager = sl8.attn_int8_fwd_chunk_cache(q, kc, ks, vc, vs, Nk=nk)
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager), step
+    st, site = sl8.last_device_status()
+    assert st == sl8.SL8_OK, (st, site)
