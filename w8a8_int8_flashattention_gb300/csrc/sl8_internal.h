@@ -118,7 +118,8 @@ cudaError_t launch_kv_finalize(bool varlen, int32_t nseq, int32_t Hkv, int32_t N
 // (sequence, head), the positions q_off .. N-1; the Q code rows of the positions before it
 // in the attention's first item are zero, those of earlier items are not written.  d_io < d (head dim 32 run as 64): the inputs hold d_io values per row and the
 // code rows are zero past them; k_partials then has d_io columns; v_f16: V is fp16
-// (copied, v_partials unused and the exponent 0), else bf16.
+// (copied, v_partials unused and the exponent 0), else bf16.  k == nullptr: Q rows only
+// (the K codes, K scales and V come from elsewhere, e.g. launch_cache_codes).
 // Grouped scales for attn_w8a8_fwd (all 1 / 0: per-row scales, the attn_int8_fwd path).
 struct QuantGroups {
   int32_t q_group = 1, k_group = 1;  // rows per shared scale, powers of two <= 64
@@ -131,8 +132,6 @@ cudaError_t launch_quant_qk(const void* q, const void* k, sl8_dtype dt, bool var
                             float* k_scales, const void* v, int32_t* v_exp, uint16_t* v16, cudaStream_t s,
                             int32_t q_off = 0, int32_t d_io = 0, bool v_f16 = false,
                             const QuantGroups& groups = QuantGroups(), const float* k_mean = nullptr);
-// k == nullptr: Q rows only (the K codes, K scales and V come from elsewhere, e.g.
-// launch_cache_codes).
 // K and V rows of a dense int8 cache (every sequence holding N positions, Lmax rows apart)
 // into the attention kernel's code workspace: K codes widened to bf16 with their scales;
 // V dequantised (code * scale) and stored as fp16 * 2^-v_exp, the exponent per (sequence,
