@@ -121,6 +121,36 @@ def test_prefill_argument_errors(lib):
     assert call(N=0) == sl8.SL8_OK
 
 
+def test_chunk_cache_argument_errors(lib):
+    keep, p = _host_buf(1 << 12)
+    f = lib.sl8_attn_int8_fwd_chunk_cache
+    # (q, q_dtype, k_cache, k_scale, v_cache, v_scale, B, Hq, Hkv, Nq, Nk, Lmax, d, causal, out, out_dtype, lse,
+    #  ws, ws_bytes, stream)
+    base = [p, sl8.SL8_BF16, p, p, p, p, 1, 4, 2, 16, 64, 64, 128, 1, p, sl8.SL8_BF16, None, p, 16, None]
+
+    def call(**kw):
+        args = list(base)
+        idx = dict(q=0, qdt=1, kc=2, ks=3, vc=4, vs=5, B=6, Hq=7, Hkv=8, Nq=9, Nk=10, Lmax=11, d=12, out=14, odt=15,
+                   ws=17, wsb=18)
+        for k, val in kw.items():
+            args[idx[k]] = val
+        return f(*args)
+
+    assert call(kc=None) == sl8.SL8_ERR_INVALID_ARG
+    assert call(vs=None) == sl8.SL8_ERR_INVALID_ARG
+    assert call(vc=p + 4) == sl8.SL8_ERR_INVALID_ARG          # misaligned cache
+    assert call(Hkv=3) == sl8.SL8_ERR_INVALID_ARG             # Hq % Hkv != 0
+    assert call(Nq=65) == sl8.SL8_ERR_INVALID_ARG             # Nq > Nk
+    assert call(Nk=65) == sl8.SL8_ERR_INVALID_ARG             # Nk > Lmax
+    assert call(qdt=sl8.SL8_F32) == sl8.SL8_ERR_INVALID_ARG   # q must be fp16 or bf16
+    assert call(odt=sl8.SL8_F32) == sl8.SL8_ERR_WORKSPACE     # any output dtype (F16, BF16, F32)
+    assert call(d=96) == sl8.SL8_ERR_UNSUPPORTED
+    assert call(d=32) == sl8.SL8_ERR_WORKSPACE               # head dim 32 is accepted (runs as 64)
+    assert call(ws=None) == sl8.SL8_ERR_WORKSPACE
+    assert call(B=0) == sl8.SL8_OK                            # empty: nothing to do
+    assert call(Nq=0) == sl8.SL8_OK
+
+
 def test_w8a8_argument_errors(lib):
     keep, p = _host_buf(1 << 12)
     f = lib.sl8_attn_w8a8_fwd
