@@ -14,9 +14,10 @@ kernels" table (attn_int8_fwd: W8A8 FlashAttention-2, causal, GQA/MQA, head dims
 an int8 KV cache, int8-V and fp16-V variants; attn_paged_decode over a paged cache, with the
 "Engine" table's k8v8 format), "Supporting kernels" table (quant_rowwise:
 symmetric per-row int8), "Quantization" table (per-row int8 with K-smoothing) and
-the "Quick start" section (q [B,Hq,N,d], k/v [B,Hkv,N,d], quantises internally).
-The readings R1-R13 that fill what the pages leave open are restated in
-``sl8_oracle.c``.
+the "Quick start" section (q [B,Hq,N,d], k/v [B,Hkv,N,d], quantises internally);
+the "SuperL8-serve" README's "Engine" table (chunked prefill onto the KV cache).
+The readings that fill what the pages leave open are restated in ``sl8_oracle.c``
+(R1-R13) and in the docstrings below (the later ones, up to R21).
 
 Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
 (closed forms, hand-derived golden fixtures, textbook fp64 attention on
