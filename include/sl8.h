@@ -265,7 +265,7 @@ SL8_API int sl8_attn_w8a8_qk_logits_debug(const void* q, const void* k, int qk_d
  *   k_scale, v_scale   device, [B][Hkv][Lmax] fp32 per-token scales.
  *   seqlens            device, [B] int32, 0 <= L_b <= Lmax.
  *   num_splits         requested number of contiguous key splits (0 = automatic: about
- *                      12 (split, sequence, kv head) work slots per SM of the current
+ *                      10 (split, sequence, kv head) work slots per SM of the current
  *                      device).  Split s covers tokens [s * split_size, (s + 1) * split_size)
  *                      with split_size = ceil(Lmax / S) rounded up to whole stages of the
  *                      split kernel (160 tokens for d <= 128, 128 for d = 256; to 16 tokens

@@ -660,7 +660,7 @@ int sl8_attn_w8a8_qk_logits_debug(const void* q, const void* k, int qk_dtype, in
 // number of the decode kernel's stages (decode_chunk_tokens(d) tokens; to 16 tokens below
 // one stage): every stage of the cache then starts on a 16-byte boundary of the scale
 // rows, and only a sequence's last split ends in a partial stage.  A request n (0: about
-// 12 work slots per SM over the B x Hkv pairs, at most one per stage) becomes
+// 10 work slots per SM over the B x Hkv pairs, at most one per stage) becomes
 // S = ceil(Lmax / split_size_for(Lmax, n, d)) splits; the split kernel and the combine
 // both use split_size_for(Lmax, S, d).
 static int32_t split_size_for(int32_t Lmax, int32_t S, int32_t d) {
@@ -675,7 +675,7 @@ int32_t sl8_attn_decode_num_splits(int32_t B, int32_t Hkv, int32_t Lmax, int32_t
   int64_t n = num_splits;
   if (n == 0) {
     const int64_t pairs = static_cast<int64_t>(B) * Hkv;
-    n = (12ll * num_sms() + pairs - 1) / pairs;
+    n = (10ll * num_sms() + pairs - 1) / pairs;
     const int64_t chunks = (Lmax + decode_chunk_tokens(d) - 1) / decode_chunk_tokens(d);
     if (n > chunks) n = chunks;
   }
