@@ -58,11 +58,6 @@ __device__ __forceinline__ void load_vec16(const void* base, int64_t i, float (&
   for (int e = 0; e < EPL; ++e) x[e] = DT == SL8_BF16 ? bf16_bits_to_float(h[e]) : f16_bits_to_float(h[e]);
 }
 
-// One quantised value: clamp(RNE(x / s), -127, 127) with an IEEE division.  s > 0.
-__device__ __forceinline__ int quant_code(float x, float s) {
-  int c = __float2int_rn(__fdiv_rn(x, s));
-  return c > 127 ? 127 : (c < -127 ? -127 : c);
-}
 // Round-half-even of |y| < 2^22 to an integer-valued float, in two additions.
 __device__ __forceinline__ float rint_add(float y) {
   constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: its ulp is 1
@@ -110,20 +105,11 @@ __device__ __forceinline__ float quant_code_rcp(float x, float s, float rs) {
   if (fabsf(__fsub_rn(y, r)) > 0.4999f) r = rint_add(__fdiv_rn(x, s));
   return fminf(fmaxf(r, -127.0f), 127.0f);
 }
-// bf16 bit pattern of an integer-valued float |c| <= 127 (exact: its low 16 bits are 0).
-__device__ __forceinline__ uint16_t code_f_to_bf16_bits(float c) {
-  return static_cast<uint16_t>(__float_as_uint(c) >> 16);
-}
 
 __device__ __forceinline__ float warp_max(float a) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
   return a;
-}
-
-// bf16 bit pattern of a small integer code (|c| <= 127 is exact in bf16).
-__device__ __forceinline__ uint16_t code_to_bf16_bits(int c) {
-  return __bfloat16_as_ushort(__float2bfloat16_rn(static_cast<float>(c)));
 }
 
 // ---------------------------------------------------------------- scheduler
