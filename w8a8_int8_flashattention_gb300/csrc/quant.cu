@@ -39,25 +39,6 @@ __device__ __forceinline__ float load_elem(const void* base, int64_t i) {
   }
 }
 
-// EPL consecutive 16-bit elements starting at element index i (16-bit aligned by the caller's layout).
-template <sl8_dtype DT, int EPL>
-__device__ __forceinline__ void load_vec16(const void* base, int64_t i, float (&x)[EPL]) {
-  const uint16_t* p = static_cast<const uint16_t*>(base) + i;
-  uint16_t h[EPL];
-  if constexpr (EPL == 8) {
-    uint4 v = *reinterpret_cast<const uint4*>(p);
-    memcpy(h, &v, 16);
-  } else if constexpr (EPL == 4) {
-    uint2 v = *reinterpret_cast<const uint2*>(p);
-    memcpy(h, &v, 8);
-  } else {
-    uint32_t v = *reinterpret_cast<const uint32_t*>(p);
-    memcpy(h, &v, 4);
-  }
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) x[e] = DT == SL8_BF16 ? bf16_bits_to_float(h[e]) : f16_bits_to_float(h[e]);
-}
-
 // Round-half-even of |y| < 2^22 to an integer-valued float, in two additions.
 __device__ __forceinline__ float rint_add(float y) {
   constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: its ulp is 1
