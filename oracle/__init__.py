@@ -17,7 +17,7 @@ symmetric per-row int8), "Quantization" table (per-row int8 with K-smoothing) an
 the "Quick start" section (q [B,Hq,N,d], k/v [B,Hkv,N,d], quantises internally);
 the "SuperL8-serve" README's "Engine" table (chunked prefill onto the KV cache).
 The readings that fill what the pages leave open are restated in ``sl8_oracle.c``
-(R1-R13) and in the docstrings below (the later ones, up to R21).
+(R1-R13) and in the docstrings below (the later ones, up to R22).
 
 Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
 (closed forms, hand-derived golden fixtures, textbook fp64 attention on
@@ -430,7 +430,7 @@ def attn_chunk_cache(q, k_codes, k_scales, v_codes, v_scales, nk, causal=True, r
 
     Source: the "SuperL8-serve" README, "Engine" table (chunked prefill onto the KV
     cache), with the cache of the "Attention kernels" table's attn_decode row (int8 codes,
-    per-token scales).  Reading (R21): q [B, Hq, Nq, d] holds the queries of positions
+    per-token scales).  Reading (R22): q [B, Hq, Nq, d] holds the queries of positions
     nk - Nq .. nk - 1; the caches [B, Hkv, Lmax, d] hold positions 0 .. nk - 1 of every
     sequence.  Row (b, hq, i) is the decode of its quantised query over cache positions
     0 .. nk - Nq + i (causal) or 0 .. nk - 1.  Returns dict(out [B,Hq,Nq,d] f64,
